@@ -1,0 +1,184 @@
+"""Python binding of libfusedlin, the fused transformer dense layer for GB300.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of libfusedlin.so (built in-tree by gemm_epilogue_tma_gb300._build).
+PyTorch supplies device memory and the current stream. If the library is
+missing, every call raises; there is no fallback path.
+
+Entry points mirror the C ABI declared in include/fusedlin.h:
+    gemm_epilogue(A, W, bias, residual, out, pattern)   seven GEMM-first patterns
+    norm_gemm(x, gamma, W, beta, bias, out, eps, norm, act)
+    swiglu_ffn(x, gamma, Wg, Wu, Wd, bias_down, out, eps, workspace)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfusedlin.so")
+
+PATTERNS = (
+    "gemm_bias_gelu", "gemm_bias_silu", "gemm_bias_relu", "gemm_bias", "gemm_bias_residual",
+    "gemm_gelu", "gemm_silu", "layernorm_gemm", "rmsnorm_gemm",
+)
+NORMS = {"rms": 0, "layer": 1}
+ACTS = {"none": 0, "gelu": 1, "silu": 2, "relu": 3}
+DTYPE_CODES = {"f16": 0, "bf16": 1}
+STATUS_NAMES = {0: "FL_OK", 1: "FL_ERR_INVALID_ARG", 2: "FL_ERR_UNSUPPORTED", 3: "FL_ERR_ALIGNMENT",
+                4: "FL_ERR_WORKSPACE", 5: "FL_ERR_CUDA", 6: "FL_ERR_TIMEOUT"}
+OPTIONS = {"tile_n": 0, "variant": 1, "timeout_ms": 2, "split_k": 3}
+
+# C ABI: name -> (restype, argtypes)
+_vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "fl_gemm_epilogue": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
+    "fl_norm_gemm": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _f, _i, _i, _i, _vp]),
+    "fl_swiglu_ffn_workspace_size": (_sz, [_i, _i, _i]),
+    "fl_swiglu_ffn": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _f, _vp, _sz, _i, _vp]),
+    "fl_last_error": (ctypes.c_char_p, []),
+    "fl_device_status": (_i, [_vp]),
+    "fl_set_option": (_i, [_i, _i]),
+    "fl_debug_wait_timeout": (_i, [_i, _vp]),
+    "fl_version": (ctypes.c_char_p, []),
+}
+
+
+class FusedLinError(RuntimeError):
+    """A libfusedlin call returned a non-OK status."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with "
+                              "`python -m gemm_epilogue_tma_gb300._build` (needs nvcc)")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype, fn.argtypes = res, args
+        _lib = handle
+    return _lib
+
+
+def last_error() -> str:
+    return lib().fl_last_error().decode()
+
+
+def version() -> str:
+    return lib().fl_version().decode()
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        raise FusedLinError(status, last_error())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float16:
+        return 0
+    if t.dtype == torch.bfloat16:
+        return 1
+    raise TypeError(f"libfusedlin computes on fp16 or bf16 tensors, got {t.dtype}")
+
+
+def _check_tensors(dt_ref, **tensors):
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous (row-major)")
+        if t.dtype != dt_ref:
+            raise TypeError(f"{name} has dtype {t.dtype}, expected {dt_ref}")
+
+
+def gemm_epilogue(A, W, bias=None, residual=None, out=None, pattern="gemm_bias_gelu", stream=None):
+    """out[M,N] = epilogue(A[M,K] W[N,K]^T) for a GEMM-first pattern name or enum value."""
+    import torch
+    p = PATTERNS.index(pattern) if isinstance(pattern, str) else int(pattern)
+    M, K = A.shape
+    N = W.shape[0]
+    if W.shape[1] != K:
+        raise ValueError(f"W has shape {tuple(W.shape)}, expected [N, {K}]")
+    if out is None:
+        out = torch.empty((M, N), dtype=A.dtype, device=A.device)
+    _check_tensors(A.dtype, A=A, W=W, bias=bias, residual=residual, out=out)
+    _check(lib().fl_gemm_epilogue(_ptr(A), _ptr(W), _ptr(bias), _ptr(residual), _ptr(out), M, N, K, p,
+                                  _dtype_code(A), _stream(stream)))
+    return out
+
+
+def norm_gemm(x, gamma, W, beta=None, bias=None, out=None, eps=1e-6, norm="rms", act="none", stream=None):
+    """out[M,N] = act(norm(x)[M,K] W[N,K]^T + bias); norm "rms" or "layer"."""
+    import torch
+    M, K = x.shape
+    N = W.shape[0]
+    if W.shape[1] != K:
+        raise ValueError(f"W has shape {tuple(W.shape)}, expected [N, {K}]")
+    if out is None:
+        out = torch.empty((M, N), dtype=x.dtype, device=x.device)
+    _check_tensors(x.dtype, x=x, gamma=gamma, W=W, beta=beta, bias=bias, out=out)
+    _check(lib().fl_norm_gemm(_ptr(x), _ptr(gamma), _ptr(beta), _ptr(W), _ptr(bias), _ptr(out), M, N, K,
+                              float(eps), NORMS[norm], ACTS[act], _dtype_code(x), _stream(stream)))
+    return out
+
+
+def swiglu_ffn_workspace_size(M: int, F: int, dtype) -> int:
+    import torch
+    code = {torch.float16: 0, torch.bfloat16: 1}.get(dtype, DTYPE_CODES.get(dtype))
+    return int(lib().fl_swiglu_ffn_workspace_size(M, F, code))
+
+
+def swiglu_ffn(x, gamma, Wg, Wu, Wd, bias_down=None, out=None, eps=1e-6, workspace=None, stream=None):
+    """Llama-style SwiGLU FFN block: out = (silu(xh Wg^T) * (xh Wu^T)) Wd^T (+ bias_down) + x."""
+    import torch
+    M, D = x.shape
+    F = Wg.shape[0]
+    if out is None:
+        out = torch.empty_like(x)
+    need = swiglu_ffn_workspace_size(M, F, x.dtype)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    _check_tensors(x.dtype, x=x, gamma=gamma, Wg=Wg, Wu=Wu, Wd=Wd, bias_down=bias_down, out=out)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().fl_swiglu_ffn(_ptr(x), _ptr(gamma), _ptr(Wg), _ptr(Wu), _ptr(Wd), _ptr(bias_down), _ptr(out),
+                               M, D, F, float(eps), _ptr(workspace), ws_bytes, _dtype_code(x), _stream(stream)))
+    return out
+
+
+def device_status(stream=None) -> None:
+    """Synchronise the stream and raise FusedLinError(FL_ERR_TIMEOUT) if a kernel's wait ran out."""
+    _check(lib().fl_device_status(_stream(stream)))
+
+
+def set_option(key: str, value: int) -> None:
+    _check(lib().fl_set_option(OPTIONS[key], int(value)))
+
+
+def debug_wait_timeout(limit_us: int, stream=None) -> None:
+    """Launch the bounded-wait probe (a wait nothing completes); read the result with device_status()."""
+    _check(lib().fl_debug_wait_timeout(int(limit_us), _stream(stream)))

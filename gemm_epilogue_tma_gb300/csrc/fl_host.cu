@@ -1,0 +1,430 @@
+// C-ABI host layer of libfusedlin: argument validation, TMA tensor-map
+// encoding, variant dispatch, and the device status word.
+//
+// Validation is pure host code and runs before any CUDA call, so a rejected
+// call neither launches nor writes anything (and can be tested without a GPU).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <climits>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/fusedlin.h"
+#include "fl_internal.h"
+
+using fl::GemmParams;
+using fl::SplitKParams;
+
+// Device status word: kernels record a bounded-wait expiry here.
+__device__ int g_fl_status;
+
+namespace {
+
+thread_local char tls_err[512] = "";
+
+fl_status fail(fl_status s, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(tls_err, sizeof(tls_err), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+fl_status ok() {
+    tls_err[0] = '\0';
+    return FL_OK;
+}
+
+std::atomic<int> g_opt_tile_n{0};
+std::atomic<int> g_opt_variant{0};
+std::atomic<int> g_opt_timeout_ms{2000};
+std::atomic<int> g_opt_split_k{0};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+    if (a == nullptr || b == nullptr || na == 0 || nb == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+// ---------------------------------------------------------------------------
+// device information (cached per device)
+// ---------------------------------------------------------------------------
+struct DeviceInfo {
+    bool ready = false;
+    int sms = 0;
+    int major = 0, minor = 0;
+    int* status = nullptr;  // device address of g_fl_status
+};
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+fl_status device_info(DeviceInfo** out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(FL_ERR_UNSUPPORTED, "no CUDA device: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return fail(FL_ERR_UNSUPPORTED, "device index %d out of range", dev);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        std::lock_guard<std::mutex> lk(g_dev_mu);
+        if (!d.ready) {
+            cudaDeviceProp prop;
+            e = cudaGetDeviceProperties(&prop, dev);
+            if (e != cudaSuccess) return fail(FL_ERR_CUDA, "cudaGetDeviceProperties: %s", cudaGetErrorString(e));
+            d.sms = prop.multiProcessorCount;
+            d.major = prop.major;
+            d.minor = prop.minor;
+            e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_fl_status);
+            if (e != cudaSuccess) return fail(FL_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+            d.ready = true;
+        }
+    }
+    if (!(d.major == 10 && d.minor == 3))
+        return fail(FL_ERR_UNSUPPORTED, "needs a compute capability 10.3 (sm_103a) device, found %d.%d", d.major,
+                    d.minor);
+    *out = &d;
+    return FL_OK;
+}
+
+// ---------------------------------------------------------------------------
+// TMA tensor maps
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+// Row-major [outer, inner] fp16/bf16 matrix, box {box_inner, box_outer},
+// 128-byte swizzle, zero fill out of range.
+fl_status encode_2d(CUtensorMap* m, int dt, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                    uint32_t box_outer) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return fail(FL_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, dt == FL_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                    const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(FL_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for a [%llu, %llu] matrix, box {%u, %u}", (int)r,
+                    (unsigned long long)outer, (unsigned long long)inner, box_inner, box_outer);
+    return FL_OK;
+}
+
+// ---------------------------------------------------------------------------
+// tile kernel dispatch
+// ---------------------------------------------------------------------------
+cudaError_t dispatch_tile(int dt, int bn, int pro, bool dual, const GemmParams& p, int grid, cudaStream_t s) {
+#define FL_CASE(DT, BN, PRO, DUAL) \
+    if (dt == DT && bn == BN && pro == PRO && dual == DUAL) return fl::launch_gemm<DT, BN, PRO, DUAL>(p, grid, s);
+    FL_CASE(0, 128, 0, false)
+    FL_CASE(0, 256, 0, false)
+    FL_CASE(0, 128, 1, false)
+    FL_CASE(0, 256, 1, false)
+    FL_CASE(0, 128, 2, false)
+    FL_CASE(0, 256, 2, false)
+    FL_CASE(0, 128, 1, true)
+    FL_CASE(1, 128, 0, false)
+    FL_CASE(1, 256, 0, false)
+    FL_CASE(1, 128, 1, false)
+    FL_CASE(1, 256, 1, false)
+    FL_CASE(1, 128, 2, false)
+    FL_CASE(1, 256, 2, false)
+    FL_CASE(1, 128, 1, true)
+#undef FL_CASE
+    return cudaErrorInvalidValue;
+}
+
+// CTA tile width. A wider tile halves the activation re-reads and the shared
+// memory traffic per MMA, but fewer tiles may leave SMs idle: take the width
+// whose whole waves of CTAs cost least.
+int choose_bn(int M, int N, bool dual, int sms) {
+    if (dual) return 128;
+    const int forced = g_opt_tile_n.load();
+    if (forced == 128 || forced == 256) return forced;
+    const long long mb = (M + fl::kBM - 1) / fl::kBM;
+    const long long t256 = mb * ((N + 255) / 256), t128 = mb * ((N + 127) / 128);
+    const long long w256 = (t256 + sms - 1) / sms, w128 = (t128 + sms - 1) / sms;
+    // relative cost of one wave: a 128-wide tile does half the MMA work of a
+    // 256-wide one but is less efficient per flop
+    const double c256 = (double)w256 * 2.0, c128 = (double)w128 * 1.15;
+    return c256 <= c128 ? 256 : 128;
+}
+
+fl_status run_tile(int dt, int pro, bool dual, const void* A, const void* W, const void* W2, const void* bias,
+                   const void* residual, const void* gamma, const void* beta, void* out, int M, int N, int K, int act,
+                   float eps, cudaStream_t stream) {
+    DeviceInfo* di = nullptr;
+    fl_status st = device_info(&di);
+    if (st != FL_OK) return st;
+    const int bn = choose_bn(M, N, dual, di->sms);
+    GemmParams p;
+    memset(&p, 0, sizeof(p));
+    if ((st = encode_2d(&p.tmA, dt, A, K, M, fl::kBK, fl::kBM)) != FL_OK) return st;
+    if ((st = encode_2d(&p.tmB, dt, W, K, N, fl::kBK, bn)) != FL_OK) return st;
+    if (dual && (st = encode_2d(&p.tmB2, dt, W2, K, N, fl::kBK, bn)) != FL_OK) return st;
+    if ((st = encode_2d(&p.tmOut, dt, out, N, M, 64, 32)) != FL_OK) return st;
+    p.bias = bias;
+    p.residual = residual;
+    p.gamma = gamma;
+    p.beta = beta;
+    p.status = di->status;
+    p.timeout_ns = (unsigned long long)g_opt_timeout_ms.load() * 1000000ull;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.num_m_blocks = (M + fl::kBM - 1) / fl::kBM;
+    p.num_n_blocks = (N + bn - 1) / bn;
+    p.num_k_blocks = (K + fl::kBK - 1) / fl::kBK;
+    p.num_tiles = p.num_m_blocks * p.num_n_blocks;
+    p.act = act;
+    p.eps = eps;
+    const int grid = p.num_tiles < di->sms ? p.num_tiles : di->sms;
+    cudaError_t e = dispatch_tile(dt, bn, pro, dual, p, grid, stream);
+    if (e != cudaSuccess) return fail(FL_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+// Common shape checks of one GEMM [M,K] x [N,K]^T.
+fl_status check_shape(const char* what, long long M, long long N, long long K) {
+    if (M < 1 || N < 1 || K < 1) return fail(FL_ERR_INVALID_ARG, "%s: sizes must be positive (M=%lld N=%lld K=%lld)", what, M, N, K);
+    if (N % 8 != 0 || K % 8 != 0)
+        return fail(FL_ERR_ALIGNMENT, "%s: N and K must be multiples of 8 (N=%lld K=%lld)", what, N, K);
+    const long long mb = (M + 127) / 128, nb = (N + 63) / 64;
+    if (mb * nb > INT_MAX / 2) return fail(FL_ERR_UNSUPPORTED, "%s: too many output tiles", what);
+    return FL_OK;
+}
+
+fl_status check_ptr(const char* name, const void* p, bool required) {
+    if (p == nullptr) {
+        if (required) return fail(FL_ERR_INVALID_ARG, "%s must not be null", name);
+        return FL_OK;
+    }
+    if (!aligned16(p)) return fail(FL_ERR_ALIGNMENT, "%s must be 16-byte aligned", name);
+    return FL_OK;
+}
+
+bool valid_dtype(int dt) { return dt == FL_F16 || dt == FL_BF16; }
+
+}  // namespace
+
+// ===========================================================================
+// C ABI
+// ===========================================================================
+extern "C" {
+
+const char* fl_last_error(void) { return tls_err; }
+
+const char* fl_version(void) { return "libfusedlin 0.1 (sm_103a, tcgen05 + TMA)"; }
+
+fl_status fl_set_option(fl_option key, int value) {
+    switch (key) {
+        case FL_OPT_TILE_N:
+            if (value != 0 && value != 128 && value != 256) return fail(FL_ERR_INVALID_ARG, "tile width must be 0, 128 or 256");
+            g_opt_tile_n = value;
+            return ok();
+        case FL_OPT_VARIANT:
+            if (value < 0 || value > 2) return fail(FL_ERR_INVALID_ARG, "variant must be 0, 1 or 2");
+            g_opt_variant = value;
+            return ok();
+        case FL_OPT_TIMEOUT_MS:
+            if (value < 1 || value > 600000) return fail(FL_ERR_INVALID_ARG, "timeout must be 1..600000 ms");
+            g_opt_timeout_ms = value;
+            return ok();
+        case FL_OPT_SPLIT_K:
+            if (value < 0 || value > 16) return fail(FL_ERR_INVALID_ARG, "split must be 0..16");
+            g_opt_split_k = value;
+            return ok();
+        default:
+            return fail(FL_ERR_INVALID_ARG, "unknown option %d", (int)key);
+    }
+}
+
+fl_status fl_gemm_epilogue(const void* A, const void* W, const void* bias, const void* residual, void* out, int M,
+                           int N, int K, fl_pattern pattern, fl_dtype dtype, void* stream) {
+    if (!valid_dtype(dtype)) return fail(FL_ERR_INVALID_ARG, "bad dtype %d", (int)dtype);
+    if ((int)pattern < 0 || (int)pattern > FL_RMSNORM_GEMM) return fail(FL_ERR_INVALID_ARG, "bad pattern %d", (int)pattern);
+    if (pattern == FL_LAYERNORM_GEMM || pattern == FL_RMSNORM_GEMM)
+        return fail(FL_ERR_INVALID_ARG, "norm patterns take gamma/eps: call fl_norm_gemm");
+    const bool uses_bias = pattern <= FL_GEMM_BIAS_RESIDUAL;
+    const bool uses_res = pattern == FL_GEMM_BIAS_RESIDUAL;
+    int act = fl::ACT_NONE;
+    if (pattern == FL_GEMM_BIAS_GELU || pattern == FL_GEMM_GELU) act = fl::ACT_GELU;
+    if (pattern == FL_GEMM_BIAS_SILU || pattern == FL_GEMM_SILU) act = fl::ACT_SILU;
+    if (pattern == FL_GEMM_BIAS_RELU) act = fl::ACT_RELU;
+    fl_status st;
+    if ((st = check_shape("fl_gemm_epilogue", M, N, K)) != FL_OK) return st;
+    if ((st = check_ptr("A", A, true)) != FL_OK) return st;
+    if ((st = check_ptr("W", W, true)) != FL_OK) return st;
+    if ((st = check_ptr("out", out, true)) != FL_OK) return st;
+    if ((st = check_ptr("bias", uses_bias ? bias : nullptr, uses_bias)) != FL_OK) return st;
+    if ((st = check_ptr("residual", uses_res ? residual : nullptr, uses_res)) != FL_OK) return st;
+    const size_t ob = (size_t)M * N * 2;
+    if (overlap(out, ob, A, (size_t)M * K * 2) || overlap(out, ob, W, (size_t)N * K * 2) ||
+        (uses_bias && overlap(out, ob, bias, (size_t)N * 2)))
+        return fail(FL_ERR_INVALID_ARG, "out overlaps an input");
+    if (uses_res && residual != out && overlap(out, ob, residual, ob))
+        return fail(FL_ERR_INVALID_ARG, "out may alias residual only exactly");
+    return run_tile(dtype, fl::PRO_NONE, false, A, W, nullptr, uses_bias ? bias : nullptr,
+                    uses_res ? residual : nullptr, nullptr, nullptr, out, M, N, K, act, 0.f,
+                    static_cast<cudaStream_t>(stream));
+}
+
+fl_status fl_norm_gemm(const void* x, const void* gamma, const void* beta, const void* W, const void* bias, void* out,
+                       int M, int N, int K, float eps, fl_norm_kind norm_kind, fl_act act, fl_dtype dtype,
+                       void* stream) {
+    if (!valid_dtype(dtype)) return fail(FL_ERR_INVALID_ARG, "bad dtype %d", (int)dtype);
+    if (norm_kind != FL_NORM_RMS && norm_kind != FL_NORM_LAYER)
+        return fail(FL_ERR_INVALID_ARG, "bad norm kind %d", (int)norm_kind);
+    if ((int)act < 0 || (int)act > FL_ACT_RELU) return fail(FL_ERR_INVALID_ARG, "bad activation %d", (int)act);
+    if (!(eps >= 0.0f) || eps > 1e30f) return fail(FL_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    fl_status st;
+    if ((st = check_shape("fl_norm_gemm", M, N, K)) != FL_OK) return st;
+    if ((st = check_ptr("x", x, true)) != FL_OK) return st;
+    if ((st = check_ptr("gamma", gamma, true)) != FL_OK) return st;
+    if ((st = check_ptr("W", W, true)) != FL_OK) return st;
+    if ((st = check_ptr("out", out, true)) != FL_OK) return st;
+    if ((st = check_ptr("bias", bias, false)) != FL_OK) return st;
+    const void* b = norm_kind == FL_NORM_LAYER ? beta : nullptr;
+    if ((st = check_ptr("beta", b, false)) != FL_OK) return st;
+    const size_t ob = (size_t)M * N * 2;
+    if (overlap(out, ob, x, (size_t)M * K * 2) || overlap(out, ob, W, (size_t)N * K * 2) ||
+        overlap(out, ob, gamma, (size_t)K * 2) || overlap(out, ob, b, (size_t)K * 2) ||
+        overlap(out, ob, bias, (size_t)N * 2))
+        return fail(FL_ERR_INVALID_ARG, "out overlaps an input");
+    const int pro = norm_kind == FL_NORM_RMS ? fl::PRO_RMS : fl::PRO_LN;
+    return run_tile(dtype, pro, false, x, W, nullptr, bias, nullptr, gamma, b, out, M, N, K, (int)act, eps,
+                    static_cast<cudaStream_t>(stream));
+}
+
+size_t fl_swiglu_ffn_workspace_size(int M, int F, fl_dtype dtype) {
+    (void)dtype;
+    if (M < 1 || F < 1) return 0;
+    return (size_t)M * (size_t)F * 2;
+}
+
+fl_status fl_swiglu_ffn(const void* x, const void* gamma, const void* Wg, const void* Wu, const void* Wd,
+                        const void* bias_down, void* out, int M, int D, int F, float eps, void* workspace,
+                        size_t workspace_bytes, fl_dtype dtype, void* stream) {
+    if (!valid_dtype(dtype)) return fail(FL_ERR_INVALID_ARG, "bad dtype %d", (int)dtype);
+    if (!(eps >= 0.0f) || eps > 1e30f) return fail(FL_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    fl_status st;
+    if ((st = check_shape("fl_swiglu_ffn (gate/up)", M, F, D)) != FL_OK) return st;
+    if ((st = check_shape("fl_swiglu_ffn (down)", M, D, F)) != FL_OK) return st;
+    if ((st = check_ptr("x", x, true)) != FL_OK) return st;
+    if ((st = check_ptr("gamma", gamma, true)) != FL_OK) return st;
+    if ((st = check_ptr("Wg", Wg, true)) != FL_OK) return st;
+    if ((st = check_ptr("Wu", Wu, true)) != FL_OK) return st;
+    if ((st = check_ptr("Wd", Wd, true)) != FL_OK) return st;
+    if ((st = check_ptr("out", out, true)) != FL_OK) return st;
+    if ((st = check_ptr("bias_down", bias_down, false)) != FL_OK) return st;
+    if (workspace == nullptr) return fail(FL_ERR_WORKSPACE, "workspace must not be null");
+    if (!aligned16(workspace)) return fail(FL_ERR_ALIGNMENT, "workspace must be 16-byte aligned");
+    const size_t need = fl_swiglu_ffn_workspace_size(M, F, dtype);
+    if (workspace_bytes < need)
+        return fail(FL_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
+    const size_t ob = (size_t)M * D * 2, wb = (size_t)F * D * 2;
+    const void* ins[6] = {x, gamma, Wg, Wu, Wd, bias_down};
+    const size_t insz[6] = {ob, (size_t)D * 2, wb, wb, wb, (size_t)D * 2};
+    for (int i = 0; i < 6; ++i) {
+        if (overlap(out, ob, ins[i], insz[i])) return fail(FL_ERR_INVALID_ARG, "out overlaps an input");
+        if (overlap(workspace, need, ins[i], insz[i])) return fail(FL_ERR_INVALID_ARG, "workspace overlaps an input");
+    }
+    if (overlap(workspace, need, out, ob)) return fail(FL_ERR_INVALID_ARG, "workspace overlaps out");
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // gate/up: h = silu(RMSNorm(x) Wg^T) * (RMSNorm(x) Wu^T)
+    st = run_tile(dtype, fl::PRO_RMS, true, x, Wg, Wu, nullptr, nullptr, gamma, nullptr, workspace, M, F, D,
+                  fl::ACT_NONE, eps, s);
+    if (st != FL_OK) return st;
+    // down: out = h Wd^T (+ bias_down) + x
+    return run_tile(dtype, fl::PRO_NONE, false, workspace, Wd, nullptr, bias_down, x, nullptr, nullptr, out, M, D, F,
+                    fl::ACT_NONE, 0.f, s);
+}
+
+fl_status fl_device_status(void* stream) {
+    DeviceInfo* di = nullptr;
+    fl_status st = device_info(&di);
+    if (st != FL_OK) return st;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(FL_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
+    int v = 0;
+    e = cudaMemcpyFromSymbol(&v, g_fl_status, sizeof(int));
+    if (e != cudaSuccess) return fail(FL_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+    if (v == 0) return ok();
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_fl_status, &zero, sizeof(int));
+    if (e != cudaSuccess) return fail(FL_ERR_CUDA, "status clear: %s", cudaGetErrorString(e));
+    return fail(FL_ERR_TIMEOUT, "a device-side wait ran past its limit (code %d, wait site %d)", v & 0xff, v >> 8);
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// bounded-wait test hook
+// ---------------------------------------------------------------------------
+namespace {
+
+__global__ void fl_wait_probe_kernel(int* status, unsigned long long limit_ns) {
+    __shared__ __align__(8) unsigned long long bar;
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(&bar));
+    if (threadIdx.x == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(a) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x != 0) return;
+    uint64_t t0, t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    for (;;) {
+        uint32_t done;
+        // nobody arrives: phase 0 never completes
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(a)
+            : "memory");
+        if (done) return;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+        if (t - t0 > limit_ns) {
+            atomicCAS(status, 0, fl::kStatusTimeout | (99 << 8));
+            return;
+        }
+    }
+}
+
+}  // namespace
+
+extern "C" fl_status fl_debug_wait_timeout(int limit_us, void* stream) {
+    if (limit_us < 1 || limit_us > 1000000) return fail(FL_ERR_INVALID_ARG, "limit_us must be 1..1000000");
+    DeviceInfo* di = nullptr;
+    fl_status st = device_info(&di);
+    if (st != FL_OK) return st;
+    fl_wait_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(di->status,
+                                                                          (unsigned long long)limit_us * 1000ull);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(FL_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+    return ok();
+}

@@ -1,0 +1,86 @@
+// Declarations shared by the C-ABI host layer and the kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace fl {
+
+enum Prologue : int { PRO_NONE = 0, PRO_RMS = 1, PRO_LN = 2 };
+enum ActKind : int { ACT_NONE = 0, ACT_GELU = 1, ACT_SILU = 2, ACT_RELU = 3 };
+enum DTypeTag : int { DT_F16 = 0, DT_BF16 = 1 };
+
+// Device status word values (low byte = code; the next byte says which wait gave up).
+constexpr int kStatusTimeout = 6;
+
+// CTA tile: 128 rows of the activation; 64 fp16/bf16 along K per stage (one
+// 128-byte swizzle row).
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+
+// Parameters of the tile kernel. Passed by value as a __grid_constant__ so the
+// tensor maps sit in parameter space, where TMA may read them.
+struct GemmParams {
+    CUtensorMap tmA;    // activation [M, K], box {64, 128}, 128B swizzle
+    CUtensorMap tmB;    // weight [N, K], box {64, BN}, 128B swizzle
+    CUtensorMap tmB2;   // second weight [N, K] of the gate/up kernel (else unused)
+    CUtensorMap tmOut;  // output [M, N], box {64, 32}, 128B swizzle
+    const void* bias;      // [N] or null
+    const void* residual;  // [M, N] or null
+    const void* gamma;     // [K] (norm prologues)
+    const void* beta;      // [K] or null (LayerNorm)
+    int* status;           // device status word
+    unsigned long long timeout_ns;
+    int M, N, K;
+    int num_m_blocks, num_n_blocks, num_k_blocks, num_tiles;
+    int act;
+    float eps;
+};
+
+// Parameters of the small-M split-K kernel.
+struct SplitKParams {
+    CUtensorMap tmW;    // weight [N, K], box {64, 128}, 128B swizzle
+    CUtensorMap tmX;    // activation [M, K], box {64, MP}, 128B swizzle
+    const void* gamma;  // [K]
+    const void* beta;   // [K] or null
+    const void* bias;   // [N] or null
+    const void* residual;  // [M, N] or null
+    void* out;          // [M, N]
+    int* status;
+    unsigned long long timeout_ns;
+    int M, N, K;
+    int k_blocks_per_split;  // 64-wide K blocks per cluster rank
+    int act;
+    float eps;
+};
+
+// Kernel launchers, explicitly instantiated in the kernel translation units.
+template <int DT, int BN, int PRO, bool DUAL>
+cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream);
+
+template <int DT, int MP, int PRO>
+cudaError_t launch_splitk(const SplitKParams& p, int n_tiles, int splits, cudaStream_t stream);
+
+// Shared-memory bytes of each tile configuration (host-visible).
+template <int BN, bool DUAL>
+struct TileCfg {
+    static constexpr int A_BYTES = kBM * kBK * 2;
+    static constexpr int B_BYTES = BN * kBK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES * (DUAL ? 2 : 1);
+    static constexpr int STAGES_RAW = (192 * 1024) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+    static constexpr int ACC_COLS = BN * (DUAL ? 2 : 1);  // one accumulator buffer
+    static constexpr int TMEM_COLS = 2 * ACC_COLS;         // double buffered
+    static constexpr int EPI_WARPS = 4;
+    static constexpr int EPI_BUF_BYTES = 32 * 128;         // 32 rows x 64 cols x 2 B per warp
+    static constexpr int OFF_EPI = STAGES * STAGE_BYTES;
+    static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * EPI_BUF_BYTES;
+    static constexpr int NUM_BARS = 3 * STAGES + 6 + 1;
+    static constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
+    static constexpr int OFF_ROWSCALE = (OFF_SLOT + 16 + 15) / 16 * 16;
+    static constexpr int SMEM_BYTES = OFF_ROWSCALE + 2 * kBM * 4 + 1024;  // + alignment slack
+};
+
+}  // namespace fl

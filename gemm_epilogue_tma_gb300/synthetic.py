@@ -121,3 +121,19 @@ def as_f64(t):
     if t is None:
         return None
     return t.detach().cpu().to(torch.float64).numpy()
+
+
+def dense_layer_inputs(M: int, N: int, K: int, dtype: str, seed=None) -> dict:
+    """Every operand any of the nine patterns reads, for sweeping all patterns on one draw.
+
+    Draw order A, W, bias, residual, gamma, beta; seed defaults to (3, dtype id, M, N, K).
+    """
+    if seed is None:
+        seed = (3, DTYPE_IDS[dtype], M, N, K)
+    rng = rng_for(*(seed if isinstance(seed, (tuple, list)) else (seed,)))
+    return {"A": _draw(rng, (M, K), 0.0, 1.0, dtype),
+            "W": _draw(rng, (N, K), 0.0, 1.0 / math.sqrt(K), dtype),
+            "bias": _draw(rng, (N,), 0.0, 0.1, dtype),
+            "residual": _draw(rng, (M, N), 0.0, 1.0, dtype),
+            "gamma": _draw(rng, (K,), 1.0, 0.1, dtype),
+            "beta": _draw(rng, (K,), 0.0, 0.1, dtype)}

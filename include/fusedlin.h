@@ -1,0 +1,176 @@
+/*
+ * libfusedlin: fused transformer dense layer on GB300 (sm_103a).
+ *
+ * One GEMM with FP32 accumulation on fp16/bf16 operands, with an optional
+ * RMSNorm / LayerNorm prologue on the activation rows and a bias /
+ * activation / residual / SwiGLU epilogue, all applied on-chip: the
+ * normalised activation and the pre-activation never pass through device
+ * memory.
+ *
+ * Operations (sources, by page and section):
+ *   - The nine fused patterns of the llm-fusion-compiler README, pattern
+ *     table "Pattern / Operations fused": gemm_bias_gelu, gemm_bias_silu,
+ *     gemm_bias_relu, gemm_bias, gemm_bias_residual, gemm_gelu, gemm_silu,
+ *     layernorm_gemm, rmsnorm_gemm. GeLU is the tanh ("fast approximation")
+ *     form: 0.5 v (1 + tanh(sqrt(2/pi) (v + 0.044715 v^3))).
+ *   - RMSNorm feeding a linear projection: the LLMBoost README, op
+ *     llm.fused_rmsnorm_linear(x, w_norm, w_proj, epsilon) (section 1) and
+ *     its CUDA kernel, 1/rms = rsqrt(sum(x^2)/d_in + epsilon) (section 3);
+ *     the same eps-inside-the-root form as the RMSNorm loop nest of the
+ *     "hackable compiler" post.
+ *   - The SwiGLU FFN block of the llm-fusion-compiler README ("FFN block
+ *     (SwiGLU style)": three GEMMs, activation, elementwise product, bias,
+ *     residual) in its Llama form: RMSNorm, gate and up projections,
+ *     silu(gate) * up, down projection, plus the pre-norm input.
+ *
+ * Conventions for every entry point:
+ *   - Layouts are row-major and dense: A/x [M, K]; weights W [N, K] (the
+ *     linear-layer layout: out = act(A W^T + bias) ...); bias [N];
+ *     residual and out [M, N]; gamma, beta [K].
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller, 16-byte
+ *     aligned. K and N (and D, F for the FFN) must be multiples of 8 so that
+ *     every row starts on a 16-byte boundary. M may be any value >= 1.
+ *   - dtype selects fp16 or bf16 for every tensor of the call; accumulation
+ *     and the epilogue arithmetic are fp32; the output is rounded to nearest
+ *     even.
+ *   - stream is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream). Every call is asynchronous on that stream.
+ *   - The library allocates no device memory per call. The FFN's hidden
+ *     activation lives in a caller-provided workspace.
+ *   - out may alias residual exactly (same pointer); no other aliasing of an
+ *     output with an input is allowed.
+ *   - Errors: a call that fails validation returns a non-zero fl_status
+ *     before launching anything and writes nothing; fl_last_error() then
+ *     returns a message (per thread). A device-side wait that exceeds its time
+ *     limit makes the kernel stop early and record FL_ERR_TIMEOUT in a device
+ *     status word, which fl_device_status() reads (see there).
+ */
+#ifndef FUSEDLIN_H
+#define FUSEDLIN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FL_OK = 0,
+    FL_ERR_INVALID_ARG = 1, /* null pointer, bad size, bad enum, forbidden aliasing */
+    FL_ERR_UNSUPPORTED = 2, /* no sm_103a device, or a size beyond what the kernels handle */
+    FL_ERR_ALIGNMENT = 3,   /* pointer not 16-byte aligned, or K/N/D/F not a multiple of 8 */
+    FL_ERR_WORKSPACE = 4,   /* FFN workspace missing or smaller than fl_swiglu_ffn_workspace_size */
+    FL_ERR_CUDA = 5,        /* a CUDA runtime or driver call failed (message in fl_last_error) */
+    FL_ERR_TIMEOUT = 6      /* a device-side wait ran past its limit (from fl_device_status) */
+} fl_status;
+
+typedef enum { FL_F16 = 0, FL_BF16 = 1 } fl_dtype;
+
+/* The nine fused patterns, in the order of the llm-fusion-compiler pattern table. */
+typedef enum {
+    FL_GEMM_BIAS_GELU = 0,     /* gelu_tanh(A W^T + bias)          */
+    FL_GEMM_BIAS_SILU = 1,     /* silu(A W^T + bias)               */
+    FL_GEMM_BIAS_RELU = 2,     /* relu(A W^T + bias)               */
+    FL_GEMM_BIAS = 3,          /* A W^T + bias                     */
+    FL_GEMM_BIAS_RESIDUAL = 4, /* A W^T + bias + residual          */
+    FL_GEMM_GELU = 5,          /* gelu_tanh(A W^T)                 */
+    FL_GEMM_SILU = 6,          /* silu(A W^T)                      */
+    FL_LAYERNORM_GEMM = 7,     /* LayerNorm(A) W^T  (fl_norm_gemm) */
+    FL_RMSNORM_GEMM = 8        /* RMSNorm(A) W^T    (fl_norm_gemm) */
+} fl_pattern;
+
+typedef enum { FL_NORM_RMS = 0, FL_NORM_LAYER = 1 } fl_norm_kind;
+
+typedef enum { FL_ACT_NONE = 0, FL_ACT_GELU_TANH = 1, FL_ACT_SILU = 2, FL_ACT_RELU = 3 } fl_act;
+
+/*
+ * out[M,N] = epilogue(A[M,K] W[N,K]^T) for the seven GEMM-first patterns
+ * (FL_GEMM_BIAS_GELU .. FL_GEMM_SILU); llm-fusion-compiler pattern table.
+ *   bias:     [N], required by the *_BIAS* patterns, ignored otherwise.
+ *   residual: [M,N], required by FL_GEMM_BIAS_RESIDUAL, ignored otherwise;
+ *             may be the same pointer as out.
+ * Epilogue order: accumulate, + bias, activation, + residual, round.
+ * FL_LAYERNORM_GEMM / FL_RMSNORM_GEMM return FL_ERR_INVALID_ARG here: they
+ * need gamma/beta/eps and are served by fl_norm_gemm.
+ */
+fl_status fl_gemm_epilogue(const void* A, const void* W, const void* bias, const void* residual,
+                           void* out, int M, int N, int K, fl_pattern pattern, fl_dtype dtype,
+                           void* stream);
+
+/*
+ * out[M,N] = act(norm(x)[M,K] W[N,K]^T + bias) with the norm as prologue;
+ * the rmsnorm_gemm / layernorm_gemm patterns of the llm-fusion-compiler
+ * table, generalised with an optional bias and activation.
+ *   FL_NORM_RMS:   norm(x) = x * gamma / sqrt(mean_k(x^2) + eps)
+ *                  (LLMBoost CUDA kernel section: rsqrt(ss / d_in + eps)).
+ *   FL_NORM_LAYER: norm(x) = (x - mean) / sqrt(var + eps) * gamma + beta,
+ *                  biased variance.
+ *   gamma: [K], required. beta: [K], LayerNorm only, NULL means zero;
+ *   ignored for RMS. bias: [N] or NULL. eps must be finite and >= 0.
+ * The RMS statistics are computed from the fp16/bf16 input in fp32; gamma is
+ * folded into the staged operand (one rounding to the dtype) and 1/rms is
+ * applied to the fp32 accumulator as a row scale.
+ */
+fl_status fl_norm_gemm(const void* x, const void* gamma, const void* beta, const void* W,
+                       const void* bias, void* out, int M, int N, int K, float eps,
+                       fl_norm_kind norm_kind, fl_act act, fl_dtype dtype, void* stream);
+
+/* Bytes of workspace fl_swiglu_ffn needs: the hidden activation h [M,F] in the dtype. */
+size_t fl_swiglu_ffn_workspace_size(int M, int F, fl_dtype dtype);
+
+/*
+ * Llama-style SwiGLU FFN block (llm-fusion-compiler "FFN block (SwiGLU
+ * style)"):
+ *   xh  = RMSNorm(x; gamma, eps)                 x [M,D], gamma [D]
+ *   h   = silu(xh Wg^T) * (xh Wu^T)              Wg, Wu [F,D]; h [M,F] in dtype
+ *   out = h Wd^T (+ bias_down) + x               Wd [D,F], bias_down [D] or NULL
+ * Two launches: a gate/up kernel that feeds one staged activation tile to both
+ * weights and writes h, then a down-projection kernel with a residual
+ * epilogue. workspace: device memory of at least
+ * fl_swiglu_ffn_workspace_size(M, F, dtype) bytes, 16-byte aligned, owned by
+ * the caller; its contents on return are h. out must not alias x.
+ */
+fl_status fl_swiglu_ffn(const void* x, const void* gamma, const void* Wg, const void* Wu,
+                        const void* Wd, const void* bias_down, void* out, int M, int D, int F,
+                        float eps, void* workspace, size_t workspace_bytes, fl_dtype dtype,
+                        void* stream);
+
+/* Message for the last non-OK status returned on this thread ("" if none). */
+const char* fl_last_error(void);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word that
+ * kernels set when a bounded wait runs out. Returns FL_OK, FL_ERR_TIMEOUT, or
+ * FL_ERR_CUDA if the synchronisation itself failed.
+ */
+fl_status fl_device_status(void* stream);
+
+/*
+ * Tuning overrides, for benchmarks and tests (process-wide, not thread-safe):
+ *   FL_OPT_TILE_N:      0 = automatic, else the CTA tile width (128 or 256).
+ *   FL_OPT_VARIANT:     0 = automatic, 1 = tile kernel, 2 = small-M split-K kernel.
+ *   FL_OPT_TIMEOUT_MS:  limit of every device-side wait (default 2000).
+ *   FL_OPT_SPLIT_K:     0 = automatic, else the K split of the small-M kernel.
+ * Returns FL_ERR_INVALID_ARG for an unknown key or a value out of range.
+ */
+typedef enum { FL_OPT_TILE_N = 0, FL_OPT_VARIANT = 1, FL_OPT_TIMEOUT_MS = 2, FL_OPT_SPLIT_K = 3 } fl_option;
+fl_status fl_set_option(fl_option key, int value);
+
+/*
+ * Test hook for the bounded-wait machinery: launches one CTA that waits on a
+ * device barrier that nothing ever completes, with a limit of `limit_us`
+ * microseconds (1..1000000). The kernel gives up, records FL_ERR_TIMEOUT in the
+ * device status word and returns; the GPU context stays usable. Follow it with
+ * fl_device_status() to read (and clear) the status.
+ */
+fl_status fl_debug_wait_timeout(int limit_us, void* stream);
+
+/* Library version string. */
+const char* fl_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FUSEDLIN_H */

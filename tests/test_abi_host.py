@@ -1,0 +1,143 @@
+"""The C ABI on the host (no GPU needed).
+
+The library loads, exports every function include/fusedlin.h declares, and
+rejects bad arguments with the documented status before touching CUDA.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gemm_epilogue_tma_gb300 as fl
+from gemm_epilogue_tma_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+OK, INVALID, UNSUPPORTED, ALIGN, WORKSPACE, CUDA, TIMEOUT = range(7)
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return fl.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "fusedlin.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(fl_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("fl_gemm_epilogue", "fl_norm_gemm", "fl_swiglu_ffn", "fl_swiglu_ffn_workspace_size",
+              "fl_last_error", "fl_device_status"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+        assert name in fl.SIGNATURES, f"binding lacks {name}"
+
+
+def test_version(L):
+    assert "sm_103a" in fl.version()
+
+
+# Fake, well-aligned device addresses: validation never dereferences them, and
+# every call below fails validation (or finds no device) before any launch.
+BASE = 0x7F0000000000
+
+
+def addr(i, off=0):
+    return ctypes.c_void_p(BASE + i * (1 << 32) + off)
+
+
+def gemm(L, A=addr(0), W=addr(1), bias=addr(2), res=addr(3), out=addr(4), M=64, N=64, K=64, p=0, dt=0):
+    return L.fl_gemm_epilogue(A, W, bias, res, out, M, N, K, p, dt, None)
+
+
+def test_gemm_epilogue_validation(L):
+    assert gemm(L, A=None) == INVALID
+    assert gemm(L, W=None) == INVALID
+    assert gemm(L, out=None) == INVALID
+    assert gemm(L, bias=None, p=0) == INVALID            # gemm_bias_gelu needs a bias
+    assert gemm(L, res=None, p=4) == INVALID             # gemm_bias_residual needs a residual
+    assert gemm(L, p=7) == INVALID and "fl_norm_gemm" in fl.last_error()
+    assert gemm(L, p=8) == INVALID
+    assert gemm(L, p=9) == INVALID and gemm(L, p=-1) == INVALID
+    assert gemm(L, dt=2) == INVALID
+    assert gemm(L, M=0) == INVALID and gemm(L, N=0) == INVALID and gemm(L, K=-8) == INVALID
+    assert gemm(L, K=60) == ALIGN and gemm(L, N=12) == ALIGN
+    assert gemm(L, A=addr(0, 8)) == ALIGN
+    assert gemm(L, out=addr(4, 2)) == ALIGN
+    assert gemm(L, bias=addr(2, 4)) == ALIGN
+    # out overlapping an input; residual may alias out only exactly
+    assert gemm(L, out=addr(0, 64)) == INVALID
+    assert gemm(L, p=4, res=addr(4, 16)) == INVALID and "alias" in fl.last_error()
+    # unused pointers are ignored (no bias for gemm_gelu, even misaligned)
+    st = gemm(L, p=5, bias=addr(2, 3), res=addr(3, 1))
+    assert st in (UNSUPPORTED, CUDA)  # reaches the device query: none on this machine
+
+
+def test_valid_call_without_gpu_reports_unsupported(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert gemm(L) == UNSUPPORTED
+    assert fl.last_error()
+    assert gemm(L, p=4, res=addr(4)) == UNSUPPORTED  # exact alias of residual and out is allowed
+
+
+def norm(L, x=addr(0), g=addr(1), b=addr(2), W=addr(3), bias=None, out=addr(4), M=64, N=64, K=64, eps=1e-6,
+         nk=0, act=0, dt=0):
+    return L.fl_norm_gemm(x, g, b, W, bias, out, M, N, K, eps, nk, act, dt, None)
+
+
+def test_norm_gemm_validation(L):
+    assert norm(L, x=None) == INVALID and norm(L, g=None) == INVALID and norm(L, W=None) == INVALID
+    assert norm(L, nk=2) == INVALID and norm(L, act=4) == INVALID and norm(L, dt=-1) == INVALID
+    assert norm(L, eps=-1.0) == INVALID and norm(L, eps=float("nan")) == INVALID
+    assert norm(L, eps=float("inf")) == INVALID
+    assert norm(L, K=20) == ALIGN
+    assert norm(L, g=addr(1, 2)) == ALIGN
+    assert norm(L, nk=1, b=addr(2, 2)) == ALIGN          # LayerNorm reads beta
+    assert norm(L, nk=0, b=addr(2, 2)) != ALIGN          # RMS ignores beta
+    assert norm(L, out=addr(3, 32)) == INVALID          # out overlaps W
+
+
+def ffn(L, x=addr(0), g=addr(1), Wg=addr(2), Wu=addr(3), Wd=addr(4), bd=None, out=addr(5), M=16, D=64, F=128,
+        eps=1e-6, ws=addr(6), wsb=None, dt=1):
+    if wsb is None:
+        wsb = M * F * 2
+    return L.fl_swiglu_ffn(x, g, Wg, Wu, Wd, bd, out, M, D, F, eps, ws, wsb, dt, None)
+
+
+def test_swiglu_validation(L):
+    assert L.fl_swiglu_ffn_workspace_size(16, 128, 1) == 16 * 128 * 2
+    assert L.fl_swiglu_ffn_workspace_size(0, 128, 1) == 0
+    assert ffn(L, ws=None) == WORKSPACE
+    assert ffn(L, wsb=16 * 128 * 2 - 1) == WORKSPACE
+    assert ffn(L, ws=addr(6, 8)) == ALIGN
+    assert ffn(L, F=100) == ALIGN and ffn(L, D=36) == ALIGN
+    assert ffn(L, Wu=None) == INVALID
+    assert ffn(L, out=addr(0)) == INVALID               # out must not alias x
+    assert ffn(L, ws=addr(5, 16)) == INVALID            # workspace overlaps out
+
+
+def test_options(L):
+    assert L.fl_set_option(0, 100) == INVALID
+    assert L.fl_set_option(0, 256) == OK and L.fl_set_option(0, 0) == OK
+    assert L.fl_set_option(1, 3) == INVALID and L.fl_set_option(1, 0) == OK
+    assert L.fl_set_option(2, 0) == INVALID and L.fl_set_option(2, 2000) == OK
+    assert L.fl_set_option(3, 17) == INVALID and L.fl_set_option(3, 0) == OK
+    assert L.fl_set_option(42, 0) == INVALID
+    assert L.fl_debug_wait_timeout(0, None) == INVALID
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(fl, "_lib", None)
+    monkeypatch.setattr(fl, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        fl.lib()

@@ -1,0 +1,239 @@
+"""CUDA path vs the float64 oracle, element by element (needs an sm_103a GPU).
+
+Every call goes through the C ABI (the ctypes binding). Small ragged shapes
+cover partial tiles in M, N and K; the workload sizes of the fused-layer
+pages are checked on every element where the oracle is quick, and on a
+seeded sample of rows (always the first and the last) where it is not.
+Tolerances are in tests/parity.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gemm_epilogue_tma_gb300 as fl
+import oracle
+from gemm_epilogue_tma_gb300 import _build
+from gemm_epilogue_tma_gb300 import synthetic as syn
+from parity import assert_close, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+GEMM_FIRST = syn.PATTERNS[:7]
+DTYPES = ("f16", "bf16")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def library():
+    _build.build()
+    fl.lib()
+    torch.cuda.set_device(0)
+    yield
+    fl.set_option("tile_n", 0)
+    fl.set_option("variant", 0)
+    fl.set_option("split_k", 0)
+    fl.device_status()
+
+
+def dev(t):
+    return None if t is None else t.cuda()
+
+
+def f64(t):
+    return syn.as_f64(t)
+
+
+def run_pattern(t, pattern, rows=None, out=None):
+    """Launch one of the nine patterns on GPU copies of t; oracle on `rows` (all if None)."""
+    eps = 1e-5 if pattern == "layernorm_gemm" else 1e-6
+    A, W = dev(t["A"]), dev(t["W"])
+    if pattern == "rmsnorm_gemm":
+        got = fl.norm_gemm(A, dev(t["gamma"]), W, eps=eps, norm="rms", out=out)
+    elif pattern == "layernorm_gemm":
+        got = fl.norm_gemm(A, dev(t["gamma"]), W, beta=dev(t["beta"]), eps=eps, norm="layer", out=out)
+    else:
+        got = fl.gemm_epilogue(A, W, bias=dev(t.get("bias")), residual=dev(t.get("residual")), pattern=pattern,
+                               out=out)
+    torch.cuda.synchronize()
+    sel = slice(None) if rows is None else rows
+    res = t.get("residual")
+    ref = oracle.fused_pattern(pattern, f64(t["A"])[sel], f64(t["W"]), f64(t.get("bias")),
+                               None if res is None else f64(res)[sel], f64(t.get("gamma")), f64(t.get("beta")),
+                               eps=eps)
+    return got[sel] if rows is not None else got, ref
+
+
+# ---------------------------------------------------------------------------
+# ragged shapes, every pattern, both dtypes, both tile widths
+# ---------------------------------------------------------------------------
+RAGGED = [(1, 8, 8), (7, 24, 40), (200, 136, 328), (129, 264, 72), (300, 520, 1000), (128, 256, 64)]
+
+
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("shape", RAGGED, ids=lambda s: "x".join(map(str, s)))
+def test_all_patterns_ragged(dt, shape):
+    M, N, K = shape
+    t = syn.dense_layer_inputs(M, N, K, dt)
+    for pattern in syn.PATTERNS:
+        got, ref = run_pattern(t, pattern)
+        assert_close(got, ref, dt, f"{pattern} {dt} {M}x{N}x{K}")
+    fl.device_status()
+
+
+@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("dt", DTYPES)
+def test_tile_widths(tile_n, dt):
+    M, N, K = 384, 776, 520
+    t = syn.dense_layer_inputs(M, N, K, dt)
+    fl.set_option("tile_n", tile_n)
+    try:
+        for pattern in ("gemm_bias_gelu", "gemm_bias_residual", "gemm_silu", "rmsnorm_gemm", "layernorm_gemm"):
+            got, ref = run_pattern(t, pattern)
+            assert_close(got, ref, dt, f"{pattern} {dt} BN={tile_n}")
+    finally:
+        fl.set_option("tile_n", 0)
+
+
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("norm", ["rms", "layer"])
+@pytest.mark.parametrize("act", ["none", "gelu", "silu", "relu"])
+def test_norm_gemm_bias_act(dt, norm, act):
+    M, N, K = 260, 200, 456
+    t = syn.norm_gemm_inputs(M, N, K, norm, dt, with_bias=True)
+    eps = 1e-5
+    got = fl.norm_gemm(dev(t["x"]), dev(t["gamma"]), dev(t["W"]), beta=dev(t["beta"]), bias=dev(t["bias"]),
+                       eps=eps, norm=norm, act=act)
+    torch.cuda.synchronize()
+    ref = oracle.norm_gemm(f64(t["x"]), f64(t["gamma"]), f64(t["beta"]), f64(t["W"]), f64(t["bias"]), eps, norm, act)
+    assert_close(got, ref, dt, f"{norm} {act} {dt}")
+
+
+def test_layernorm_without_beta_and_offset_rows():
+    """beta = NULL means zero; rows with a large common offset normalise without cancellation."""
+    M, N, K = 130, 64, 192
+    t = syn.norm_gemm_inputs(M, N, K, "layer", "f16")
+    x = (t["x"].double() * 0.5 + 40.0).to(torch.float16)
+    got = fl.norm_gemm(dev(x), dev(t["gamma"]), dev(t["W"]), eps=1e-5, norm="layer")
+    torch.cuda.synchronize()
+    ref = oracle.norm_gemm(f64(x), f64(t["gamma"]), None, f64(t["W"]), None, 1e-5, "layer")
+    assert_close(got, ref, "f16", "layernorm offset rows")
+
+
+def test_residual_aliases_out():
+    M, N, K = 256, 384, 512
+    t = syn.gemm_inputs(M, N, K, "gemm_bias_residual", "bf16")
+    res = dev(t["residual"])
+    got = fl.gemm_epilogue(dev(t["A"]), dev(t["W"]), bias=dev(t["bias"]), residual=res, out=res,
+                           pattern="gemm_bias_residual")
+    torch.cuda.synchronize()
+    assert got.data_ptr() == res.data_ptr()
+    ref = oracle.gemm_epilogue(f64(t["A"]), f64(t["W"]), f64(t["bias"]), f64(t["residual"]), "gemm_bias_residual")
+    assert_close(got, ref, "bf16", "residual aliasing out")
+
+
+def test_no_write_outside_out():
+    """A sentinel region on both sides of out stays untouched (ragged tails are clipped)."""
+    M, N, K = 131, 72, 136
+    t = syn.dense_layer_inputs(M, N, K, "f16")
+    pad = 4096
+    buf = torch.full((pad + M * N + pad,), 1234.0, dtype=torch.float16, device="cuda")
+    out = buf[pad:pad + M * N].view(M, N)
+    for pattern in ("gemm_bias_gelu", "gemm_bias_residual", "rmsnorm_gemm", "layernorm_gemm"):
+        got, ref = run_pattern(t, pattern, out=out)
+        assert_close(got, ref, "f16", pattern)
+        assert bool((buf[:pad] == 1234.0).all()) and bool((buf[pad + M * N:] == 1234.0).all()), pattern
+
+
+def test_repeatable_bitwise():
+    M, N, K = 384, 512, 768
+    t = syn.dense_layer_inputs(M, N, K, "bf16")
+    a = run_pattern(t, "rmsnorm_gemm")[0].clone()
+    b = run_pattern(t, "rmsnorm_gemm")[0]
+    assert torch.equal(a, b)
+
+
+# ---------------------------------------------------------------------------
+# the workloads of the pages, at full size
+# ---------------------------------------------------------------------------
+def test_gemm_bias_gelu_512x1024x1024_all_elements():
+    """fp16 gemm_bias_gelu, A[512,1024], W[1024,1024], bias[1024], seed 0."""
+    t = syn.gemm_inputs(512, 1024, 1024, "gemm_bias_gelu", "f16", seed=0)
+    got, ref = run_pattern(t, "gemm_bias_gelu")
+    assert_close(got, ref, "f16", "gemm_bias_gelu 512x1024x1024")
+
+
+def test_rmsnorm_gemm_512x4096x4096_all_elements():
+    """fp16 rmsnorm_gemm, x[512,4096], gamma ~ N(1,0.1), eps 1e-6, W[4096,4096], no bias."""
+    t = syn.gemm_inputs(512, 4096, 4096, "rmsnorm_gemm", "f16")
+    got, ref = run_pattern(t, "rmsnorm_gemm")
+    assert_close(got, ref, "f16", "rmsnorm_gemm 512x4096x4096")
+
+
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("M", [512, 1024, 2048, 4096])
+def test_nine_patterns_n4096_k4096_sampled_rows(dt, M):
+    t = syn.dense_layer_inputs(M, 4096, 4096, dt)
+    rows = sample_rows(M)
+    for pattern in syn.PATTERNS:
+        got, ref = run_pattern(t, pattern, rows=rows)
+        assert_close(got, ref, dt, f"{pattern} {dt} M={M}")
+    fl.device_status()
+
+
+def test_swiglu_ffn_4096x4096x11008_sampled_rows():
+    """bf16 Llama-style FFN block: x[4096,4096], Wg/Wu[11008,4096], Wd[4096,11008], + x."""
+    M, D, F = 4096, 4096, 11008
+    t = syn.swiglu_inputs(M, D, F, "bf16")
+    g = {k: dev(v) for k, v in t.items()}
+    ws = torch.empty(fl.swiglu_ffn_workspace_size(M, F, torch.bfloat16), dtype=torch.uint8, device="cuda")
+    got = fl.swiglu_ffn(g["x"], g["gamma"], g["Wg"], g["Wu"], g["Wd"], eps=1e-6, workspace=ws)
+    torch.cuda.synchronize()
+    rows = sample_rows(M, n=64)
+    f = {k: f64(v) for k, v in t.items()}
+    ref = oracle.swiglu_ffn(f["x"][rows], f["gamma"], f["Wg"], f["Wu"], f["Wd"], None, 1e-6, "bf16")
+    assert_close(got[rows], ref, "bf16", "swiglu 4096x4096x11008")
+    # the workspace holds h: check it against the oracle's unrounded hidden activation too
+    h = ws.view(torch.bfloat16).view(M, F)[rows]
+    href = oracle.swiglu_hidden(f["x"][rows], f["gamma"], f["Wg"], f["Wu"], 1e-6)
+    assert_close(h, href, "bf16", "swiglu hidden h")
+
+
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("with_bias", [False, True])
+@pytest.mark.parametrize("shape", [(1, 64, 128), (136, 256, 384), (300, 264, 520)], ids=lambda s: "x".join(map(str, s)))
+def test_swiglu_ffn_small_all_elements(dt, with_bias, shape):
+    M, D, F = shape
+    t = syn.swiglu_inputs(M, D, F, dt, with_bias=with_bias)
+    g = {k: dev(v) for k, v in t.items()}
+    got = fl.swiglu_ffn(g["x"], g["gamma"], g["Wg"], g["Wu"], g["Wd"], bias_down=g["bias_down"], eps=1e-6)
+    torch.cuda.synchronize()
+    f = {k: f64(v) for k, v in t.items()}
+    ref = oracle.swiglu_ffn(f["x"], f["gamma"], f["Wg"], f["Wu"], f["Wd"], f["bias_down"], 1e-6, dt)
+    assert_close(got, ref, dt, f"swiglu {dt} {shape}")
+
+
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("D", [1024, 2048, 4096])
+@pytest.mark.parametrize("M", [1, 32, 128, 512, 1024])
+def test_decode_sweep_rmsnorm_all_elements(dt, D, M):
+    """rmsnorm_gemm with square W[D,D]: the decode-shape sweep of the LLMBoost page."""
+    t = syn.norm_gemm_inputs(M, D, D, "rms", dt)
+    got = fl.norm_gemm(dev(t["x"]), dev(t["gamma"]), dev(t["W"]), eps=1e-6, norm="rms")
+    torch.cuda.synchronize()
+    ref = oracle.norm_gemm(f64(t["x"]), f64(t["gamma"]), None, f64(t["W"]), None, 1e-6, "rms")
+    assert_close(got, ref, dt, f"decode rms {dt} M={M} D={D}")
+
+
+# ---------------------------------------------------------------------------
+# bounded waits
+# ---------------------------------------------------------------------------
+def test_bounded_wait_reports_timeout_and_context_survives():
+    fl.device_status()  # clean slate
+    fl.debug_wait_timeout(2000)  # a wait that nothing completes, 2 ms limit
+    with pytest.raises(fl.FusedLinError) as e:
+        fl.device_status()
+    assert e.value.status == 6
+    fl.device_status()  # cleared
+    # the context still works
+    t = syn.gemm_inputs(64, 64, 64, "gemm_bias", "f16")
+    got, ref = run_pattern(t, "gemm_bias")
+    assert_close(got, ref, "f16", "after timeout")
