@@ -1,0 +1,480 @@
+"""Throughput of the fused dense layer on GB300, one JSON line on stdout.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+A step is one call of the hot path over one batch of synthetic input. The
+default workload is the fused RMSNorm -> linear layer in fp16 with
+x[512, 4096], gamma[4096], eps 1e-6 and W[4096, 4096], no bias (the shape of
+the LLMBoost fused_rmsnorm_linear benchmark). Inputs rotate over enough copies
+to exceed the 129 MB L2 between steps, so every step reads its operands from
+HBM.
+
+--impl ours (default): the CUDA path through the C ABI; `value` is device
+throughput with inputs resident in HBM; `e2e` repeats it through the same
+call with pinned host buffers, host<->device copies inside the timed region.
+--impl reference: the float64 CPU oracle on the host cores, one bounded
+sample of the workload per step.
+
+With torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the path has no exchange step); the time is the maximum over ranks and the
+value counts the work of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused-kernel TFLOP/s & % of GB300 tensor peak; GB/s vs HBM at decode shapes"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# The pages' own number for this exact workload: fused RMSNorm -> Linear,
+# [512,4096] x [4096,4096] fp16, 0.208 ms on an A30 (LLMBoost benchmark table).
+PAGE_FUSED_MS = 0.208
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+WORKLOADS = {
+    "rmsnorm_gemm_f16_512x4096x4096": dict(kind="norm", norm="rms", dtype="f16", M=512, N=4096, K=4096, eps=1e-6),
+    "gemm_bias_gelu_f16_512x1024x1024": dict(kind="pattern", pattern="gemm_bias_gelu", dtype="f16", M=512, N=1024,
+                                             K=1024),
+    "swiglu_ffn_bf16_4096x4096x11008": dict(kind="swiglu", dtype="bf16", M=4096, D=4096, F=11008, eps=1e-6),
+}
+
+
+def parse_workload(name: str) -> dict:
+    """A named workload, or kind:args: pattern:<name>:<dt>:M:N:K, norm:<rms|layer>:<dt>:M:N:K,
+    swiglu:<dt>:M:D:F."""
+    if name in WORKLOADS:
+        return dict(WORKLOADS[name], name=name)
+    parts = name.split(":")
+    if parts[0] == "pattern":
+        _, pat, dt, M, N, K = parts
+        return dict(kind="pattern", pattern=pat, dtype=dt, M=int(M), N=int(N), K=int(K), name=name)
+    if parts[0] == "norm":
+        _, nm, dt, M, N, K = parts
+        return dict(kind="norm", norm=nm, dtype=dt, M=int(M), N=int(N), K=int(K), eps=1e-6 if nm == "rms" else 1e-5,
+                    name=name)
+    if parts[0] == "swiglu":
+        _, dt, M, D, F = parts
+        return dict(kind="swiglu", dtype=dt, M=int(M), D=int(D), F=int(F), eps=1e-6, name=name)
+    raise SystemExit(f"unknown workload {name}")
+
+
+def describe(w: dict) -> str:
+    if w["kind"] == "norm":
+        nm = "rmsnorm_gemm" if w["norm"] == "rms" else "layernorm_gemm"
+        return f"{nm} {w['dtype']}: x[{w['M']},{w['K']}] gamma[{w['K']}] eps={w['eps']:g} W[{w['N']},{w['K']}], no bias"
+    if w["kind"] == "pattern":
+        return f"{w['pattern']} {w['dtype']}: A[{w['M']},{w['K']}] W[{w['N']},{w['K']}]"
+    return (f"swiglu_ffn {w['dtype']}: x[{w['M']},{w['D']}] RMSNorm, Wg/Wu[{w['F']},{w['D']}], "
+            f"Wd[{w['D']},{w['F']}], + x")
+
+
+def flops_per_step(w: dict) -> float:
+    """2MNK plus the epilogue / prologue element ops (norm 3 per input element,
+    row scale 1 per output, bias 1, gelu 8, silu 4, relu 1, residual 1, SwiGLU product 1)."""
+    if w["kind"] == "swiglu":
+        M, D, F = w["M"], w["D"], w["F"]
+        return 6.0 * M * D * F + 3 * M * D + 2 * M * F + 4 * M * F + M * F + M * D
+    M, N, K = w["M"], w["N"], w["K"]
+    f = 2.0 * M * N * K
+    if w["kind"] == "norm":
+        return f + 3 * M * K + M * N
+    p = w["pattern"]
+    f += M * N * (("bias" in p) + 8 * ("gelu" in p) + 4 * ("silu" in p) + ("relu" in p) + ("residual" in p))
+    return f
+
+
+def bytes_per_step(w: dict) -> float:
+    """Algorithmic HBM bytes: every operand read once, the output written once."""
+    e = 2
+    if w["kind"] == "swiglu":
+        M, D, F = w["M"], w["D"], w["F"]
+        return e * (M * D + D + 2 * F * D + 2 * M * F + D * F + M * D + M * D)
+    M, N, K = w["M"], w["N"], w["K"]
+    b = e * (M * K + N * K + M * N)
+    if w["kind"] == "norm":
+        b += e * K * (2 if w["norm"] == "layer" else 1)
+    else:
+        p = w["pattern"]
+        b += e * N * ("bias" in p) + e * M * N * ("residual" in p)
+    return b
+
+
+def make_inputs(w: dict):
+    from gemm_epilogue_tma_gb300 import synthetic as syn
+    if w["kind"] == "norm":
+        return syn.norm_gemm_inputs(w["M"], w["N"], w["K"], w["norm"], w["dtype"])
+    if w["kind"] == "pattern":
+        return syn.gemm_inputs(w["M"], w["N"], w["K"], w["pattern"], w["dtype"])
+    return syn.swiglu_inputs(w["M"], w["D"], w["F"], w["dtype"])
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_sources_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gemm_epilogue_tma_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from a committed ncu capture, if the kernel sources are unchanged since."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    rec = d.get(workload)
+    if not rec or rec.get("sources") != kernel_sources_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock, power and throttle reasons in the background."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, interval_ms: int = 50):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", str(interval_ms)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [c.strip() for c in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        inside = [s for (t, s) in self.samples if t0 <= t <= t1 + 0.05]
+        window = "timed_region"
+        if not inside:
+            inside = [s for (_, s) in self.samples]
+            window = "whole_run"
+        mhz, maxmhz, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for s in inside:
+            try:
+                mhz.append(float(s[1]))
+                maxmhz.append(float(s[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, s[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        if not mhz:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": window}
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": max(maxmhz), "reasons": sorted(reasons),
+                "samples": len(mhz), "window": window}
+
+
+def dist_setup():
+    """Rank, world size, and a process group when launched by torchrun."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Maximum of a per-rank float over the process group (identity for one rank)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def cpu_cores_used() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def oracle_step(w: dict, f64: dict, row0: int, rows: int):
+    """The float64 oracle on rows [row0, row0+rows) of the workload (rows are independent)."""
+    import oracle
+    sl = slice(row0, row0 + rows)
+    if w["kind"] == "norm":
+        return oracle.norm_gemm(f64["x"][sl], f64["gamma"], f64.get("beta"), f64["W"], None, w["eps"], w["norm"])
+    if w["kind"] == "pattern":
+        r = f64.get("residual")
+        return oracle.gemm_epilogue(f64["A"][sl], f64["W"], f64.get("bias"), None if r is None else r[sl],
+                                    w["pattern"])
+    return oracle.swiglu_ffn(f64["x"][sl], f64["gamma"], f64["Wg"], f64["Wu"], f64["Wd"], None, w["eps"], w["dtype"])
+
+
+def rows_of(w):
+    return w["M"]
+
+
+def flops_of_rows(w, rows):
+    return flops_per_step(w) * rows / rows_of(w)
+
+
+def cpu_baseline(w: dict, seconds: float = 10.0, rows_per_call: int = 16) -> dict:
+    """The oracle as it stands, timed on a bounded sample of the workload's rows."""
+    from gemm_epilogue_tma_gb300 import synthetic as syn
+    t = make_inputs(w)
+    f64 = {k: syn.as_f64(v) for k, v in t.items() if v is not None}
+    M = rows_of(w)
+    rows_per_call = min(rows_per_call, M)
+    done, t0 = 0, time.perf_counter()
+    while True:
+        oracle_step(w, f64, done % max(1, M - rows_per_call + 1), rows_per_call)
+        done += rows_per_call
+        el = time.perf_counter() - t0
+        if el >= seconds or done >= 64 * M:
+            break
+    tf = flops_of_rows(w, done) / el / 1e12
+    return {"value": tf, "unit": "TFLOP/s", "cores": cpu_cores_used(), "kind": "oracle",
+            "sample": f"{done} rows of {M} ({rows_per_call} per call) in {el:.1f} s, float64 NumPy"}
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+def run_reference(args, w: dict, rank: int, world: int):
+    if rank != 0:
+        return
+    from gemm_epilogue_tma_gb300 import synthetic as syn
+    t = make_inputs(w)
+    f64 = {k: syn.as_f64(v) for k, v in t.items() if v is not None}
+    M = rows_of(w)
+    rows = 1  # one row of the workload per step keeps --steps K within minutes
+    for i in range(args.warmup):
+        oracle_step(w, f64, i % M, rows)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle_step(w, f64, i % M, rows)
+    el = time.perf_counter() - t0
+    value = flops_of_rows(w, rows * args.steps) / el / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": describe(w), "name": w["name"], "sample_rows_per_step": rows,
+                   "parallelism": "replicas"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores_used(), "kind": "oracle",
+                         "sample": f"{rows} row of {M} per step, float64 NumPy oracle"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w: dict, rank: int, world: int, local: int):
+    import torch
+
+    import gemm_epilogue_tma_gb300 as fl
+
+    torch.cuda.set_device(local)
+    fl.lib()
+    dev = torch.device("cuda", local)
+    t = make_inputs(w)
+    set_bytes = sum(v.numel() * v.element_size() for v in t.values() if v is not None)
+    out_shape = (w["M"], w["N"]) if w["kind"] != "swiglu" else (w["M"], w["D"])
+    out_bytes = out_shape[0] * out_shape[1] * 2
+    nsets = max(2, int(3 * L2_BYTES // (set_bytes + out_bytes)) + 1)
+    sets = []
+    for _ in range(nsets):
+        g = {k: (v.to(dev) if v is not None else None) for k, v in t.items()}
+        g["out"] = torch.empty(out_shape, dtype=t[next(iter(t))].dtype, device=dev)
+        if w["kind"] == "swiglu":
+            g["ws"] = torch.empty(fl.swiglu_ffn_workspace_size(w["M"], w["F"], w["dtype"]), dtype=torch.uint8,
+                                  device=dev)
+        sets.append(g)
+    launches_per_step = 2 if w["kind"] == "swiglu" else 1
+
+    def step(g, stream=None):
+        if w["kind"] == "norm":
+            fl.norm_gemm(g["x"], g["gamma"], g["W"], beta=g.get("beta"), out=g["out"], eps=w["eps"],
+                         norm=w["norm"], stream=stream)
+        elif w["kind"] == "pattern":
+            fl.gemm_epilogue(g["A"], g["W"], bias=g.get("bias"), residual=g.get("residual"), out=g["out"],
+                             pattern=w["pattern"], stream=stream)
+        else:
+            fl.swiglu_ffn(g["x"], g["gamma"], g["Wg"], g["Wu"], g["Wd"], out=g["out"], eps=w["eps"],
+                          workspace=g["ws"], stream=stream)
+
+    stream = torch.cuda.current_stream(dev)
+    sampler = ClockSampler(local) if rank == 0 else None
+    for i in range(args.warmup):
+        step(sets[i % nsets])
+    torch.cuda.synchronize()
+    fl.device_status()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(sets[i % nsets])
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    barrier(world)
+    ms = ev0.elapsed_time(ev1)
+    fl.device_status()
+    ms_max = max_over_ranks(ms, world)
+    clocks = sampler.summary(wall0, wall1) if sampler else None
+    if sampler:
+        sampler.stop()
+
+    # end to end through the same call: pinned host inputs in, result back to pinned host
+    host = {k: (v.pin_memory() if v is not None else None) for k, v in t.items()}
+    hout = torch.empty(out_shape, dtype=sets[0]["out"].dtype).pin_memory()
+    g = sets[0]
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+    e2e_steps = max(3, min(args.steps, 200))
+
+    def e2e_step():
+        for k, v in host.items():
+            if v is not None:
+                g[k].copy_(v, non_blocking=True)
+        step(g)
+        hout.copy_(g["out"], non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    fl.device_status()
+
+    if rank != 0:
+        return
+    flops = flops_per_step(w)
+    value = flops * args.steps * world / (ms_max / 1e3) / 1e12
+    per_launch_ms = ms / args.steps
+    peaks, peak_src = load_peaks()
+    tensor_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    # dominant kernel: the only one for single-launch workloads; for the FFN the
+    # two launches are reported together
+    achieved = flops / (per_launch_ms / 1e3) / 1e12
+    traffic = recorded_traffic(w["name"])
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": tensor_peak, "unit": "TFLOP/s",
+                "frac": achieved / tensor_peak, "traffic": traffic,
+                "peak_source": f"bf16_tflops (burst, fp16 dense rate equal) of {peak_src}",
+                "algorithmic_bytes": bytes_per_step(w),
+                "hbm_gbs": bytes_per_step(w) / (per_launch_ms / 1e3) / 1e9,
+                "hbm_frac": bytes_per_step(w) / (per_launch_ms / 1e3) / 1e9 / float(peaks.get("hbm_gbs", 6800.0))}
+    vs = None
+    if w["name"] == "rmsnorm_gemm_f16_512x4096x4096":
+        vs = value / world / (flops / (PAGE_FUSED_MS / 1e3) / 1e12)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": vs, "dtype": w["dtype"], "data": "synthetic",
+        "config": {"workload": describe(w), "name": w["name"],
+                   "l2": f"inputs rotate over {nsets} copies ({nsets * (set_bytes + out_bytes) / 2**20:.0f} MiB "
+                         f"> 129 MB L2)",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "vs_baseline_ref": "A30 fused RMSNorm->Linear 0.208 ms (LLMBoost page), other hardware"},
+        "roofline": roofline,
+        "e2e": {"value": flops * e2e_steps * world / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out_bytes},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, seconds=args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="rmsnorm_gemm_f16_512x4096x4096")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be at least 3")
+    w = parse_workload(args.workload)
+    rank, world, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+        backend = "gloo" if args.impl == "reference" else "nccl"
+        dist.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, w, rank, world)
+        else:
+            run_ours(args, w, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
