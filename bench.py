@@ -329,6 +329,9 @@ def run_ours(args, w: dict, rank: int, world: int, local: int):
 
     torch.cuda.set_device(local)
     fl.lib()
+    fl.set_option("tile_n", args.tile_n)
+    fl.set_option("variant", args.variant)
+    fl.set_option("split_k", args.split_k)
     dev = torch.device("cuda", local)
     t = make_inputs(w)
     set_bytes = sum(v.numel() * v.element_size() for v in t.values() if v is not None)
@@ -456,6 +459,9 @@ def main(argv=None):
     ap.add_argument("--workload", default="rmsnorm_gemm_f16_512x4096x4096")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tile-n", type=int, default=0, help="force the CTA tile width (128/256; 0 = auto)")
+    ap.add_argument("--variant", type=int, default=0, help="force 1 = tile kernel, 2 = small-M split-K kernel")
+    ap.add_argument("--split-k", type=int, default=0, help="force the K split of the small-M kernel")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")

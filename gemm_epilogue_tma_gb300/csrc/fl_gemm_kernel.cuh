@@ -45,6 +45,10 @@ struct DTypeOps<DT_F16> {
     __device__ static __forceinline__ float2 unpack(uint32_t u) {
         return __half22float2(*reinterpret_cast<__half2*>(&u));
     }
+    __device__ static __forceinline__ uint32_t mul2(uint32_t a, uint32_t b) {
+        __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+        return *reinterpret_cast<uint32_t*>(&r);
+    }
 };
 
 template <>
@@ -56,6 +60,10 @@ struct DTypeOps<DT_BF16> {
     }
     __device__ static __forceinline__ float2 unpack(uint32_t u) {
         return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&u));
+    }
+    __device__ static __forceinline__ uint32_t mul2(uint32_t a, uint32_t b) {
+        __nv_bfloat162 r = __hmul2(*reinterpret_cast<__nv_bfloat162*>(&a), *reinterpret_cast<__nv_bfloat162*>(&b));
+        return *reinterpret_cast<uint32_t*>(&r);
     }
 };
 
@@ -160,6 +168,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     const uint32_t drain_bar = bar0 + 8u * (3 * S + 6);
     const uint32_t slot_addr = sbase + C::OFF_SLOT;
     float* rowscale = reinterpret_cast<float*>(smem + C::OFF_ROWSCALE);  // [2][128]
+    auto gb_slot = [&](int s) { return sbase + C::OFF_GB + 256u * s; };  // gamma | beta slices
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -184,6 +193,8 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         tma_prefetch_desc(&p.tmB);
         if (DUAL) tma_prefetch_desc(&p.tmB2);
         tma_prefetch_desc(&p.tmOut);
+        if (PRO != PRO_NONE) tma_prefetch_desc(&p.tmGamma);
+        if (PRO == PRO_LN && p.beta != nullptr) tma_prefetch_desc(&p.tmBeta);
     }
     if (warp == 1) {
         tmem_alloc(slot_addr, C::TMEM_COLS);
@@ -201,7 +212,8 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
             uint32_t ph = 0;
             int issued = 0;
             bool ok = true;
-            const uint32_t main_bytes = C::STAGE_BYTES;
+            const uint32_t main_bytes = C::STAGE_BYTES + (PRO != PRO_NONE ? 128u : 0u) +
+                                        (PRO == PRO_LN && p.beta != nullptr ? 128u : 0u);
             for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
                 const int m0 = (tile % p.num_m_blocks) * kBM;
                 const int n0 = (tile / p.num_m_blocks) * BN;
@@ -218,6 +230,11 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                         if (!stats) {
                             tma_load_2d(stage_b(s), &p.tmB, full_bar(s), kb * kBK, n0);
                             if (DUAL) tma_load_2d(stage_b2(s), &p.tmB2, full_bar(s), kb * kBK, n0);
+                            if (PRO != PRO_NONE) {
+                                tma_load_2d(gb_slot(s), &p.tmGamma, full_bar(s), kb * kBK, 0);
+                                if (PRO == PRO_LN && p.beta != nullptr)
+                                    tma_load_2d(gb_slot(s) + 128, &p.tmBeta, full_bar(s), kb * kBK, 0);
+                            }
                         }
                         ++issued;
                         if (++s == S) {
@@ -301,7 +318,6 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         uint32_t ph = 0;
         int it = 0;
         bool ok = true;
-        const __half* g16 = reinterpret_cast<const __half*>(p.gamma);
         for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
             float mean = 0.f, rstd = 1.f, ss = 0.f;
             if (PRO == PRO_LN) {
@@ -355,40 +371,55 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                     ok = false;
                     break;
                 }
+                // gamma (and beta) of this K block arrived with the stage; columns
+                // past K are zero in x, gamma and beta, so they stay zero
                 const uint32_t row = stage_a(s) + t * 128;
-                const int k0 = kb * kBK;
+                const uint32_t gsl = gb_slot(s);
+                uint4 xv[8], gv[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int k = k0 + j * 8;
-                    if (k < p.K) {
-                        const uint32_t addr = row + ((j ^ sw) << 4);
-                        uint4 v = ld_shared_v4(addr);
-                        const uint4 gv = ldg_v4(g16 + k);
-                        uint32_t xin[4] = {v.x, v.y, v.z, v.w};
-                        uint32_t gin[4] = {gv.x, gv.y, gv.z, gv.w};
-                        uint32_t bin[4] = {0u, 0u, 0u, 0u};
-                        if (PRO == PRO_LN && p.beta != nullptr) {
-                            const uint4 bv = ldg_v4(reinterpret_cast<const __half*>(p.beta) + k);
-                            bin[0] = bv.x; bin[1] = bv.y; bin[2] = bv.z; bin[3] = bv.w;
-                        }
-                        uint32_t o[4];
+                for (int j = 0; j < 8; ++j) xv[j] = ld_shared_v4(row + ((j ^ sw) << 4));
+#pragma unroll
+                for (int j = 0; j < 8; ++j) gv[j] = ld_shared_v4(gsl + j * 16);
+                if (PRO == PRO_RMS) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t xw[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
-                            const float2 x2 = Ops::unpack(xin[q]);
-                            const float2 g2 = Ops::unpack(gin[q]);
-                            if (PRO == PRO_RMS) {
-                                ss = fmaf(x2.x, x2.x, ss);
-                                ss = fmaf(x2.y, x2.y, ss);
-                                o[q] = Ops::pack(x2.x * g2.x, x2.y * g2.y);
-                            } else {
-                                const float2 b2 = Ops::unpack(bin[q]);
-                                o[q] = Ops::pack(fmaf((x2.x - mean) * rstd, g2.x, b2.x),
-                                                 fmaf((x2.y - mean) * rstd, g2.y, b2.y));
-                            }
+                            const float2 f = Ops::unpack(xw[q]);
+                            ss = fmaf(f.x, f.x, ss);
+                            ss = fmaf(f.y, f.y, ss);
                         }
-                        st_shared_v4(addr, o[0], o[1], o[2], o[3]);
+                        // the product of two 16-bit values rounded once: same as
+                        // rounding the exact fp32 product
+                        xv[j].x = Ops::mul2(xv[j].x, gv[j].x);
+                        xv[j].y = Ops::mul2(xv[j].y, gv[j].y);
+                        xv[j].z = Ops::mul2(xv[j].z, gv[j].z);
+                        xv[j].w = Ops::mul2(xv[j].w, gv[j].w);
+                    }
+                } else {
+                    uint4 bv[8];
+                    const bool has_beta = p.beta != nullptr;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        bv[j] = has_beta ? ld_shared_v4(gsl + 128 + j * 16) : make_uint4(0u, 0u, 0u, 0u);
+                    const float nb = -mean * rstd;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        uint32_t xw[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+                        const uint32_t gw[4] = {gv[j].x, gv[j].y, gv[j].z, gv[j].w};
+                        const uint32_t bw[4] = {bv[j].x, bv[j].y, bv[j].z, bv[j].w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float2 f = Ops::unpack(xw[q]), g2 = Ops::unpack(gw[q]), b2 = Ops::unpack(bw[q]);
+                            xw[q] = Ops::pack(fmaf(fmaf(f.x, rstd, nb), g2.x, b2.x),
+                                              fmaf(fmaf(f.y, rstd, nb), g2.y, b2.y));
+                        }
+                        xv[j] = make_uint4(xw[0], xw[1], xw[2], xw[3]);
                     }
                 }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) st_shared_v4(row + ((j ^ sw) << 4), xv[j].x, xv[j].y, xv[j].z, xv[j].w);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(xform_bar(s));

@@ -115,9 +115,9 @@ EncodeTiledFn encode_fn() {
 }
 
 // Row-major [outer, inner] fp16/bf16 matrix, box {box_inner, box_outer},
-// 128-byte swizzle, zero fill out of range.
+// 128-byte swizzle (or none), zero fill out of range.
 fl_status encode_2d(CUtensorMap* m, int dt, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
-                    uint32_t box_outer) {
+                    uint32_t box_outer, bool swizzle = true) {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr) return fail(FL_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     cuuint64_t dims[2] = {inner, outer};
@@ -126,7 +126,8 @@ fl_status encode_2d(CUtensorMap* m, int dt, const void* ptr, uint64_t inner, uin
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(m, dt == FL_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
                     const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(FL_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for a [%llu, %llu] matrix, box {%u, %u}", (int)r,
                     (unsigned long long)outer, (unsigned long long)inner, box_inner, box_outer);
@@ -186,6 +187,9 @@ fl_status run_tile(int dt, int pro, bool dual, const void* A, const void* W, con
     if ((st = encode_2d(&p.tmB, dt, W, K, N, fl::kBK, bn)) != FL_OK) return st;
     if (dual && (st = encode_2d(&p.tmB2, dt, W2, K, N, fl::kBK, bn)) != FL_OK) return st;
     if ((st = encode_2d(&p.tmOut, dt, out, N, M, 64, 32)) != FL_OK) return st;
+    if (pro != fl::PRO_NONE && (st = encode_2d(&p.tmGamma, dt, gamma, K, 1, fl::kBK, 1, false)) != FL_OK) return st;
+    if (pro == fl::PRO_LN && beta != nullptr && (st = encode_2d(&p.tmBeta, dt, beta, K, 1, fl::kBK, 1, false)) != FL_OK)
+        return st;
     p.bias = bias;
     p.residual = residual;
     p.gamma = gamma;

@@ -27,6 +27,8 @@ struct GemmParams {
     CUtensorMap tmB;    // weight [N, K], box {64, BN}, 128B swizzle
     CUtensorMap tmB2;   // second weight [N, K] of the gate/up kernel (else unused)
     CUtensorMap tmOut;  // output [M, N], box {64, 32}, 128B swizzle
+    CUtensorMap tmGamma;  // gamma as a [1, K] matrix, box {64, 1} (norm prologues)
+    CUtensorMap tmBeta;   // beta as a [1, K] matrix, box {64, 1} (LayerNorm with beta)
     const void* bias;      // [N] or null
     const void* residual;  // [M, N] or null
     const void* gamma;     // [K] (norm prologues)
@@ -80,7 +82,9 @@ struct TileCfg {
     static constexpr int NUM_BARS = 3 * STAGES + 6 + 1;
     static constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_ROWSCALE = (OFF_SLOT + 16 + 15) / 16 * 16;
-    static constexpr int SMEM_BYTES = OFF_ROWSCALE + 2 * kBM * 4 + 1024;  // + alignment slack
+    // per stage: the gamma and beta slices of the K block (64 x 2 B each)
+    static constexpr int OFF_GB = (OFF_ROWSCALE + 2 * kBM * 4 + 127) / 128 * 128;
+    static constexpr int SMEM_BYTES = OFF_GB + STAGES * 256 + 1024;  // + alignment slack
 };
 
 }  // namespace fl
