@@ -1,0 +1,118 @@
+// Device helpers shared by the kernels: 16-bit packing, bounded mbarrier
+// waits, activations and vector shared-memory access.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "fl_internal.h"
+#include "fl_ptx.cuh"
+
+namespace fl {
+
+template <int DT>
+struct DTypeOps;
+
+template <>
+struct DTypeOps<DT_F16> {
+    static constexpr uint32_t kFormat = 0;
+    __device__ static __forceinline__ uint32_t pack(float a, float b) {
+        __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+    __device__ static __forceinline__ float2 unpack(uint32_t u) {
+        return __half22float2(*reinterpret_cast<__half2*>(&u));
+    }
+    __device__ static __forceinline__ uint32_t mul2(uint32_t a, uint32_t b) {
+        __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+        return *reinterpret_cast<uint32_t*>(&r);
+    }
+};
+
+template <>
+struct DTypeOps<DT_BF16> {
+    static constexpr uint32_t kFormat = 1;
+    __device__ static __forceinline__ uint32_t pack(float a, float b) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+    __device__ static __forceinline__ float2 unpack(uint32_t u) {
+        return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&u));
+    }
+    __device__ static __forceinline__ uint32_t mul2(uint32_t a, uint32_t b) {
+        __nv_bfloat162 r = __hmul2(*reinterpret_cast<__nv_bfloat162*>(&a), *reinterpret_cast<__nv_bfloat162*>(&b));
+        return *reinterpret_cast<uint32_t*>(&r);
+    }
+};
+
+// ---------------------------------------------------------------------------
+// bounded waits
+// ---------------------------------------------------------------------------
+// Waits for the phase of parity `parity` of `bar`. Gives up (returns false)
+// after timeout_ns, or early once another role has recorded a failure.
+static __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, int* status,
+                                           unsigned long long timeout_ns, int where) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63) == 0) {
+            if (*reinterpret_cast<volatile int*>(status) != 0) return false;
+            if (globaltimer_ns() - t0 > timeout_ns) {
+                atomicCAS(status, 0, kStatusTimeout | (where << 8));
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, int* status,
+                                         unsigned long long timeout_ns, int where) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_bar_slow(bar, parity, status, timeout_ns, where);
+}
+
+// Time-bounded only: used while draining after a failure.
+static __device__ __noinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity, unsigned long long ns) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > ns) return false;
+    }
+    return true;
+}
+
+__device__ __forceinline__ float act_apply(int act, float v) {
+    switch (act) {
+        case ACT_GELU: {
+            const float c = 0.7978845608028654f;  // sqrt(2 / pi)
+            return 0.5f * v * (1.0f + tanhf(c * (v + 0.044715f * v * v * v)));
+        }
+        case ACT_SILU:
+            return v / (1.0f + __expf(-v));
+        case ACT_RELU:
+            return fmaxf(v, 0.0f);
+        default:
+            return v;
+    }
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint4 ldg_v4(const void* p) {
+    return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+}  // namespace fl

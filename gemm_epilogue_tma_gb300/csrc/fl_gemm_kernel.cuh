@@ -24,118 +24,10 @@
 // drained with bounded waits, and TMEM is released before exit.
 #pragma once
 
-#include <cuda_bf16.h>
-#include <cuda_fp16.h>
-
-#include "fl_internal.h"
-#include "fl_ptx.cuh"
+#include "fl_common.cuh"
+#include "fl_fold.cuh"
 
 namespace fl {
-
-template <int DT>
-struct DTypeOps;
-
-template <>
-struct DTypeOps<DT_F16> {
-    static constexpr uint32_t kFormat = 0;
-    __device__ static __forceinline__ uint32_t pack(float a, float b) {
-        __half2 h = __floats2half2_rn(a, b);
-        return *reinterpret_cast<uint32_t*>(&h);
-    }
-    __device__ static __forceinline__ float2 unpack(uint32_t u) {
-        return __half22float2(*reinterpret_cast<__half2*>(&u));
-    }
-    __device__ static __forceinline__ uint32_t mul2(uint32_t a, uint32_t b) {
-        __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
-        return *reinterpret_cast<uint32_t*>(&r);
-    }
-};
-
-template <>
-struct DTypeOps<DT_BF16> {
-    static constexpr uint32_t kFormat = 1;
-    __device__ static __forceinline__ uint32_t pack(float a, float b) {
-        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-        return *reinterpret_cast<uint32_t*>(&h);
-    }
-    __device__ static __forceinline__ float2 unpack(uint32_t u) {
-        return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&u));
-    }
-    __device__ static __forceinline__ uint32_t mul2(uint32_t a, uint32_t b) {
-        __nv_bfloat162 r = __hmul2(*reinterpret_cast<__nv_bfloat162*>(&a), *reinterpret_cast<__nv_bfloat162*>(&b));
-        return *reinterpret_cast<uint32_t*>(&r);
-    }
-};
-
-// ---------------------------------------------------------------------------
-// bounded waits
-// ---------------------------------------------------------------------------
-// Waits for the phase of parity `parity` of `bar`. Gives up (returns false)
-// after timeout_ns, or early once another role has recorded a failure.
-static __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, int* status,
-                                           unsigned long long timeout_ns, int where) {
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63) == 0) {
-            if (*reinterpret_cast<volatile int*>(status) != 0) return false;
-            if (globaltimer_ns() - t0 > timeout_ns) {
-                atomicCAS(status, 0, kStatusTimeout | (where << 8));
-                return false;
-            }
-        }
-    }
-}
-
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, int* status,
-                                         unsigned long long timeout_ns, int where) {
-    if (mbar_try_wait(bar, parity)) return true;
-    return wait_bar_slow(bar, parity, status, timeout_ns, where);
-}
-
-// Time-bounded only: used while draining after a failure.
-static __device__ __noinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity, unsigned long long ns) {
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer_ns() - t0 > ns) return false;
-    }
-    return true;
-}
-
-__device__ __forceinline__ float act_apply(int act, float v) {
-    switch (act) {
-        case ACT_GELU: {
-            const float c = 0.7978845608028654f;  // sqrt(2 / pi)
-            return 0.5f * v * (1.0f + tanhf(c * (v + 0.044715f * v * v * v)));
-        }
-        case ACT_SILU:
-            return v / (1.0f + __expf(-v));
-        case ACT_RELU:
-            return fmaxf(v, 0.0f);
-        default:
-            return v;
-    }
-}
-
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-    uint4 v;
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(addr)
-                 : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-                 "r"(d)
-                 : "memory");
-}
-
-__device__ __forceinline__ uint4 ldg_v4(const void* p) {
-    return __ldg(reinterpret_cast<const uint4*>(p));
-}
 
 // ---------------------------------------------------------------------------
 // the kernel
@@ -204,6 +96,10 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + C::OFF_SLOT);
+    // Everything above overlaps the previous kernel on the stream; every
+    // global-memory access below waits for it.
+    griddep_wait();
+    if (threadIdx.x == 0) griddep_launch_dependents();
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -312,50 +208,31 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         }
     } else if (PRO != PRO_NONE && warp >= 4 && warp < 8) {
         // ------------------------------------------------------------ transform
-        const int t = threadIdx.x - 128;  // tile row
-        const int sw = t & 7;
+        const int t = threadIdx.x - 128;
+        const int j = t & 7;
         int s = 0;
         uint32_t ph = 0;
         int it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
-            float mean = 0.f, rstd = 1.f, ss = 0.f;
+            float mean[8], rstd[8], ss[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                mean[i] = 0.f;
+                rstd[i] = 1.f;
+                ss[i] = 0.f;
+            }
             if (PRO == PRO_LN) {
-                float n = 0.f, m2 = 0.f;
+                // statistics pass over the row block (Chan merges, no cancellation)
+                RowMoments mo[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mo[i] = RowMoments{0.f, 0.f, 0.f};
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!wait_bar(full_bar(s), ph, p.status, p.timeout_ns, 5)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t row = stage_a(s) + t * 128;
-                    const int valid = min(kBK, p.K - kb * kBK);  // multiple of 8
-                    float xs[64];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        uint4 v = ld_shared_v4(row + ((j ^ sw) << 4));
-                        float2 a = Ops::unpack(v.x), b = Ops::unpack(v.y), c = Ops::unpack(v.z),
-                               e = Ops::unpack(v.w);
-                        xs[j * 8 + 0] = a.x; xs[j * 8 + 1] = a.y; xs[j * 8 + 2] = b.x; xs[j * 8 + 3] = b.y;
-                        xs[j * 8 + 4] = c.x; xs[j * 8 + 5] = c.y; xs[j * 8 + 6] = e.x; xs[j * 8 + 7] = e.y;
-                    }
-                    // out-of-range K columns are zero-filled by TMA: they add 0 to the sum,
-                    // and are excluded from the deviation sum below by the count
-                    float sum = 0.f;
-#pragma unroll
-                    for (int e = 0; e < 64; ++e) sum += xs[e];
-                    const float cnt = (float)valid;
-                    const float cm = sum / cnt;
-                    float cm2 = 0.f;
-#pragma unroll
-                    for (int e = 0; e < 64; ++e) {
-                        const float dlt = xs[e] - cm;
-                        cm2 += (e < valid) ? dlt * dlt : 0.f;
-                    }
-                    const float nn = n + cnt;
-                    const float delta = cm - mean;
-                    mean += delta * (cnt / nn);
-                    m2 += cm2 + delta * delta * (n * cnt / nn);
-                    n = nn;
+                    ln_stats_stage<DT>(stage_a(s), t, 8, kb * kBK + j * 8 < p.K, mo);
                     __syncwarp();
                     if (lane == 0) mbar_arrive(xform_bar(s));
                     if (++s == S) {
@@ -364,7 +241,12 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                     }
                 }
                 if (!ok) break;
-                rstd = rsqrtf(m2 / (float)p.K + p.eps);
+                ln_stats_allreduce(mo, 8);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    mean[i] = mo[i].mean;
+                    rstd[i] = rsqrtf(mo[i].m2 / (float)p.K + p.eps);
+                }
             }
             for (int kb = 0; kb < nk; ++kb) {
                 if (!wait_bar(full_bar(s), ph, p.status, p.timeout_ns, 6)) {
@@ -373,53 +255,10 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                 }
                 // gamma (and beta) of this K block arrived with the stage; columns
                 // past K are zero in x, gamma and beta, so they stay zero
-                const uint32_t row = stage_a(s) + t * 128;
-                const uint32_t gsl = gb_slot(s);
-                uint4 xv[8], gv[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) xv[j] = ld_shared_v4(row + ((j ^ sw) << 4));
-#pragma unroll
-                for (int j = 0; j < 8; ++j) gv[j] = ld_shared_v4(gsl + j * 16);
-                if (PRO == PRO_RMS) {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const uint32_t xw[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const float2 f = Ops::unpack(xw[q]);
-                            ss = fmaf(f.x, f.x, ss);
-                            ss = fmaf(f.y, f.y, ss);
-                        }
-                        // the product of two 16-bit values rounded once: same as
-                        // rounding the exact fp32 product
-                        xv[j].x = Ops::mul2(xv[j].x, gv[j].x);
-                        xv[j].y = Ops::mul2(xv[j].y, gv[j].y);
-                        xv[j].z = Ops::mul2(xv[j].z, gv[j].z);
-                        xv[j].w = Ops::mul2(xv[j].w, gv[j].w);
-                    }
-                } else {
-                    uint4 bv[8];
-                    const bool has_beta = p.beta != nullptr;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        bv[j] = has_beta ? ld_shared_v4(gsl + 128 + j * 16) : make_uint4(0u, 0u, 0u, 0u);
-                    const float nb = -mean * rstd;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        uint32_t xw[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
-                        const uint32_t gw[4] = {gv[j].x, gv[j].y, gv[j].z, gv[j].w};
-                        const uint32_t bw[4] = {bv[j].x, bv[j].y, bv[j].z, bv[j].w};
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const float2 f = Ops::unpack(xw[q]), g2 = Ops::unpack(gw[q]), b2 = Ops::unpack(bw[q]);
-                            xw[q] = Ops::pack(fmaf(fmaf(f.x, rstd, nb), g2.x, b2.x),
-                                              fmaf(fmaf(f.y, rstd, nb), g2.y, b2.y));
-                        }
-                        xv[j] = make_uint4(xw[0], xw[1], xw[2], xw[3]);
-                    }
-                }
-#pragma unroll
-                for (int j = 0; j < 8; ++j) st_shared_v4(row + ((j ^ sw) << 4), xv[j].x, xv[j].y, xv[j].z, xv[j].w);
+                if (PRO == PRO_RMS)
+                    fold_rms_stage<DT>(stage_a(s), gb_slot(s), t, 8, ss);
+                else
+                    fold_ln_stage<DT>(stage_a(s), gb_slot(s), p.beta != nullptr, t, 8, mean, rstd);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(xform_bar(s));
@@ -434,8 +273,14 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                 // released that accumulator buffer for this tile
                 const int buf = it & 1;
                 const uint32_t tph = (it >> 1) & 1;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) ss[i] = row_allreduce8(ss[i]);
                 if (!wait_bar(tempty_bar(buf), tph ^ 1u, p.status, p.timeout_ns, 7)) break;
-                rowscale[buf * kBM + t] = rsqrtf(ss / (float)p.K + p.eps);
+                if (j == 0) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        rowscale[buf * kBM + (t >> 3) + 16 * i] = rsqrtf(ss[i] / (float)p.K + p.eps);
+                }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(sready_bar(buf));
             }
@@ -570,9 +415,17 @@ cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    const int threads = PRO != PRO_NONE ? 384 : 256;
-    kern<<<grid, threads, C::SMEM_BYTES, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(PRO != PRO_NONE ? 384 : 256, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = p.pdl;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 }  // namespace fl

@@ -18,7 +18,6 @@
 #include "fl_internal.h"
 
 using fl::GemmParams;
-using fl::SplitKParams;
 
 // Device status word: kernels record a bounded-wait expiry here.
 __device__ int g_fl_status;
@@ -44,6 +43,7 @@ std::atomic<int> g_opt_tile_n{0};
 std::atomic<int> g_opt_variant{0};
 std::atomic<int> g_opt_timeout_ms{2000};
 std::atomic<int> g_opt_split_k{0};
+std::atomic<int> g_opt_pdl{1};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -158,6 +158,71 @@ cudaError_t dispatch_tile(int dt, int bn, int pro, bool dual, const GemmParams& 
     return cudaErrorInvalidValue;
 }
 
+cudaError_t dispatch_splitk(int dt, int bn, int pro, const GemmParams& p, int grid, int splits, cudaStream_t s) {
+#define FL_CASE(DT, BN, PRO) \
+    if (dt == DT && bn == BN && pro == PRO) return fl::launch_splitk<DT, BN, PRO>(p, grid, splits, s);
+    FL_CASE(0, 64, 0)
+    FL_CASE(0, 64, 1)
+    FL_CASE(0, 64, 2)
+    FL_CASE(0, 128, 0)
+    FL_CASE(0, 128, 1)
+    FL_CASE(0, 128, 2)
+    FL_CASE(1, 64, 0)
+    FL_CASE(1, 64, 1)
+    FL_CASE(1, 64, 2)
+    FL_CASE(1, 128, 0)
+    FL_CASE(1, 128, 1)
+    FL_CASE(1, 128, 2)
+#undef FL_CASE
+    return cudaErrorInvalidValue;
+}
+
+// Split-K plan for shapes with too few output tiles to fill the GPU: 64-wide
+// weight tiles, and as many K splits (one cluster, at most 8) as keep every
+// SM streaming weights. Returns false when the tile kernel is the better fit.
+struct SplitPlan {
+    int bn, splits, kps;
+};
+
+bool plan_splitk(int M, int N, int K, int sms, SplitPlan* plan) {
+    const int variant = g_opt_variant.load();
+    if (variant == 1) return false;
+    const int nk = (K + fl::kBK - 1) / fl::kBK;
+    const int mb = (M + fl::kBM - 1) / fl::kBM;
+    // 128-wide weight tiles stage more bytes per pipeline slot (more bytes in
+    // flight per SM); 64-wide ones give twice the CTAs. Prefer 128 unless it
+    // leaves a quarter of the CTAs unused.
+    auto ctas_for = [&](int b) {
+        const int tl = mb * ((N + b - 1) / b);
+        int sp = sms / (tl > 0 ? tl : 1);
+        if (sp > 8) sp = 8;
+        while (sp > 1 && nk / sp < 2) --sp;
+        return tl * (sp < 1 ? 1 : sp);
+    };
+    const int forced_bn = g_opt_tile_n.load();
+    const int bn = forced_bn == 128 ? 128 : forced_bn == 256 ? 64 : (ctas_for(128) * 4 >= ctas_for(64) * 3 ? 128 : 64);
+    const int tiles = mb * ((N + bn - 1) / bn);
+    if (variant == 0) {
+        // few rows only: with more than one row block the tile kernel reuses the
+        // weight tile across rows and is the better fit
+        if (mb > 1 || (long long)((N + 127) / 128) * 2 > sms) return false;
+    }
+    int splits = g_opt_split_k.load();
+    if (splits <= 0) {
+        splits = sms / (tiles > 0 ? tiles : 1);
+        if (splits > 8) splits = 8;
+        if (splits < 1) splits = 1;
+        while (splits > 1 && nk / splits < 2) --splits;  // at least two K blocks per split
+    }
+    if (splits > nk) splits = nk;
+    if (splits < 1) splits = 1;
+    const int kps = (nk + splits - 1) / splits;
+    plan->bn = bn;
+    plan->kps = kps;
+    plan->splits = (nk + kps - 1) / kps;  // every split gets at least one K block
+    return true;
+}
+
 // CTA tile width. A wider tile halves the activation re-reads and the shared
 // memory traffic per MMA, but fewer tiles may leave SMs idle: take the width
 // whose whole waves of CTAs cost least.
@@ -174,12 +239,54 @@ int choose_bn(int M, int N, bool dual, int sms) {
     return c256 <= c128 ? 256 : 128;
 }
 
+fl_status run_splitk(int dt, int pro, const void* A, const void* W, const void* bias, const void* residual,
+                     const void* gamma, const void* beta, void* out, int M, int N, int K, int act, float eps,
+                     const SplitPlan& plan, DeviceInfo* di, cudaStream_t stream) {
+    GemmParams p;
+    memset(&p, 0, sizeof(p));
+    const int a_rows = M >= fl::kBM ? fl::kBM : (M + 15) / 16 * 16;
+    fl_status st;
+    if ((st = encode_2d(&p.tmA, dt, A, K, M, fl::kBK, a_rows)) != FL_OK) return st;
+    if ((st = encode_2d(&p.tmB, dt, W, K, N, fl::kBK, plan.bn)) != FL_OK) return st;
+    if (pro != fl::PRO_NONE && (st = encode_2d(&p.tmGamma, dt, gamma, K, 1, fl::kBK, 1, false)) != FL_OK) return st;
+    if (pro == fl::PRO_LN && beta != nullptr && (st = encode_2d(&p.tmBeta, dt, beta, K, 1, fl::kBK, 1, false)) != FL_OK)
+        return st;
+    p.bias = bias;
+    p.residual = residual;
+    p.gamma = gamma;
+    p.beta = beta;
+    p.a_ptr = A;
+    p.out_ptr = out;
+    p.status = di->status;
+    p.timeout_ns = (unsigned long long)g_opt_timeout_ms.load() * 1000000ull;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.num_m_blocks = (M + fl::kBM - 1) / fl::kBM;
+    p.num_n_blocks = (N + plan.bn - 1) / plan.bn;
+    p.num_k_blocks = (K + fl::kBK - 1) / fl::kBK;
+    p.num_tiles = p.num_m_blocks * p.num_n_blocks;
+    p.act = act;
+    p.eps = eps;
+    p.splits = plan.splits;
+    p.kps = plan.kps;
+    p.a_rows = a_rows;
+    p.pdl = g_opt_pdl.load();
+    const int grid = p.num_tiles * plan.splits;
+    cudaError_t e = dispatch_splitk(dt, plan.bn, pro, p, grid, plan.splits, stream);
+    if (e != cudaSuccess) return fail(FL_ERR_CUDA, "split-K kernel launch failed: %s", cudaGetErrorString(e));
+    return ok();
+}
+
 fl_status run_tile(int dt, int pro, bool dual, const void* A, const void* W, const void* W2, const void* bias,
                    const void* residual, const void* gamma, const void* beta, void* out, int M, int N, int K, int act,
                    float eps, cudaStream_t stream) {
     DeviceInfo* di = nullptr;
     fl_status st = device_info(&di);
     if (st != FL_OK) return st;
+    SplitPlan plan;
+    if (!dual && plan_splitk(M, N, K, di->sms, &plan))
+        return run_splitk(dt, pro, A, W, bias, residual, gamma, beta, out, M, N, K, act, eps, plan, di, stream);
     const int bn = choose_bn(M, N, dual, di->sms);
     GemmParams p;
     memset(&p, 0, sizeof(p));
@@ -205,6 +312,7 @@ fl_status run_tile(int dt, int pro, bool dual, const void* A, const void* W, con
     p.num_tiles = p.num_m_blocks * p.num_n_blocks;
     p.act = act;
     p.eps = eps;
+    p.pdl = g_opt_pdl.load();
     const int grid = p.num_tiles < di->sms ? p.num_tiles : di->sms;
     cudaError_t e = dispatch_tile(dt, bn, pro, dual, p, grid, stream);
     if (e != cudaSuccess) return fail(FL_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
@@ -258,8 +366,12 @@ fl_status fl_set_option(fl_option key, int value) {
             g_opt_timeout_ms = value;
             return ok();
         case FL_OPT_SPLIT_K:
-            if (value < 0 || value > 16) return fail(FL_ERR_INVALID_ARG, "split must be 0..16");
+            if (value < 0 || value > 8) return fail(FL_ERR_INVALID_ARG, "split must be 0..8");
             g_opt_split_k = value;
+            return ok();
+        case FL_OPT_PDL:
+            if (value < 0 || value > 1) return fail(FL_ERR_INVALID_ARG, "pdl must be 0 or 1");
+            g_opt_pdl = value;
             return ok();
         default:
             return fail(FL_ERR_INVALID_ARG, "unknown option %d", (int)key);

@@ -1,0 +1,11 @@
+// Split-K kernel instances (bf16): few output tiles, weights streamed once.
+#include "fl_splitk_kernel.cuh"
+
+namespace fl {
+template cudaError_t launch_splitk<DT_BF16, 64, PRO_NONE>(const GemmParams&, int, int, cudaStream_t);
+template cudaError_t launch_splitk<DT_BF16, 64, PRO_RMS>(const GemmParams&, int, int, cudaStream_t);
+template cudaError_t launch_splitk<DT_BF16, 64, PRO_LN>(const GemmParams&, int, int, cudaStream_t);
+template cudaError_t launch_splitk<DT_BF16, 128, PRO_NONE>(const GemmParams&, int, int, cudaStream_t);
+template cudaError_t launch_splitk<DT_BF16, 128, PRO_RMS>(const GemmParams&, int, int, cudaStream_t);
+template cudaError_t launch_splitk<DT_BF16, 128, PRO_LN>(const GemmParams&, int, int, cudaStream_t);
+}  // namespace fl

@@ -1,0 +1,11 @@
+// Split-K kernel instances (f16): few output tiles, weights streamed once.
+#include "fl_splitk_kernel.cuh"
+
+namespace fl {
+template cudaError_t launch_splitk<DT_F16, 64, PRO_NONE>(const GemmParams&, int, int, cudaStream_t);
+template cudaError_t launch_splitk<DT_F16, 64, PRO_RMS>(const GemmParams&, int, int, cudaStream_t);
+template cudaError_t launch_splitk<DT_F16, 64, PRO_LN>(const GemmParams&, int, int, cudaStream_t);
+template cudaError_t launch_splitk<DT_F16, 128, PRO_NONE>(const GemmParams&, int, int, cudaStream_t);
+template cudaError_t launch_splitk<DT_F16, 128, PRO_RMS>(const GemmParams&, int, int, cudaStream_t);
+template cudaError_t launch_splitk<DT_F16, 128, PRO_LN>(const GemmParams&, int, int, cudaStream_t);
+}  // namespace fl

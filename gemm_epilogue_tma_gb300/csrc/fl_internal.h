@@ -33,37 +33,47 @@ struct GemmParams {
     const void* residual;  // [M, N] or null
     const void* gamma;     // [K] (norm prologues)
     const void* beta;      // [K] or null (LayerNorm)
+    const void* a_ptr;     // activation [M, K] (LayerNorm statistics of the split-K kernel)
+    void* out_ptr;         // output [M, N] (split-K kernel stores directly)
     int* status;           // device status word
     unsigned long long timeout_ns;
     int M, N, K;
     int num_m_blocks, num_n_blocks, num_k_blocks, num_tiles;
     int act;
     float eps;
-};
-
-// Parameters of the small-M split-K kernel.
-struct SplitKParams {
-    CUtensorMap tmW;    // weight [N, K], box {64, 128}, 128B swizzle
-    CUtensorMap tmX;    // activation [M, K], box {64, MP}, 128B swizzle
-    const void* gamma;  // [K]
-    const void* beta;   // [K] or null
-    const void* bias;   // [N] or null
-    const void* residual;  // [M, N] or null
-    void* out;          // [M, N]
-    int* status;
-    unsigned long long timeout_ns;
-    int M, N, K;
-    int k_blocks_per_split;  // 64-wide K blocks per cluster rank
-    int act;
-    float eps;
+    int splits;    // split-K kernel: CTAs per cluster, one K range each
+    int kps;       // split-K kernel: 64-wide K blocks per split
+    int a_rows;    // split-K kernel: rows of the activation box (128, or M rounded up to 16)
+    int pdl;       // launch with a programmatic dependency on the previous kernel of the stream
 };
 
 // Kernel launchers, explicitly instantiated in the kernel translation units.
 template <int DT, int BN, int PRO, bool DUAL>
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream);
 
-template <int DT, int MP, int PRO>
-cudaError_t launch_splitk(const SplitKParams& p, int n_tiles, int splits, cudaStream_t stream);
+template <int DT, int BN, int PRO>
+cudaError_t launch_splitk(const GemmParams& p, int grid, int splits, cudaStream_t stream);
+
+// Shared-memory layout of the split-K kernel.
+template <int BN>
+struct SplitCfg {
+    static constexpr int A_BYTES = kBM * kBK * 2;
+    static constexpr int B_BYTES = BN * kBK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES_RAW = (192 * 1024) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+    static constexpr int RED_STRIDE = BN + 4;  // fp32 partial row, padded against bank conflicts
+    static constexpr int RED_BYTES = kBM * RED_STRIDE * 4;
+    static constexpr int RING_BYTES = STAGES * STAGE_BYTES > RED_BYTES ? STAGES * STAGE_BYTES : RED_BYTES;
+    static constexpr int TMEM_COLS = BN < 32 ? 32 : BN;
+    static constexpr int OFF_BAR = RING_BYTES;
+    static constexpr int NUM_BARS = 3 * STAGES + 2;
+    static constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
+    static constexpr int OFF_SS = (OFF_SLOT + 16 + 15) / 16 * 16;   // [128] partial sum of squares
+    static constexpr int OFF_LN = OFF_SS + kBM * 4;                 // [128] float2 mean, rstd
+    static constexpr int OFF_GB = (OFF_LN + kBM * 8 + 127) / 128 * 128;
+    static constexpr int SMEM_BYTES = OFF_GB + STAGES * 256 + 1024;
+};
 
 // Shared-memory bytes of each tile configuration (host-visible).
 template <int BN, bool DUAL>

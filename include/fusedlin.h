@@ -151,10 +151,20 @@ fl_status fl_device_status(void* stream);
  *   FL_OPT_TILE_N:      0 = automatic, else the CTA tile width (128 or 256).
  *   FL_OPT_VARIANT:     0 = automatic, 1 = tile kernel, 2 = small-M split-K kernel.
  *   FL_OPT_TIMEOUT_MS:  limit of every device-side wait (default 2000).
- *   FL_OPT_SPLIT_K:     0 = automatic, else the K split of the small-M kernel.
+ *   FL_OPT_SPLIT_K:     0 = automatic, else the K split of the small-M kernel (1..8).
+ *   FL_OPT_PDL:         1 (default) = launch each kernel with a programmatic
+ *                       dependency on the previous kernel of the stream, so its
+ *                       set-up overlaps that kernel's tail (all of its memory
+ *                       accesses still wait for it); 0 = plain stream order.
  * Returns FL_ERR_INVALID_ARG for an unknown key or a value out of range.
  */
-typedef enum { FL_OPT_TILE_N = 0, FL_OPT_VARIANT = 1, FL_OPT_TIMEOUT_MS = 2, FL_OPT_SPLIT_K = 3 } fl_option;
+typedef enum {
+    FL_OPT_TILE_N = 0,
+    FL_OPT_VARIANT = 1,
+    FL_OPT_TIMEOUT_MS = 2,
+    FL_OPT_SPLIT_K = 3,
+    FL_OPT_PDL = 4
+} fl_option;
 fl_status fl_set_option(fl_option key, int value);
 
 /*

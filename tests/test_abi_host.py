@@ -131,7 +131,8 @@ def test_options(L):
     assert L.fl_set_option(0, 256) == OK and L.fl_set_option(0, 0) == OK
     assert L.fl_set_option(1, 3) == INVALID and L.fl_set_option(1, 0) == OK
     assert L.fl_set_option(2, 0) == INVALID and L.fl_set_option(2, 2000) == OK
-    assert L.fl_set_option(3, 17) == INVALID and L.fl_set_option(3, 0) == OK
+    assert L.fl_set_option(3, 9) == INVALID and L.fl_set_option(3, 0) == OK
+    assert L.fl_set_option(4, 2) == INVALID and L.fl_set_option(4, 0) == OK and L.fl_set_option(4, 1) == OK
     assert L.fl_set_option(42, 0) == INVALID
     assert L.fl_debug_wait_timeout(0, None) == INVALID
 

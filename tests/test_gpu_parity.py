@@ -152,6 +152,49 @@ def test_repeatable_bitwise():
 
 
 # ---------------------------------------------------------------------------
+# the split-K variant (cluster of K ranges, reduction through distributed
+# shared memory), forced on shapes it would not pick by itself too
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("splits", [1, 2, 3, 8])
+@pytest.mark.parametrize("shape", [(1, 64, 512), (17, 200, 1000), (128, 136, 4096), (300, 264, 520)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_splitk_variant_all_patterns(dt, splits, shape):
+    M, N, K = shape
+    t = syn.dense_layer_inputs(M, N, K, dt)
+    fl.set_option("variant", 2)
+    fl.set_option("split_k", splits)
+    try:
+        for pattern in syn.PATTERNS:
+            got, ref = run_pattern(t, pattern)
+            assert_close(got, ref, dt, f"split-K x{splits} {pattern} {dt} {M}x{N}x{K}")
+        fl.device_status()
+    finally:
+        fl.set_option("variant", 0)
+        fl.set_option("split_k", 0)
+
+
+@pytest.mark.parametrize("dt", DTYPES)
+def test_splitk_wide_tiles_and_norm_bias_act(dt):
+    M, N, K = 96, 392, 1536
+    t = syn.norm_gemm_inputs(M, N, K, "layer", dt, with_bias=True)
+    fl.set_option("variant", 2)
+    fl.set_option("tile_n", 128)
+    try:
+        for norm in ("rms", "layer"):
+            for act in ("gelu", "relu"):
+                got = fl.norm_gemm(dev(t["x"]), dev(t["gamma"]), dev(t["W"]), beta=dev(t["beta"]),
+                                   bias=dev(t["bias"]), eps=1e-5, norm=norm, act=act)
+                torch.cuda.synchronize()
+                ref = oracle.norm_gemm(f64(t["x"]), f64(t["gamma"]), f64(t["beta"]), f64(t["W"]), f64(t["bias"]),
+                                       1e-5, norm, act)
+                assert_close(got, ref, dt, f"split-K BN=128 {norm} {act}")
+    finally:
+        fl.set_option("variant", 0)
+        fl.set_option("tile_n", 0)
+
+
+# ---------------------------------------------------------------------------
 # the workloads of the pages, at full size
 # ---------------------------------------------------------------------------
 def test_gemm_bias_gelu_512x1024x1024_all_elements():
