@@ -155,6 +155,95 @@ __device__ __forceinline__ void fold_ln_stage(uint32_t stage, uint32_t gb_slice,
     }
 }
 
+// ---------------------------------------------------------------------------
+// Thread-per-row forms, for folding into tensor memory: thread t of the
+// transform warpgroup owns row t (TMEM lane t), reads its 8 chunks (one per
+// quarter-warp bank group, no conflicts) and returns the folded row as 32
+// packed 32-bit columns in K order, ready for tcgen05.st.
+// ---------------------------------------------------------------------------
+template <int DT>
+__device__ __forceinline__ void fold_rms_row(uint32_t stage, uint32_t gamma_slice, int t, float (&ss)[8],
+                                             uint32_t (&o)[32]) {
+    using Ops = DTypeOps<DT>;
+    const int sw = t & 7;
+    uint4 xv[8], gv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) xv[j] = ld_shared_v4(stage + t * 128 + ((j ^ sw) << 4));
+#pragma unroll
+    for (int j = 0; j < 8; ++j) gv[j] = ld_shared_v4(gamma_slice + j * 16);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float2 a = Ops::unpack(xv[j].x), b = Ops::unpack(xv[j].y), c = Ops::unpack(xv[j].z),
+                     d = Ops::unpack(xv[j].w);
+        float s0 = a.x * a.x, s1 = a.y * a.y;
+        s0 = fmaf(b.x, b.x, s0);
+        s1 = fmaf(b.y, b.y, s1);
+        s0 = fmaf(c.x, c.x, s0);
+        s1 = fmaf(c.y, c.y, s1);
+        s0 = fmaf(d.x, d.x, s0);
+        s1 = fmaf(d.y, d.y, s1);
+        ss[j] += s0 + s1;
+        o[4 * j + 0] = Ops::mul2(xv[j].x, gv[j].x);
+        o[4 * j + 1] = Ops::mul2(xv[j].y, gv[j].y);
+        o[4 * j + 2] = Ops::mul2(xv[j].z, gv[j].z);
+        o[4 * j + 3] = Ops::mul2(xv[j].w, gv[j].w);
+    }
+}
+
+// LayerNorm moments of one row's K block (nvalid chunks of 8 lie inside K).
+template <int DT>
+__device__ __forceinline__ void ln_stats_row(uint32_t stage, int t, int nvalid, RowMoments& mo) {
+    using Ops = DTypeOps<DT>;
+    if (nvalid <= 0) return;
+    const int sw = t & 7;
+    float v[64];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint4 x = ld_shared_v4(stage + t * 128 + ((j ^ sw) << 4));
+        const float2 a = Ops::unpack(x.x), b = Ops::unpack(x.y), c = Ops::unpack(x.z), d = Ops::unpack(x.w);
+        v[8 * j + 0] = a.x; v[8 * j + 1] = a.y; v[8 * j + 2] = b.x; v[8 * j + 3] = b.y;
+        v[8 * j + 4] = c.x; v[8 * j + 5] = c.y; v[8 * j + 6] = d.x; v[8 * j + 7] = d.y;
+    }
+    // out-of-range chunks are zero-filled: they add nothing to the sum
+    float part[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        part[j] = ((v[8 * j] + v[8 * j + 1]) + (v[8 * j + 2] + v[8 * j + 3])) +
+                  ((v[8 * j + 4] + v[8 * j + 5]) + (v[8 * j + 6] + v[8 * j + 7]));
+    const float cnt = 8.f * (float)nvalid;
+    const float cm = (((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]))) / cnt;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        float q = 0.f;
+        if (j < nvalid) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) q = fmaf(v[8 * j + e] - cm, v[8 * j + e] - cm, q);
+        }
+        part[j] = q;
+    }
+    const float m2 = ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
+    mo = merge_moments(mo, RowMoments{cnt, cm, m2});
+}
+
+template <int DT>
+__device__ __forceinline__ void fold_ln_row(uint32_t stage, uint32_t gb_slice, bool has_beta, int t, float mean,
+                                            float rstd, uint32_t (&o)[32]) {
+    using Ops = DTypeOps<DT>;
+    const int sw = t & 7;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint4 x = ld_shared_v4(stage + t * 128 + ((j ^ sw) << 4));
+        const uint4 g = ld_shared_v4(gb_slice + j * 16);
+        const uint4 b = has_beta ? ld_shared_v4(gb_slice + 128 + j * 16) : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, gw[4] = {g.x, g.y, g.z, g.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float2 f = Ops::unpack(xw[q]), g2 = Ops::unpack(gw[q]), b2 = Ops::unpack(bw[q]);
+            o[4 * j + q] = Ops::pack(fmaf((f.x - mean) * rstd, g2.x, b2.x), fmaf((f.y - mean) * rstd, g2.y, b2.y));
+        }
+    }
+}
+
 // Sum of the 8 lanes that share a row (RMS).
 __device__ __forceinline__ float row_allreduce8(float v) {
     v += __shfl_xor_sync(0xffffffffu, v, 1);

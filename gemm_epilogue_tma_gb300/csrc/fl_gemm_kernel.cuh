@@ -41,6 +41,14 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     constexpr int EPI_WARP0 = PRO != PRO_NONE ? 8 : 4;
     constexpr uint32_t IDESC = umma_idesc_f16(Ops::kFormat, kBM, BN);
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "tile width");
+    // Norm prologue with one weight and a 128-wide tile: the folded activation
+    // goes to tensor memory (one 32-column slot per stage after the two
+    // accumulators) and the MMA reads it from there, which takes the fold's
+    // shared-memory writes and the MMA's activation reads off shared memory.
+    constexpr bool ATMEM = PRO != PRO_NONE && BN == 128 && !DUAL;
+    constexpr uint32_t TMEM_ALLOC = ATMEM ? 512u : (uint32_t)C::TMEM_COLS;
+    constexpr uint32_t A_COL0 = 2u * C::ACC_COLS;
+    static_assert(!ATMEM || A_COL0 + 32u * S <= 512u, "activation slots must fit in tensor memory");
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -89,7 +97,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         if (PRO == PRO_LN && p.beta != nullptr) tma_prefetch_desc(&p.tmBeta);
     }
     if (warp == 1) {
-        tmem_alloc(slot_addr, C::TMEM_COLS);
+        tmem_alloc(slot_addr, TMEM_ALLOC);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -186,6 +194,11 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                     const uint64_t db = sw128_kmajor_desc(stage_b(s));
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
+                        if (ATMEM) {
+                            // 16 K elements = 8 columns of the stage's activation slot
+                            umma_f16_ts(d, tmem_base + A_COL0 + 32u * s + 8u * kk, db + 2 * kk, IDESC, (kb | kk) != 0);
+                            continue;
+                        }
                         // +32 bytes per 16-element K step inside the swizzled row
                         umma_f16_ss(d, da + 2 * kk, db + 2 * kk, IDESC, (kb | kk) != 0);
                         if (DUAL) {
@@ -205,6 +218,69 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
             // Drain: all MMAs issued by this thread complete before TMEM is released.
             umma_commit(drain_bar);
             wait_bar_drain(drain_bar, 0, 20000000ull);
+        }
+    } else if (ATMEM && warp >= 4 && warp < 8) {
+        // ------------------------------------------------------------ transform into TMEM
+        const int t = threadIdx.x - 128;  // tile row = TMEM lane
+        const uint32_t a_lane = (uint32_t)(32 * (warp & 3)) << 16;
+        int s = 0;
+        uint32_t ph = 0;
+        int it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
+            float mean = 0.f, rstd = 1.f;
+            float ss[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ss[i] = 0.f;
+            if (PRO == PRO_LN) {
+                RowMoments mo{0.f, 0.f, 0.f};
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!wait_bar(full_bar(s), ph, p.status, p.timeout_ns, 5)) {
+                        ok = false;
+                        break;
+                    }
+                    ln_stats_row<DT>(stage_a(s), t, min(8, (p.K - kb * kBK) / 8), mo);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(xform_bar(s));
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mean = mo.mean;
+                rstd = rsqrtf(mo.m2 / (float)p.K + p.eps);
+            }
+            for (int kb = 0; kb < nk; ++kb) {
+                if (!wait_bar(full_bar(s), ph, p.status, p.timeout_ns, 6)) {
+                    ok = false;
+                    break;
+                }
+                uint32_t o[32];
+                if (PRO == PRO_RMS)
+                    fold_rms_row<DT>(stage_a(s), gb_slot(s), t, ss, o);
+                else
+                    fold_ln_row<DT>(stage_a(s), gb_slot(s), p.beta != nullptr, t, mean, rstd, o);
+                tmem_st_32x32b_x32(tmem_base + a_lane + A_COL0 + 32u * s, o);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(xform_bar(s));
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (!ok) break;
+            if (PRO == PRO_RMS) {
+                const int buf = it & 1;
+                const uint32_t tph = (it >> 1) & 1;
+                if (!wait_bar(tempty_bar(buf), tph ^ 1u, p.status, p.timeout_ns, 7)) break;
+                const float sum = ((ss[0] + ss[1]) + (ss[2] + ss[3])) + ((ss[4] + ss[5]) + (ss[6] + ss[7]));
+                rowscale[buf * kBM + t] = rsqrtf(sum / (float)p.K + p.eps);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sready_bar(buf));
+            }
         }
     } else if (PRO != PRO_NONE && warp >= 4 && warp < 8) {
         // ------------------------------------------------------------ transform
@@ -401,7 +477,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, C::TMEM_COLS);
+        tmem_dealloc(tmem_base, TMEM_ALLOC);
     }
 }
 

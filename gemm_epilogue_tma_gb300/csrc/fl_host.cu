@@ -184,7 +184,23 @@ struct SplitPlan {
     int bn, splits, kps;
 };
 
-bool plan_splitk(int M, int N, int K, int sms, SplitPlan* plan) {
+int max_clusters(int dt, int bn, int pro, int splits) {
+    // cached per (dtype, width, prologue, cluster size); single device assumed per process slot
+    static std::atomic<int> cache[2][2][3][9];
+    const int bi = bn == 128 ? 1 : 0;
+    int v = cache[dt][bi][pro][splits].load();
+    if (v != 0) return v;
+#define FL_Q(DT, BN, PRO) \
+    if (dt == DT && bn == BN && pro == PRO) v = fl::splitk_max_clusters<DT, BN, PRO>(splits);
+    FL_Q(0, 64, 0) FL_Q(0, 64, 1) FL_Q(0, 64, 2) FL_Q(0, 128, 0) FL_Q(0, 128, 1) FL_Q(0, 128, 2)
+    FL_Q(1, 64, 0) FL_Q(1, 64, 1) FL_Q(1, 64, 2) FL_Q(1, 128, 0) FL_Q(1, 128, 1) FL_Q(1, 128, 2)
+#undef FL_Q
+    if (v <= 0) v = -1;
+    cache[dt][bi][pro][splits] = v;
+    return v;
+}
+
+bool plan_splitk(int dt, int pro, int M, int N, int K, int sms, SplitPlan* plan) {
     const int variant = g_opt_variant.load();
     if (variant == 1) return false;
     const int nk = (K + fl::kBK - 1) / fl::kBK;
@@ -203,9 +219,9 @@ bool plan_splitk(int M, int N, int K, int sms, SplitPlan* plan) {
     const int bn = forced_bn == 128 ? 128 : forced_bn == 256 ? 64 : (ctas_for(128) * 4 >= ctas_for(64) * 3 ? 128 : 64);
     const int tiles = mb * ((N + bn - 1) / bn);
     if (variant == 0) {
-        // few rows only: with more than one row block the tile kernel reuses the
-        // weight tile across rows and is the better fit
-        if (mb > 1 || (long long)((N + 127) / 128) * 2 > sms) return false;
+        // the tile kernel fills at least half the SMs: it reuses each staged
+        // tile across the whole K loop and needs no reduction
+        if ((long long)mb * ((N + 127) / 128) * 2 > sms || nk < 4) return false;
     }
     int splits = g_opt_split_k.load();
     if (splits <= 0) {
@@ -216,6 +232,13 @@ bool plan_splitk(int M, int N, int K, int sms, SplitPlan* plan) {
     }
     if (splits > nk) splits = nk;
     if (splits < 1) splits = 1;
+    // every cluster of the grid resident at once (one wave): the cluster shape
+    // limits how many fit on the GPCs
+    while (splits > 1) {
+        const int mc = max_clusters(dt, bn, pro, splits);
+        if (mc < 0 || tiles <= mc) break;
+        --splits;
+    }
     const int kps = (nk + splits - 1) / splits;
     plan->bn = bn;
     plan->kps = kps;
@@ -285,7 +308,7 @@ fl_status run_tile(int dt, int pro, bool dual, const void* A, const void* W, con
     fl_status st = device_info(&di);
     if (st != FL_OK) return st;
     SplitPlan plan;
-    if (!dual && plan_splitk(M, N, K, di->sms, &plan))
+    if (!dual && plan_splitk(dt, pro, M, N, K, di->sms, &plan))
         return run_splitk(dt, pro, A, W, bias, residual, gamma, beta, out, M, N, K, act, eps, plan, di, stream);
     const int bn = choose_bn(M, N, dual, di->sms);
     GemmParams p;

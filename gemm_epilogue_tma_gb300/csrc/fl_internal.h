@@ -54,6 +54,9 @@ cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream);
 template <int DT, int BN, int PRO>
 cudaError_t launch_splitk(const GemmParams& p, int grid, int splits, cudaStream_t stream);
 
+template <int DT, int BN, int PRO>
+int splitk_max_clusters(int splits);
+
 // Shared-memory layout of the split-K kernel.
 template <int BN>
 struct SplitCfg {

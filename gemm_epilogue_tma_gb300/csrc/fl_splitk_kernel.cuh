@@ -362,6 +362,32 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     }
 }
 
+// How many clusters of `splits` CTAs of this kernel can be resident at once.
+template <int DT, int BN, int PRO>
+int splitk_max_clusters(int splits) {
+    using C = SplitCfg<BN>;
+    auto kern = fl_splitk_kernel<DT, BN, PRO>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(splits, 1, 1);
+    cfg.blockDim = dim3(PRO != PRO_NONE ? 384 : 256, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = splits;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
 template <int DT, int BN, int PRO>
 cudaError_t launch_splitk(const GemmParams& p, int grid, int splits, cudaStream_t stream) {
     using C = SplitCfg<BN>;
