@@ -35,6 +35,7 @@ SIGNATURES = {
     "fl_norm_gemm": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _f, _i, _i, _i, _vp]),
     "fl_swiglu_ffn_workspace_size": (_sz, [_i, _i, _i]),
     "fl_swiglu_ffn": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _f, _vp, _sz, _i, _vp]),
+    "fl_swiglu_ffn_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _f, _i, _vp]),
     "fl_last_error": (ctypes.c_char_p, []),
     "fl_device_status": (_i, [_vp]),
     "fl_set_option": (_i, [_i, _i]),
@@ -167,6 +168,21 @@ def swiglu_ffn(x, gamma, Wg, Wu, Wd, bias_down=None, out=None, eps=1e-6, workspa
     ws_bytes = workspace.numel() * workspace.element_size()
     _check(lib().fl_swiglu_ffn(_ptr(x), _ptr(gamma), _ptr(Wg), _ptr(Wu), _ptr(Wd), _ptr(bias_down), _ptr(out),
                                M, D, F, float(eps), _ptr(workspace), ws_bytes, _dtype_code(x), _stream(stream)))
+    return out
+
+
+def swiglu_ffn_noalloc(x, gamma, Wg, Wu, Wd, bias_down=None, out=None, eps=1e-6, stream=None):
+    """swiglu_ffn for callers that may not allocate device memory: h lives in the
+    library's fixed 8 MiB device array (M * F * 2 bytes at most). Calls whose
+    kernels overlap on the GPU race on that array."""
+    import torch
+    M, D = x.shape
+    F = Wg.shape[0]
+    if out is None:
+        out = torch.empty_like(x)
+    _check_tensors(x.dtype, x=x, gamma=gamma, Wg=Wg, Wu=Wu, Wd=Wd, bias_down=bias_down, out=out)
+    _check(lib().fl_swiglu_ffn_noalloc(_ptr(x), _ptr(gamma), _ptr(Wg), _ptr(Wu), _ptr(Wd), _ptr(bias_down),
+                                       _ptr(out), M, D, F, float(eps), _dtype_code(x), _stream(stream)))
     return out
 
 

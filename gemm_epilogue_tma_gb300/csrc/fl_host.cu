@@ -365,6 +365,8 @@ bool valid_dtype(int dt) { return dt == FL_F16 || dt == FL_BF16; }
 
 }  // namespace
 
+int fl::set_last_error(int status, const char* message) { return fail((fl_status)status, "%s", message); }
+
 // ===========================================================================
 // C ABI
 // ===========================================================================

@@ -47,6 +47,9 @@ struct GemmParams {
     int pdl;       // launch with a programmatic dependency on the previous kernel of the stream
 };
 
+// Records a status message for fl_last_error() on this thread; returns status.
+int set_last_error(int status, const char* message);
+
 // Kernel launchers, explicitly instantiated in the kernel translation units.
 template <int DT, int BN, int PRO, bool DUAL>
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream);

@@ -136,6 +136,28 @@ fl_status fl_swiglu_ffn(const void* x, const void* gamma, const void* Wg, const 
                         float eps, void* workspace, size_t workspace_bytes, fl_dtype dtype,
                         void* stream);
 
+/*
+ * fl_swiglu_ffn without a workspace argument, for callers that may not
+ * allocate device memory at call time: an inference engine or plugin that
+ * owns a fixed, pre-planned memory budget, or code that runs where an
+ * allocation is not allowed. The pages have no counterpart; this is a
+ * library convenience.
+ *   Arguments and results are those of fl_swiglu_ffn; the hidden activation
+ *   h [M,F] is kept in one fixed 8 MiB device array that the library holds on
+ *   every GPU that loads it, until the process exits. M * F * 2 must be at
+ *   most 8 MiB (for example M = 256 at F = 11008); larger calls return
+ *   FL_ERR_WORKSPACE without launching.
+ *   The call allocates nothing. Its first call on a device looks up the
+ *   array's device address for that device (cudaGetSymbolAddress); make that
+ *   first call before any stream capture.
+ *   All calls share the array and it keeps the last call's h: two calls whose
+ *   kernels overlap on the GPU (different streams, or different host threads)
+ *   race on it and give wrong results.
+ */
+fl_status fl_swiglu_ffn_noalloc(const void* x, const void* gamma, const void* Wg, const void* Wu,
+                                const void* Wd, const void* bias_down, void* out, int M, int D,
+                                int F, float eps, fl_dtype dtype, void* stream);
+
 /* Message for the last non-OK status returned on this thread ("" if none). */
 const char* fl_last_error(void);
 
