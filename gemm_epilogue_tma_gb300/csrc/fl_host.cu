@@ -202,7 +202,7 @@ int max_clusters(int dt, int bn, int pro, int splits) {
 
 bool plan_splitk(int dt, int pro, int M, int N, int K, int sms, SplitPlan* plan) {
     const int variant = g_opt_variant.load();
-    if (variant == 1) return false;
+    if (variant == 1 || variant == 3) return false;
     const int nk = (K + fl::kBK - 1) / fl::kBK;
     const int mb = (M + fl::kBM - 1) / fl::kBM;
     // 128-wide weight tiles stage more bytes per pipeline slot (more bytes in
@@ -244,6 +244,87 @@ bool plan_splitk(int dt, int pro, int M, int N, int K, int sms, SplitPlan* plan)
     plan->kps = kps;
     plan->splits = (nk + kps - 1) / kps;  // every split gets at least one K block
     return true;
+}
+
+int pair_max(int dt, int bn, int pro) {
+    static std::atomic<int> cache[2][2][3];
+    const int bi = bn == 256 ? 1 : 0;
+    int v = cache[dt][bi][pro].load();
+    if (v != 0) return v;
+#define FL_Q(DT, BN, PRO) \
+    if (dt == DT && bn == BN && pro == PRO) v = fl::pair_max_clusters<DT, BN, PRO>();
+    FL_Q(0, 128, 0) FL_Q(0, 128, 1) FL_Q(0, 128, 2) FL_Q(0, 256, 0) FL_Q(0, 256, 1) FL_Q(0, 256, 2)
+    FL_Q(1, 128, 0) FL_Q(1, 128, 1) FL_Q(1, 128, 2) FL_Q(1, 256, 0) FL_Q(1, 256, 1) FL_Q(1, 256, 2)
+#undef FL_Q
+    if (v <= 0) v = -1;
+    cache[dt][bi][pro] = v;
+    return v;
+}
+
+cudaError_t dispatch_pair(int dt, int bn, int pro, const GemmParams& p, int grid, cudaStream_t s) {
+#define FL_CASE(DT, BN, PRO) \
+    if (dt == DT && bn == BN && pro == PRO) return fl::launch_pair<DT, BN, PRO>(p, grid, s);
+    FL_CASE(0, 128, 0) FL_CASE(0, 128, 1) FL_CASE(0, 128, 2) FL_CASE(0, 256, 0) FL_CASE(0, 256, 1) FL_CASE(0, 256, 2)
+    FL_CASE(1, 128, 0) FL_CASE(1, 128, 1) FL_CASE(1, 128, 2) FL_CASE(1, 256, 0) FL_CASE(1, 256, 1) FL_CASE(1, 256, 2)
+#undef FL_CASE
+    return cudaErrorInvalidValue;
+}
+
+// The CTA-pair kernel when its tiles keep most resident pairs busy (it halves
+// each SM's weight traffic through shared memory). Tile width 256 when that
+// fills the pairs, else 128. FL_OPT_VARIANT = 3 forces it (FL_OPT_TILE_N picks
+// the width).
+bool use_pair(int dt, int pro, int M, int N, int* pairs, int* bn_out) {
+    const int variant = g_opt_variant.load();
+    if (variant == 1 || variant == 2) return false;
+    const int forced = g_opt_tile_n.load();
+    const long long mp = (M + 255) / 256;
+    const long long t256 = mp * ((N + 255) / 256), t128 = mp * ((N + 127) / 128);
+    // automatic choice: 256-wide pair tiles that keep 80 % of the resident pairs
+    // busy; a 128-wide pair tile moves as many shared-memory bytes per MMA as
+    // the single-CTA 128 x 256 tile and measures no faster, so it is only used
+    // when forced
+    int bn = forced == 128 || forced == 256 ? forced : 256;
+    const int maxp = pair_max(dt, bn, pro);
+    if (maxp <= 0) return false;
+    const long long tiles = bn == 256 ? t256 : t128;
+    if (variant != 3 && (bn != 256 || tiles * 5 < (long long)maxp * 4)) return false;
+    *pairs = (int)(tiles < maxp ? tiles : maxp);
+    *bn_out = bn;
+    return true;
+}
+
+fl_status run_pair(int dt, int pro, const void* A, const void* W, const void* bias, const void* residual,
+                   const void* gamma, const void* beta, void* out, int M, int N, int K, int act, float eps, int pairs,
+                   int bn, DeviceInfo* di, cudaStream_t stream) {
+    GemmParams p;
+    memset(&p, 0, sizeof(p));
+    fl_status st;
+    if ((st = encode_2d(&p.tmA, dt, A, K, M, fl::kBK, fl::kBM)) != FL_OK) return st;
+    if ((st = encode_2d(&p.tmB, dt, W, K, N, fl::kBK, bn / 2)) != FL_OK) return st;
+    if ((st = encode_2d(&p.tmOut, dt, out, N, M, 64, 32)) != FL_OK) return st;
+    if (pro != fl::PRO_NONE && (st = encode_2d(&p.tmGamma, dt, gamma, K, 1, fl::kBK, 1, false)) != FL_OK) return st;
+    if (pro == fl::PRO_LN && beta != nullptr && (st = encode_2d(&p.tmBeta, dt, beta, K, 1, fl::kBK, 1, false)) != FL_OK)
+        return st;
+    p.bias = bias;
+    p.residual = residual;
+    p.gamma = gamma;
+    p.beta = beta;
+    p.status = di->status;
+    p.timeout_ns = (unsigned long long)g_opt_timeout_ms.load() * 1000000ull;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.num_m_blocks = (M + 255) / 256;  // row blocks of a pair tile
+    p.num_n_blocks = (N + bn - 1) / bn;
+    p.num_k_blocks = (K + fl::kBK - 1) / fl::kBK;
+    p.num_tiles = p.num_m_blocks * p.num_n_blocks;
+    p.act = act;
+    p.eps = eps;
+    p.pdl = g_opt_pdl.load();
+    cudaError_t e = dispatch_pair(dt, bn, pro, p, 2 * pairs, stream);
+    if (e != cudaSuccess) return fail(FL_ERR_CUDA, "pair kernel launch failed: %s", cudaGetErrorString(e));
+    return ok();
 }
 
 // CTA tile width. A wider tile halves the activation re-reads and the shared
@@ -307,6 +388,9 @@ fl_status run_tile(int dt, int pro, bool dual, const void* A, const void* W, con
     DeviceInfo* di = nullptr;
     fl_status st = device_info(&di);
     if (st != FL_OK) return st;
+    int pairs = 0, pair_bn = 256;
+    if (!dual && use_pair(dt, pro, M, N, &pairs, &pair_bn))
+        return run_pair(dt, pro, A, W, bias, residual, gamma, beta, out, M, N, K, act, eps, pairs, pair_bn, di, stream);
     SplitPlan plan;
     if (!dual && plan_splitk(dt, pro, M, N, K, di->sms, &plan))
         return run_splitk(dt, pro, A, W, bias, residual, gamma, beta, out, M, N, K, act, eps, plan, di, stream);
@@ -383,7 +467,7 @@ fl_status fl_set_option(fl_option key, int value) {
             g_opt_tile_n = value;
             return ok();
         case FL_OPT_VARIANT:
-            if (value < 0 || value > 2) return fail(FL_ERR_INVALID_ARG, "variant must be 0, 1 or 2");
+            if (value < 0 || value > 3) return fail(FL_ERR_INVALID_ARG, "variant must be 0..3");
             g_opt_variant = value;
             return ok();
         case FL_OPT_TIMEOUT_MS:

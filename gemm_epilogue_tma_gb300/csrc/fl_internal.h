@@ -60,6 +60,12 @@ cudaError_t launch_splitk(const GemmParams& p, int grid, int splits, cudaStream_
 template <int DT, int BN, int PRO>
 int splitk_max_clusters(int splits);
 
+template <int DT, int BN, int PRO>
+cudaError_t launch_pair(const GemmParams& p, int grid, cudaStream_t stream);
+
+template <int DT, int BN, int PRO>
+int pair_max_clusters();
+
 // Shared-memory layout of the split-K kernel.
 template <int BN>
 struct SplitCfg {

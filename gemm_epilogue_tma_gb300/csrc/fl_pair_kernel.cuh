@@ -1,0 +1,555 @@
+// CTA-pair fused dense-layer kernel for sm_103a (tcgen05.mma.cta_group::2).
+//
+// A cluster of two CTAs on two SMs computes one 256 x 256 output tile per
+// step: CTA r stages activation rows [128 r, 128 r + 128) of the tile and
+// weight rows [128 r, 128 r + 128) of its 256 columns; the leader (rank 0)
+// issues one 256 x 256 x 16 MMA per K slice, whose operands come from both
+// shared memories and whose accumulator rows land 128 / 128 in the two tensor
+// memories. Each SM therefore stages and reads only half of the weight tile:
+// per 64-wide K slice an SM moves 64 KB through shared memory for 512 cycles
+// of MMA work (a single-CTA 128 x 256 tile moves 96 KB for the same work).
+//
+// Plain patterns keep both operands in shared memory and double-buffer the
+// accumulator (2 x 256 TMEM columns). Norm prologues fold the activation into
+// tensor memory (thread t of the transform warpgroup owns row t), so the MMA
+// reads A from TMEM; the accumulator is then single-buffered (256 columns +
+// 6 x 32 activation columns; with 128-wide tiles both accumulator buffers
+// still fit).
+//
+// Barriers: `full` (leader) counts the bytes of both CTAs' weight halves (and,
+// for plain patterns, of both activation halves) through the pair form of the
+// TMA load; `afull` (each CTA) counts that CTA's activation and gamma/beta
+// slices for its fold; `xform` (leader) collects the fold warps of both CTAs;
+// `empty`, `tfull` are signalled in both CTAs by multicast commits; `tempty`
+// (leader) collects both CTAs' epilogue warps. Every wait is bounded.
+#pragma once
+
+#include "fl_common.cuh"
+#include "fl_fold.cuh"
+
+namespace fl {
+
+template <int BN_, int PRO, bool ATMEM_ = true>
+struct PairCfg {
+    static constexpr int BN = BN_;       // output columns of a pair tile (128 or 256)
+    static constexpr int HALF = BN / 2;  // weight rows staged per CTA
+    static constexpr int A_BYTES = kBM * kBK * 2;
+    static constexpr int B_BYTES = HALF * kBK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr bool ATMEM = PRO != PRO_NONE && ATMEM_;  // fold into TMEM (else in place in smem)
+    static constexpr int STAGES_RAW = (192 * 1024) / STAGE_BYTES;
+    static constexpr int STAGES = ATMEM ? (STAGES_RAW > 6 ? 6 : STAGES_RAW) : (STAGES_RAW > 8 ? 8 : STAGES_RAW);
+    // double-buffer the accumulator unless the activation slots need the room
+    static constexpr int NBUF = (ATMEM && 2 * BN + 32 * STAGES > 512) ? 1 : 2;
+    static constexpr int ACC_COLS = BN;
+    static constexpr int A_COL0 = NBUF * ACC_COLS;
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int EPI_BUF_BYTES = 32 * 128;
+    static constexpr int OFF_EPI = STAGES * STAGE_BYTES;
+    static constexpr int OFF_BAR = OFF_EPI + 4 * EPI_BUF_BYTES;
+    static constexpr int NUM_BARS = 4 * STAGES + 8;
+    static constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
+    static constexpr int OFF_ROWSCALE = (OFF_SLOT + 16 + 15) / 16 * 16;
+    static constexpr int OFF_GB = (OFF_ROWSCALE + 2 * kBM * 4 + 127) / 128 * 128;
+    static constexpr int SMEM_BYTES = OFF_GB + STAGES * 256 + 1024;
+    static_assert(!ATMEM || A_COL0 + 32 * STAGES <= TMEM_COLS, "activation slots must fit in tensor memory");
+};
+
+// Fold mode of the pair kernel's norm prologues: into tensor memory (the
+// in-place shared-memory fold is kept for comparison; it measures slower).
+constexpr bool kPairFoldToTmem = true;
+
+template <int DT, int BN, int PRO>
+__global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
+    fl_pair_kernel(const __grid_constant__ GemmParams p) {
+    using C = PairCfg<BN, PRO, kPairFoldToTmem>;
+    using Ops = DTypeOps<DT>;
+    constexpr int S = C::STAGES;
+    constexpr int EPI_WARP0 = PRO != PRO_NONE ? 8 : 4;
+    constexpr uint32_t IDESC = umma_idesc_f16(Ops::kFormat, 2 * kBM, C::BN);
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    const uint32_t sbase = (raw_addr + 1023u) & ~1023u;
+    uint8_t* smem = smem_raw + (sbase - raw_addr);
+
+    auto stage_a = [&](int s) { return sbase + s * C::STAGE_BYTES; };
+    auto stage_b = [&](int s) { return sbase + s * C::STAGE_BYTES + C::A_BYTES; };
+    const uint32_t bar0 = sbase + C::OFF_BAR;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto afull_bar = [&](int s) { return bar0 + 8u * (S + s); };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (2 * S + s); };
+    auto xform_bar = [&](int s) { return bar0 + 8u * (3 * S + s); };
+    auto tfull_bar = [&](int b) { return bar0 + 8u * (4 * S + b); };
+    auto tempty_bar = [&](int b) { return bar0 + 8u * (4 * S + 2 + b); };
+    auto sready_bar = [&](int b) { return bar0 + 8u * (4 * S + 4 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (4 * S + 6);
+    const uint32_t tdone_bar = bar0 + 8u * (4 * S + 7);  // this CTA's epilogue finished a tile
+    const uint32_t slot_addr = sbase + C::OFF_SLOT;
+    float* rowscale = reinterpret_cast<float*>(smem + C::OFF_ROWSCALE);
+    auto gb_slot = [&](int s) { return sbase + C::OFF_GB + 256u * s; };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank() & 1u;
+    const bool leader = rank == 0;
+    auto lead = [&](uint32_t local_addr) { return mapa_cluster(local_addr, 0); };  // leader's copy
+    const int nk = p.num_k_blocks;
+    const int npairs = (int)gridDim.x / 2;
+    const int pair = (int)blockIdx.x / 2;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(afull_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+            mbar_init(xform_bar(s), 8);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull_bar(b), 1);
+            mbar_init(tempty_bar(b), 8);
+            mbar_init(sready_bar(b), 4);
+        }
+        mbar_init(drain_bar, 1);
+        mbar_init(tdone_bar, 4);
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&p.tmA);
+        tma_prefetch_desc(&p.tmB);
+        tma_prefetch_desc(&p.tmOut);
+        if (PRO != PRO_NONE) tma_prefetch_desc(&p.tmGamma);
+        if (PRO == PRO_LN && p.beta != nullptr) tma_prefetch_desc(&p.tmBeta);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(slot_addr, C::TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_barrier_sync();  // both CTAs' barriers exist before either signals the other
+    tc_fence_after();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + C::OFF_SLOT);
+    griddep_wait();
+    if (threadIdx.x == 0) griddep_launch_dependents();
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer (both CTAs)
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int issued = 0;
+            bool ok = true;
+            const uint32_t gb_bytes = PRO != PRO_NONE ? 128u + (PRO == PRO_LN && p.beta != nullptr ? 128u : 0u) : 0u;
+            for (int tile = pair; ok && tile < p.num_tiles; tile += npairs) {
+                const int m0 = (tile % p.num_m_blocks) * 2 * kBM + (int)rank * kBM;
+                const int nh = (tile / p.num_m_blocks) * C::BN + (int)rank * C::HALF;
+                const int passes = PRO == PRO_LN ? 2 : 1;
+                for (int pass = 0; ok && pass < passes; ++pass) {
+                    const bool stats = PRO == PRO_LN && pass == 0;
+                    for (int kb = 0; kb < nk; ++kb) {
+                        if (!wait_bar(empty_bar(s), ph ^ 1u, p.status, p.timeout_ns, 31)) {
+                            ok = false;
+                            break;
+                        }
+                        if (stats) {
+                            mbar_arrive_expect_tx(afull_bar(s), (uint32_t)C::A_BYTES);
+                            tma_load_2d(stage_a(s), &p.tmA, afull_bar(s), kb * kBK, m0);
+                            if (leader) mbar_arrive(full_bar(s));  // keeps full's phases in step with the ring
+                        } else if (PRO == PRO_NONE) {
+                            if (leader) mbar_arrive_expect_tx(full_bar(s), 2u * C::STAGE_BYTES);
+                            const uint32_t fb = lead(full_bar(s));
+                            tma_load_2d_pair(stage_a(s), &p.tmA, fb, kb * kBK, m0);
+                            tma_load_2d_pair(stage_b(s), &p.tmB, fb, kb * kBK, nh);
+                        } else {
+                            mbar_arrive_expect_tx(afull_bar(s), (uint32_t)C::A_BYTES + gb_bytes);
+                            tma_load_2d(stage_a(s), &p.tmA, afull_bar(s), kb * kBK, m0);
+                            tma_load_2d(gb_slot(s), &p.tmGamma, afull_bar(s), kb * kBK, 0);
+                            if (PRO == PRO_LN && p.beta != nullptr)
+                                tma_load_2d(gb_slot(s) + 128, &p.tmBeta, afull_bar(s), kb * kBK, 0);
+                            if (leader) mbar_arrive_expect_tx(full_bar(s), 2u * C::B_BYTES);
+                            tma_load_2d_pair(stage_b(s), &p.tmB, lead(full_bar(s)), kb * kBK, nh);
+                        }
+                        ++issued;
+                        if (++s == S) {
+                            s = 0;
+                            ph ^= 1u;
+                        }
+                    }
+                }
+            }
+            // Drain: the leader's `full` covers both CTAs' pair loads; each CTA's
+            // `afull` covers its own activation loads.
+            const int pending = issued < S ? issued : S;
+            for (int i = 1; i <= pending; ++i) {
+                const int idx = issued - i;
+                const uint32_t par = (uint32_t)((idx / S) & 1);
+                if (leader) wait_bar_drain(full_bar(idx % S), par, 20000000ull);
+                if (PRO != PRO_NONE) wait_bar_drain(afull_bar(idx % S), par, 20000000ull);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer (leader)
+        if (lane == 0 && leader) {
+            int s = 0;
+            uint32_t ph = 0;
+            int it = 0;
+            bool ok = true;
+            for (int tile = pair; ok && tile < p.num_tiles; tile += npairs, ++it) {
+                const int buf = C::NBUF == 2 ? (it & 1) : 0;
+                const uint32_t tph = C::NBUF == 2 ? (uint32_t)((it >> 1) & 1) : (uint32_t)(it & 1);
+                if (PRO == PRO_LN) {
+                    // statistics pass: both CTAs' fold warps read these stages; release them in both
+                    for (int kb = 0; kb < nk; ++kb) {
+                        if (!wait_bar_cluster(xform_bar(s), ph, p.status, p.timeout_ns, 32) ||
+                            !wait_bar(full_bar(s), ph, p.status, p.timeout_ns, 33)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive(empty_bar(s));
+                        mbar_arrive_cluster(mapa_cluster(empty_bar(s), 1));
+                        if (++s == S) {
+                            s = 0;
+                            ph ^= 1u;
+                        }
+                    }
+                    if (!ok) break;
+                }
+                if (!wait_bar_cluster(tempty_bar(buf), tph ^ 1u, p.status, p.timeout_ns, 34)) break;
+                tc_fence_after();
+                const uint32_t d = tmem_base + (uint32_t)(buf * C::ACC_COLS);
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!wait_bar_cluster(full_bar(s), ph, p.status, p.timeout_ns, 35)) {
+                        ok = false;
+                        break;
+                    }
+                    if (PRO != PRO_NONE && !wait_bar_cluster(xform_bar(s), ph, p.status, p.timeout_ns, 36)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t da = sw128_kmajor_desc(stage_a(s));
+                    const uint64_t db = sw128_kmajor_desc(stage_b(s));
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        if (C::ATMEM)
+                            umma_f16_ts_pair(d, tmem_base + (uint32_t)C::A_COL0 + 32u * s + 8u * kk, db + 2 * kk, IDESC,
+                                             (kb | kk) != 0);
+                        else
+                            umma_f16_ss_pair(d, da + 2 * kk, db + 2 * kk, IDESC, (kb | kk) != 0);
+                    }
+                    umma_commit_pair(empty_bar(s), (uint16_t)0x3);
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit_pair(tfull_bar(buf), (uint16_t)0x3);
+            }
+            umma_commit_pair(drain_bar, (uint16_t)0x1);
+            wait_bar_drain(drain_bar, 0, 20000000ull);
+        }
+    } else if (PRO != PRO_NONE && !C::ATMEM && warp >= 4 && warp < 8) {
+        // ------------------------------------------------------------ fold in place in smem (both CTAs)
+        const int t = threadIdx.x - 128;
+        const int j = t & 7;
+        int s = 0;
+        uint32_t ph = 0;
+        int it = 0;
+        bool ok = true;
+        for (int tile = pair; ok && tile < p.num_tiles; tile += npairs, ++it) {
+            float mean[8], rstd[8], ss[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                mean[i] = 0.f;
+                rstd[i] = 1.f;
+                ss[i] = 0.f;
+            }
+            if (PRO == PRO_LN) {
+                RowMoments mo[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mo[i] = RowMoments{0.f, 0.f, 0.f};
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!wait_bar(afull_bar(s), ph, p.status, p.timeout_ns, 37)) {
+                        ok = false;
+                        break;
+                    }
+                    ln_stats_stage<DT>(stage_a(s), t, 8, kb * kBK + j * 8 < p.K, mo);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(lead(xform_bar(s)));
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                ln_stats_allreduce(mo, 8);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    mean[i] = mo[i].mean;
+                    rstd[i] = rsqrtf(mo[i].m2 / (float)p.K + p.eps);
+                }
+            }
+            for (int kb = 0; kb < nk; ++kb) {
+                if (!wait_bar(afull_bar(s), ph, p.status, p.timeout_ns, 38)) {
+                    ok = false;
+                    break;
+                }
+                if (PRO == PRO_RMS)
+                    fold_rms_stage<DT>(stage_a(s), gb_slot(s), t, 8, ss);
+                else
+                    fold_ln_stage<DT>(stage_a(s), gb_slot(s), p.beta != nullptr, t, 8, mean, rstd);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(lead(xform_bar(s)));
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (!ok) break;
+            if (PRO == PRO_RMS) {
+                const int rb = it & 1;
+                const uint32_t tph = (uint32_t)(it & 1);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) ss[i] = row_allreduce8(ss[i]);
+                if (!wait_bar(tdone_bar, tph ^ 1u, p.status, p.timeout_ns, 39)) break;
+                if (j == 0) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) rowscale[rb * kBM + (t >> 3) + 16 * i] = rsqrtf(ss[i] / (float)p.K + p.eps);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sready_bar(rb));
+            }
+        }
+    } else if (PRO != PRO_NONE && warp >= 4 && warp < 8) {
+        // ------------------------------------------------------------ fold into TMEM (both CTAs)
+        const int t = threadIdx.x - 128;
+        const uint32_t a_lane = (uint32_t)(32 * (warp & 3)) << 16;
+        int s = 0;
+        uint32_t ph = 0;
+        int it = 0;
+        bool ok = true;
+        for (int tile = pair; ok && tile < p.num_tiles; tile += npairs, ++it) {
+            float mean = 0.f, rstd = 1.f;
+            float ss[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ss[i] = 0.f;
+            if (PRO == PRO_LN) {
+                RowMoments mo{0.f, 0.f, 0.f};
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!wait_bar(afull_bar(s), ph, p.status, p.timeout_ns, 37)) {
+                        ok = false;
+                        break;
+                    }
+                    ln_stats_row<DT>(stage_a(s), t, min(8, (p.K - kb * kBK) / 8), mo);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(lead(xform_bar(s)));
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mean = mo.mean;
+                rstd = rsqrtf(mo.m2 / (float)p.K + p.eps);
+            }
+            for (int kb = 0; kb < nk; ++kb) {
+                if (!wait_bar(afull_bar(s), ph, p.status, p.timeout_ns, 38)) {
+                    ok = false;
+                    break;
+                }
+                uint32_t o[32];
+                if (PRO == PRO_RMS)
+                    fold_rms_row<DT>(stage_a(s), gb_slot(s), t, ss, o);
+                else
+                    fold_ln_row<DT>(stage_a(s), gb_slot(s), p.beta != nullptr, t, mean, rstd, o);
+                tmem_st_32x32b_x32(tmem_base + a_lane + (uint32_t)C::A_COL0 + 32u * s, o);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(lead(xform_bar(s)));
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (!ok) break;
+            if (PRO == PRO_RMS) {
+                // row scales of tile `it` go to buffer it & 1; this CTA's epilogue of
+                // tile it - 2 (same buffer) has read it once it has finished tile it - 1
+                const int rb = it & 1;
+                const uint32_t tph = (uint32_t)(it & 1);
+                if (!wait_bar(tdone_bar, tph ^ 1u, p.status, p.timeout_ns, 39)) break;
+                const float sum = ((ss[0] + ss[1]) + (ss[2] + ss[3])) + ((ss[4] + ss[5]) + (ss[6] + ss[7]));
+                rowscale[rb * kBM + t] = rsqrtf(sum / (float)p.K + p.eps);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sready_bar(rb));
+            }
+        }
+    } else if (warp >= EPI_WARP0) {
+        // ------------------------------------------------------------ epilogue (both CTAs)
+        const int q = warp & 3;
+        const uint32_t ebuf = sbase + C::OFF_EPI + q * C::EPI_BUF_BYTES;
+        const uint32_t my_row_addr = ebuf + lane * 128;
+        const int sw = lane & 7;
+        int it = 0;
+        using T = uint16_t;
+        const T* bias = reinterpret_cast<const T*>(p.bias);
+        const T* res = reinterpret_cast<const T*>(p.residual);
+        for (int tile = pair; tile < p.num_tiles; tile += npairs, ++it) {
+            const int m0 = (tile % p.num_m_blocks) * 2 * kBM + (int)rank * kBM;
+            const int n0 = (tile / p.num_m_blocks) * C::BN;
+            const int buf = C::NBUF == 2 ? (it & 1) : 0;
+            const uint32_t tph = C::NBUF == 2 ? (uint32_t)((it >> 1) & 1) : (uint32_t)(it & 1);
+            if (!wait_bar(tfull_bar(buf), tph, p.status, p.timeout_ns, 40)) break;
+            tc_fence_after();
+            float rs = 1.f;
+            if (PRO == PRO_RMS) {
+                if (!wait_bar(sready_bar(it & 1), (uint32_t)((it >> 1) & 1), p.status, p.timeout_ns, 41)) break;
+                rs = rowscale[(it & 1) * kBM + q * 32 + lane];
+            }
+            const int row = m0 + q * 32 + lane;
+            const bool row_ok = row < p.M;
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * C::ACC_COLS);
+            if (m0 + q * 32 < p.M) {
+                for (int c = 0; c < C::BN / 64; ++c) {
+                    const int col0 = n0 + c * 64;
+                    if (col0 >= p.N) break;
+                    if (lane == 0) bulk_wait_group_read<0>();
+                    __syncwarp();
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int cbase = col0 + h * 32;
+                        uint32_t acc[32];
+                        tmem_ld_32x32b_x32(tbase + c * 64 + h * 32, acc);
+                        tmem_ld_wait();
+                        float v[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(acc[e]) * rs;
+                        if (bias != nullptr) {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                if (cbase + j * 8 < p.N) {
+                                    const uint4 bv = ldg_v4(bias + cbase + j * 8);
+                                    const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) {
+                                        const float2 b2 = Ops::unpack(bw[e]);
+                                        v[j * 8 + 2 * e] += b2.x;
+                                        v[j * 8 + 2 * e + 1] += b2.y;
+                                    }
+                                }
+                            }
+                        }
+                        if (p.act != ACT_NONE) {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) v[e] = act_apply(p.act, v[e]);
+                        }
+                        if (res != nullptr && row_ok) {
+                            const T* rrow = res + (size_t)row * p.N;
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                if (cbase + j * 8 < p.N) {
+                                    const uint4 rv = *reinterpret_cast<const uint4*>(rrow + cbase + j * 8);
+                                    const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) {
+                                        const float2 r2 = Ops::unpack(rw[e]);
+                                        v[j * 8 + 2 * e] += r2.x;
+                                        v[j * 8 + 2 * e + 1] += r2.y;
+                                    }
+                                }
+                            }
+                        }
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int chunk = h * 4 + j;
+                            st_shared_v4(my_row_addr + ((chunk ^ sw) << 4), Ops::pack(v[j * 8 + 0], v[j * 8 + 1]),
+                                         Ops::pack(v[j * 8 + 2], v[j * 8 + 3]), Ops::pack(v[j * 8 + 4], v[j * 8 + 5]),
+                                         Ops::pack(v[j * 8 + 6], v[j * 8 + 7]));
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&p.tmOut, ebuf, col0, m0 + q * 32);
+                        bulk_commit_group();
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive_cluster(lead(tempty_bar(buf)));
+                mbar_arrive(tdone_bar);
+            }
+        }
+        if (lane == 0) bulk_wait_group<0>();
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    cluster_barrier_sync();  // neither CTA's barriers or TMEM go away while the other may use them
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    }
+}
+
+// How many CTA pairs of this kernel can be resident at once.
+template <int DT, int BN, int PRO>
+int pair_max_clusters() {
+    using C = PairCfg<BN, PRO, kPairFoldToTmem>;
+    auto kern = fl_pair_kernel<DT, BN, PRO>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(PRO != PRO_NONE ? 384 : 256, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+template <int DT, int BN, int PRO>
+cudaError_t launch_pair(const GemmParams& p, int grid, cudaStream_t stream) {
+    using C = PairCfg<BN, PRO, kPairFoldToTmem>;
+    auto kern = fl_pair_kernel<DT, BN, PRO>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(PRO != PRO_NONE ? 384 : 256, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = p.pdl;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+}  // namespace fl

@@ -171,7 +171,9 @@ fl_status fl_device_status(void* stream);
 /*
  * Tuning overrides, for benchmarks and tests (process-wide, not thread-safe):
  *   FL_OPT_TILE_N:      0 = automatic, else the CTA tile width (128 or 256).
- *   FL_OPT_VARIANT:     0 = automatic, 1 = tile kernel, 2 = small-M split-K kernel.
+ *   FL_OPT_VARIANT:     0 = automatic, 1 = tile kernel, 2 = small-M split-K kernel,
+ *                       3 = CTA-pair kernel (256 x 256 tiles on two SMs; not
+ *                       used by the SwiGLU gate/up kernel).
  *   FL_OPT_TIMEOUT_MS:  limit of every device-side wait (default 2000).
  *   FL_OPT_SPLIT_K:     0 = automatic, else the K split of the small-M kernel (1..8).
  *   FL_OPT_PDL:         1 (default) = launch each kernel with a programmatic

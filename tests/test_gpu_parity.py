@@ -195,6 +195,56 @@ def test_splitk_wide_tiles_and_norm_bias_act(dt):
 
 
 # ---------------------------------------------------------------------------
+# the CTA-pair kernel (cta_group::2, 256 x 256 tiles on two SMs), forced
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("shape", [(1, 8, 8), (200, 136, 328), (300, 520, 1000), (512, 512, 512), (640, 264, 2056),
+                                   (1536, 1280, 648)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_pair_variant_all_patterns(dt, tile_n, shape):
+    """Includes a shape with several tiles per pair (persistent loop, buffer reuse)."""
+    M, N, K = shape
+    t = syn.dense_layer_inputs(M, N, K, dt)
+    fl.set_option("variant", 3)
+    fl.set_option("tile_n", tile_n)
+    try:
+        rows = sample_rows(M, n=384)
+        for pattern in syn.PATTERNS:
+            got, ref = run_pattern(t, pattern, rows=rows)
+            assert_close(got, ref, dt, f"pair BN={tile_n} {pattern} {dt} {M}x{N}x{K}")
+        fl.device_status()
+    finally:
+        fl.set_option("variant", 0)
+        fl.set_option("tile_n", 0)
+
+
+@pytest.mark.parametrize("dt", DTYPES)
+def test_pair_norm_bias_act_residual_alias(dt):
+    M, N, K = 777, 520, 776
+    t = syn.norm_gemm_inputs(M, N, K, "layer", dt, with_bias=True)
+    fl.set_option("variant", 3)
+    try:
+        for norm in ("rms", "layer"):
+            for act in ("silu", "gelu"):
+                got = fl.norm_gemm(dev(t["x"]), dev(t["gamma"]), dev(t["W"]), beta=dev(t["beta"]),
+                                   bias=dev(t["bias"]), eps=1e-5, norm=norm, act=act)
+                torch.cuda.synchronize()
+                ref = oracle.norm_gemm(f64(t["x"]), f64(t["gamma"]), f64(t["beta"]), f64(t["W"]), f64(t["bias"]),
+                                       1e-5, norm, act)
+                assert_close(got, ref, dt, f"pair {norm} {act}")
+        r = syn.gemm_inputs(M, N, K, "gemm_bias_residual", dt)
+        res = dev(r["residual"])
+        fl.gemm_epilogue(dev(r["A"]), dev(r["W"]), bias=dev(r["bias"]), residual=res, out=res,
+                         pattern="gemm_bias_residual")
+        torch.cuda.synchronize()
+        ref = oracle.gemm_epilogue(f64(r["A"]), f64(r["W"]), f64(r["bias"]), f64(r["residual"]), "gemm_bias_residual")
+        assert_close(res, ref, dt, "pair residual alias")
+    finally:
+        fl.set_option("variant", 0)
+
+
+# ---------------------------------------------------------------------------
 # the workloads of the pages, at full size
 # ---------------------------------------------------------------------------
 def test_gemm_bias_gelu_512x1024x1024_all_elements():
