@@ -93,6 +93,22 @@ __device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, 
     return wait_bar_cluster_slow(bar, parity, status, timeout_ns, where);
 }
 
+// Bounded wait with cluster-scope acquire (data written by a peer CTA).
+__device__ __noinline__ static bool wait_bar_acquire_cluster(uint32_t bar, uint32_t parity, int* status,
+                                                             unsigned long long timeout_ns, int where) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_try_wait_acquire_cluster(bar, parity)) return true;
+        if ((i & 63) == 63) {
+            if (*reinterpret_cast<volatile int*>(status) != 0) return false;
+            if (globaltimer_ns() - t0 > timeout_ns) {
+                atomicCAS(status, 0, kStatusTimeout | (where << 8));
+                return false;
+            }
+        }
+    }
+}
+
 // Time-bounded only: used while draining after a failure.
 static __device__ __noinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity, unsigned long long ns) {
     const uint64_t t0 = globaltimer_ns();

@@ -246,57 +246,80 @@ bool plan_splitk(int dt, int pro, int M, int N, int K, int sms, SplitPlan* plan)
     return true;
 }
 
-int pair_max(int dt, int bn, int pro) {
-    static std::atomic<int> cache[2][2][3];
-    const int bi = bn == 256 ? 1 : 0;
-    int v = cache[dt][bi][pro].load();
+int pair_max(int dt, int bn, int pro, int ks) {
+    // resident clusters (of 2 * ks CTAs) of each pair-kernel instance, cached
+    static std::atomic<int> cache[2][3][3];
+    const int ci = ks == 2 ? 2 : (bn == 256 ? 1 : 0);
+    int v = cache[dt][ci][pro].load();
     if (v != 0) return v;
-#define FL_Q(DT, BN, PRO) \
-    if (dt == DT && bn == BN && pro == PRO) v = fl::pair_max_clusters<DT, BN, PRO>();
-    FL_Q(0, 128, 0) FL_Q(0, 128, 1) FL_Q(0, 128, 2) FL_Q(0, 256, 0) FL_Q(0, 256, 1) FL_Q(0, 256, 2)
-    FL_Q(1, 128, 0) FL_Q(1, 128, 1) FL_Q(1, 128, 2) FL_Q(1, 256, 0) FL_Q(1, 256, 1) FL_Q(1, 256, 2)
+#define FL_Q(DT, BN, PRO, KS) \
+    if (dt == DT && bn == BN && pro == PRO && ks == KS) v = fl::pair_max_clusters<DT, BN, PRO, KS>();
+    FL_Q(0, 128, 0, 1) FL_Q(0, 128, 1, 1) FL_Q(0, 128, 2, 1) FL_Q(0, 256, 0, 1) FL_Q(0, 256, 1, 1) FL_Q(0, 256, 2, 1)
+    FL_Q(1, 128, 0, 1) FL_Q(1, 128, 1, 1) FL_Q(1, 128, 2, 1) FL_Q(1, 256, 0, 1) FL_Q(1, 256, 1, 1) FL_Q(1, 256, 2, 1)
+    FL_Q(0, 256, 0, 2) FL_Q(0, 256, 1, 2) FL_Q(0, 256, 2, 2) FL_Q(1, 256, 0, 2) FL_Q(1, 256, 1, 2) FL_Q(1, 256, 2, 2)
 #undef FL_Q
     if (v <= 0) v = -1;
-    cache[dt][bi][pro] = v;
+    cache[dt][ci][pro] = v;
     return v;
 }
 
-cudaError_t dispatch_pair(int dt, int bn, int pro, const GemmParams& p, int grid, cudaStream_t s) {
-#define FL_CASE(DT, BN, PRO) \
-    if (dt == DT && bn == BN && pro == PRO) return fl::launch_pair<DT, BN, PRO>(p, grid, s);
-    FL_CASE(0, 128, 0) FL_CASE(0, 128, 1) FL_CASE(0, 128, 2) FL_CASE(0, 256, 0) FL_CASE(0, 256, 1) FL_CASE(0, 256, 2)
-    FL_CASE(1, 128, 0) FL_CASE(1, 128, 1) FL_CASE(1, 128, 2) FL_CASE(1, 256, 0) FL_CASE(1, 256, 1) FL_CASE(1, 256, 2)
+cudaError_t dispatch_pair(int dt, int bn, int pro, int ks, const GemmParams& p, int grid, cudaStream_t s) {
+#define FL_CASE(DT, BN, PRO, KS) \
+    if (dt == DT && bn == BN && pro == PRO && ks == KS) return fl::launch_pair<DT, BN, PRO, KS>(p, grid, s);
+    FL_CASE(0, 128, 0, 1) FL_CASE(0, 128, 1, 1) FL_CASE(0, 128, 2, 1)
+    FL_CASE(0, 256, 0, 1) FL_CASE(0, 256, 1, 1) FL_CASE(0, 256, 2, 1)
+    FL_CASE(1, 128, 0, 1) FL_CASE(1, 128, 1, 1) FL_CASE(1, 128, 2, 1)
+    FL_CASE(1, 256, 0, 1) FL_CASE(1, 256, 1, 1) FL_CASE(1, 256, 2, 1)
+    FL_CASE(0, 256, 0, 2) FL_CASE(0, 256, 1, 2) FL_CASE(0, 256, 2, 2)
+    FL_CASE(1, 256, 0, 2) FL_CASE(1, 256, 1, 2) FL_CASE(1, 256, 2, 2)
 #undef FL_CASE
     return cudaErrorInvalidValue;
 }
 
-// The CTA-pair kernel when its tiles keep most resident pairs busy (it halves
-// each SM's weight traffic through shared memory). Tile width 256 when that
-// fills the pairs, else 128. FL_OPT_VARIANT = 3 forces it (FL_OPT_TILE_N picks
-// the width).
-bool use_pair(int dt, int pro, int M, int N, int* pairs, int* bn_out) {
+struct PairPlan {
+    int bn, ks, clusters;
+};
+
+// The CTA-pair kernel, when its 256-wide tiles keep 80 % of the resident pairs
+// busy: directly, or with each tile's K range split over two pairs (a cluster
+// of four) when there are half as many tiles. A 128-wide pair tile moves as
+// many shared-memory bytes per MMA as the single-CTA 128 x 256 tile and
+// measures no faster, so it is used only when forced (FL_OPT_VARIANT = 3 with
+// FL_OPT_TILE_N = 128; FL_OPT_SPLIT_K = 2 forces the K split).
+bool use_pair(int dt, int pro, int M, int N, int K, PairPlan* plan) {
     const int variant = g_opt_variant.load();
     if (variant == 1 || variant == 2) return false;
-    const int forced = g_opt_tile_n.load();
+    const int forced_bn = g_opt_tile_n.load();
+    const int forced_split = g_opt_split_k.load();
     const long long mp = (M + 255) / 256;
     const long long t256 = mp * ((N + 255) / 256), t128 = mp * ((N + 127) / 128);
-    // automatic choice: 256-wide pair tiles that keep 80 % of the resident pairs
-    // busy; a 128-wide pair tile moves as many shared-memory bytes per MMA as
-    // the single-CTA 128 x 256 tile and measures no faster, so it is only used
-    // when forced
-    int bn = forced == 128 || forced == 256 ? forced : 256;
-    const int maxp = pair_max(dt, bn, pro);
+    const int nk = (K + fl::kBK - 1) / fl::kBK;
+    if (variant == 3 && forced_bn == 128) {
+        const int maxp = pair_max(dt, 128, pro, 1);
+        if (maxp <= 0) return false;
+        *plan = PairPlan{128, 1, (int)(t128 < maxp ? t128 : maxp)};
+        return true;
+    }
+    const int maxp = pair_max(dt, 256, pro, 1);
     if (maxp <= 0) return false;
-    const long long tiles = bn == 256 ? t256 : t128;
-    if (variant != 3 && (bn != 256 || tiles * 5 < (long long)maxp * 4)) return false;
-    *pairs = (int)(tiles < maxp ? tiles : maxp);
-    *bn_out = bn;
+    const bool fills = t256 * 5 >= (long long)maxp * 4;
+    const int maxq = pair_max(dt, 256, pro, 2);
+    const bool split_fits = maxq > 0 && t256 <= maxq && nk >= 8;
+    const bool split = forced_split == 2 ? split_fits
+                                         : (!fills && split_fits && t256 * 2 * 5 >= (long long)maxp * 4);
+    if (split) {
+        *plan = PairPlan{256, 2, (int)t256};
+        return true;
+    }
+    if (variant != 3 && !fills) return false;
+    *plan = PairPlan{256, 1, (int)(t256 < maxp ? t256 : maxp)};
     return true;
 }
 
 fl_status run_pair(int dt, int pro, const void* A, const void* W, const void* bias, const void* residual,
-                   const void* gamma, const void* beta, void* out, int M, int N, int K, int act, float eps, int pairs,
-                   int bn, DeviceInfo* di, cudaStream_t stream) {
+                   const void* gamma, const void* beta, void* out, int M, int N, int K, int act, float eps,
+                   const PairPlan& plan, DeviceInfo* di, cudaStream_t stream) {
+    const int bn = plan.bn;
     GemmParams p;
     memset(&p, 0, sizeof(p));
     fl_status st;
@@ -322,7 +345,9 @@ fl_status run_pair(int dt, int pro, const void* A, const void* W, const void* bi
     p.act = act;
     p.eps = eps;
     p.pdl = g_opt_pdl.load();
-    cudaError_t e = dispatch_pair(dt, bn, pro, p, 2 * pairs, stream);
+    p.splits = plan.ks;
+    p.kps = (p.num_k_blocks + plan.ks - 1) / plan.ks;
+    cudaError_t e = dispatch_pair(dt, bn, pro, plan.ks, p, 2 * plan.ks * plan.clusters, stream);
     if (e != cudaSuccess) return fail(FL_ERR_CUDA, "pair kernel launch failed: %s", cudaGetErrorString(e));
     return ok();
 }
@@ -388,9 +413,9 @@ fl_status run_tile(int dt, int pro, bool dual, const void* A, const void* W, con
     DeviceInfo* di = nullptr;
     fl_status st = device_info(&di);
     if (st != FL_OK) return st;
-    int pairs = 0, pair_bn = 256;
-    if (!dual && use_pair(dt, pro, M, N, &pairs, &pair_bn))
-        return run_pair(dt, pro, A, W, bias, residual, gamma, beta, out, M, N, K, act, eps, pairs, pair_bn, di, stream);
+    PairPlan pplan;
+    if (!dual && use_pair(dt, pro, M, N, K, &pplan))
+        return run_pair(dt, pro, A, W, bias, residual, gamma, beta, out, M, N, K, act, eps, pplan, di, stream);
     SplitPlan plan;
     if (!dual && plan_splitk(dt, pro, M, N, K, di->sms, &plan))
         return run_splitk(dt, pro, A, W, bias, residual, gamma, beta, out, M, N, K, act, eps, plan, di, stream);

@@ -60,10 +60,10 @@ cudaError_t launch_splitk(const GemmParams& p, int grid, int splits, cudaStream_
 template <int DT, int BN, int PRO>
 int splitk_max_clusters(int splits);
 
-template <int DT, int BN, int PRO>
+template <int DT, int BN, int PRO, int KS>
 cudaError_t launch_pair(const GemmParams& p, int grid, cudaStream_t stream);
 
-template <int DT, int BN, int PRO>
+template <int DT, int BN, int PRO, int KS>
 int pair_max_clusters();
 
 // Shared-memory layout of the split-K kernel.

@@ -29,25 +29,31 @@
 
 namespace fl {
 
-template <int BN_, int PRO, bool ATMEM_ = true>
+template <int BN_, int PRO, int KS = 1>
 struct PairCfg {
     static constexpr int BN = BN_;       // output columns of a pair tile (128 or 256)
     static constexpr int HALF = BN / 2;  // weight rows staged per CTA
     static constexpr int A_BYTES = kBM * kBK * 2;
     static constexpr int B_BYTES = HALF * kBK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr bool ATMEM = PRO != PRO_NONE && ATMEM_;  // fold into TMEM (else in place in smem)
+    static constexpr bool ATMEM = PRO != PRO_NONE;  // norm prologues fold into TMEM
     static constexpr int STAGES_RAW = (192 * 1024) / STAGE_BYTES;
     static constexpr int STAGES = ATMEM ? (STAGES_RAW > 6 ? 6 : STAGES_RAW) : (STAGES_RAW > 8 ? 8 : STAGES_RAW);
     // double-buffer the accumulator unless the activation slots need the room
-    static constexpr int NBUF = (ATMEM && 2 * BN + 32 * STAGES > 512) ? 1 : 2;
+    // (split-K clusters compute one tile each)
+    static constexpr int NBUF = (KS == 2 || (ATMEM && 2 * BN + 32 * STAGES > 512)) ? 1 : 2;
     static constexpr int ACC_COLS = BN;
     static constexpr int A_COL0 = NBUF * ACC_COLS;
     static constexpr int TMEM_COLS = 512;
     static constexpr int EPI_BUF_BYTES = 32 * 128;
     static constexpr int OFF_EPI = STAGES * STAGE_BYTES;
     static constexpr int OFF_BAR = OFF_EPI + 4 * EPI_BUF_BYTES;
-    static constexpr int NUM_BARS = 4 * STAGES + 8;
+    static constexpr int NUM_BARS = 4 * STAGES + 10;
+    // split-K exchange: the K-partner's half of the partial tile, fp32 rows
+    // padded against bank conflicts, written into this CTA's (idle) ring
+    static constexpr int RECV_STRIDE = BN / 2 + 4;
+    static constexpr int OFF_RECV_SS = kBM * RECV_STRIDE * 4;
+    static_assert(KS == 1 || OFF_RECV_SS + kBM * 4 <= STAGES * STAGE_BYTES, "exchange buffer fits in the ring");
     static constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_ROWSCALE = (OFF_SLOT + 16 + 15) / 16 * 16;
     static constexpr int OFF_GB = (OFF_ROWSCALE + 2 * kBM * 4 + 127) / 128 * 128;
@@ -55,14 +61,11 @@ struct PairCfg {
     static_assert(!ATMEM || A_COL0 + 32 * STAGES <= TMEM_COLS, "activation slots must fit in tensor memory");
 };
 
-// Fold mode of the pair kernel's norm prologues: into tensor memory (the
-// in-place shared-memory fold is kept for comparison; it measures slower).
-constexpr bool kPairFoldToTmem = true;
-
-template <int DT, int BN, int PRO>
+template <int DT, int BN, int PRO, int KS>
 __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     fl_pair_kernel(const __grid_constant__ GemmParams p) {
-    using C = PairCfg<BN, PRO, kPairFoldToTmem>;
+    using C = PairCfg<BN, PRO, KS>;
+    static_assert(KS == 1 || (KS == 2 && BN == 256), "split-K pairs use 256-wide tiles");
     using Ops = DTypeOps<DT>;
     constexpr int S = C::STAGES;
     constexpr int EPI_WARP0 = PRO != PRO_NONE ? 8 : 4;
@@ -85,18 +88,29 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     auto sready_bar = [&](int b) { return bar0 + 8u * (4 * S + 4 + b); };
     const uint32_t drain_bar = bar0 + 8u * (4 * S + 6);
     const uint32_t tdone_bar = bar0 + 8u * (4 * S + 7);  // this CTA's epilogue finished a tile
+    const uint32_t ringfree_bar = bar0 + 8u * (4 * S + 8);  // split-K: the K-partner may write my ring
+    const uint32_t recvd_bar = bar0 + 8u * (4 * S + 9);     // split-K: the K-partner's half has arrived
     const uint32_t slot_addr = sbase + C::OFF_SLOT;
     float* rowscale = reinterpret_cast<float*>(smem + C::OFF_ROWSCALE);
     auto gb_slot = [&](int s) { return sbase + C::OFF_GB + 256u * s; };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = cluster_rank() & 1u;
+    // Cluster of 2 (one pair) or, with KS = 2, of 4: two pairs, one per K half
+    // of the same tile. Pair peers differ in rank bit 0; the leader is even.
+    const uint32_t crank = cluster_rank();
+    const uint32_t rank = crank & 1u;
+    const uint32_t lead_rank = crank & ~1u;
     const bool leader = rank == 0;
-    auto lead = [&](uint32_t local_addr) { return mapa_cluster(local_addr, 0); };  // leader's copy
+    const uint16_t pair_mask = (uint16_t)(0x3u << lead_rank);
+    auto lead = [&](uint32_t local_addr) { return mapa_cluster(local_addr, lead_rank); };  // leader's copy
     const int nk = p.num_k_blocks;
-    const int npairs = (int)gridDim.x / 2;
-    const int pair = (int)blockIdx.x / 2;
+    const int khalf = KS == 2 ? (int)(crank >> 1) : 0;
+    const int kb_begin = KS == 2 ? khalf * p.kps : 0;
+    const int kb_end = KS == 2 ? min(nk, kb_begin + p.kps) : nk;
+    // KS = 1: persistent pairs stride over the tiles; KS = 2: one tile per cluster
+    const int npairs = KS == 2 ? p.num_tiles : (int)gridDim.x / 2;
+    const int pair = KS == 2 ? (int)blockIdx.x / 4 : (int)blockIdx.x / 2;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -112,6 +126,8 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         }
         mbar_init(drain_bar, 1);
         mbar_init(tdone_bar, 4);
+        mbar_init(ringfree_bar, 4);
+        mbar_init(recvd_bar, 4);
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -147,7 +163,8 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                 const int passes = PRO == PRO_LN ? 2 : 1;
                 for (int pass = 0; ok && pass < passes; ++pass) {
                     const bool stats = PRO == PRO_LN && pass == 0;
-                    for (int kb = 0; kb < nk; ++kb) {
+                    const int k0 = stats ? 0 : kb_begin, k1 = stats ? nk : kb_end;
+                    for (int kb = k0; kb < k1; ++kb) {
                         if (!wait_bar(empty_bar(s), ph ^ 1u, p.status, p.timeout_ns, 31)) {
                             ok = false;
                             break;
@@ -207,7 +224,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                             break;
                         }
                         mbar_arrive(empty_bar(s));
-                        mbar_arrive_cluster(mapa_cluster(empty_bar(s), 1));
+                        mbar_arrive_cluster(mapa_cluster(empty_bar(s), crank ^ 1u));
                         if (++s == S) {
                             s = 0;
                             ph ^= 1u;
@@ -218,7 +235,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                 if (!wait_bar_cluster(tempty_bar(buf), tph ^ 1u, p.status, p.timeout_ns, 34)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(buf * C::ACC_COLS);
-                for (int kb = 0; kb < nk; ++kb) {
+                for (int kb = kb_begin; kb < kb_end; ++kb) {
                     if (!wait_bar_cluster(full_bar(s), ph, p.status, p.timeout_ns, 35)) {
                         ok = false;
                         break;
@@ -232,96 +249,24 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                     const uint64_t db = sw128_kmajor_desc(stage_b(s));
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
+                        const uint32_t acc = (kb != kb_begin) || (kk != 0);
                         if (C::ATMEM)
                             umma_f16_ts_pair(d, tmem_base + (uint32_t)C::A_COL0 + 32u * s + 8u * kk, db + 2 * kk, IDESC,
-                                             (kb | kk) != 0);
+                                             acc);
                         else
-                            umma_f16_ss_pair(d, da + 2 * kk, db + 2 * kk, IDESC, (kb | kk) != 0);
+                            umma_f16_ss_pair(d, da + 2 * kk, db + 2 * kk, IDESC, acc);
                     }
-                    umma_commit_pair(empty_bar(s), (uint16_t)0x3);
+                    umma_commit_pair(empty_bar(s), pair_mask);
                     if (++s == S) {
                         s = 0;
                         ph ^= 1u;
                     }
                 }
                 if (!ok) break;
-                umma_commit_pair(tfull_bar(buf), (uint16_t)0x3);
+                umma_commit_pair(tfull_bar(buf), pair_mask);
             }
-            umma_commit_pair(drain_bar, (uint16_t)0x1);
+            umma_commit_pair(drain_bar, (uint16_t)(1u << lead_rank));
             wait_bar_drain(drain_bar, 0, 20000000ull);
-        }
-    } else if (PRO != PRO_NONE && !C::ATMEM && warp >= 4 && warp < 8) {
-        // ------------------------------------------------------------ fold in place in smem (both CTAs)
-        const int t = threadIdx.x - 128;
-        const int j = t & 7;
-        int s = 0;
-        uint32_t ph = 0;
-        int it = 0;
-        bool ok = true;
-        for (int tile = pair; ok && tile < p.num_tiles; tile += npairs, ++it) {
-            float mean[8], rstd[8], ss[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                mean[i] = 0.f;
-                rstd[i] = 1.f;
-                ss[i] = 0.f;
-            }
-            if (PRO == PRO_LN) {
-                RowMoments mo[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mo[i] = RowMoments{0.f, 0.f, 0.f};
-                for (int kb = 0; kb < nk; ++kb) {
-                    if (!wait_bar(afull_bar(s), ph, p.status, p.timeout_ns, 37)) {
-                        ok = false;
-                        break;
-                    }
-                    ln_stats_stage<DT>(stage_a(s), t, 8, kb * kBK + j * 8 < p.K, mo);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster(lead(xform_bar(s)));
-                    if (++s == S) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
-                }
-                if (!ok) break;
-                ln_stats_allreduce(mo, 8);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    mean[i] = mo[i].mean;
-                    rstd[i] = rsqrtf(mo[i].m2 / (float)p.K + p.eps);
-                }
-            }
-            for (int kb = 0; kb < nk; ++kb) {
-                if (!wait_bar(afull_bar(s), ph, p.status, p.timeout_ns, 38)) {
-                    ok = false;
-                    break;
-                }
-                if (PRO == PRO_RMS)
-                    fold_rms_stage<DT>(stage_a(s), gb_slot(s), t, 8, ss);
-                else
-                    fold_ln_stage<DT>(stage_a(s), gb_slot(s), p.beta != nullptr, t, 8, mean, rstd);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(lead(xform_bar(s)));
-                if (++s == S) {
-                    s = 0;
-                    ph ^= 1u;
-                }
-            }
-            if (!ok) break;
-            if (PRO == PRO_RMS) {
-                const int rb = it & 1;
-                const uint32_t tph = (uint32_t)(it & 1);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) ss[i] = row_allreduce8(ss[i]);
-                if (!wait_bar(tdone_bar, tph ^ 1u, p.status, p.timeout_ns, 39)) break;
-                if (j == 0) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) rowscale[rb * kBM + (t >> 3) + 16 * i] = rsqrtf(ss[i] / (float)p.K + p.eps);
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(sready_bar(rb));
-            }
         }
     } else if (PRO != PRO_NONE && warp >= 4 && warp < 8) {
         // ------------------------------------------------------------ fold into TMEM (both CTAs)
@@ -355,7 +300,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                 mean = mo.mean;
                 rstd = rsqrtf(mo.m2 / (float)p.K + p.eps);
             }
-            for (int kb = 0; kb < nk; ++kb) {
+            for (int kb = kb_begin; kb < kb_end; ++kb) {
                 if (!wait_bar(afull_bar(s), ph, p.status, p.timeout_ns, 38)) {
                     ok = false;
                     break;
@@ -383,11 +328,144 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                 const uint32_t tph = (uint32_t)(it & 1);
                 if (!wait_bar(tdone_bar, tph ^ 1u, p.status, p.timeout_ns, 39)) break;
                 const float sum = ((ss[0] + ss[1]) + (ss[2] + ss[3])) + ((ss[4] + ss[5]) + (ss[6] + ss[7]));
-                rowscale[rb * kBM + t] = rsqrtf(sum / (float)p.K + p.eps);
+                // split-K: the raw partial sum; the epilogue adds the K-partner's
+                rowscale[rb * kBM + t] = KS == 2 ? sum : rsqrtf(sum / (float)p.K + p.eps);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(sready_bar(rb));
             }
         }
+    } else if (KS == 2 && warp >= EPI_WARP0) {
+        // ------------------------------------------------------------ split-K epilogue
+        // Each CTA owns half of the tile's columns (its K half's index); it ships
+        // the other half of its fp32 partial to the K-partner (same rows, other
+        // K half) and adds the partner's share of its own half.
+        const int q = warp & 3;
+        const int rl = q * 32 + lane;  // tile row = TMEM lane
+        const uint32_t ebuf = sbase + C::OFF_EPI + q * C::EPI_BUF_BYTES;
+        const uint32_t my_row_addr = ebuf + lane * 128;
+        const int sw = lane & 7;
+        const uint32_t partner = crank ^ 2u;
+        constexpr int HALF_N = C::BN / 2;
+        const int tile = pair;
+        const int m0 = (tile % p.num_m_blocks) * 2 * kBM + (int)rank * kBM;
+        const int n0 = (tile / p.num_m_blocks) * C::BN;
+        const int own_c0 = khalf * HALF_N, oth_c0 = (1 - khalf) * HALF_N;
+        const uint32_t tl = tmem_base + ((uint32_t)(q * 32) << 16);
+        const uint32_t recv_row = sbase + (uint32_t)(rl * C::RECV_STRIDE) * 4u;
+        using T = uint16_t;
+        const T* bias = reinterpret_cast<const T*>(p.bias);
+        const T* res = reinterpret_cast<const T*>(p.residual);
+        bool ok = wait_bar(tfull_bar(0), 0, p.status, p.timeout_ns, 42);
+        tc_fence_after();
+        float ss_own = 0.f;
+        if (ok && PRO == PRO_RMS) {
+            ok = wait_bar(sready_bar(0), 0, p.status, p.timeout_ns, 43);
+            if (ok) ss_own = rowscale[rl];
+        }
+        // this pair's MMAs are done, so this CTA's ring may take the partner's half
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_cluster(ringfree_bar, partner));
+        if (ok) ok = wait_bar_cluster(ringfree_bar, 0, p.status, p.timeout_ns, 44);
+        if (ok) {
+            const uint32_t dst = mapa_cluster(recv_row, partner);
+#pragma unroll 1
+            for (int c = 0; c < HALF_N / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(tl + (uint32_t)(oth_c0 + 32 * c), v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    st_cluster_v4(dst + (uint32_t)(32 * c + 4 * j) * 4u, v[4 * j], v[4 * j + 1], v[4 * j + 2],
+                                  v[4 * j + 3]);
+            }
+            if (PRO == PRO_RMS) st_cluster_f32(mapa_cluster(sbase + C::OFF_RECV_SS + rl * 4, partner), ss_own);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive_release_cluster(mapa_cluster(recvd_bar, partner));
+        if (ok) ok = wait_bar_acquire_cluster(recvd_bar, 0, p.status, p.timeout_ns, 45);
+        if (ok) {
+            float rs = 1.f;
+            if (PRO == PRO_RMS) {
+                const float ss = ss_own + *reinterpret_cast<volatile float*>(smem + C::OFF_RECV_SS + rl * 4);
+                rs = rsqrtf(ss / (float)p.K + p.eps);
+            }
+            const int row = m0 + rl;
+            const bool row_ok = row < p.M;
+            if (m0 + q * 32 < p.M) {
+                for (int c = 0; c < HALF_N / 64; ++c) {
+                    const int col0 = n0 + own_c0 + c * 64;
+                    if (col0 >= p.N) break;
+                    if (lane == 0) bulk_wait_group_read<0>();
+                    __syncwarp();
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int cbase = col0 + h * 32;
+                        const int lc = c * 64 + h * 32;  // column within the own half
+                        uint32_t acc[32];
+                        tmem_ld_32x32b_x32(tl + (uint32_t)(own_c0 + lc), acc);
+                        tmem_ld_wait();
+                        float v[32];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const uint4 r4 = ld_shared_v4(recv_row + (uint32_t)(lc + 4 * j) * 4u);
+                            v[4 * j + 0] = (__uint_as_float(acc[4 * j + 0]) + __uint_as_float(r4.x)) * rs;
+                            v[4 * j + 1] = (__uint_as_float(acc[4 * j + 1]) + __uint_as_float(r4.y)) * rs;
+                            v[4 * j + 2] = (__uint_as_float(acc[4 * j + 2]) + __uint_as_float(r4.z)) * rs;
+                            v[4 * j + 3] = (__uint_as_float(acc[4 * j + 3]) + __uint_as_float(r4.w)) * rs;
+                        }
+                        if (bias != nullptr) {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                if (cbase + j * 8 < p.N) {
+                                    const uint4 bv = ldg_v4(bias + cbase + j * 8);
+                                    const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) {
+                                        const float2 b2 = Ops::unpack(bw[e]);
+                                        v[j * 8 + 2 * e] += b2.x;
+                                        v[j * 8 + 2 * e + 1] += b2.y;
+                                    }
+                                }
+                            }
+                        }
+                        if (p.act != ACT_NONE) {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) v[e] = act_apply(p.act, v[e]);
+                        }
+                        if (res != nullptr && row_ok) {
+                            const T* rrow = res + (size_t)row * p.N;
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                if (cbase + j * 8 < p.N) {
+                                    const uint4 rv = *reinterpret_cast<const uint4*>(rrow + cbase + j * 8);
+                                    const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) {
+                                        const float2 r2 = Ops::unpack(rw[e]);
+                                        v[j * 8 + 2 * e] += r2.x;
+                                        v[j * 8 + 2 * e + 1] += r2.y;
+                                    }
+                                }
+                            }
+                        }
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int chunk = h * 4 + j;
+                            st_shared_v4(my_row_addr + ((chunk ^ sw) << 4), Ops::pack(v[j * 8 + 0], v[j * 8 + 1]),
+                                         Ops::pack(v[j * 8 + 2], v[j * 8 + 3]), Ops::pack(v[j * 8 + 4], v[j * 8 + 5]),
+                                         Ops::pack(v[j * 8 + 6], v[j * 8 + 7]));
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&p.tmOut, ebuf, col0, m0 + q * 32);
+                        bulk_commit_group();
+                    }
+                }
+            }
+        }
+        if (lane == 0) bulk_wait_group<0>();
     } else if (warp >= EPI_WARP0) {
         // ------------------------------------------------------------ epilogue (both CTAs)
         const int q = warp & 3;
@@ -500,19 +578,19 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
 }
 
 // How many CTA pairs of this kernel can be resident at once.
-template <int DT, int BN, int PRO>
+template <int DT, int BN, int PRO, int KS>
 int pair_max_clusters() {
-    using C = PairCfg<BN, PRO, kPairFoldToTmem>;
-    auto kern = fl_pair_kernel<DT, BN, PRO>;
+    using C = PairCfg<BN, PRO, KS>;
+    auto kern = fl_pair_kernel<DT, BN, PRO, KS>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2, 1, 1);
+    cfg.gridDim = dim3(2 * KS, 1, 1);
     cfg.blockDim = dim3(PRO != PRO_NONE ? 384 : 256, 1, 1);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = 2 * KS;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -525,10 +603,10 @@ int pair_max_clusters() {
     return n;
 }
 
-template <int DT, int BN, int PRO>
+template <int DT, int BN, int PRO, int KS>
 cudaError_t launch_pair(const GemmParams& p, int grid, cudaStream_t stream) {
-    using C = PairCfg<BN, PRO, kPairFoldToTmem>;
-    auto kern = fl_pair_kernel<DT, BN, PRO>;
+    using C = PairCfg<BN, PRO, KS>;
+    auto kern = fl_pair_kernel<DT, BN, PRO, KS>;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
@@ -542,7 +620,7 @@ cudaError_t launch_pair(const GemmParams& p, int grid, cudaStream_t stream) {
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = 2 * KS;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -220,6 +220,25 @@ def test_pair_variant_all_patterns(dt, tile_n, shape):
 
 
 @pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("shape", [(256, 256, 512), (300, 520, 1000), (512, 1024, 520), (777, 264, 4096)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_pair_split_k_all_patterns(dt, shape):
+    """Two pairs per tile, one per K half, partials exchanged through distributed shared memory."""
+    M, N, K = shape
+    t = syn.dense_layer_inputs(M, N, K, dt)
+    fl.set_option("variant", 3)
+    fl.set_option("split_k", 2)
+    try:
+        for pattern in syn.PATTERNS:
+            got, ref = run_pattern(t, pattern)
+            assert_close(got, ref, dt, f"pair split-K {pattern} {dt} {M}x{N}x{K}")
+        fl.device_status()
+    finally:
+        fl.set_option("variant", 0)
+        fl.set_option("split_k", 0)
+
+
+@pytest.mark.parametrize("dt", DTYPES)
 def test_pair_norm_bias_act_residual_alias(dt):
     M, N, K = 777, 520, 776
     t = syn.norm_gemm_inputs(M, N, K, "layer", dt, with_bias=True)
