@@ -10,6 +10,19 @@
 
 namespace fl {
 
+// Phase timestamps (SM clock) for timing studies: compiled in with -DFL_TRACE
+// only; slot s of CTA b goes to trace[b * 16 + s].
+#ifdef FL_TRACE
+#define FL_MARK(p, slot)                                                                   \
+    do {                                                                                   \
+        if ((p).trace != nullptr) (p).trace[blockIdx.x * 16 + (slot)] = (unsigned long long)clock64(); \
+    } while (0)
+#else
+#define FL_MARK(p, slot) \
+    do {                 \
+    } while (0)
+#endif
+
 template <int DT>
 struct DTypeOps;
 

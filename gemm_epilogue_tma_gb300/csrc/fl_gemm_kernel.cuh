@@ -105,7 +105,16 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + C::OFF_SLOT);
     // Everything above overlaps the previous kernel on the stream; every
-    // global-memory access below waits for it.
+    // global-memory access below waits for it. The L2 prefetch of the first
+    // weight tiles may run early: L2 is the point of coherence, so it cannot
+    // return stale data.
+    if (warp == 0 && lane == 0 && blockIdx.x < p.num_tiles) {
+        const int n0 = (blockIdx.x / p.num_m_blocks) * BN;
+        for (int kb = 0; kb < S && kb < nk; ++kb) {
+            tma_prefetch_2d(&p.tmB, kb * kBK, n0);
+            if (DUAL) tma_prefetch_2d(&p.tmB2, kb * kBK, n0);
+        }
+    }
     griddep_wait();
     if (threadIdx.x == 0) griddep_launch_dependents();
 
@@ -469,7 +478,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar(buf));
         }
-        if (lane == 0) bulk_wait_group<0>();
+        if (lane == 0) bulk_wait_group_read<0>();  // global writes complete with the grid
     }
 
     __syncwarp();

@@ -12,6 +12,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <cstdlib>
 #include <mutex>
 
 #include "../../include/fusedlin.h"
@@ -347,6 +348,9 @@ fl_status run_pair(int dt, int pro, const void* A, const void* W, const void* bi
     p.pdl = g_opt_pdl.load();
     p.splits = plan.ks;
     p.kps = (p.num_k_blocks + plan.ks - 1) / plan.ks;
+#ifdef FL_TRACE
+    if (const char* tp = getenv("FL_TRACE_PTR")) p.trace = reinterpret_cast<unsigned long long*>(strtoull(tp, nullptr, 10));
+#endif
     cudaError_t e = dispatch_pair(dt, bn, pro, plan.ks, p, 2 * plan.ks * plan.clusters, stream);
     if (e != cudaSuccess) return fail(FL_ERR_CUDA, "pair kernel launch failed: %s", cudaGetErrorString(e));
     return ok();

@@ -45,6 +45,7 @@ struct GemmParams {
     int kps;       // split-K kernel: 64-wide K blocks per split
     int a_rows;    // split-K kernel: rows of the activation box (128, or M rounded up to 16)
     int pdl;       // launch with a programmatic dependency on the previous kernel of the stream
+    unsigned long long* trace;  // phase timestamps, builds with FL_TRACE only (else unused, null)
 };
 
 // Records a status message for fl_last_error() on this thread; returns status.

@@ -53,7 +53,13 @@ struct PairCfg {
     // padded against bank conflicts, written into this CTA's (idle) ring
     static constexpr int RECV_STRIDE = BN / 2 + 4;
     static constexpr int OFF_RECV_SS = kBM * RECV_STRIDE * 4;
-    static_assert(KS == 1 || OFF_RECV_SS + kBM * 4 <= STAGES * STAGE_BYTES, "exchange buffer fits in the ring");
+    static constexpr int XCHG_BYTES = OFF_RECV_SS + kBM * 4;  // partial half + row sums of squares
+    static constexpr int OFF_SEND = 96 * 1024;                 // outgoing copy, same layout
+    static_assert(KS == 1 || OFF_SEND + XCHG_BYTES <= STAGES * STAGE_BYTES, "exchange buffers fit in the ring");
+    static_assert(XCHG_BYTES <= OFF_SEND && XCHG_BYTES % 16 == 0, "exchange layout");
+    // second set of epilogue staging buffers (split-K: the ring is idle by then)
+    static constexpr int OFF_EPI2 = (XCHG_BYTES + 1023) / 1024 * 1024;
+    static_assert(KS == 1 || OFF_EPI2 + 4 * EPI_BUF_BYTES <= OFF_SEND, "second staging set fits in the ring");
     static constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_ROWSCALE = (OFF_SLOT + 16 + 15) / 16 * 16;
     static constexpr int OFF_GB = (OFF_ROWSCALE + 2 * kBM * 4 + 127) / 128 * 128;
@@ -66,6 +72,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     fl_pair_kernel(const __grid_constant__ GemmParams p) {
     using C = PairCfg<BN, PRO, KS>;
     static_assert(KS == 1 || (KS == 2 && BN == 256), "split-K pairs use 256-wide tiles");
+    if (threadIdx.x == 0) FL_MARK(p, 0);
     using Ops = DTypeOps<DT>;
     constexpr int S = C::STAGES;
     constexpr int EPI_WARP0 = PRO != PRO_NONE ? 8 : 4;
@@ -127,7 +134,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         mbar_init(drain_bar, 1);
         mbar_init(tdone_bar, 4);
         mbar_init(ringfree_bar, 4);
-        mbar_init(recvd_bar, 4);
+        mbar_init(recvd_bar, 1);
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -146,8 +153,15 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     cluster_barrier_sync();  // both CTAs' barriers exist before either signals the other
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + C::OFF_SLOT);
+    // L2 prefetch of this CTA's first weight tiles overlaps the previous kernel
+    // (L2 is the point of coherence); every other global access waits for it.
+    if (warp == 0 && lane == 0 && pair < p.num_tiles) {
+        const int nh = (pair / p.num_m_blocks) * C::BN + (int)rank * C::HALF;
+        for (int kb = kb_begin; kb < kb_begin + S && kb < kb_end; ++kb) tma_prefetch_2d(&p.tmB, kb * kBK, nh);
+    }
     griddep_wait();
     if (threadIdx.x == 0) griddep_launch_dependents();
+    if (threadIdx.x == 0) FL_MARK(p, 1);
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer (both CTAs)
@@ -187,6 +201,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                             if (leader) mbar_arrive_expect_tx(full_bar(s), 2u * C::B_BYTES);
                             tma_load_2d_pair(stage_b(s), &p.tmB, lead(full_bar(s)), kb * kBK, nh);
                         }
+                        if (issued == 0) FL_MARK(p, 2);
                         ++issued;
                         if (++s == S) {
                             s = 0;
@@ -245,6 +260,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                         break;
                     }
                     tc_fence_after();
+                    if (kb == kb_begin && it == 0) FL_MARK(p, 3);
                     const uint64_t da = sw128_kmajor_desc(stage_a(s));
                     const uint64_t db = sw128_kmajor_desc(stage_b(s));
 #pragma unroll
@@ -264,6 +280,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                 }
                 if (!ok) break;
                 umma_commit_pair(tfull_bar(buf), pair_mask);
+                FL_MARK(p, 4);
             }
             umma_commit_pair(drain_bar, (uint16_t)(1u << lead_rank));
             wait_bar_drain(drain_bar, 0, 20000000ull);
@@ -310,6 +327,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                     fold_rms_row<DT>(stage_a(s), gb_slot(s), t, ss, o);
                 else
                     fold_ln_row<DT>(stage_a(s), gb_slot(s), p.beta != nullptr, t, mean, rstd, o);
+                if (t == 0 && kb == kb_begin && it == 0) FL_MARK(p, 10);
                 tmem_st_32x32b_x32(tmem_base + a_lane + (uint32_t)C::A_COL0 + 32u * s, o);
                 tmem_st_wait();
                 tc_fence_before();
@@ -342,7 +360,6 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         const int q = warp & 3;
         const int rl = q * 32 + lane;  // tile row = TMEM lane
         const uint32_t ebuf = sbase + C::OFF_EPI + q * C::EPI_BUF_BYTES;
-        const uint32_t my_row_addr = ebuf + lane * 128;
         const int sw = lane & 7;
         const uint32_t partner = crank ^ 2u;
         constexpr int HALF_N = C::BN / 2;
@@ -357,6 +374,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         const T* res = reinterpret_cast<const T*>(p.residual);
         bool ok = wait_bar(tfull_bar(0), 0, p.status, p.timeout_ns, 42);
         tc_fence_after();
+        if (threadIdx.x == 32 * EPI_WARP0) FL_MARK(p, 5);
         float ss_own = 0.f;
         if (ok && PRO == PRO_RMS) {
             ok = wait_bar(sready_bar(0), 0, p.status, p.timeout_ns, 43);
@@ -365,9 +383,10 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         // this pair's MMAs are done, so this CTA's ring may take the partner's half
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(mapa_cluster(ringfree_bar, partner));
-        if (ok) ok = wait_bar_cluster(ringfree_bar, 0, p.status, p.timeout_ns, 44);
+        if (threadIdx.x == 32 * EPI_WARP0) mbar_arrive_expect_tx(recvd_bar, (uint32_t)C::XCHG_BYTES);
+        // stage the outgoing half (and the row's sum of squares) in this CTA's ring
         if (ok) {
-            const uint32_t dst = mapa_cluster(recv_row, partner);
+            const uint32_t src_row = sbase + C::OFF_SEND + (uint32_t)(rl * C::RECV_STRIDE) * 4u;
 #pragma unroll 1
             for (int c = 0; c < HALF_N / 32; ++c) {
                 uint32_t v[32];
@@ -375,14 +394,24 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                    st_cluster_v4(dst + (uint32_t)(32 * c + 4 * j) * 4u, v[4 * j], v[4 * j + 1], v[4 * j + 2],
-                                  v[4 * j + 3]);
+                    st_shared_v4(src_row + (uint32_t)(32 * c + 4 * j) * 4u, v[4 * j], v[4 * j + 1], v[4 * j + 2],
+                                 v[4 * j + 3]);
             }
-            if (PRO == PRO_RMS) st_cluster_f32(mapa_cluster(sbase + C::OFF_RECV_SS + rl * 4, partner), ss_own);
+            if (PRO == PRO_RMS)
+                *reinterpret_cast<volatile float*>(smem + C::OFF_SEND + C::OFF_RECV_SS + rl * 4) = ss_own;
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive_release_cluster(mapa_cluster(recvd_bar, partner));
-        if (ok) ok = wait_bar_acquire_cluster(recvd_bar, 0, p.status, p.timeout_ns, 45);
+        fence_proxy_async_smem();
+        named_bar_sync(2, 128);
+        if (ok && threadIdx.x == 32 * EPI_WARP0) {
+            // one bulk copy into the partner's receive buffer once its ring is free
+            if (wait_bar_cluster(ringfree_bar, 0, p.status, p.timeout_ns, 44)) {
+                bulk_copy_to_cluster(mapa_cluster(sbase, partner), sbase + C::OFF_SEND, (uint32_t)C::XCHG_BYTES,
+                                     mapa_cluster(recvd_bar, partner));
+            }
+        }
+        if (threadIdx.x == 32 * EPI_WARP0) FL_MARK(p, 6);
+        if (ok) ok = wait_bar(recvd_bar, 0, p.status, p.timeout_ns, 45);
+        if (threadIdx.x == 32 * EPI_WARP0) FL_MARK(p, 7);
         if (ok) {
             float rs = 1.f;
             if (PRO == PRO_RMS) {
@@ -395,8 +424,9 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                 for (int c = 0; c < HALF_N / 64; ++c) {
                     const int col0 = n0 + own_c0 + c * 64;
                     if (col0 >= p.N) break;
-                    if (lane == 0) bulk_wait_group_read<0>();
-                    __syncwarp();
+                    // the two 64-column chunks use two staging buffers
+                    const uint32_t sbuf = c == 0 ? ebuf : sbase + C::OFF_EPI2 + q * C::EPI_BUF_BYTES;
+                    const uint32_t srow = sbuf + lane * 128;
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int cbase = col0 + h * 32;
@@ -451,7 +481,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             const int chunk = h * 4 + j;
-                            st_shared_v4(my_row_addr + ((chunk ^ sw) << 4), Ops::pack(v[j * 8 + 0], v[j * 8 + 1]),
+                            st_shared_v4(srow + ((chunk ^ sw) << 4), Ops::pack(v[j * 8 + 0], v[j * 8 + 1]),
                                          Ops::pack(v[j * 8 + 2], v[j * 8 + 3]), Ops::pack(v[j * 8 + 4], v[j * 8 + 5]),
                                          Ops::pack(v[j * 8 + 6], v[j * 8 + 7]));
                         }
@@ -459,13 +489,13 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&p.tmOut, ebuf, col0, m0 + q * 32);
+                        tma_store_2d(&p.tmOut, sbuf, col0, m0 + q * 32);
                         bulk_commit_group();
                     }
                 }
             }
         }
-        if (lane == 0) bulk_wait_group<0>();
+        if (lane == 0) bulk_wait_group_read<0>();  // global writes complete with the grid
     } else if (warp >= EPI_WARP0) {
         // ------------------------------------------------------------ epilogue (both CTAs)
         const int q = warp & 3;
@@ -564,13 +594,15 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                 mbar_arrive(tdone_bar);
             }
         }
-        if (lane == 0) bulk_wait_group<0>();
+        if (lane == 0) bulk_wait_group_read<0>();  // global writes complete with the grid
     }
 
     __syncwarp();
     tc_fence_before();
     __syncthreads();
+    if (threadIdx.x == 0) FL_MARK(p, 8);
     cluster_barrier_sync();  // neither CTA's barriers or TMEM go away while the other may use them
+    if (threadIdx.x == 0) FL_MARK(p, 9);
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc_pair(tmem_base, C::TMEM_COLS);

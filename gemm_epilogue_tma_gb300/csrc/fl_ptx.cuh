@@ -109,6 +109,13 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// L2 prefetch of a 2-D box (no shared-memory destination, no completion).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* m, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(m)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 // Shared -> global; out-of-range elements of the box are not written.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src, int32_t x,
                                              int32_t y) {
@@ -337,6 +344,16 @@ __device__ __forceinline__ uint32_t mbar_try_wait_acquire_cluster(uint32_t bar, 
         : "r"(bar), "r"(parity)
         : "memory");
     return done;
+}
+
+// Bulk copy from this CTA's shared memory into another CTA's (dst and bar are
+// shared::cluster addresses in the destination CTA); completion is counted in
+// bytes on the destination's barrier.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "r"(src), "r"(bytes), "r"(bar)
+        : "memory");
 }
 
 // Stores into another CTA's shared memory (shared::cluster address).

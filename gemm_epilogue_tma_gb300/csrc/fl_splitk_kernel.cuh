@@ -131,7 +131,11 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + C::OFF_SLOT);
     // Everything above overlaps the previous kernel on the stream; every
-    // global-memory access below waits for it.
+    // global-memory access below waits for it, except the L2 prefetch of this
+    // CTA's first weight tiles (L2 is the point of coherence).
+    if (warp == 0 && lane == 0) {
+        for (int kb = kb0; kb < kb0 + S && kb < kb1; ++kb) tma_prefetch_2d(&p.tmB, kb * kBK, n0);
+    }
     griddep_wait();
     if (threadIdx.x == 0) griddep_launch_dependents();
 
