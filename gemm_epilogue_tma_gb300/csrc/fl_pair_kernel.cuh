@@ -115,9 +115,21 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     const int khalf = KS == 2 ? (int)(crank >> 1) : 0;
     const int kb_begin = KS == 2 ? khalf * p.kps : 0;
     const int kb_end = KS == 2 ? min(nk, kb_begin + p.kps) : nk;
-    // KS = 1: persistent pairs stride over the tiles; KS = 2: one tile per cluster
+    // KS = 1: each persistent pair takes a contiguous range of tiles in
+    // row-block-major order, so consecutive tiles mostly share their activation
+    // rows (LayerNorm statistics are then computed once per row block);
+    // KS = 2: one tile per cluster.
     const int npairs = KS == 2 ? p.num_tiles : (int)gridDim.x / 2;
     const int pair = KS == 2 ? (int)blockIdx.x / 4 : (int)blockIdx.x / 2;
+    int t_begin = pair, t_end = pair + 1;
+    if (KS == 1) {
+        const int base = p.num_tiles / npairs, extra = p.num_tiles % npairs;
+        t_begin = pair * base + min(pair, extra);
+        t_end = t_begin + base + (pair < extra ? 1 : 0);
+    }
+    auto tile_mb = [&](int t) { return t / p.num_n_blocks; };
+    auto tile_nb = [&](int t) { return t % p.num_n_blocks; };
+    auto needs_stats = [&](int t) { return PRO == PRO_LN && (t == t_begin || tile_mb(t) != tile_mb(t - 1)); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -155,8 +167,8 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + C::OFF_SLOT);
     // L2 prefetch of this CTA's first weight tiles overlaps the previous kernel
     // (L2 is the point of coherence); every other global access waits for it.
-    if (warp == 0 && lane == 0 && pair < p.num_tiles) {
-        const int nh = (pair / p.num_m_blocks) * C::BN + (int)rank * C::HALF;
+    if (warp == 0 && lane == 0 && t_begin < t_end) {
+        const int nh = tile_nb(t_begin) * C::BN + (int)rank * C::HALF;
         for (int kb = kb_begin; kb < kb_begin + S && kb < kb_end; ++kb) tma_prefetch_2d(&p.tmB, kb * kBK, nh);
     }
     griddep_wait();
@@ -171,12 +183,12 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
             int issued = 0;
             bool ok = true;
             const uint32_t gb_bytes = PRO != PRO_NONE ? 128u + (PRO == PRO_LN && p.beta != nullptr ? 128u : 0u) : 0u;
-            for (int tile = pair; ok && tile < p.num_tiles; tile += npairs) {
-                const int m0 = (tile % p.num_m_blocks) * 2 * kBM + (int)rank * kBM;
-                const int nh = (tile / p.num_m_blocks) * C::BN + (int)rank * C::HALF;
-                const int passes = PRO == PRO_LN ? 2 : 1;
+            for (int tile = t_begin; ok && tile < t_end; ++tile) {
+                const int m0 = tile_mb(tile) * 2 * kBM + (int)rank * kBM;
+                const int nh = tile_nb(tile) * C::BN + (int)rank * C::HALF;
+                const int passes = needs_stats(tile) ? 2 : 1;
                 for (int pass = 0; ok && pass < passes; ++pass) {
-                    const bool stats = PRO == PRO_LN && pass == 0;
+                    const bool stats = passes == 2 && pass == 0;
                     const int k0 = stats ? 0 : kb_begin, k1 = stats ? nk : kb_end;
                     for (int kb = k0; kb < k1; ++kb) {
                         if (!wait_bar(empty_bar(s), ph ^ 1u, p.status, p.timeout_ns, 31)) {
@@ -227,10 +239,10 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
             uint32_t ph = 0;
             int it = 0;
             bool ok = true;
-            for (int tile = pair; ok && tile < p.num_tiles; tile += npairs, ++it) {
+            for (int tile = t_begin; ok && tile < t_end; ++tile, ++it) {
                 const int buf = C::NBUF == 2 ? (it & 1) : 0;
                 const uint32_t tph = C::NBUF == 2 ? (uint32_t)((it >> 1) & 1) : (uint32_t)(it & 1);
-                if (PRO == PRO_LN) {
+                if (needs_stats(tile)) {
                     // statistics pass: both CTAs' fold warps read these stages; release them in both
                     for (int kb = 0; kb < nk; ++kb) {
                         if (!wait_bar_cluster(xform_bar(s), ph, p.status, p.timeout_ns, 32) ||
@@ -293,12 +305,12 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         uint32_t ph = 0;
         int it = 0;
         bool ok = true;
-        for (int tile = pair; ok && tile < p.num_tiles; tile += npairs, ++it) {
-            float mean = 0.f, rstd = 1.f;
+        float mean = 0.f, rstd = 1.f;  // LayerNorm statistics of the current row block
+        for (int tile = t_begin; ok && tile < t_end; ++tile, ++it) {
             float ss[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) ss[i] = 0.f;
-            if (PRO == PRO_LN) {
+            if (needs_stats(tile)) {
                 RowMoments mo{0.f, 0.f, 0.f};
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!wait_bar(afull_bar(s), ph, p.status, p.timeout_ns, 37)) {
@@ -364,8 +376,8 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         const uint32_t partner = crank ^ 2u;
         constexpr int HALF_N = C::BN / 2;
         const int tile = pair;
-        const int m0 = (tile % p.num_m_blocks) * 2 * kBM + (int)rank * kBM;
-        const int n0 = (tile / p.num_m_blocks) * C::BN;
+        const int m0 = tile_mb(tile) * 2 * kBM + (int)rank * kBM;
+        const int n0 = tile_nb(tile) * C::BN;
         const int own_c0 = khalf * HALF_N, oth_c0 = (1 - khalf) * HALF_N;
         const uint32_t tl = tmem_base + ((uint32_t)(q * 32) << 16);
         const uint32_t recv_row = sbase + (uint32_t)(rl * C::RECV_STRIDE) * 4u;
@@ -506,9 +518,9 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         using T = uint16_t;
         const T* bias = reinterpret_cast<const T*>(p.bias);
         const T* res = reinterpret_cast<const T*>(p.residual);
-        for (int tile = pair; tile < p.num_tiles; tile += npairs, ++it) {
-            const int m0 = (tile % p.num_m_blocks) * 2 * kBM + (int)rank * kBM;
-            const int n0 = (tile / p.num_m_blocks) * C::BN;
+        for (int tile = t_begin; tile < t_end; ++tile, ++it) {
+            const int m0 = tile_mb(tile) * 2 * kBM + (int)rank * kBM;
+            const int n0 = tile_nb(tile) * C::BN;
             const int buf = C::NBUF == 2 ? (it & 1) : 0;
             const uint32_t tph = C::NBUF == 2 ? (uint32_t)((it >> 1) & 1) : (uint32_t)(it & 1);
             if (!wait_bar(tfull_bar(buf), tph, p.status, p.timeout_ns, 40)) break;
