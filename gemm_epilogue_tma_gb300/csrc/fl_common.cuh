@@ -131,14 +131,22 @@ static __device__ __noinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity
     return true;
 }
 
+// v / (1 + e^-z): the logistic factor of SiLU (z = v) and of the tanh GeLU
+// (0.5 v (1 + tanh u) = v / (1 + e^(-2u))). The exponent is clamped at 80 so
+// the divisor stays finite (the quotient is then ~v e^-80, i.e. 0 to output
+// precision), which keeps the fast divide in its exact range.
+__device__ __forceinline__ float logistic_mul(float v, float z) {
+    return __fdividef(v, 1.0f + __expf(fminf(-z, 80.0f)));
+}
+
 __device__ __forceinline__ float act_apply(int act, float v) {
     switch (act) {
         case ACT_GELU: {
-            const float c = 0.7978845608028654f;  // sqrt(2 / pi)
-            return 0.5f * v * (1.0f + tanhf(c * (v + 0.044715f * v * v * v)));
+            const float c2 = 1.5957691216057308f;  // 2 sqrt(2 / pi)
+            return logistic_mul(v, c2 * fmaf(0.044715f * v, v * v, v));
         }
         case ACT_SILU:
-            return v / (1.0f + __expf(-v));
+            return logistic_mul(v, v);
         case ACT_RELU:
             return fmaxf(v, 0.0f);
         default:

@@ -416,7 +416,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                             for (int e = 0; e < 32; ++e) {
                                 const float gt = __uint_as_float(acc[e]) * rs;
                                 const float u = __uint_as_float(up[e]) * rs;
-                                v[e] = gt / (1.0f + __expf(-gt)) * u;
+                                v[e] = logistic_mul(gt, gt) * u;
                             }
                         } else {
                             tmem_ld_wait();

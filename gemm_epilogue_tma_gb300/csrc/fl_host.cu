@@ -405,6 +405,9 @@ fl_status run_splitk(int dt, int pro, const void* A, const void* W, const void* 
     p.kps = plan.kps;
     p.a_rows = a_rows;
     p.pdl = g_opt_pdl.load();
+#ifdef FL_TRACE
+    if (const char* tp = getenv("FL_TRACE_PTR")) p.trace = reinterpret_cast<unsigned long long*>(strtoull(tp, nullptr, 10));
+#endif
     const int grid = p.num_tiles * plan.splits;
     cudaError_t e = dispatch_splitk(dt, plan.bn, pro, p, grid, plan.splits, stream);
     if (e != cudaSuccess) return fail(FL_ERR_CUDA, "split-K kernel launch failed: %s", cudaGetErrorString(e));

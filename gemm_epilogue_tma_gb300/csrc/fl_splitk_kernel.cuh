@@ -66,6 +66,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 template <int DT, int BN, int PRO>
 __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     fl_splitk_kernel(const __grid_constant__ GemmParams p) {
+    if (threadIdx.x == 0) FL_MARK(p, 0);
     using C = SplitCfg<BN>;
     using Ops = DTypeOps<DT>;
     constexpr int S = C::STAGES;
@@ -138,6 +139,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     }
     griddep_wait();
     if (threadIdx.x == 0) griddep_launch_dependents();
+    if (threadIdx.x == 0) FL_MARK(p, 1);
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -157,6 +159,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                     if (PRO == PRO_LN && p.beta != nullptr)
                         tma_load_2d(gb_slot(s) + 128, &p.tmBeta, full_bar(s), kb * kBK, 0);
                 }
+                if (issued == 0) FL_MARK(p, 2);
                 ++issued;
                 if (++s == S) {
                     s = 0;
@@ -182,6 +185,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                     break;
                 }
                 tc_fence_after();
+                if (kb == kb0) FL_MARK(p, 3);
                 const uint64_t da = sw128_kmajor_desc(stage_a(s));
                 const uint64_t db = sw128_kmajor_desc(stage_b(s));
 #pragma unroll
@@ -194,6 +198,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                 }
             }
             if (ok) umma_commit(tfull_bar);
+            FL_MARK(p, 4);
             umma_commit(drain_bar);
             wait_bar_drain(drain_bar, 0, 20000000ull);
         }
@@ -275,6 +280,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         const int r = q * 32 + lane;
         if (wait_bar(tfull_bar, 0, p.status, p.timeout_ns, 24)) {
             tc_fence_after();
+            if (threadIdx.x == 32 * EPI_WARP0) FL_MARK(p, 5);
             if (q * 32 < rows) {
                 const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16);
                 const uint32_t dst = red_base + (uint32_t)(r * C::RED_STRIDE) * 4u;
@@ -296,8 +302,10 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     __syncwarp();
     tc_fence_before();
     __syncthreads();
+    if (threadIdx.x == 0) FL_MARK(p, 6);
     // partials of every CTA of the cluster are written and visible after this
     cluster_sync_all();
+    if (threadIdx.x == 0) FL_MARK(p, 7);
 
     // ---------------------------------------------------------------- reduction + epilogue
     {
@@ -358,8 +366,11 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                                                              Ops::pack(v[4], v[5]), Ops::pack(v[6], v[7]));
         }
     }
+    __syncthreads();
+    if (threadIdx.x == 0) FL_MARK(p, 8);
     // no CTA leaves while a peer may still read its shared memory
     cluster_sync_all();
+    if (threadIdx.x == 0) FL_MARK(p, 9);
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, C::TMEM_COLS);
