@@ -74,34 +74,15 @@ __device__ __forceinline__ void fold_rms_stage(uint32_t stage, uint32_t gamma_sl
         }
 }
 
-// LayerNorm statistics: merge this thread's chunk of the K block into the
-// running moments of its rows. `valid` says whether the chunk lies inside K
-// (out-of-range chunks are zero-filled and must not count).
+// LayerNorm statistics, chunk-parallel: this thread's chunk of each of its
+// rows is added to per-row shifted sums (see ShiftedSums below); `valid` says
+// whether the chunk lies inside K (zero-filled chunks must not count).
+struct ShiftedSums;
 template <int DT>
-__device__ __forceinline__ void ln_stats_stage(uint32_t stage, int t, int ni, bool valid, RowMoments (&mo)[8]) {
-    using Ops = DTypeOps<DT>;
-    if (!valid) return;
-    const int j = t & 7;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        if (i < ni) {
-            const uint4 v = ld_shared_v4(fold_row_addr(stage, (t >> 3) + 16 * i, j));
-            const float2 a = Ops::unpack(v.x), b = Ops::unpack(v.y), c = Ops::unpack(v.z), d = Ops::unpack(v.w);
-            const float cm = (((a.x + a.y) + (b.x + b.y)) + ((c.x + c.y) + (d.x + d.y))) * 0.125f;
-            float q0 = (a.x - cm) * (a.x - cm), q1 = (a.y - cm) * (a.y - cm);
-            q0 = fmaf(b.x - cm, b.x - cm, q0);
-            q1 = fmaf(b.y - cm, b.y - cm, q1);
-            q0 = fmaf(c.x - cm, c.x - cm, q0);
-            q1 = fmaf(c.y - cm, c.y - cm, q1);
-            q0 = fmaf(d.x - cm, d.x - cm, q0);
-            q1 = fmaf(d.y - cm, d.y - cm, q1);
-            mo[i] = merge_moments(mo[i], RowMoments{8.f, cm, q0 + q1});
-        }
-    }
-}
+__device__ __forceinline__ void ln_sums_stage(uint32_t stage, int t, int ni, bool valid, ShiftedSums (&st)[8]);
 
-// Merge the moments of the 8 lanes that share each row; every lane ends with
-// the row's full moments.
+// Moments of the 8 lanes that share each row, merged (Chan et al.) in a fixed
+// order so every lane ends with the same full-row moments.
 __device__ __forceinline__ void ln_stats_allreduce(RowMoments (&mo)[8], int ni) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -112,7 +93,6 @@ __device__ __forceinline__ void ln_stats_allreduce(RowMoments (&mo)[8], int ni) 
                 other.n = __shfl_xor_sync(0xffffffffu, mo[i].n, o);
                 other.mean = __shfl_xor_sync(0xffffffffu, mo[i].mean, o);
                 other.m2 = __shfl_xor_sync(0xffffffffu, mo[i].m2, o);
-                // merge in a fixed order (lower lane first) so both partners agree bit for bit
                 mo[i] = (threadIdx.x & o) ? merge_moments(other, mo[i]) : merge_moments(mo[i], other);
             }
         }
@@ -190,9 +170,17 @@ __device__ __forceinline__ void fold_rms_row(uint32_t stage, uint32_t gamma_slic
     }
 }
 
-// LayerNorm moments of one row's K block (nvalid chunks of 8 lie inside K).
+// LayerNorm moments of one row by shifted sums: with a shift c near the row
+// mean (the mean of the row's first 8 elements), accumulate n, S1 = sum(x - c)
+// and S2 = sum((x - c)^2) in fp32; then mean = c + S1 / n and
+// m2 = S2 - S1^2 / n, whose subtraction loses only about log2(1 + (mean-c)^2 /
+// var) bits. One pass per K block, no division per block.
+struct ShiftedSums {
+    float c, s1, s2, n;
+};
+
 template <int DT>
-__device__ __forceinline__ void ln_stats_row(uint32_t stage, int t, int nvalid, RowMoments& mo) {
+__device__ __forceinline__ void ln_sums_row(uint32_t stage, int t, int nvalid, ShiftedSums& st) {
     using Ops = DTypeOps<DT>;
     if (nvalid <= 0) return;
     const int sw = t & 7;
@@ -204,25 +192,50 @@ __device__ __forceinline__ void ln_stats_row(uint32_t stage, int t, int nvalid, 
         v[8 * j + 0] = a.x; v[8 * j + 1] = a.y; v[8 * j + 2] = b.x; v[8 * j + 3] = b.y;
         v[8 * j + 4] = c.x; v[8 * j + 5] = c.y; v[8 * j + 6] = d.x; v[8 * j + 7] = d.y;
     }
-    // out-of-range chunks are zero-filled: they add nothing to the sum
-    float part[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-        part[j] = ((v[8 * j] + v[8 * j + 1]) + (v[8 * j + 2] + v[8 * j + 3])) +
-                  ((v[8 * j + 4] + v[8 * j + 5]) + (v[8 * j + 6] + v[8 * j + 7]));
-    const float cnt = 8.f * (float)nvalid;
-    const float cm = (((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]))) / cnt;
+    if (st.n == 0.f)
+        st.c = (((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]))) * 0.125f;
+    float a1[4] = {0.f, 0.f, 0.f, 0.f}, a2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        float q = 0.f;
         if (j < nvalid) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) q = fmaf(v[8 * j + e] - cm, v[8 * j + e] - cm, q);
+            for (int e = 0; e < 8; ++e) {
+                const float dlt = v[8 * j + e] - st.c;
+                a1[e & 3] += dlt;
+                a2[e & 3] = fmaf(dlt, dlt, a2[e & 3]);
+            }
         }
-        part[j] = q;
     }
-    const float m2 = ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
-    mo = merge_moments(mo, RowMoments{cnt, cm, m2});
+    st.s1 += (a1[0] + a1[1]) + (a1[2] + a1[3]);
+    st.s2 += (a2[0] + a2[1]) + (a2[2] + a2[3]);
+    st.n += 8.f * (float)nvalid;
+}
+
+__device__ __forceinline__ RowMoments ln_sums_moments(const ShiftedSums& st) {
+    if (st.n == 0.f) return RowMoments{0.f, 0.f, 0.f};
+    const float d = st.s1 / st.n;
+    return RowMoments{st.n, st.c + d, fmaxf(st.s2 - st.s1 * d, 0.f)};
+}
+
+template <int DT>
+__device__ __forceinline__ void ln_sums_stage(uint32_t stage, int t, int ni, bool valid, ShiftedSums (&st)[8]) {
+    using Ops = DTypeOps<DT>;
+    if (!valid) return;
+    const int j = t & 7;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        if (i < ni) {
+            const uint4 x = ld_shared_v4(fold_row_addr(stage, (t >> 3) + 16 * i, j));
+            const float2 a = Ops::unpack(x.x), b = Ops::unpack(x.y), c = Ops::unpack(x.z), d = Ops::unpack(x.w);
+            if (st[i].n == 0.f) st[i].c = (((a.x + a.y) + (b.x + b.y)) + ((c.x + c.y) + (d.x + d.y))) * 0.125f;
+            const float cc = st[i].c;
+            const float e0 = a.x - cc, e1 = a.y - cc, e2 = b.x - cc, e3 = b.y - cc;
+            const float e4 = c.x - cc, e5 = c.y - cc, e6 = d.x - cc, e7 = d.y - cc;
+            st[i].s1 += ((e0 + e1) + (e2 + e3)) + ((e4 + e5) + (e6 + e7));
+            st[i].s2 += ((e0 * e0 + e1 * e1) + (e2 * e2 + e3 * e3)) + ((e4 * e4 + e5 * e5) + (e6 * e6 + e7 * e7));
+            st[i].n += 8.f;
+        }
+    }
 }
 
 template <int DT>

@@ -242,13 +242,13 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
 #pragma unroll
             for (int i = 0; i < 8; ++i) ss[i] = 0.f;
             if (PRO == PRO_LN) {
-                RowMoments mo{0.f, 0.f, 0.f};
+                ShiftedSums sums{0.f, 0.f, 0.f, 0.f};
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!wait_bar(full_bar(s), ph, p.status, p.timeout_ns, 5)) {
                         ok = false;
                         break;
                     }
-                    ln_stats_row<DT>(stage_a(s), t, min(8, (p.K - kb * kBK) / 8), mo);
+                    ln_sums_row<DT>(stage_a(s), t, min(8, (p.K - kb * kBK) / 8), sums);
                     __syncwarp();
                     if (lane == 0) mbar_arrive(xform_bar(s));
                     if (++s == S) {
@@ -257,6 +257,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                     }
                 }
                 if (!ok) break;
+                const RowMoments mo = ln_sums_moments(sums);
                 mean = mo.mean;
                 rstd = rsqrtf(mo.m2 / (float)p.K + p.eps);
             }
@@ -309,15 +310,15 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
             }
             if (PRO == PRO_LN) {
                 // statistics pass over the row block (Chan merges, no cancellation)
-                RowMoments mo[8];
+                ShiftedSums sums[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) mo[i] = RowMoments{0.f, 0.f, 0.f};
+                for (int i = 0; i < 8; ++i) sums[i] = ShiftedSums{0.f, 0.f, 0.f, 0.f};
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!wait_bar(full_bar(s), ph, p.status, p.timeout_ns, 5)) {
                         ok = false;
                         break;
                     }
-                    ln_stats_stage<DT>(stage_a(s), t, 8, kb * kBK + j * 8 < p.K, mo);
+                    ln_sums_stage<DT>(stage_a(s), t, 8, kb * kBK + j * 8 < p.K, sums);
                     __syncwarp();
                     if (lane == 0) mbar_arrive(xform_bar(s));
                     if (++s == S) {
@@ -326,6 +327,9 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                     }
                 }
                 if (!ok) break;
+                RowMoments mo[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mo[i] = ln_sums_moments(sums[i]);
                 ln_stats_allreduce(mo, 8);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {

@@ -48,7 +48,7 @@ struct PairCfg {
     static constexpr int EPI_BUF_BYTES = 32 * 128;
     static constexpr int OFF_EPI = STAGES * STAGE_BYTES;
     static constexpr int OFF_BAR = OFF_EPI + 4 * EPI_BUF_BYTES;
-    static constexpr int NUM_BARS = 4 * STAGES + 10;
+    static constexpr int NUM_BARS = 4 * STAGES + 11;
     // split-K exchange: the K-partner's half of the partial tile, fp32 rows
     // padded against bank conflicts, written into this CTA's (idle) ring
     static constexpr int RECV_STRIDE = BN / 2 + 4;
@@ -63,7 +63,9 @@ struct PairCfg {
     static constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_ROWSCALE = (OFF_SLOT + 16 + 15) / 16 * 16;
     static constexpr int OFF_GB = (OFF_ROWSCALE + 2 * kBM * 4 + 127) / 128 * 128;
-    static constexpr int SMEM_BYTES = OFF_GB + STAGES * 256 + 1024;
+    // split-K LayerNorm: row moments (n, mean, m2) sent by the K-partner
+    static constexpr int OFF_LNX = OFF_GB + STAGES * 256;
+    static constexpr int SMEM_BYTES = OFF_LNX + kBM * 12 + 1024;
     static_assert(!ATMEM || A_COL0 + 32 * STAGES <= TMEM_COLS, "activation slots must fit in tensor memory");
 };
 
@@ -97,6 +99,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     const uint32_t tdone_bar = bar0 + 8u * (4 * S + 7);  // this CTA's epilogue finished a tile
     const uint32_t ringfree_bar = bar0 + 8u * (4 * S + 8);  // split-K: the K-partner may write my ring
     const uint32_t recvd_bar = bar0 + 8u * (4 * S + 9);     // split-K: the K-partner's half has arrived
+    const uint32_t lnx_bar = bar0 + 8u * (4 * S + 10);      // split-K LayerNorm: partner's row moments arrived
     const uint32_t slot_addr = sbase + C::OFF_SLOT;
     float* rowscale = reinterpret_cast<float*>(smem + C::OFF_ROWSCALE);
     auto gb_slot = [&](int s) { return sbase + C::OFF_GB + 256u * s; };
@@ -147,6 +150,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         mbar_init(tdone_bar, 4);
         mbar_init(ringfree_bar, 4);
         mbar_init(recvd_bar, 1);
+        mbar_init(lnx_bar, 4);
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -189,7 +193,9 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                 const int passes = needs_stats(tile) ? 2 : 1;
                 for (int pass = 0; ok && pass < passes; ++pass) {
                     const bool stats = passes == 2 && pass == 0;
-                    const int k0 = stats ? 0 : kb_begin, k1 = stats ? nk : kb_end;
+                    // statistics cover the whole row, or this pair's K half when the
+                    // K-partner supplies the other half's moments
+                    const int k0 = (stats && KS == 1) ? 0 : kb_begin, k1 = (stats && KS == 1) ? nk : kb_end;
                     for (int kb = k0; kb < k1; ++kb) {
                         if (!wait_bar(empty_bar(s), ph ^ 1u, p.status, p.timeout_ns, 31)) {
                             ok = false;
@@ -244,7 +250,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                 const uint32_t tph = C::NBUF == 2 ? (uint32_t)((it >> 1) & 1) : (uint32_t)(it & 1);
                 if (needs_stats(tile)) {
                     // statistics pass: both CTAs' fold warps read these stages; release them in both
-                    for (int kb = 0; kb < nk; ++kb) {
+                    for (int kb = KS == 1 ? 0 : kb_begin; kb < (KS == 1 ? nk : kb_end); ++kb) {
                         if (!wait_bar_cluster(xform_bar(s), ph, p.status, p.timeout_ns, 32) ||
                             !wait_bar(full_bar(s), ph, p.status, p.timeout_ns, 33)) {
                             ok = false;
@@ -311,13 +317,15 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
 #pragma unroll
             for (int i = 0; i < 8; ++i) ss[i] = 0.f;
             if (needs_stats(tile)) {
-                RowMoments mo{0.f, 0.f, 0.f};
-                for (int kb = 0; kb < nk; ++kb) {
+                // row t's moments by shifted sums (one pass, no division per K block)
+                ShiftedSums sums{0.f, 0.f, 0.f, 0.f};
+                const int sk0 = KS == 1 ? 0 : kb_begin, sk1 = KS == 1 ? nk : kb_end;
+                for (int kb = sk0; kb < sk1; ++kb) {
                     if (!wait_bar(afull_bar(s), ph, p.status, p.timeout_ns, 37)) {
                         ok = false;
                         break;
                     }
-                    ln_stats_row<DT>(stage_a(s), t, min(8, (p.K - kb * kBK) / 8), mo);
+                    ln_sums_row<DT>(stage_a(s), t, min(8, (p.K - kb * kBK) / 8), sums);
                     __syncwarp();
                     if (lane == 0) mbar_arrive_cluster(lead(xform_bar(s)));
                     if (++s == S) {
@@ -326,8 +334,28 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                     }
                 }
                 if (!ok) break;
+                RowMoments mo = ln_sums_moments(sums);
+                if (KS == 2) {
+                    // send this K half's moments to the K-partner, merge with its half
+                    float* lnx = reinterpret_cast<float*>(smem + C::OFF_LNX);
+                    const uint32_t partner = crank ^ 2u;
+                    const uint32_t a = mapa_cluster(smem_u32(lnx + t * 3), partner);
+                    st_cluster_f32(a, mo.n);
+                    st_cluster_f32(a + 4, mo.mean);
+                    st_cluster_f32(a + 8, mo.m2);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_release_cluster(mapa_cluster(lnx_bar, partner));
+                    if (!wait_bar_acquire_cluster(lnx_bar, 0, p.status, p.timeout_ns, 46)) {
+                        ok = false;
+                        break;
+                    }
+                    const RowMoments other{lnx[t * 3], lnx[t * 3 + 1], lnx[t * 3 + 2]};
+                    // the lower K half first, so both pairs get the same bits
+                    mo = khalf == 0 ? merge_moments(mo, other) : merge_moments(other, mo);
+                }
                 mean = mo.mean;
                 rstd = rsqrtf(mo.m2 / (float)p.K + p.eps);
+                if (t == 0 && it == 0) FL_MARK(p, 11);
             }
             for (int kb = kb_begin; kb < kb_end; ++kb) {
                 if (!wait_bar(afull_bar(s), ph, p.status, p.timeout_ns, 38)) {
