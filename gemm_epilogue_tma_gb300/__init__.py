@@ -26,7 +26,7 @@ ACTS = {"none": 0, "gelu": 1, "silu": 2, "relu": 3}
 DTYPE_CODES = {"f16": 0, "bf16": 1}
 STATUS_NAMES = {0: "FL_OK", 1: "FL_ERR_INVALID_ARG", 2: "FL_ERR_UNSUPPORTED", 3: "FL_ERR_ALIGNMENT",
                 4: "FL_ERR_WORKSPACE", 5: "FL_ERR_CUDA", 6: "FL_ERR_TIMEOUT"}
-OPTIONS = {"tile_n": 0, "variant": 1, "timeout_ms": 2, "split_k": 3, "pdl": 4}
+OPTIONS = {"tile_n": 0, "variant": 1, "timeout_ms": 2, "split_k": 3, "pdl": 4, "weight_preload": 5}
 
 # C ABI: name -> (restype, argtypes)
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t

@@ -10,12 +10,18 @@
 
 namespace fl {
 
-// Phase timestamps (SM clock) for timing studies: compiled in with -DFL_TRACE
-// only; slot s of CTA b goes to trace[b * 16 + s].
+// Phase timestamps for timing studies: compiled in with -DFL_TRACE only;
+// slot s of CTA b goes to trace[b * 16 + s]. SM clock cycles, or global
+// nanoseconds (comparable across SMs and launches) with -DFL_TRACE_GLOBALTIMER.
 #ifdef FL_TRACE
+#ifdef FL_TRACE_GLOBALTIMER
+#define FL_TRACE_NOW() globaltimer_ns()
+#else
+#define FL_TRACE_NOW() clock64()
+#endif
 #define FL_MARK(p, slot)                                                                   \
     do {                                                                                   \
-        if ((p).trace != nullptr) (p).trace[blockIdx.x * 16 + (slot)] = (unsigned long long)clock64(); \
+        if ((p).trace != nullptr) (p).trace[blockIdx.x * 16 + (slot)] = (unsigned long long)FL_TRACE_NOW(); \
     } while (0)
 #else
 #define FL_MARK(p, slot) \
@@ -161,6 +167,16 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
                  : "r"(addr)
                  : "memory");
     return v;
+}
+
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,

@@ -45,6 +45,7 @@ std::atomic<int> g_opt_variant{0};
 std::atomic<int> g_opt_timeout_ms{2000};
 std::atomic<int> g_opt_split_k{0};
 std::atomic<int> g_opt_pdl{1};
+std::atomic<int> g_opt_preload{0};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -182,22 +183,46 @@ cudaError_t dispatch_splitk(int dt, int bn, int pro, const GemmParams& p, int gr
 // weight tiles, and as many K splits (one cluster, at most 8) as keep every
 // SM streaming weights. Returns false when the tile kernel is the better fit.
 struct SplitPlan {
-    int bn, splits, kps;
+    int bn, splits, kps, a_rows;
+    fl::SplitGeom geom;
 };
 
-int max_clusters(int dt, int bn, int pro, int splits) {
-    // cached per (dtype, width, prologue, cluster size); single device assumed per process slot
-    static std::atomic<int> cache[2][2][3][9];
+// Ring of the split-K kernel for a tile width, activation box height and
+// cluster size: the two-CTAs-per-SM budget when it holds at least four
+// stages and the reduction exchange, else the one-CTA budget. Returns false
+// if neither holds the exchange.
+template <int BN>
+bool split_geom_bn(int a_rows, int splits, fl::SplitGeom* g) {
+    using C = fl::SplitCfg<BN>;
+    const int stage = a_rows * 128 + C::B_BYTES;
+    const int xbytes = C::xchg_bytes(splits, a_rows);
+    int stages = std::min(C::MAX_STAGES, C::RING_SMALL / stage);
+    if (stages < 4 || xbytes > stages * stage) stages = std::min(C::MAX_STAGES, C::RING_LARGE / stage);
+    if (xbytes > stages * stage) return false;
+    g->stages = stages;
+    g->stage_bytes = stage;
+    g->smem_bytes = C::smem_bytes(stages, stage);
+    return true;
+}
+
+bool split_geom(int bn, int a_rows, int splits, fl::SplitGeom* g) {
+    return bn == 128 ? split_geom_bn<128>(a_rows, splits, g) : split_geom_bn<64>(a_rows, splits, g);
+}
+
+int max_clusters(int dt, int bn, int pro, int splits, int a_rows, int smem) {
+    // cached per (dtype, width, prologue, cluster size, box height); single device assumed per process slot
+    static std::atomic<int> cache[2][2][3][9][8];
     const int bi = bn == 128 ? 1 : 0;
-    int v = cache[dt][bi][pro][splits].load();
+    const int ai = (a_rows / 16 - 1) & 7;
+    int v = cache[dt][bi][pro][splits][ai].load();
     if (v != 0) return v;
 #define FL_Q(DT, BN, PRO) \
-    if (dt == DT && bn == BN && pro == PRO) v = fl::splitk_max_clusters<DT, BN, PRO>(splits);
+    if (dt == DT && bn == BN && pro == PRO) v = fl::splitk_max_clusters<DT, BN, PRO>(splits, smem);
     FL_Q(0, 64, 0) FL_Q(0, 64, 1) FL_Q(0, 64, 2) FL_Q(0, 128, 0) FL_Q(0, 128, 1) FL_Q(0, 128, 2)
     FL_Q(1, 64, 0) FL_Q(1, 64, 1) FL_Q(1, 64, 2) FL_Q(1, 128, 0) FL_Q(1, 128, 1) FL_Q(1, 128, 2)
 #undef FL_Q
     if (v <= 0) v = -1;
-    cache[dt][bi][pro][splits] = v;
+    cache[dt][bi][pro][splits][ai] = v;
     return v;
 }
 
@@ -233,17 +258,23 @@ bool plan_splitk(int dt, int pro, int M, int N, int K, int sms, SplitPlan* plan)
     }
     if (splits > nk) splits = nk;
     if (splits < 1) splits = 1;
+    const int a_rows = M >= fl::kBM ? fl::kBM : (M + 15) / 16 * 16;
     // every cluster of the grid resident at once (one wave): the cluster shape
     // limits how many fit on the GPCs
-    while (splits > 1) {
-        const int mc = max_clusters(dt, bn, pro, splits);
+    fl::SplitGeom geom;
+    for (;; --splits) {
+        if (splits < 1) return false;
+        if (!split_geom(bn, a_rows, splits, &geom)) continue;
+        if (splits == 1) break;
+        const int mc = max_clusters(dt, bn, pro, splits, a_rows, geom.smem_bytes);
         if (mc < 0 || tiles <= mc) break;
-        --splits;
     }
     const int kps = (nk + splits - 1) / splits;
     plan->bn = bn;
     plan->kps = kps;
     plan->splits = (nk + kps - 1) / kps;  // every split gets at least one K block
+    plan->a_rows = a_rows;
+    if (!split_geom(bn, a_rows, plan->splits, &plan->geom)) return false;
     return true;
 }
 
@@ -377,7 +408,7 @@ fl_status run_splitk(int dt, int pro, const void* A, const void* W, const void* 
                      const SplitPlan& plan, DeviceInfo* di, cudaStream_t stream) {
     GemmParams p;
     memset(&p, 0, sizeof(p));
-    const int a_rows = M >= fl::kBM ? fl::kBM : (M + 15) / 16 * 16;
+    const int a_rows = plan.a_rows;
     fl_status st;
     if ((st = encode_2d(&p.tmA, dt, A, K, M, fl::kBK, a_rows)) != FL_OK) return st;
     if ((st = encode_2d(&p.tmB, dt, W, K, N, fl::kBK, plan.bn)) != FL_OK) return st;
@@ -404,7 +435,22 @@ fl_status run_splitk(int dt, int pro, const void* A, const void* W, const void* 
     p.splits = plan.splits;
     p.kps = plan.kps;
     p.a_rows = a_rows;
+    p.s_stages = plan.geom.stages;
+    p.s_stage_bytes = plan.geom.stage_bytes;
     p.pdl = g_opt_pdl.load();
+    p.w_preload = g_opt_preload.load();
+    p.s_one_per_sm = plan.geom.smem_bytes * 2 + 2048 > 228 * 1024;  // one CTA per SM
+    {
+        const int nch = plan.bn / 8, s = plan.splits;
+        for (int d = 0; d <= s; ++d) p.xc_c0[d] = (unsigned char)(d * nch / s);
+        for (int d = 0; d < s; ++d)
+            for (int ch = p.xc_c0[d]; ch < p.xc_c0[d + 1]; ++ch) {
+                p.xc_owner[ch] = (unsigned char)d;
+                p.xc_pos[ch] = (unsigned char)(ch - p.xc_c0[d]);
+            }
+        p.xc_stride = (nch + s - 1) / s * 8 + 4;
+        p.inv_k = 1.0f / (float)K;
+    }
 #ifdef FL_TRACE
     if (const char* tp = getenv("FL_TRACE_PTR")) p.trace = reinterpret_cast<unsigned long long*>(strtoull(tp, nullptr, 10));
 #endif
@@ -513,6 +559,10 @@ fl_status fl_set_option(fl_option key, int value) {
         case FL_OPT_PDL:
             if (value < 0 || value > 1) return fail(FL_ERR_INVALID_ARG, "pdl must be 0 or 1");
             g_opt_pdl = value;
+            return ok();
+        case FL_OPT_WEIGHT_PRELOAD:
+            if (value < 0 || value > 1) return fail(FL_ERR_INVALID_ARG, "weight preload must be 0 or 1");
+            g_opt_preload = value;
             return ok();
         default:
             return fail(FL_ERR_INVALID_ARG, "unknown option %d", (int)key);

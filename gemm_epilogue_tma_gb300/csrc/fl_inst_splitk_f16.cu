@@ -8,10 +8,10 @@ template cudaError_t launch_splitk<DT_F16, 64, PRO_LN>(const GemmParams&, int, i
 template cudaError_t launch_splitk<DT_F16, 128, PRO_NONE>(const GemmParams&, int, int, cudaStream_t);
 template cudaError_t launch_splitk<DT_F16, 128, PRO_RMS>(const GemmParams&, int, int, cudaStream_t);
 template cudaError_t launch_splitk<DT_F16, 128, PRO_LN>(const GemmParams&, int, int, cudaStream_t);
-template int splitk_max_clusters<DT_F16, 64, PRO_NONE>(int);
-template int splitk_max_clusters<DT_F16, 64, PRO_RMS>(int);
-template int splitk_max_clusters<DT_F16, 64, PRO_LN>(int);
-template int splitk_max_clusters<DT_F16, 128, PRO_NONE>(int);
-template int splitk_max_clusters<DT_F16, 128, PRO_RMS>(int);
-template int splitk_max_clusters<DT_F16, 128, PRO_LN>(int);
+template int splitk_max_clusters<DT_F16, 64, PRO_NONE>(int, int);
+template int splitk_max_clusters<DT_F16, 64, PRO_RMS>(int, int);
+template int splitk_max_clusters<DT_F16, 64, PRO_LN>(int, int);
+template int splitk_max_clusters<DT_F16, 128, PRO_NONE>(int, int);
+template int splitk_max_clusters<DT_F16, 128, PRO_RMS>(int, int);
+template int splitk_max_clusters<DT_F16, 128, PRO_LN>(int, int);
 }  // namespace fl

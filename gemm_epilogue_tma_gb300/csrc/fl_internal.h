@@ -45,6 +45,17 @@ struct GemmParams {
     int kps;       // split-K kernel: 64-wide K blocks per split
     int a_rows;    // split-K kernel: rows of the activation box (128, or M rounded up to 16)
     int pdl;       // launch with a programmatic dependency on the previous kernel of the stream
+    // split-K reduction exchange, laid out on the host (tile columns in
+    // 8-column chunks, rank r owning chunks [xc_c0[r], xc_c0[r + 1]))
+    int w_preload;               // weights may be read before the programmatic dependency resolves
+    int s_one_per_sm;           // split-K kernel: the ring leaves room for one CTA per SM only
+    int s_stages;                // split-K kernel: pipeline stages of the ring
+    int s_stage_bytes;           // split-K kernel: bytes per stage (activation box + weight tile)
+    int xc_stride;              // floats per exchange slot row
+    unsigned char xc_owner[32];  // owning rank of each chunk
+    unsigned char xc_pos[32];    // chunk's position within its owner's slice
+    unsigned char xc_c0[12];     // first chunk of each rank; [splits] = chunk count
+    float inv_k;                 // 1 / K
     unsigned long long* trace;  // phase timestamps, builds with FL_TRACE only (else unused, null)
 };
 
@@ -59,7 +70,7 @@ template <int DT, int BN, int PRO>
 cudaError_t launch_splitk(const GemmParams& p, int grid, int splits, cudaStream_t stream);
 
 template <int DT, int BN, int PRO>
-int splitk_max_clusters(int splits);
+int splitk_max_clusters(int splits, int smem_bytes);
 
 template <int DT, int BN, int PRO, int KS>
 cudaError_t launch_pair(const GemmParams& p, int grid, cudaStream_t stream);
@@ -67,25 +78,57 @@ cudaError_t launch_pair(const GemmParams& p, int grid, cudaStream_t stream);
 template <int DT, int BN, int PRO, int KS>
 int pair_max_clusters();
 
-// Shared-memory layout of the split-K kernel.
+// Shared-memory layout of the split-K kernel: a fixed block of barriers and
+// small buffers, then the ring, sized at launch from the activation box
+// height (a decode step stages 16 activation rows, not 128), so small-M
+// instances fit two CTAs per SM and the next kernel's CTAs can be resident
+// (prefetching their weights) while this one finishes.
 template <int BN>
 struct SplitCfg {
-    static constexpr int A_BYTES = kBM * kBK * 2;
+    static constexpr int A_MAX_BYTES = kBM * kBK * 2;  // what one MMA reads of A (128 rows)
     static constexpr int B_BYTES = BN * kBK * 2;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES_RAW = (192 * 1024) / STAGE_BYTES;
-    static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
-    static constexpr int RED_STRIDE = BN + 4;  // fp32 partial row, padded against bank conflicts
-    static constexpr int RED_BYTES = kBM * RED_STRIDE * 4;
-    static constexpr int RING_BYTES = STAGES * STAGE_BYTES > RED_BYTES ? STAGES * STAGE_BYTES : RED_BYTES;
+    static constexpr int MAX_STAGES = 8;
     static constexpr int TMEM_COLS = BN < 32 ? 32 : BN;
-    static constexpr int OFF_BAR = RING_BYTES;
-    static constexpr int NUM_BARS = 3 * STAGES + 2;
+    static constexpr int NUM_BARS = 3 * MAX_STAGES + 4;
+    static constexpr int OFF_BAR = 0;
     static constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_SS = (OFF_SLOT + 16 + 15) / 16 * 16;   // [128] partial sum of squares
     static constexpr int OFF_LN = OFF_SS + kBM * 4;                 // [128] float2 mean, rstd
     static constexpr int OFF_GB = (OFF_LN + kBM * 8 + 127) / 128 * 128;
-    static constexpr int SMEM_BYTES = OFF_GB + STAGES * 256 + 1024;
+    static constexpr int OFF_RING = (OFF_GB + MAX_STAGES * 256 + 1023) / 1024 * 1024;
+    // Ring budgets: two CTAs per SM, else one.
+    static constexpr int RING_SMALL = 100 * 1024;
+    static constexpr int RING_LARGE = 192 * 1024;
+    // Reduction exchange (in the ring once the main loop is over). Rank r of
+    // the cluster owns the 8-column chunks [r C / s, (r + 1) C / s) of the
+    // tile (C = BN / 8 chunks, s ranks). A slot holds one rank's fp32 partial
+    // of one owner's columns, `rows` rows of xchg_stride(s) floats: the widest
+    // slice plus 4 (the first of them carries the row's partial sum of
+    // squares). An owner receives s slots (its own included), a sender keeps
+    // s - 1 outgoing ones. A stride of 4 mod 8 words keeps rows on distinct
+    // banks for 16-byte accesses.
+    static constexpr int CHUNKS = BN / 8;
+    __host__ __device__ static constexpr int xchg_stride(int s) { return (CHUNKS + s - 1) / s * 8 + 4; }
+    __host__ __device__ static constexpr int xchg_bytes(int s, int rows) {
+        return (2 * s - 1) * rows * xchg_stride(s) * 4;
+    }
+    static constexpr bool xchg_fits_large() {
+        for (int s = 1; s <= 8; ++s)
+            if (xchg_bytes(s, kBM) > RING_LARGE / (kBM * 128 + B_BYTES) * (kBM * 128 + B_BYTES)) return false;
+        return true;
+    }
+    static_assert(xchg_fits_large(), "the reduction exchange must fit in the large ring");
+    // dynamic shared memory of a launch: fixed block, ring, room for one
+    // MMA's 128-row read of A from the last stage, alignment slack
+    __host__ __device__ static constexpr int smem_bytes(int stages, int stage_bytes) {
+        return OFF_RING + stages * stage_bytes + (stage_bytes < A_MAX_BYTES ? A_MAX_BYTES - stage_bytes : 0) + 1024;
+    }
+    static constexpr int SMEM_MAX = OFF_RING + RING_LARGE + 1024 + 16 * 1024;
+};
+
+// Ring geometry of one split-K launch (host side).
+struct SplitGeom {
+    int stages, stage_bytes, smem_bytes;
 };
 
 // Shared-memory bytes of each tile configuration (host-visible).

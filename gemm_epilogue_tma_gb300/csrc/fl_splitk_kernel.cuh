@@ -9,12 +9,17 @@
 // as the real rows (M rounded up to 16), so a decode step stages little more
 // than the weights.
 //
-// Reduction: each CTA drains its fp32 partial tile from TMEM into its own
-// shared memory (with its partial RMS sum of squares), the cluster barrier
-// publishes it, and every CTA then sums an interleaved slice of the tile over
-// distributed shared memory (ld.shared::cluster), applies the epilogue (row
-// scale, bias, activation, residual) and stores 16-byte vectors. No global
-// scratch memory is used.
+// Reduction: rank r of the cluster owns a slice of the tile's columns. Once
+// its MMAs are done, a CTA tells its peers that its ring is free, drains its
+// fp32 partial tile from TMEM into per-owner slots (with its partial RMS sum
+// of squares per row), and sends each peer's slot with one bulk copy into
+// that peer's ring (completion counted in bytes on the peer's barrier). Each
+// owner then sums the `splits` partials of its slice from its own shared
+// memory, applies the epilogue (row scale, bias, activation, residual) and
+// stores 16-byte vectors. No global scratch memory is used, and the only
+// cluster-wide barrier is split: arrived at once a CTA's incoming data is
+// in, waited on just before exit, so no CTA leaves while a peer may still
+// read or write its shared memory.
 //
 // LayerNorm needs the row statistics before the fold: the transform warps
 // compute them at the start from the activation rows (two passes over L2,
@@ -63,14 +68,22 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Warp roles: 0 TMA producer, 1 MMA issuer, then four transform warps (norm
+// prologues; idle pair otherwise), then four epilogue warps (warp w reads
+// TMEM lanes 32 (w % 4) ...). Every warp joins the final reduction. Ten warps
+// at under 100 registers leave room for two CTAs per SM.
+template <int PRO>
+constexpr int splitk_threads() { return PRO != PRO_NONE ? 320 : 256; }
+
 template <int DT, int BN, int PRO>
-__global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
+__global__ void __launch_bounds__(splitk_threads<PRO>(), 1)
     fl_splitk_kernel(const __grid_constant__ GemmParams p) {
     if (threadIdx.x == 0) FL_MARK(p, 0);
     using C = SplitCfg<BN>;
     using Ops = DTypeOps<DT>;
-    constexpr int S = C::STAGES;
-    constexpr int EPI_WARP0 = PRO != PRO_NONE ? 8 : 4;
+    constexpr int S = C::MAX_STAGES;  // barrier slots; the ring uses p.s_stages of them
+    constexpr int XF_WARP0 = 2;
+    constexpr int EPI_WARP0 = PRO != PRO_NONE ? 6 : 4;
     constexpr uint32_t IDESC = umma_idesc_f16(Ops::kFormat, kBM, BN);
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile width");
 
@@ -79,19 +92,25 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     const uint32_t sbase = (raw_addr + 1023u) & ~1023u;
     uint8_t* smem = smem_raw + (sbase - raw_addr);
 
-    auto stage_a = [&](int s) { return sbase + s * C::STAGE_BYTES; };
-    auto stage_b = [&](int s) { return sbase + s * C::STAGE_BYTES + C::A_BYTES; };
+    const int box_rows = p.a_rows;             // rows the activation box stages
+    const uint32_t a_bytes = (uint32_t)box_rows * 128u;
+    const int NS = p.s_stages;
+    const uint32_t ring = sbase + C::OFF_RING;
+    const uint32_t stage_bytes = (uint32_t)p.s_stage_bytes;
+    auto stage_a = [&](int s) { return ring + (uint32_t)s * stage_bytes; };
+    auto stage_b = [&](int s) { return ring + (uint32_t)s * stage_bytes + a_bytes; };
     const uint32_t bar0 = sbase + C::OFF_BAR;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
     auto xform_bar = [&](int s) { return bar0 + 8u * (2 * S + s); };
     const uint32_t tfull_bar = bar0 + 8u * (3 * S);
     const uint32_t drain_bar = bar0 + 8u * (3 * S + 1);
+    const uint32_t peerfree_bar = bar0 + 8u * (3 * S + 2);  // every peer's ring may take my partials
+    const uint32_t recvd_bar = bar0 + 8u * (3 * S + 3);     // every peer's partial of my slice is here
     const uint32_t slot_addr = sbase + C::OFF_SLOT;
     float* ssbuf = reinterpret_cast<float*>(smem + C::OFF_SS);
     float2* lnstat = reinterpret_cast<float2*>(smem + C::OFF_LN);
     auto gb_slot = [&](int s) { return sbase + C::OFF_GB + 256u * s; };
-    const uint32_t red_base = sbase;  // the ring, reused once the main loop is over
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -104,17 +123,17 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     const int kb0 = rank * p.kps;
     const int kb1 = min(nk, kb0 + p.kps);
     const int rows = min(kBM, p.M - m0);       // real rows of this tile
-    const int box_rows = p.a_rows;             // rows the activation box stages
-    const uint32_t a_bytes = (uint32_t)box_rows * 128u;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
+        for (int s = 0; s < NS; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
             mbar_init(xform_bar(s), 4);
         }
         mbar_init(tfull_bar, 1);
         mbar_init(drain_bar, 1);
+        mbar_init(peerfree_bar, splits > 1 ? splits - 1 : 1);
+        mbar_init(recvd_bar, 1);
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -130,30 +149,54 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // first half of the barrier that makes every CTA's barriers exist before
+    // a peer signals them (published by fence.mbarrier_init); its wait comes
+    // right before the first remote access
+    cluster_arrive_relaxed();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + C::OFF_SLOT);
-    // Everything above overlaps the previous kernel on the stream; every
-    // global-memory access below waits for it, except the L2 prefetch of this
-    // CTA's first weight tiles (L2 is the point of coherence).
+    // Everything above overlaps the previous kernel on the stream; global
+    // memory is read only after it, with two exceptions for the weights:
+    // with preload allowed (the caller guarantees that kernel does not write
+    // W), the first ring stages' weight tiles go straight into shared memory
+    // (the stage barrier expects the whole stage, so the MMA still waits for
+    // the activation tile loaded after the dependency); else, when this CTA
+    // has the SM to itself, an L2 prefetch of those tiles (L2 is the point of
+    // coherence). With two CTAs per SM the prefetch would compete with the
+    // previous kernel's stream for lines it then loses.
+    const int npre = p.w_preload ? min(NS, kb1 - kb0) : 0;
+    const uint32_t stage_tx = a_bytes + (uint32_t)C::B_BYTES + (PRO != PRO_NONE ? 128u : 0u) +
+                              (PRO == PRO_LN && p.beta != nullptr ? 128u : 0u);
     if (warp == 0 && lane == 0) {
-        for (int kb = kb0; kb < kb0 + S && kb < kb1; ++kb) tma_prefetch_2d(&p.tmB, kb * kBK, n0);
+        for (int i = 0; i < npre; ++i) {
+            mbar_arrive_expect_tx(full_bar(i), stage_tx);
+            tma_load_2d(stage_b(i), &p.tmB, full_bar(i), (kb0 + i) * kBK, n0);
+        }
+        if (p.s_one_per_sm)
+            for (int kb = kb0 + npre; kb < kb0 + NS && kb < kb1; ++kb) tma_prefetch_2d(&p.tmB, kb * kBK, n0);
     }
     griddep_wait();
-    if (threadIdx.x == 0) griddep_launch_dependents();
+    // The next kernel may launch now when its CTAs can only use idle SMs; with
+    // two CTAs per SM it launches once this CTA's weight stream is over (see
+    // the MMA issuer), so its early weight loads fill the tail of this one
+    // instead of competing with its main loop.
+    if (threadIdx.x == 0 && p.s_one_per_sm) griddep_launch_dependents();
     if (threadIdx.x == 0) FL_MARK(p, 1);
 
+    bool ring_idle = false;  // MMA thread: every MMA of this CTA has completed
+    __shared__ int xchg_ok;  // every partial of my slice is in (epilogue lead)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             int s = 0;
             uint32_t ph = 0;
             int issued = 0;
-            const uint32_t bytes = a_bytes + (uint32_t)C::B_BYTES + (PRO != PRO_NONE ? 128u : 0u) +
-                                   (PRO == PRO_LN && p.beta != nullptr ? 128u : 0u);
             for (int kb = kb0; kb < kb1; ++kb) {
-                if (!wait_bar(empty_bar(s), ph ^ 1u, p.status, p.timeout_ns, 21)) break;
-                mbar_arrive_expect_tx(full_bar(s), bytes);
+                if (kb - kb0 >= npre) {  // a preloaded stage is fresh and already expects its bytes
+                    if (!wait_bar(empty_bar(s), ph ^ 1u, p.status, p.timeout_ns, 21)) break;
+                    mbar_arrive_expect_tx(full_bar(s), stage_tx);
+                    tma_load_2d(stage_b(s), &p.tmB, full_bar(s), kb * kBK, n0);
+                }
                 tma_load_2d(stage_a(s), &p.tmA, full_bar(s), kb * kBK, m0);
-                tma_load_2d(stage_b(s), &p.tmB, full_bar(s), kb * kBK, n0);
                 if (PRO != PRO_NONE) {
                     tma_load_2d(gb_slot(s), &p.tmGamma, full_bar(s), kb * kBK, 0);
                     if (PRO == PRO_LN && p.beta != nullptr)
@@ -161,15 +204,15 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                 }
                 if (issued == 0) FL_MARK(p, 2);
                 ++issued;
-                if (++s == S) {
+                if (++s == NS) {
                     s = 0;
                     ph ^= 1u;
                 }
             }
-            const int pending = issued < S ? issued : S;
+            const int pending = issued < NS ? issued : NS;
             for (int i = 1; i <= pending; ++i) {
                 const int idx = issued - i;
-                wait_bar_drain(full_bar(idx % S), (uint32_t)((idx / S) & 1), 20000000ull);
+                wait_bar_drain(full_bar(idx % NS), (uint32_t)((idx / NS) & 1), 20000000ull);
             }
         }
     } else if (warp == 1) {
@@ -192,7 +235,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                 for (int kk = 0; kk < kBK / 16; ++kk)
                     umma_f16_ss(tmem_base, da + 2 * kk, db + 2 * kk, IDESC, (kb != kb0) || (kk != 0));
                 umma_commit(empty_bar(s));
-                if (++s == S) {
+                if (++s == NS) {
                     s = 0;
                     ph ^= 1u;
                 }
@@ -200,11 +243,12 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
             if (ok) umma_commit(tfull_bar);
             FL_MARK(p, 4);
             umma_commit(drain_bar);
-            wait_bar_drain(drain_bar, 0, 20000000ull);
+            ring_idle = wait_bar_drain(drain_bar, 0, 20000000ull) && ok;
+            if (!p.s_one_per_sm) griddep_launch_dependents();
         }
-    } else if (PRO != PRO_NONE && warp >= 4 && warp < 8) {
+    } else if (PRO != PRO_NONE && warp >= XF_WARP0 && warp < XF_WARP0 + 4) {
         // ------------------------------------------------------------ transform
-        const int t = threadIdx.x - 128;
+        const int t = threadIdx.x - 32 * XF_WARP0;
         const int ni = box_rows / 16;  // rows of this thread: t/8 + 16 i
         float mean[8], rstd[8], ss[8];
 #pragma unroll
@@ -216,7 +260,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         if (PRO == PRO_LN) {
             // statistics of the whole row: warp w takes rows w, w + 4, ...
             const uint16_t* xg = reinterpret_cast<const uint16_t*>(p.a_ptr);
-            for (int r = warp - 4; r < rows; r += 4) {
+            for (int r = warp - XF_WARP0; r < rows; r += 4) {
                 const uint16_t* xr = xg + (size_t)(m0 + r) * p.K;
                 float a = 0.f;
                 for (int k = lane * 8; k < p.K; k += 256) {
@@ -262,7 +306,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(xform_bar(s));
-            if (++s == S) {
+            if (++s == NS) {
                 s = 0;
                 ph ^= 1u;
             }
@@ -273,87 +317,184 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                 const float v = row_allreduce8(ss[i]);
                 if ((t & 7) == 0 && i < ni) ssbuf[(t >> 3) + 16 * i] = v;
             }
+            named_bar_arrive(3, 256);  // hand the partial sums to the epilogue warps
         }
     } else if (warp >= EPI_WARP0) {
-        // ------------------------------------------------------------ TMEM -> shared partial
+        // ------------------------------------------------------------ reduction exchange + epilogue
+        // This tail runs on few warps with little to overlap it, so its
+        // index arithmetic comes from host-built tables (no divisions).
         const int q = warp & 3;
-        const int r = q * 32 + lane;
-        if (wait_bar(tfull_bar, 0, p.status, p.timeout_ns, 24)) {
+        const int r = q * 32 + lane;                 // the row this thread drains
+        const int t = threadIdx.x - 32 * EPI_WARP0;  // 0..127
+        const int me = rank;
+        const int stride = p.xc_stride;              // floats per slot row
+        const uint32_t slot_bytes = (uint32_t)(rows * stride) * 4u;
+        const uint32_t row_off = (uint32_t)(r * stride) * 4u;
+        // slots in the (now idle) ring: [0, splits) received, indexed by
+        // sender (my own partial of my slice among them); then splits - 1
+        // outgoing, indexed by owner, skipping me
+        auto slot_index = [&](int d) { return d == me ? me : splits + d - (d > me ? 1 : 0); };
+        const bool lead = t == 0;
+        {
+            // bring the parameters the tail reads into this SM's constant
+            // cache while the main loop runs (a miss there costs an L2
+            // round trip on the critical path)
+            uint32_t touch = (uint32_t)p.xc_stride ^ p.xc_owner[lane] ^ p.xc_pos[lane] ^ p.xc_c0[lane & 7] ^
+                             __float_as_uint(p.inv_k) ^ __float_as_uint(p.eps) ^ (uint32_t)p.act ^ (uint32_t)p.N ^
+                             (uint32_t)reinterpret_cast<uintptr_t>(p.residual) ^
+                             (uint32_t)reinterpret_cast<uintptr_t>(p.out_ptr) ^
+                             (uint32_t)reinterpret_cast<uintptr_t>(p.bias);
+            asm volatile("" ::"r"(touch));
+        }
+
+        bool ok = wait_bar(tfull_bar, 0, p.status, p.timeout_ns, 24);
+        __syncwarp();
+        cluster_wait();  // every CTA of the cluster has initialised its barriers
+        float ssr = 0.f;
+        if (PRO == PRO_RMS) {
+            named_bar_sync(3, 256);  // the transform warps have written ssbuf
+            if (r < rows) ssr = ssbuf[r];
+        }
+        if (ok) {
             tc_fence_after();
-            if (threadIdx.x == 32 * EPI_WARP0) FL_MARK(p, 5);
+            if (lead) FL_MARK(p, 5);
+            if (lead && splits > 1) mbar_arrive_expect_tx(recvd_bar, (uint32_t)(splits - 1) * slot_bytes);
             if (q * 32 < rows) {
                 const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16);
-                const uint32_t dst = red_base + (uint32_t)(r * C::RED_STRIDE) * 4u;
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(taddr + c * 32, v);
+                // two 32-column loads in flight per wait
+                constexpr int NB = BN / 32 < 2 ? 1 : 2;
+#pragma unroll
+                for (int c = 0; c < BN / 32; c += NB) {
+                    uint32_t v[NB][32];
+#pragma unroll
+                    for (int b = 0; b < NB; ++b) tmem_ld_32x32b_x32(taddr + (c + b) * 32, v[b]);
                     tmem_ld_wait();
                     if (r < rows) {
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            st_shared_v4(dst + (c * 32 + j * 4) * 4, v[j * 4], v[j * 4 + 1], v[j * 4 + 2], v[j * 4 + 3]);
+                        for (int b = 0; b < NB; ++b) {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const int ch = (c + b) * 4 + j;
+                                const uint32_t dst = ring + (uint32_t)slot_index(p.xc_owner[ch]) * slot_bytes +
+                                                     row_off + (uint32_t)p.xc_pos[ch] * 32u;
+                                st_shared_v4(dst, v[b][j * 8], v[b][j * 8 + 1], v[b][j * 8 + 2], v[b][j * 8 + 3]);
+                                st_shared_v4(dst + 16, v[b][j * 8 + 4], v[b][j * 8 + 5], v[b][j * 8 + 6],
+                                             v[b][j * 8 + 7]);
+                            }
+                        }
                     }
                 }
+                if (PRO == PRO_RMS && r < rows) {
+                    const uint32_t ss_off = row_off + (uint32_t)(stride - 4) * 4u;
+#pragma unroll
+                    for (int d = 0; d < 8; ++d)
+                        if (d < splits) st_shared_f32(ring + (uint32_t)slot_index(d) * slot_bytes + ss_off, ssr);
+                }
             }
+            if (lead) FL_MARK(p, 10);
+            tc_fence_before();
+            fence_proxy_async_smem();  // outgoing slots are read by the bulk copies
+            named_bar_sync(2, 128);
+            if (lead && splits > 1) {
+                if (wait_bar_cluster(peerfree_bar, 0, p.status, p.timeout_ns, 25)) {
+                    const uint32_t src0 = ring + (uint32_t)splits * slot_bytes;
+                    const uint32_t dst = ring + (uint32_t)me * slot_bytes;
+                    for (int d = 0, k = 0; d < splits; ++d) {
+                        if (d == me) continue;
+                        bulk_copy_to_cluster(mapa_shared(dst, (uint32_t)d), src0 + (uint32_t)k * slot_bytes, slot_bytes,
+                                             mapa_shared(recvd_bar, (uint32_t)d));
+                        ++k;
+                    }
+                }
+                FL_MARK(p, 6);
+            }
+            if (splits > 1) ok = wait_bar_cluster(recvd_bar, 0, p.status, p.timeout_ns, 26);
+            if (lead) FL_MARK(p, 7);
         }
+        if (lead) xchg_ok = ok ? 1 : 0;
+        __syncwarp();
+        // my incoming partials are in, so every peer's copy to me has read
+        // its source: the second half of the lifetime barrier can open
+        cluster_arrive_relaxed();
+        if (lead) FL_MARK(p, 11);
     }
 
+    if (warp < EPI_WARP0) {
+        __syncwarp();
+        cluster_wait();  // every CTA of the cluster has initialised its barriers
+        if (warp == 1 && lane == 0 && ring_idle && splits > 1) {
+            // my MMAs are done with my ring: peers may write their partials
+            // of my slice into it
+            for (int d = 0; d < splits; ++d)
+                if (d != rank) mbar_arrive_cluster(mapa_shared(peerfree_bar, (uint32_t)d));
+        }
+        __syncwarp();
+        cluster_arrive_relaxed();  // nothing below touches another CTA
+    }
+    // ---------------------------------------------------------------- reduction + epilogue
+    // Every thread of the CTA sums the `splits` partials of my slice (rows x
+    // w chunks of 8 columns; 8, or 16, threads per row, one chunk each),
+    // scales, adds bias, activation and residual, and stores 16 bytes.
+    const int xc0 = p.xc_c0[rank];
+    const int xw = p.xc_c0[rank + 1] - xc0;
+    const int xsh = xw > 8 ? 4 : 3;
+    const int xch = threadIdx.x & ((1 << xsh) - 1);
+    const int xcol = n0 + (xc0 + xch) * 8;
+    const bool xmine = xch < xw && xcol < p.N;
+    float bb[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) bb[e] = 0.f;
+    if (xmine && p.bias != nullptr) {  // in flight across the barrier
+        const uint4 bv = ldg_v4(reinterpret_cast<const uint16_t*>(p.bias) + xcol);
+        const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 b2 = Ops::unpack(bw[e]);
+            bb[2 * e] = b2.x;
+            bb[2 * e + 1] = b2.y;
+        }
+    }
     __syncwarp();
     tc_fence_before();
-    __syncthreads();
-    if (threadIdx.x == 0) FL_MARK(p, 6);
-    // partials of every CTA of the cluster are written and visible after this
-    cluster_sync_all();
-    if (threadIdx.x == 0) FL_MARK(p, 7);
-
-    // ---------------------------------------------------------------- reduction + epilogue
-    {
-        const bool failed = *reinterpret_cast<volatile int*>(p.status) != 0;
-        const int cpr = BN / 8;  // 8-column chunks per row
-        const int items = rows * cpr;
+    __syncthreads();  // the epilogue warps saw every partial of my slice land
+    if (threadIdx.x == 0) FL_MARK(p, 12);
+    if (xchg_ok && xmine) {
         using T = uint16_t;
-        const T* bias = reinterpret_cast<const T*>(p.bias);
         const T* res = reinterpret_cast<const T*>(p.residual);
         T* out = reinterpret_cast<T*>(p.out_ptr);
-        for (int i = rank + splits * (int)threadIdx.x; !failed && i < items; i += splits * (int)blockDim.x) {
-            const int row = i / cpr, chunk = i % cpr;
-            const int col = n0 + chunk * 8;
-            if (col >= p.N) continue;
+        const int stride = p.xc_stride;
+        const uint32_t slot_bytes = (uint32_t)(rows * stride) * 4u;
+        const int nthreads = (int)blockDim.x;
+        for (int row = (int)threadIdx.x >> xsh; row < rows; row += nthreads >> xsh) {
+            const size_t g = (size_t)(m0 + row) * p.N + xcol;
+            uint4 rv = make_uint4(0u, 0u, 0u, 0u);
+            if (res != nullptr) rv = *reinterpret_cast<const uint4*>(res + g);
             float v[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) v[e] = 0.f;
             float ss = 0.f;
-            const uint32_t off = red_base + (uint32_t)(row * C::RED_STRIDE + chunk * 8) * 4u;
-            for (int qr = 0; qr < splits; ++qr) {
-                const uint32_t a = mapa_shared(off, (uint32_t)qr);
-                const float4 lo = ld_cluster_v4(a), hi = ld_cluster_v4(a + 16);
-                v[0] += lo.x; v[1] += lo.y; v[2] += lo.z; v[3] += lo.w;
-                v[4] += hi.x; v[5] += hi.y; v[6] += hi.z; v[7] += hi.w;
-                if (PRO == PRO_RMS) ss += ld_cluster_f32(mapa_shared(smem_u32(ssbuf + row), (uint32_t)qr));
-            }
-            if (PRO == PRO_RMS) {
-                const float rs = rsqrtf(ss / (float)p.K + p.eps);
+            const uint32_t a0 = ring + (uint32_t)(row * stride + xch * 8) * 4u;
+            const uint32_t s0 = ring + (uint32_t)(row * stride + stride - 4) * 4u;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] *= rs;
-            }
-            if (bias != nullptr) {
-                const uint4 bv = ldg_v4(bias + col);
-                const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 b2 = Ops::unpack(bw[e]);
-                    v[2 * e] += b2.x;
-                    v[2 * e + 1] += b2.y;
+            for (int src = 0; src < 8; ++src) {
+                if (src < splits) {
+                    const uint32_t a = a0 + (uint32_t)src * slot_bytes;
+                    const uint4 lo = ld_shared_v4(a), hi = ld_shared_v4(a + 16);
+                    v[0] += __uint_as_float(lo.x); v[1] += __uint_as_float(lo.y);
+                    v[2] += __uint_as_float(lo.z); v[3] += __uint_as_float(lo.w);
+                    v[4] += __uint_as_float(hi.x); v[5] += __uint_as_float(hi.y);
+                    v[6] += __uint_as_float(hi.z); v[7] += __uint_as_float(hi.w);
+                    if (PRO == PRO_RMS) ss += ld_shared_f32(s0 + (uint32_t)src * slot_bytes);
                 }
             }
+            const float rs = PRO == PRO_RMS ? rsqrtf(fmaf(ss, p.inv_k, p.eps)) : 1.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = fmaf(v[e], rs, bb[e]);
             if (p.act != ACT_NONE) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) v[e] = act_apply(p.act, v[e]);
             }
-            const size_t g = (size_t)(m0 + row) * p.N + col;
             if (res != nullptr) {
-                const uint4 rv = *reinterpret_cast<const uint4*>(res + g);
                 const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -362,14 +503,15 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                     v[2 * e + 1] += r2.y;
                 }
             }
+            if (threadIdx.x == 0) FL_MARK(p, 13);
             *reinterpret_cast<uint4*>(out + g) = make_uint4(Ops::pack(v[0], v[1]), Ops::pack(v[2], v[3]),
                                                              Ops::pack(v[4], v[5]), Ops::pack(v[6], v[7]));
         }
     }
-    __syncthreads();
     if (threadIdx.x == 0) FL_MARK(p, 8);
-    // no CTA leaves while a peer may still read its shared memory
-    cluster_sync_all();
+    __syncwarp();
+    // no CTA leaves while a peer may still read or write its shared memory
+    cluster_wait();
     if (threadIdx.x == 0) FL_MARK(p, 9);
     if (warp == 1) {
         tc_fence_after();
@@ -377,17 +519,27 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     }
 }
 
-// How many clusters of `splits` CTAs of this kernel can be resident at once.
 template <int DT, int BN, int PRO>
-int splitk_max_clusters(int splits) {
-    using C = SplitCfg<BN>;
+cudaError_t splitk_configure() {
+    static cudaError_t state = [] {
+        auto kern = fl_splitk_kernel<DT, BN, PRO>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SplitCfg<BN>::SMEM_MAX);
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        return e;
+    }();
+    return state;
+}
+
+// How many clusters of `splits` CTAs of this kernel, each with `smem_bytes`
+// of dynamic shared memory, can be resident at once.
+template <int DT, int BN, int PRO>
+int splitk_max_clusters(int splits, int smem_bytes) {
+    if (splitk_configure<DT, BN, PRO>() != cudaSuccess) return 0;
     auto kern = fl_splitk_kernel<DT, BN, PRO>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
-        return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(splits, 1, 1);
-    cfg.blockDim = dim3(PRO != PRO_NONE ? 384 : 256, 1, 1);
-    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.blockDim = dim3(splitk_threads<PRO>(), 1, 1);
+    cfg.dynamicSmemBytes = smem_bytes;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = splits;
@@ -407,16 +559,12 @@ template <int DT, int BN, int PRO>
 cudaError_t launch_splitk(const GemmParams& p, int grid, int splits, cudaStream_t stream) {
     using C = SplitCfg<BN>;
     auto kern = fl_splitk_kernel<DT, BN, PRO>;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    cudaError_t e = splitk_configure<DT, BN, PRO>();
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
-    cfg.blockDim = dim3(PRO != PRO_NONE ? 384 : 256, 1, 1);
-    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.blockDim = dim3(splitk_threads<PRO>(), 1, 1);
+    cfg.dynamicSmemBytes = C::smem_bytes(p.s_stages, p.s_stage_bytes);
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;

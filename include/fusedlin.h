@@ -180,6 +180,16 @@ fl_status fl_device_status(void* stream);
  *                       dependency on the previous kernel of the stream, so its
  *                       set-up overlaps that kernel's tail (all of its memory
  *                       accesses still wait for it); 0 = plain stream order.
+ *   FL_OPT_WEIGHT_PRELOAD: 0 (default) or 1. With 1 the caller promises that
+ *                       no kernel on the stream writes the weight matrix W
+ *                       between its last host-ordered write and this call (the
+ *                       usual case: weights are read-only across a layer
+ *                       sequence). The small-M split-K kernel then stages its
+ *                       first weight tiles into shared memory before its
+ *                       programmatic dependency on the previous kernel
+ *                       resolves, so the weight stream of a decode step starts
+ *                       while the previous layer finishes. Activations, gamma,
+ *                       beta, bias and residual are still read only after it.
  * Returns FL_ERR_INVALID_ARG for an unknown key or a value out of range.
  */
 typedef enum {
@@ -187,7 +197,8 @@ typedef enum {
     FL_OPT_VARIANT = 1,
     FL_OPT_TIMEOUT_MS = 2,
     FL_OPT_SPLIT_K = 3,
-    FL_OPT_PDL = 4
+    FL_OPT_PDL = 4,
+    FL_OPT_WEIGHT_PRELOAD = 5
 } fl_option;
 fl_status fl_set_option(fl_option key, int value);
 

@@ -133,6 +133,7 @@ def test_options(L):
     assert L.fl_set_option(2, 0) == INVALID and L.fl_set_option(2, 2000) == OK
     assert L.fl_set_option(3, 9) == INVALID and L.fl_set_option(3, 0) == OK
     assert L.fl_set_option(4, 2) == INVALID and L.fl_set_option(4, 0) == OK and L.fl_set_option(4, 1) == OK
+    assert L.fl_set_option(5, 2) == INVALID and L.fl_set_option(5, 1) == OK and L.fl_set_option(5, 0) == OK
     assert L.fl_set_option(42, 0) == INVALID
     assert L.fl_debug_wait_timeout(0, None) == INVALID
 

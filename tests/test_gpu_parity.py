@@ -175,6 +175,26 @@ def test_splitk_variant_all_patterns(dt, splits, shape):
 
 
 @pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("splits", [4, 5, 6, 7])
+def test_splitk_uneven_column_slices(dt, splits):
+    # 16 eight-column chunks over 5, 6 or 7 ranks: owners of unequal width
+    M, N, K = 200, 392, 2048
+    t = syn.dense_layer_inputs(M, N, K, dt)
+    fl.set_option("variant", 2)
+    fl.set_option("tile_n", 128)
+    fl.set_option("split_k", splits)
+    try:
+        for pattern in syn.PATTERNS:
+            got, ref = run_pattern(t, pattern)
+            assert_close(got, ref, dt, f"split-K x{splits} BN=128 {pattern} {dt}")
+        fl.device_status()
+    finally:
+        fl.set_option("variant", 0)
+        fl.set_option("tile_n", 0)
+        fl.set_option("split_k", 0)
+
+
+@pytest.mark.parametrize("dt", DTYPES)
 def test_splitk_wide_tiles_and_norm_bias_act(dt):
     M, N, K = 96, 392, 1536
     t = syn.norm_gemm_inputs(M, N, K, "layer", dt, with_bias=True)
@@ -333,6 +353,36 @@ def test_decode_sweep_rmsnorm_all_elements(dt, D, M):
     torch.cuda.synchronize()
     ref = oracle.norm_gemm(f64(t["x"]), f64(t["gamma"]), None, f64(t["W"]), None, 1e-6, "rms")
     assert_close(got, ref, dt, f"decode rms {dt} M={M} D={D}")
+
+
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("M,D", [(1, 4096), (16, 1024), (32, 2048), (128, 1024)])
+def test_weight_preload_chained_layers(dt, M, D):
+    """Two decode layers back to back on one stream, the second reading the first's output.
+
+    With weight preload the second kernel stages weight tiles before the first
+    has finished; its activation (the first's output, overwritten with NaN by
+    a kernel just before) must still be read after it.
+    """
+    t1 = syn.norm_gemm_inputs(M, D, D, "rms", dt, seed=11)
+    t2 = syn.norm_gemm_inputs(M, D, D, "rms", dt, seed=12)
+    g1 = {k: dev(v) for k, v in t1.items()}
+    g2 = {k: dev(v) for k, v in t2.items()}
+    fl.set_option("weight_preload", 1)
+    try:
+        y1 = torch.empty((M, D), dtype=g1["x"].dtype, device="cuda")
+        for _ in range(3):
+            y1.fill_(float("nan"))
+            fl.norm_gemm(g1["x"], g1["gamma"], g1["W"], out=y1, eps=1e-6, norm="rms")
+            y2 = fl.norm_gemm(y1, g2["gamma"], g2["W"], eps=1e-6, norm="rms")
+        torch.cuda.synchronize()
+        fl.device_status()
+    finally:
+        fl.set_option("weight_preload", 0)
+    ref1 = oracle.norm_gemm(f64(t1["x"]), f64(t1["gamma"]), None, f64(t1["W"]), None, 1e-6, "rms")
+    assert_close(y1, ref1, dt, f"preload layer 1 {dt} M={M} D={D}")
+    ref2 = oracle.norm_gemm(f64(y1.cpu()), f64(t2["gamma"]), None, f64(t2["W"]), None, 1e-6, "rms")
+    assert_close(y2, ref2, dt, f"preload layer 2 {dt} M={M} D={D}")
 
 
 # ---------------------------------------------------------------------------
