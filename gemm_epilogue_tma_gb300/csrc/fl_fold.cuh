@@ -7,30 +7,14 @@
 // of rows t/8 + 16 i, i < box_rows / 16. A warp therefore touches four whole
 // rows per access (no bank conflicts), every warp has work even for a 16-row
 // decode box, and each thread needs a single 16-byte slice of gamma / beta.
-// Per-row results (RMS sum of squares, LayerNorm moments) are merged across
-// the 8 lanes that share a row with butterfly shuffles.
+// Per-row RMS sums of squares are merged across the 8 lanes that share a row
+// with butterfly shuffles. LayerNorm folds with row statistics computed ahead
+// of the GEMM by the statistics kernel.
 #pragma once
 
 #include "fl_common.cuh"
 
 namespace fl {
-
-struct RowMoments {  // running count, mean and sum of squared deviations
-    float n, mean, m2;
-};
-
-// Chan et al.'s pairwise merge of two partial moment sets.
-__device__ __forceinline__ RowMoments merge_moments(RowMoments a, RowMoments b) {
-    const float n = a.n + b.n;
-    if (n == 0.f) return a;
-    const float d = b.mean - a.mean;
-    const float wb = b.n / n;
-    RowMoments r;
-    r.n = n;
-    r.mean = a.mean + d * wb;
-    r.m2 = a.m2 + b.m2 + d * d * a.n * wb;
-    return r;
-}
 
 __device__ __forceinline__ uint32_t fold_row_addr(uint32_t stage, int row, int j) {
     return stage + row * 128 + ((j ^ (row & 7)) << 4);
@@ -72,31 +56,6 @@ __device__ __forceinline__ void fold_rms_stage(uint32_t stage, uint32_t gamma_sl
             const uint32_t a = fold_row_addr(stage, (t >> 3) + 16 * i, j);
             st_shared_v4(a, xv[i].x, xv[i].y, xv[i].z, xv[i].w);
         }
-}
-
-// LayerNorm statistics, chunk-parallel: this thread's chunk of each of its
-// rows is added to per-row shifted sums (see ShiftedSums below); `valid` says
-// whether the chunk lies inside K (zero-filled chunks must not count).
-struct ShiftedSums;
-template <int DT>
-__device__ __forceinline__ void ln_sums_stage(uint32_t stage, int t, int ni, bool valid, ShiftedSums (&st)[8]);
-
-// Moments of the 8 lanes that share each row, merged (Chan et al.) in a fixed
-// order so every lane ends with the same full-row moments.
-__device__ __forceinline__ void ln_stats_allreduce(RowMoments (&mo)[8], int ni) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        if (i < ni) {
-#pragma unroll
-            for (int o = 1; o < 8; o <<= 1) {
-                RowMoments other;
-                other.n = __shfl_xor_sync(0xffffffffu, mo[i].n, o);
-                other.mean = __shfl_xor_sync(0xffffffffu, mo[i].mean, o);
-                other.m2 = __shfl_xor_sync(0xffffffffu, mo[i].m2, o);
-                mo[i] = (threadIdx.x & o) ? merge_moments(other, mo[i]) : merge_moments(mo[i], other);
-            }
-        }
-    }
 }
 
 // LayerNorm fold: chunk := (x - mean) * rstd * gamma + beta, in fp32, rounded once.
@@ -170,89 +129,53 @@ __device__ __forceinline__ void fold_rms_row(uint32_t stage, uint32_t gamma_slic
     }
 }
 
-// LayerNorm moments of one row by shifted sums: with a shift c near the row
-// mean (the mean of the row's first 8 elements), accumulate n, S1 = sum(x - c)
-// and S2 = sum((x - c)^2) in fp32; then mean = c + S1 / n and
-// m2 = S2 - S1^2 / n, whose subtraction loses only about log2(1 + (mean-c)^2 /
-// var) bits. One pass per K block, no division per block.
-struct ShiftedSums {
-    float c, s1, s2, n;
-};
-
+// LayerNorm, thread-per-row: gamma and beta of the K block are first widened
+// to fp32 once per stage (threads 0-31 take gamma, 32-63 beta, one 16-bit
+// pair each; zeros without beta), then every thread reads them back with
+// broadcast loads instead of unpacking all 64 columns itself. The caller
+// synchronises the 128 transform threads between the two steps.
 template <int DT>
-__device__ __forceinline__ void ln_sums_row(uint32_t stage, int t, int nvalid, ShiftedSums& st) {
+__device__ __forceinline__ void ln_widen_gb(uint32_t gb_slice, uint32_t gbf_slice, bool has_beta, int t) {
     using Ops = DTypeOps<DT>;
-    if (nvalid <= 0) return;
-    const int sw = t & 7;
-    float v[64];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const uint4 x = ld_shared_v4(stage + t * 128 + ((j ^ sw) << 4));
-        const float2 a = Ops::unpack(x.x), b = Ops::unpack(x.y), c = Ops::unpack(x.z), d = Ops::unpack(x.w);
-        v[8 * j + 0] = a.x; v[8 * j + 1] = a.y; v[8 * j + 2] = b.x; v[8 * j + 3] = b.y;
-        v[8 * j + 4] = c.x; v[8 * j + 5] = c.y; v[8 * j + 6] = d.x; v[8 * j + 7] = d.y;
-    }
-    if (st.n == 0.f)
-        st.c = (((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]))) * 0.125f;
-    float a1[4] = {0.f, 0.f, 0.f, 0.f}, a2[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        if (j < nvalid) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float dlt = v[8 * j + e] - st.c;
-                a1[e & 3] += dlt;
-                a2[e & 3] = fmaf(dlt, dlt, a2[e & 3]);
-            }
+    if (t < 64) {
+        const bool beta = t >= 32;
+        const int i = t & 31;
+        float2 v = make_float2(0.f, 0.f);
+        if (!beta || has_beta) {
+            uint32_t w;
+            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w) : "r"(gb_slice + (beta ? 128u : 0u) + 4u * i));
+            v = Ops::unpack(w);
         }
-    }
-    st.s1 += (a1[0] + a1[1]) + (a1[2] + a1[3]);
-    st.s2 += (a2[0] + a2[1]) + (a2[2] + a2[3]);
-    st.n += 8.f * (float)nvalid;
-}
-
-__device__ __forceinline__ RowMoments ln_sums_moments(const ShiftedSums& st) {
-    if (st.n == 0.f) return RowMoments{0.f, 0.f, 0.f};
-    const float d = st.s1 / st.n;
-    return RowMoments{st.n, st.c + d, fmaxf(st.s2 - st.s1 * d, 0.f)};
-}
-
-template <int DT>
-__device__ __forceinline__ void ln_sums_stage(uint32_t stage, int t, int ni, bool valid, ShiftedSums (&st)[8]) {
-    using Ops = DTypeOps<DT>;
-    if (!valid) return;
-    const int j = t & 7;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        if (i < ni) {
-            const uint4 x = ld_shared_v4(fold_row_addr(stage, (t >> 3) + 16 * i, j));
-            const float2 a = Ops::unpack(x.x), b = Ops::unpack(x.y), c = Ops::unpack(x.z), d = Ops::unpack(x.w);
-            if (st[i].n == 0.f) st[i].c = (((a.x + a.y) + (b.x + b.y)) + ((c.x + c.y) + (d.x + d.y))) * 0.125f;
-            const float cc = st[i].c;
-            const float e0 = a.x - cc, e1 = a.y - cc, e2 = b.x - cc, e3 = b.y - cc;
-            const float e4 = c.x - cc, e5 = c.y - cc, e6 = d.x - cc, e7 = d.y - cc;
-            st[i].s1 += ((e0 + e1) + (e2 + e3)) + ((e4 + e5) + (e6 + e7));
-            st[i].s2 += ((e0 * e0 + e1 * e1) + (e2 * e2 + e3 * e3)) + ((e4 * e4 + e5 * e5) + (e6 * e6 + e7 * e7));
-            st[i].n += 8.f;
-        }
+        asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(gbf_slice + (beta ? 256u : 0u) + 8u * i), "f"(v.x),
+                     "f"(v.y)
+                     : "memory");
     }
 }
 
+// Row t := (x - mean) * rstd * gamma + beta, as fma(fma(x, rstd, -mean * rstd),
+// gamma, beta) in fp32 (the fp32 error stays relative to |mean| * 2^-24,
+// far below the one rounding to the dtype). The row's eight chunks are all
+// requested before any is used, and gamma/beta (fp32, gbf[0..15] = gamma,
+// gbf[16..31] = beta as float4) are plain loads the compiler may schedule.
 template <int DT>
-__device__ __forceinline__ void fold_ln_row(uint32_t stage, uint32_t gb_slice, bool has_beta, int t, float mean,
-                                            float rstd, uint32_t (&o)[32]) {
+__device__ __forceinline__ void fold_ln_row(uint32_t stage, const float4* gbf, int t, float rstd, float nmr,
+                                            uint32_t (&o)[32]) {
     using Ops = DTypeOps<DT>;
     const int sw = t & 7;
+    uint4 xv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) xv[j] = ld_shared_v4(stage + t * 128 + ((j ^ sw) << 4));
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        const uint4 x = ld_shared_v4(stage + t * 128 + ((j ^ sw) << 4));
-        const uint4 g = ld_shared_v4(gb_slice + j * 16);
-        const uint4 b = has_beta ? ld_shared_v4(gb_slice + 128 + j * 16) : make_uint4(0u, 0u, 0u, 0u);
-        const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, gw[4] = {g.x, g.y, g.z, g.w}, bw[4] = {b.x, b.y, b.z, b.w};
+        const float4 g0 = gbf[2 * j], g1 = gbf[2 * j + 1], b0 = gbf[16 + 2 * j], b1 = gbf[16 + 2 * j + 1];
+        const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+        const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+        const uint32_t xw[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const float2 f = Ops::unpack(xw[q]), g2 = Ops::unpack(gw[q]), b2 = Ops::unpack(bw[q]);
-            o[4 * j + q] = Ops::pack(fmaf((f.x - mean) * rstd, g2.x, b2.x), fmaf((f.y - mean) * rstd, g2.y, b2.y));
+            const float2 f = Ops::unpack(xw[q]);
+            o[4 * j + q] = Ops::pack(fmaf(fmaf(f.x, rstd, nmr), g[2 * q], b[2 * q]),
+                                     fmaf(fmaf(f.y, rstd, nmr), g[2 * q + 1], b[2 * q + 1]));
         }
     }
 }

@@ -69,6 +69,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     const uint32_t slot_addr = sbase + C::OFF_SLOT;
     float* rowscale = reinterpret_cast<float*>(smem + C::OFF_ROWSCALE);  // [2][128]
     auto gb_slot = [&](int s) { return sbase + C::OFF_GB + 256u * s; };  // gamma | beta slices
+    auto gbf_slot = [&](int s) { return sbase + C::OFF_GBF + 512u * s; };  // the same in fp32 (LayerNorm)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -130,30 +131,24 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
             for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
                 const int m0 = (tile % p.num_m_blocks) * kBM;
                 const int n0 = (tile / p.num_m_blocks) * BN;
-                const int passes = PRO == PRO_LN ? 2 : 1;
-                for (int pass = 0; ok && pass < passes; ++pass) {
-                    const bool stats = PRO == PRO_LN && pass == 0;
-                    for (int kb = 0; kb < nk; ++kb) {
-                        if (!wait_bar(empty_bar(s), ph ^ 1u, p.status, p.timeout_ns, 1)) {
-                            ok = false;
-                            break;
-                        }
-                        mbar_arrive_expect_tx(full_bar(s), stats ? (uint32_t)C::A_BYTES : main_bytes);
-                        tma_load_2d(stage_a(s), &p.tmA, full_bar(s), kb * kBK, m0);
-                        if (!stats) {
-                            tma_load_2d(stage_b(s), &p.tmB, full_bar(s), kb * kBK, n0);
-                            if (DUAL) tma_load_2d(stage_b2(s), &p.tmB2, full_bar(s), kb * kBK, n0);
-                            if (PRO != PRO_NONE) {
-                                tma_load_2d(gb_slot(s), &p.tmGamma, full_bar(s), kb * kBK, 0);
-                                if (PRO == PRO_LN && p.beta != nullptr)
-                                    tma_load_2d(gb_slot(s) + 128, &p.tmBeta, full_bar(s), kb * kBK, 0);
-                            }
-                        }
-                        ++issued;
-                        if (++s == S) {
-                            s = 0;
-                            ph ^= 1u;
-                        }
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!wait_bar(empty_bar(s), ph ^ 1u, p.status, p.timeout_ns, 1)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full_bar(s), main_bytes);
+                    tma_load_2d(stage_a(s), &p.tmA, full_bar(s), kb * kBK, m0);
+                    tma_load_2d(stage_b(s), &p.tmB, full_bar(s), kb * kBK, n0);
+                    if (DUAL) tma_load_2d(stage_b2(s), &p.tmB2, full_bar(s), kb * kBK, n0);
+                    if (PRO != PRO_NONE) {
+                        tma_load_2d(gb_slot(s), &p.tmGamma, full_bar(s), kb * kBK, 0);
+                        if (PRO == PRO_LN && p.beta != nullptr)
+                            tma_load_2d(gb_slot(s) + 128, &p.tmBeta, full_bar(s), kb * kBK, 0);
+                    }
+                    ++issued;
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
                     }
                 }
             }
@@ -174,21 +169,6 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
             for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
                 const int buf = it & 1;
                 const uint32_t tph = (it >> 1) & 1;
-                if (PRO == PRO_LN) {
-                    // statistics pass: the transform warps read these stages; release them
-                    for (int kb = 0; kb < nk; ++kb) {
-                        if (!wait_bar(xform_bar(s), ph, p.status, p.timeout_ns, 2)) {
-                            ok = false;
-                            break;
-                        }
-                        mbar_arrive(empty_bar(s));
-                        if (++s == S) {
-                            s = 0;
-                            ph ^= 1u;
-                        }
-                    }
-                    if (!ok) break;
-                }
                 if (!wait_bar(tempty_bar(buf), tph ^ 1u, p.status, p.timeout_ns, 3)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(buf * C::ACC_COLS);
@@ -237,32 +217,28 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         int it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
-            float mean = 0.f, rstd = 1.f;
+            float rstd = 1.f, nmr = 0.f;  // LayerNorm: 1/std and -mean/std of row t
             float ss[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) ss[i] = 0.f;
             if (PRO == PRO_LN) {
-                ShiftedSums sums{0.f, 0.f, 0.f, 0.f};
-                for (int kb = 0; kb < nk; ++kb) {
-                    if (!wait_bar(full_bar(s), ph, p.status, p.timeout_ns, 5)) {
-                        ok = false;
-                        break;
-                    }
-                    ln_sums_row<DT>(stage_a(s), t, min(8, (p.K - kb * kBK) / 8), sums);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(xform_bar(s));
-                    if (++s == S) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
+                const int row = (tile % p.num_m_blocks) * kBM + t;
+                if (row < p.M) {
+                    const float2 st = reinterpret_cast<const float2*>(p.ln_stats)[row];
+                    rstd = st.y;
+                    nmr = -st.x * st.y;
                 }
-                if (!ok) break;
-                const RowMoments mo = ln_sums_moments(sums);
-                mean = mo.mean;
-                rstd = rsqrtf(mo.m2 / (float)p.K + p.eps);
             }
             for (int kb = 0; kb < nk; ++kb) {
-                if (!wait_bar(full_bar(s), ph, p.status, p.timeout_ns, 6)) {
+                bool got = wait_bar(full_bar(s), ph, p.status, p.timeout_ns, 6);
+                if (PRO == PRO_LN) {
+                    // widen this stage's gamma/beta; all 128 transform threads
+                    // meet here every step and agree whether the wait succeeded
+                    if (got) ln_widen_gb<DT>(gb_slot(s), gbf_slot(s), p.beta != nullptr, t);
+                    __syncwarp();
+                    got = named_bar_and(1, 128, got);
+                }
+                if (!got) {
                     ok = false;
                     break;
                 }
@@ -270,7 +246,8 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                 if (PRO == PRO_RMS)
                     fold_rms_row<DT>(stage_a(s), gb_slot(s), t, ss, o);
                 else
-                    fold_ln_row<DT>(stage_a(s), gb_slot(s), p.beta != nullptr, t, mean, rstd, o);
+                    fold_ln_row<DT>(stage_a(s), reinterpret_cast<const float4*>(smem + C::OFF_GBF + 512 * s), t, rstd,
+                                    nmr, o);
                 tmem_st_32x32b_x32(tmem_base + a_lane + A_COL0 + 32u * s, o);
                 tmem_st_wait();
                 tc_fence_before();
@@ -295,7 +272,6 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     } else if (PRO != PRO_NONE && warp >= 4 && warp < 8) {
         // ------------------------------------------------------------ transform
         const int t = threadIdx.x - 128;
-        const int j = t & 7;
         int s = 0;
         uint32_t ph = 0;
         int it = 0;
@@ -309,32 +285,15 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                 ss[i] = 0.f;
             }
             if (PRO == PRO_LN) {
-                // statistics pass over the row block (Chan merges, no cancellation)
-                ShiftedSums sums[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) sums[i] = ShiftedSums{0.f, 0.f, 0.f, 0.f};
-                for (int kb = 0; kb < nk; ++kb) {
-                    if (!wait_bar(full_bar(s), ph, p.status, p.timeout_ns, 5)) {
-                        ok = false;
-                        break;
-                    }
-                    ln_sums_stage<DT>(stage_a(s), t, 8, kb * kBK + j * 8 < p.K, sums);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(xform_bar(s));
-                    if (++s == S) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
-                }
-                if (!ok) break;
-                RowMoments mo[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mo[i] = ln_sums_moments(sums[i]);
-                ln_stats_allreduce(mo, 8);
+                // rows (t >> 3) + 16 i of the tile
+                const int r0 = (tile % p.num_m_blocks) * kBM + (t >> 3);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    mean[i] = mo[i].mean;
-                    rstd[i] = rsqrtf(mo[i].m2 / (float)p.K + p.eps);
+                    if (r0 + 16 * i < p.M) {
+                        const float2 st = reinterpret_cast<const float2*>(p.ln_stats)[r0 + 16 * i];
+                        mean[i] = st.x;
+                        rstd[i] = st.y;
+                    }
                 }
             }
             for (int kb = 0; kb < nk; ++kb) {
@@ -365,7 +324,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
 #pragma unroll
                 for (int i = 0; i < 8; ++i) ss[i] = row_allreduce8(ss[i]);
                 if (!wait_bar(tempty_bar(buf), tph ^ 1u, p.status, p.timeout_ns, 7)) break;
-                if (j == 0) {
+                if ((t & 7) == 0) {
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
                         rowscale[buf * kBM + (t >> 3) + 16 * i] = rsqrtf(ss[i] / (float)p.K + p.eps);

@@ -63,6 +63,9 @@ struct DeviceInfo {
     int sms = 0;
     int major = 0, minor = 0;
     int* status = nullptr;  // device address of g_fl_status
+    // stream-ordered pool for per-call scratch (LayerNorm row statistics);
+    // the library's own, so the process's default pool keeps its settings
+    cudaMemPool_t pool = nullptr;
 };
 constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
@@ -85,6 +88,15 @@ fl_status device_info(DeviceInfo** out) {
             d.minor = prop.minor;
             e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_fl_status);
             if (e != cudaSuccess) return fail(FL_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+            cudaMemPoolProps props = {};
+            props.allocType = cudaMemAllocationTypePinned;
+            props.location.type = cudaMemLocationTypeDevice;
+            props.location.id = dev;
+            e = cudaMemPoolCreate(&d.pool, &props);
+            if (e != cudaSuccess) return fail(FL_ERR_CUDA, "cudaMemPoolCreate: %s", cudaGetErrorString(e));
+            // keep freed scratch in the pool instead of returning it at every synchronisation
+            uint64_t keep = 64ull << 20;
+            cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
             d.ready = true;
         }
     }
@@ -349,11 +361,12 @@ bool use_pair(int dt, int pro, int M, int N, int K, PairPlan* plan) {
 }
 
 fl_status run_pair(int dt, int pro, const void* A, const void* W, const void* bias, const void* residual,
-                   const void* gamma, const void* beta, void* out, int M, int N, int K, int act, float eps,
-                   const PairPlan& plan, DeviceInfo* di, cudaStream_t stream) {
+                   const void* gamma, const void* beta, const void* ln_stats, void* out, int M, int N, int K, int act,
+                   float eps, const PairPlan& plan, DeviceInfo* di, cudaStream_t stream) {
     const int bn = plan.bn;
     GemmParams p;
     memset(&p, 0, sizeof(p));
+    p.ln_stats = ln_stats;
     fl_status st;
     if ((st = encode_2d(&p.tmA, dt, A, K, M, fl::kBK, fl::kBM)) != FL_OK) return st;
     if ((st = encode_2d(&p.tmB, dt, W, K, N, fl::kBK, bn / 2)) != FL_OK) return st;
@@ -404,10 +417,11 @@ int choose_bn(int M, int N, bool dual, int sms) {
 }
 
 fl_status run_splitk(int dt, int pro, const void* A, const void* W, const void* bias, const void* residual,
-                     const void* gamma, const void* beta, void* out, int M, int N, int K, int act, float eps,
-                     const SplitPlan& plan, DeviceInfo* di, cudaStream_t stream) {
+                     const void* gamma, const void* beta, const void* ln_stats, void* out, int M, int N, int K,
+                     int act, float eps, const SplitPlan& plan, DeviceInfo* di, cudaStream_t stream) {
     GemmParams p;
     memset(&p, 0, sizeof(p));
+    p.ln_stats = ln_stats;
     const int a_rows = plan.a_rows;
     fl_status st;
     if ((st = encode_2d(&p.tmA, dt, A, K, M, fl::kBK, a_rows)) != FL_OK) return st;
@@ -460,21 +474,22 @@ fl_status run_splitk(int dt, int pro, const void* A, const void* W, const void* 
     return ok();
 }
 
-fl_status run_tile(int dt, int pro, bool dual, const void* A, const void* W, const void* W2, const void* bias,
-                   const void* residual, const void* gamma, const void* beta, void* out, int M, int N, int K, int act,
-                   float eps, cudaStream_t stream) {
-    DeviceInfo* di = nullptr;
-    fl_status st = device_info(&di);
-    if (st != FL_OK) return st;
+fl_status run_kernels(int dt, int pro, bool dual, const void* A, const void* W, const void* W2, const void* bias,
+                      const void* residual, const void* gamma, const void* beta, const void* ln_stats, void* out, int M,
+                      int N, int K, int act, float eps, DeviceInfo* di, cudaStream_t stream) {
+    fl_status st;
     PairPlan pplan;
     if (!dual && use_pair(dt, pro, M, N, K, &pplan))
-        return run_pair(dt, pro, A, W, bias, residual, gamma, beta, out, M, N, K, act, eps, pplan, di, stream);
+        return run_pair(dt, pro, A, W, bias, residual, gamma, beta, ln_stats, out, M, N, K, act, eps, pplan, di,
+                        stream);
     SplitPlan plan;
     if (!dual && plan_splitk(dt, pro, M, N, K, di->sms, &plan))
-        return run_splitk(dt, pro, A, W, bias, residual, gamma, beta, out, M, N, K, act, eps, plan, di, stream);
+        return run_splitk(dt, pro, A, W, bias, residual, gamma, beta, ln_stats, out, M, N, K, act, eps, plan, di,
+                          stream);
     const int bn = choose_bn(M, N, dual, di->sms);
     GemmParams p;
     memset(&p, 0, sizeof(p));
+    p.ln_stats = ln_stats;
     if ((st = encode_2d(&p.tmA, dt, A, K, M, fl::kBK, fl::kBM)) != FL_OK) return st;
     if ((st = encode_2d(&p.tmB, dt, W, K, N, fl::kBK, bn)) != FL_OK) return st;
     if (dual && (st = encode_2d(&p.tmB2, dt, W2, K, N, fl::kBK, bn)) != FL_OK) return st;
@@ -502,6 +517,30 @@ fl_status run_tile(int dt, int pro, bool dual, const void* A, const void* W, con
     cudaError_t e = dispatch_tile(dt, bn, pro, dual, p, grid, stream);
     if (e != cudaSuccess) return fail(FL_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
     return ok();
+}
+
+// One fused call. LayerNorm first computes the row statistics (8 bytes per
+// row of stream-ordered scratch from the library pool, freed on the stream
+// right after the GEMM kernel that reads them).
+fl_status run_tile(int dt, int pro, bool dual, const void* A, const void* W, const void* W2, const void* bias,
+                   const void* residual, const void* gamma, const void* beta, void* out, int M, int N, int K, int act,
+                   float eps, cudaStream_t stream) {
+    DeviceInfo* di = nullptr;
+    fl_status st = device_info(&di);
+    if (st != FL_OK) return st;
+    void* stats = nullptr;
+    if (pro == fl::PRO_LN) {
+        cudaError_t e = cudaMallocFromPoolAsync(&stats, (size_t)M * 8, di->pool, stream);
+        if (e != cudaSuccess) return fail(FL_ERR_CUDA, "LayerNorm statistics scratch: %s", cudaGetErrorString(e));
+        e = fl::launch_ln_stats(dt, A, M, K, eps, stats, g_opt_pdl.load(), stream);
+        if (e != cudaSuccess) {
+            cudaFreeAsync(stats, stream);
+            return fail(FL_ERR_CUDA, "LayerNorm statistics kernel launch failed: %s", cudaGetErrorString(e));
+        }
+    }
+    st = run_kernels(dt, pro, dual, A, W, W2, bias, residual, gamma, beta, stats, out, M, N, K, act, eps, di, stream);
+    if (stats != nullptr) cudaFreeAsync(stats, stream);
+    return st;
 }
 
 // Common shape checks of one GEMM [M,K] x [N,K]^T.

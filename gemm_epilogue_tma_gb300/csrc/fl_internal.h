@@ -33,7 +33,8 @@ struct GemmParams {
     const void* residual;  // [M, N] or null
     const void* gamma;     // [K] (norm prologues)
     const void* beta;      // [K] or null (LayerNorm)
-    const void* a_ptr;     // activation [M, K] (LayerNorm statistics of the split-K kernel)
+    const void* a_ptr;     // activation [M, K]
+    const void* ln_stats;  // LayerNorm: float2 (mean, 1/sqrt(var + eps)) per activation row
     void* out_ptr;         // output [M, N] (split-K kernel stores directly)
     int* status;           // device status word
     unsigned long long timeout_ns;
@@ -61,6 +62,10 @@ struct GemmParams {
 
 // Records a status message for fl_last_error() on this thread; returns status.
 int set_last_error(int status, const char* message);
+
+// LayerNorm row statistics of x [M, K] into stats (M float2: mean, rstd).
+cudaError_t launch_ln_stats(int dt, const void* x, int M, int K, float eps, void* stats, int pdl,
+                            cudaStream_t stream);
 
 // Kernel launchers, explicitly instantiated in the kernel translation units.
 template <int DT, int BN, int PRO, bool DUAL>
@@ -93,8 +98,7 @@ struct SplitCfg {
     static constexpr int OFF_BAR = 0;
     static constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_SS = (OFF_SLOT + 16 + 15) / 16 * 16;   // [128] partial sum of squares
-    static constexpr int OFF_LN = OFF_SS + kBM * 4;                 // [128] float2 mean, rstd
-    static constexpr int OFF_GB = (OFF_LN + kBM * 8 + 127) / 128 * 128;
+    static constexpr int OFF_GB = (OFF_SS + kBM * 4 + 127) / 128 * 128;
     static constexpr int OFF_RING = (OFF_GB + MAX_STAGES * 256 + 1023) / 1024 * 1024;
     // Ring budgets: two CTAs per SM, else one.
     static constexpr int RING_SMALL = 100 * 1024;
@@ -150,7 +154,8 @@ struct TileCfg {
     static constexpr int OFF_ROWSCALE = (OFF_SLOT + 16 + 15) / 16 * 16;
     // per stage: the gamma and beta slices of the K block (64 x 2 B each)
     static constexpr int OFF_GB = (OFF_ROWSCALE + 2 * kBM * 4 + 127) / 128 * 128;
-    static constexpr int SMEM_BYTES = OFF_GB + STAGES * 256 + 1024;  // + alignment slack
+    static constexpr int OFF_GBF = OFF_GB + STAGES * 256;  // LayerNorm: gamma | beta widened to fp32
+    static constexpr int SMEM_BYTES = OFF_GBF + STAGES * 512 + 1024;  // + alignment slack
 };
 
 }  // namespace fl

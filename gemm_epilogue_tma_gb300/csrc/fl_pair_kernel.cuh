@@ -48,13 +48,20 @@ struct PairCfg {
     static constexpr int EPI_BUF_BYTES = 32 * 128;
     static constexpr int OFF_EPI = STAGES * STAGE_BYTES;
     static constexpr int OFF_BAR = OFF_EPI + 4 * EPI_BUF_BYTES;
-    static constexpr int NUM_BARS = 4 * STAGES + 11;
-    // split-K exchange: the K-partner's half of the partial tile, fp32 rows
-    // padded against bank conflicts, written into this CTA's (idle) ring
-    static constexpr int RECV_STRIDE = BN / 2 + 4;
-    static constexpr int OFF_RECV_SS = kBM * RECV_STRIDE * 4;
-    static constexpr int XCHG_BYTES = OFF_RECV_SS + kBM * 4;  // partial half + row sums of squares
-    static constexpr int OFF_SEND = 96 * 1024;                 // outgoing copy, same layout
+    // split-K exchange: the K-partner's half of the partial tile, written into
+    // this CTA's (idle) ring in 32-column chunks, each as four 32-row blocks
+    // (one per epilogue warp, one bulk copy each), so the receiver finishes a
+    // chunk while the next is in flight. A block row is 32 fp32 values plus 4
+    // words (the first carries the row's partial sum of squares in chunk 0):
+    // 36 words keep rows on distinct banks for 16-byte accesses.
+    static constexpr int XCOLS = 32;
+    static constexpr int NCHUNK = BN / 2 / XCOLS;
+    static constexpr int XROW = XCOLS + 4;                      // words per block row
+    static constexpr int XBLOCK = 32 * XROW * 4;                // one warp's rows of one chunk
+    static constexpr int XCHUNK = 4 * XBLOCK;
+    static constexpr int XCHG_BYTES = NCHUNK * XCHUNK;
+    static constexpr int OFF_SEND = 96 * 1024;                  // outgoing blocks, same layout
+    static constexpr int NUM_BARS = 4 * STAGES + 10 + 4 * NCHUNK;
     static_assert(KS == 1 || OFF_SEND + XCHG_BYTES <= STAGES * STAGE_BYTES, "exchange buffers fit in the ring");
     static_assert(XCHG_BYTES <= OFF_SEND && XCHG_BYTES % 16 == 0, "exchange layout");
     // second set of epilogue staging buffers (split-K: the ring is idle by then)
@@ -63,9 +70,8 @@ struct PairCfg {
     static constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_ROWSCALE = (OFF_SLOT + 16 + 15) / 16 * 16;
     static constexpr int OFF_GB = (OFF_ROWSCALE + 2 * kBM * 4 + 127) / 128 * 128;
-    // split-K LayerNorm: row moments (n, mean, m2) sent by the K-partner
-    static constexpr int OFF_LNX = OFF_GB + STAGES * 256;
-    static constexpr int SMEM_BYTES = OFF_LNX + kBM * 12 + 1024;
+    static constexpr int OFF_GBF = OFF_GB + STAGES * 256;  // LayerNorm: gamma | beta widened to fp32
+    static constexpr int SMEM_BYTES = OFF_GBF + (PRO == PRO_LN ? STAGES * 512 : 0) + 1024;
     static_assert(!ATMEM || A_COL0 + 32 * STAGES <= TMEM_COLS, "activation slots must fit in tensor memory");
 };
 
@@ -98,11 +104,12 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     const uint32_t drain_bar = bar0 + 8u * (4 * S + 6);
     const uint32_t tdone_bar = bar0 + 8u * (4 * S + 7);  // this CTA's epilogue finished a tile
     const uint32_t ringfree_bar = bar0 + 8u * (4 * S + 8);  // split-K: the K-partner may write my ring
-    const uint32_t recvd_bar = bar0 + 8u * (4 * S + 9);     // split-K: the K-partner's half has arrived
-    const uint32_t lnx_bar = bar0 + 8u * (4 * S + 10);      // split-K LayerNorm: partner's row moments arrived
+    // split-K: block (warp q, chunk c) of the K-partner's half has arrived
+    auto recvd_bar = [&](int q, int c) { return bar0 + 8u * (4 * S + 10 + q * C::NCHUNK + c); };
     const uint32_t slot_addr = sbase + C::OFF_SLOT;
     float* rowscale = reinterpret_cast<float*>(smem + C::OFF_ROWSCALE);
     auto gb_slot = [&](int s) { return sbase + C::OFF_GB + 256u * s; };
+    auto gbf_slot = [&](int s) { return sbase + C::OFF_GBF + 512u * s; };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -120,8 +127,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     const int kb_end = KS == 2 ? min(nk, kb_begin + p.kps) : nk;
     // KS = 1: each persistent pair takes a contiguous range of tiles in
     // row-block-major order, so consecutive tiles mostly share their activation
-    // rows (LayerNorm statistics are then computed once per row block);
-    // KS = 2: one tile per cluster.
+    // rows; KS = 2: one tile per cluster.
     const int npairs = KS == 2 ? p.num_tiles : (int)gridDim.x / 2;
     const int pair = KS == 2 ? (int)blockIdx.x / 4 : (int)blockIdx.x / 2;
     int t_begin = pair, t_end = pair + 1;
@@ -132,7 +138,6 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     }
     auto tile_mb = [&](int t) { return t / p.num_n_blocks; };
     auto tile_nb = [&](int t) { return t % p.num_n_blocks; };
-    auto needs_stats = [&](int t) { return PRO == PRO_LN && (t == t_begin || tile_mb(t) != tile_mb(t - 1)); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -149,8 +154,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         mbar_init(drain_bar, 1);
         mbar_init(tdone_bar, 4);
         mbar_init(ringfree_bar, 4);
-        mbar_init(recvd_bar, 1);
-        mbar_init(lnx_bar, 4);
+        for (int i = 0; i < 4 * C::NCHUNK; ++i) mbar_init(recvd_bar(i / C::NCHUNK, i % C::NCHUNK), 1);
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -190,41 +194,30 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
             for (int tile = t_begin; ok && tile < t_end; ++tile) {
                 const int m0 = tile_mb(tile) * 2 * kBM + (int)rank * kBM;
                 const int nh = tile_nb(tile) * C::BN + (int)rank * C::HALF;
-                const int passes = needs_stats(tile) ? 2 : 1;
-                for (int pass = 0; ok && pass < passes; ++pass) {
-                    const bool stats = passes == 2 && pass == 0;
-                    // statistics cover the whole row, or this pair's K half when the
-                    // K-partner supplies the other half's moments
-                    const int k0 = (stats && KS == 1) ? 0 : kb_begin, k1 = (stats && KS == 1) ? nk : kb_end;
-                    for (int kb = k0; kb < k1; ++kb) {
-                        if (!wait_bar(empty_bar(s), ph ^ 1u, p.status, p.timeout_ns, 31)) {
-                            ok = false;
-                            break;
-                        }
-                        if (stats) {
-                            mbar_arrive_expect_tx(afull_bar(s), (uint32_t)C::A_BYTES);
-                            tma_load_2d(stage_a(s), &p.tmA, afull_bar(s), kb * kBK, m0);
-                            if (leader) mbar_arrive(full_bar(s));  // keeps full's phases in step with the ring
-                        } else if (PRO == PRO_NONE) {
-                            if (leader) mbar_arrive_expect_tx(full_bar(s), 2u * C::STAGE_BYTES);
-                            const uint32_t fb = lead(full_bar(s));
-                            tma_load_2d_pair(stage_a(s), &p.tmA, fb, kb * kBK, m0);
-                            tma_load_2d_pair(stage_b(s), &p.tmB, fb, kb * kBK, nh);
-                        } else {
-                            mbar_arrive_expect_tx(afull_bar(s), (uint32_t)C::A_BYTES + gb_bytes);
-                            tma_load_2d(stage_a(s), &p.tmA, afull_bar(s), kb * kBK, m0);
-                            tma_load_2d(gb_slot(s), &p.tmGamma, afull_bar(s), kb * kBK, 0);
-                            if (PRO == PRO_LN && p.beta != nullptr)
-                                tma_load_2d(gb_slot(s) + 128, &p.tmBeta, afull_bar(s), kb * kBK, 0);
-                            if (leader) mbar_arrive_expect_tx(full_bar(s), 2u * C::B_BYTES);
-                            tma_load_2d_pair(stage_b(s), &p.tmB, lead(full_bar(s)), kb * kBK, nh);
-                        }
-                        if (issued == 0) FL_MARK(p, 2);
-                        ++issued;
-                        if (++s == S) {
-                            s = 0;
-                            ph ^= 1u;
-                        }
+                for (int kb = kb_begin; kb < kb_end; ++kb) {
+                    if (!wait_bar(empty_bar(s), ph ^ 1u, p.status, p.timeout_ns, 31)) {
+                        ok = false;
+                        break;
+                    }
+                    if (PRO == PRO_NONE) {
+                        if (leader) mbar_arrive_expect_tx(full_bar(s), 2u * C::STAGE_BYTES);
+                        const uint32_t fb = lead(full_bar(s));
+                        tma_load_2d_pair(stage_a(s), &p.tmA, fb, kb * kBK, m0);
+                        tma_load_2d_pair(stage_b(s), &p.tmB, fb, kb * kBK, nh);
+                    } else {
+                        mbar_arrive_expect_tx(afull_bar(s), (uint32_t)C::A_BYTES + gb_bytes);
+                        tma_load_2d(stage_a(s), &p.tmA, afull_bar(s), kb * kBK, m0);
+                        tma_load_2d(gb_slot(s), &p.tmGamma, afull_bar(s), kb * kBK, 0);
+                        if (PRO == PRO_LN && p.beta != nullptr)
+                            tma_load_2d(gb_slot(s) + 128, &p.tmBeta, afull_bar(s), kb * kBK, 0);
+                        if (leader) mbar_arrive_expect_tx(full_bar(s), 2u * C::B_BYTES);
+                        tma_load_2d_pair(stage_b(s), &p.tmB, lead(full_bar(s)), kb * kBK, nh);
+                    }
+                    if (issued == 0) FL_MARK(p, 2);
+                    ++issued;
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
                     }
                 }
             }
@@ -248,23 +241,6 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
             for (int tile = t_begin; ok && tile < t_end; ++tile, ++it) {
                 const int buf = C::NBUF == 2 ? (it & 1) : 0;
                 const uint32_t tph = C::NBUF == 2 ? (uint32_t)((it >> 1) & 1) : (uint32_t)(it & 1);
-                if (needs_stats(tile)) {
-                    // statistics pass: both CTAs' fold warps read these stages; release them in both
-                    for (int kb = KS == 1 ? 0 : kb_begin; kb < (KS == 1 ? nk : kb_end); ++kb) {
-                        if (!wait_bar_cluster(xform_bar(s), ph, p.status, p.timeout_ns, 32) ||
-                            !wait_bar(full_bar(s), ph, p.status, p.timeout_ns, 33)) {
-                            ok = false;
-                            break;
-                        }
-                        mbar_arrive(empty_bar(s));
-                        mbar_arrive_cluster(mapa_cluster(empty_bar(s), crank ^ 1u));
-                        if (++s == S) {
-                            s = 0;
-                            ph ^= 1u;
-                        }
-                    }
-                    if (!ok) break;
-                }
                 if (!wait_bar_cluster(tempty_bar(buf), tph ^ 1u, p.status, p.timeout_ns, 34)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(buf * C::ACC_COLS);
@@ -311,54 +287,29 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         uint32_t ph = 0;
         int it = 0;
         bool ok = true;
-        float mean = 0.f, rstd = 1.f;  // LayerNorm statistics of the current row block
         for (int tile = t_begin; ok && tile < t_end; ++tile, ++it) {
             float ss[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) ss[i] = 0.f;
-            if (needs_stats(tile)) {
-                // row t's moments by shifted sums (one pass, no division per K block)
-                ShiftedSums sums{0.f, 0.f, 0.f, 0.f};
-                const int sk0 = KS == 1 ? 0 : kb_begin, sk1 = KS == 1 ? nk : kb_end;
-                for (int kb = sk0; kb < sk1; ++kb) {
-                    if (!wait_bar(afull_bar(s), ph, p.status, p.timeout_ns, 37)) {
-                        ok = false;
-                        break;
-                    }
-                    ln_sums_row<DT>(stage_a(s), t, min(8, (p.K - kb * kBK) / 8), sums);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster(lead(xform_bar(s)));
-                    if (++s == S) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
+            float rstd = 1.f, nmr = 0.f;  // LayerNorm: 1/std and -mean/std of row t of this tile
+            if (PRO == PRO_LN) {
+                const int row = tile_mb(tile) * 2 * kBM + (int)rank * kBM + t;
+                if (row < p.M) {
+                    const float2 st = reinterpret_cast<const float2*>(p.ln_stats)[row];
+                    rstd = st.y;
+                    nmr = -st.x * st.y;
                 }
-                if (!ok) break;
-                RowMoments mo = ln_sums_moments(sums);
-                if (KS == 2) {
-                    // send this K half's moments to the K-partner, merge with its half
-                    float* lnx = reinterpret_cast<float*>(smem + C::OFF_LNX);
-                    const uint32_t partner = crank ^ 2u;
-                    const uint32_t a = mapa_cluster(smem_u32(lnx + t * 3), partner);
-                    st_cluster_f32(a, mo.n);
-                    st_cluster_f32(a + 4, mo.mean);
-                    st_cluster_f32(a + 8, mo.m2);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_release_cluster(mapa_cluster(lnx_bar, partner));
-                    if (!wait_bar_acquire_cluster(lnx_bar, 0, p.status, p.timeout_ns, 46)) {
-                        ok = false;
-                        break;
-                    }
-                    const RowMoments other{lnx[t * 3], lnx[t * 3 + 1], lnx[t * 3 + 2]};
-                    // the lower K half first, so both pairs get the same bits
-                    mo = khalf == 0 ? merge_moments(mo, other) : merge_moments(other, mo);
-                }
-                mean = mo.mean;
-                rstd = rsqrtf(mo.m2 / (float)p.K + p.eps);
-                if (t == 0 && it == 0) FL_MARK(p, 11);
             }
             for (int kb = kb_begin; kb < kb_end; ++kb) {
-                if (!wait_bar(afull_bar(s), ph, p.status, p.timeout_ns, 38)) {
+                bool got = wait_bar(afull_bar(s), ph, p.status, p.timeout_ns, 38);
+                if (PRO == PRO_LN) {
+                    // widen this stage's gamma/beta; all 128 fold threads meet
+                    // here every step and agree whether the wait succeeded
+                    if (got) ln_widen_gb<DT>(gb_slot(s), gbf_slot(s), p.beta != nullptr, t);
+                    __syncwarp();
+                    got = named_bar_and(1, 128, got);
+                }
+                if (!got) {
                     ok = false;
                     break;
                 }
@@ -366,7 +317,8 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                 if (PRO == PRO_RMS)
                     fold_rms_row<DT>(stage_a(s), gb_slot(s), t, ss, o);
                 else
-                    fold_ln_row<DT>(stage_a(s), gb_slot(s), p.beta != nullptr, t, mean, rstd, o);
+                    fold_ln_row<DT>(stage_a(s), reinterpret_cast<const float4*>(smem + C::OFF_GBF + 512 * s), t, rstd,
+                                    nmr, o);
                 if (t == 0 && kb == kb_begin && it == 0) FL_MARK(p, 10);
                 tmem_st_32x32b_x32(tmem_base + a_lane + (uint32_t)C::A_COL0 + 32u * s, o);
                 tmem_st_wait();
@@ -408,7 +360,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         const int n0 = tile_nb(tile) * C::BN;
         const int own_c0 = khalf * HALF_N, oth_c0 = (1 - khalf) * HALF_N;
         const uint32_t tl = tmem_base + ((uint32_t)(q * 32) << 16);
-        const uint32_t recv_row = sbase + (uint32_t)(rl * C::RECV_STRIDE) * 4u;
+        const uint32_t row_off = (uint32_t)(rl * C::XROW) * 4u;  // within a chunk
         using T = uint16_t;
         const T* bias = reinterpret_cast<const T*>(p.bias);
         const T* res = reinterpret_cast<const T*>(p.residual);
@@ -422,42 +374,38 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         }
         // this pair's MMAs are done, so this CTA's ring may take the partner's half
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(mapa_cluster(ringfree_bar, partner));
-        if (threadIdx.x == 32 * EPI_WARP0) mbar_arrive_expect_tx(recvd_bar, (uint32_t)C::XCHG_BYTES);
-        // stage the outgoing half (and the row's sum of squares) in this CTA's ring
-        if (ok) {
-            const uint32_t src_row = sbase + C::OFF_SEND + (uint32_t)(rl * C::RECV_STRIDE) * 4u;
+        if (lane == 0) {
+            mbar_arrive_cluster(mapa_cluster(ringfree_bar, partner));
+            for (int c = 0; c < C::NCHUNK; ++c) mbar_arrive_expect_tx(recvd_bar(q, c), (uint32_t)C::XBLOCK);
+        }
+        // ship the outgoing half chunk by chunk: each warp stages its rows and
+        // sends them with one bulk copy as soon as the partner's ring is free
+        bool peer_ready = false;
 #pragma unroll 1
-            for (int c = 0; c < HALF_N / 32; ++c) {
+        for (int c = 0; c < C::NCHUNK; ++c) {
+            const uint32_t blk = (uint32_t)(c * C::XCHUNK + q * C::XBLOCK);
+            if (ok) {
                 uint32_t v[32];
-                tmem_ld_32x32b_x32(tl + (uint32_t)(oth_c0 + 32 * c), v);
+                tmem_ld_32x32b_x32(tl + (uint32_t)(oth_c0 + C::XCOLS * c), v);
                 tmem_ld_wait();
+                const uint32_t src_row = sbase + C::OFF_SEND + (uint32_t)(c * C::XCHUNK) + row_off;
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                    st_shared_v4(src_row + (uint32_t)(32 * c + 4 * j) * 4u, v[4 * j], v[4 * j + 1], v[4 * j + 2],
-                                 v[4 * j + 3]);
+                    st_shared_v4(src_row + (uint32_t)(4 * j) * 4u, v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                if (PRO == PRO_RMS && c == 0) st_shared_f32(src_row + (uint32_t)C::XCOLS * 4u, ss_own);
             }
-            if (PRO == PRO_RMS)
-                *reinterpret_cast<volatile float*>(smem + C::OFF_SEND + C::OFF_RECV_SS + rl * 4) = ss_own;
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(2, 128);
-        if (ok && threadIdx.x == 32 * EPI_WARP0) {
-            // one bulk copy into the partner's receive buffer once its ring is free
-            if (wait_bar_cluster(ringfree_bar, 0, p.status, p.timeout_ns, 44)) {
-                bulk_copy_to_cluster(mapa_cluster(sbase, partner), sbase + C::OFF_SEND, (uint32_t)C::XCHG_BYTES,
-                                     mapa_cluster(recvd_bar, partner));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (ok && lane == 0) {
+                if (!peer_ready) peer_ready = wait_bar_cluster(ringfree_bar, 0, p.status, p.timeout_ns, 44);
+                if (peer_ready)
+                    bulk_copy_to_cluster(mapa_cluster(sbase + blk, partner), sbase + C::OFF_SEND + blk,
+                                         (uint32_t)C::XBLOCK, mapa_cluster(recvd_bar(q, c), partner));
             }
         }
         if (threadIdx.x == 32 * EPI_WARP0) FL_MARK(p, 6);
-        if (ok) ok = wait_bar(recvd_bar, 0, p.status, p.timeout_ns, 45);
-        if (threadIdx.x == 32 * EPI_WARP0) FL_MARK(p, 7);
         if (ok) {
             float rs = 1.f;
-            if (PRO == PRO_RMS) {
-                const float ss = ss_own + *reinterpret_cast<volatile float*>(smem + C::OFF_RECV_SS + rl * 4);
-                rs = rsqrtf(ss / (float)p.K + p.eps);
-            }
             const int row = m0 + rl;
             const bool row_ok = row < p.M;
             if (m0 + q * 32 < p.M) {
@@ -470,14 +418,21 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int cbase = col0 + h * 32;
-                        const int lc = c * 64 + h * 32;  // column within the own half
+                        const int xc = c * 2 + h;        // exchange chunk
+                        const int lc = xc * C::XCOLS;    // column within the own half
+                        const uint32_t recv_row = sbase + (uint32_t)(xc * C::XCHUNK) + row_off;
+                        if (!wait_bar_cluster(recvd_bar(q, xc), 0, p.status, p.timeout_ns, 45)) ok = false;
+                        if (PRO == PRO_RMS && xc == 0) {
+                            const float ss = ss_own + ld_shared_f32(recv_row + (uint32_t)C::XCOLS * 4u);
+                            rs = rsqrtf(fmaf(ss, 1.0f / (float)p.K, p.eps));
+                        }
                         uint32_t acc[32];
                         tmem_ld_32x32b_x32(tl + (uint32_t)(own_c0 + lc), acc);
                         tmem_ld_wait();
                         float v[32];
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
-                            const uint4 r4 = ld_shared_v4(recv_row + (uint32_t)(lc + 4 * j) * 4u);
+                            const uint4 r4 = ld_shared_v4(recv_row + (uint32_t)(4 * j) * 4u);
                             v[4 * j + 0] = (__uint_as_float(acc[4 * j + 0]) + __uint_as_float(r4.x)) * rs;
                             v[4 * j + 1] = (__uint_as_float(acc[4 * j + 1]) + __uint_as_float(r4.y)) * rs;
                             v[4 * j + 2] = (__uint_as_float(acc[4 * j + 2]) + __uint_as_float(r4.z)) * rs;
@@ -535,6 +490,11 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                 }
             }
         }
+        if (threadIdx.x == 32 * EPI_WARP0) FL_MARK(p, 13);
+        // every block of the partner's has landed (tiles cut by N skip chunks)
+        // before this CTA may reach the exit barrier
+        if (ok)
+            for (int c = 0; c < C::NCHUNK; ++c) wait_bar_cluster(recvd_bar(q, c), 0, p.status, p.timeout_ns, 46);
         if (lane == 0) bulk_wait_group_read<0>();  // global writes complete with the grid
     } else if (warp >= EPI_WARP0) {
         // ------------------------------------------------------------ epilogue (both CTAs)

@@ -21,9 +21,8 @@
 // in, waited on just before exit, so no CTA leaves while a peer may still
 // read or write its shared memory.
 //
-// LayerNorm needs the row statistics before the fold: the transform warps
-// compute them at the start from the activation rows (two passes over L2,
-// coalesced warp loads), which is cheap because the activation is small.
+// LayerNorm folds with row statistics computed once per call by a separate
+// small kernel (read here after the programmatic dependency resolves).
 #pragma once
 
 #include "fl_common.cuh"
@@ -59,12 +58,6 @@ __device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr) {
 __device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
     float v;
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
 }
 
@@ -109,7 +102,6 @@ __global__ void __launch_bounds__(splitk_threads<PRO>(), 1)
     const uint32_t recvd_bar = bar0 + 8u * (3 * S + 3);     // every peer's partial of my slice is here
     const uint32_t slot_addr = sbase + C::OFF_SLOT;
     float* ssbuf = reinterpret_cast<float*>(smem + C::OFF_SS);
-    float2* lnstat = reinterpret_cast<float2*>(smem + C::OFF_LN);
     auto gb_slot = [&](int s) { return sbase + C::OFF_GB + 256u * s; };
 
     const int warp = threadIdx.x >> 5;
@@ -258,38 +250,12 @@ __global__ void __launch_bounds__(splitk_threads<PRO>(), 1)
             ss[i] = 0.f;
         }
         if (PRO == PRO_LN) {
-            // statistics of the whole row: warp w takes rows w, w + 4, ...
-            const uint16_t* xg = reinterpret_cast<const uint16_t*>(p.a_ptr);
-            for (int r = warp - XF_WARP0; r < rows; r += 4) {
-                const uint16_t* xr = xg + (size_t)(m0 + r) * p.K;
-                float a = 0.f;
-                for (int k = lane * 8; k < p.K; k += 256) {
-                    const uint4 v = ldg_v4(xr + k);
-                    const float2 f0 = Ops::unpack(v.x), f1 = Ops::unpack(v.y), f2 = Ops::unpack(v.z),
-                                 f3 = Ops::unpack(v.w);
-                    a += ((f0.x + f0.y) + (f1.x + f1.y)) + ((f2.x + f2.y) + (f3.x + f3.y));
-                }
-                const float mu = warp_sum(a) / (float)p.K;
-                float q = 0.f;
-                for (int k = lane * 8; k < p.K; k += 256) {
-                    const uint4 v = ldg_v4(xr + k);
-                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 f = Ops::unpack(w4[e]);
-                        q = fmaf(f.x - mu, f.x - mu, q);
-                        q = fmaf(f.y - mu, f.y - mu, q);
-                    }
-                }
-                const float var = warp_sum(q) / (float)p.K;
-                if (lane == 0) lnstat[r] = make_float2(mu, rsqrtf(var + p.eps));
-            }
-            named_bar_sync(1, 128);
+            const float2* stats = reinterpret_cast<const float2*>(p.ln_stats);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int r = (t >> 3) + 16 * i;
                 if (i < ni && r < rows) {
-                    const float2 st = lnstat[r];
+                    const float2 st = stats[m0 + r];
                     mean[i] = st.x;
                     rstd[i] = st.y;
                 }

@@ -111,6 +111,13 @@ fl_status fl_gemm_epilogue(const void* A, const void* W, const void* bias, const
  * The RMS statistics are computed from the fp16/bf16 input in fp32; gamma is
  * folded into the staged operand (one rounding to the dtype) and 1/rms is
  * applied to the fp32 accumulator as a row scale.
+ * LayerNorm first runs a small statistics kernel on `stream` that writes each
+ * row's mean and 1/sqrt(var + eps) (fp32, shifted sums) to M * 8 bytes of
+ * scratch taken from a library-owned stream-ordered memory pool and freed on
+ * `stream` after the GEMM kernel; the GEMM kernel then folds
+ * (x - mean) * rstd * gamma + beta into its staged operand (one rounding).
+ * Works under CUDA graph capture; returns FL_ERR_CUDA if the scratch cannot
+ * be allocated.
  */
 fl_status fl_norm_gemm(const void* x, const void* gamma, const void* beta, const void* W,
                        const void* bias, void* out, int M, int N, int K, float eps,

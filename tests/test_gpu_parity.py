@@ -356,6 +356,37 @@ def test_decode_sweep_rmsnorm_all_elements(dt, D, M):
 
 
 @pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("shape", [(200, 264, 520), (512, 512, 1024), (1, 128, 256)], ids=lambda s: "x".join(map(str, s)))
+def test_layernorm_captured_in_cuda_graph(dt, shape):
+    """LayerNorm takes stream-ordered scratch for its row statistics: it must
+    capture into a CUDA graph and give the same result on every replay."""
+    M, N, K = shape
+    t = syn.norm_gemm_inputs(M, N, K, "layer", dt)
+    g = {k: dev(v) for k, v in t.items()}
+    out = torch.empty((M, N), dtype=g["x"].dtype, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fl.norm_gemm(g["x"], g["gamma"], g["W"], beta=g["beta"], out=out, eps=1e-5, norm="layer")
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        fl.norm_gemm(g["x"], g["gamma"], g["W"], beta=g["beta"], out=out, eps=1e-5, norm="layer")
+    ref = oracle.norm_gemm(f64(t["x"]), f64(t["gamma"]), f64(t["beta"]), f64(t["W"]), None, 1e-5, "layer")
+    first = None
+    for _ in range(3):
+        out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert_close(out, ref, dt, f"graph layernorm {dt} {shape}")
+        if first is None:
+            first = out.clone()
+        else:
+            assert torch.equal(out, first)
+    fl.device_status()
+
+
+@pytest.mark.parametrize("dt", DTYPES)
 @pytest.mark.parametrize("M,D", [(1, 4096), (16, 1024), (32, 2048), (128, 1024)])
 def test_weight_preload_chained_layers(dt, M, D):
     """Two decode layers back to back on one stream, the second reading the first's output.
