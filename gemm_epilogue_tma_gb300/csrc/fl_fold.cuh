@@ -129,53 +129,35 @@ __device__ __forceinline__ void fold_rms_row(uint32_t stage, uint32_t gamma_slic
     }
 }
 
-// LayerNorm, thread-per-row: gamma and beta of the K block are first widened
-// to fp32 once per stage (threads 0-31 take gamma, 32-63 beta, one 16-bit
-// pair each; zeros without beta), then every thread reads them back with
-// broadcast loads instead of unpacking all 64 columns itself. The caller
-// synchronises the 128 transform threads between the two steps.
-template <int DT>
-__device__ __forceinline__ void ln_widen_gb(uint32_t gb_slice, uint32_t gbf_slice, bool has_beta, int t) {
-    using Ops = DTypeOps<DT>;
-    if (t < 64) {
-        const bool beta = t >= 32;
-        const int i = t & 31;
-        float2 v = make_float2(0.f, 0.f);
-        if (!beta || has_beta) {
-            uint32_t w;
-            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w) : "r"(gb_slice + (beta ? 128u : 0u) + 4u * i));
-            v = Ops::unpack(w);
-        }
-        asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(gbf_slice + (beta ? 256u : 0u) + 8u * i), "f"(v.x),
-                     "f"(v.y)
-                     : "memory");
-    }
-}
-
-// Row t := (x - mean) * rstd * gamma + beta, as fma(fma(x, rstd, -mean * rstd),
-// gamma, beta) in fp32 (the fp32 error stays relative to |mean| * 2^-24,
-// far below the one rounding to the dtype). The row's eight chunks are all
-// requested before any is used, and gamma/beta (fp32, gbf[0..15] = gamma,
-// gbf[16..31] = beta as float4) are plain loads the compiler may schedule.
-template <int DT>
-__device__ __forceinline__ void fold_ln_row(uint32_t stage, const float4* gbf, int t, float rstd, float nmr,
-                                            uint32_t (&o)[32]) {
+// LayerNorm, thread-per-row: row t, chunks [J0, J0 + NJ) of the K block :=
+// fma(fma(x, rstd, -mean * rstd), gamma, beta) in fp32, one rounding to the
+// dtype (the fp32 error stays relative to |mean| * 2^-24, far below it).
+// Every shared-memory load (x, gamma, beta) is issued before any result is
+// used: under the TMA and MMA traffic of the main loop a load takes a few
+// hundred cycles, so the fold costs one such round, not one per chunk.
+template <int DT, int NJ, int J0>
+__device__ __forceinline__ void fold_ln_row(uint32_t stage, uint32_t gb_slice, bool has_beta, int t, float rstd,
+                                            float nmr, uint32_t (&o)[4 * NJ]) {
     using Ops = DTypeOps<DT>;
     const int sw = t & 7;
-    uint4 xv[8];
+    uint4 xv[NJ], gv[NJ], bv[NJ];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) xv[j] = ld_shared_v4(stage + t * 128 + ((j ^ sw) << 4));
+    for (int jj = 0; jj < NJ; ++jj) xv[jj] = ld_shared_v4(stage + t * 128 + (((J0 + jj) ^ sw) << 4));
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const float4 g0 = gbf[2 * j], g1 = gbf[2 * j + 1], b0 = gbf[16 + 2 * j], b1 = gbf[16 + 2 * j + 1];
-        const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-        const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-        const uint32_t xw[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+    for (int jj = 0; jj < NJ; ++jj) gv[jj] = ld_shared_v4(gb_slice + (J0 + jj) * 16);
+#pragma unroll
+    for (int jj = 0; jj < NJ; ++jj)
+        bv[jj] = has_beta ? ld_shared_v4(gb_slice + 128 + (J0 + jj) * 16) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int jj = 0; jj < NJ; ++jj) {
+        const uint32_t xw[4] = {xv[jj].x, xv[jj].y, xv[jj].z, xv[jj].w};
+        const uint32_t gw[4] = {gv[jj].x, gv[jj].y, gv[jj].z, gv[jj].w};
+        const uint32_t bw[4] = {bv[jj].x, bv[jj].y, bv[jj].z, bv[jj].w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const float2 f = Ops::unpack(xw[q]);
-            o[4 * j + q] = Ops::pack(fmaf(fmaf(f.x, rstd, nmr), g[2 * q], b[2 * q]),
-                                     fmaf(fmaf(f.y, rstd, nmr), g[2 * q + 1], b[2 * q + 1]));
+            const float2 f = Ops::unpack(xw[q]), g = Ops::unpack(gw[q]), b = Ops::unpack(bw[q]);
+            o[4 * jj + q] =
+                Ops::pack(fmaf(fmaf(f.x, rstd, nmr), g.x, b.x), fmaf(fmaf(f.y, rstd, nmr), g.y, b.y));
         }
     }
 }

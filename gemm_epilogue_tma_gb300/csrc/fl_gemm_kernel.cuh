@@ -69,7 +69,6 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     const uint32_t slot_addr = sbase + C::OFF_SLOT;
     float* rowscale = reinterpret_cast<float*>(smem + C::OFF_ROWSCALE);  // [2][128]
     auto gb_slot = [&](int s) { return sbase + C::OFF_GB + 256u * s; };  // gamma | beta slices
-    auto gbf_slot = [&](int s) { return sbase + C::OFF_GBF + 512u * s; };  // the same in fp32 (LayerNorm)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -230,24 +229,19 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                 }
             }
             for (int kb = 0; kb < nk; ++kb) {
-                bool got = wait_bar(full_bar(s), ph, p.status, p.timeout_ns, 6);
-                if (PRO == PRO_LN) {
-                    // widen this stage's gamma/beta; all 128 transform threads
-                    // meet here every step and agree whether the wait succeeded
-                    if (got) ln_widen_gb<DT>(gb_slot(s), gbf_slot(s), p.beta != nullptr, t);
-                    __syncwarp();
-                    got = named_bar_and(1, 128, got);
-                }
-                if (!got) {
+                if (!wait_bar(full_bar(s), ph, p.status, p.timeout_ns, 6)) {
                     ok = false;
                     break;
                 }
                 uint32_t o[32];
-                if (PRO == PRO_RMS)
+                if (PRO == PRO_RMS) {
                     fold_rms_row<DT>(stage_a(s), gb_slot(s), t, ss, o);
-                else
-                    fold_ln_row<DT>(stage_a(s), reinterpret_cast<const float4*>(smem + C::OFF_GBF + 512 * s), t, rstd,
-                                    nmr, o);
+                } else {
+                    uint32_t (&lo)[16] = *reinterpret_cast<uint32_t(*)[16]>(&o[0]);
+                    uint32_t (&hi)[16] = *reinterpret_cast<uint32_t(*)[16]>(&o[16]);
+                    fold_ln_row<DT, 4, 0>(stage_a(s), gb_slot(s), p.beta != nullptr, t, rstd, nmr, lo);
+                    fold_ln_row<DT, 4, 4>(stage_a(s), gb_slot(s), p.beta != nullptr, t, rstd, nmr, hi);
+                }
                 tmem_st_32x32b_x32(tmem_base + a_lane + A_COL0 + 32u * s, o);
                 tmem_st_wait();
                 tc_fence_before();

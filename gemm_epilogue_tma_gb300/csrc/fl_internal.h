@@ -154,8 +154,7 @@ struct TileCfg {
     static constexpr int OFF_ROWSCALE = (OFF_SLOT + 16 + 15) / 16 * 16;
     // per stage: the gamma and beta slices of the K block (64 x 2 B each)
     static constexpr int OFF_GB = (OFF_ROWSCALE + 2 * kBM * 4 + 127) / 128 * 128;
-    static constexpr int OFF_GBF = OFF_GB + STAGES * 256;  // LayerNorm: gamma | beta widened to fp32
-    static constexpr int SMEM_BYTES = OFF_GBF + STAGES * 512 + 1024;  // + alignment slack
+    static constexpr int SMEM_BYTES = OFF_GB + STAGES * 256 + 1024;  // + alignment slack
 };
 
 }  // namespace fl

@@ -70,8 +70,7 @@ struct PairCfg {
     static constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_ROWSCALE = (OFF_SLOT + 16 + 15) / 16 * 16;
     static constexpr int OFF_GB = (OFF_ROWSCALE + 2 * kBM * 4 + 127) / 128 * 128;
-    static constexpr int OFF_GBF = OFF_GB + STAGES * 256;  // LayerNorm: gamma | beta widened to fp32
-    static constexpr int SMEM_BYTES = OFF_GBF + (PRO == PRO_LN ? STAGES * 512 : 0) + 1024;
+    static constexpr int SMEM_BYTES = OFF_GB + STAGES * 256 + 1024;
     static_assert(!ATMEM || A_COL0 + 32 * STAGES <= TMEM_COLS, "activation slots must fit in tensor memory");
 };
 
@@ -84,6 +83,10 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     using Ops = DTypeOps<DT>;
     constexpr int S = C::STAGES;
     constexpr int EPI_WARP0 = PRO != PRO_NONE ? 8 : 4;
+    // LayerNorm with a single accumulator buffer: the epilogue warps, idle
+    // while a tile's MMAs run, fold the upper half (chunks 4-7) of every K
+    // block of that tile; the fold warps take chunks 0-3.
+    constexpr bool FOLD2 = PRO == PRO_LN && C::NBUF == 1;
     constexpr uint32_t IDESC = umma_idesc_f16(Ops::kFormat, 2 * kBM, C::BN);
 
     extern __shared__ uint8_t smem_raw[];
@@ -109,7 +112,6 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     const uint32_t slot_addr = sbase + C::OFF_SLOT;
     float* rowscale = reinterpret_cast<float*>(smem + C::OFF_ROWSCALE);
     auto gb_slot = [&](int s) { return sbase + C::OFF_GB + 256u * s; };
-    auto gbf_slot = [&](int s) { return sbase + C::OFF_GBF + 512u * s; };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -144,7 +146,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
             mbar_init(full_bar(s), 1);
             mbar_init(afull_bar(s), 1);
             mbar_init(empty_bar(s), 1);
-            mbar_init(xform_bar(s), 8);
+            mbar_init(xform_bar(s), FOLD2 ? 16 : 8);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar(b), 1);
@@ -182,6 +184,35 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     griddep_wait();
     if (threadIdx.x == 0) griddep_launch_dependents();
     if (threadIdx.x == 0) FL_MARK(p, 1);
+
+    // Epilogue warps' half of the LayerNorm fold for one tile (FOLD2): row rl,
+    // chunks 4-7 of each K block into the upper 16 columns of its TMEM slot.
+    // They walk the ring in the same order as the fold warps (fs, fph).
+    auto fold_upper = [&](int tile, int rl, int& fs, uint32_t& fph) -> bool {
+        const int row = tile_mb(tile) * 2 * kBM + (int)rank * kBM + rl;
+        float rstd = 1.f, nmr = 0.f;
+        if (row < p.M) {
+            const float2 st = reinterpret_cast<const float2*>(p.ln_stats)[row];
+            rstd = st.y;
+            nmr = -st.x * st.y;
+        }
+        const uint32_t a_lane = (uint32_t)(rl & ~31) << 16;
+        for (int kb = kb_begin; kb < kb_end; ++kb) {
+            if (!wait_bar(afull_bar(fs), fph, p.status, p.timeout_ns, 47)) return false;
+            uint32_t o[16];
+            fold_ln_row<DT, 4, 4>(stage_a(fs), gb_slot(fs), p.beta != nullptr, rl, rstd, nmr, o);
+            tmem_st_32x32b_x16(tmem_base + a_lane + (uint32_t)C::A_COL0 + 32u * fs + 16u, o);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0) mbar_arrive_cluster(lead(xform_bar(fs)));
+            if (++fs == S) {
+                fs = 0;
+                fph ^= 1u;
+            }
+        }
+        return true;
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer (both CTAs)
@@ -301,26 +332,29 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                 }
             }
             for (int kb = kb_begin; kb < kb_end; ++kb) {
-                bool got = wait_bar(afull_bar(s), ph, p.status, p.timeout_ns, 38);
-                if (PRO == PRO_LN) {
-                    // widen this stage's gamma/beta; all 128 fold threads meet
-                    // here every step and agree whether the wait succeeded
-                    if (got) ln_widen_gb<DT>(gb_slot(s), gbf_slot(s), p.beta != nullptr, t);
-                    __syncwarp();
-                    got = named_bar_and(1, 128, got);
-                }
-                if (!got) {
+                if (!wait_bar(afull_bar(s), ph, p.status, p.timeout_ns, 38)) {
                     ok = false;
                     break;
                 }
-                uint32_t o[32];
-                if (PRO == PRO_RMS)
-                    fold_rms_row<DT>(stage_a(s), gb_slot(s), t, ss, o);
-                else
-                    fold_ln_row<DT>(stage_a(s), reinterpret_cast<const float4*>(smem + C::OFF_GBF + 512 * s), t, rstd,
-                                    nmr, o);
-                if (t == 0 && kb == kb_begin && it == 0) FL_MARK(p, 10);
-                tmem_st_32x32b_x32(tmem_base + a_lane + (uint32_t)C::A_COL0 + 32u * s, o);
+                const uint32_t aslot = tmem_base + a_lane + (uint32_t)C::A_COL0 + 32u * s;
+                if (FOLD2) {
+                    uint32_t o[16];
+                    fold_ln_row<DT, 4, 0>(stage_a(s), gb_slot(s), p.beta != nullptr, t, rstd, nmr, o);
+                    if (t == 0 && kb == kb_begin && it == 0) FL_MARK(p, 10);
+                    tmem_st_32x32b_x16(aslot, o);
+                } else {
+                    uint32_t o[32];
+                    if (PRO == PRO_RMS) {
+                        fold_rms_row<DT>(stage_a(s), gb_slot(s), t, ss, o);
+                    } else {
+                        uint32_t (&lo)[16] = *reinterpret_cast<uint32_t(*)[16]>(&o[0]);
+                        uint32_t (&hi)[16] = *reinterpret_cast<uint32_t(*)[16]>(&o[16]);
+                        fold_ln_row<DT, 4, 0>(stage_a(s), gb_slot(s), p.beta != nullptr, t, rstd, nmr, lo);
+                        fold_ln_row<DT, 4, 4>(stage_a(s), gb_slot(s), p.beta != nullptr, t, rstd, nmr, hi);
+                    }
+                    if (t == 0 && kb == kb_begin && it == 0) FL_MARK(p, 10);
+                    tmem_st_32x32b_x32(aslot, o);
+                }
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
@@ -364,7 +398,13 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         using T = uint16_t;
         const T* bias = reinterpret_cast<const T*>(p.bias);
         const T* res = reinterpret_cast<const T*>(p.residual);
-        bool ok = wait_bar(tfull_bar(0), 0, p.status, p.timeout_ns, 42);
+        bool ok = true;
+        if (FOLD2) {
+            int fs = 0;
+            uint32_t fph = 0;
+            ok = fold_upper(tile, rl, fs, fph);
+        }
+        ok = ok && wait_bar(tfull_bar(0), 0, p.status, p.timeout_ns, 42);
         tc_fence_after();
         if (threadIdx.x == 32 * EPI_WARP0) FL_MARK(p, 5);
         float ss_own = 0.f;
@@ -503,6 +543,8 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         const uint32_t my_row_addr = ebuf + lane * 128;
         const int sw = lane & 7;
         int it = 0;
+        int fs = 0;  // ring position of the fold half (FOLD2)
+        uint32_t fph = 0;
         using T = uint16_t;
         const T* bias = reinterpret_cast<const T*>(p.bias);
         const T* res = reinterpret_cast<const T*>(p.residual);
@@ -511,6 +553,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
             const int n0 = tile_nb(tile) * C::BN;
             const int buf = C::NBUF == 2 ? (it & 1) : 0;
             const uint32_t tph = C::NBUF == 2 ? (uint32_t)((it >> 1) & 1) : (uint32_t)(it & 1);
+            if (FOLD2 && !fold_upper(tile, q * 32 + (threadIdx.x & 31), fs, fph)) break;
             if (!wait_bar(tfull_bar(buf), tph, p.status, p.timeout_ns, 40)) break;
             tc_fence_after();
             float rs = 1.f;
