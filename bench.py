@@ -82,6 +82,16 @@ def describe(w: dict) -> str:
             f"Wd[{w['D']},{w['F']}], + x")
 
 
+def launches_of(w) -> int:
+    """Kernels of this library one step launches: the SwiGLU block is two fused
+    GEMMs; LayerNorm adds its row-statistics pass ahead of the fused GEMM."""
+    if w["kind"] == "swiglu":
+        return 2
+    if w["kind"] == "norm" and w["norm"] == "layer":
+        return 2
+    return 1
+
+
 def flops_per_step(w: dict) -> float:
     """2MNK plus the epilogue / prologue element ops (norm 3 per input element,
     row scale 1 per output, bias 1, gelu 8, silu 4, relu 1, residual 1, SwiGLU product 1)."""
@@ -349,7 +359,7 @@ def run_ours(args, w: dict, rank: int, world: int, local: int):
             g["ws"] = torch.empty(fl.swiglu_ffn_workspace_size(w["M"], w["F"], w["dtype"]), dtype=torch.uint8,
                                   device=dev)
         sets.append(g)
-    launches_per_step = 2 if w["kind"] == "swiglu" else 1
+    launches_per_step = launches_of(w)
 
     def step(g, stream=None):
         if w["kind"] == "norm":

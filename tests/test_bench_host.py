@@ -34,6 +34,13 @@ def test_flops_of_patterns_and_ffn():
         bench.parse_workload("nonsense:1")
 
 
+def test_kernel_launches_per_step():
+    assert bench.launches_of(bench.parse_workload("rmsnorm_gemm_f16_512x4096x4096")) == 1
+    assert bench.launches_of(bench.parse_workload("norm:layer:f16:512:4096:4096")) == 2
+    assert bench.launches_of(bench.parse_workload("pattern:gemm_bias:bf16:8:16:32")) == 1
+    assert bench.launches_of(bench.parse_workload("swiglu_ffn_bf16_4096x4096x11008")) == 2
+
+
 def _free_port():
     s = socket.socket()
     s.bind(("127.0.0.1", 0))
