@@ -564,18 +564,32 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
             const int row = m0 + q * 32 + lane;
             const bool row_ok = row < p.M;
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * C::ACC_COLS);
-            if (m0 + q * 32 < p.M) {
-                for (int c = 0; c < C::BN / 64; ++c) {
+            // 64-column chunks this warp stores (rows or columns past the
+            // output are skipped); the accumulator goes back to the MMA right
+            // after the last chunk's TMEM load
+            int nchunks = 0;
+            if (m0 + q * 32 < p.M)
+                while (nchunks < C::BN / 64 && n0 + nchunks * 64 < p.N) ++nchunks;
+            bool released = false;
+            auto release_acc = [&]() {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive_cluster(lead(tempty_bar(buf)));
+                    mbar_arrive(tdone_bar);
+                }
+                released = true;
+            };
+            {
+                for (int c = 0; c < nchunks; ++c) {
                     const int col0 = n0 + c * 64;
-                    if (col0 >= p.N) break;
-                    if (lane == 0) bulk_wait_group_read<0>();
-                    __syncwarp();
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int cbase = col0 + h * 32;
                         uint32_t acc[32];
                         tmem_ld_32x32b_x32(tbase + c * 64 + h * 32, acc);
                         tmem_ld_wait();
+                        if (h == 1 && c == nchunks - 1) release_acc();
                         float v[32];
 #pragma unroll
                         for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(acc[e]) * rs;
@@ -614,6 +628,11 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                                 }
                             }
                         }
+                        if (h == 0) {
+                            // the previous chunk's TMA store has read the staging buffer
+                            if (lane == 0) bulk_wait_group_read<0>();
+                            __syncwarp();
+                        }
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             const int chunk = h * 4 + j;
@@ -630,12 +649,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                     }
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive_cluster(lead(tempty_bar(buf)));
-                mbar_arrive(tdone_bar);
-            }
+            if (!released) release_acc();
         }
         if (lane == 0) bulk_wait_group_read<0>();  // global writes complete with the grid
     }
