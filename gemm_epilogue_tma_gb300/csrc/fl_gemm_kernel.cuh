@@ -373,7 +373,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                             for (int e = 0; e < 32; ++e) {
                                 const float gt = __uint_as_float(acc[e]) * rs;
                                 const float u = __uint_as_float(up[e]) * rs;
-                                v[e] = logistic_mul(gt, gt) * u;
+                                v[e] = act_apply(ACT_SILU, gt) * u;
                             }
                         } else {
                             tmem_ld_wait();

@@ -70,7 +70,9 @@ struct PairCfg {
     static constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_ROWSCALE = (OFF_SLOT + 16 + 15) / 16 * 16;
     static constexpr int OFF_GB = (OFF_ROWSCALE + 2 * kBM * 4 + 127) / 128 * 128;
-    static constexpr int SMEM_BYTES = OFF_GB + STAGES * 256 + 1024;
+    // each epilogue warp's copy of the tile's bias slice (BN x 16-bit)
+    static constexpr int OFF_BIAS = OFF_GB + STAGES * 256;
+    static constexpr int SMEM_BYTES = OFF_BIAS + 4 * BN * 2 + 1024;
     static_assert(!ATMEM || A_COL0 + 32 * STAGES <= TMEM_COLS, "activation slots must fit in tensor memory");
 };
 
@@ -184,6 +186,23 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     griddep_wait();
     if (threadIdx.x == 0) griddep_launch_dependents();
     if (threadIdx.x == 0) FL_MARK(p, 1);
+
+    // The bias of tile columns [n0, n0 + BN) into this epilogue warp's own
+    // shared buffer (one 16-byte load per lane and 256 columns; zeros past N),
+    // before the accumulator is waited for: the epilogue then reads it with
+    // broadcast shared loads instead of global loads on its critical path.
+    auto stage_bias = [&](int n0, int q) -> uint32_t {
+        const uint32_t buf = sbase + C::OFF_BIAS + (uint32_t)(q * C::BN * 2);
+        if (p.bias != nullptr) {
+            const uint16_t* b = reinterpret_cast<const uint16_t*>(p.bias);
+            for (int c = (int)(threadIdx.x & 31) * 8; c < C::BN; c += 256) {
+                const uint4 v = n0 + c < p.N ? ldg_v4(b + n0 + c) : make_uint4(0u, 0u, 0u, 0u);
+                st_shared_v4(buf + (uint32_t)c * 2u, v.x, v.y, v.z, v.w);
+            }
+        }
+        __syncwarp();
+        return buf;
+    };
 
     // Epilogue warps' half of the LayerNorm fold for one tile (FOLD2): row rl,
     // chunks 4-7 of each K block into the upper 16 columns of its TMEM slot.
@@ -393,6 +412,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         const int m0 = tile_mb(tile) * 2 * kBM + (int)rank * kBM;
         const int n0 = tile_nb(tile) * C::BN;
         const int own_c0 = khalf * HALF_N, oth_c0 = (1 - khalf) * HALF_N;
+        const uint32_t bias_s = stage_bias(n0, q);
         const uint32_t tl = tmem_base + ((uint32_t)(q * 32) << 16);
         const uint32_t row_off = (uint32_t)(rl * C::XROW) * 4u;  // within a chunk
         using T = uint16_t;
@@ -461,6 +481,16 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                         const int xc = c * 2 + h;        // exchange chunk
                         const int lc = xc * C::XCOLS;    // column within the own half
                         const uint32_t recv_row = sbase + (uint32_t)(xc * C::XCHUNK) + row_off;
+                        // residual of these 32 columns, requested before the waits
+                        // and TMEM loads below so its latency overlaps them
+                        uint4 rres[4];
+                        if (res != nullptr && row_ok) {
+                            const T* rrow = res + (size_t)row * p.N;
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                rres[j] = cbase + j * 8 < p.N ? *reinterpret_cast<const uint4*>(rrow + cbase + j * 8)
+                                                              : make_uint4(0u, 0u, 0u, 0u);
+                        }
                         if (!wait_bar_cluster(recvd_bar(q, xc), 0, p.status, p.timeout_ns, 45)) ok = false;
                         if (PRO == PRO_RMS && xc == 0) {
                             const float ss = ss_own + ld_shared_f32(recv_row + (uint32_t)C::XCOLS * 4u);
@@ -482,7 +512,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
                                 if (cbase + j * 8 < p.N) {
-                                    const uint4 bv = ldg_v4(bias + cbase + j * 8);
+                                    const uint4 bv = ld_shared_v4(bias_s + (uint32_t)(cbase + j * 8 - n0) * 2u);
                                     const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
                                     for (int e = 0; e < 4; ++e) {
@@ -498,12 +528,10 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                             for (int e = 0; e < 32; ++e) v[e] = act_apply(p.act, v[e]);
                         }
                         if (res != nullptr && row_ok) {
-                            const T* rrow = res + (size_t)row * p.N;
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
                                 if (cbase + j * 8 < p.N) {
-                                    const uint4 rv = *reinterpret_cast<const uint4*>(rrow + cbase + j * 8);
-                                    const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
+                                    const uint32_t rw[4] = {rres[j].x, rres[j].y, rres[j].z, rres[j].w};
 #pragma unroll
                                     for (int e = 0; e < 4; ++e) {
                                         const float2 r2 = Ops::unpack(rw[e]);
@@ -553,6 +581,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
             const int n0 = tile_nb(tile) * C::BN;
             const int buf = C::NBUF == 2 ? (it & 1) : 0;
             const uint32_t tph = C::NBUF == 2 ? (uint32_t)((it >> 1) & 1) : (uint32_t)(it & 1);
+            const uint32_t bias_s = stage_bias(n0, q);
             if (FOLD2 && !fold_upper(tile, q * 32 + (threadIdx.x & 31), fs, fph)) break;
             if (!wait_bar(tfull_bar(buf), tph, p.status, p.timeout_ns, 40)) break;
             tc_fence_after();
@@ -586,6 +615,16 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int cbase = col0 + h * 32;
+                        // residual of these 32 columns, requested before the waits
+                        // and TMEM loads below so its latency overlaps them
+                        uint4 rres[4];
+                        if (res != nullptr && row_ok) {
+                            const T* rrow = res + (size_t)row * p.N;
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                rres[j] = cbase + j * 8 < p.N ? *reinterpret_cast<const uint4*>(rrow + cbase + j * 8)
+                                                              : make_uint4(0u, 0u, 0u, 0u);
+                        }
                         uint32_t acc[32];
                         tmem_ld_32x32b_x32(tbase + c * 64 + h * 32, acc);
                         tmem_ld_wait();
@@ -597,7 +636,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
                                 if (cbase + j * 8 < p.N) {
-                                    const uint4 bv = ldg_v4(bias + cbase + j * 8);
+                                    const uint4 bv = ld_shared_v4(bias_s + (uint32_t)(cbase + j * 8 - n0) * 2u);
                                     const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
                                     for (int e = 0; e < 4; ++e) {
@@ -613,12 +652,10 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                             for (int e = 0; e < 32; ++e) v[e] = act_apply(p.act, v[e]);
                         }
                         if (res != nullptr && row_ok) {
-                            const T* rrow = res + (size_t)row * p.N;
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
                                 if (cbase + j * 8 < p.N) {
-                                    const uint4 rv = *reinterpret_cast<const uint4*>(rrow + cbase + j * 8);
-                                    const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
+                                    const uint32_t rw[4] = {rres[j].x, rres[j].y, rres[j].z, rres[j].w};
 #pragma unroll
                                     for (int e = 0; e < 4; ++e) {
                                         const float2 r2 = Ops::unpack(rw[e]);
