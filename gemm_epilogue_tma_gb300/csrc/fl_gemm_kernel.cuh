@@ -6,13 +6,17 @@
 //   warp 0        TMA producer: fills an S-stage ring of (A, W[, W2]) K-slices
 //                 (64 elements = 128 B per row, 128-byte swizzle).
 //   warp 1        TMEM owner and MMA issuer: one thread issues
-//                 tcgen05.mma.cta_group::1.kind::f16 (128 x BN x 16) into a
-//                 double-buffered fp32 accumulator in tensor memory.
-//   warps 4-7     (norm prologues only) transform warpgroup, thread t <-> tile
-//                 row t: RMS accumulates sum(x^2) and folds gamma into the
-//                 staged operand in place; LayerNorm first streams the row
-//                 block once for mean / variance (Chan's pairwise merge), then
-//                 writes (x - mean) * rstd * gamma + beta in place.
+//                 tcgen05.mma.cta_group::1.kind::f16 (128 x BN x 16) into an
+//                 fp32 accumulator in tensor memory, double-buffered where the
+//                 columns allow (the epilogue of a tile then overlaps the next
+//                 tile's MMAs).
+//   warps 4-7     (norm prologues only) transform warpgroup. With 128-wide
+//                 tiles (one or two weights) thread t folds tile row t
+//                 (RMS: x * gamma and sum(x^2); LayerNorm: (x - mean) * rstd
+//                 * gamma + beta with the row statistics computed ahead of the
+//                 GEMM) into a 32-column tensor-memory slot, and the MMA reads
+//                 A from there; with 256-wide tiles the fold rewrites the
+//                 staged operand in place.
 //   last 4 warps  epilogue: tcgen05.ld 32 columns at a time, row scale (RMS),
 //                 bias, activation, residual, round, stage in 128B-swizzled
 //                 shared memory, TMA store (which clips the ragged tails).
@@ -45,9 +49,13 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     // goes to tensor memory (one 32-column slot per stage after the two
     // accumulators) and the MMA reads it from there, which takes the fold's
     // shared-memory writes and the MMA's activation reads off shared memory.
-    constexpr bool ATMEM = PRO != PRO_NONE && BN == 128 && !DUAL;
+    constexpr bool ATMEM = PRO != PRO_NONE && BN == 128;
+    // accumulator buffers: two (the epilogue of a tile overlaps the next
+    // tile's MMAs) unless the activation slots then no longer fit (the
+    // gate/up kernel: 2 x 256 accumulator columns)
+    constexpr int NBUF = 2 * C::ACC_COLS + (ATMEM ? 32 * S : 0) <= 512 ? 2 : 1;
     constexpr uint32_t TMEM_ALLOC = ATMEM ? 512u : (uint32_t)C::TMEM_COLS;
-    constexpr uint32_t A_COL0 = 2u * C::ACC_COLS;
+    constexpr uint32_t A_COL0 = (uint32_t)NBUF * C::ACC_COLS;
     static_assert(!ATMEM || A_COL0 + 32u * S <= 512u, "activation slots must fit in tensor memory");
 
     extern __shared__ uint8_t smem_raw[];
@@ -166,8 +174,8 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
             int it = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++it) {
-                const int buf = it & 1;
-                const uint32_t tph = (it >> 1) & 1;
+                const int buf = NBUF == 2 ? (it & 1) : 0;
+                const uint32_t tph = NBUF == 2 ? (uint32_t)((it >> 1) & 1) : (uint32_t)(it & 1);
                 if (!wait_bar(tempty_bar(buf), tph ^ 1u, p.status, p.timeout_ns, 3)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(buf * C::ACC_COLS);
@@ -184,7 +192,12 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                     for (int kk = 0; kk < kBK / 16; ++kk) {
                         if (ATMEM) {
                             // 16 K elements = 8 columns of the stage's activation slot
-                            umma_f16_ts(d, tmem_base + A_COL0 + 32u * s + 8u * kk, db + 2 * kk, IDESC, (kb | kk) != 0);
+                            const uint32_t ta = tmem_base + A_COL0 + 32u * s + 8u * kk;
+                            umma_f16_ts(d, ta, db + 2 * kk, IDESC, (kb | kk) != 0);
+                            if (DUAL) {
+                                const uint64_t db2 = sw128_kmajor_desc(stage_b2(s));
+                                umma_f16_ts(d + BN, ta, db2 + 2 * kk, IDESC, (kb | kk) != 0);
+                            }
                             continue;
                         }
                         // +32 bytes per 16-element K step inside the swizzled row
@@ -254,8 +267,8 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
             }
             if (!ok) break;
             if (PRO == PRO_RMS) {
-                const int buf = it & 1;
-                const uint32_t tph = (it >> 1) & 1;
+                const int buf = NBUF == 2 ? (it & 1) : 0;
+                const uint32_t tph = NBUF == 2 ? (uint32_t)((it >> 1) & 1) : (uint32_t)(it & 1);
                 if (!wait_bar(tempty_bar(buf), tph ^ 1u, p.status, p.timeout_ns, 7)) break;
                 const float sum = ((ss[0] + ss[1]) + (ss[2] + ss[3])) + ((ss[4] + ss[5]) + (ss[6] + ss[7]));
                 rowscale[buf * kBM + t] = rsqrtf(sum / (float)p.K + p.eps);
@@ -313,8 +326,8 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
             if (PRO == PRO_RMS) {
                 // the row scale of buffer (it & 1) is free once the epilogue has
                 // released that accumulator buffer for this tile
-                const int buf = it & 1;
-                const uint32_t tph = (it >> 1) & 1;
+                const int buf = NBUF == 2 ? (it & 1) : 0;
+                const uint32_t tph = NBUF == 2 ? (uint32_t)((it >> 1) & 1) : (uint32_t)(it & 1);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) ss[i] = row_allreduce8(ss[i]);
                 if (!wait_bar(tempty_bar(buf), tph ^ 1u, p.status, p.timeout_ns, 7)) break;
@@ -340,8 +353,8 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
             const int m0 = (tile % p.num_m_blocks) * kBM;
             const int n0 = (tile / p.num_m_blocks) * BN;
-            const int buf = it & 1;
-            const uint32_t tph = (it >> 1) & 1;
+            const int buf = NBUF == 2 ? (it & 1) : 0;
+            const uint32_t tph = NBUF == 2 ? (uint32_t)((it >> 1) & 1) : (uint32_t)(it & 1);
             if (!wait_bar(tfull_bar(buf), tph, p.status, p.timeout_ns, 8)) break;
             tc_fence_after();
             float rs = 1.f;
@@ -352,13 +365,22 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
             const int row = m0 + q * 32 + lane;
             const bool row_ok = row < p.M;
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * C::ACC_COLS);
-            if (m0 + q * 32 < p.M) {
-                for (int c = 0; c < BN / 64; ++c) {
+            // 64-column chunks this warp stores (rows or columns past the
+            // output are skipped); the accumulator goes back to the MMA right
+            // after the last chunk's TMEM load
+            int nchunks = 0;
+            if (m0 + q * 32 < p.M)
+                while (nchunks < BN / 64 && n0 + nchunks * 64 < p.N) ++nchunks;
+            bool released = false;
+            auto release_acc = [&]() {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar(buf));
+                released = true;
+            };
+            {
+                for (int c = 0; c < nchunks; ++c) {
                     const int col0 = n0 + c * 64;
-                    if (col0 >= p.N) break;
-                    // staging buffer of this warp is reused: the previous store must have read it
-                    if (lane == 0) bulk_wait_group_read<0>();
-                    __syncwarp();
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int cbase = col0 + h * 32;
@@ -369,6 +391,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                             uint32_t up[32];
                             tmem_ld_32x32b_x32(tbase + BN + c * 64 + h * 32, up);
                             tmem_ld_wait();
+                            if (h == 1 && c == nchunks - 1) release_acc();
 #pragma unroll
                             for (int e = 0; e < 32; ++e) {
                                 const float gt = __uint_as_float(acc[e]) * rs;
@@ -377,6 +400,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                             }
                         } else {
                             tmem_ld_wait();
+                            if (h == 1 && c == nchunks - 1) release_acc();
 #pragma unroll
                             for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(acc[e]) * rs;
                             if (bias != nullptr) {
@@ -413,6 +437,11 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                                 }
                             }
                         }
+                        if (h == 0) {
+                            // the previous chunk's TMA store has read the staging buffer
+                            if (lane == 0) bulk_wait_group_read<0>();
+                            __syncwarp();
+                        }
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             const int chunk = h * 4 + j;  // 16-byte chunk of the 128-byte row
@@ -431,9 +460,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                     }
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(tempty_bar(buf));
+            if (!released) release_acc();
         }
         if (lane == 0) bulk_wait_group_read<0>();  // global writes complete with the grid
     }

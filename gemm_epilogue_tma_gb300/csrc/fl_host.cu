@@ -307,9 +307,14 @@ int pair_max(int dt, int bn, int pro, int ks) {
     return v;
 }
 
-cudaError_t dispatch_pair(int dt, int bn, int pro, int ks, const GemmParams& p, int grid, cudaStream_t s) {
+cudaError_t dispatch_pair(int dt, int bn, int pro, int ks, bool dual, const GemmParams& p, int grid, cudaStream_t s) {
+    if (dual) {
+        if (bn != 256 || pro != fl::PRO_RMS || ks != 1) return cudaErrorInvalidValue;
+        return dt == 0 ? fl::launch_pair<0, 256, fl::PRO_RMS, 1, true>(p, grid, s)
+                       : fl::launch_pair<1, 256, fl::PRO_RMS, 1, true>(p, grid, s);
+    }
 #define FL_CASE(DT, BN, PRO, KS) \
-    if (dt == DT && bn == BN && pro == PRO && ks == KS) return fl::launch_pair<DT, BN, PRO, KS>(p, grid, s);
+    if (dt == DT && bn == BN && pro == PRO && ks == KS) return fl::launch_pair<DT, BN, PRO, KS, false>(p, grid, s);
     FL_CASE(0, 128, 0, 1) FL_CASE(0, 128, 1, 1) FL_CASE(0, 128, 2, 1)
     FL_CASE(0, 256, 0, 1) FL_CASE(0, 256, 1, 1) FL_CASE(0, 256, 2, 1)
     FL_CASE(1, 128, 0, 1) FL_CASE(1, 128, 1, 1) FL_CASE(1, 128, 2, 1)
@@ -330,9 +335,20 @@ struct PairPlan {
 // many shared-memory bytes per MMA as the single-CTA 128 x 256 tile and
 // measures no faster, so it is used only when forced (FL_OPT_VARIANT = 3 with
 // FL_OPT_TILE_N = 128; FL_OPT_SPLIT_K = 2 forces the K split).
-bool use_pair(int dt, int pro, int M, int N, int K, PairPlan* plan) {
+bool use_pair(int dt, int pro, int M, int N, int K, PairPlan* plan, bool dual) {
     const int variant = g_opt_variant.load();
     if (variant == 1 || variant == 2) return false;
+    if (dual) {
+        // SwiGLU gate/up: 128 output columns per 256 x 256 pair tile (Wg and Wu
+        // stacked); no K split, no 128-wide variant
+        if (pro != fl::PRO_RMS) return false;
+        const long long tiles = (long long)((M + 255) / 256) * ((N + 127) / 128);
+        const int maxp = pair_max(dt, 256, pro, 1);
+        if (maxp <= 0) return false;
+        if (variant != 3 && tiles * 5 < (long long)maxp * 4) return false;
+        *plan = PairPlan{256, 1, (int)(tiles < maxp ? tiles : maxp)};
+        return true;
+    }
     const int forced_bn = g_opt_tile_n.load();
     const int forced_split = g_opt_split_k.load();
     const long long mp = (M + 255) / 256;
@@ -360,9 +376,9 @@ bool use_pair(int dt, int pro, int M, int N, int K, PairPlan* plan) {
     return true;
 }
 
-fl_status run_pair(int dt, int pro, const void* A, const void* W, const void* bias, const void* residual,
-                   const void* gamma, const void* beta, const void* ln_stats, void* out, int M, int N, int K, int act,
-                   float eps, const PairPlan& plan, DeviceInfo* di, cudaStream_t stream) {
+fl_status run_pair(int dt, int pro, bool dual, const void* A, const void* W, const void* W2, const void* bias,
+                   const void* residual, const void* gamma, const void* beta, const void* ln_stats, void* out, int M,
+                   int N, int K, int act, float eps, const PairPlan& plan, DeviceInfo* di, cudaStream_t stream) {
     const int bn = plan.bn;
     GemmParams p;
     memset(&p, 0, sizeof(p));
@@ -370,6 +386,7 @@ fl_status run_pair(int dt, int pro, const void* A, const void* W, const void* bi
     fl_status st;
     if ((st = encode_2d(&p.tmA, dt, A, K, M, fl::kBK, fl::kBM)) != FL_OK) return st;
     if ((st = encode_2d(&p.tmB, dt, W, K, N, fl::kBK, bn / 2)) != FL_OK) return st;
+    if (dual && (st = encode_2d(&p.tmB2, dt, W2, K, N, fl::kBK, bn / 2)) != FL_OK) return st;
     if ((st = encode_2d(&p.tmOut, dt, out, N, M, 64, 32)) != FL_OK) return st;
     if (pro != fl::PRO_NONE && (st = encode_2d(&p.tmGamma, dt, gamma, K, 1, fl::kBK, 1, false)) != FL_OK) return st;
     if (pro == fl::PRO_LN && beta != nullptr && (st = encode_2d(&p.tmBeta, dt, beta, K, 1, fl::kBK, 1, false)) != FL_OK)
@@ -384,7 +401,7 @@ fl_status run_pair(int dt, int pro, const void* A, const void* W, const void* bi
     p.N = N;
     p.K = K;
     p.num_m_blocks = (M + 255) / 256;  // row blocks of a pair tile
-    p.num_n_blocks = (N + bn - 1) / bn;
+    p.num_n_blocks = (N + (dual ? bn / 2 : bn) - 1) / (dual ? bn / 2 : bn);  // output columns of a tile
     p.num_k_blocks = (K + fl::kBK - 1) / fl::kBK;
     p.num_tiles = p.num_m_blocks * p.num_n_blocks;
     p.act = act;
@@ -395,7 +412,7 @@ fl_status run_pair(int dt, int pro, const void* A, const void* W, const void* bi
 #ifdef FL_TRACE
     if (const char* tp = getenv("FL_TRACE_PTR")) p.trace = reinterpret_cast<unsigned long long*>(strtoull(tp, nullptr, 10));
 #endif
-    cudaError_t e = dispatch_pair(dt, bn, pro, plan.ks, p, 2 * plan.ks * plan.clusters, stream);
+    cudaError_t e = dispatch_pair(dt, bn, pro, plan.ks, dual, p, 2 * plan.ks * plan.clusters, stream);
     if (e != cudaSuccess) return fail(FL_ERR_CUDA, "pair kernel launch failed: %s", cudaGetErrorString(e));
     return ok();
 }
@@ -479,9 +496,9 @@ fl_status run_kernels(int dt, int pro, bool dual, const void* A, const void* W, 
                       int N, int K, int act, float eps, DeviceInfo* di, cudaStream_t stream) {
     fl_status st;
     PairPlan pplan;
-    if (!dual && use_pair(dt, pro, M, N, K, &pplan))
-        return run_pair(dt, pro, A, W, bias, residual, gamma, beta, ln_stats, out, M, N, K, act, eps, pplan, di,
-                        stream);
+    if (use_pair(dt, pro, M, N, K, &pplan, dual))
+        return run_pair(dt, pro, dual, A, W, W2, bias, residual, gamma, beta, ln_stats, out, M, N, K, act, eps, pplan,
+                        di, stream);
     SplitPlan plan;
     if (!dual && plan_splitk(dt, pro, M, N, K, di->sms, &plan))
         return run_splitk(dt, pro, A, W, bias, residual, gamma, beta, ln_stats, out, M, N, K, act, eps, plan, di,

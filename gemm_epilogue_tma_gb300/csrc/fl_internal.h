@@ -77,7 +77,7 @@ cudaError_t launch_splitk(const GemmParams& p, int grid, int splits, cudaStream_
 template <int DT, int BN, int PRO>
 int splitk_max_clusters(int splits, int smem_bytes);
 
-template <int DT, int BN, int PRO, int KS>
+template <int DT, int BN, int PRO, int KS, bool DUAL>
 cudaError_t launch_pair(const GemmParams& p, int grid, cudaStream_t stream);
 
 template <int DT, int BN, int PRO, int KS>

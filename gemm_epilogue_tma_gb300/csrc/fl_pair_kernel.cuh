@@ -76,10 +76,16 @@ struct PairCfg {
     static_assert(!ATMEM || A_COL0 + 32 * STAGES <= TMEM_COLS, "activation slots must fit in tensor memory");
 };
 
-template <int DT, int BN, int PRO, int KS>
+// DUAL (SwiGLU gate/up): the 256-row weight tile of a pair is rows
+// [n0, n0 + 128) of Wg (even CTA) stacked over the same rows of Wu (odd CTA),
+// so one 256 x 256 MMA yields gate | up for 128 output columns, and the
+// epilogue writes silu(gate) * up.
+template <int DT, int BN, int PRO, int KS, bool DUAL>
 __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     fl_pair_kernel(const __grid_constant__ GemmParams p) {
     using C = PairCfg<BN, PRO, KS>;
+    static_assert(!DUAL || (BN == 256 && KS == 1), "gate/up pairs use 256-wide tiles without a K split");
+    constexpr int OUT_COLS = DUAL ? BN / 2 : BN;  // output columns of a tile
     static_assert(KS == 1 || (KS == 2 && BN == 256), "split-K pairs use 256-wide tiles");
     if (threadIdx.x == 0) FL_MARK(p, 0);
     using Ops = DTypeOps<DT>;
@@ -180,8 +186,9 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     // L2 prefetch of this CTA's first weight tiles overlaps the previous kernel
     // (L2 is the point of coherence); every other global access waits for it.
     if (warp == 0 && lane == 0 && t_begin < t_end) {
-        const int nh = tile_nb(t_begin) * C::BN + (int)rank * C::HALF;
-        for (int kb = kb_begin; kb < kb_begin + S && kb < kb_end; ++kb) tma_prefetch_2d(&p.tmB, kb * kBK, nh);
+        const int nh = DUAL ? tile_nb(t_begin) * OUT_COLS : tile_nb(t_begin) * C::BN + (int)rank * C::HALF;
+        const CUtensorMap* tb = DUAL && rank ? &p.tmB2 : &p.tmB;
+        for (int kb = kb_begin; kb < kb_begin + S && kb < kb_end; ++kb) tma_prefetch_2d(tb, kb * kBK, nh);
     }
     griddep_wait();
     if (threadIdx.x == 0) griddep_launch_dependents();
@@ -243,7 +250,10 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
             const uint32_t gb_bytes = PRO != PRO_NONE ? 128u + (PRO == PRO_LN && p.beta != nullptr ? 128u : 0u) : 0u;
             for (int tile = t_begin; ok && tile < t_end; ++tile) {
                 const int m0 = tile_mb(tile) * 2 * kBM + (int)rank * kBM;
-                const int nh = tile_nb(tile) * C::BN + (int)rank * C::HALF;
+                // this CTA's weight rows: its half of the tile, or (DUAL) the
+                // tile's rows of Wg / Wu
+                const int nh = DUAL ? tile_nb(tile) * OUT_COLS : tile_nb(tile) * C::BN + (int)rank * C::HALF;
+                const CUtensorMap* tb = DUAL && rank ? &p.tmB2 : &p.tmB;
                 for (int kb = kb_begin; kb < kb_end; ++kb) {
                     if (!wait_bar(empty_bar(s), ph ^ 1u, p.status, p.timeout_ns, 31)) {
                         ok = false;
@@ -253,7 +263,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                         if (leader) mbar_arrive_expect_tx(full_bar(s), 2u * C::STAGE_BYTES);
                         const uint32_t fb = lead(full_bar(s));
                         tma_load_2d_pair(stage_a(s), &p.tmA, fb, kb * kBK, m0);
-                        tma_load_2d_pair(stage_b(s), &p.tmB, fb, kb * kBK, nh);
+                        tma_load_2d_pair(stage_b(s), tb, fb, kb * kBK, nh);
                     } else {
                         mbar_arrive_expect_tx(afull_bar(s), (uint32_t)C::A_BYTES + gb_bytes);
                         tma_load_2d(stage_a(s), &p.tmA, afull_bar(s), kb * kBK, m0);
@@ -261,7 +271,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                         if (PRO == PRO_LN && p.beta != nullptr)
                             tma_load_2d(gb_slot(s) + 128, &p.tmBeta, afull_bar(s), kb * kBK, 0);
                         if (leader) mbar_arrive_expect_tx(full_bar(s), 2u * C::B_BYTES);
-                        tma_load_2d_pair(stage_b(s), &p.tmB, lead(full_bar(s)), kb * kBK, nh);
+                        tma_load_2d_pair(stage_b(s), tb, lead(full_bar(s)), kb * kBK, nh);
                     }
                     if (issued == 0) FL_MARK(p, 2);
                     ++issued;
@@ -578,7 +588,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         const T* res = reinterpret_cast<const T*>(p.residual);
         for (int tile = t_begin; tile < t_end; ++tile, ++it) {
             const int m0 = tile_mb(tile) * 2 * kBM + (int)rank * kBM;
-            const int n0 = tile_nb(tile) * C::BN;
+            const int n0 = tile_nb(tile) * OUT_COLS;
             const int buf = C::NBUF == 2 ? (it & 1) : 0;
             const uint32_t tph = C::NBUF == 2 ? (uint32_t)((it >> 1) & 1) : (uint32_t)(it & 1);
             const uint32_t bias_s = stage_bias(n0, q);
@@ -598,7 +608,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
             // after the last chunk's TMEM load
             int nchunks = 0;
             if (m0 + q * 32 < p.M)
-                while (nchunks < C::BN / 64 && n0 + nchunks * 64 < p.N) ++nchunks;
+                while (nchunks < OUT_COLS / 64 && n0 + nchunks * 64 < p.N) ++nchunks;
             bool released = false;
             auto release_acc = [&]() {
                 tc_fence_before();
@@ -627,12 +637,23 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                         }
                         uint32_t acc[32];
                         tmem_ld_32x32b_x32(tbase + c * 64 + h * 32, acc);
-                        tmem_ld_wait();
-                        if (h == 1 && c == nchunks - 1) release_acc();
                         float v[32];
+                        if (DUAL) {
+                            // gate in accumulator columns [0, 128), up in [128, 256)
+                            uint32_t up[32];
+                            tmem_ld_32x32b_x32(tbase + OUT_COLS + c * 64 + h * 32, up);
+                            tmem_ld_wait();
+                            if (h == 1 && c == nchunks - 1) release_acc();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(acc[e]) * rs;
-                        if (bias != nullptr) {
+                            for (int e = 0; e < 32; ++e)
+                                v[e] = act_apply(ACT_SILU, __uint_as_float(acc[e]) * rs) * (__uint_as_float(up[e]) * rs);
+                        } else {
+                            tmem_ld_wait();
+                            if (h == 1 && c == nchunks - 1) release_acc();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(acc[e]) * rs;
+                        }
+                        if (!DUAL && bias != nullptr) {
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
                                 if (cbase + j * 8 < p.N) {
@@ -647,11 +668,11 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                                 }
                             }
                         }
-                        if (p.act != ACT_NONE) {
+                        if (!DUAL && p.act != ACT_NONE) {
 #pragma unroll
                             for (int e = 0; e < 32; ++e) v[e] = act_apply(p.act, v[e]);
                         }
-                        if (res != nullptr && row_ok) {
+                        if (!DUAL && res != nullptr && row_ok) {
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
                                 if (cbase + j * 8 < p.N) {
@@ -707,7 +728,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
 template <int DT, int BN, int PRO, int KS>
 int pair_max_clusters() {
     using C = PairCfg<BN, PRO, KS>;
-    auto kern = fl_pair_kernel<DT, BN, PRO, KS>;
+    auto kern = fl_pair_kernel<DT, BN, PRO, KS, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg = {};
@@ -729,10 +750,10 @@ int pair_max_clusters() {
     return n;
 }
 
-template <int DT, int BN, int PRO, int KS>
+template <int DT, int BN, int PRO, int KS, bool DUAL>
 cudaError_t launch_pair(const GemmParams& p, int grid, cudaStream_t stream) {
     using C = PairCfg<BN, PRO, KS>;
-    auto kern = fl_pair_kernel<DT, BN, PRO, KS>;
+    auto kern = fl_pair_kernel<DT, BN, PRO, KS, DUAL>;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);

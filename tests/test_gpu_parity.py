@@ -356,6 +356,26 @@ def test_decode_sweep_rmsnorm_all_elements(dt, D, M):
 
 
 @pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("with_bias", [False, True])
+@pytest.mark.parametrize("shape", [(136, 256, 384), (300, 264, 520), (512, 128, 1024)], ids=lambda s: "x".join(map(str, s)))
+def test_swiglu_ffn_on_cta_pairs(dt, with_bias, shape):
+    """Gate/up on the CTA-pair kernel (Wg and Wu stacked in one weight tile), forced on small shapes."""
+    M, D, F = shape
+    t = syn.swiglu_inputs(M, D, F, dt, with_bias=with_bias)
+    g = {k: dev(v) for k, v in t.items()}
+    fl.set_option("variant", 3)
+    try:
+        got = fl.swiglu_ffn(g["x"], g["gamma"], g["Wg"], g["Wu"], g["Wd"], bias_down=g["bias_down"], eps=1e-6)
+        torch.cuda.synchronize()
+        fl.device_status()
+    finally:
+        fl.set_option("variant", 0)
+    f = {k: f64(v) for k, v in t.items()}
+    ref = oracle.swiglu_ffn(f["x"], f["gamma"], f["Wg"], f["Wu"], f["Wd"], f["bias_down"], 1e-6, dt)
+    assert_close(got, ref, dt, f"swiglu pairs {dt} {shape}")
+
+
+@pytest.mark.parametrize("dt", DTYPES)
 @pytest.mark.parametrize("shape", [(200, 264, 520), (512, 512, 1024), (1, 128, 256)], ids=lambda s: "x".join(map(str, s)))
 def test_layernorm_captured_in_cuda_graph(dt, shape):
     """LayerNorm takes stream-ordered scratch for its row statistics: it must
