@@ -82,6 +82,25 @@ def describe(w: dict) -> str:
             f"Wd[{w['D']},{w['F']}], + x")
 
 
+def roofline_of(flops: float, nbytes: float, per_launch_ms: float, peaks: dict, peak_src: str, traffic):
+    """Roofline record of one step: bound by tensor throughput or by HBM bandwidth,
+    whichever the step's arithmetic intensity puts it under (the ridge point of
+    the measured peaks), with both fractions reported."""
+    tensor_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    secs = per_launch_ms / 1e3
+    tflops = flops / secs / 1e12
+    gbs = nbytes / secs / 1e9
+    ridge = tensor_peak * 1e12 / (hbm_peak * 1e9)  # flop per byte
+    common = {"traffic": traffic, "algorithmic_bytes": nbytes, "tflops": tflops, "tensor_frac": tflops / tensor_peak,
+              "hbm_gbs": gbs, "hbm_frac": gbs / hbm_peak, "intensity": flops / nbytes}
+    if flops / nbytes < ridge:
+        return {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
+                "peak_source": f"hbm_gbs (copy) of {peak_src}", **common}
+    return {"bound": "tensor", "achieved": tflops, "peak": tensor_peak, "unit": "TFLOP/s", "frac": tflops / tensor_peak,
+            "peak_source": f"bf16_tflops (burst, fp16 dense rate equal) of {peak_src}", **common}
+
+
 def launches_of(w) -> int:
     """Kernels of this library one step launches: the SwiGLU block is two fused
     GEMMs; LayerNorm adds its row-statistics pass ahead of the fused GEMM."""
@@ -457,17 +476,8 @@ def run_ours(args, w: dict, rank: int, world: int, local: int):
     value = flops * args.steps * world / (ms_max / 1e3) / 1e12
     per_launch_ms = ms / args.steps
     peaks, peak_src = load_peaks()
-    tensor_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    # dominant kernel: the only one for single-launch workloads; for the FFN the
-    # two launches are reported together
-    achieved = flops / (per_launch_ms / 1e3) / 1e12
     traffic = recorded_traffic(w["name"])
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": tensor_peak, "unit": "TFLOP/s",
-                "frac": achieved / tensor_peak, "traffic": traffic,
-                "peak_source": f"bf16_tflops (burst, fp16 dense rate equal) of {peak_src}",
-                "algorithmic_bytes": bytes_per_step(w),
-                "hbm_gbs": bytes_per_step(w) / (per_launch_ms / 1e3) / 1e9,
-                "hbm_frac": bytes_per_step(w) / (per_launch_ms / 1e3) / 1e9 / float(peaks.get("hbm_gbs", 6800.0))}
+    roofline = roofline_of(flops, bytes_per_step(w), per_launch_ms, peaks, peak_src, traffic)
     vs = None
     if w["name"] == "rmsnorm_gemm_f16_512x4096x4096":
         vs = value / world / (flops / (PAGE_FUSED_MS / 1e3) / 1e12)

@@ -34,6 +34,18 @@ def test_flops_of_patterns_and_ffn():
         bench.parse_workload("nonsense:1")
 
 
+def test_roofline_bound_follows_arithmetic_intensity():
+    peaks = {"bf16_tflops": 1955.0, "hbm_gbs": 6684.0}
+    d = bench.parse_workload("norm:rms:f16:1:4096:4096")  # decode: ~1 flop per byte
+    r = bench.roofline_of(bench.flops_per_step(d), bench.bytes_per_step(d), 0.010, peaks, "measured", None)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert abs(r["achieved"] - bench.bytes_per_step(d) / 10e-6 / 1e9) < 1e-6 and abs(r["frac"] - r["hbm_frac"]) < 1e-12
+    h = bench.parse_workload("rmsnorm_gemm_f16_512x4096x4096")  # ~400 flop per byte
+    r = bench.roofline_of(bench.flops_per_step(h), bench.bytes_per_step(h), 0.019, peaks, "measured", 123)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and r["traffic"] == 123
+    assert abs(r["frac"] - r["tensor_frac"]) < 1e-12 and r["hbm_frac"] < r["tensor_frac"]
+
+
 def test_kernel_launches_per_step():
     assert bench.launches_of(bench.parse_workload("rmsnorm_gemm_f16_512x4096x4096")) == 1
     assert bench.launches_of(bench.parse_workload("norm:layer:f16:512:4096:4096")) == 2
