@@ -20,6 +20,24 @@ __device__ __forceinline__ uint32_t fold_row_addr(uint32_t stage, int row, int j
     return stage + row * 128 + ((j ^ (row & 7)) << 4);
 }
 
+// s0 += lo^2, s1 += hi^2 for the two 16-bit values of u, without widening
+// them first: the mixed-precision FMA (fp32 result and addend, 16-bit
+// factors; sm_100 and later) squares exactly in fp32 and rounds once, the same
+// value as fmaf on the widened inputs, in one instruction per element.
+template <int DT>
+__device__ __forceinline__ void sq_acc2(uint32_t u, float& s0, float& s1) {
+    if (DT == DT_F16)
+        asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+            "fma.rn.f32.f16 %0, lo, lo, %0;\n\tfma.rn.f32.f16 %1, hi, hi, %1;\n\t}"
+            : "+f"(s0), "+f"(s1)
+            : "r"(u));
+    else
+        asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+            "fma.rn.f32.bf16 %0, lo, lo, %0;\n\tfma.rn.f32.bf16 %1, hi, hi, %1;\n\t}"
+            : "+f"(s0), "+f"(s1)
+            : "r"(u));
+}
+
 // RMS: accumulate x^2 of this thread's chunks into ss[i] and replace the
 // chunks by x * gamma (one rounding, as the 16-bit product rounded once).
 template <int DT>
@@ -34,15 +52,11 @@ __device__ __forceinline__ void fold_rms_stage(uint32_t stage, uint32_t gamma_sl
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         if (i < ni) {
-            const float2 a = Ops::unpack(xv[i].x), b = Ops::unpack(xv[i].y), c = Ops::unpack(xv[i].z),
-                         d = Ops::unpack(xv[i].w);
-            float s0 = a.x * a.x, s1 = a.y * a.y;
-            s0 = fmaf(b.x, b.x, s0);
-            s1 = fmaf(b.y, b.y, s1);
-            s0 = fmaf(c.x, c.x, s0);
-            s1 = fmaf(c.y, c.y, s1);
-            s0 = fmaf(d.x, d.x, s0);
-            s1 = fmaf(d.y, d.y, s1);
+            float s0 = 0.f, s1 = 0.f;
+            sq_acc2<DT>(xv[i].x, s0, s1);
+            sq_acc2<DT>(xv[i].y, s0, s1);
+            sq_acc2<DT>(xv[i].z, s0, s1);
+            sq_acc2<DT>(xv[i].w, s0, s1);
             ss[i] += s0 + s1;
             xv[i].x = Ops::mul2(xv[i].x, g.x);
             xv[i].y = Ops::mul2(xv[i].y, g.y);
@@ -96,70 +110,98 @@ __device__ __forceinline__ void fold_ln_stage(uint32_t stage, uint32_t gb_slice,
 
 // ---------------------------------------------------------------------------
 // Thread-per-row forms, for folding into tensor memory: thread t of the
-// transform warpgroup owns row t (TMEM lane t), reads its 8 chunks (one per
-// quarter-warp bank group, no conflicts) and returns the folded row as 32
-// packed 32-bit columns in K order, ready for tcgen05.st.
+// transform warpgroup owns row t (TMEM lane t), reads chunks [j0, j0 + NJ) of
+// its row (one per quarter-warp bank group, no conflicts) and returns them
+// folded as 4 * NJ packed 32-bit columns in K order, ready for tcgen05.st.
+//
+// Each fold is split into a load part, which issues every shared-memory load
+// the fold needs (x, gamma and, for LayerNorm, beta), and a compute part, so a
+// caller can keep the loads of the next K block in flight while it computes
+// and stores this one: under the TMA and MMA traffic of the main loop a shared
+// load takes a few hundred cycles.
 // ---------------------------------------------------------------------------
-template <int DT>
-__device__ __forceinline__ void fold_rms_row(uint32_t stage, uint32_t gamma_slice, int t, float (&ss)[8],
-                                             uint32_t (&o)[32]) {
-    using Ops = DTypeOps<DT>;
+template <int NJ, bool LN>
+struct FoldRegs {
+    uint4 x[NJ];
+    uint4 g[NJ];
+    uint4 b[LN ? NJ : 1];
+};
+
+template <int NJ, bool LN>
+__device__ __forceinline__ void fold_row_load(FoldRegs<NJ, LN>& r, uint32_t stage, uint32_t gb_slice, bool has_beta,
+                                              int t, int j0) {
     const int sw = t & 7;
-    uint4 xv[8], gv[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) xv[j] = ld_shared_v4(stage + t * 128 + ((j ^ sw) << 4));
+    for (int jj = 0; jj < NJ; ++jj) r.x[jj] = ld_shared_v4(stage + t * 128 + (((j0 + jj) ^ sw) << 4));
 #pragma unroll
-    for (int j = 0; j < 8; ++j) gv[j] = ld_shared_v4(gamma_slice + j * 16);
+    for (int jj = 0; jj < NJ; ++jj) r.g[jj] = ld_shared_v4(gb_slice + (j0 + jj) * 16);
+    if (LN) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const float2 a = Ops::unpack(xv[j].x), b = Ops::unpack(xv[j].y), c = Ops::unpack(xv[j].z),
-                     d = Ops::unpack(xv[j].w);
-        float s0 = a.x * a.x, s1 = a.y * a.y;
-        s0 = fmaf(b.x, b.x, s0);
-        s1 = fmaf(b.y, b.y, s1);
-        s0 = fmaf(c.x, c.x, s0);
-        s1 = fmaf(c.y, c.y, s1);
-        s0 = fmaf(d.x, d.x, s0);
-        s1 = fmaf(d.y, d.y, s1);
-        ss[j] += s0 + s1;
-        o[4 * j + 0] = Ops::mul2(xv[j].x, gv[j].x);
-        o[4 * j + 1] = Ops::mul2(xv[j].y, gv[j].y);
-        o[4 * j + 2] = Ops::mul2(xv[j].z, gv[j].z);
-        o[4 * j + 3] = Ops::mul2(xv[j].w, gv[j].w);
+        for (int jj = 0; jj < NJ; ++jj)
+            r.b[jj] = has_beta ? ld_shared_v4(gb_slice + 128 + (j0 + jj) * 16) : make_uint4(0u, 0u, 0u, 0u);
     }
 }
 
-// LayerNorm, thread-per-row: row t, chunks [J0, J0 + NJ) of the K block :=
-// fma(fma(x, rstd, -mean * rstd), gamma, beta) in fp32, one rounding to the
-// dtype (the fp32 error stays relative to |mean| * 2^-24, far below it).
-// Every shared-memory load (x, gamma, beta) is issued before any result is
-// used: under the TMA and MMA traffic of the main loop a load takes a few
-// hundred cycles, so the fold costs one such round, not one per chunk.
-template <int DT, int NJ, int J0>
-__device__ __forceinline__ void fold_ln_row(uint32_t stage, uint32_t gb_slice, bool has_beta, int t, float rstd,
-                                            float nmr, uint32_t (&o)[4 * NJ]) {
+// RMS: ss[jj] += sum of x^2 over chunk jj; the chunk := x * gamma (one
+// rounding, as the 16-bit product rounded once).
+template <int DT, int NJ>
+__device__ __forceinline__ void fold_rms_compute(const FoldRegs<NJ, false>& r, float (&ss)[NJ],
+                                                 uint32_t (&o)[4 * NJ]) {
     using Ops = DTypeOps<DT>;
-    const int sw = t & 7;
-    uint4 xv[NJ], gv[NJ], bv[NJ];
 #pragma unroll
-    for (int jj = 0; jj < NJ; ++jj) xv[jj] = ld_shared_v4(stage + t * 128 + (((J0 + jj) ^ sw) << 4));
-#pragma unroll
-    for (int jj = 0; jj < NJ; ++jj) gv[jj] = ld_shared_v4(gb_slice + (J0 + jj) * 16);
-#pragma unroll
-    for (int jj = 0; jj < NJ; ++jj)
-        bv[jj] = has_beta ? ld_shared_v4(gb_slice + 128 + (J0 + jj) * 16) : make_uint4(0u, 0u, 0u, 0u);
+    for (int j = 0; j < NJ; ++j) {
+        float s0 = 0.f, s1 = 0.f;
+        sq_acc2<DT>(r.x[j].x, s0, s1);
+        sq_acc2<DT>(r.x[j].y, s0, s1);
+        sq_acc2<DT>(r.x[j].z, s0, s1);
+        sq_acc2<DT>(r.x[j].w, s0, s1);
+        ss[j] += s0 + s1;
+        o[4 * j + 0] = Ops::mul2(r.x[j].x, r.g[j].x);
+        o[4 * j + 1] = Ops::mul2(r.x[j].y, r.g[j].y);
+        o[4 * j + 2] = Ops::mul2(r.x[j].z, r.g[j].z);
+        o[4 * j + 3] = Ops::mul2(r.x[j].w, r.g[j].w);
+    }
+}
+
+// LayerNorm: chunk := fma(fma(x, rstd, -mean * rstd), gamma, beta) in fp32,
+// one rounding to the dtype (the fp32 error stays relative to
+// |mean| * 2^-24, far below it). Element pairs go through the paired fp32
+// FMA: the fold's arithmetic sits on the main loop's critical path.
+template <int DT, int NJ>
+__device__ __forceinline__ void fold_ln_compute(const FoldRegs<NJ, true>& r, float rstd, float nmr,
+                                                uint32_t (&o)[4 * NJ]) {
+    using Ops = DTypeOps<DT>;
+    const float2 r2 = make_float2(rstd, rstd), n2 = make_float2(nmr, nmr);
 #pragma unroll
     for (int jj = 0; jj < NJ; ++jj) {
-        const uint32_t xw[4] = {xv[jj].x, xv[jj].y, xv[jj].z, xv[jj].w};
-        const uint32_t gw[4] = {gv[jj].x, gv[jj].y, gv[jj].z, gv[jj].w};
-        const uint32_t bw[4] = {bv[jj].x, bv[jj].y, bv[jj].z, bv[jj].w};
+        const uint32_t xw[4] = {r.x[jj].x, r.x[jj].y, r.x[jj].z, r.x[jj].w};
+        const uint32_t gw[4] = {r.g[jj].x, r.g[jj].y, r.g[jj].z, r.g[jj].w};
+        const uint32_t bw[4] = {r.b[jj].x, r.b[jj].y, r.b[jj].z, r.b[jj].w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const float2 f = Ops::unpack(xw[q]), g = Ops::unpack(gw[q]), b = Ops::unpack(bw[q]);
-            o[4 * jj + q] =
-                Ops::pack(fmaf(fmaf(f.x, rstd, nmr), g.x, b.x), fmaf(fmaf(f.y, rstd, nmr), g.y, b.y));
+            const float2 y = ffma2(ffma2(f, r2, n2), g, b);
+            o[4 * jj + q] = Ops::pack(y.x, y.y);
         }
     }
+}
+
+// Whole-row RMS fold (chunks 0-7), loads issued before any use.
+template <int DT>
+__device__ __forceinline__ void fold_rms_row(uint32_t stage, uint32_t gamma_slice, int t, float (&ss)[8],
+                                             uint32_t (&o)[32]) {
+    FoldRegs<8, false> r;
+    fold_row_load(r, stage, gamma_slice, false, t, 0);
+    fold_rms_compute<DT>(r, ss, o);
+}
+
+// LayerNorm fold of chunks [J0, J0 + NJ) of row t, loads issued before any use.
+template <int DT, int NJ, int J0>
+__device__ __forceinline__ void fold_ln_row(uint32_t stage, uint32_t gb_slice, bool has_beta, int t, float rstd,
+                                            float nmr, uint32_t (&o)[4 * NJ]) {
+    FoldRegs<NJ, true> r;
+    fold_row_load(r, stage, gb_slice, has_beta, t, J0);
+    fold_ln_compute<DT>(r, rstd, nmr, o);
 }
 
 // Sum of the 8 lanes that share a row (RMS).

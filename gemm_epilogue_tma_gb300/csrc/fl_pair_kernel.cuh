@@ -93,7 +93,8 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     constexpr int EPI_WARP0 = PRO != PRO_NONE ? 8 : 4;
     // LayerNorm with a single accumulator buffer: the epilogue warps, idle
     // while a tile's MMAs run, fold the upper half (chunks 4-7) of every K
-    // block of that tile; the fold warps take chunks 0-3.
+    // block of that tile; the fold warps take chunks 0-3. (Splitting the
+    // cheaper RMS fold the same way was measured slower.)
     constexpr bool FOLD2 = PRO == PRO_LN && C::NBUF == 1;
     constexpr uint32_t IDESC = umma_idesc_f16(Ops::kFormat, 2 * kBM, C::BN);
 
@@ -211,32 +212,60 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         return buf;
     };
 
-    // Epilogue warps' half of the LayerNorm fold for one tile (FOLD2): row rl,
-    // chunks 4-7 of each K block into the upper 16 columns of its TMEM slot.
-    // They walk the ring in the same order as the fold warps (fs, fph).
-    auto fold_upper = [&](int tile, int rl, int& fs, uint32_t& fph) -> bool {
-        const int row = tile_mb(tile) * 2 * kBM + (int)rank * kBM + rl;
+    // One tile's fold of chunks [j0, j0 + 4) of every K block of row rl into
+    // the lower (j0 = 0) or upper (j0 = 4) 16 columns of the stage's TMEM slot
+    // (FOLD2: the fold warps take chunks 0-3, the epilogue warps 4-7). The
+    // loads of block kb + 1 go into the other register set once block kb has
+    // been handed to the MMA: issuing them before block kb's TMEM store, to
+    // overlap their latency with its arithmetic, was measured 15 % slower (the
+    // store, and with it the hand-off, then waits behind them). (fs, fph): ring
+    // position, kept by the caller across tiles; ssum: RMS sum of squares of
+    // the row over these chunks.
+    auto fold_tile = [&](int tile, int rl, int j0, int& fs, uint32_t& fph, float& ssum, int site) -> bool {
         float rstd = 1.f, nmr = 0.f;
-        if (row < p.M) {
-            const float2 st = reinterpret_cast<const float2*>(p.ln_stats)[row];
-            rstd = st.y;
-            nmr = -st.x * st.y;
+        if (PRO == PRO_LN) {
+            const int row = tile_mb(tile) * 2 * kBM + (int)rank * kBM + rl;
+            if (row < p.M) {
+                const float2 st = reinterpret_cast<const float2*>(p.ln_stats)[row];
+                rstd = st.y;
+                nmr = -st.x * st.y;
+            }
         }
-        const uint32_t a_lane = (uint32_t)(rl & ~31) << 16;
-        for (int kb = kb_begin; kb < kb_end; ++kb) {
-            if (!wait_bar(afull_bar(fs), fph, p.status, p.timeout_ns, 47)) return false;
+        float ss[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint32_t a_cols = tmem_base + ((uint32_t)(rl & ~31) << 16) + (uint32_t)C::A_COL0 + 4u * (uint32_t)j0;
+        const bool has_beta = p.beta != nullptr;
+        using R = FoldRegs<4, PRO == PRO_LN>;
+        R ra, rb;
+        if (!wait_bar(afull_bar(fs), fph, p.status, p.timeout_ns, site)) return false;
+        fold_row_load(ra, stage_a(fs), gb_slot(fs), has_beta, rl, j0);
+        // one K block: fold `cur` (ring position fs), then load the next into `nxt`
+        auto step = [&](R& cur, R& nxt, bool has_next) -> bool {
             uint32_t o[16];
-            fold_ln_row<DT, 4, 4>(stage_a(fs), gb_slot(fs), p.beta != nullptr, rl, rstd, nmr, o);
-            tmem_st_32x32b_x16(tmem_base + a_lane + (uint32_t)C::A_COL0 + 32u * fs + 16u, o);
+            if constexpr (PRO == PRO_LN)
+                fold_ln_compute<DT>(cur, rstd, nmr, o);
+            else
+                fold_rms_compute<DT>(cur, ss, o);
+            tmem_st_32x32b_x16(a_cols + 32u * (uint32_t)fs, o);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if ((threadIdx.x & 31) == 0) mbar_arrive_cluster(lead(xform_bar(fs)));
+            if (lane == 0) mbar_arrive_cluster(lead(xform_bar(fs)));
             if (++fs == S) {
                 fs = 0;
                 fph ^= 1u;
             }
+            if (has_next) {
+                if (!wait_bar(afull_bar(fs), fph, p.status, p.timeout_ns, site)) return false;
+                fold_row_load(nxt, stage_a(fs), gb_slot(fs), has_beta, rl, j0);
+            }
+            return true;
+        };
+        for (int kb = kb_begin; kb < kb_end; kb += 2) {
+            if (!step(ra, rb, kb + 1 < kb_end)) return false;
+            if (kb + 1 >= kb_end) break;
+            if (!step(rb, ra, kb + 2 < kb_end)) return false;
         }
+        ssum = (ss[0] + ss[1]) + (ss[2] + ss[3]);
         return true;
     };
 
@@ -348,30 +377,27 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         int it = 0;
         bool ok = true;
         for (int tile = t_begin; ok && tile < t_end; ++tile, ++it) {
-            float ss[8];
+            float ssum = 0.f;  // RMS: the row's sum of squares over the chunks folded here
+            if (FOLD2) {
+                ok = fold_tile(tile, t, 0, s, ph, ssum, 38);
+            } else {
+                float ss[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) ss[i] = 0.f;
-            float rstd = 1.f, nmr = 0.f;  // LayerNorm: 1/std and -mean/std of row t of this tile
-            if (PRO == PRO_LN) {
-                const int row = tile_mb(tile) * 2 * kBM + (int)rank * kBM + t;
-                if (row < p.M) {
-                    const float2 st = reinterpret_cast<const float2*>(p.ln_stats)[row];
-                    rstd = st.y;
-                    nmr = -st.x * st.y;
+                for (int i = 0; i < 8; ++i) ss[i] = 0.f;
+                float rstd = 1.f, nmr = 0.f;  // LayerNorm: 1/std and -mean/std of row t of this tile
+                if (PRO == PRO_LN) {
+                    const int row = tile_mb(tile) * 2 * kBM + (int)rank * kBM + t;
+                    if (row < p.M) {
+                        const float2 st = reinterpret_cast<const float2*>(p.ln_stats)[row];
+                        rstd = st.y;
+                        nmr = -st.x * st.y;
+                    }
                 }
-            }
-            for (int kb = kb_begin; kb < kb_end; ++kb) {
-                if (!wait_bar(afull_bar(s), ph, p.status, p.timeout_ns, 38)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t aslot = tmem_base + a_lane + (uint32_t)C::A_COL0 + 32u * s;
-                if (FOLD2) {
-                    uint32_t o[16];
-                    fold_ln_row<DT, 4, 0>(stage_a(s), gb_slot(s), p.beta != nullptr, t, rstd, nmr, o);
-                    if (t == 0 && kb == kb_begin && it == 0) FL_MARK(p, 10);
-                    tmem_st_32x32b_x16(aslot, o);
-                } else {
+                for (int kb = kb_begin; kb < kb_end; ++kb) {
+                    if (!wait_bar(afull_bar(s), ph, p.status, p.timeout_ns, 38)) {
+                        ok = false;
+                        break;
+                    }
                     uint32_t o[32];
                     if (PRO == PRO_RMS) {
                         fold_rms_row<DT>(stage_a(s), gb_slot(s), t, ss, o);
@@ -382,16 +408,17 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                         fold_ln_row<DT, 4, 4>(stage_a(s), gb_slot(s), p.beta != nullptr, t, rstd, nmr, hi);
                     }
                     if (t == 0 && kb == kb_begin && it == 0) FL_MARK(p, 10);
-                    tmem_st_32x32b_x32(aslot, o);
+                    tmem_st_32x32b_x32(tmem_base + a_lane + (uint32_t)C::A_COL0 + 32u * s, o);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(lead(xform_bar(s)));
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(lead(xform_bar(s)));
-                if (++s == S) {
-                    s = 0;
-                    ph ^= 1u;
-                }
+                ssum = ((ss[0] + ss[1]) + (ss[2] + ss[3])) + ((ss[4] + ss[5]) + (ss[6] + ss[7]));
             }
             if (!ok) break;
             if (PRO == PRO_RMS) {
@@ -400,9 +427,9 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                 const int rb = it & 1;
                 const uint32_t tph = (uint32_t)(it & 1);
                 if (!wait_bar(tdone_bar, tph ^ 1u, p.status, p.timeout_ns, 39)) break;
-                const float sum = ((ss[0] + ss[1]) + (ss[2] + ss[3])) + ((ss[4] + ss[5]) + (ss[6] + ss[7]));
-                // split-K: the raw partial sum; the epilogue adds the K-partner's
-                rowscale[rb * kBM + t] = KS == 2 ? sum : rsqrtf(sum / (float)p.K + p.eps);
+                // split-K or split fold: the raw partial sum, which the epilogue
+                // completes (the K-partner's, the upper chunks')
+                rowscale[rb * kBM + t] = (KS == 2 || FOLD2) ? ssum : rsqrtf(ssum / (float)p.K + p.eps);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(sready_bar(rb));
             }
@@ -429,10 +456,11 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         const T* bias = reinterpret_cast<const T*>(p.bias);
         const T* res = reinterpret_cast<const T*>(p.residual);
         bool ok = true;
+        float ss_upper = 0.f;  // RMS, split fold: the row's sum of squares over chunks 4-7
         if (FOLD2) {
             int fs = 0;
             uint32_t fph = 0;
-            ok = fold_upper(tile, rl, fs, fph);
+            ok = fold_tile(tile, rl, 4, fs, fph, ss_upper, 47);
         }
         ok = ok && wait_bar(tfull_bar(0), 0, p.status, p.timeout_ns, 42);
         tc_fence_after();
@@ -440,7 +468,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         float ss_own = 0.f;
         if (ok && PRO == PRO_RMS) {
             ok = wait_bar(sready_bar(0), 0, p.status, p.timeout_ns, 43);
-            if (ok) ss_own = rowscale[rl];
+            if (ok) ss_own = rowscale[rl] + ss_upper;
         }
         // this pair's MMAs are done, so this CTA's ring may take the partner's half
         __syncwarp();
@@ -592,13 +620,15 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
             const int buf = C::NBUF == 2 ? (it & 1) : 0;
             const uint32_t tph = C::NBUF == 2 ? (uint32_t)((it >> 1) & 1) : (uint32_t)(it & 1);
             const uint32_t bias_s = stage_bias(n0, q);
-            if (FOLD2 && !fold_upper(tile, q * 32 + (threadIdx.x & 31), fs, fph)) break;
+            float ss_upper = 0.f;  // RMS, split fold: the row's sum of squares over chunks 4-7
+            if (FOLD2 && !fold_tile(tile, q * 32 + lane, 4, fs, fph, ss_upper, 47)) break;
             if (!wait_bar(tfull_bar(buf), tph, p.status, p.timeout_ns, 40)) break;
             tc_fence_after();
             float rs = 1.f;
             if (PRO == PRO_RMS) {
                 if (!wait_bar(sready_bar(it & 1), (uint32_t)((it >> 1) & 1), p.status, p.timeout_ns, 41)) break;
                 rs = rowscale[(it & 1) * kBM + q * 32 + lane];
+                if (FOLD2) rs = rsqrtf((rs + ss_upper) / (float)p.K + p.eps);
             }
             const int row = m0 + q * 32 + lane;
             const bool row_ok = row < p.M;
