@@ -178,9 +178,11 @@ fl_status fl_device_status(void* stream);
 /*
  * Tuning overrides, for benchmarks and tests (process-wide, not thread-safe):
  *   FL_OPT_TILE_N:      0 = automatic, else the CTA tile width (128 or 256).
- *   FL_OPT_VARIANT:     0 = automatic, 1 = tile kernel, 2 = small-M split-K kernel,
- *                       3 = CTA-pair kernel (256 x 256 tiles on two SMs; not
- *                       used by the SwiGLU gate/up kernel).
+ *   FL_OPT_VARIANT:     0 = automatic, 1 = tile kernel, 2 = small-M split-K kernel
+ *                       (not used by the SwiGLU gate/up kernel, which then
+ *                       takes the tile kernel), 3 = CTA-pair kernel (256 x 256
+ *                       tiles on two SMs; for the gate/up kernel, Wg and Wu
+ *                       rows stacked in one tile).
  *   FL_OPT_TIMEOUT_MS:  limit of every device-side wait (default 2000).
  *   FL_OPT_SPLIT_K:     0 = automatic, else the K split of the small-M kernel (1..8).
  *   FL_OPT_PDL:         1 (default) = launch each kernel with a programmatic
@@ -195,8 +197,10 @@ fl_status fl_device_status(void* stream);
  *                       first weight tiles into shared memory before its
  *                       programmatic dependency on the previous kernel
  *                       resolves, so the weight stream of a decode step starts
- *                       while the previous layer finishes. Activations, gamma,
- *                       beta, bias and residual are still read only after it.
+ *                       while the previous layer finishes (the other kernels,
+ *                       which hold their SMs to the end of a grid, gained
+ *                       nothing from it). Activations, gamma, beta, bias and
+ *                       residual are still read only after it.
  * Returns FL_ERR_INVALID_ARG for an unknown key or a value out of range.
  */
 typedef enum {

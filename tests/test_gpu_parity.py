@@ -436,6 +436,55 @@ def test_weight_preload_chained_layers(dt, M, D):
     assert_close(y2, ref2, dt, f"preload layer 2 {dt} M={M} D={D}")
 
 
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("norm,M,D", [("rms", 512, 1024), ("rms", 4096, 2048), ("layer", 512, 1024),
+                                      ("layer", 4096, 2048), (None, 512, 1024), (None, 4096, 2048)])
+def test_weight_preload_chained_layers_on_cta_pairs(dt, norm, M, D):
+    """The weight-preload promise on the CTA-pair kernel (one tile per K-split
+    cluster at M=512, several tiles per pair at M=4096): two layers back to back,
+    the second reading the first's output, which a kernel just before overwrites
+    with NaN, so an activation read ahead of the dependency would show."""
+    kind = norm or "plain"
+    if norm is None:
+        t1 = syn.gemm_inputs(M, D, D, "gemm_bias", dt, seed=21)
+        t2 = syn.gemm_inputs(M, D, D, "gemm_bias", dt, seed=22)
+        x1, W1, W2 = dev(t1["A"]), dev(t1["W"]), dev(t2["W"])
+        b1, b2 = dev(t1["bias"]), dev(t2["bias"])
+    else:
+        t1 = syn.norm_gemm_inputs(M, D, D, norm, dt, seed=21)
+        t2 = syn.norm_gemm_inputs(M, D, D, norm, dt, seed=22)
+        x1, W1, W2 = dev(t1["x"]), dev(t1["W"]), dev(t2["W"])
+        g1, g2, be1, be2 = dev(t1["gamma"]), dev(t2["gamma"]), dev(t1["beta"]), dev(t2["beta"])
+    eps = 1e-5
+
+    def layer(x, W, i, out=None):
+        if norm is None:
+            return fl.gemm_epilogue(x, W, bias=(b1, b2)[i], out=out, pattern="gemm_bias")
+        return fl.norm_gemm(x, (g1, g2)[i], W, beta=(be1, be2)[i], out=out, eps=eps, norm=norm)
+
+    fl.set_option("variant", 3)
+    fl.set_option("weight_preload", 1)
+    try:
+        y1 = torch.empty((M, D), dtype=x1.dtype, device="cuda")
+        for _ in range(3):
+            y1.fill_(float("nan"))
+            layer(x1, W1, 0, out=y1)
+            y2 = layer(y1, W2, 1)
+        torch.cuda.synchronize()
+        fl.device_status()
+    finally:
+        fl.set_option("weight_preload", 0)
+        fl.set_option("variant", 0)
+    if norm is None:
+        ref1 = oracle.gemm_epilogue(f64(t1["A"]), f64(t1["W"]), f64(t1["bias"]), None, "gemm_bias")
+        ref2 = oracle.gemm_epilogue(f64(y1.cpu()), f64(t2["W"]), f64(t2["bias"]), None, "gemm_bias")
+    else:
+        ref1 = oracle.norm_gemm(f64(t1["x"]), f64(t1["gamma"]), f64(t1["beta"]), f64(t1["W"]), None, eps, norm)
+        ref2 = oracle.norm_gemm(f64(y1.cpu()), f64(t2["gamma"]), f64(t2["beta"]), f64(t2["W"]), None, eps, norm)
+    assert_close(y1, ref1, dt, f"pair preload layer 1 {kind} {dt} M={M} D={D}")
+    assert_close(y2, ref2, dt, f"pair preload layer 2 {kind} {dt} M={M} D={D}")
+
+
 # ---------------------------------------------------------------------------
 # bounded waits
 # ---------------------------------------------------------------------------
