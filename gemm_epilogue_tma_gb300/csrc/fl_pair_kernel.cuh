@@ -191,8 +191,15 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         const CUtensorMap* tb = DUAL && rank ? &p.tmB2 : &p.tmB;
         for (int kb = kb_begin; kb < kb_begin + S && kb < kb_end; ++kb) tma_prefetch_2d(tb, kb * kBK, nh);
     }
-    griddep_wait();
-    if (threadIdx.x == 0) griddep_launch_dependents();
+    // LayerNorm: this grid directly follows the row-statistics kernel, which
+    // lets dependents launch only after its own dependency wait, so every
+    // kernel before it has completed and every input but the statistics is
+    // final when this grid starts. Only the warps that read the statistics
+    // (fold, and with the split fold epilogue, warps) wait for it; the
+    // producer fills the ring meanwhile.
+    constexpr int kTrigger = PRO == PRO_LN ? 128 : 0;
+    if (PRO != PRO_LN || warp >= 4) griddep_wait();
+    if (threadIdx.x == kTrigger) griddep_launch_dependents();
     if (threadIdx.x == 0) FL_MARK(p, 1);
 
     // The bias of tile columns [n0, n0 + BN) into this epilogue warp's own
