@@ -30,18 +30,6 @@
 
 namespace fl {
 
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-    return r;
-}
-
 // Warp roles: 0 TMA producer, 1 MMA issuer, then four transform warps (norm
 // prologues; idle pair otherwise), then four epilogue warps (warp w reads
 // TMEM lanes 32 (w % 4) ...). Every warp joins the final reduction. Ten warps
@@ -88,7 +76,7 @@ __global__ void __launch_bounds__(splitk_threads<PRO>(), 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int splits = p.splits;
-    const int rank = (int)cluster_ctarank();
+    const int rank = (int)cluster_rank();
     const int tile = blockIdx.x / splits;
     const int m0 = (tile % p.num_m_blocks) * kBM;
     const int n0 = (tile / p.num_m_blocks) * BN;
@@ -348,8 +336,8 @@ __global__ void __launch_bounds__(splitk_threads<PRO>(), 1)
                     const uint32_t dst = ring + (uint32_t)me * slot_bytes;
                     for (int d = 0, k = 0; d < splits; ++d) {
                         if (d == me) continue;
-                        bulk_copy_to_cluster(mapa_shared(dst, (uint32_t)d), src0 + (uint32_t)k * slot_bytes, slot_bytes,
-                                             mapa_shared(recvd_bar, (uint32_t)d));
+                        bulk_copy_to_cluster(mapa_cluster(dst, (uint32_t)d), src0 + (uint32_t)k * slot_bytes, slot_bytes,
+                                             mapa_cluster(recvd_bar, (uint32_t)d));
                         ++k;
                     }
                 }
@@ -373,7 +361,7 @@ __global__ void __launch_bounds__(splitk_threads<PRO>(), 1)
             // my MMAs are done with my ring: peers may write their partials
             // of my slice into it
             for (int d = 0; d < splits; ++d)
-                if (d != rank) mbar_arrive_cluster(mapa_shared(peerfree_bar, (uint32_t)d));
+                if (d != rank) mbar_arrive_cluster(mapa_cluster(peerfree_bar, (uint32_t)d));
         }
         __syncwarp();
         cluster_arrive_relaxed();  // nothing below touches another CTA
