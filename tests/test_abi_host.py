@@ -35,6 +35,24 @@ def test_header_declares_the_boundary():
         assert n in names
 
 
+def header_enum(type_name):
+    """{enumerator: value} of `typedef enum { ... } type_name;` in include/fusedlin.h."""
+    src = open(os.path.join(ROOT, "include", "fusedlin.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    body = re.search(r"typedef enum\s*\{([^}]*)\}\s*" + type_name + r"\s*;", src).group(1)
+    return {k: int(v) for k, v in re.findall(r"(FL_[A-Z0-9_]+)\s*=\s*(\d+)", body)}
+
+
+def test_binding_enums_match_header():
+    pat = header_enum("fl_pattern")
+    assert {k[3:].lower(): v for k, v in pat.items()} == {n: i for i, n in enumerate(fl.PATTERNS)}
+    assert {k[len("FL_NORM_"):].lower(): v for k, v in header_enum("fl_norm_kind").items()} == fl.NORMS
+    acts = {k[len("FL_ACT_"):].lower().replace("_tanh", ""): v for k, v in header_enum("fl_act").items()}
+    assert acts == fl.ACTS
+    assert {k[3:].lower(): v for k, v in header_enum("fl_dtype").items()} == fl.DTYPE_CODES
+    assert {k[len("FL_OPT_"):].lower(): v for k, v in header_enum("fl_option").items()} == fl.OPTIONS
+
+
 def test_every_declared_symbol_is_exported(L):
     for name in declared_functions():
         assert hasattr(L, name), name
