@@ -59,7 +59,9 @@ bool overlap(const void* a, size_t na, const void* b, size_t nb) {
 // device information (cached per device)
 // ---------------------------------------------------------------------------
 struct DeviceInfo {
-    bool ready = false;
+    // set (release) once every field below is filled; read (acquire) before
+    // any of them, so a thread that sees it set also sees the fields
+    std::atomic<bool> ready{false};
     int sms = 0;
     int major = 0, minor = 0;
     int* status = nullptr;  // device address of g_fl_status
@@ -77,9 +79,9 @@ fl_status device_info(DeviceInfo** out) {
     if (e != cudaSuccess) return fail(FL_ERR_UNSUPPORTED, "no CUDA device: %s", cudaGetErrorString(e));
     if (dev < 0 || dev >= kMaxDevices) return fail(FL_ERR_UNSUPPORTED, "device index %d out of range", dev);
     DeviceInfo& d = g_dev[dev];
-    if (!d.ready) {
+    if (!d.ready.load(std::memory_order_acquire)) {
         std::lock_guard<std::mutex> lk(g_dev_mu);
-        if (!d.ready) {
+        if (!d.ready.load(std::memory_order_relaxed)) {
             cudaDeviceProp prop;
             e = cudaGetDeviceProperties(&prop, dev);
             if (e != cudaSuccess) return fail(FL_ERR_CUDA, "cudaGetDeviceProperties: %s", cudaGetErrorString(e));
@@ -97,7 +99,7 @@ fl_status device_info(DeviceInfo** out) {
             // keep freed scratch in the pool instead of returning it at every synchronisation
             uint64_t keep = 64ull << 20;
             cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
-            d.ready = true;
+            d.ready.store(true, std::memory_order_release);
         }
     }
     if (!(d.major == 10 && d.minor == 3))

@@ -57,7 +57,15 @@ fl_status scratch_address(void** out) {
 extern "C" fl_status fl_swiglu_ffn_noalloc(const void* x, const void* gamma, const void* Wg, const void* Wu,
                                            const void* Wd, const void* bias_down, void* out, int M, int D, int F,
                                            float eps, fl_dtype dtype, void* stream) {
-    if (M >= 1 && F >= 1 && (size_t)M * (size_t)F * 2 > kScratchBytes) {
+    // Host checks that need no device come first, so a rejected call makes no
+    // CUDA call at all (fl_swiglu_ffn repeats them with the full set of rules).
+    if (dtype != FL_F16 && dtype != FL_BF16)
+        return (fl_status)fl::set_last_error(FL_ERR_INVALID_ARG, "fl_swiglu_ffn_noalloc: bad dtype");
+    if (M < 1 || D < 1 || F < 1)
+        return (fl_status)fl::set_last_error(FL_ERR_INVALID_ARG, "fl_swiglu_ffn_noalloc: sizes must be positive");
+    if (x == nullptr || gamma == nullptr || Wg == nullptr || Wu == nullptr || Wd == nullptr || out == nullptr)
+        return (fl_status)fl::set_last_error(FL_ERR_INVALID_ARG, "fl_swiglu_ffn_noalloc: a required pointer is null");
+    if ((size_t)M * (size_t)F * 2 > kScratchBytes) {
         char msg[256];
         snprintf(msg, sizeof(msg),
                  "fl_swiglu_ffn_noalloc: h [%d, %d] needs %zu bytes, more than the library's fixed %zu-byte array; "

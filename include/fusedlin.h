@@ -35,8 +35,13 @@
  *     even.
  *   - stream is a cudaStream_t passed as void* (NULL = the legacy default
  *     stream). Every call is asynchronous on that stream.
- *   - The library allocates no device memory per call. The FFN's hidden
- *     activation lives in a caller-provided workspace.
+ *   - Device memory: fl_gemm_epilogue and the RMS form of fl_norm_gemm allocate
+ *     nothing. The LayerNorm form of fl_norm_gemm takes 8 bytes per row of
+ *     stream-ordered scratch for its row statistics from a library-owned
+ *     memory pool and frees it on the stream after the GEMM (see there).
+ *     fl_swiglu_ffn keeps its hidden activation in a caller-provided
+ *     workspace; fl_swiglu_ffn_noalloc keeps it in a fixed 8 MiB array of the
+ *     library instead. The library's other device state is one status word.
  *   - out may alias residual exactly (same pointer); no other aliasing of an
  *     output with an input is allowed.
  *   - Errors: a call that fails validation returns a non-zero fl_status
@@ -155,8 +160,12 @@ fl_status fl_swiglu_ffn(const void* x, const void* gamma, const void* Wg, const 
  *   most 8 MiB (for example M = 256 at F = 11008); larger calls return
  *   FL_ERR_WORKSPACE without launching.
  *   The call allocates nothing. Its first call on a device looks up the
- *   array's device address for that device (cudaGetSymbolAddress); make that
- *   first call before any stream capture.
+ *   array's device address for that device (cudaGetSymbolAddress); under
+ *   lazy module loading that lookup is also what loads the library's device
+ *   code and reserves the 8 MiB. So make the first call on each device at
+ *   initialisation time, before any stream capture. Sizes, dtype and
+ *   pointers are checked on the host before that lookup: a rejected call
+ *   makes no CUDA call.
  *   All calls share the array and it keeps the last call's h: two calls whose
  *   kernels overlap on the GPU (different streams, or different host threads)
  *   race on it and give wrong results.

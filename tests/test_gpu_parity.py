@@ -14,6 +14,7 @@ import gemm_epilogue_tma_gb300 as fl
 import oracle
 from gemm_epilogue_tma_gb300 import _build
 from gemm_epilogue_tma_gb300 import synthetic as syn
+import parity
 from parity import assert_close, sample_rows
 
 pytestmark = pytest.mark.gpu
@@ -43,7 +44,8 @@ def f64(t):
 
 
 def run_pattern(t, pattern, rows=None, out=None):
-    """Launch one of the nine patterns on GPU copies of t; oracle on `rows` (all if None)."""
+    """Launch one of the nine patterns on GPU copies of t; oracle and unfused
+    chain on `rows` (all if None). Returns (got, ref, chain)."""
     eps = 1e-5 if pattern == "layernorm_gemm" else 1e-6
     A, W = dev(t["A"]), dev(t["W"])
     if pattern == "rmsnorm_gemm":
@@ -56,10 +58,15 @@ def run_pattern(t, pattern, rows=None, out=None):
     torch.cuda.synchronize()
     sel = slice(None) if rows is None else rows
     res = t.get("residual")
-    ref = oracle.fused_pattern(pattern, f64(t["A"])[sel], f64(t["W"]), f64(t.get("bias")),
-                               None if res is None else f64(res)[sel], f64(t.get("gamma")), f64(t.get("beta")),
-                               eps=eps)
-    return got[sel] if rows is not None else got, ref
+    args = (f64(t["A"])[sel], f64(t["W"]), f64(t.get("bias")), None if res is None else f64(res)[sel],
+            f64(t.get("gamma")), f64(t.get("beta")))
+    ref = oracle.fused_pattern(pattern, *args, eps=eps)
+    chain = parity.chain_pattern(pattern, *args, eps, syn_dtype(t))
+    return (got[sel] if rows is not None else got), ref, chain
+
+
+def syn_dtype(t):
+    return "bf16" if t["A"].dtype == torch.bfloat16 else "f16"
 
 
 # ---------------------------------------------------------------------------
@@ -74,8 +81,8 @@ def test_all_patterns_ragged(dt, shape):
     M, N, K = shape
     t = syn.dense_layer_inputs(M, N, K, dt)
     for pattern in syn.PATTERNS:
-        got, ref = run_pattern(t, pattern)
-        assert_close(got, ref, dt, f"{pattern} {dt} {M}x{N}x{K}")
+        got, ref, chain = run_pattern(t, pattern)
+        assert_close(got, ref, dt, f"{pattern} {dt} {M}x{N}x{K}", chain=chain)
     fl.device_status()
 
 
@@ -87,8 +94,8 @@ def test_tile_widths(tile_n, dt):
     fl.set_option("tile_n", tile_n)
     try:
         for pattern in ("gemm_bias_gelu", "gemm_bias_residual", "gemm_silu", "rmsnorm_gemm", "layernorm_gemm"):
-            got, ref = run_pattern(t, pattern)
-            assert_close(got, ref, dt, f"{pattern} {dt} BN={tile_n}")
+            got, ref, chain = run_pattern(t, pattern)
+            assert_close(got, ref, dt, f"{pattern} {dt} BN={tile_n}", chain=chain)
     finally:
         fl.set_option("tile_n", 0)
 
@@ -103,8 +110,9 @@ def test_norm_gemm_bias_act(dt, norm, act):
     got = fl.norm_gemm(dev(t["x"]), dev(t["gamma"]), dev(t["W"]), beta=dev(t["beta"]), bias=dev(t["bias"]),
                        eps=eps, norm=norm, act=act)
     torch.cuda.synchronize()
-    ref = oracle.norm_gemm(f64(t["x"]), f64(t["gamma"]), f64(t["beta"]), f64(t["W"]), f64(t["bias"]), eps, norm, act)
-    assert_close(got, ref, dt, f"{norm} {act} {dt}")
+    args = (f64(t["x"]), f64(t["gamma"]), f64(t["beta"]), f64(t["W"]), f64(t["bias"]), eps, norm, act)
+    ref = oracle.norm_gemm(*args)
+    assert_close(got, ref, dt, f"{norm} {act} {dt}", chain=parity.chain_norm_gemm(*args, dt))
 
 
 def test_layernorm_without_beta_and_offset_rows():
@@ -116,6 +124,79 @@ def test_layernorm_without_beta_and_offset_rows():
     torch.cuda.synchronize()
     ref = oracle.norm_gemm(f64(x), f64(t["gamma"]), None, f64(t["W"]), None, 1e-5, "layer")
     assert_close(got, ref, "f16", "layernorm offset rows")
+
+
+# ---------------------------------------------------------------------------
+# degenerate rows: an all-zero row (a padding token) and constant rows
+# (LayerNorm variance exactly zero). Each has one correct result the oracle
+# gives exactly: RMS of a zero row scales 0 by 1/sqrt(eps), so out = 0;
+# LayerNorm of a zero or constant row is beta, so out = beta W^T.
+# ---------------------------------------------------------------------------
+def _with_degenerate_rows(x, values):
+    x = x.clone()
+    for i, v in enumerate(values):
+        if i < x.shape[0]:
+            x[i] = v
+    return x
+
+
+EDGE_VARIANTS = {
+    # name: (options, shape)
+    "auto": ({}, (133, 200, 456)),
+    "tile": ({"variant": 1}, (133, 200, 456)),
+    "splitk": ({"variant": 2, "split_k": 3}, (40, 136, 1000)),
+    "pair": ({"variant": 3}, (300, 264, 520)),
+    "pair_ksplit": ({"variant": 3, "split_k": 2}, (300, 520, 1000)),
+}
+
+
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("norm", ["rms", "layer"])
+@pytest.mark.parametrize("variant", list(EDGE_VARIANTS))
+def test_zero_and_constant_rows(dt, norm, variant):
+    opts, (M, N, K) = EDGE_VARIANTS[variant]
+    t = syn.norm_gemm_inputs(M, N, K, norm, dt, with_bias=True)
+    # zero row, constant rows of small, negative and large magnitude, then a
+    # row with a single non-zero entry
+    x = _with_degenerate_rows(t["x"], [0.0, 0.75, -3.0, 40.0])
+    x[4].zero_()
+    x[4, K // 2] = 2.5
+    eps = 1e-5
+    for k, v in opts.items():
+        fl.set_option(k, v)
+    try:
+        got = fl.norm_gemm(dev(x), dev(t["gamma"]), dev(t["W"]), beta=dev(t["beta"]), bias=dev(t["bias"]), eps=eps,
+                           norm=norm, act="none")
+        torch.cuda.synchronize()
+        fl.device_status()
+    finally:
+        for k in opts:
+            fl.set_option(k, 0)
+    args = (f64(x), f64(t["gamma"]), f64(t["beta"]), f64(t["W"]), f64(t["bias"]), eps, norm, "none")
+    ref = oracle.norm_gemm(*args)
+    assert_close(got, ref, dt, f"degenerate rows {norm} {dt} {variant}", chain=parity.chain_norm_gemm(*args, dt))
+    # the exact results of the zero row
+    want0 = (np.zeros(N) if norm == "rms" else f64(t["beta"]) @ f64(t["W"]).T) + f64(t["bias"])
+    tmax = parity.TOL[dt][0]
+    assert np.abs(got[0].double().cpu().numpy() - want0).max() <= tmax, f"zero row {norm} {dt} {variant}"
+
+
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("norm", ["rms", "layer"])
+@pytest.mark.parametrize("D", [1024, 4096])
+@pytest.mark.parametrize("row", ["zero", "constant"])
+def test_decode_single_degenerate_row(dt, norm, D, row):
+    """M = 1 (one decode token) whose row is all zeros or constant."""
+    t = syn.norm_gemm_inputs(1, D, D, norm, dt)
+    x = torch.zeros_like(t["x"]) if row == "zero" else torch.full_like(t["x"], -1.5)
+    eps = 1e-5
+    got = fl.norm_gemm(dev(x), dev(t["gamma"]), dev(t["W"]), beta=dev(t.get("beta")), eps=eps, norm=norm)
+    torch.cuda.synchronize()
+    fl.device_status()
+    ref = oracle.norm_gemm(f64(x), f64(t["gamma"]), f64(t.get("beta")), f64(t["W"]), None, eps, norm)
+    assert_close(got, ref, dt, f"decode {row} row {norm} {dt} D={D}")
+    if row == "zero" and norm == "rms":
+        assert bool((got == 0).all()), "RMSNorm of a zero row must give exactly zero"
 
 
 def test_residual_aliases_out():
@@ -138,8 +219,8 @@ def test_no_write_outside_out():
     buf = torch.full((pad + M * N + pad,), 1234.0, dtype=torch.float16, device="cuda")
     out = buf[pad:pad + M * N].view(M, N)
     for pattern in ("gemm_bias_gelu", "gemm_bias_residual", "rmsnorm_gemm", "layernorm_gemm"):
-        got, ref = run_pattern(t, pattern, out=out)
-        assert_close(got, ref, "f16", pattern)
+        got, ref, chain = run_pattern(t, pattern, out=out)
+        assert_close(got, ref, "f16", pattern, chain=chain)
         assert bool((buf[:pad] == 1234.0).all()) and bool((buf[pad + M * N:] == 1234.0).all()), pattern
 
 
@@ -166,8 +247,8 @@ def test_splitk_variant_all_patterns(dt, splits, shape):
     fl.set_option("split_k", splits)
     try:
         for pattern in syn.PATTERNS:
-            got, ref = run_pattern(t, pattern)
-            assert_close(got, ref, dt, f"split-K x{splits} {pattern} {dt} {M}x{N}x{K}")
+            got, ref, chain = run_pattern(t, pattern)
+            assert_close(got, ref, dt, f"split-K x{splits} {pattern} {dt} {M}x{N}x{K}", chain=chain)
         fl.device_status()
     finally:
         fl.set_option("variant", 0)
@@ -185,8 +266,8 @@ def test_splitk_uneven_column_slices(dt, splits):
     fl.set_option("split_k", splits)
     try:
         for pattern in syn.PATTERNS:
-            got, ref = run_pattern(t, pattern)
-            assert_close(got, ref, dt, f"split-K x{splits} BN=128 {pattern} {dt}")
+            got, ref, chain = run_pattern(t, pattern)
+            assert_close(got, ref, dt, f"split-K x{splits} BN=128 {pattern} {dt}", chain=chain)
         fl.device_status()
     finally:
         fl.set_option("variant", 0)
@@ -206,9 +287,9 @@ def test_splitk_wide_tiles_and_norm_bias_act(dt):
                 got = fl.norm_gemm(dev(t["x"]), dev(t["gamma"]), dev(t["W"]), beta=dev(t["beta"]),
                                    bias=dev(t["bias"]), eps=1e-5, norm=norm, act=act)
                 torch.cuda.synchronize()
-                ref = oracle.norm_gemm(f64(t["x"]), f64(t["gamma"]), f64(t["beta"]), f64(t["W"]), f64(t["bias"]),
-                                       1e-5, norm, act)
-                assert_close(got, ref, dt, f"split-K BN=128 {norm} {act}")
+                args = (f64(t["x"]), f64(t["gamma"]), f64(t["beta"]), f64(t["W"]), f64(t["bias"]), 1e-5, norm, act)
+                ref = oracle.norm_gemm(*args)
+                assert_close(got, ref, dt, f"split-K BN=128 {norm} {act}", chain=parity.chain_norm_gemm(*args, dt))
     finally:
         fl.set_option("variant", 0)
         fl.set_option("tile_n", 0)
@@ -231,8 +312,8 @@ def test_pair_variant_all_patterns(dt, tile_n, shape):
     try:
         rows = sample_rows(M, n=384)
         for pattern in syn.PATTERNS:
-            got, ref = run_pattern(t, pattern, rows=rows)
-            assert_close(got, ref, dt, f"pair BN={tile_n} {pattern} {dt} {M}x{N}x{K}")
+            got, ref, chain = run_pattern(t, pattern, rows=rows)
+            assert_close(got, ref, dt, f"pair BN={tile_n} {pattern} {dt} {M}x{N}x{K}", chain=chain)
         fl.device_status()
     finally:
         fl.set_option("variant", 0)
@@ -250,8 +331,8 @@ def test_pair_split_k_all_patterns(dt, shape):
     fl.set_option("split_k", 2)
     try:
         for pattern in syn.PATTERNS:
-            got, ref = run_pattern(t, pattern)
-            assert_close(got, ref, dt, f"pair split-K {pattern} {dt} {M}x{N}x{K}")
+            got, ref, chain = run_pattern(t, pattern)
+            assert_close(got, ref, dt, f"pair split-K {pattern} {dt} {M}x{N}x{K}", chain=chain)
         fl.device_status()
     finally:
         fl.set_option("variant", 0)
@@ -269,9 +350,9 @@ def test_pair_norm_bias_act_residual_alias(dt):
                 got = fl.norm_gemm(dev(t["x"]), dev(t["gamma"]), dev(t["W"]), beta=dev(t["beta"]),
                                    bias=dev(t["bias"]), eps=1e-5, norm=norm, act=act)
                 torch.cuda.synchronize()
-                ref = oracle.norm_gemm(f64(t["x"]), f64(t["gamma"]), f64(t["beta"]), f64(t["W"]), f64(t["bias"]),
-                                       1e-5, norm, act)
-                assert_close(got, ref, dt, f"pair {norm} {act}")
+                args = (f64(t["x"]), f64(t["gamma"]), f64(t["beta"]), f64(t["W"]), f64(t["bias"]), 1e-5, norm, act)
+                ref = oracle.norm_gemm(*args)
+                assert_close(got, ref, dt, f"pair {norm} {act}", chain=parity.chain_norm_gemm(*args, dt))
         r = syn.gemm_inputs(M, N, K, "gemm_bias_residual", dt)
         res = dev(r["residual"])
         fl.gemm_epilogue(dev(r["A"]), dev(r["W"]), bias=dev(r["bias"]), residual=res, out=res,
@@ -289,15 +370,15 @@ def test_pair_norm_bias_act_residual_alias(dt):
 def test_gemm_bias_gelu_512x1024x1024_all_elements():
     """fp16 gemm_bias_gelu, A[512,1024], W[1024,1024], bias[1024], seed 0."""
     t = syn.gemm_inputs(512, 1024, 1024, "gemm_bias_gelu", "f16", seed=0)
-    got, ref = run_pattern(t, "gemm_bias_gelu")
-    assert_close(got, ref, "f16", "gemm_bias_gelu 512x1024x1024")
+    got, ref, chain = run_pattern(t, "gemm_bias_gelu")
+    assert_close(got, ref, "f16", "gemm_bias_gelu 512x1024x1024", chain=chain)
 
 
 def test_rmsnorm_gemm_512x4096x4096_all_elements():
     """fp16 rmsnorm_gemm, x[512,4096], gamma ~ N(1,0.1), eps 1e-6, W[4096,4096], no bias."""
     t = syn.gemm_inputs(512, 4096, 4096, "rmsnorm_gemm", "f16")
-    got, ref = run_pattern(t, "rmsnorm_gemm")
-    assert_close(got, ref, "f16", "rmsnorm_gemm 512x4096x4096")
+    got, ref, chain = run_pattern(t, "rmsnorm_gemm")
+    assert_close(got, ref, "f16", "rmsnorm_gemm 512x4096x4096", chain=chain)
 
 
 @pytest.mark.parametrize("dt", DTYPES)
@@ -306,8 +387,8 @@ def test_nine_patterns_n4096_k4096_sampled_rows(dt, M):
     t = syn.dense_layer_inputs(M, 4096, 4096, dt)
     rows = sample_rows(M)
     for pattern in syn.PATTERNS:
-        got, ref = run_pattern(t, pattern, rows=rows)
-        assert_close(got, ref, dt, f"{pattern} {dt} M={M}")
+        got, ref, chain = run_pattern(t, pattern, rows=rows)
+        assert_close(got, ref, dt, f"{pattern} {dt} M={M}", chain=chain)
     fl.device_status()
 
 
@@ -322,7 +403,8 @@ def test_swiglu_ffn_4096x4096x11008_sampled_rows():
     rows = sample_rows(M, n=64)
     f = {k: f64(v) for k, v in t.items()}
     ref = oracle.swiglu_ffn(f["x"][rows], f["gamma"], f["Wg"], f["Wu"], f["Wd"], None, 1e-6, "bf16")
-    assert_close(got[rows], ref, "bf16", "swiglu 4096x4096x11008")
+    chain = parity.chain_swiglu_ffn(f["x"][rows], f["gamma"], f["Wg"], f["Wu"], f["Wd"], None, 1e-6, "bf16")
+    assert_close(got[rows], ref, "bf16", "swiglu 4096x4096x11008", chain=chain)
     # the workspace holds h: check it against the oracle's unrounded hidden activation too
     h = ws.view(torch.bfloat16).view(M, F)[rows]
     href = oracle.swiglu_hidden(f["x"][rows], f["gamma"], f["Wg"], f["Wu"], 1e-6)
@@ -340,7 +422,8 @@ def test_swiglu_ffn_small_all_elements(dt, with_bias, shape):
     torch.cuda.synchronize()
     f = {k: f64(v) for k, v in t.items()}
     ref = oracle.swiglu_ffn(f["x"], f["gamma"], f["Wg"], f["Wu"], f["Wd"], f["bias_down"], 1e-6, dt)
-    assert_close(got, ref, dt, f"swiglu {dt} {shape}")
+    chain = parity.chain_swiglu_ffn(f["x"], f["gamma"], f["Wg"], f["Wu"], f["Wd"], f["bias_down"], 1e-6, dt)
+    assert_close(got, ref, dt, f"swiglu {dt} {shape}", chain=chain)
 
 
 @pytest.mark.parametrize("dt", DTYPES)
@@ -351,8 +434,9 @@ def test_decode_sweep_rmsnorm_all_elements(dt, D, M):
     t = syn.norm_gemm_inputs(M, D, D, "rms", dt)
     got = fl.norm_gemm(dev(t["x"]), dev(t["gamma"]), dev(t["W"]), eps=1e-6, norm="rms")
     torch.cuda.synchronize()
-    ref = oracle.norm_gemm(f64(t["x"]), f64(t["gamma"]), None, f64(t["W"]), None, 1e-6, "rms")
-    assert_close(got, ref, dt, f"decode rms {dt} M={M} D={D}")
+    args = (f64(t["x"]), f64(t["gamma"]), None, f64(t["W"]), None, 1e-6, "rms", "none")
+    ref = oracle.norm_gemm(*args)
+    assert_close(got, ref, dt, f"decode rms {dt} M={M} D={D}", chain=parity.chain_norm_gemm(*args, dt))
 
 
 @pytest.mark.parametrize("dt", DTYPES)
@@ -372,7 +456,8 @@ def test_swiglu_ffn_on_cta_pairs(dt, with_bias, shape):
         fl.set_option("variant", 0)
     f = {k: f64(v) for k, v in t.items()}
     ref = oracle.swiglu_ffn(f["x"], f["gamma"], f["Wg"], f["Wu"], f["Wd"], f["bias_down"], 1e-6, dt)
-    assert_close(got, ref, dt, f"swiglu pairs {dt} {shape}")
+    chain = parity.chain_swiglu_ffn(f["x"], f["gamma"], f["Wg"], f["Wu"], f["Wd"], f["bias_down"], 1e-6, dt)
+    assert_close(got, ref, dt, f"swiglu pairs {dt} {shape}", chain=chain)
 
 
 @pytest.mark.parametrize("dt", DTYPES)
@@ -497,5 +582,5 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     fl.device_status()  # cleared
     # the context still works
     t = syn.gemm_inputs(64, 64, 64, "gemm_bias", "f16")
-    got, ref = run_pattern(t, "gemm_bias")
-    assert_close(got, ref, "f16", "after timeout")
+    got, ref, chain = run_pattern(t, "gemm_bias")
+    assert_close(got, ref, "f16", "after timeout", chain=chain)
