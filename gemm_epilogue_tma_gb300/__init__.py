@@ -8,6 +8,9 @@ missing, every call raises; there is no fallback path.
 Entry points mirror the C ABI declared in include/fusedlin.h:
     gemm_epilogue(A, W, bias, residual, out, pattern)   seven GEMM-first patterns
     norm_gemm(x, gamma, W, beta, bias, out, eps, norm, act)
+    norm_gemm_multi(x, gamma, Ws, beta, biases, outs, acts, eps, norm)   one norm, several weights
+    input_bias_gemm(A, bias_in, W, bias, residual, out, act)             (A + bias_in) W^T epilogue
+    rms_norm(x, gamma, out, eps)                                          standalone RMSNorm
     swiglu_ffn(x, gamma, Wg, Wu, Wd, bias_down, out, eps, workspace)
 """
 from __future__ import annotations
@@ -36,6 +39,9 @@ SIGNATURES = {
     "fl_swiglu_ffn_workspace_size": (_sz, [_i, _i, _i]),
     "fl_swiglu_ffn": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _f, _vp, _sz, _i, _vp]),
     "fl_swiglu_ffn_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _f, _i, _vp]),
+    "fl_norm_gemm_multi": (_i, [_vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _i, _i, _f, _i, _i, _vp]),
+    "fl_input_bias_gemm": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
+    "fl_rms_norm": (_i, [_vp, _vp, _vp, _i, _i, _f, _i, _vp]),
     "fl_last_error": (ctypes.c_char_p, []),
     "fl_device_status": (_i, [_vp]),
     "fl_set_option": (_i, [_i, _i]),
@@ -143,6 +149,65 @@ def norm_gemm(x, gamma, W, beta=None, bias=None, out=None, eps=1e-6, norm="rms",
     _check_tensors(x.dtype, x=x, gamma=gamma, W=W, beta=beta, bias=bias, out=out)
     _check(lib().fl_norm_gemm(_ptr(x), _ptr(gamma), _ptr(beta), _ptr(W), _ptr(bias), _ptr(out), M, N, K,
                               float(eps), NORMS[norm], ACTS[act], _dtype_code(x), _stream(stream)))
+    return out
+
+
+MAX_OUTPUTS = 4
+
+
+def norm_gemm_multi(x, gamma, Ws, beta=None, biases=None, outs=None, acts=None, eps=1e-6, norm="rms", stream=None):
+    """outs[i][M,N_i] = act_i(norm(x) Ws[i]^T + biases[i]) for every weight in one launch."""
+    import torch
+    n = len(Ws)
+    if not 1 <= n <= MAX_OUTPUTS:
+        raise ValueError(f"1..{MAX_OUTPUTS} weights, got {n}")
+    M, K = x.shape
+    for i, W in enumerate(Ws):
+        if W.shape[1] != K:
+            raise ValueError(f"Ws[{i}] has shape {tuple(W.shape)}, expected [N, {K}]")
+    if outs is None:
+        outs = [torch.empty((M, W.shape[0]), dtype=x.dtype, device=x.device) for W in Ws]
+    biases = list(biases) if biases is not None else [None] * n
+    acts = list(acts) if acts is not None else ["none"] * n
+    if len(outs) != n or len(biases) != n or len(acts) != n:
+        raise ValueError("Ws, outs, biases and acts must have the same length")
+    _check_tensors(x.dtype, x=x, gamma=gamma, beta=beta,
+                   **{f"W{i}": W for i, W in enumerate(Ws)}, **{f"out{i}": o for i, o in enumerate(outs)},
+                   **{f"bias{i}": b for i, b in enumerate(biases)})
+    arr = ctypes.c_void_p * n
+    W_arr = arr(*[W.data_ptr() for W in Ws])
+    b_arr = arr(*[(b.data_ptr() if b is not None else None) for b in biases])
+    o_arr = arr(*[o.data_ptr() for o in outs])
+    N_arr = (ctypes.c_int * n)(*[W.shape[0] for W in Ws])
+    a_arr = (ctypes.c_int * n)(*[ACTS[a] for a in acts])
+    _check(lib().fl_norm_gemm_multi(_ptr(x), _ptr(gamma), _ptr(beta), n, W_arr, b_arr, o_arr, N_arr, a_arr, M, K,
+                                    float(eps), NORMS[norm], _dtype_code(x), _stream(stream)))
+    return outs
+
+
+def input_bias_gemm(A, bias_in, W, bias=None, residual=None, out=None, act="none", stream=None):
+    """out[M,N] = act((A + bias_in) W^T + bias) (+ residual); bias_in runs along K."""
+    import torch
+    M, K = A.shape
+    N = W.shape[0]
+    if W.shape[1] != K:
+        raise ValueError(f"W has shape {tuple(W.shape)}, expected [N, {K}]")
+    if out is None:
+        out = torch.empty((M, N), dtype=A.dtype, device=A.device)
+    _check_tensors(A.dtype, A=A, bias_in=bias_in, W=W, bias=bias, residual=residual, out=out)
+    _check(lib().fl_input_bias_gemm(_ptr(A), _ptr(bias_in), _ptr(W), _ptr(bias), _ptr(residual), _ptr(out), M, N,
+                                    K, ACTS[act], _dtype_code(A), _stream(stream)))
+    return out
+
+
+def rms_norm(x, gamma, out=None, eps=1e-6, stream=None):
+    """out[M,K] = x * gamma / sqrt(mean(x^2) + eps), rounded once (out may be x)."""
+    import torch
+    M, K = x.shape
+    if out is None:
+        out = torch.empty_like(x)
+    _check_tensors(x.dtype, x=x, gamma=gamma, out=out)
+    _check(lib().fl_rms_norm(_ptr(x), _ptr(gamma), _ptr(out), M, K, float(eps), _dtype_code(x), _stream(stream)))
     return out
 
 

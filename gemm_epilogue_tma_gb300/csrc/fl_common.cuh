@@ -46,6 +46,11 @@ struct DTypeOps<DT_F16> {
         __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
         return *reinterpret_cast<uint32_t*>(&r);
     }
+    // a + b per 16-bit lane, rounded once (IEEE addition)
+    __device__ static __forceinline__ uint32_t add2(uint32_t a, uint32_t b) {
+        __half2 r = __hadd2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+        return *reinterpret_cast<uint32_t*>(&r);
+    }
 };
 
 template <>
@@ -69,6 +74,10 @@ struct DTypeOps<DT_BF16> {
     }
     __device__ static __forceinline__ uint32_t mul2(uint32_t a, uint32_t b) {
         __nv_bfloat162 r = __hmul2(*reinterpret_cast<__nv_bfloat162*>(&a), *reinterpret_cast<__nv_bfloat162*>(&b));
+        return *reinterpret_cast<uint32_t*>(&r);
+    }
+    __device__ static __forceinline__ uint32_t add2(uint32_t a, uint32_t b) {
+        __nv_bfloat162 r = __hadd2(*reinterpret_cast<__nv_bfloat162*>(&a), *reinterpret_cast<__nv_bfloat162*>(&b));
         return *reinterpret_cast<uint32_t*>(&r);
     }
 };
@@ -128,6 +137,21 @@ static __device__ __noinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity
         if (globaltimer_ns() - t0 > ns) return false;
     }
     return true;
+}
+
+// Output of a global column block: the outputs of a launch lie side by side
+// along N, output i taking column blocks [nb0[i], nb0[i + 1]).
+struct OutSel {
+    int oi;  // output index
+    int nb;  // column block within that output
+};
+
+__device__ __forceinline__ OutSel out_sel(const GemmParams& p, int nb) {
+    int oi = 0;
+#pragma unroll
+    for (int i = 1; i < kMaxOut; ++i)
+        if (i < p.n_out && nb >= p.nb0[i]) oi = i;
+    return OutSel{oi, nb - p.nb0[oi]};
 }
 
 // Hardware tanh (one special-function op; relative error about 2^-11).

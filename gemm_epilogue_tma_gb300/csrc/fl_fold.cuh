@@ -1,5 +1,5 @@
-// Norm prologue work on a staged activation tile, shared by the tile and the
-// split-K kernels.
+// Prologue work on a staged activation tile (RMSNorm, LayerNorm, input bias),
+// shared by the tile, CTA-pair and split-K kernels.
 //
 // The activation stage holds `box_rows` rows of 64 fp16/bf16 (128 bytes, 128B
 // swizzle: the 16-byte chunk j of row r sits at chunk position j ^ (r & 7)).
@@ -70,6 +70,23 @@ __device__ __forceinline__ void fold_rms_stage(uint32_t stage, uint32_t gamma_sl
             const uint32_t a = fold_row_addr(stage, (t >> 3) + 16 * i, j);
             st_shared_v4(a, xv[i].x, xv[i].y, xv[i].z, xv[i].w);
         }
+}
+
+// Input-bias fold: chunk := x + b (b along K), rounded once to the dtype.
+template <int DT>
+__device__ __forceinline__ void fold_add_stage(uint32_t stage, uint32_t b_slice, int t, int ni) {
+    using Ops = DTypeOps<DT>;
+    const int j = t & 7;
+    const uint4 b = ld_shared_v4(b_slice + j * 16);
+    uint4 xv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        if (i < ni) xv[i] = ld_shared_v4(fold_row_addr(stage, (t >> 3) + 16 * i, j));
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        if (i < ni)
+            st_shared_v4(fold_row_addr(stage, (t >> 3) + 16 * i, j), Ops::add2(xv[i].x, b.x), Ops::add2(xv[i].y, b.y),
+                         Ops::add2(xv[i].z, b.z), Ops::add2(xv[i].w, b.w));
 }
 
 // LayerNorm fold: chunk := (x - mean) * rstd * gamma + beta, in fp32, rounded once.
@@ -163,6 +180,19 @@ __device__ __forceinline__ void fold_rms_compute(const FoldRegs<NJ, false>& r, f
     }
 }
 
+// Input bias: chunk := x + b (the bias slice sits where gamma would).
+template <int DT, int NJ>
+__device__ __forceinline__ void fold_add_compute(const FoldRegs<NJ, false>& r, uint32_t (&o)[4 * NJ]) {
+    using Ops = DTypeOps<DT>;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+        o[4 * j + 0] = Ops::add2(r.x[j].x, r.g[j].x);
+        o[4 * j + 1] = Ops::add2(r.x[j].y, r.g[j].y);
+        o[4 * j + 2] = Ops::add2(r.x[j].z, r.g[j].z);
+        o[4 * j + 3] = Ops::add2(r.x[j].w, r.g[j].w);
+    }
+}
+
 // LayerNorm: chunk := fma(fma(x, rstd, -mean * rstd), gamma, beta) in fp32,
 // one rounding to the dtype (the fp32 error stays relative to
 // |mean| * 2^-24, far below it). Element pairs go through the paired fp32
@@ -193,6 +223,14 @@ __device__ __forceinline__ void fold_rms_row(uint32_t stage, uint32_t gamma_slic
     FoldRegs<8, false> r;
     fold_row_load(r, stage, gamma_slice, false, t, 0);
     fold_rms_compute<DT>(r, ss, o);
+}
+
+// Whole-row input-bias fold (chunks 0-7), loads issued before any use.
+template <int DT>
+__device__ __forceinline__ void fold_add_row(uint32_t stage, uint32_t b_slice, int t, uint32_t (&o)[32]) {
+    FoldRegs<8, false> r;
+    fold_row_load(r, stage, b_slice, false, t, 0);
+    fold_add_compute<DT>(r, o);
 }
 
 // LayerNorm fold of chunks [J0, J0 + NJ) of row t, loads issued before any use.

@@ -98,9 +98,11 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&p.tmA);
-        tma_prefetch_desc(&p.tmB);
+        for (int i = 0; i < p.n_out; ++i) {
+            tma_prefetch_desc(&p.tmB[i]);
+            tma_prefetch_desc(&p.tmOut[i]);
+        }
         if (DUAL) tma_prefetch_desc(&p.tmB2);
-        tma_prefetch_desc(&p.tmOut);
         if (PRO != PRO_NONE) tma_prefetch_desc(&p.tmGamma);
         if (PRO == PRO_LN && p.beta != nullptr) tma_prefetch_desc(&p.tmBeta);
     }
@@ -117,9 +119,10 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     // weight tiles may run early: L2 is the point of coherence, so it cannot
     // return stale data.
     if (warp == 0 && lane == 0 && blockIdx.x < p.num_tiles) {
-        const int n0 = (blockIdx.x / p.num_m_blocks) * BN;
+        const OutSel o = out_sel(p, blockIdx.x / p.num_m_blocks);
+        const int n0 = o.nb * BN;
         for (int kb = 0; kb < S && kb < nk; ++kb) {
-            tma_prefetch_2d(&p.tmB, kb * kBK, n0);
+            tma_prefetch_2d(&p.tmB[o.oi], kb * kBK, n0);
             if (DUAL) tma_prefetch_2d(&p.tmB2, kb * kBK, n0);
         }
     }
@@ -137,7 +140,9 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                                         (PRO == PRO_LN && p.beta != nullptr ? 128u : 0u);
             for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
                 const int m0 = (tile % p.num_m_blocks) * kBM;
-                const int n0 = (tile / p.num_m_blocks) * BN;
+                const OutSel o = out_sel(p, tile / p.num_m_blocks);
+                const int n0 = o.nb * BN;
+                const CUtensorMap* tb = &p.tmB[o.oi];
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!wait_bar(empty_bar(s), ph ^ 1u, p.status, p.timeout_ns, 1)) {
                         ok = false;
@@ -145,7 +150,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                     }
                     mbar_arrive_expect_tx(full_bar(s), main_bytes);
                     tma_load_2d(stage_a(s), &p.tmA, full_bar(s), kb * kBK, m0);
-                    tma_load_2d(stage_b(s), &p.tmB, full_bar(s), kb * kBK, n0);
+                    tma_load_2d(stage_b(s), tb, full_bar(s), kb * kBK, n0);
                     if (DUAL) tma_load_2d(stage_b2(s), &p.tmB2, full_bar(s), kb * kBK, n0);
                     if (PRO != PRO_NONE) {
                         tma_load_2d(gb_slot(s), &p.tmGamma, full_bar(s), kb * kBK, 0);
@@ -249,6 +254,8 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                 uint32_t o[32];
                 if (PRO == PRO_RMS) {
                     fold_rms_row<DT>(stage_a(s), gb_slot(s), t, ss, o);
+                } else if (PRO == PRO_ADD) {
+                    fold_add_row<DT>(stage_a(s), gb_slot(s), t, o);
                 } else {
                     uint32_t (&lo)[16] = *reinterpret_cast<uint32_t(*)[16]>(&o[0]);
                     uint32_t (&hi)[16] = *reinterpret_cast<uint32_t(*)[16]>(&o[16]);
@@ -312,6 +319,8 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                 // past K are zero in x, gamma and beta, so they stay zero
                 if (PRO == PRO_RMS)
                     fold_rms_stage<DT>(stage_a(s), gb_slot(s), t, 8, ss);
+                else if (PRO == PRO_ADD)
+                    fold_add_stage<DT>(stage_a(s), gb_slot(s), t, 8);
                 else
                     fold_ln_stage<DT>(stage_a(s), gb_slot(s), p.beta != nullptr, t, 8, mean, rstd);
                 fence_proxy_async_smem();
@@ -348,11 +357,14 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         const int sw = lane & 7;
         int it = 0;
         using T = uint16_t;
-        const T* bias = reinterpret_cast<const T*>(p.bias);
         const T* res = reinterpret_cast<const T*>(p.residual);
         for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
             const int m0 = (tile % p.num_m_blocks) * kBM;
-            const int n0 = (tile / p.num_m_blocks) * BN;
+            const OutSel o = out_sel(p, tile / p.num_m_blocks);
+            const int n0 = o.nb * BN;
+            const int N = p.N[o.oi];
+            const int act = p.act[o.oi];
+            const T* bias = reinterpret_cast<const T*>(p.bias[o.oi]);
             const int buf = NBUF == 2 ? (it & 1) : 0;
             const uint32_t tph = NBUF == 2 ? (uint32_t)((it >> 1) & 1) : (uint32_t)(it & 1);
             if (!wait_bar(tfull_bar(buf), tph, p.status, p.timeout_ns, 8)) break;
@@ -370,7 +382,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
             // after the last chunk's TMEM load
             int nchunks = 0;
             if (m0 + q * 32 < p.M)
-                while (nchunks < BN / 64 && n0 + nchunks * 64 < p.N) ++nchunks;
+                while (nchunks < BN / 64 && n0 + nchunks * 64 < N) ++nchunks;
             bool released = false;
             auto release_acc = [&]() {
                 tc_fence_before();
@@ -406,7 +418,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                             if (bias != nullptr) {
 #pragma unroll
                                 for (int j = 0; j < 4; ++j) {
-                                    if (cbase + j * 8 < p.N) {
+                                    if (cbase + j * 8 < N) {
                                         const uint4 bv = ldg_v4(bias + cbase + j * 8);
                                         const float2 b0 = Ops::unpack(bv.x), b1 = Ops::unpack(bv.y),
                                                      b2 = Ops::unpack(bv.z), b3 = Ops::unpack(bv.w);
@@ -417,15 +429,15 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                                     }
                                 }
                             }
-                            if (p.act != ACT_NONE) {
+                            if (act != ACT_NONE) {
 #pragma unroll
-                                for (int e = 0; e < 32; ++e) v[e] = act_apply(p.act, v[e]);
+                                for (int e = 0; e < 32; ++e) v[e] = act_apply(act, v[e]);
                             }
                             if (res != nullptr && row_ok) {
-                                const T* rrow = res + (size_t)row * p.N;
+                                const T* rrow = res + (size_t)row * N;
 #pragma unroll
                                 for (int j = 0; j < 4; ++j) {
-                                    if (cbase + j * 8 < p.N) {
+                                    if (cbase + j * 8 < N) {
                                         const uint4 rv = *reinterpret_cast<const uint4*>(rrow + cbase + j * 8);
                                         const float2 r0 = Ops::unpack(rv.x), r1 = Ops::unpack(rv.y),
                                                      r2 = Ops::unpack(rv.z), r3 = Ops::unpack(rv.w);
@@ -455,7 +467,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&p.tmOut, ebuf, col0, m0 + q * 32);
+                        tma_store_2d(&p.tmOut[o.oi], ebuf, col0, m0 + q * 32);
                         bulk_commit_group();
                     }
                 }

@@ -151,6 +151,59 @@ fl_status encode_2d(CUtensorMap* m, int dt, const void* ptr, uint64_t inner, uin
 }
 
 // ---------------------------------------------------------------------------
+// outputs of one launch
+// ---------------------------------------------------------------------------
+// One or more outputs computed from the same (prologue-transformed)
+// activation: output i = act_i(A' W_i^T + bias_i), laid side by side along N.
+struct OutDesc {
+    const void* W;     // [N, K]
+    const void* bias;  // [N] or null
+    void* out;         // [M, N]
+    int N;
+    int act;
+};
+struct Outs {
+    int n = 0;
+    OutDesc o[fl::kMaxOut];
+};
+
+Outs single_out(const void* W, const void* bias, void* out, int N, int act) {
+    Outs r;
+    r.n = 1;
+    r.o[0] = OutDesc{W, bias, out, N, act};
+    return r;
+}
+
+// Column blocks of width b over all outputs (each output starts a new block).
+long long nblocks(const Outs& outs, int b) {
+    long long n = 0;
+    for (int i = 0; i < outs.n; ++i) n += (outs.o[i].N + b - 1) / b;
+    return n;
+}
+
+// Per-output parameters of a launch whose tiles are `width` columns wide.
+// The weight maps have boxes of `b_rows` rows.
+fl_status fill_outputs(GemmParams& p, int dt, const Outs& outs, int M, int K, int width, int b_rows) {
+    fl_status st;
+    p.n_out = outs.n;
+    int nb = 0;
+    for (int i = 0; i < outs.n; ++i) {
+        const OutDesc& o = outs.o[i];
+        if ((st = encode_2d(&p.tmB[i], dt, o.W, K, o.N, fl::kBK, b_rows)) != FL_OK) return st;
+        if ((st = encode_2d(&p.tmOut[i], dt, o.out, o.N, M, 64, 32)) != FL_OK) return st;
+        p.bias[i] = o.bias;
+        p.out_ptr[i] = o.out;
+        p.N[i] = o.N;
+        p.act[i] = o.act;
+        p.nb0[i] = nb;
+        nb += (o.N + width - 1) / width;
+    }
+    for (int i = outs.n; i <= fl::kMaxOut; ++i) p.nb0[i] = nb;
+    p.num_n_blocks = nb;
+    return FL_OK;
+}
+
+// ---------------------------------------------------------------------------
 // tile kernel dispatch
 // ---------------------------------------------------------------------------
 cudaError_t dispatch_tile(int dt, int bn, int pro, bool dual, const GemmParams& p, int grid, cudaStream_t s) {
@@ -162,6 +215,8 @@ cudaError_t dispatch_tile(int dt, int bn, int pro, bool dual, const GemmParams& 
     FL_CASE(0, 256, 1, false)
     FL_CASE(0, 128, 2, false)
     FL_CASE(0, 256, 2, false)
+    FL_CASE(0, 128, 3, false)
+    FL_CASE(0, 256, 3, false)
     FL_CASE(0, 128, 1, true)
     FL_CASE(1, 128, 0, false)
     FL_CASE(1, 256, 0, false)
@@ -169,6 +224,8 @@ cudaError_t dispatch_tile(int dt, int bn, int pro, bool dual, const GemmParams& 
     FL_CASE(1, 256, 1, false)
     FL_CASE(1, 128, 2, false)
     FL_CASE(1, 256, 2, false)
+    FL_CASE(1, 128, 3, false)
+    FL_CASE(1, 256, 3, false)
     FL_CASE(1, 128, 1, true)
 #undef FL_CASE
     return cudaErrorInvalidValue;
@@ -177,18 +234,10 @@ cudaError_t dispatch_tile(int dt, int bn, int pro, bool dual, const GemmParams& 
 cudaError_t dispatch_splitk(int dt, int bn, int pro, const GemmParams& p, int grid, int splits, cudaStream_t s) {
 #define FL_CASE(DT, BN, PRO) \
     if (dt == DT && bn == BN && pro == PRO) return fl::launch_splitk<DT, BN, PRO>(p, grid, splits, s);
-    FL_CASE(0, 64, 0)
-    FL_CASE(0, 64, 1)
-    FL_CASE(0, 64, 2)
-    FL_CASE(0, 128, 0)
-    FL_CASE(0, 128, 1)
-    FL_CASE(0, 128, 2)
-    FL_CASE(1, 64, 0)
-    FL_CASE(1, 64, 1)
-    FL_CASE(1, 64, 2)
-    FL_CASE(1, 128, 0)
-    FL_CASE(1, 128, 1)
-    FL_CASE(1, 128, 2)
+    FL_CASE(0, 64, 0) FL_CASE(0, 64, 1) FL_CASE(0, 64, 2) FL_CASE(0, 64, 3)
+    FL_CASE(0, 128, 0) FL_CASE(0, 128, 1) FL_CASE(0, 128, 2) FL_CASE(0, 128, 3)
+    FL_CASE(1, 64, 0) FL_CASE(1, 64, 1) FL_CASE(1, 64, 2) FL_CASE(1, 64, 3)
+    FL_CASE(1, 128, 0) FL_CASE(1, 128, 1) FL_CASE(1, 128, 2) FL_CASE(1, 128, 3)
 #undef FL_CASE
     return cudaErrorInvalidValue;
 }
@@ -225,22 +274,23 @@ bool split_geom(int bn, int a_rows, int splits, fl::SplitGeom* g) {
 
 int max_clusters(int dt, int bn, int pro, int splits, int a_rows, int smem) {
     // cached per (dtype, width, prologue, cluster size, box height); single device assumed per process slot
-    static std::atomic<int> cache[2][2][3][9][8];
+    static std::atomic<int> cache[2][2][4][9][8];
     const int bi = bn == 128 ? 1 : 0;
     const int ai = (a_rows / 16 - 1) & 7;
     int v = cache[dt][bi][pro][splits][ai].load();
     if (v != 0) return v;
 #define FL_Q(DT, BN, PRO) \
     if (dt == DT && bn == BN && pro == PRO) v = fl::splitk_max_clusters<DT, BN, PRO>(splits, smem);
-    FL_Q(0, 64, 0) FL_Q(0, 64, 1) FL_Q(0, 64, 2) FL_Q(0, 128, 0) FL_Q(0, 128, 1) FL_Q(0, 128, 2)
-    FL_Q(1, 64, 0) FL_Q(1, 64, 1) FL_Q(1, 64, 2) FL_Q(1, 128, 0) FL_Q(1, 128, 1) FL_Q(1, 128, 2)
+    FL_Q(0, 64, 0) FL_Q(0, 64, 1) FL_Q(0, 64, 2) FL_Q(0, 64, 3) FL_Q(0, 128, 0) FL_Q(0, 128, 1) FL_Q(0, 128, 2)
+    FL_Q(0, 128, 3) FL_Q(1, 64, 0) FL_Q(1, 64, 1) FL_Q(1, 64, 2) FL_Q(1, 64, 3) FL_Q(1, 128, 0) FL_Q(1, 128, 1)
+    FL_Q(1, 128, 2) FL_Q(1, 128, 3)
 #undef FL_Q
     if (v <= 0) v = -1;
     cache[dt][bi][pro][splits][ai] = v;
     return v;
 }
 
-bool plan_splitk(int dt, int pro, int M, int N, int K, int sms, SplitPlan* plan) {
+bool plan_splitk(int dt, int pro, int M, const Outs& outs, int K, int sms, SplitPlan* plan) {
     const int variant = g_opt_variant.load();
     if (variant == 1 || variant == 3) return false;
     const int nk = (K + fl::kBK - 1) / fl::kBK;
@@ -249,23 +299,23 @@ bool plan_splitk(int dt, int pro, int M, int N, int K, int sms, SplitPlan* plan)
     // flight per SM); 64-wide ones give twice the CTAs. Prefer 128 unless it
     // leaves a quarter of the CTAs unused.
     auto ctas_for = [&](int b) {
-        const int tl = mb * ((N + b - 1) / b);
-        int sp = sms / (tl > 0 ? tl : 1);
+        const long long tl = mb * nblocks(outs, b);
+        long long sp = sms / (tl > 0 ? tl : 1);
         if (sp > 8) sp = 8;
         while (sp > 1 && nk / sp < 2) --sp;
         return tl * (sp < 1 ? 1 : sp);
     };
     const int forced_bn = g_opt_tile_n.load();
     const int bn = forced_bn == 128 ? 128 : forced_bn == 256 ? 64 : (ctas_for(128) * 4 >= ctas_for(64) * 3 ? 128 : 64);
-    const int tiles = mb * ((N + bn - 1) / bn);
+    const long long tiles = mb * nblocks(outs, bn);
     if (variant == 0) {
         // the tile kernel fills at least half the SMs: it reuses each staged
         // tile across the whole K loop and needs no reduction
-        if ((long long)mb * ((N + 127) / 128) * 2 > sms || nk < 4) return false;
+        if ((long long)mb * nblocks(outs, 128) * 2 > sms || nk < 4) return false;
     }
     int splits = g_opt_split_k.load();
     if (splits <= 0) {
-        splits = sms / (tiles > 0 ? tiles : 1);
+        splits = (int)(sms / (tiles > 0 ? tiles : 1));
         if (splits > 8) splits = 8;
         if (splits < 1) splits = 1;
         while (splits > 1 && nk / splits < 2) --splits;  // at least two K blocks per split
@@ -294,15 +344,18 @@ bool plan_splitk(int dt, int pro, int M, int N, int K, int sms, SplitPlan* plan)
 
 int pair_max(int dt, int bn, int pro, int ks) {
     // resident clusters (of 2 * ks CTAs) of each pair-kernel instance, cached
-    static std::atomic<int> cache[2][3][3];
+    static std::atomic<int> cache[2][3][4];
     const int ci = ks == 2 ? 2 : (bn == 256 ? 1 : 0);
     int v = cache[dt][ci][pro].load();
     if (v != 0) return v;
 #define FL_Q(DT, BN, PRO, KS) \
     if (dt == DT && bn == BN && pro == PRO && ks == KS) v = fl::pair_max_clusters<DT, BN, PRO, KS>();
-    FL_Q(0, 128, 0, 1) FL_Q(0, 128, 1, 1) FL_Q(0, 128, 2, 1) FL_Q(0, 256, 0, 1) FL_Q(0, 256, 1, 1) FL_Q(0, 256, 2, 1)
-    FL_Q(1, 128, 0, 1) FL_Q(1, 128, 1, 1) FL_Q(1, 128, 2, 1) FL_Q(1, 256, 0, 1) FL_Q(1, 256, 1, 1) FL_Q(1, 256, 2, 1)
-    FL_Q(0, 256, 0, 2) FL_Q(0, 256, 1, 2) FL_Q(0, 256, 2, 2) FL_Q(1, 256, 0, 2) FL_Q(1, 256, 1, 2) FL_Q(1, 256, 2, 2)
+    FL_Q(0, 128, 0, 1) FL_Q(0, 128, 1, 1) FL_Q(0, 128, 2, 1) FL_Q(0, 128, 3, 1)
+    FL_Q(0, 256, 0, 1) FL_Q(0, 256, 1, 1) FL_Q(0, 256, 2, 1) FL_Q(0, 256, 3, 1)
+    FL_Q(1, 128, 0, 1) FL_Q(1, 128, 1, 1) FL_Q(1, 128, 2, 1) FL_Q(1, 128, 3, 1)
+    FL_Q(1, 256, 0, 1) FL_Q(1, 256, 1, 1) FL_Q(1, 256, 2, 1) FL_Q(1, 256, 3, 1)
+    FL_Q(0, 256, 0, 2) FL_Q(0, 256, 1, 2) FL_Q(0, 256, 2, 2) FL_Q(0, 256, 3, 2)
+    FL_Q(1, 256, 0, 2) FL_Q(1, 256, 1, 2) FL_Q(1, 256, 2, 2) FL_Q(1, 256, 3, 2)
 #undef FL_Q
     if (v <= 0) v = -1;
     cache[dt][ci][pro] = v;
@@ -317,12 +370,12 @@ cudaError_t dispatch_pair(int dt, int bn, int pro, int ks, bool dual, const Gemm
     }
 #define FL_CASE(DT, BN, PRO, KS) \
     if (dt == DT && bn == BN && pro == PRO && ks == KS) return fl::launch_pair<DT, BN, PRO, KS, false>(p, grid, s);
-    FL_CASE(0, 128, 0, 1) FL_CASE(0, 128, 1, 1) FL_CASE(0, 128, 2, 1)
-    FL_CASE(0, 256, 0, 1) FL_CASE(0, 256, 1, 1) FL_CASE(0, 256, 2, 1)
-    FL_CASE(1, 128, 0, 1) FL_CASE(1, 128, 1, 1) FL_CASE(1, 128, 2, 1)
-    FL_CASE(1, 256, 0, 1) FL_CASE(1, 256, 1, 1) FL_CASE(1, 256, 2, 1)
-    FL_CASE(0, 256, 0, 2) FL_CASE(0, 256, 1, 2) FL_CASE(0, 256, 2, 2)
-    FL_CASE(1, 256, 0, 2) FL_CASE(1, 256, 1, 2) FL_CASE(1, 256, 2, 2)
+    FL_CASE(0, 128, 0, 1) FL_CASE(0, 128, 1, 1) FL_CASE(0, 128, 2, 1) FL_CASE(0, 128, 3, 1)
+    FL_CASE(0, 256, 0, 1) FL_CASE(0, 256, 1, 1) FL_CASE(0, 256, 2, 1) FL_CASE(0, 256, 3, 1)
+    FL_CASE(1, 128, 0, 1) FL_CASE(1, 128, 1, 1) FL_CASE(1, 128, 2, 1) FL_CASE(1, 128, 3, 1)
+    FL_CASE(1, 256, 0, 1) FL_CASE(1, 256, 1, 1) FL_CASE(1, 256, 2, 1) FL_CASE(1, 256, 3, 1)
+    FL_CASE(0, 256, 0, 2) FL_CASE(0, 256, 1, 2) FL_CASE(0, 256, 2, 2) FL_CASE(0, 256, 3, 2)
+    FL_CASE(1, 256, 0, 2) FL_CASE(1, 256, 1, 2) FL_CASE(1, 256, 2, 2) FL_CASE(1, 256, 3, 2)
 #undef FL_CASE
     return cudaErrorInvalidValue;
 }
@@ -337,14 +390,14 @@ struct PairPlan {
 // many shared-memory bytes per MMA as the single-CTA 128 x 256 tile and
 // measures no faster, so it is used only when forced (FL_OPT_VARIANT = 3 with
 // FL_OPT_TILE_N = 128; FL_OPT_SPLIT_K = 2 forces the K split).
-bool use_pair(int dt, int pro, int M, int N, int K, PairPlan* plan, bool dual) {
+bool use_pair(int dt, int pro, int M, const Outs& outs, int K, PairPlan* plan, bool dual) {
     const int variant = g_opt_variant.load();
     if (variant == 1 || variant == 2) return false;
     if (dual) {
         // SwiGLU gate/up: 128 output columns per 256 x 256 pair tile (Wg and Wu
         // stacked); no K split, no 128-wide variant
         if (pro != fl::PRO_RMS) return false;
-        const long long tiles = (long long)((M + 255) / 256) * ((N + 127) / 128);
+        const long long tiles = (long long)((M + 255) / 256) * nblocks(outs, 128);
         const int maxp = pair_max(dt, 256, pro, 1);
         if (maxp <= 0) return false;
         if (variant != 3 && tiles * 5 < (long long)maxp * 4) return false;
@@ -354,7 +407,7 @@ bool use_pair(int dt, int pro, int M, int N, int K, PairPlan* plan, bool dual) {
     const int forced_bn = g_opt_tile_n.load();
     const int forced_split = g_opt_split_k.load();
     const long long mp = (M + 255) / 256;
-    const long long t256 = mp * ((N + 255) / 256), t128 = mp * ((N + 127) / 128);
+    const long long t256 = mp * nblocks(outs, 256), t128 = mp * nblocks(outs, 128);
     const int nk = (K + fl::kBK - 1) / fl::kBK;
     if (variant == 3 && forced_bn == 128) {
         const int maxp = pair_max(dt, 128, pro, 1);
@@ -378,37 +431,47 @@ bool use_pair(int dt, int pro, int M, int N, int K, PairPlan* plan, bool dual) {
     return true;
 }
 
-fl_status run_pair(int dt, int pro, bool dual, const void* A, const void* W, const void* W2, const void* bias,
-                   const void* residual, const void* gamma, const void* beta, const void* ln_stats, void* out, int M,
-                   int N, int K, int act, float eps, const PairPlan& plan, DeviceInfo* di, cudaStream_t stream) {
-    const int bn = plan.bn;
-    GemmParams p;
-    memset(&p, 0, sizeof(p));
+// Fields every launch shares.
+void fill_common(GemmParams& p, const void* A, const void* residual, const void* gamma, const void* beta,
+                 const void* ln_stats, int M, int K, float eps, DeviceInfo* di) {
     p.ln_stats = ln_stats;
-    fl_status st;
-    if ((st = encode_2d(&p.tmA, dt, A, K, M, fl::kBK, fl::kBM)) != FL_OK) return st;
-    if ((st = encode_2d(&p.tmB, dt, W, K, N, fl::kBK, bn / 2)) != FL_OK) return st;
-    if (dual && (st = encode_2d(&p.tmB2, dt, W2, K, N, fl::kBK, bn / 2)) != FL_OK) return st;
-    if ((st = encode_2d(&p.tmOut, dt, out, N, M, 64, 32)) != FL_OK) return st;
-    if (pro != fl::PRO_NONE && (st = encode_2d(&p.tmGamma, dt, gamma, K, 1, fl::kBK, 1, false)) != FL_OK) return st;
-    if (pro == fl::PRO_LN && beta != nullptr && (st = encode_2d(&p.tmBeta, dt, beta, K, 1, fl::kBK, 1, false)) != FL_OK)
-        return st;
-    p.bias = bias;
     p.residual = residual;
     p.gamma = gamma;
     p.beta = beta;
+    p.a_ptr = A;
     p.status = di->status;
     p.timeout_ns = (unsigned long long)g_opt_timeout_ms.load() * 1000000ull;
     p.M = M;
-    p.N = N;
     p.K = K;
-    p.num_m_blocks = (M + 255) / 256;  // row blocks of a pair tile
-    p.num_n_blocks = (N + (dual ? bn / 2 : bn) - 1) / (dual ? bn / 2 : bn);  // output columns of a tile
     p.num_k_blocks = (K + fl::kBK - 1) / fl::kBK;
-    p.num_tiles = p.num_m_blocks * p.num_n_blocks;
-    p.act = act;
     p.eps = eps;
     p.pdl = g_opt_pdl.load();
+}
+
+fl_status encode_prologue(GemmParams& p, int dt, int pro, const void* gamma, const void* beta, int K) {
+    fl_status st;
+    if (pro != fl::PRO_NONE && (st = encode_2d(&p.tmGamma, dt, gamma, K, 1, fl::kBK, 1, false)) != FL_OK) return st;
+    if (pro == fl::PRO_LN && beta != nullptr && (st = encode_2d(&p.tmBeta, dt, beta, K, 1, fl::kBK, 1, false)) != FL_OK)
+        return st;
+    return FL_OK;
+}
+
+fl_status run_pair(int dt, int pro, bool dual, const void* A, const Outs& outs, const void* W2, const void* residual,
+                   const void* gamma, const void* beta, const void* ln_stats, int M, int K, float eps,
+                   const PairPlan& plan, DeviceInfo* di, cudaStream_t stream) {
+    const int bn = plan.bn;
+    GemmParams p;
+    memset(&p, 0, sizeof(p));
+    fill_common(p, A, residual, gamma, beta, ln_stats, M, K, eps, di);
+    fl_status st;
+    if ((st = encode_2d(&p.tmA, dt, A, K, M, fl::kBK, fl::kBM)) != FL_OK) return st;
+    // output columns of a tile: the pair's 256-row weight tile holds bn
+    // columns of one weight, or (gate/up) bn / 2 columns of Wg over Wu
+    if ((st = fill_outputs(p, dt, outs, M, K, dual ? bn / 2 : bn, bn / 2)) != FL_OK) return st;
+    if (dual && (st = encode_2d(&p.tmB2, dt, W2, K, outs.o[0].N, fl::kBK, bn / 2)) != FL_OK) return st;
+    if ((st = encode_prologue(p, dt, pro, gamma, beta, K)) != FL_OK) return st;
+    p.num_m_blocks = (M + 255) / 256;  // row blocks of a pair tile
+    p.num_tiles = p.num_m_blocks * p.num_n_blocks;
     p.splits = plan.ks;
     p.kps = (p.num_k_blocks + plan.ks - 1) / plan.ks;
 #ifdef FL_TRACE
@@ -422,12 +485,12 @@ fl_status run_pair(int dt, int pro, bool dual, const void* A, const void* W, con
 // CTA tile width. A wider tile halves the activation re-reads and the shared
 // memory traffic per MMA, but fewer tiles may leave SMs idle: take the width
 // whose whole waves of CTAs cost least.
-int choose_bn(int M, int N, bool dual, int sms) {
+int choose_bn(int M, const Outs& outs, bool dual, int sms) {
     if (dual) return 128;
     const int forced = g_opt_tile_n.load();
     if (forced == 128 || forced == 256) return forced;
     const long long mb = (M + fl::kBM - 1) / fl::kBM;
-    const long long t256 = mb * ((N + 255) / 256), t128 = mb * ((N + 127) / 128);
+    const long long t256 = mb * nblocks(outs, 256), t128 = mb * nblocks(outs, 128);
     const long long w256 = (t256 + sms - 1) / sms, w128 = (t128 + sms - 1) / sms;
     // relative cost of one wave: a 128-wide tile does half the MMA work of a
     // 256-wide one but is less efficient per flop
@@ -435,42 +498,24 @@ int choose_bn(int M, int N, bool dual, int sms) {
     return c256 <= c128 ? 256 : 128;
 }
 
-fl_status run_splitk(int dt, int pro, const void* A, const void* W, const void* bias, const void* residual,
-                     const void* gamma, const void* beta, const void* ln_stats, void* out, int M, int N, int K,
-                     int act, float eps, const SplitPlan& plan, DeviceInfo* di, cudaStream_t stream) {
+fl_status run_splitk(int dt, int pro, const void* A, const Outs& outs, const void* residual, const void* gamma,
+                     const void* beta, const void* ln_stats, int M, int K, float eps, const SplitPlan& plan,
+                     DeviceInfo* di, cudaStream_t stream) {
     GemmParams p;
     memset(&p, 0, sizeof(p));
-    p.ln_stats = ln_stats;
+    fill_common(p, A, residual, gamma, beta, ln_stats, M, K, eps, di);
     const int a_rows = plan.a_rows;
     fl_status st;
     if ((st = encode_2d(&p.tmA, dt, A, K, M, fl::kBK, a_rows)) != FL_OK) return st;
-    if ((st = encode_2d(&p.tmB, dt, W, K, N, fl::kBK, plan.bn)) != FL_OK) return st;
-    if (pro != fl::PRO_NONE && (st = encode_2d(&p.tmGamma, dt, gamma, K, 1, fl::kBK, 1, false)) != FL_OK) return st;
-    if (pro == fl::PRO_LN && beta != nullptr && (st = encode_2d(&p.tmBeta, dt, beta, K, 1, fl::kBK, 1, false)) != FL_OK)
-        return st;
-    p.bias = bias;
-    p.residual = residual;
-    p.gamma = gamma;
-    p.beta = beta;
-    p.a_ptr = A;
-    p.out_ptr = out;
-    p.status = di->status;
-    p.timeout_ns = (unsigned long long)g_opt_timeout_ms.load() * 1000000ull;
-    p.M = M;
-    p.N = N;
-    p.K = K;
+    if ((st = fill_outputs(p, dt, outs, M, K, plan.bn, plan.bn)) != FL_OK) return st;
+    if ((st = encode_prologue(p, dt, pro, gamma, beta, K)) != FL_OK) return st;
     p.num_m_blocks = (M + fl::kBM - 1) / fl::kBM;
-    p.num_n_blocks = (N + plan.bn - 1) / plan.bn;
-    p.num_k_blocks = (K + fl::kBK - 1) / fl::kBK;
     p.num_tiles = p.num_m_blocks * p.num_n_blocks;
-    p.act = act;
-    p.eps = eps;
     p.splits = plan.splits;
     p.kps = plan.kps;
     p.a_rows = a_rows;
     p.s_stages = plan.geom.stages;
     p.s_stage_bytes = plan.geom.stage_bytes;
-    p.pdl = g_opt_pdl.load();
     p.w_preload = g_opt_preload.load();
     p.s_one_per_sm = plan.geom.smem_bytes * 2 + 2048 > 228 * 1024;  // one CTA per SM
     {
@@ -493,45 +538,26 @@ fl_status run_splitk(int dt, int pro, const void* A, const void* W, const void* 
     return ok();
 }
 
-fl_status run_kernels(int dt, int pro, bool dual, const void* A, const void* W, const void* W2, const void* bias,
-                      const void* residual, const void* gamma, const void* beta, const void* ln_stats, void* out, int M,
-                      int N, int K, int act, float eps, DeviceInfo* di, cudaStream_t stream) {
+fl_status run_kernels(int dt, int pro, bool dual, const void* A, const Outs& outs, const void* W2,
+                      const void* residual, const void* gamma, const void* beta, const void* ln_stats, int M, int K,
+                      float eps, DeviceInfo* di, cudaStream_t stream) {
     fl_status st;
     PairPlan pplan;
-    if (use_pair(dt, pro, M, N, K, &pplan, dual))
-        return run_pair(dt, pro, dual, A, W, W2, bias, residual, gamma, beta, ln_stats, out, M, N, K, act, eps, pplan,
-                        di, stream);
+    if (use_pair(dt, pro, M, outs, K, &pplan, dual))
+        return run_pair(dt, pro, dual, A, outs, W2, residual, gamma, beta, ln_stats, M, K, eps, pplan, di, stream);
     SplitPlan plan;
-    if (!dual && plan_splitk(dt, pro, M, N, K, di->sms, &plan))
-        return run_splitk(dt, pro, A, W, bias, residual, gamma, beta, ln_stats, out, M, N, K, act, eps, plan, di,
-                          stream);
-    const int bn = choose_bn(M, N, dual, di->sms);
+    if (!dual && plan_splitk(dt, pro, M, outs, K, di->sms, &plan))
+        return run_splitk(dt, pro, A, outs, residual, gamma, beta, ln_stats, M, K, eps, plan, di, stream);
+    const int bn = choose_bn(M, outs, dual, di->sms);
     GemmParams p;
     memset(&p, 0, sizeof(p));
-    p.ln_stats = ln_stats;
+    fill_common(p, A, residual, gamma, beta, ln_stats, M, K, eps, di);
     if ((st = encode_2d(&p.tmA, dt, A, K, M, fl::kBK, fl::kBM)) != FL_OK) return st;
-    if ((st = encode_2d(&p.tmB, dt, W, K, N, fl::kBK, bn)) != FL_OK) return st;
-    if (dual && (st = encode_2d(&p.tmB2, dt, W2, K, N, fl::kBK, bn)) != FL_OK) return st;
-    if ((st = encode_2d(&p.tmOut, dt, out, N, M, 64, 32)) != FL_OK) return st;
-    if (pro != fl::PRO_NONE && (st = encode_2d(&p.tmGamma, dt, gamma, K, 1, fl::kBK, 1, false)) != FL_OK) return st;
-    if (pro == fl::PRO_LN && beta != nullptr && (st = encode_2d(&p.tmBeta, dt, beta, K, 1, fl::kBK, 1, false)) != FL_OK)
-        return st;
-    p.bias = bias;
-    p.residual = residual;
-    p.gamma = gamma;
-    p.beta = beta;
-    p.status = di->status;
-    p.timeout_ns = (unsigned long long)g_opt_timeout_ms.load() * 1000000ull;
-    p.M = M;
-    p.N = N;
-    p.K = K;
+    if ((st = fill_outputs(p, dt, outs, M, K, bn, bn)) != FL_OK) return st;
+    if (dual && (st = encode_2d(&p.tmB2, dt, W2, K, outs.o[0].N, fl::kBK, bn)) != FL_OK) return st;
+    if ((st = encode_prologue(p, dt, pro, gamma, beta, K)) != FL_OK) return st;
     p.num_m_blocks = (M + fl::kBM - 1) / fl::kBM;
-    p.num_n_blocks = (N + bn - 1) / bn;
-    p.num_k_blocks = (K + fl::kBK - 1) / fl::kBK;
     p.num_tiles = p.num_m_blocks * p.num_n_blocks;
-    p.act = act;
-    p.eps = eps;
-    p.pdl = g_opt_pdl.load();
     const int grid = p.num_tiles < di->sms ? p.num_tiles : di->sms;
     cudaError_t e = dispatch_tile(dt, bn, pro, dual, p, grid, stream);
     if (e != cudaSuccess) return fail(FL_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
@@ -540,10 +566,10 @@ fl_status run_kernels(int dt, int pro, bool dual, const void* A, const void* W, 
 
 // One fused call. LayerNorm first computes the row statistics (8 bytes per
 // row of stream-ordered scratch from the library pool, freed on the stream
-// right after the GEMM kernel that reads them).
-fl_status run_tile(int dt, int pro, bool dual, const void* A, const void* W, const void* W2, const void* bias,
-                   const void* residual, const void* gamma, const void* beta, void* out, int M, int N, int K, int act,
-                   float eps, cudaStream_t stream) {
+// right after the GEMM kernel that reads them), once for all outputs.
+fl_status run_tile(int dt, int pro, bool dual, const void* A, const Outs& outs, const void* W2,
+                   const void* residual, const void* gamma, const void* beta, int M, int K, float eps,
+                   cudaStream_t stream) {
     DeviceInfo* di = nullptr;
     fl_status st = device_info(&di);
     if (st != FL_OK) return st;
@@ -557,7 +583,7 @@ fl_status run_tile(int dt, int pro, bool dual, const void* A, const void* W, con
             return fail(FL_ERR_CUDA, "LayerNorm statistics kernel launch failed: %s", cudaGetErrorString(e));
         }
     }
-    st = run_kernels(dt, pro, dual, A, W, W2, bias, residual, gamma, beta, stats, out, M, N, K, act, eps, di, stream);
+    st = run_kernels(dt, pro, dual, A, outs, W2, residual, gamma, beta, stats, M, K, eps, di, stream);
     if (stats != nullptr) cudaFreeAsync(stats, stream);
     return st;
 }
@@ -652,9 +678,8 @@ fl_status fl_gemm_epilogue(const void* A, const void* W, const void* bias, const
         return fail(FL_ERR_INVALID_ARG, "out overlaps an input");
     if (uses_res && residual != out && overlap(out, ob, residual, ob))
         return fail(FL_ERR_INVALID_ARG, "out may alias residual only exactly");
-    return run_tile(dtype, fl::PRO_NONE, false, A, W, nullptr, uses_bias ? bias : nullptr,
-                    uses_res ? residual : nullptr, nullptr, nullptr, out, M, N, K, act, 0.f,
-                    static_cast<cudaStream_t>(stream));
+    return run_tile(dtype, fl::PRO_NONE, false, A, single_out(W, uses_bias ? bias : nullptr, out, N, act), nullptr,
+                    uses_res ? residual : nullptr, nullptr, nullptr, M, K, 0.f, static_cast<cudaStream_t>(stream));
 }
 
 fl_status fl_norm_gemm(const void* x, const void* gamma, const void* beta, const void* W, const void* bias, void* out,
@@ -680,8 +705,97 @@ fl_status fl_norm_gemm(const void* x, const void* gamma, const void* beta, const
         overlap(out, ob, bias, (size_t)N * 2))
         return fail(FL_ERR_INVALID_ARG, "out overlaps an input");
     const int pro = norm_kind == FL_NORM_RMS ? fl::PRO_RMS : fl::PRO_LN;
-    return run_tile(dtype, pro, false, x, W, nullptr, bias, nullptr, gamma, b, out, M, N, K, (int)act, eps,
+    return run_tile(dtype, pro, false, x, single_out(W, bias, out, N, (int)act), nullptr, nullptr, gamma, b, M, K, eps,
                     static_cast<cudaStream_t>(stream));
+}
+
+fl_status fl_norm_gemm_multi(const void* x, const void* gamma, const void* beta, int n_out, const void* const* W,
+                             const void* const* bias, void* const* out, const int* N, const int* act, int M, int K,
+                             float eps, fl_norm_kind norm_kind, fl_dtype dtype, void* stream) {
+    if (!valid_dtype(dtype)) return fail(FL_ERR_INVALID_ARG, "bad dtype %d", (int)dtype);
+    if (norm_kind != FL_NORM_RMS && norm_kind != FL_NORM_LAYER)
+        return fail(FL_ERR_INVALID_ARG, "bad norm kind %d", (int)norm_kind);
+    if (n_out < 1 || n_out > FL_MAX_OUTPUTS)
+        return fail(FL_ERR_INVALID_ARG, "n_out must be 1..%d, got %d", FL_MAX_OUTPUTS, n_out);
+    if (W == nullptr || out == nullptr || N == nullptr)
+        return fail(FL_ERR_INVALID_ARG, "W, out and N arrays must not be null");
+    if (!(eps >= 0.0f) || eps > 1e30f) return fail(FL_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    fl_status st;
+    if ((st = check_ptr("x", x, true)) != FL_OK) return st;
+    if ((st = check_ptr("gamma", gamma, true)) != FL_OK) return st;
+    const void* b = norm_kind == FL_NORM_LAYER ? beta : nullptr;
+    if ((st = check_ptr("beta", b, false)) != FL_OK) return st;
+    Outs outs;
+    outs.n = n_out;
+    for (int i = 0; i < n_out; ++i) {
+        const int a = act != nullptr ? act[i] : FL_ACT_NONE;
+        if (a < 0 || a > FL_ACT_RELU) return fail(FL_ERR_INVALID_ARG, "bad activation %d for output %d", a, i);
+        if ((st = check_shape("fl_norm_gemm_multi", M, N[i], K)) != FL_OK) return st;
+        if ((st = check_ptr("W[i]", W[i], true)) != FL_OK) return st;
+        if ((st = check_ptr("out[i]", out[i], true)) != FL_OK) return st;
+        const void* bi = bias != nullptr ? bias[i] : nullptr;
+        if ((st = check_ptr("bias[i]", bi, false)) != FL_OK) return st;
+        outs.o[i] = OutDesc{W[i], bi, out[i], N[i], a};
+    }
+    // every output overlaps no input and no other output
+    for (int i = 0; i < n_out; ++i) {
+        const size_t ob = (size_t)M * N[i] * 2;
+        if (overlap(out[i], ob, x, (size_t)M * K * 2) || overlap(out[i], ob, gamma, (size_t)K * 2) ||
+            overlap(out[i], ob, b, (size_t)K * 2))
+            return fail(FL_ERR_INVALID_ARG, "out[%d] overlaps an input", i);
+        for (int j = 0; j < n_out; ++j) {
+            if (overlap(out[i], ob, outs.o[j].W, (size_t)N[j] * K * 2) ||
+                overlap(out[i], ob, outs.o[j].bias, (size_t)N[j] * 2))
+                return fail(FL_ERR_INVALID_ARG, "out[%d] overlaps an input", i);
+            if (j != i && overlap(out[i], ob, out[j], (size_t)M * N[j] * 2))
+                return fail(FL_ERR_INVALID_ARG, "out[%d] overlaps out[%d]", i, j);
+        }
+    }
+    const int pro = norm_kind == FL_NORM_RMS ? fl::PRO_RMS : fl::PRO_LN;
+    return run_tile(dtype, pro, false, x, outs, nullptr, nullptr, gamma, b, M, K, eps,
+                    static_cast<cudaStream_t>(stream));
+}
+
+fl_status fl_input_bias_gemm(const void* A, const void* bias_in, const void* W, const void* bias, const void* residual,
+                             void* out, int M, int N, int K, fl_act act, fl_dtype dtype, void* stream) {
+    if (!valid_dtype(dtype)) return fail(FL_ERR_INVALID_ARG, "bad dtype %d", (int)dtype);
+    if ((int)act < 0 || (int)act > FL_ACT_RELU) return fail(FL_ERR_INVALID_ARG, "bad activation %d", (int)act);
+    fl_status st;
+    if ((st = check_shape("fl_input_bias_gemm", M, N, K)) != FL_OK) return st;
+    if ((st = check_ptr("A", A, true)) != FL_OK) return st;
+    if ((st = check_ptr("bias_in", bias_in, true)) != FL_OK) return st;
+    if ((st = check_ptr("W", W, true)) != FL_OK) return st;
+    if ((st = check_ptr("out", out, true)) != FL_OK) return st;
+    if ((st = check_ptr("bias", bias, false)) != FL_OK) return st;
+    if ((st = check_ptr("residual", residual, false)) != FL_OK) return st;
+    const size_t ob = (size_t)M * N * 2;
+    if (overlap(out, ob, A, (size_t)M * K * 2) || overlap(out, ob, W, (size_t)N * K * 2) ||
+        overlap(out, ob, bias_in, (size_t)K * 2) || overlap(out, ob, bias, (size_t)N * 2))
+        return fail(FL_ERR_INVALID_ARG, "out overlaps an input");
+    if (residual != nullptr && residual != out && overlap(out, ob, residual, ob))
+        return fail(FL_ERR_INVALID_ARG, "out may alias residual only exactly");
+    return run_tile(dtype, fl::PRO_ADD, false, A, single_out(W, bias, out, N, (int)act), nullptr, residual, bias_in,
+                    nullptr, M, K, 0.f, static_cast<cudaStream_t>(stream));
+}
+
+fl_status fl_rms_norm(const void* x, const void* gamma, void* out, int M, int K, float eps, fl_dtype dtype,
+                      void* stream) {
+    if (!valid_dtype(dtype)) return fail(FL_ERR_INVALID_ARG, "bad dtype %d", (int)dtype);
+    if (!(eps >= 0.0f) || eps > 1e30f) return fail(FL_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    if (M < 1 || K < 1) return fail(FL_ERR_INVALID_ARG, "fl_rms_norm: sizes must be positive (M=%d K=%d)", M, K);
+    if (K % 8 != 0) return fail(FL_ERR_ALIGNMENT, "fl_rms_norm: K must be a multiple of 8 (K=%d)", K);
+    fl_status st;
+    if ((st = check_ptr("x", x, true)) != FL_OK) return st;
+    if ((st = check_ptr("gamma", gamma, true)) != FL_OK) return st;
+    if ((st = check_ptr("out", out, true)) != FL_OK) return st;
+    const size_t xb = (size_t)M * K * 2;
+    if (out != x && overlap(out, xb, x, xb)) return fail(FL_ERR_INVALID_ARG, "out may alias x only exactly");
+    if (overlap(out, xb, gamma, (size_t)K * 2)) return fail(FL_ERR_INVALID_ARG, "out overlaps gamma");
+    DeviceInfo* di = nullptr;
+    if ((st = device_info(&di)) != FL_OK) return st;
+    cudaError_t e = fl::launch_rms_norm(dtype, x, gamma, out, M, K, eps, g_opt_pdl.load(), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(FL_ERR_CUDA, "RMSNorm kernel launch failed: %s", cudaGetErrorString(e));
+    return ok();
 }
 
 size_t fl_swiglu_ffn_workspace_size(int M, int F, fl_dtype dtype) {
@@ -720,12 +834,12 @@ fl_status fl_swiglu_ffn(const void* x, const void* gamma, const void* Wg, const 
     if (overlap(workspace, need, out, ob)) return fail(FL_ERR_INVALID_ARG, "workspace overlaps out");
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     // gate/up: h = silu(RMSNorm(x) Wg^T) * (RMSNorm(x) Wu^T)
-    st = run_tile(dtype, fl::PRO_RMS, true, x, Wg, Wu, nullptr, nullptr, gamma, nullptr, workspace, M, F, D,
-                  fl::ACT_NONE, eps, s);
+    st = run_tile(dtype, fl::PRO_RMS, true, x, single_out(Wg, nullptr, workspace, F, fl::ACT_NONE), Wu, nullptr, gamma,
+                  nullptr, M, D, eps, s);
     if (st != FL_OK) return st;
     // down: out = h Wd^T (+ bias_down) + x
-    return run_tile(dtype, fl::PRO_NONE, false, workspace, Wd, nullptr, bias_down, x, nullptr, nullptr, out, M, D, F,
-                    fl::ACT_NONE, 0.f, s);
+    return run_tile(dtype, fl::PRO_NONE, false, workspace, single_out(Wd, bias_down, out, D, fl::ACT_NONE), nullptr, x,
+                    nullptr, nullptr, M, F, 0.f, s);
 }
 
 fl_status fl_device_status(void* stream) {

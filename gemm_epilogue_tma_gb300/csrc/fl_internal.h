@@ -8,7 +8,9 @@
 
 namespace fl {
 
-enum Prologue : int { PRO_NONE = 0, PRO_RMS = 1, PRO_LN = 2 };
+// Prologues applied to the staged activation: none, RMSNorm, LayerNorm, or
+// the elementwise input bias (x + b, b along K).
+enum Prologue : int { PRO_NONE = 0, PRO_RMS = 1, PRO_LN = 2, PRO_ADD = 3 };
 enum ActKind : int { ACT_NONE = 0, ACT_GELU = 1, ACT_SILU = 2, ACT_RELU = 3 };
 enum DTypeTag : int { DT_F16 = 0, DT_BF16 = 1 };
 
@@ -20,27 +22,36 @@ constexpr int kStatusTimeout = 6;
 constexpr int kBM = 128;
 constexpr int kBK = 64;
 
+// Outputs one launch may write: several weights applied to the same
+// (normalised) activation, side by side along N (horizontal fusion).
+constexpr int kMaxOut = 4;
+
 // Parameters of the tile kernel. Passed by value as a __grid_constant__ so the
 // tensor maps sit in parameter space, where TMA may read them.
 struct GemmParams {
-    CUtensorMap tmA;    // activation [M, K], box {64, 128}, 128B swizzle
-    CUtensorMap tmB;    // weight [N, K], box {64, BN}, 128B swizzle
-    CUtensorMap tmB2;   // second weight [N, K] of the gate/up kernel (else unused)
-    CUtensorMap tmOut;  // output [M, N], box {64, 32}, 128B swizzle
-    CUtensorMap tmGamma;  // gamma as a [1, K] matrix, box {64, 1} (norm prologues)
+    CUtensorMap tmA;             // activation [M, K], box {64, 128}, 128B swizzle
+    CUtensorMap tmB[kMaxOut];    // weight of output i [N_i, K], box {64, BN}, 128B swizzle
+    CUtensorMap tmB2;            // second weight [N, K] of the gate/up kernel (else unused)
+    CUtensorMap tmOut[kMaxOut];  // output i [M, N_i], box {64, 32}, 128B swizzle
+    CUtensorMap tmGamma;  // gamma (RMS, LayerNorm) or the input bias, as a [1, K] matrix, box {64, 1}
     CUtensorMap tmBeta;   // beta as a [1, K] matrix, box {64, 1} (LayerNorm with beta)
-    const void* bias;      // [N] or null
-    const void* residual;  // [M, N] or null
-    const void* gamma;     // [K] (norm prologues)
+    const void* bias[kMaxOut];  // output bias [N_i] or null
+    const void* residual;  // [M, N] or null (single-output launches only)
+    const void* gamma;     // [K] (prologues)
     const void* beta;      // [K] or null (LayerNorm)
     const void* a_ptr;     // activation [M, K]
     const void* ln_stats;  // LayerNorm: float2 (mean, 1/sqrt(var + eps)) per activation row
-    void* out_ptr;         // output [M, N] (split-K kernel stores directly)
+    void* out_ptr[kMaxOut];  // output i [M, N_i] (split-K kernel stores directly)
     int* status;           // device status word
     unsigned long long timeout_ns;
-    int M, N, K;
+    int M, K;
+    int N[kMaxOut];        // columns of output i
+    int act[kMaxOut];      // activation of output i
+    int n_out;             // outputs of this launch (1 .. kMaxOut)
+    // first column block (in tiles of this launch's width) of each output;
+    // nb0[n_out] is the total, num_n_blocks
+    int nb0[kMaxOut + 1];
     int num_m_blocks, num_n_blocks, num_k_blocks, num_tiles;
-    int act;
     float eps;
     int splits;    // split-K kernel: CTAs per cluster, one K range each
     int kps;       // split-K kernel: 64-wide K blocks per split
@@ -65,6 +76,10 @@ int set_last_error(int status, const char* message);
 
 // LayerNorm row statistics of x [M, K] into stats (M float2: mean, rstd).
 cudaError_t launch_ln_stats(int dt, const void* x, int M, int K, float eps, void* stats, int pdl,
+                            cudaStream_t stream);
+
+// Standalone RMSNorm y = x * gamma / sqrt(mean(x^2) + eps) of x [M, K].
+cudaError_t launch_rms_norm(int dt, const void* x, const void* gamma, void* y, int M, int K, float eps, int pdl,
                             cudaStream_t stream);
 
 // Kernel launchers, explicitly instantiated in the kernel translation units.

@@ -178,8 +178,11 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&p.tmA);
-        tma_prefetch_desc(&p.tmB);
-        tma_prefetch_desc(&p.tmOut);
+        for (int i = 0; i < p.n_out; ++i) {
+            tma_prefetch_desc(&p.tmB[i]);
+            tma_prefetch_desc(&p.tmOut[i]);
+        }
+        if (DUAL) tma_prefetch_desc(&p.tmB2);
         if (PRO != PRO_NONE) tma_prefetch_desc(&p.tmGamma);
         if (PRO == PRO_LN && p.beta != nullptr) tma_prefetch_desc(&p.tmBeta);
     }
@@ -195,8 +198,9 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     // L2 prefetch of this CTA's first weight tiles overlaps the previous kernel
     // (L2 is the point of coherence); every other global access waits for it.
     if (warp == 0 && lane == 0 && t_begin < t_end) {
-        const int nh = DUAL ? tile_nb(t_begin) * OUT_COLS : tile_nb(t_begin) * C::BN + (int)rank * C::HALF;
-        const CUtensorMap* tb = DUAL && rank ? &p.tmB2 : &p.tmB;
+        const OutSel o = out_sel(p, tile_nb(t_begin));
+        const int nh = DUAL ? o.nb * OUT_COLS : o.nb * C::BN + (int)rank * C::HALF;
+        const CUtensorMap* tb = DUAL && rank ? &p.tmB2 : &p.tmB[o.oi];
         for (int kb = kb_begin; kb < kb_begin + S && kb < kb_end; ++kb) tma_prefetch_2d(tb, kb * kBK, nh);
     }
     // LayerNorm: this grid directly follows the row-statistics kernel, which
@@ -214,12 +218,12 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     // shared buffer (one 16-byte load per lane and 256 columns; zeros past N),
     // before the accumulator is waited for: the epilogue then reads it with
     // broadcast shared loads instead of global loads on its critical path.
-    auto stage_bias = [&](int n0, int q) -> uint32_t {
+    auto stage_bias = [&](int n0, int q, int oi) -> uint32_t {
         const uint32_t buf = sbase + C::OFF_BIAS + (uint32_t)(q * C::BN * 2);
-        if (p.bias != nullptr) {
-            const uint16_t* b = reinterpret_cast<const uint16_t*>(p.bias);
+        if (p.bias[oi] != nullptr) {
+            const uint16_t* b = reinterpret_cast<const uint16_t*>(p.bias[oi]);
             for (int c = (int)(threadIdx.x & 31) * 8; c < C::BN; c += 256) {
-                const uint4 v = n0 + c < p.N ? ldg_v4(b + n0 + c) : make_uint4(0u, 0u, 0u, 0u);
+                const uint4 v = n0 + c < p.N[oi] ? ldg_v4(b + n0 + c) : make_uint4(0u, 0u, 0u, 0u);
                 st_shared_v4(buf + (uint32_t)c * 2u, v.x, v.y, v.z, v.w);
             }
         }
@@ -258,6 +262,8 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
             uint32_t o[16];
             if constexpr (PRO == PRO_LN)
                 fold_ln_compute<DT>(cur, rstd, nmr, o);
+            else if constexpr (PRO == PRO_ADD)
+                fold_add_compute<DT>(cur, o);
             else
                 fold_rms_compute<DT>(cur, ss, o);
             tmem_st_32x32b_x16(a_cols + 32u * (uint32_t)fs, o);
@@ -296,8 +302,9 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                 const int m0 = tile_mb(tile) * 2 * kBM + (int)rank * kBM;
                 // this CTA's weight rows: its half of the tile, or (DUAL) the
                 // tile's rows of Wg / Wu
-                const int nh = DUAL ? tile_nb(tile) * OUT_COLS : tile_nb(tile) * C::BN + (int)rank * C::HALF;
-                const CUtensorMap* tb = DUAL && rank ? &p.tmB2 : &p.tmB;
+                const OutSel o = out_sel(p, tile_nb(tile));
+                const int nh = DUAL ? o.nb * OUT_COLS : o.nb * C::BN + (int)rank * C::HALF;
+                const CUtensorMap* tb = DUAL && rank ? &p.tmB2 : &p.tmB[o.oi];
                 for (int kb = kb_begin; kb < kb_end; ++kb) {
                     if (!wait_bar(empty_bar(s), ph ^ 1u, p.status, p.timeout_ns, 31)) {
                         ok = false;
@@ -416,6 +423,8 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                     uint32_t o[32];
                     if (PRO == PRO_RMS) {
                         fold_rms_row<DT>(stage_a(s), gb_slot(s), t, ss, o);
+                    } else if (PRO == PRO_ADD) {
+                        fold_add_row<DT>(stage_a(s), gb_slot(s), t, o);
                     } else {
                         uint32_t (&lo)[16] = *reinterpret_cast<uint32_t(*)[16]>(&o[0]);
                         uint32_t (&hi)[16] = *reinterpret_cast<uint32_t(*)[16]>(&o[16]);
@@ -462,13 +471,16 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         constexpr int HALF_N = C::BN / 2;
         const int tile = pair;
         const int m0 = tile_mb(tile) * 2 * kBM + (int)rank * kBM;
-        const int n0 = tile_nb(tile) * C::BN;
+        const OutSel osel = out_sel(p, tile_nb(tile));
+        const int n0 = osel.nb * C::BN;
+        const int N = p.N[osel.oi];
+        const int act = p.act[osel.oi];
         const int own_c0 = khalf * HALF_N, oth_c0 = (1 - khalf) * HALF_N;
-        const uint32_t bias_s = stage_bias(n0, q);
+        const uint32_t bias_s = stage_bias(n0, q, osel.oi);
         const uint32_t tl = tmem_base + ((uint32_t)(q * 32) << 16);
         const uint32_t row_off = (uint32_t)(rl * C::XROW) * 4u;  // within a chunk
         using T = uint16_t;
-        const T* bias = reinterpret_cast<const T*>(p.bias);
+        const T* bias = reinterpret_cast<const T*>(p.bias[osel.oi]);
         const T* res = reinterpret_cast<const T*>(p.residual);
         bool ok = true;
         float ss_upper = 0.f;  // RMS, split fold: the row's sum of squares over chunks 4-7
@@ -524,7 +536,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
             if (m0 + q * 32 < p.M) {
                 for (int c = 0; c < HALF_N / 64; ++c) {
                     const int col0 = n0 + own_c0 + c * 64;
-                    if (col0 >= p.N) break;
+                    if (col0 >= N) break;
                     // the two 64-column chunks use two staging buffers
                     const uint32_t sbuf = c == 0 ? ebuf : sbase + C::OFF_EPI2 + q * C::EPI_BUF_BYTES;
                     const uint32_t srow = sbuf + lane * 128;
@@ -538,11 +550,11 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                         // and TMEM loads below so its latency overlaps them
                         uint4 rres[4];
                         if (res != nullptr && row_ok) {
-                            const T* rrow = res + (size_t)row * p.N;
+                            const T* rrow = res + (size_t)row * N;
 #pragma unroll
                             for (int j = 0; j < 4; ++j)
-                                rres[j] = cbase + j * 8 < p.N ? *reinterpret_cast<const uint4*>(rrow + cbase + j * 8)
-                                                              : make_uint4(0u, 0u, 0u, 0u);
+                                rres[j] = cbase + j * 8 < N ? *reinterpret_cast<const uint4*>(rrow + cbase + j * 8)
+                                                            : make_uint4(0u, 0u, 0u, 0u);
                         }
                         if (!wait_bar_cluster(recvd_bar(q, xc), 0, p.status, p.timeout_ns, 45)) ok = false;
                         if (PRO == PRO_RMS && xc == 0) {
@@ -564,7 +576,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                         if (bias != nullptr) {
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
-                                if (cbase + j * 8 < p.N) {
+                                if (cbase + j * 8 < N) {
                                     const uint4 bv = ld_shared_v4(bias_s + (uint32_t)(cbase + j * 8 - n0) * 2u);
                                     const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
@@ -576,14 +588,14 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                                 }
                             }
                         }
-                        if (p.act != ACT_NONE) {
+                        if (act != ACT_NONE) {
 #pragma unroll
-                            for (int e = 0; e < 32; ++e) v[e] = act_apply(p.act, v[e]);
+                            for (int e = 0; e < 32; ++e) v[e] = act_apply(act, v[e]);
                         }
                         if (res != nullptr && row_ok) {
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
-                                if (cbase + j * 8 < p.N) {
+                                if (cbase + j * 8 < N) {
                                     const uint32_t rw[4] = {rres[j].x, rres[j].y, rres[j].z, rres[j].w};
 #pragma unroll
                                     for (int e = 0; e < 4; ++e) {
@@ -605,7 +617,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&p.tmOut, sbuf, col0, m0 + q * 32);
+                        tma_store_2d(&p.tmOut[osel.oi], sbuf, col0, m0 + q * 32);
                         bulk_commit_group();
                     }
                 }
@@ -627,14 +639,17 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         int fs = 0;  // ring position of the fold half (FOLD2)
         uint32_t fph = 0;
         using T = uint16_t;
-        const T* bias = reinterpret_cast<const T*>(p.bias);
         const T* res = reinterpret_cast<const T*>(p.residual);
         for (int tile = t_begin; tile < t_end; tile += t_step, ++it) {
             const int m0 = tile_mb(tile) * 2 * kBM + (int)rank * kBM;
-            const int n0 = tile_nb(tile) * OUT_COLS;
+            const OutSel osel = out_sel(p, tile_nb(tile));
+            const int n0 = osel.nb * OUT_COLS;
+            const int N = p.N[osel.oi];
+            const int act = p.act[osel.oi];
+            const T* bias = reinterpret_cast<const T*>(p.bias[osel.oi]);
             const int buf = C::NBUF == 2 ? (it & 1) : 0;
             const uint32_t tph = C::NBUF == 2 ? (uint32_t)((it >> 1) & 1) : (uint32_t)(it & 1);
-            const uint32_t bias_s = stage_bias(n0, q);
+            const uint32_t bias_s = stage_bias(n0, q, osel.oi);
             float ss_upper = 0.f;  // RMS, split fold: the row's sum of squares over chunks 4-7
             if (FOLD2 && !fold_tile(tile, q * 32 + lane, 4, fs, fph, ss_upper, 47)) break;
             if (!wait_bar(tfull_bar(buf), tph, p.status, p.timeout_ns, 40)) break;
@@ -653,7 +668,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
             // after the last chunk's TMEM load
             int nchunks = 0;
             if (m0 + q * 32 < p.M)
-                while (nchunks < OUT_COLS / 64 && n0 + nchunks * 64 < p.N) ++nchunks;
+                while (nchunks < OUT_COLS / 64 && n0 + nchunks * 64 < N) ++nchunks;
             bool released = false;
             auto release_acc = [&]() {
                 tc_fence_before();
@@ -674,11 +689,11 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                         // and TMEM loads below so its latency overlaps them
                         uint4 rres[4];
                         if (res != nullptr && row_ok) {
-                            const T* rrow = res + (size_t)row * p.N;
+                            const T* rrow = res + (size_t)row * N;
 #pragma unroll
                             for (int j = 0; j < 4; ++j)
-                                rres[j] = cbase + j * 8 < p.N ? *reinterpret_cast<const uint4*>(rrow + cbase + j * 8)
-                                                              : make_uint4(0u, 0u, 0u, 0u);
+                                rres[j] = cbase + j * 8 < N ? *reinterpret_cast<const uint4*>(rrow + cbase + j * 8)
+                                                            : make_uint4(0u, 0u, 0u, 0u);
                         }
                         uint32_t acc[32];
                         tmem_ld_32x32b_x32(tbase + c * 64 + h * 32, acc);
@@ -701,7 +716,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                         if (!DUAL && bias != nullptr) {
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
-                                if (cbase + j * 8 < p.N) {
+                                if (cbase + j * 8 < N) {
                                     const uint4 bv = ld_shared_v4(bias_s + (uint32_t)(cbase + j * 8 - n0) * 2u);
                                     const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
@@ -713,14 +728,14 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                                 }
                             }
                         }
-                        if (!DUAL && p.act != ACT_NONE) {
+                        if (!DUAL && act != ACT_NONE) {
 #pragma unroll
-                            for (int e = 0; e < 32; ++e) v[e] = act_apply(p.act, v[e]);
+                            for (int e = 0; e < 32; ++e) v[e] = act_apply(act, v[e]);
                         }
                         if (!DUAL && res != nullptr && row_ok) {
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
-                                if (cbase + j * 8 < p.N) {
+                                if (cbase + j * 8 < N) {
                                     const uint32_t rw[4] = {rres[j].x, rres[j].y, rres[j].z, rres[j].w};
 #pragma unroll
                                     for (int e = 0; e < 4; ++e) {
@@ -747,7 +762,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&p.tmOut, ebuf, col0, m0 + q * 32);
+                        tma_store_2d(&p.tmOut[osel.oi], ebuf, col0, m0 + q * 32);
                         bulk_commit_group();
                     }
                 }

@@ -79,7 +79,9 @@ __global__ void __launch_bounds__(splitk_threads<PRO>(), 1)
     const int rank = (int)cluster_rank();
     const int tile = blockIdx.x / splits;
     const int m0 = (tile % p.num_m_blocks) * kBM;
-    const int n0 = (tile / p.num_m_blocks) * BN;
+    const OutSel osel = out_sel(p, tile / p.num_m_blocks);
+    const int n0 = osel.nb * BN;
+    const CUtensorMap* tmB = &p.tmB[osel.oi];
     const int nk = p.num_k_blocks;
     const int kb0 = rank * p.kps;
     const int kb1 = min(nk, kb0 + p.kps);
@@ -99,7 +101,7 @@ __global__ void __launch_bounds__(splitk_threads<PRO>(), 1)
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&p.tmA);
-        tma_prefetch_desc(&p.tmB);
+        tma_prefetch_desc(tmB);
         if (PRO != PRO_NONE) tma_prefetch_desc(&p.tmGamma);
         if (PRO == PRO_LN && p.beta != nullptr) tma_prefetch_desc(&p.tmBeta);
     }
@@ -130,10 +132,10 @@ __global__ void __launch_bounds__(splitk_threads<PRO>(), 1)
     if (warp == 0 && lane == 0) {
         for (int i = 0; i < npre; ++i) {
             mbar_arrive_expect_tx(full_bar(i), stage_tx);
-            tma_load_2d(stage_b(i), &p.tmB, full_bar(i), (kb0 + i) * kBK, n0);
+            tma_load_2d(stage_b(i), tmB, full_bar(i), (kb0 + i) * kBK, n0);
         }
         if (p.s_one_per_sm)
-            for (int kb = kb0 + npre; kb < kb0 + NS && kb < kb1; ++kb) tma_prefetch_2d(&p.tmB, kb * kBK, n0);
+            for (int kb = kb0 + npre; kb < kb0 + NS && kb < kb1; ++kb) tma_prefetch_2d(tmB, kb * kBK, n0);
     }
     griddep_wait();
     // The next kernel may launch now when its CTAs can only use idle SMs; with
@@ -155,7 +157,7 @@ __global__ void __launch_bounds__(splitk_threads<PRO>(), 1)
                 if (kb - kb0 >= npre) {  // a preloaded stage is fresh and already expects its bytes
                     if (!wait_bar(empty_bar(s), ph ^ 1u, p.status, p.timeout_ns, 21)) break;
                     mbar_arrive_expect_tx(full_bar(s), stage_tx);
-                    tma_load_2d(stage_b(s), &p.tmB, full_bar(s), kb * kBK, n0);
+                    tma_load_2d(stage_b(s), tmB, full_bar(s), kb * kBK, n0);
                 }
                 tma_load_2d(stage_a(s), &p.tmA, full_bar(s), kb * kBK, m0);
                 if (PRO != PRO_NONE) {
@@ -236,6 +238,8 @@ __global__ void __launch_bounds__(splitk_threads<PRO>(), 1)
             if (!wait_bar(full_bar(s), ph, p.status, p.timeout_ns, 23)) break;
             if (PRO == PRO_RMS)
                 fold_rms_stage<DT>(stage_a(s), gb_slot(s), t, ni, ss);
+            else if (PRO == PRO_ADD)
+                fold_add_stage<DT>(stage_a(s), gb_slot(s), t, ni);
             else
                 fold_ln_stage<DT>(stage_a(s), gb_slot(s), p.beta != nullptr, t, ni, mean, rstd);
             fence_proxy_async_smem();
@@ -275,10 +279,10 @@ __global__ void __launch_bounds__(splitk_threads<PRO>(), 1)
             // cache while the main loop runs (a miss there costs an L2
             // round trip on the critical path)
             uint32_t touch = (uint32_t)p.xc_stride ^ p.xc_owner[lane] ^ p.xc_pos[lane] ^ p.xc_c0[lane & 7] ^
-                             __float_as_uint(p.inv_k) ^ __float_as_uint(p.eps) ^ (uint32_t)p.act ^ (uint32_t)p.N ^
-                             (uint32_t)reinterpret_cast<uintptr_t>(p.residual) ^
-                             (uint32_t)reinterpret_cast<uintptr_t>(p.out_ptr) ^
-                             (uint32_t)reinterpret_cast<uintptr_t>(p.bias);
+                             __float_as_uint(p.inv_k) ^ __float_as_uint(p.eps) ^ (uint32_t)p.act[osel.oi] ^
+                             (uint32_t)p.N[osel.oi] ^ (uint32_t)reinterpret_cast<uintptr_t>(p.residual) ^
+                             (uint32_t)reinterpret_cast<uintptr_t>(p.out_ptr[osel.oi]) ^
+                             (uint32_t)reinterpret_cast<uintptr_t>(p.bias[osel.oi]);
             asm volatile("" ::"r"(touch));
         }
 
@@ -375,12 +379,15 @@ __global__ void __launch_bounds__(splitk_threads<PRO>(), 1)
     const int xsh = xw > 8 ? 4 : 3;
     const int xch = threadIdx.x & ((1 << xsh) - 1);
     const int xcol = n0 + (xc0 + xch) * 8;
-    const bool xmine = xch < xw && xcol < p.N;
+    const int N = p.N[osel.oi];
+    const int act = p.act[osel.oi];
+    const void* obias = p.bias[osel.oi];
+    const bool xmine = xch < xw && xcol < N;
     float bb[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) bb[e] = 0.f;
-    if (xmine && p.bias != nullptr) {  // in flight across the barrier
-        const uint4 bv = ldg_v4(reinterpret_cast<const uint16_t*>(p.bias) + xcol);
+    if (xmine && obias != nullptr) {  // in flight across the barrier
+        const uint4 bv = ldg_v4(reinterpret_cast<const uint16_t*>(obias) + xcol);
         const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -396,12 +403,12 @@ __global__ void __launch_bounds__(splitk_threads<PRO>(), 1)
     if (xchg_ok && xmine) {
         using T = uint16_t;
         const T* res = reinterpret_cast<const T*>(p.residual);
-        T* out = reinterpret_cast<T*>(p.out_ptr);
+        T* out = reinterpret_cast<T*>(p.out_ptr[osel.oi]);
         const int stride = p.xc_stride;
         const uint32_t slot_bytes = (uint32_t)(rows * stride) * 4u;
         const int nthreads = (int)blockDim.x;
         for (int row = (int)threadIdx.x >> xsh; row < rows; row += nthreads >> xsh) {
-            const size_t g = (size_t)(m0 + row) * p.N + xcol;
+            const size_t g = (size_t)(m0 + row) * N + xcol;
             uint4 rv = make_uint4(0u, 0u, 0u, 0u);
             if (res != nullptr) rv = *reinterpret_cast<const uint4*>(res + g);
             float v[8];
@@ -425,9 +432,9 @@ __global__ void __launch_bounds__(splitk_threads<PRO>(), 1)
             const float rs = PRO == PRO_RMS ? rsqrtf(fmaf(ss, p.inv_k, p.eps)) : 1.f;
 #pragma unroll
             for (int e = 0; e < 8; ++e) v[e] = fmaf(v[e], rs, bb[e]);
-            if (p.act != ACT_NONE) {
+            if (act != ACT_NONE) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] = act_apply(p.act, v[e]);
+                for (int e = 0; e < 8; ++e) v[e] = act_apply(act, v[e]);
             }
             if (res != nullptr) {
                 const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};

@@ -128,6 +128,59 @@ fl_status fl_norm_gemm(const void* x, const void* gamma, const void* beta, const
                        const void* bias, void* out, int M, int N, int K, float eps,
                        fl_norm_kind norm_kind, fl_act act, fl_dtype dtype, void* stream);
 
+/* Most outputs one fl_norm_gemm_multi call computes. */
+#define FL_MAX_OUTPUTS 4
+
+/*
+ * Several consumers of one normalised activation in one launch (horizontal
+ * fusion: operators sharing a common input, the inferensys "Fusion Compiler"
+ * glossary, fusion groups). For i < n_out:
+ *   out_i[M, N_i] = act_i(norm(x)[M, K] W_i[N_i, K]^T + bias_i)
+ * with norm(x) as in fl_norm_gemm. This is the case the LLMBoost README's
+ * "one-user safety guard" leaves unfused (a normalised tensor with two or
+ * more consumers, e.g. the Q, K and V projections or an MoE gate): here the
+ * LayerNorm statistics are computed once for all outputs, the RMS statistics
+ * come with the fold, and every output's tiles share one launch (one grid
+ * over the outputs side by side along N), so no consumer waits for another
+ * and none rereads a materialised norm(x).
+ *   n_out:  1 .. FL_MAX_OUTPUTS.
+ *   W[i]:   [N_i, K] device pointers; out[i]: [M, N_i] device pointers.
+ *   bias:   NULL (no bias anywhere) or an array whose entries are [N_i] or NULL.
+ *   N[i]:   multiples of 8. act: NULL (no activation) or one fl_act per output.
+ * The arrays themselves are host memory, read during the call only. Outputs
+ * may not overlap each other or any input. Memory and errors as fl_norm_gemm.
+ */
+fl_status fl_norm_gemm_multi(const void* x, const void* gamma, const void* beta, int n_out,
+                             const void* const* W, const void* const* bias, void* const* out,
+                             const int* N, const int* act, int M, int K, float eps,
+                             fl_norm_kind norm_kind, fl_dtype dtype, void* stream);
+
+/*
+ * Elementwise input prologue (the "hackable compiler" post's example
+ * torch.relu(torch.matmul(x + bias, w)), whose prologue adds a bias along K
+ * inside the reduction loop):
+ *   out[M,N] = act((A[M,K] + bias_in[K]) W[N,K]^T + bias[N]) (+ residual[M,N])
+ * A + bias_in is formed in the staged operand (rounded once to the dtype) and
+ * never stored. bias_in: required. bias, residual: [N], [M,N] or NULL;
+ * residual may be the same pointer as out. Epilogue order as fl_gemm_epilogue.
+ * Allocates nothing.
+ */
+fl_status fl_input_bias_gemm(const void* A, const void* bias_in, const void* W, const void* bias,
+                             const void* residual, void* out, int M, int N, int K, fl_act act,
+                             fl_dtype dtype, void* stream);
+
+/*
+ * Standalone RMSNorm, out[M,K] = x * gamma / sqrt(mean_k(x^2) + eps), computed
+ * in fp32 and rounded once: the generated RMSNorm kernel of the "hackable
+ * compiler" post (sum of squares, times 1/K, plus eps, rsqrt, times x, times
+ * the weight). For a normalised tensor with more consumers than
+ * fl_norm_gemm_multi takes, or consumers that are not GEMMs. out may be x
+ * itself (in place) but may not otherwise overlap x or gamma. K must be a
+ * multiple of 8. Allocates nothing. Bound by HBM bandwidth.
+ */
+fl_status fl_rms_norm(const void* x, const void* gamma, void* out, int M, int K, float eps,
+                      fl_dtype dtype, void* stream);
+
 /* Bytes of workspace fl_swiglu_ffn needs: the hidden activation h [M,F] in the dtype. */
 size_t fl_swiglu_ffn_workspace_size(int M, int F, fl_dtype dtype);
 

@@ -195,6 +195,18 @@ def norm_gemm(x, gamma, beta, W, bias, eps: float, norm: str, act: str = "none")
     return _epilogue(linear(xh, W), bias, act, None)
 
 
+def input_bias_gemm(A, bias_in, W, bias, residual, act: str = "none"):
+    """Elementwise input prologue: act((A + bias_in) W^T + bias) (+ residual).
+
+    The hackable-compiler page's example torch.relu(torch.matmul(x + bias, w))
+    adds a bias along K to the activation inside the reduction loop (its
+    Loop IR "prologue (inside reduce)"); this is that prologue followed by
+    the usual epilogue. bias_in has K entries; bias and residual may be absent.
+    """
+    Ab = np.asarray(A, dtype=np.float64) + np.asarray(bias_in, dtype=np.float64)[None, :]
+    return _epilogue(linear(Ab, W), bias, act, residual)
+
+
 def fused_pattern(pattern: str, A, W, bias=None, residual=None, gamma=None, beta=None,
                   eps: float = 1e-6):
     """Any of the nine patterns by name (norm patterns: no bias, no activation)."""

@@ -138,3 +138,15 @@ def chain_swiglu_ffn(x, gamma, Wg, Wu, Wd, bias_down, eps, dtype):
     h = _r(_r(oracle.silu(g), dtype) * u, dtype)
     d = _r(_bias_add(oracle.linear(h, Wd), bias_down), dtype)
     return _r(d + np.asarray(x, dtype=np.float64), dtype)
+
+
+def chain_input_bias_gemm(A, bias_in, W, bias, residual, act, dtype):
+    """A + bias_in stored in the dtype, then linear (+ bias) stored, then the
+    activation and the residual add, each stored."""
+    Ab = _r(np.asarray(A, dtype=np.float64) + np.asarray(bias_in, dtype=np.float64)[None, :], dtype)
+    y = _r(_bias_add(oracle.linear(Ab, W), bias), dtype)
+    if act != "none":
+        y = _r(oracle.ACTIVATIONS[act](y), dtype)
+    if residual is not None:
+        y = _r(y + np.asarray(residual, dtype=np.float64), dtype)
+    return y

@@ -161,3 +161,58 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(fl, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         fl.lib()
+
+
+def multi(L, x=addr(0), g=addr(1), b=None, n=3, Ws=None, biases=None, outs=None, Ns=None, acts=None, M=64, K=64,
+          eps=1e-6, nk=0, dt=0):
+    Ws = Ws if Ws is not None else [addr(10 + i) for i in range(n)]
+    outs = outs if outs is not None else [addr(20 + i) for i in range(n)]
+    Ns = Ns if Ns is not None else [64] * n
+    arr = ctypes.c_void_p * max(n, 1)
+    W_arr = arr(*Ws[:max(n, 1)]) if Ws else None
+    o_arr = arr(*outs[:max(n, 1)]) if outs else None
+    b_arr = arr(*biases) if biases is not None else None
+    N_arr = (ctypes.c_int * max(n, 1))(*Ns[:max(n, 1)])
+    a_arr = (ctypes.c_int * max(n, 1))(*acts) if acts is not None else None
+    return L.fl_norm_gemm_multi(x, g, b, n, W_arr, b_arr, o_arr, N_arr, a_arr, M, K, eps, nk, dt, None)
+
+
+def test_norm_gemm_multi_validation(L):
+    assert multi(L, n=0) == INVALID and multi(L, n=5, Ws=[addr(10 + i) for i in range(5)],
+                                              outs=[addr(20 + i) for i in range(5)], Ns=[64] * 5) == INVALID
+    assert multi(L, x=None) == INVALID and multi(L, g=None) == INVALID
+    assert multi(L, Ws=[addr(10), None, addr(12)]) == INVALID
+    assert multi(L, outs=[addr(20), addr(21), None]) == INVALID
+    assert multi(L, Ns=[64, 60, 64]) == ALIGN
+    assert multi(L, Ns=[64, 0, 64]) == INVALID
+    assert multi(L, acts=[0, 4, 0]) == INVALID
+    assert multi(L, nk=3) == INVALID and multi(L, dt=2) == INVALID and multi(L, eps=-1.0) == INVALID
+    assert multi(L, biases=[None, addr(30, 2), None]) == ALIGN
+    # outputs overlapping each other or an input
+    assert multi(L, outs=[addr(20), addr(20, 64), addr(22)]) == INVALID and "out[" in fl.last_error()
+    assert multi(L, outs=[addr(20), addr(11), addr(22)]) == INVALID   # out[1] is W[1]
+    assert multi(L, outs=[addr(0, 32), addr(21), addr(22)]) == INVALID  # out[0] overlaps x
+    st = multi(L)  # valid: reaches the device query
+    assert st in (OK, UNSUPPORTED, CUDA)
+
+
+def test_input_bias_gemm_validation(L):
+    def call(A=addr(0), bi=addr(1), W=addr(2), bias=None, res=None, out=addr(4), M=64, N=64, K=64, act=0, dt=0):
+        return L.fl_input_bias_gemm(A, bi, W, bias, res, out, M, N, K, act, dt, None)
+    assert call(A=None) == INVALID and call(bi=None) == INVALID and call(W=None) == INVALID
+    assert call(out=None) == INVALID and call(act=5) == INVALID and call(dt=3) == INVALID
+    assert call(K=12) == ALIGN and call(bi=addr(1, 2)) == ALIGN
+    assert call(out=addr(2, 16)) == INVALID                   # out overlaps W
+    assert call(res=addr(4, 16)) == INVALID and "alias" in fl.last_error()
+    assert call(res=addr(4)) in (OK, UNSUPPORTED, CUDA)        # exact alias allowed
+
+
+def test_rms_norm_validation(L):
+    def call(x=addr(0), g=addr(1), out=addr(2), M=4, K=64, eps=1e-6, dt=0):
+        return L.fl_rms_norm(x, g, out, M, K, eps, dt, None)
+    assert call(x=None) == INVALID and call(g=None) == INVALID and call(out=None) == INVALID
+    assert call(M=0) == INVALID and call(K=0) == INVALID and call(K=20) == ALIGN
+    assert call(eps=float("nan")) == INVALID and call(dt=5) == INVALID
+    assert call(out=addr(0, 16)) == INVALID                    # partial overlap with x
+    assert call(out=addr(1)) == INVALID                        # out overlaps gamma
+    assert call(out=addr(0)) in (OK, UNSUPPORTED, CUDA)        # in place

@@ -1,0 +1,198 @@
+"""CUDA path vs the float64 oracle for the horizontal-fusion, input-prologue
+and standalone-RMSNorm entry points (needs an sm_103a GPU).
+
+* fl_norm_gemm_multi: one normalised activation feeding several weights in one
+  launch; every output is compared element by element with oracle.norm_gemm
+  for its own weight, bias and activation.
+* fl_input_bias_gemm: act((A + bias_in) W^T + bias) (+ residual) against
+  oracle.input_bias_gemm.
+* fl_rms_norm: against oracle.rms_norm.
+Tolerances (and the bf16 unfused-chain guard) are in tests/parity.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gemm_epilogue_tma_gb300 as fl
+import oracle
+import parity
+from gemm_epilogue_tma_gb300 import _build
+from gemm_epilogue_tma_gb300 import synthetic as syn
+from parity import assert_close, sample_rows
+
+pytestmark = pytest.mark.gpu
+DTYPES = ("f16", "bf16")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def library():
+    _build.build()
+    fl.lib()
+    torch.cuda.set_device(0)
+    yield
+    for k in ("tile_n", "variant", "split_k"):
+        fl.set_option(k, 0)
+    fl.device_status()
+
+
+def f64(t):
+    return syn.as_f64(t)
+
+
+def dev(t):
+    return None if t is None else t.cuda()
+
+
+def multi_inputs(M, Ns, K, norm, dt, seed=0):
+    """x, gamma, beta and one (W, bias) per output, from one seeded generator."""
+    rng = syn.rng_for(41, seed, syn.DTYPE_IDS[dt], M, K, *Ns)
+    draw = lambda shape, mean, std: syn._draw(rng, shape, mean, std, dt)
+    x = draw((M, K), 0.0, 1.0)
+    Ws = [draw((N, K), 0.0, 1.0 / np.sqrt(K)) for N in Ns]
+    biases = [draw((N,), 0.0, 0.1) for N in Ns]
+    gamma = draw((K,), 1.0, 0.1)
+    beta = draw((K,), 0.0, 0.1) if norm == "layer" else None
+    return x, gamma, beta, Ws, biases
+
+
+def run_multi(M, Ns, K, norm, dt, acts=None, with_bias=True, rows=None, opts=None):
+    x, gamma, beta, Ws, biases = multi_inputs(M, Ns, K, norm, dt)
+    acts = acts or ["none"] * len(Ns)
+    eps = 1e-5 if norm == "layer" else 1e-6
+    for k, v in (opts or {}).items():
+        fl.set_option(k, v)
+    try:
+        outs = fl.norm_gemm_multi(dev(x), dev(gamma), [dev(W) for W in Ws], beta=dev(beta),
+                                  biases=[dev(b) for b in biases] if with_bias else None, acts=acts, eps=eps,
+                                  norm=norm)
+        torch.cuda.synchronize()
+        fl.device_status()
+    finally:
+        for k in (opts or {}):
+            fl.set_option(k, 0)
+    sel = slice(None) if rows is None else rows
+    for i, (W, b, act, out) in enumerate(zip(Ws, biases, acts, outs)):
+        args = (f64(x)[sel], f64(gamma), f64(beta), f64(W), f64(b) if with_bias else None, eps, norm, act)
+        ref = oracle.norm_gemm(*args)
+        assert_close(out[sel], ref, dt, f"multi {norm} {dt} {M}x{Ns}x{K} out{i}",
+                     chain=parity.chain_norm_gemm(*args, dt))
+    return outs
+
+
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("norm", ["rms", "layer"])
+@pytest.mark.parametrize("shape", [(300, (200, 136, 72), 520), (129, (264, 8), 72), (1, (64, 32, 32, 16), 128),
+                                   (512, (512, 256, 256), 1024)],
+                         ids=lambda s: f"{s[0]}x{'-'.join(map(str, s[1]))}x{s[2]}")
+def test_multi_ragged(dt, norm, shape):
+    M, Ns, K = shape
+    run_multi(M, Ns, K, norm, dt, acts=["none", "gelu", "silu", "relu"][:len(Ns)])
+
+
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("variant", ["tile", "splitk", "pair", "pair_ksplit"])
+def test_multi_forced_variants(dt, variant):
+    opts = {"tile": {"variant": 1}, "splitk": {"variant": 2, "split_k": 3}, "pair": {"variant": 3},
+            "pair_ksplit": {"variant": 3, "split_k": 2}}[variant]
+    run_multi(300, (264, 136, 520), 1000, "rms", dt, acts=["silu", "none", "gelu"], opts=opts)
+    run_multi(200, (136, 72), 520, "layer", dt, opts=opts)
+
+
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("M", [1, 32, 4096])
+def test_multi_qkv(dt, M):
+    """Q, K, V projections of one RMSNorm'd activation: D = 4096, grouped K/V of 1024."""
+    rows = sample_rows(M, n=128)
+    run_multi(M, (4096, 1024, 1024), 4096, "rms", dt, with_bias=False, rows=rows)
+
+
+def test_multi_output_and_single_call_agree():
+    """An output of a two-output launch and the single-output call of the same
+    weight both meet the bound against the oracle (the two calls may take
+    different kernels: twice the tiles changes the dispatch)."""
+    x, gamma, beta, Ws, biases = multi_inputs(384, (512, 512), 768, "rms", "bf16")
+    outs = fl.norm_gemm_multi(dev(x), dev(gamma), [dev(W) for W in Ws], biases=[dev(b) for b in biases],
+                              acts=["gelu", "none"])
+    one = fl.norm_gemm(dev(x), dev(gamma), dev(Ws[1]), bias=dev(biases[1]), eps=1e-6, norm="rms")
+    torch.cuda.synchronize()
+    ref = oracle.norm_gemm(f64(x), f64(gamma), None, f64(Ws[1]), f64(biases[1]), 1e-6, "rms")
+    assert_close(one, ref, "bf16", "single")
+    assert_close(outs[1], ref, "bf16", "multi out1")
+
+
+# ---------------------------------------------------------------------------
+# input-bias prologue
+# ---------------------------------------------------------------------------
+def run_input_bias(M, N, K, dt, act, with_bias, with_res, opts=None, seed=0, rows=None):
+    rng = syn.rng_for(42, seed, syn.DTYPE_IDS[dt], M, N, K)
+    draw = lambda shape, mean, std: syn._draw(rng, shape, mean, std, dt)
+    A, W = draw((M, K), 0.0, 1.0), draw((N, K), 0.0, 1.0 / np.sqrt(K))
+    bi, b, r = draw((K,), 0.0, 0.5), draw((N,), 0.0, 0.1), draw((M, N), 0.0, 1.0)
+    for k, v in (opts or {}).items():
+        fl.set_option(k, v)
+    try:
+        got = fl.input_bias_gemm(dev(A), dev(bi), dev(W), bias=dev(b) if with_bias else None,
+                                 residual=dev(r) if with_res else None, act=act)
+        torch.cuda.synchronize()
+        fl.device_status()
+    finally:
+        for k in (opts or {}):
+            fl.set_option(k, 0)
+    sel = slice(None) if rows is None else rows
+    args = (f64(A)[sel], f64(bi), f64(W), f64(b) if with_bias else None, f64(r)[sel] if with_res else None, act)
+    ref = oracle.input_bias_gemm(*args)
+    assert_close(got[sel], ref, dt, f"input bias {dt} {act} {M}x{N}x{K} b={with_bias} r={with_res}",
+                 chain=parity.chain_input_bias_gemm(*args, dt))
+
+
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("act", ["none", "gelu", "silu", "relu"])
+@pytest.mark.parametrize("shape", [(1, 8, 8), (200, 136, 328), (300, 520, 1000)], ids=lambda s: "x".join(map(str, s)))
+def test_input_bias_ragged(dt, act, shape):
+    M, N, K = shape
+    run_input_bias(M, N, K, dt, act, with_bias=True, with_res=act == "none")
+    run_input_bias(M, N, K, dt, act, with_bias=False, with_res=False)
+
+
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("variant", ["tile128", "tile256", "splitk", "pair", "pair_ksplit"])
+def test_input_bias_forced_variants(dt, variant):
+    opts = {"tile128": {"variant": 1, "tile_n": 128}, "tile256": {"variant": 1, "tile_n": 256},
+            "splitk": {"variant": 2, "split_k": 4}, "pair": {"variant": 3},
+            "pair_ksplit": {"variant": 3, "split_k": 2}}[variant]
+    run_input_bias(300, 520, 1000, dt, "relu", with_bias=True, with_res=False, opts=opts)
+
+
+def test_input_bias_large():
+    """The plain-pattern workload size with the prologue, on sampled rows."""
+    run_input_bias(2048, 4096, 4096, "f16", "gelu", with_bias=True, with_res=False, rows=sample_rows(2048))
+
+
+# ---------------------------------------------------------------------------
+# standalone RMSNorm
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("shape", [(1, 8), (7, 264), (300, 4096), (33, 4104), (64, 11008), (4096, 4096)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_rms_norm(dt, shape):
+    M, K = shape
+    t = syn.norm_gemm_inputs(M, 8, K, "rms", dt)
+    x = t["x"].clone()
+    if M > 2:
+        x[1] = 0.0  # a zero row normalises to zero
+    got = fl.rms_norm(dev(x), dev(t["gamma"]), eps=1e-6)
+    torch.cuda.synchronize()
+    ref = oracle.rms_norm(f64(x), f64(t["gamma"]), 1e-6)
+    assert_close(got, ref, dt, f"rms_norm {dt} {M}x{K}", chain=oracle.round_to_dtype(ref, dt))
+    if M > 2:
+        assert bool((got[1] == 0).all())
+
+
+def test_rms_norm_in_place():
+    t = syn.norm_gemm_inputs(129, 8, 4096 + 2048, "rms", "bf16")
+    x = dev(t["x"])
+    y = fl.rms_norm(x, dev(t["gamma"]), out=x, eps=1e-6)
+    torch.cuda.synchronize()
+    assert y.data_ptr() == x.data_ptr()
+    ref = oracle.rms_norm(f64(t["x"]), f64(t["gamma"]), 1e-6)
+    assert_close(y, ref, "bf16", "rms_norm in place")

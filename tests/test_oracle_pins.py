@@ -415,6 +415,61 @@ def test_swiglu_degenerate_weights():
 
 
 # ----------------------------------------------------------------------------
+# 7b. the elementwise input prologue (x + bias along K, then the GEMM)
+# ----------------------------------------------------------------------------
+
+def check_input_bias_bruteforce(fn):
+    rng = np.random.default_rng(31)
+    for (M, N, K) in [(1, 1, 1), (3, 2, 7), (5, 8, 16), (4, 7, 7)]:
+        A, W = dyadic(rng, M, K), dyadic(rng, N, K)
+        bi, b, r = dyadic(rng, K), dyadic(rng, N), dyadic(rng, M, N)
+        for act in ("none", "gelu", "silu", "relu"):
+            for use_b, use_r in ((False, False), (True, False), (True, True)):
+                # exact rational (A + bias_in) first: the sums are over that
+                acc = bf_linear(np.array([[float(Fraction(float(A[m, k])) + Fraction(float(bi[k])))
+                                           for k in range(K)] for m in range(M)]), W)
+                want = np.empty_like(acc)
+                for m in range(M):
+                    for n in range(N):
+                        v = bf_act(act, acc[m, n] + (float(b[n]) if use_b else 0.0))
+                        want[m, n] = v + (float(r[m, n]) if use_r else 0.0)
+                got = fn(A, bi, W, b if use_b else None, r if use_r else None, act)
+                np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+def test_input_bias_bruteforce():
+    check_input_bias_bruteforce(O.input_bias_gemm)
+
+
+def test_input_bias_page_example_against_torch():
+    """The page's example relu(matmul(x + bias, w)), x (16, 64), bias (64,), w (64, 16):
+    w is [K, N] there, so W = w^T in the linear-layer layout."""
+    g = torch.Generator().manual_seed(5)
+    x = torch.randn(16, 64, generator=g, dtype=torch.float64)
+    bias = torch.randn(64, generator=g, dtype=torch.float64)
+    w = torch.randn(64, 16, generator=g, dtype=torch.float64)
+    want = torch.relu(torch.matmul(x + bias, w)).numpy()
+    got = O.input_bias_gemm(x.numpy(), bias.numpy(), w.numpy().T, None, None, "relu")
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+    # and with an output bias and residual, against F.linear
+    ob, res = torch.randn(16, generator=g, dtype=torch.float64), torch.randn(16, 16, generator=g, dtype=torch.float64)
+    want = (F.silu(F.linear(x + bias, w.T, ob)) + res).numpy()
+    got = O.input_bias_gemm(x.numpy(), bias.numpy(), w.numpy().T, ob.numpy(), res.numpy(), "silu")
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+def test_input_bias_reduces_to_gemm_patterns():
+    rng = np.random.default_rng(32)
+    A, W, b = rand(rng, 6, 24), rand(rng, 10, 24, scale=0.2), rand(rng, 10)
+    np.testing.assert_array_equal(O.input_bias_gemm(A, np.zeros(24), W, b, None, "gelu"),
+                                  O.gemm_epilogue(A, W, b, None, "gemm_bias_gelu"))
+    # W = I: the output is act(A + bias_in + bias)
+    bi = rand(rng, 24)
+    np.testing.assert_allclose(O.input_bias_gemm(A, bi, np.eye(24), None, None, "relu"),
+                               np.maximum(A + bi[None, :], 0.0), rtol=0, atol=1e-15)
+
+
+# ----------------------------------------------------------------------------
 # 8. planted mistakes: each plausible slip in a copy of the oracle fails a pin
 # ----------------------------------------------------------------------------
 
@@ -496,3 +551,14 @@ def test_planted_mistakes_are_caught():
 
     for bad in (h_unrounded, swapped, no_residual):
         assert _fails(check_swiglu_bruteforce, bad), bad.__name__
+
+    # input prologue: bias_in dropped, or added to the output instead of the input
+    def no_bias_in(A, bi, W, b, r, act):
+        return O.input_bias_gemm(A, np.zeros_like(bi), W, b, r, act)
+
+    def bias_in_after(A, bi, W, b, r, act):
+        y = O._epilogue(O.linear(A, W), b, act, r)
+        return y + (bi[None, :y.shape[1]] if y.shape[1] <= bi.shape[0] else 0.0)
+
+    for bad in (no_bias_in, bias_in_after):
+        assert _fails(check_input_bias_bruteforce, bad), bad.__name__
