@@ -55,10 +55,21 @@ WORKLOADS = {
 
 def parse_workload(name: str) -> dict:
     """A named workload, or kind:args: pattern:<name>:<dt>:M:N:K, norm:<rms|layer>:<dt>:M:N:K,
-    swiglu:<dt>:M:D:F."""
+    swiglu:<dt>:M:D:F, multi:<rms|layer>:<dt>:M:K:N1,N2,.. (one norm, several weights),
+    biasin:<dt>:M:N:K:<act> (input-bias prologue), rmsnorm:<dt>:M:K (standalone RMSNorm)."""
     if name in WORKLOADS:
         return dict(WORKLOADS[name], name=name)
     parts = name.split(":")
+    if parts[0] == "multi":
+        _, nm, dt, M, K, Ns = parts
+        return dict(kind="multi", norm=nm, dtype=dt, M=int(M), K=int(K), Ns=[int(n) for n in Ns.split(",")],
+                    eps=1e-6 if nm == "rms" else 1e-5, name=name)
+    if parts[0] == "biasin":
+        _, dt, M, N, K, act = parts
+        return dict(kind="biasin", dtype=dt, M=int(M), N=int(N), K=int(K), act=act, name=name)
+    if parts[0] == "rmsnorm":
+        _, dt, M, K = parts
+        return dict(kind="rmsnorm", dtype=dt, M=int(M), K=int(K), eps=1e-6, name=name)
     if parts[0] == "pattern":
         _, pat, dt, M, N, K = parts
         return dict(kind="pattern", pattern=pat, dtype=dt, M=int(M), N=int(N), K=int(K), name=name)
@@ -78,6 +89,15 @@ def describe(w: dict) -> str:
         return f"{nm} {w['dtype']}: x[{w['M']},{w['K']}] gamma[{w['K']}] eps={w['eps']:g} W[{w['N']},{w['K']}], no bias"
     if w["kind"] == "pattern":
         return f"{w['pattern']} {w['dtype']}: A[{w['M']},{w['K']}] W[{w['N']},{w['K']}]"
+    if w["kind"] == "multi":
+        nm = "rmsnorm" if w["norm"] == "rms" else "layernorm"
+        ws = ", ".join(f"W{i}[{n},{w['K']}]" for i, n in enumerate(w["Ns"]))
+        return f"{nm} feeding {len(w['Ns'])} weights {w['dtype']}: x[{w['M']},{w['K']}] eps={w['eps']:g}, {ws}"
+    if w["kind"] == "biasin":
+        return (f"input-bias prologue {w['dtype']}: act={w['act']}((A[{w['M']},{w['K']}] + b_in[{w['K']}]) "
+                f"W[{w['N']},{w['K']}]^T + bias)")
+    if w["kind"] == "rmsnorm":
+        return f"standalone rmsnorm {w['dtype']}: x[{w['M']},{w['K']}] gamma[{w['K']}] eps={w['eps']:g}"
     return (f"swiglu_ffn {w['dtype']}: x[{w['M']},{w['D']}] RMSNorm, Wg/Wu[{w['F']},{w['D']}], "
             f"Wd[{w['D']},{w['F']}], + x")
 
@@ -101,11 +121,15 @@ def roofline_of(flops: float, nbytes: float, per_launch_ms: float, peaks: dict, 
             "peak_source": f"bf16_tflops (burst, fp16 dense rate equal) of {peak_src}", **common}
 
 
-def launches_of(w) -> int:
+def launches_of(w, separate=False) -> int:
     """Kernels of this library one step launches: the SwiGLU block is two fused
-    GEMMs; LayerNorm adds its row-statistics pass ahead of the fused GEMM."""
+    GEMMs; LayerNorm adds its row-statistics pass ahead of the fused GEMM; a
+    multi-consumer step is one launch (or one call per weight with --separate)."""
     if w["kind"] == "swiglu":
         return 2
+    if w["kind"] == "multi":
+        calls = len(w["Ns"]) if separate else 1
+        return calls * (2 if w["norm"] == "layer" else 1)
     if w["kind"] == "norm" and w["norm"] == "layer":
         return 2
     return 1
@@ -117,8 +141,16 @@ def flops_per_step(w: dict) -> float:
     if w["kind"] == "swiglu":
         M, D, F = w["M"], w["D"], w["F"]
         return 6.0 * M * D * F + 3 * M * D + 2 * M * F + 4 * M * F + M * F + M * D
+    if w["kind"] == "multi":
+        M, K = w["M"], w["K"]
+        return sum(2.0 * M * N * K + M * N for N in w["Ns"]) + 3 * M * K
+    if w["kind"] == "rmsnorm":
+        return 4.0 * w["M"] * w["K"]  # square-accumulate (2), scale by 1/rms and by gamma (2)
     M, N, K = w["M"], w["N"], w["K"]
     f = 2.0 * M * N * K
+    if w["kind"] == "biasin":
+        acts = {"none": 0, "gelu": 8, "silu": 4, "relu": 1}
+        return f + M * K + M * N * (1 + acts[w["act"]])
     if w["kind"] == "norm":
         return f + 3 * M * K + M * N
     p = w["pattern"]
@@ -132,8 +164,15 @@ def bytes_per_step(w: dict) -> float:
     if w["kind"] == "swiglu":
         M, D, F = w["M"], w["D"], w["F"]
         return e * (M * D + D + 2 * F * D + 2 * M * F + D * F + M * D + M * D)
+    if w["kind"] == "multi":
+        M, K = w["M"], w["K"]
+        return e * (M * K + K * (2 if w["norm"] == "layer" else 1) + sum(N * K + M * N for N in w["Ns"]))
+    if w["kind"] == "rmsnorm":
+        return e * (2 * w["M"] * w["K"] + w["K"])
     M, N, K = w["M"], w["N"], w["K"]
     b = e * (M * K + N * K + M * N)
+    if w["kind"] == "biasin":
+        return b + e * (K + N)
     if w["kind"] == "norm":
         b += e * K * (2 if w["norm"] == "layer" else 1)
     else:
@@ -148,7 +187,28 @@ def make_inputs(w: dict):
         return syn.norm_gemm_inputs(w["M"], w["N"], w["K"], w["norm"], w["dtype"])
     if w["kind"] == "pattern":
         return syn.gemm_inputs(w["M"], w["N"], w["K"], w["pattern"], w["dtype"])
+    if w["kind"] == "multi":
+        t = syn.multi_inputs(w["M"], w["Ns"], w["K"], w["norm"], w["dtype"])
+        return {k: v for k, v in t.items() if not k.startswith("bias")}  # the timed calls use no output bias
+    if w["kind"] == "biasin":
+        t = syn.input_bias_inputs(w["M"], w["N"], w["K"], w["dtype"])
+        t.pop("residual")
+        return t
+    if w["kind"] == "rmsnorm":
+        t = syn.norm_gemm_inputs(w["M"], 8, w["K"], "rms", w["dtype"])
+        return {"x": t["x"], "gamma": t["gamma"]}
     return syn.swiglu_inputs(w["M"], w["D"], w["F"], w["dtype"])
+
+
+def out_shapes(w: dict):
+    """Shapes of the tensors one step writes."""
+    if w["kind"] == "multi":
+        return [(w["M"], N) for N in w["Ns"]]
+    if w["kind"] == "swiglu":
+        return [(w["M"], w["D"])]
+    if w["kind"] == "rmsnorm":
+        return [(w["M"], w["K"])]
+    return [(w["M"], w["N"])]
 
 
 # ---------------------------------------------------------------------------
@@ -300,6 +360,13 @@ def oracle_step(w: dict, f64: dict, row0: int, rows: int):
         r = f64.get("residual")
         return oracle.gemm_epilogue(f64["A"][sl], f64["W"], f64.get("bias"), None if r is None else r[sl],
                                     w["pattern"])
+    if w["kind"] == "multi":
+        return [oracle.norm_gemm(f64["x"][sl], f64["gamma"], f64.get("beta"), f64[f"W{i}"], None, w["eps"], w["norm"])
+                for i in range(len(w["Ns"]))]
+    if w["kind"] == "biasin":
+        return oracle.input_bias_gemm(f64["A"][sl], f64["bias_in"], f64["W"], f64["bias"], None, w["act"])
+    if w["kind"] == "rmsnorm":
+        return oracle.rms_norm(f64["x"][sl], f64["gamma"], w["eps"])
     return oracle.swiglu_ffn(f64["x"][sl], f64["gamma"], f64["Wg"], f64["Wu"], f64["Wd"], None, w["eps"], w["dtype"])
 
 
@@ -378,21 +445,35 @@ def run_ours(args, w: dict, rank: int, world: int, local: int):
     dev = torch.device("cuda", local)
     t = make_inputs(w)
     set_bytes = sum(v.numel() * v.element_size() for v in t.values() if v is not None)
-    out_shape = (w["M"], w["N"]) if w["kind"] != "swiglu" else (w["M"], w["D"])
-    out_bytes = out_shape[0] * out_shape[1] * 2
+    shapes = out_shapes(w)
+    out_bytes = sum(a * b * 2 for a, b in shapes)
     nsets = max(2, int(3 * L2_BYTES // (set_bytes + out_bytes)) + 1)
     sets = []
     for _ in range(nsets):
         g = {k: (v.to(dev) if v is not None else None) for k, v in t.items()}
-        g["out"] = torch.empty(out_shape, dtype=t[next(iter(t))].dtype, device=dev)
+        g["outs"] = [torch.empty(sh, dtype=t[next(iter(t))].dtype, device=dev) for sh in shapes]
+        g["out"] = g["outs"][0]
         if w["kind"] == "swiglu":
             g["ws"] = torch.empty(fl.swiglu_ffn_workspace_size(w["M"], w["F"], w["dtype"]), dtype=torch.uint8,
                                   device=dev)
         sets.append(g)
-    launches_per_step = launches_of(w)
+    launches_per_step = launches_of(w, args.separate)
+    n_out = len(shapes)
 
     def step(g, stream=None):
-        if w["kind"] == "norm":
+        if w["kind"] == "multi" and args.separate:
+            for i in range(n_out):
+                fl.norm_gemm(g["x"], g["gamma"], g[f"W{i}"], beta=g.get("beta"), out=g["outs"][i], eps=w["eps"],
+                             norm=w["norm"], stream=stream)
+        elif w["kind"] == "multi":
+            fl.norm_gemm_multi(g["x"], g["gamma"], [g[f"W{i}"] for i in range(n_out)], beta=g.get("beta"),
+                               outs=g["outs"], eps=w["eps"], norm=w["norm"], stream=stream)
+        elif w["kind"] == "biasin":
+            fl.input_bias_gemm(g["A"], g["bias_in"], g["W"], bias=g["bias"], out=g["out"], act=w["act"],
+                               stream=stream)
+        elif w["kind"] == "rmsnorm":
+            fl.rms_norm(g["x"], g["gamma"], out=g["out"], eps=w["eps"], stream=stream)
+        elif w["kind"] == "norm":
             fl.norm_gemm(g["x"], g["gamma"], g["W"], beta=g.get("beta"), out=g["out"], eps=w["eps"],
                          norm=w["norm"], stream=stream)
         elif w["kind"] == "pattern":
@@ -467,7 +548,7 @@ def run_ours(args, w: dict, rank: int, world: int, local: int):
 
     # end to end through the same call: pinned host inputs in, result back to pinned host
     host = {k: (v.pin_memory() if v is not None else None) for k, v in t.items()}
-    hout = torch.empty(out_shape, dtype=sets[0]["out"].dtype).pin_memory()
+    houts = [torch.empty(sh, dtype=sets[0]["out"].dtype).pin_memory() for sh in shapes]
     g = sets[0]
     h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
     e2e_steps = max(3, min(args.steps, 200))
@@ -477,7 +558,8 @@ def run_ours(args, w: dict, rank: int, world: int, local: int):
             if v is not None:
                 g[k].copy_(v, non_blocking=True)
         step(g)
-        hout.copy_(g["out"], non_blocking=True)
+        for ho, o in zip(houts, g["outs"]):
+            ho.copy_(o, non_blocking=True)
 
     for _ in range(3):
         e2e_step()
@@ -539,6 +621,8 @@ def main(argv=None):
     ap.add_argument("--variant", type=int, default=0, help="force 1 = tile kernel, 2 = small-M split-K kernel")
     ap.add_argument("--split-k", type=int, default=0, help="force the K split of the small-M kernel")
     ap.add_argument("--no-graph", action="store_true", help="time plain stream calls instead of graph replays")
+    ap.add_argument("--separate", action="store_true",
+                    help="multi workloads: one fl_norm_gemm call per weight instead of one fl_norm_gemm_multi call")
     ap.add_argument("--load-seconds", type=float, default=0.3,
                     help="untimed busy replays right before the timed region, sampled for the clock record")
     ap.add_argument("--no-weight-preload", action="store_true",

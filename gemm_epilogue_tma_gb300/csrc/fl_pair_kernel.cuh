@@ -91,11 +91,20 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     using Ops = DTypeOps<DT>;
     constexpr int S = C::STAGES;
     constexpr int EPI_WARP0 = PRO != PRO_NONE ? 8 : 4;
-    // LayerNorm with a single accumulator buffer: the epilogue warps, idle
-    // while a tile's MMAs run, fold the upper half (chunks 4-7) of every K
-    // block of that tile; the fold warps take chunks 0-3. (Splitting the
-    // cheaper RMS fold the same way was measured slower.)
-    constexpr bool FOLD2 = PRO == PRO_LN && C::NBUF == 1;
+    // Prologues with a single accumulator buffer: the epilogue warps, idle
+    // while a tile's MMAs run, take a share of the fold. SHARE_ALT: the fold
+    // warps fold whole rows of the even K blocks (by a running block index)
+    // and the epilogue warps those of the odd ones, so each warpgroup has two
+    // MMA steps for one fold; SHARE_SPLIT: the fold warps fold chunks 0-3 of
+    // every K block and the epilogue warps chunks 4-7.
+    constexpr int SHARE_NONE = 0, SHARE_SPLIT = 1, SHARE_ALT = 2;
+#ifndef FL_PAIR_SHARE
+#define FL_PAIR_SHARE 2
+#endif
+    constexpr int SHARE = (PRO != PRO_NONE && C::NBUF == 1) ? FL_PAIR_SHARE : SHARE_NONE;
+    constexpr bool FOLD2 = SHARE != SHARE_NONE;
+    static_assert(SHARE != SHARE_ALT || S % 2 == 0, "alternating folds need an even ring: a warpgroup's "
+                  "blocks k and k + S must share a stage's phase sequence");
     constexpr uint32_t IDESC = umma_idesc_f16(Ops::kFormat, 2 * kBM, C::BN);
 
     extern __shared__ uint8_t smem_raw[];
@@ -163,7 +172,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
             mbar_init(full_bar(s), 1);
             mbar_init(afull_bar(s), 1);
             mbar_init(empty_bar(s), 1);
-            mbar_init(xform_bar(s), FOLD2 ? 16 : 8);
+            mbar_init(xform_bar(s), SHARE == SHARE_SPLIT ? 16 : 8);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar(b), 1);
@@ -240,6 +249,11 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     // store, and with it the hand-off, then waits behind them). (fs, fph): ring
     // position, kept by the caller across tiles; ssum: RMS sum of squares of
     // the row over these chunks.
+    //
+    // SHARE_ALT (fold_share below): warpgroup wg folds whole rows of the K
+    // blocks whose running index g (counted over every block of every tile,
+    // the same in both warpgroups) has parity wg, and only advances its ring
+    // position over the others.
     auto fold_tile = [&](int tile, int rl, int j0, int& fs, uint32_t& fph, float& ssum, int site) -> bool {
         float rstd = 1.f, nmr = 0.f;
         if (PRO == PRO_LN) {
@@ -288,6 +302,56 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         }
         ssum = (ss[0] + ss[1]) + (ss[2] + ss[3]);
         return true;
+    };
+
+    auto fold_alt = [&](int tile, int rl, int wg, int& fs, uint32_t& fph, int& g, float& ssum, int site) -> bool {
+        float rstd = 1.f, nmr = 0.f;
+        if (PRO == PRO_LN) {
+            const int row = tile_mb(tile) * 2 * kBM + (int)rank * kBM + rl;
+            if (row < p.M) {
+                const float2 st = reinterpret_cast<const float2*>(p.ln_stats)[row];
+                rstd = st.y;
+                nmr = -st.x * st.y;
+            }
+        }
+        float ss[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ss[i] = 0.f;
+        const uint32_t a_cols = tmem_base + ((uint32_t)(rl & ~31) << 16) + (uint32_t)C::A_COL0;
+        const bool has_beta = p.beta != nullptr;
+        for (int kb = kb_begin; kb < kb_end; ++kb, ++g) {
+            if ((g & 1) == wg) {
+                if (!wait_bar(afull_bar(fs), fph, p.status, p.timeout_ns, site)) return false;
+                uint32_t o[32];
+                if (PRO == PRO_RMS) {
+                    fold_rms_row<DT>(stage_a(fs), gb_slot(fs), rl, ss, o);
+                } else if (PRO == PRO_ADD) {
+                    fold_add_row<DT>(stage_a(fs), gb_slot(fs), rl, o);
+                } else {
+                    uint32_t (&lo)[16] = *reinterpret_cast<uint32_t(*)[16]>(&o[0]);
+                    uint32_t (&hi)[16] = *reinterpret_cast<uint32_t(*)[16]>(&o[16]);
+                    fold_ln_row<DT, 4, 0>(stage_a(fs), gb_slot(fs), has_beta, rl, rstd, nmr, lo);
+                    fold_ln_row<DT, 4, 4>(stage_a(fs), gb_slot(fs), has_beta, rl, rstd, nmr, hi);
+                }
+                tmem_st_32x32b_x32(a_cols + 32u * (uint32_t)fs, o);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(lead(xform_bar(fs)));
+            }
+            if (++fs == S) {
+                fs = 0;
+                fph ^= 1u;
+            }
+        }
+        ssum = ((ss[0] + ss[1]) + (ss[2] + ss[3])) + ((ss[4] + ss[5]) + (ss[6] + ss[7]));
+        return true;
+    };
+
+    // This warpgroup's share of a tile's fold (wg 0: fold warps, 1: epilogue warps).
+    auto fold_share = [&](int tile, int rl, int wg, int& fs, uint32_t& fph, int& g, float& ssum, int site) -> bool {
+        if constexpr (SHARE == SHARE_ALT) return fold_alt(tile, rl, wg, fs, fph, g, ssum, site);
+        return fold_tile(tile, rl, 4 * wg, fs, fph, ssum, site);
     };
 
     if (warp == 0) {
@@ -397,11 +461,12 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         int s = 0;
         uint32_t ph = 0;
         int it = 0;
+        int g = 0;  // running K-block index (SHARE_ALT)
         bool ok = true;
         for (int tile = t_begin; ok && tile < t_end; tile += t_step, ++it) {
-            float ssum = 0.f;  // RMS: the row's sum of squares over the chunks folded here
+            float ssum = 0.f;  // RMS: the row's sum of squares over the blocks / chunks folded here
             if (FOLD2) {
-                ok = fold_tile(tile, t, 0, s, ph, ssum, 38);
+                ok = fold_share(tile, t, 0, s, ph, g, ssum, 38);
             } else {
                 float ss[8];
 #pragma unroll
@@ -483,11 +548,11 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         const T* bias = reinterpret_cast<const T*>(p.bias[osel.oi]);
         const T* res = reinterpret_cast<const T*>(p.residual);
         bool ok = true;
-        float ss_upper = 0.f;  // RMS, split fold: the row's sum of squares over chunks 4-7
+        float ss_upper = 0.f;  // RMS, shared fold: the row's sum of squares over this warpgroup's share
         if (FOLD2) {
-            int fs = 0;
+            int fs = 0, g = 0;
             uint32_t fph = 0;
-            ok = fold_tile(tile, rl, 4, fs, fph, ss_upper, 47);
+            ok = fold_share(tile, rl, 1, fs, fph, g, ss_upper, 47);
         }
         ok = ok && wait_bar(tfull_bar(0), 0, p.status, p.timeout_ns, 42);
         tc_fence_after();
@@ -636,7 +701,8 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         const uint32_t my_row_addr = ebuf + lane * 128;
         const int sw = lane & 7;
         int it = 0;
-        int fs = 0;  // ring position of the fold half (FOLD2)
+        int fs = 0;  // ring position and running K-block index of the fold share
+        int g = 0;
         uint32_t fph = 0;
         using T = uint16_t;
         const T* res = reinterpret_cast<const T*>(p.residual);
@@ -650,8 +716,8 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
             const int buf = C::NBUF == 2 ? (it & 1) : 0;
             const uint32_t tph = C::NBUF == 2 ? (uint32_t)((it >> 1) & 1) : (uint32_t)(it & 1);
             const uint32_t bias_s = stage_bias(n0, q, osel.oi);
-            float ss_upper = 0.f;  // RMS, split fold: the row's sum of squares over chunks 4-7
-            if (FOLD2 && !fold_tile(tile, q * 32 + lane, 4, fs, fph, ss_upper, 47)) break;
+            float ss_upper = 0.f;  // RMS, shared fold: the row's sum of squares over this warpgroup's share
+            if (FOLD2 && !fold_share(tile, q * 32 + lane, 1, fs, fph, g, ss_upper, 47)) break;
             if (!wait_bar(tfull_bar(buf), tph, p.status, p.timeout_ns, 40)) break;
             tc_fence_after();
             float rs = 1.f;

@@ -137,3 +137,30 @@ def dense_layer_inputs(M: int, N: int, K: int, dtype: str, seed=None) -> dict:
             "residual": _draw(rng, (M, N), 0.0, 1.0, dtype),
             "gamma": _draw(rng, (K,), 1.0, 0.1, dtype),
             "beta": _draw(rng, (K,), 0.0, 0.1, dtype)}
+
+
+def multi_inputs(M: int, Ns, K: int, norm: str, dtype: str, seed=None) -> dict:
+    """Inputs of one multi-consumer norm call: x[M,K], gamma[K], beta[K] (LayerNorm),
+    then W_i[N_i,K] and bias_i[N_i] per output (keys W0, bias0, W1, bias1, ...)."""
+    if seed is None:
+        seed = (41, DTYPE_IDS[dtype], M, K, *Ns)
+    rng = rng_for(*(seed if isinstance(seed, (tuple, list)) else (seed,)))
+    out = {"x": _draw(rng, (M, K), 0.0, 1.0, dtype)}
+    for i, N in enumerate(Ns):
+        out[f"W{i}"] = _draw(rng, (N, K), 0.0, 1.0 / math.sqrt(K), dtype)
+        out[f"bias{i}"] = _draw(rng, (N,), 0.0, 0.1, dtype)
+    out["gamma"] = _draw(rng, (K,), 1.0, 0.1, dtype)
+    out["beta"] = _draw(rng, (K,), 0.0, 0.1, dtype) if norm == "layer" else None
+    return out
+
+
+def input_bias_inputs(M: int, N: int, K: int, dtype: str, seed=None) -> dict:
+    """Inputs of one input-prologue call: A[M,K], bias_in[K] ~ N(0, 0.5), W[N,K], bias[N], residual[M,N]."""
+    if seed is None:
+        seed = (42, DTYPE_IDS[dtype], M, N, K)
+    rng = rng_for(*(seed if isinstance(seed, (tuple, list)) else (seed,)))
+    return {"A": _draw(rng, (M, K), 0.0, 1.0, dtype),
+            "W": _draw(rng, (N, K), 0.0, 1.0 / math.sqrt(K), dtype),
+            "bias_in": _draw(rng, (K,), 0.0, 0.5, dtype),
+            "bias": _draw(rng, (N,), 0.0, 0.1, dtype),
+            "residual": _draw(rng, (M, N), 0.0, 1.0, dtype)}

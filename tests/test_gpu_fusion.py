@@ -43,16 +43,10 @@ def dev(t):
     return None if t is None else t.cuda()
 
 
-def multi_inputs(M, Ns, K, norm, dt, seed=0):
+def multi_inputs(M, Ns, K, norm, dt):
     """x, gamma, beta and one (W, bias) per output, from one seeded generator."""
-    rng = syn.rng_for(41, seed, syn.DTYPE_IDS[dt], M, K, *Ns)
-    draw = lambda shape, mean, std: syn._draw(rng, shape, mean, std, dt)
-    x = draw((M, K), 0.0, 1.0)
-    Ws = [draw((N, K), 0.0, 1.0 / np.sqrt(K)) for N in Ns]
-    biases = [draw((N,), 0.0, 0.1) for N in Ns]
-    gamma = draw((K,), 1.0, 0.1)
-    beta = draw((K,), 0.0, 0.1) if norm == "layer" else None
-    return x, gamma, beta, Ws, biases
+    t = syn.multi_inputs(M, Ns, K, norm, dt)
+    return t["x"], t["gamma"], t["beta"], [t[f"W{i}"] for i in range(len(Ns))], [t[f"bias{i}"] for i in range(len(Ns))]
 
 
 def run_multi(M, Ns, K, norm, dt, acts=None, with_bias=True, rows=None, opts=None):
@@ -124,10 +118,8 @@ def test_multi_output_and_single_call_agree():
 # input-bias prologue
 # ---------------------------------------------------------------------------
 def run_input_bias(M, N, K, dt, act, with_bias, with_res, opts=None, seed=0, rows=None):
-    rng = syn.rng_for(42, seed, syn.DTYPE_IDS[dt], M, N, K)
-    draw = lambda shape, mean, std: syn._draw(rng, shape, mean, std, dt)
-    A, W = draw((M, K), 0.0, 1.0), draw((N, K), 0.0, 1.0 / np.sqrt(K))
-    bi, b, r = draw((K,), 0.0, 0.5), draw((N,), 0.0, 0.1), draw((M, N), 0.0, 1.0)
+    t = syn.input_bias_inputs(M, N, K, dt, seed=(42, seed, syn.DTYPE_IDS[dt], M, N, K))
+    A, W, bi, b, r = t["A"], t["W"], t["bias_in"], t["bias"], t["residual"]
     for k, v in (opts or {}).items():
         fl.set_option(k, v)
     try:
