@@ -70,6 +70,9 @@ def parse_workload(name: str) -> dict:
     if parts[0] == "rmsnorm":
         _, dt, M, K = parts
         return dict(kind="rmsnorm", dtype=dt, M=int(M), K=int(K), eps=1e-6, name=name)
+    if parts[0] == "layer":
+        _, dt, M, D, Dkv, F = parts
+        return dict(kind="layer", dtype=dt, M=int(M), D=int(D), Dkv=int(Dkv), F=int(F), eps=1e-6, name=name)
     if parts[0] == "pattern":
         _, pat, dt, M, N, K = parts
         return dict(kind="pattern", pattern=pat, dtype=dt, M=int(M), N=int(N), K=int(K), name=name)
@@ -98,6 +101,9 @@ def describe(w: dict) -> str:
                 f"W[{w['N']},{w['K']}]^T + bias)")
     if w["kind"] == "rmsnorm":
         return f"standalone rmsnorm {w['dtype']}: x[{w['M']},{w['K']}] gamma[{w['K']}] eps={w['eps']:g}"
+    if w["kind"] == "layer":
+        return (f"decoder layer dense part {w['dtype']}: M={w['M']} D={w['D']} Dkv={w['Dkv']} F={w['F']} "
+                f"(RMSNorm+QKV, attention output projection + residual, RMSNorm+SwiGLU FFN + residual)")
     return (f"swiglu_ffn {w['dtype']}: x[{w['M']},{w['D']}] RMSNorm, Wg/Wu[{w['F']},{w['D']}], "
             f"Wd[{w['D']},{w['F']}], + x")
 
@@ -127,6 +133,8 @@ def launches_of(w, separate=False) -> int:
     multi-consumer step is one launch (or one call per weight with --separate)."""
     if w["kind"] == "swiglu":
         return 2
+    if w["kind"] == "layer":
+        return 4  # QKV, output projection, gate/up, down
     if w["kind"] == "multi":
         calls = len(w["Ns"]) if separate else 1
         return calls * (2 if w["norm"] == "layer" else 1)
@@ -146,6 +154,11 @@ def flops_per_step(w: dict) -> float:
         return sum(2.0 * M * N * K + M * N for N in w["Ns"]) + 3 * M * K
     if w["kind"] == "rmsnorm":
         return 4.0 * w["M"] * w["K"]  # square-accumulate (2), scale by 1/rms and by gamma (2)
+    if w["kind"] == "layer":
+        M, D, Dkv, F = w["M"], w["D"], w["Dkv"], w["F"]
+        return (2.0 * M * D * (D + 2 * Dkv) + 3 * M * D + M * (D + 2 * Dkv)  # RMSNorm + QKV
+                + 2.0 * M * D * D + 2 * M * D                                 # output projection, bias, residual
+                + 6.0 * M * D * F + 3 * M * D + 2 * M * F + 4 * M * F + M * F + M * D)  # FFN
     M, N, K = w["M"], w["N"], w["K"]
     f = 2.0 * M * N * K
     if w["kind"] == "biasin":
@@ -169,6 +182,11 @@ def bytes_per_step(w: dict) -> float:
         return e * (M * K + K * (2 if w["norm"] == "layer" else 1) + sum(N * K + M * N for N in w["Ns"]))
     if w["kind"] == "rmsnorm":
         return e * (2 * w["M"] * w["K"] + w["K"])
+    if w["kind"] == "layer":
+        M, D, Dkv, F = w["M"], w["D"], w["Dkv"], w["F"]
+        weights = D * (D + 2 * Dkv) + D * D + 3 * D * F + 2 * D
+        acts = M * D + M * (D + 2 * Dkv) + M * D + M * D + 2 * M * F + M * D  # x, q/k/v, attn, h, h_ffn w+r, out
+        return e * (weights + acts)
     M, N, K = w["M"], w["N"], w["K"]
     b = e * (M * K + N * K + M * N)
     if w["kind"] == "biasin":
@@ -197,6 +215,8 @@ def make_inputs(w: dict):
     if w["kind"] == "rmsnorm":
         t = syn.norm_gemm_inputs(w["M"], 8, w["K"], "rms", w["dtype"])
         return {"x": t["x"], "gamma": t["gamma"]}
+    if w["kind"] == "layer":
+        return syn.layer_inputs(w["M"], w["D"], w["Dkv"], w["F"], w["dtype"])
     return syn.swiglu_inputs(w["M"], w["D"], w["F"], w["dtype"])
 
 
@@ -208,7 +228,18 @@ def out_shapes(w: dict):
         return [(w["M"], w["D"])]
     if w["kind"] == "rmsnorm":
         return [(w["M"], w["K"])]
+    if w["kind"] == "layer":  # out, then q, k, v, h
+        M, D, Dkv = w["M"], w["D"], w["Dkv"]
+        return [(M, D), (M, D), (M, Dkv), (M, Dkv), (M, D)]
     return [(w["M"], w["N"])]
+
+
+def e2e_input_keys(w: dict, t: dict):
+    """Inputs copied host to device each end-to-end step: a decoder layer's
+    activations (its weights stay resident), else every input."""
+    if w["kind"] == "layer":
+        return ["x", "attn"]
+    return [k for k, v in t.items() if v is not None]
 
 
 # ---------------------------------------------------------------------------
@@ -367,6 +398,11 @@ def oracle_step(w: dict, f64: dict, row0: int, rows: int):
         return oracle.input_bias_gemm(f64["A"][sl], f64["bias_in"], f64["W"], f64["bias"], None, w["act"])
     if w["kind"] == "rmsnorm":
         return oracle.rms_norm(f64["x"][sl], f64["gamma"], w["eps"])
+    if w["kind"] == "layer":
+        x, a = f64["x"][sl], f64["attn"][sl]
+        qkv = [oracle.norm_gemm(x, f64["gamma_attn"], None, f64[W], None, w["eps"], "rms") for W in ("Wq", "Wk", "Wv")]
+        h = oracle.linear(a, f64["Wo"]) + x
+        return qkv, oracle.swiglu_ffn(h, f64["gamma_ffn"], f64["Wg"], f64["Wu"], f64["Wd"], None, w["eps"], w["dtype"])
     return oracle.swiglu_ffn(f64["x"][sl], f64["gamma"], f64["Wg"], f64["Wu"], f64["Wd"], None, w["eps"], w["dtype"])
 
 
@@ -447,12 +483,18 @@ def run_ours(args, w: dict, rank: int, world: int, local: int):
     set_bytes = sum(v.numel() * v.element_size() for v in t.values() if v is not None)
     shapes = out_shapes(w)
     out_bytes = sum(a * b * 2 for a, b in shapes)
-    nsets = max(2, int(3 * L2_BYTES // (set_bytes + out_bytes)) + 1)
+    # enough input copies to exceed the L2 three times over between reuses
+    # (capped for tiny workloads, whose copies then stay in L2: said in config)
+    nsets = min(256, max(2, int(3 * L2_BYTES // (set_bytes + out_bytes)) + 1))
     sets = []
     for _ in range(nsets):
         g = {k: (v.to(dev) if v is not None else None) for k, v in t.items()}
         g["outs"] = [torch.empty(sh, dtype=t[next(iter(t))].dtype, device=dev) for sh in shapes]
         g["out"] = g["outs"][0]
+        if w["kind"] == "layer":
+            o = g["outs"]
+            g["layer"] = fl.DecoderLayer(eps=w["eps"], out=o[0], q=o[1], k=o[2], v=o[3], h=o[4], bias_o=None,
+                                         **{k: v for k, v in g.items() if k not in ("outs", "out")})
         if w["kind"] == "swiglu":
             g["ws"] = torch.empty(fl.swiglu_ffn_workspace_size(w["M"], w["F"], w["dtype"]), dtype=torch.uint8,
                                   device=dev)
@@ -461,7 +503,13 @@ def run_ours(args, w: dict, rank: int, world: int, local: int):
     n_out = len(shapes)
 
     def step(g, stream=None):
-        if w["kind"] == "multi" and args.separate:
+        if w["kind"] == "layer":
+            for half in (0, 1):
+                if args.separate:
+                    g["layer"].issue(half, stream=stream)
+                else:
+                    g["layer"].launch(half, stream=stream)
+        elif w["kind"] == "multi" and args.separate:
             for i in range(n_out):
                 fl.norm_gemm(g["x"], g["gamma"], g[f"W{i}"], beta=g.get("beta"), out=g["outs"][i], eps=w["eps"],
                              norm=w["norm"], stream=stream)
@@ -547,7 +595,7 @@ def run_ours(args, w: dict, rank: int, world: int, local: int):
         sampler.stop()
 
     # end to end through the same call: pinned host inputs in, result back to pinned host
-    host = {k: (v.pin_memory() if v is not None else None) for k, v in t.items()}
+    host = {k: t[k].pin_memory() for k in e2e_input_keys(w, t)}
     houts = [torch.empty(sh, dtype=sets[0]["out"].dtype).pin_memory() for sh in shapes]
     g = sets[0]
     h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
@@ -591,9 +639,12 @@ def run_ours(args, w: dict, rank: int, world: int, local: int):
         "vs_baseline": vs, "dtype": w["dtype"], "data": "synthetic",
         "config": {"workload": describe(w), "name": w["name"],
                    "l2": f"inputs rotate over {nsets} copies ({nsets * (set_bytes + out_bytes) / 2**20:.0f} MiB "
-                         f"> 129 MB L2)",
+                         + ("> 129 MB L2)" if nsets * (set_bytes + out_bytes) > L2_BYTES else
+                            "< 129 MB L2: the operands are L2-resident)"),
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "launch": "stream calls" if args.no_graph else f"CUDA graphs of {nsets} library calls, replayed",
+                   "launch": ("two fl_layer graph launches per step" if w["kind"] == "layer" and not args.separate
+                              else "stream calls" if args.no_graph
+                              else f"CUDA graphs of {nsets} library calls, replayed"),
                    "weights": "read-only; " + ("read after the previous step" if args.no_weight_preload else
                                                "first tiles staged before the programmatic dependency resolves"),
                    "vs_baseline_ref": "A30 fused RMSNorm->Linear 0.208 ms (LLMBoost page), other hardware"},
@@ -631,6 +682,10 @@ def main(argv=None):
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")
     w = parse_workload(args.workload)
+    if w["kind"] == "layer":
+        # the layer is its own pair of CUDA graphs (or, with --separate, the
+        # same library calls issued directly): timed as stream calls
+        args.no_graph = True
     rank, world, local = dist_setup()
     if world > 1:
         import torch.distributed as dist

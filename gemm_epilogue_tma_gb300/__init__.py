@@ -31,6 +31,14 @@ STATUS_NAMES = {0: "FL_OK", 1: "FL_ERR_INVALID_ARG", 2: "FL_ERR_UNSUPPORTED", 3:
                 4: "FL_ERR_WORKSPACE", 5: "FL_ERR_CUDA", 6: "FL_ERR_TIMEOUT"}
 OPTIONS = {"tile_n": 0, "variant": 1, "timeout_ms": 2, "split_k": 3, "pdl": 4, "weight_preload": 5}
 
+class LayerDesc(ctypes.Structure):
+    """fl_layer_desc: sizes, dtype, eps and the device pointers of one decoder layer's dense part."""
+    _fields_ = [("dtype", ctypes.c_int), ("M", ctypes.c_int), ("D", ctypes.c_int), ("Dkv", ctypes.c_int),
+                ("F", ctypes.c_int), ("eps", ctypes.c_float)] + [
+        (name, ctypes.c_void_p) for name in ("x", "gamma_attn", "Wq", "Wk", "Wv", "q", "k", "v", "attn", "Wo",
+                                             "bias_o", "h", "gamma_ffn", "Wg", "Wu", "Wd", "out")]
+
+
 # C ABI: name -> (restype, argtypes)
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 SIGNATURES = {
@@ -42,6 +50,10 @@ SIGNATURES = {
     "fl_norm_gemm_multi": (_i, [_vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _i, _i, _f, _i, _i, _vp]),
     "fl_input_bias_gemm": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
     "fl_rms_norm": (_i, [_vp, _vp, _vp, _i, _i, _f, _i, _vp]),
+    "fl_layer_create": (_i, [ctypes.POINTER(LayerDesc), ctypes.POINTER(_vp)]),
+    "fl_layer_launch": (_i, [_vp, _i, _vp]),
+    "fl_layer_issue": (_i, [_vp, _i, _vp]),
+    "fl_layer_destroy": (None, [_vp]),
     "fl_last_error": (ctypes.c_char_p, []),
     "fl_device_status": (_i, [_vp]),
     "fl_set_option": (_i, [_i, _i]),
@@ -209,6 +221,50 @@ def rms_norm(x, gamma, out=None, eps=1e-6, stream=None):
     _check_tensors(x.dtype, x=x, gamma=gamma, out=out)
     _check(lib().fl_rms_norm(_ptr(x), _ptr(gamma), _ptr(out), M, K, float(eps), _dtype_code(x), _stream(stream)))
     return out
+
+
+class DecoderLayer:
+    """The dense part of a decoder layer captured into two CUDA graphs (fl_layer_*).
+
+    half 0: q, k, v = RMSNorm(x) [Wq; Wk; Wv]^T; the caller's attention then
+    writes attn; half 1: h = attn Wo^T (+ bias_o) + x, out = SwiGLU_FFN(h) + h.
+    Every tensor is fixed for the life of the layer (the graphs hold their
+    addresses): write new inputs into x and attn in place.
+    """
+
+    NAMES = ("x", "gamma_attn", "Wq", "Wk", "Wv", "q", "k", "v", "attn", "Wo", "bias_o", "h", "gamma_ffn", "Wg",
+             "Wu", "Wd", "out")
+
+    def __init__(self, eps=1e-6, **tensors):
+        x = tensors["x"]
+        M, D = x.shape
+        F = tensors["Wg"].shape[0]
+        Dkv = tensors["Wk"].shape[0]
+        _check_tensors(x.dtype, **tensors)
+        self.tensors = tensors  # keep every buffer alive while the graphs exist
+        desc = LayerDesc(dtype=_dtype_code(x), M=M, D=D, Dkv=Dkv, F=F, eps=float(eps),
+                         **{n: (tensors[n].data_ptr() if tensors.get(n) is not None else None) for n in self.NAMES})
+        h = ctypes.c_void_p()
+        _check(lib().fl_layer_create(ctypes.byref(desc), ctypes.byref(h)))
+        self._h = h
+
+    def launch(self, half: int, stream=None) -> None:
+        _check(lib().fl_layer_launch(self._h, int(half), _stream(stream)))
+
+    def issue(self, half: int, stream=None) -> None:
+        """The same half as ordinary library calls (no graph)."""
+        _check(lib().fl_layer_issue(self._h, int(half), _stream(stream)))
+
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            lib().fl_layer_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def swiglu_ffn_workspace_size(M: int, F: int, dtype) -> int:

@@ -11,7 +11,9 @@
 namespace fl {
 
 // Phase timestamps for timing studies: compiled in with -DFL_TRACE only;
-// slot s of CTA b goes to trace[b * 16 + s]. SM clock cycles, or global
+// slot s of CTA b goes to trace[b * FL_TRACE_SLOTS + s] (16 phase slots; 64
+// with -DFL_TRACE_STEPS, whose slots 16-63 time eight K steps of the main
+// loop: producer issue, fold hand-off, MMA waits). SM clock cycles, or global
 // nanoseconds (comparable across SMs and launches) with -DFL_TRACE_GLOBALTIMER.
 #ifdef FL_TRACE
 #ifdef FL_TRACE_GLOBALTIMER
@@ -19,13 +21,30 @@ namespace fl {
 #else
 #define FL_TRACE_NOW() clock64()
 #endif
+#ifdef FL_TRACE_STEPS
+#define FL_TRACE_SLOTS 64
+#else
+#define FL_TRACE_SLOTS 16
+#endif
 #define FL_MARK(p, slot)                                                                   \
     do {                                                                                   \
-        if ((p).trace != nullptr) (p).trace[blockIdx.x * 16 + (slot)] = (unsigned long long)FL_TRACE_NOW(); \
+        if ((p).trace != nullptr)                                                          \
+            (p).trace[blockIdx.x * FL_TRACE_SLOTS + (slot)] = (unsigned long long)FL_TRACE_NOW(); \
     } while (0)
 #else
 #define FL_MARK(p, slot) \
     do {                 \
+    } while (0)
+#endif
+// Per-step marks: K step j (8 <= j < 16 of a CTA's first tile) into slot base + j - 8.
+#ifdef FL_TRACE_STEPS
+#define FL_MARK_STEP(p, base, j)                                  \
+    do {                                                          \
+        if ((j) >= 8 && (j) < 16) FL_MARK(p, (base) + (j) - 8);   \
+    } while (0)
+#else
+#define FL_MARK_STEP(p, base, j) \
+    do {                         \
     } while (0)
 #endif
 

@@ -793,7 +793,8 @@ fl_status fl_rms_norm(const void* x, const void* gamma, void* out, int M, int K,
     if (overlap(out, xb, gamma, (size_t)K * 2)) return fail(FL_ERR_INVALID_ARG, "out overlaps gamma");
     DeviceInfo* di = nullptr;
     if ((st = device_info(&di)) != FL_OK) return st;
-    cudaError_t e = fl::launch_rms_norm(dtype, x, gamma, out, M, K, eps, g_opt_pdl.load(), static_cast<cudaStream_t>(stream));
+    cudaError_t e = fl::launch_rms_norm(dtype, x, gamma, out, M, K, eps, g_opt_pdl.load(), di->sms,
+                                          static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(FL_ERR_CUDA, "RMSNorm kernel launch failed: %s", cudaGetErrorString(e));
     return ok();
 }

@@ -80,7 +80,7 @@ cudaError_t launch_ln_stats(int dt, const void* x, int M, int K, float eps, void
 
 // Standalone RMSNorm y = x * gamma / sqrt(mean(x^2) + eps) of x [M, K].
 cudaError_t launch_rms_norm(int dt, const void* x, const void* gamma, void* y, int M, int K, float eps, int pdl,
-                            cudaStream_t stream);
+                            int sms, cudaStream_t stream);
 
 // Kernel launchers, explicitly instantiated in the kernel translation units.
 template <int DT, int BN, int PRO, bool DUAL>

@@ -1,0 +1,180 @@
+// The dense part of a decoder layer, captured once into CUDA graphs and then
+// launched as two graph launches per step.
+//
+// A transformer decoder step issues a handful of short kernels per layer; at
+// decode sizes (a few tokens, D = 1024 .. 4096) each takes a few
+// microseconds, so the host launch path and the gaps between launches are a
+// large share of the step. Capturing the layer's library calls into a graph
+// once (the "Fusion Compiler" glossary's interaction with CUDA Graph capture)
+// removes both: the graph is replayed with one launch per half, and the
+// kernels inside keep their programmatic dependencies on one another.
+//
+// The layer is split where the attention core sits, which this library does
+// not compute:
+//   half 0: q, k, v = RMSNorm(x; gamma_attn) [Wq; Wk; Wv]^T   (one fused launch)
+//   -- the caller's attention writes attn [M, D] --
+//   half 1: h   = attn Wo^T (+ bias_o) + x
+//           out = SwiGLU_FFN(h; gamma_ffn, Wg, Wu, Wd) + h      (RMSNorm fused)
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "../../include/fusedlin.h"
+#include "fl_internal.h"
+
+struct fl_layer {
+    fl_layer_desc d;
+    cudaStream_t capture = nullptr;
+    cudaGraph_t graph[2] = {nullptr, nullptr};
+    cudaGraphExec_t exec[2] = {nullptr, nullptr};
+    void* ffn_workspace = nullptr;  // the FFN's hidden activation [M, F]
+    size_t ffn_bytes = 0;
+    void* zero_bias = nullptr;      // [D] zeros when the output projection has no bias
+};
+
+namespace {
+
+fl_status err(fl_status s, const char* msg) { return (fl_status)fl::set_last_error(s, msg); }
+
+fl_status cuda_err(cudaError_t e, const char* what) {
+    char msg[256];
+    snprintf(msg, sizeof(msg), "fl_layer: %s: %s", what, cudaGetErrorString(e));
+    return err(FL_ERR_CUDA, msg);
+}
+
+void release(fl_layer* L) {
+    for (int i = 0; i < 2; ++i) {
+        if (L->exec[i] != nullptr) cudaGraphExecDestroy(L->exec[i]);
+        if (L->graph[i] != nullptr) cudaGraphDestroy(L->graph[i]);
+    }
+    if (L->capture != nullptr) cudaStreamDestroy(L->capture);
+    if (L->ffn_workspace != nullptr) cudaFree(L->ffn_workspace);
+    if (L->zero_bias != nullptr) cudaFree(L->zero_bias);
+    delete L;
+}
+
+// The library calls of one half, issued on `s`.
+fl_status issue_half(const fl_layer* L, int half, cudaStream_t s) {
+    const fl_layer_desc& d = L->d;
+    if (half == 0) {
+        const void* W[3] = {d.Wq, d.Wk, d.Wv};
+        void* out[3] = {d.q, d.k, d.v};
+        const int N[3] = {d.D, d.Dkv, d.Dkv};
+        return fl_norm_gemm_multi(d.x, d.gamma_attn, nullptr, 3, W, nullptr, out, N, nullptr, d.M, d.D, d.eps,
+                                  FL_NORM_RMS, d.dtype, s);
+    }
+    const void* bo = d.bias_o != nullptr ? d.bias_o : L->zero_bias;
+    fl_status st = fl_gemm_epilogue(d.attn, d.Wo, bo, d.x, d.h, d.M, d.D, d.D, FL_GEMM_BIAS_RESIDUAL, d.dtype, s);
+    if (st != FL_OK) return st;
+    return fl_swiglu_ffn(d.h, d.gamma_ffn, d.Wg, d.Wu, d.Wd, nullptr, d.out, d.M, d.D, d.F, d.eps, L->ffn_workspace,
+                         L->ffn_bytes, d.dtype, s);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" fl_status fl_layer_create(const fl_layer_desc* desc, fl_layer** layer) {
+    if (layer == nullptr) return err(FL_ERR_INVALID_ARG, "fl_layer_create: null layer handle");
+    *layer = nullptr;
+    if (desc == nullptr) return err(FL_ERR_INVALID_ARG, "fl_layer_create: null description");
+    const fl_layer_desc& d = *desc;
+    if (d.dtype != FL_F16 && d.dtype != FL_BF16) return err(FL_ERR_INVALID_ARG, "fl_layer_create: bad dtype");
+    if (d.M < 1 || d.D < 1 || d.Dkv < 1 || d.F < 1) return err(FL_ERR_INVALID_ARG, "fl_layer_create: sizes must be positive");
+    if (d.D % 8 || d.Dkv % 8 || d.F % 8) return err(FL_ERR_ALIGNMENT, "fl_layer_create: D, Dkv and F must be multiples of 8");
+    if (!(d.eps >= 0.0f) || d.eps > 1e30f) return err(FL_ERR_INVALID_ARG, "fl_layer_create: eps must be finite and >= 0");
+    const void* req[] = {d.x, d.gamma_attn, d.Wq, d.Wk, d.Wv, d.q, d.k, d.v, d.attn, d.Wo, d.h, d.gamma_ffn, d.Wg,
+                         d.Wu, d.Wd, d.out};
+    for (const void* p : req) {
+        if (p == nullptr) return err(FL_ERR_INVALID_ARG, "fl_layer_create: a required pointer is null");
+        if (!aligned16(p)) return err(FL_ERR_ALIGNMENT, "fl_layer_create: pointers must be 16-byte aligned");
+    }
+    if (d.bias_o != nullptr && !aligned16(d.bias_o)) return err(FL_ERR_ALIGNMENT, "fl_layer_create: bias_o alignment");
+    if (d.h == d.x || d.out == d.h) return err(FL_ERR_INVALID_ARG, "fl_layer_create: h must differ from x and out");
+
+    fl_layer* L = new (std::nothrow) fl_layer();
+    if (L == nullptr) return err(FL_ERR_INVALID_ARG, "fl_layer_create: out of host memory");
+    L->d = d;
+    cudaError_t e;
+    L->ffn_bytes = fl_swiglu_ffn_workspace_size(d.M, d.F, d.dtype);
+    if ((e = cudaMalloc(&L->ffn_workspace, L->ffn_bytes)) != cudaSuccess) {
+        release(L);
+        return cuda_err(e, "FFN workspace");
+    }
+    if (d.bias_o == nullptr) {
+        if ((e = cudaMalloc(&L->zero_bias, (size_t)d.D * 2)) != cudaSuccess ||
+            (e = cudaMemset(L->zero_bias, 0, (size_t)d.D * 2)) != cudaSuccess) {
+            release(L);
+            return cuda_err(e, "zero bias");
+        }
+    }
+    if ((e = cudaStreamCreateWithFlags(&L->capture, cudaStreamNonBlocking)) != cudaSuccess) {
+        release(L);
+        return cuda_err(e, "capture stream");
+    }
+    // One uncaptured pass first: it validates every call and does the one-time
+    // set-up (device query, kernel attributes, occupancy queries, module
+    // loading) outside the capture, where those calls are allowed.
+    for (int half = 0; half < 2; ++half) {
+        const fl_status st = issue_half(L, half, L->capture);
+        if (st != FL_OK) {
+            char msg[512];
+            snprintf(msg, sizeof(msg), "fl_layer_create (half %d): %s", half, fl_last_error());
+            release(L);
+            return err(st, msg);
+        }
+    }
+    if ((e = cudaStreamSynchronize(L->capture)) != cudaSuccess) {
+        release(L);
+        return cuda_err(e, "set-up pass");
+    }
+    for (int half = 0; half < 2; ++half) {
+        if ((e = cudaStreamBeginCapture(L->capture, cudaStreamCaptureModeThreadLocal)) != cudaSuccess) {
+            release(L);
+            return cuda_err(e, "begin capture");
+        }
+        const fl_status st = issue_half(L, half, L->capture);
+        cudaGraph_t g = nullptr;
+        e = cudaStreamEndCapture(L->capture, &g);
+        L->graph[half] = g;
+        if (st != FL_OK) {
+            // keep the library call's own message
+            char msg[512];
+            snprintf(msg, sizeof(msg), "fl_layer_create (half %d): %s", half, fl_last_error());
+            release(L);
+            return err(st, msg);
+        }
+        if (e != cudaSuccess) {
+            release(L);
+            return cuda_err(e, "end capture");
+        }
+        if ((e = cudaGraphInstantiate(&L->exec[half], g, 0)) != cudaSuccess) {
+            release(L);
+            return cuda_err(e, "graph instantiate");
+        }
+    }
+    *layer = L;
+    fl::set_last_error(FL_OK, "");
+    return FL_OK;
+}
+
+extern "C" fl_status fl_layer_launch(fl_layer* layer, int half, void* stream) {
+    if (layer == nullptr) return err(FL_ERR_INVALID_ARG, "fl_layer_launch: null layer");
+    if (half < 0 || half > 1) return err(FL_ERR_INVALID_ARG, "fl_layer_launch: half must be 0 or 1");
+    const cudaError_t e = cudaGraphLaunch(layer->exec[half], static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_err(e, "graph launch");
+    fl::set_last_error(FL_OK, "");
+    return FL_OK;
+}
+
+extern "C" fl_status fl_layer_issue(const fl_layer* layer, int half, void* stream) {
+    if (layer == nullptr) return err(FL_ERR_INVALID_ARG, "fl_layer_issue: null layer");
+    if (half < 0 || half > 1) return err(FL_ERR_INVALID_ARG, "fl_layer_issue: half must be 0 or 1");
+    return issue_half(layer, half, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" void fl_layer_destroy(fl_layer* layer) {
+    if (layer != nullptr) release(layer);
+}

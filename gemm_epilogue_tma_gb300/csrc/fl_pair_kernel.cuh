@@ -322,6 +322,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         for (int kb = kb_begin; kb < kb_end; ++kb, ++g) {
             if ((g & 1) == wg) {
                 if (!wait_bar(afull_bar(fs), fph, p.status, p.timeout_ns, site)) return false;
+                if (rl == 0 && tile == t_begin) FL_MARK_STEP(p, 24, kb - kb_begin);
                 uint32_t o[32];
                 if (PRO == PRO_RMS) {
                     fold_rms_row<DT>(stage_a(fs), gb_slot(fs), rl, ss, o);
@@ -338,6 +339,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(lead(xform_bar(fs)));
+                if (rl == 0 && tile == t_begin) FL_MARK_STEP(p, 32, kb - kb_begin);
             }
             if (++fs == S) {
                 fs = 0;
@@ -374,6 +376,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                         ok = false;
                         break;
                     }
+                    if (tile == t_begin) FL_MARK_STEP(p, 16, kb - kb_begin);
                     if (PRO == PRO_NONE) {
                         if (leader) mbar_arrive_expect_tx(full_bar(s), 2u * C::STAGE_BYTES);
                         const uint32_t fb = lead(full_bar(s));
@@ -420,14 +423,17 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(buf * C::ACC_COLS);
                 for (int kb = kb_begin; kb < kb_end; ++kb) {
+                    if (it == 0) FL_MARK_STEP(p, 40, kb - kb_begin);
                     if (!wait_bar_cluster(full_bar(s), ph, p.status, p.timeout_ns, 35)) {
                         ok = false;
                         break;
                     }
+                    if (it == 0) FL_MARK_STEP(p, 48, kb - kb_begin);
                     if (PRO != PRO_NONE && !wait_bar_cluster(xform_bar(s), ph, p.status, p.timeout_ns, 36)) {
                         ok = false;
                         break;
                     }
+                    if (it == 0) FL_MARK_STEP(p, 56, kb - kb_begin);
                     tc_fence_after();
                     if (kb == kb_begin && it == 0) FL_MARK(p, 3);
                     const uint64_t da = sw128_kmajor_desc(stage_a(s));
@@ -485,6 +491,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                         ok = false;
                         break;
                     }
+                    if (t == 0 && it == 0) FL_MARK_STEP(p, 24, kb - kb_begin);
                     uint32_t o[32];
                     if (PRO == PRO_RMS) {
                         fold_rms_row<DT>(stage_a(s), gb_slot(s), t, ss, o);
@@ -502,6 +509,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive_cluster(lead(xform_bar(s)));
+                    if (t == 0 && it == 0) FL_MARK_STEP(p, 32, kb - kb_begin);
                     if (++s == S) {
                         s = 0;
                         ph ^= 1u;

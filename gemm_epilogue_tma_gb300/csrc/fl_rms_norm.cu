@@ -4,7 +4,8 @@
 // written after the generated RMSNorm kernel of the "hackable compiler" post
 // (sum of squares, times 1/K, plus eps, rsqrt, times x, times the weight).
 //
-// Bound by HBM: x is read once and y written once. One warp per row; every
+// Bound by HBM: x is read once and y written once. One warp per row (rows
+// grid-stride over at most two CTAs per SM, so no partial last wave); every
 // lane moves 16-byte vectors at a 512-byte stride (coalesced across the
 // warp). Rows of up to 4096 elements stay in registers between the sum of
 // squares and the scaling (16 vectors per lane, all issued before the first
@@ -53,14 +54,27 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// One row per warp, rows taken grid-stride by a grid of at most two waves'
+// worth of CTAs.
+template <int DT>
+__device__ __forceinline__ void rms_norm_row(const uint16_t* x, const uint16_t* __restrict__ gamma, uint16_t* y,
+                                             int row, int K, float eps, int lane);
+
 template <int DT>
 __global__ void __launch_bounds__(256) fl_rms_norm_kernel(const uint16_t* x, const uint16_t* __restrict__ gamma,
                                                           uint16_t* y, int M, int K, float eps) {
     griddep_wait();  // x may come from the previous kernel on the stream
-    griddep_launch_dependents();
     const int lane = threadIdx.x & 31;
-    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (row >= M) return;
+    for (int row = blockIdx.x * 8 + (threadIdx.x >> 5); row < M; row += gridDim.x * 8)
+        rms_norm_row<DT>(x, gamma, y, row, K, eps, lane);
+    // The next kernel is let in only once this CTA's rows are done: letting
+    // it in earlier would park its CTAs on SM slots this grid still needs.
+    griddep_launch_dependents();
+}
+
+template <int DT>
+__device__ __forceinline__ void rms_norm_row(const uint16_t* x, const uint16_t* __restrict__ gamma, uint16_t* y,
+                                             int row, int K, float eps, int lane) {
     const uint16_t* xr = x + (size_t)row * K;
     uint16_t* yr = y + (size_t)row * K;
     float s0 = 0.f, s1 = 0.f;
@@ -100,9 +114,10 @@ __global__ void __launch_bounds__(256) fl_rms_norm_kernel(const uint16_t* x, con
 }  // namespace
 
 cudaError_t launch_rms_norm(int dt, const void* x, const void* gamma, void* y, int M, int K, float eps, int pdl,
-                            cudaStream_t stream) {
+                            int sms, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((M + 7) / 8), 1, 1);
+    const int ctas = (M + 7) / 8;
+    cfg.gridDim = dim3((unsigned)(ctas < 2 * sms ? ctas : 2 * sms), 1, 1);
     cfg.blockDim = dim3(256, 1, 1);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

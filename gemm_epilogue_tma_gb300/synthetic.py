@@ -164,3 +164,19 @@ def input_bias_inputs(M: int, N: int, K: int, dtype: str, seed=None) -> dict:
             "bias_in": _draw(rng, (K,), 0.0, 0.5, dtype),
             "bias": _draw(rng, (N,), 0.0, 0.1, dtype),
             "residual": _draw(rng, (M, N), 0.0, 1.0, dtype)}
+
+
+def layer_inputs(M: int, D: int, Dkv: int, F: int, dtype: str, seed=None) -> dict:
+    """Inputs of one decoder layer's dense part: x[M,D], gamma_attn[D], Wq[D,D],
+    Wk/Wv[Dkv,D], attn[M,D] (stands in for the attention output), Wo[D,D],
+    gamma_ffn[D], Wg/Wu[F,D], Wd[D,F]."""
+    if seed is None:
+        seed = (43, DTYPE_IDS[dtype], M, D, Dkv, F)
+    rng = rng_for(*(seed if isinstance(seed, (tuple, list)) else (seed,)))
+    s = 1.0 / math.sqrt(D)
+    return {"x": _draw(rng, (M, D), 0.0, 1.0, dtype), "gamma_attn": _draw(rng, (D,), 1.0, 0.1, dtype),
+            "Wq": _draw(rng, (D, D), 0.0, s, dtype), "Wk": _draw(rng, (Dkv, D), 0.0, s, dtype),
+            "Wv": _draw(rng, (Dkv, D), 0.0, s, dtype), "attn": _draw(rng, (M, D), 0.0, 1.0, dtype),
+            "Wo": _draw(rng, (D, D), 0.0, s, dtype), "gamma_ffn": _draw(rng, (D,), 1.0, 0.1, dtype),
+            "Wg": _draw(rng, (F, D), 0.0, s, dtype), "Wu": _draw(rng, (F, D), 0.0, s, dtype),
+            "Wd": _draw(rng, (D, F), 0.0, 1.0 / math.sqrt(F), dtype)}

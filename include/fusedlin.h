@@ -227,6 +227,69 @@ fl_status fl_swiglu_ffn_noalloc(const void* x, const void* gamma, const void* Wg
                                 const void* Wd, const void* bias_down, void* out, int M, int D,
                                 int F, float eps, fl_dtype dtype, void* stream);
 
+/*
+ * The dense part of a Llama-style decoder layer, captured into CUDA graphs.
+ * At decode sizes every kernel of a layer takes a few microseconds, so host
+ * launch costs and the gaps between launches weigh as much as the kernels;
+ * capturing the layer once and replaying it removes them (the "Fusion
+ * Compiler" glossary pairs fusion with CUDA Graph capture as the coarse-grained
+ * launch optimisation). The layer is split where the attention core sits,
+ * which this library does not compute:
+ *   half 0:  q, k, v = RMSNorm(x; gamma_attn) [Wq; Wk; Wv]^T       (fl_norm_gemm_multi)
+ *   ... the caller's attention reads q, k, v and writes attn ...
+ *   half 1:  h   = attn Wo^T (+ bias_o) + x                        (fl_gemm_epilogue)
+ *            out = silu(hn Wg^T) * (hn Wu^T) Wd^T + h, hn = RMSNorm(h; gamma_ffn)   (fl_swiglu_ffn)
+ * Shapes: x, attn, h, out, q [M, D]; k, v [M, Dkv]; Wq, Wo [D, D];
+ * Wk, Wv [Dkv, D]; Wg, Wu [F, D]; Wd [D, F]; gamma_* and bias_o [D]. All are
+ * caller-owned device pointers, fixed for the life of the layer: the graphs
+ * hold them. bias_o may be NULL (no bias). eps is the RMSNorm epsilon of both
+ * norms.
+ */
+typedef struct {
+    fl_dtype dtype;
+    int M, D, Dkv, F;
+    float eps;
+    const void* x;
+    const void* gamma_attn;
+    const void* Wq;
+    const void* Wk;
+    const void* Wv;
+    void* q;
+    void* k;
+    void* v;
+    const void* attn;
+    const void* Wo;
+    const void* bias_o;
+    void* h;
+    const void* gamma_ffn;
+    const void* Wg;
+    const void* Wu;
+    const void* Wd;
+    void* out;
+} fl_layer_desc;
+
+typedef struct fl_layer fl_layer;
+
+/*
+ * Validates the description, allocates the layer's own device memory (the
+ * FFN hidden activation, M * F * 2 bytes, and D zeros when bias_o is NULL),
+ * runs both halves once uncaptured (the one-time kernel set-up; this writes
+ * q, k, v, h and out from whatever x and attn hold), then captures each half
+ * into a CUDA graph on an internal stream and instantiates it. Call it at
+ * initialisation, not inside another stream capture. On failure *layer is
+ * NULL and nothing is left allocated.
+ */
+fl_status fl_layer_create(const fl_layer_desc* desc, fl_layer** layer);
+
+/* Launches half 0 or 1 as one graph launch on `stream`; allocates nothing. */
+fl_status fl_layer_launch(fl_layer* layer, int half, void* stream);
+
+/* Issues the same half as ordinary library calls on `stream` (no graph), for comparison. */
+fl_status fl_layer_issue(const fl_layer* layer, int half, void* stream);
+
+/* Frees the graphs, the internal stream and the layer's device memory. NULL is a no-op. */
+void fl_layer_destroy(fl_layer* layer);
+
 /* Message for the last non-OK status returned on this thread ("" if none). */
 const char* fl_last_error(void);
 

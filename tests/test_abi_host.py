@@ -216,3 +216,30 @@ def test_rms_norm_validation(L):
     assert call(out=addr(0, 16)) == INVALID                    # partial overlap with x
     assert call(out=addr(1)) == INVALID                        # out overlaps gamma
     assert call(out=addr(0)) in (OK, UNSUPPORTED, CUDA)        # in place
+
+
+def test_layer_create_validation(L):
+    names = fl.DecoderLayer.NAMES
+
+    def desc(**over):
+        d = fl.LayerDesc(dtype=0, M=4, D=64, Dkv=32, F=128, eps=1e-6,
+                         **{n: BASE + i * (1 << 32) for i, n in enumerate(names)})
+        d.bias_o = None
+        for k, v in over.items():
+            setattr(d, k, v)
+        return d
+
+    h = ctypes.c_void_p(1234)
+    assert L.fl_layer_create(None, ctypes.byref(h)) == INVALID and not h.value
+    assert L.fl_layer_create(ctypes.byref(desc(dtype=3)), ctypes.byref(h)) == INVALID
+    assert L.fl_layer_create(ctypes.byref(desc(M=0)), ctypes.byref(h)) == INVALID
+    assert L.fl_layer_create(ctypes.byref(desc(Dkv=20)), ctypes.byref(h)) == ALIGN
+    assert L.fl_layer_create(ctypes.byref(desc(Wo=None)), ctypes.byref(h)) == INVALID
+    assert L.fl_layer_create(ctypes.byref(desc(q=BASE + 8)), ctypes.byref(h)) == ALIGN
+    assert L.fl_layer_create(ctypes.byref(desc(eps=-1.0)), ctypes.byref(h)) == INVALID
+    d = desc()
+    d.h = d.x
+    assert L.fl_layer_create(ctypes.byref(d), ctypes.byref(h)) == INVALID
+    assert not h.value
+    assert L.fl_layer_launch(None, 0, None) == INVALID
+    L.fl_layer_destroy(None)  # no-op
