@@ -583,6 +583,7 @@ def run_ours(args, w: dict, rank: int, world: int, local: int):
     wall0 = time.time()
     ev0.record(stream)
     timed_steps()
+    enqueue_s = time.time() - wall0  # host time to issue the K steps (stream calls: the launch path's cost)
     ev1.record(stream)
     torch.cuda.synchronize()
     wall1 = time.time()
@@ -647,7 +648,8 @@ def run_ours(args, w: dict, rank: int, world: int, local: int):
                               else f"CUDA graphs of {nsets} library calls, replayed"),
                    "weights": "read-only; " + ("read after the previous step" if args.no_weight_preload else
                                                "first tiles staged before the programmatic dependency resolves"),
-                   "vs_baseline_ref": "A30 fused RMSNorm->Linear 0.208 ms (LLMBoost page), other hardware"},
+                   "vs_baseline_ref": "A30 fused RMSNorm->Linear 0.208 ms (LLMBoost page), other hardware",
+                   "host_enqueue_us_per_step": enqueue_s * 1e6 / args.steps},
         "roofline": roofline,
         "e2e": {"value": flops * e2e_steps * world / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out_bytes},

@@ -16,11 +16,18 @@ namespace fl {
 // loop: producer issue, fold hand-off, MMA waits). SM clock cycles, or global
 // nanoseconds (comparable across SMs and launches) with -DFL_TRACE_GLOBALTIMER.
 #ifdef FL_TRACE
+// (read with a memory clobber, so the compiler keeps the mark where it is
+// written relative to barriers and memory operations)
+__device__ __forceinline__ unsigned long long fl_trace_now() {
+    unsigned long long t;
 #ifdef FL_TRACE_GLOBALTIMER
-#define FL_TRACE_NOW() globaltimer_ns()
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t)::"memory");
 #else
-#define FL_TRACE_NOW() clock64()
+    asm volatile("mov.u64 %0, %%clock64;" : "=l"(t)::"memory");
 #endif
+    return t;
+}
+#define FL_TRACE_NOW() fl_trace_now()
 #ifdef FL_TRACE_STEPS
 #define FL_TRACE_SLOTS 64
 #else

@@ -231,7 +231,16 @@ cudaError_t dispatch_tile(int dt, int bn, int pro, bool dual, const GemmParams& 
     return cudaErrorInvalidValue;
 }
 
-cudaError_t dispatch_splitk(int dt, int bn, int pro, const GemmParams& p, int grid, int splits, cudaStream_t s) {
+cudaError_t dispatch_splitk(int dt, int bn, int pro, bool dual, const GemmParams& p, int grid, int splits,
+                            cudaStream_t s) {
+    if (dual) {
+        if (pro != fl::PRO_RMS) return cudaErrorInvalidValue;
+        if (bn == 64) return dt == 0 ? fl::launch_splitk<0, 64, fl::PRO_RMS, true>(p, grid, splits, s)
+                                     : fl::launch_splitk<1, 64, fl::PRO_RMS, true>(p, grid, splits, s);
+        if (bn == 128) return dt == 0 ? fl::launch_splitk<0, 128, fl::PRO_RMS, true>(p, grid, splits, s)
+                                      : fl::launch_splitk<1, 128, fl::PRO_RMS, true>(p, grid, splits, s);
+        return cudaErrorInvalidValue;
+    }
 #define FL_CASE(DT, BN, PRO) \
     if (dt == DT && bn == BN && pro == PRO) return fl::launch_splitk<DT, BN, PRO>(p, grid, splits, s);
     FL_CASE(0, 64, 0) FL_CASE(0, 64, 1) FL_CASE(0, 64, 2) FL_CASE(0, 64, 3)
@@ -254,10 +263,10 @@ struct SplitPlan {
 // cluster size: the two-CTAs-per-SM budget when it holds at least four
 // stages and the reduction exchange, else the one-CTA budget. Returns false
 // if neither holds the exchange.
-template <int BN>
+template <int BN, bool DUAL>
 bool split_geom_bn(int a_rows, int splits, fl::SplitGeom* g) {
-    using C = fl::SplitCfg<BN>;
-    const int stage = a_rows * 128 + C::B_BYTES;
+    using C = fl::SplitCfg<BN, DUAL>;
+    const int stage = a_rows * 128 + C::STAGE_B_BYTES;
     const int xbytes = C::xchg_bytes(splits, a_rows);
     int stages = std::min(C::MAX_STAGES, C::RING_SMALL / stage);
     if (stages < 4 || xbytes > stages * stage) stages = std::min(C::MAX_STAGES, C::RING_LARGE / stage);
@@ -268,17 +277,29 @@ bool split_geom_bn(int a_rows, int splits, fl::SplitGeom* g) {
     return true;
 }
 
-bool split_geom(int bn, int a_rows, int splits, fl::SplitGeom* g) {
-    return bn == 128 ? split_geom_bn<128>(a_rows, splits, g) : split_geom_bn<64>(a_rows, splits, g);
+bool split_geom(int bn, bool dual, int a_rows, int splits, fl::SplitGeom* g) {
+    if (dual) return bn == 128 ? split_geom_bn<128, true>(a_rows, splits, g) : split_geom_bn<64, true>(a_rows, splits, g);
+    return bn == 128 ? split_geom_bn<128, false>(a_rows, splits, g) : split_geom_bn<64, false>(a_rows, splits, g);
 }
 
-int max_clusters(int dt, int bn, int pro, int splits, int a_rows, int smem) {
-    // cached per (dtype, width, prologue, cluster size, box height); single device assumed per process slot
-    static std::atomic<int> cache[2][2][4][9][8];
+int max_clusters(int dt, int bn, int pro, bool dual, int splits, int a_rows, int smem) {
+    // cached per (dtype, width, prologue, dual, cluster size, box height); single device assumed per process slot
+    static std::atomic<int> cache[2][2][4][2][9][8];
     const int bi = bn == 128 ? 1 : 0;
     const int ai = (a_rows / 16 - 1) & 7;
-    int v = cache[dt][bi][pro][splits][ai].load();
+    int v = cache[dt][bi][pro][dual ? 1 : 0][splits][ai].load();
     if (v != 0) return v;
+    if (dual) {
+        if (pro == fl::PRO_RMS) {
+            if (bn == 64) v = dt == 0 ? fl::splitk_max_clusters<0, 64, fl::PRO_RMS, true>(splits, smem)
+                                      : fl::splitk_max_clusters<1, 64, fl::PRO_RMS, true>(splits, smem);
+            else v = dt == 0 ? fl::splitk_max_clusters<0, 128, fl::PRO_RMS, true>(splits, smem)
+                             : fl::splitk_max_clusters<1, 128, fl::PRO_RMS, true>(splits, smem);
+        }
+        if (v <= 0) v = -1;
+        cache[dt][bi][pro][1][splits][ai] = v;
+        return v;
+    }
 #define FL_Q(DT, BN, PRO) \
     if (dt == DT && bn == BN && pro == PRO) v = fl::splitk_max_clusters<DT, BN, PRO>(splits, smem);
     FL_Q(0, 64, 0) FL_Q(0, 64, 1) FL_Q(0, 64, 2) FL_Q(0, 64, 3) FL_Q(0, 128, 0) FL_Q(0, 128, 1) FL_Q(0, 128, 2)
@@ -286,11 +307,14 @@ int max_clusters(int dt, int bn, int pro, int splits, int a_rows, int smem) {
     FL_Q(1, 128, 2) FL_Q(1, 128, 3)
 #undef FL_Q
     if (v <= 0) v = -1;
-    cache[dt][bi][pro][splits][ai] = v;
+    cache[dt][bi][pro][0][splits][ai] = v;
     return v;
 }
 
-bool plan_splitk(int dt, int pro, int M, const Outs& outs, int K, int sms, SplitPlan* plan) {
+// dual: the SwiGLU gate/up form (two weights, SwiGLU epilogue), taken for
+// decode row counts (one 128-row block), where the CTA-pair and tile kernels
+// would run mostly empty 256- or 128-row MMAs over the whole K range.
+bool plan_splitk(int dt, int pro, bool dual, int M, const Outs& outs, int K, int sms, SplitPlan* plan) {
     const int variant = g_opt_variant.load();
     if (variant == 1 || variant == 3) return false;
     const int nk = (K + fl::kBK - 1) / fl::kBK;
@@ -308,7 +332,8 @@ bool plan_splitk(int dt, int pro, int M, const Outs& outs, int K, int sms, Split
     const int forced_bn = g_opt_tile_n.load();
     const int bn = forced_bn == 128 ? 128 : forced_bn == 256 ? 64 : (ctas_for(128) * 4 >= ctas_for(64) * 3 ? 128 : 64);
     const long long tiles = mb * nblocks(outs, bn);
-    if (variant == 0) {
+    if (dual && (mb > 1 || pro != fl::PRO_RMS)) return false;
+    if (variant == 0 && !dual) {
         // the tile kernel fills at least half the SMs: it reuses each staged
         // tile across the whole K loop and needs no reduction
         if ((long long)mb * nblocks(outs, 128) * 2 > sms || nk < 4) return false;
@@ -328,9 +353,9 @@ bool plan_splitk(int dt, int pro, int M, const Outs& outs, int K, int sms, Split
     fl::SplitGeom geom;
     for (;; --splits) {
         if (splits < 1) return false;
-        if (!split_geom(bn, a_rows, splits, &geom)) continue;
+        if (!split_geom(bn, dual, a_rows, splits, &geom)) continue;
         if (splits == 1) break;
-        const int mc = max_clusters(dt, bn, pro, splits, a_rows, geom.smem_bytes);
+        const int mc = max_clusters(dt, bn, pro, dual, splits, a_rows, geom.smem_bytes);
         if (mc < 0 || tiles <= mc) break;
     }
     const int kps = (nk + splits - 1) / splits;
@@ -338,7 +363,7 @@ bool plan_splitk(int dt, int pro, int M, const Outs& outs, int K, int sms, Split
     plan->kps = kps;
     plan->splits = (nk + kps - 1) / kps;  // every split gets at least one K block
     plan->a_rows = a_rows;
-    if (!split_geom(bn, a_rows, plan->splits, &plan->geom)) return false;
+    if (!split_geom(bn, dual, a_rows, plan->splits, &plan->geom)) return false;
     return true;
 }
 
@@ -395,8 +420,10 @@ bool use_pair(int dt, int pro, int M, const Outs& outs, int K, PairPlan* plan, b
     if (variant == 1 || variant == 2) return false;
     if (dual) {
         // SwiGLU gate/up: 128 output columns per 256 x 256 pair tile (Wg and Wu
-        // stacked); no K split, no 128-wide variant
+        // stacked); no K split, no 128-wide variant. Decode row counts (one
+        // 128-row block) take the split-K form instead.
         if (pro != fl::PRO_RMS) return false;
+        if (variant != 3 && M <= fl::kBM) return false;
         const long long tiles = (long long)((M + 255) / 256) * nblocks(outs, 128);
         const int maxp = pair_max(dt, 256, pro, 1);
         if (maxp <= 0) return false;
@@ -498,9 +525,9 @@ int choose_bn(int M, const Outs& outs, bool dual, int sms) {
     return c256 <= c128 ? 256 : 128;
 }
 
-fl_status run_splitk(int dt, int pro, const void* A, const Outs& outs, const void* residual, const void* gamma,
-                     const void* beta, const void* ln_stats, int M, int K, float eps, const SplitPlan& plan,
-                     DeviceInfo* di, cudaStream_t stream) {
+fl_status run_splitk(int dt, int pro, bool dual, const void* A, const Outs& outs, const void* W2,
+                     const void* residual, const void* gamma, const void* beta, const void* ln_stats, int M, int K,
+                     float eps, const SplitPlan& plan, DeviceInfo* di, cudaStream_t stream) {
     GemmParams p;
     memset(&p, 0, sizeof(p));
     fill_common(p, A, residual, gamma, beta, ln_stats, M, K, eps, di);
@@ -508,6 +535,7 @@ fl_status run_splitk(int dt, int pro, const void* A, const Outs& outs, const voi
     fl_status st;
     if ((st = encode_2d(&p.tmA, dt, A, K, M, fl::kBK, a_rows)) != FL_OK) return st;
     if ((st = fill_outputs(p, dt, outs, M, K, plan.bn, plan.bn)) != FL_OK) return st;
+    if (dual && (st = encode_2d(&p.tmB2, dt, W2, K, outs.o[0].N, fl::kBK, plan.bn)) != FL_OK) return st;
     if ((st = encode_prologue(p, dt, pro, gamma, beta, K)) != FL_OK) return st;
     p.num_m_blocks = (M + fl::kBM - 1) / fl::kBM;
     p.num_tiles = p.num_m_blocks * p.num_n_blocks;
@@ -526,14 +554,14 @@ fl_status run_splitk(int dt, int pro, const void* A, const Outs& outs, const voi
                 p.xc_owner[ch] = (unsigned char)d;
                 p.xc_pos[ch] = (unsigned char)(ch - p.xc_c0[d]);
             }
-        p.xc_stride = (nch + s - 1) / s * 8 + 4;
+        p.xc_stride = (nch + s - 1) / s * 8 * (dual ? 2 : 1) + 4;  // SplitCfg::xchg_stride
         p.inv_k = 1.0f / (float)K;
     }
 #ifdef FL_TRACE
     if (const char* tp = getenv("FL_TRACE_PTR")) p.trace = reinterpret_cast<unsigned long long*>(strtoull(tp, nullptr, 10));
 #endif
     const int grid = p.num_tiles * plan.splits;
-    cudaError_t e = dispatch_splitk(dt, plan.bn, pro, p, grid, plan.splits, stream);
+    cudaError_t e = dispatch_splitk(dt, plan.bn, pro, dual, p, grid, plan.splits, stream);
     if (e != cudaSuccess) return fail(FL_ERR_CUDA, "split-K kernel launch failed: %s", cudaGetErrorString(e));
     return ok();
 }
@@ -546,8 +574,8 @@ fl_status run_kernels(int dt, int pro, bool dual, const void* A, const Outs& out
     if (use_pair(dt, pro, M, outs, K, &pplan, dual))
         return run_pair(dt, pro, dual, A, outs, W2, residual, gamma, beta, ln_stats, M, K, eps, pplan, di, stream);
     SplitPlan plan;
-    if (!dual && plan_splitk(dt, pro, M, outs, K, di->sms, &plan))
-        return run_splitk(dt, pro, A, outs, residual, gamma, beta, ln_stats, M, K, eps, plan, di, stream);
+    if (plan_splitk(dt, pro, dual, M, outs, K, di->sms, &plan))
+        return run_splitk(dt, pro, dual, A, outs, W2, residual, gamma, beta, ln_stats, M, K, eps, plan, di, stream);
     const int bn = choose_bn(M, outs, dual, di->sms);
     GemmParams p;
     memset(&p, 0, sizeof(p));

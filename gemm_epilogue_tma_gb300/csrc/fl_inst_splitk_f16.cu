@@ -1,4 +1,5 @@
-// Split-K kernel instances (f16): few output tiles, weights streamed once.
+// Split-K kernel instances (f16): few output tiles, weights streamed once; the
+// SwiGLU gate/up form (two weights) for decode row counts.
 #include "fl_splitk_kernel.cuh"
 
 namespace fl {
@@ -14,4 +15,8 @@ template int splitk_max_clusters<DT_F16, 64, PRO_LN>(int, int);
 template int splitk_max_clusters<DT_F16, 128, PRO_NONE>(int, int);
 template int splitk_max_clusters<DT_F16, 128, PRO_RMS>(int, int);
 template int splitk_max_clusters<DT_F16, 128, PRO_LN>(int, int);
+template cudaError_t launch_splitk<DT_F16, 64, PRO_RMS, true>(const GemmParams&, int, int, cudaStream_t);
+template cudaError_t launch_splitk<DT_F16, 128, PRO_RMS, true>(const GemmParams&, int, int, cudaStream_t);
+template int splitk_max_clusters<DT_F16, 64, PRO_RMS, true>(int, int);
+template int splitk_max_clusters<DT_F16, 128, PRO_RMS, true>(int, int);
 }  // namespace fl

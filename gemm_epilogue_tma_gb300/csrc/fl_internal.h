@@ -86,10 +86,10 @@ cudaError_t launch_rms_norm(int dt, const void* x, const void* gamma, void* y, i
 template <int DT, int BN, int PRO, bool DUAL>
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream);
 
-template <int DT, int BN, int PRO>
+template <int DT, int BN, int PRO, bool DUAL = false>
 cudaError_t launch_splitk(const GemmParams& p, int grid, int splits, cudaStream_t stream);
 
-template <int DT, int BN, int PRO>
+template <int DT, int BN, int PRO, bool DUAL = false>
 int splitk_max_clusters(int splits, int smem_bytes);
 
 template <int DT, int BN, int PRO, int KS, bool DUAL>
@@ -103,12 +103,19 @@ int pair_max_clusters();
 // height (a decode step stages 16 activation rows, not 128), so small-M
 // instances fit two CTAs per SM and the next kernel's CTAs can be resident
 // (prefetching their weights) while this one finishes.
-template <int BN>
+//
+// DUAL (SwiGLU gate/up): every stage holds a tile of Wg and one of Wu after the
+// activation box, the MMA fills two accumulators (gate in TMEM columns
+// [0, BN), up in [BN, 2 BN)), and the exchange carries both per chunk.
+template <int BN, bool DUAL = false>
 struct SplitCfg {
     static constexpr int A_MAX_BYTES = kBM * kBK * 2;  // what one MMA reads of A (128 rows)
-    static constexpr int B_BYTES = BN * kBK * 2;
+    static constexpr int NW = DUAL ? 2 : 1;            // weight tiles per stage
+    static constexpr int B_BYTES = BN * kBK * 2;       // one weight tile
+    static constexpr int STAGE_B_BYTES = NW * B_BYTES;
     static constexpr int MAX_STAGES = 8;
-    static constexpr int TMEM_COLS = BN < 32 ? 32 : BN;
+    static constexpr int TMEM_COLS = NW * BN < 32 ? 32 : NW * BN;
+    static constexpr int CHUNK_FLOATS = 8 * NW;        // floats of one 8-column chunk in an exchange slot
     static constexpr int NUM_BARS = 3 * MAX_STAGES + 4;
     static constexpr int OFF_BAR = 0;
     static constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
@@ -127,16 +134,19 @@ struct SplitCfg {
     // s - 1 outgoing ones. A stride of 4 mod 8 words keeps rows on distinct
     // banks for 16-byte accesses.
     static constexpr int CHUNKS = BN / 8;
-    __host__ __device__ static constexpr int xchg_stride(int s) { return (CHUNKS + s - 1) / s * 8 + 4; }
+    __host__ __device__ static constexpr int xchg_stride(int s) { return (CHUNKS + s - 1) / s * CHUNK_FLOATS + 4; }
     __host__ __device__ static constexpr int xchg_bytes(int s, int rows) {
         return (2 * s - 1) * rows * xchg_stride(s) * 4;
     }
     static constexpr bool xchg_fits_large() {
         for (int s = 1; s <= 8; ++s)
-            if (xchg_bytes(s, kBM) > RING_LARGE / (kBM * 128 + B_BYTES) * (kBM * 128 + B_BYTES)) return false;
+            if (xchg_bytes(s, kBM) > RING_LARGE / (kBM * 128 + STAGE_B_BYTES) * (kBM * 128 + STAGE_B_BYTES))
+                return false;
         return true;
     }
-    static_assert(xchg_fits_large(), "the reduction exchange must fit in the large ring");
+    // (single weight: every cluster size fits; the gate/up form's exchange is
+    // twice as wide, and the host lowers its split until it fits)
+    static_assert(DUAL || xchg_fits_large(), "the reduction exchange must fit in the large ring");
     // dynamic shared memory of a launch: fixed block, ring, room for one
     // MMA's 128-row read of A from the last stage, alignment slack
     __host__ __device__ static constexpr int smem_bytes(int stages, int stage_bytes) {

@@ -23,6 +23,10 @@
 //
 // LayerNorm folds with row statistics computed once per call by a separate
 // small kernel (read here after the programmatic dependency resolves).
+//
+// DUAL (SwiGLU gate/up at decode sizes): each stage carries a tile of Wg and
+// one of Wu, two accumulators are exchanged together, and the owner writes
+// h = silu(gate / rms) * (up / rms).
 #pragma once
 
 #include "fl_common.cuh"
@@ -37,11 +41,12 @@ namespace fl {
 template <int PRO>
 constexpr int splitk_threads() { return PRO != PRO_NONE ? 320 : 256; }
 
-template <int DT, int BN, int PRO>
+template <int DT, int BN, int PRO, bool DUAL>
 __global__ void __launch_bounds__(splitk_threads<PRO>(), 1)
     fl_splitk_kernel(const __grid_constant__ GemmParams p) {
     if (threadIdx.x == 0) FL_MARK(p, 0);
-    using C = SplitCfg<BN>;
+    using C = SplitCfg<BN, DUAL>;
+    static_assert(!DUAL || PRO == PRO_RMS, "the gate/up kernel has the RMS prologue");
     using Ops = DTypeOps<DT>;
     constexpr int S = C::MAX_STAGES;  // barrier slots; the ring uses p.s_stages of them
     constexpr int XF_WARP0 = 2;
@@ -61,6 +66,7 @@ __global__ void __launch_bounds__(splitk_threads<PRO>(), 1)
     const uint32_t stage_bytes = (uint32_t)p.s_stage_bytes;
     auto stage_a = [&](int s) { return ring + (uint32_t)s * stage_bytes; };
     auto stage_b = [&](int s) { return ring + (uint32_t)s * stage_bytes + a_bytes; };
+    auto stage_b2 = [&](int s) { return ring + (uint32_t)s * stage_bytes + a_bytes + (uint32_t)C::B_BYTES; };
     const uint32_t bar0 = sbase + C::OFF_BAR;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
@@ -102,6 +108,7 @@ __global__ void __launch_bounds__(splitk_threads<PRO>(), 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&p.tmA);
         tma_prefetch_desc(tmB);
+        if (DUAL) tma_prefetch_desc(&p.tmB2);
         if (PRO != PRO_NONE) tma_prefetch_desc(&p.tmGamma);
         if (PRO == PRO_LN && p.beta != nullptr) tma_prefetch_desc(&p.tmBeta);
     }
@@ -127,15 +134,19 @@ __global__ void __launch_bounds__(splitk_threads<PRO>(), 1)
     // coherence). With two CTAs per SM the prefetch would compete with the
     // previous kernel's stream for lines it then loses.
     const int npre = p.w_preload ? min(NS, kb1 - kb0) : 0;
-    const uint32_t stage_tx = a_bytes + (uint32_t)C::B_BYTES + (PRO != PRO_NONE ? 128u : 0u) +
+    const uint32_t stage_tx = a_bytes + (uint32_t)C::STAGE_B_BYTES + (PRO != PRO_NONE ? 128u : 0u) +
                               (PRO == PRO_LN && p.beta != nullptr ? 128u : 0u);
     if (warp == 0 && lane == 0) {
         for (int i = 0; i < npre; ++i) {
             mbar_arrive_expect_tx(full_bar(i), stage_tx);
             tma_load_2d(stage_b(i), tmB, full_bar(i), (kb0 + i) * kBK, n0);
+            if (DUAL) tma_load_2d(stage_b2(i), &p.tmB2, full_bar(i), (kb0 + i) * kBK, n0);
         }
         if (p.s_one_per_sm)
-            for (int kb = kb0 + npre; kb < kb0 + NS && kb < kb1; ++kb) tma_prefetch_2d(tmB, kb * kBK, n0);
+            for (int kb = kb0 + npre; kb < kb0 + NS && kb < kb1; ++kb) {
+                tma_prefetch_2d(tmB, kb * kBK, n0);
+                if (DUAL) tma_prefetch_2d(&p.tmB2, kb * kBK, n0);
+            }
     }
     griddep_wait();
     // The next kernel may launch now when its CTAs can only use idle SMs; with
@@ -158,6 +169,7 @@ __global__ void __launch_bounds__(splitk_threads<PRO>(), 1)
                     if (!wait_bar(empty_bar(s), ph ^ 1u, p.status, p.timeout_ns, 21)) break;
                     mbar_arrive_expect_tx(full_bar(s), stage_tx);
                     tma_load_2d(stage_b(s), tmB, full_bar(s), kb * kBK, n0);
+                    if (DUAL) tma_load_2d(stage_b2(s), &p.tmB2, full_bar(s), kb * kBK, n0);
                 }
                 tma_load_2d(stage_a(s), &p.tmA, full_bar(s), kb * kBK, m0);
                 if (PRO != PRO_NONE) {
@@ -195,8 +207,12 @@ __global__ void __launch_bounds__(splitk_threads<PRO>(), 1)
                 const uint64_t da = sw128_kmajor_desc(stage_a(s));
                 const uint64_t db = sw128_kmajor_desc(stage_b(s));
 #pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk)
+                for (int kk = 0; kk < kBK / 16; ++kk) {
                     umma_f16_ss(tmem_base, da + 2 * kk, db + 2 * kk, IDESC, (kb != kb0) || (kk != 0));
+                    if (DUAL)
+                        umma_f16_ss(tmem_base + BN, da + 2 * kk, sw128_kmajor_desc(stage_b2(s)) + 2 * kk, IDESC,
+                                    (kb != kb0) || (kk != 0));
+                }
                 umma_commit(empty_bar(s));
                 if (++s == NS) {
                     s = 0;
@@ -300,10 +316,33 @@ __global__ void __launch_bounds__(splitk_threads<PRO>(), 1)
             if (lead && splits > 1) mbar_arrive_expect_tx(recvd_bar, (uint32_t)(splits - 1) * slot_bytes);
             if (q * 32 < rows) {
                 const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16);
+                if constexpr (DUAL) {
+                    // gate and up of one 32-column group per wait; a chunk's
+                    // slot entry is its 8 gate values, then its 8 up values
+#pragma unroll
+                    for (int c = 0; c < BN / 32; ++c) {
+                        uint32_t g[32], u[32];
+                        tmem_ld_32x32b_x32(taddr + c * 32, g);
+                        tmem_ld_32x32b_x32(taddr + BN + c * 32, u);
+                        tmem_ld_wait();
+                        if (r < rows) {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const int ch = c * 4 + j;
+                                const uint32_t dst = ring + (uint32_t)slot_index(p.xc_owner[ch]) * slot_bytes +
+                                                     row_off + (uint32_t)p.xc_pos[ch] * (uint32_t)(C::CHUNK_FLOATS * 4);
+                                st_shared_v4(dst, g[j * 8], g[j * 8 + 1], g[j * 8 + 2], g[j * 8 + 3]);
+                                st_shared_v4(dst + 16, g[j * 8 + 4], g[j * 8 + 5], g[j * 8 + 6], g[j * 8 + 7]);
+                                st_shared_v4(dst + 32, u[j * 8], u[j * 8 + 1], u[j * 8 + 2], u[j * 8 + 3]);
+                                st_shared_v4(dst + 48, u[j * 8 + 4], u[j * 8 + 5], u[j * 8 + 6], u[j * 8 + 7]);
+                            }
+                        }
+                    }
+                }
                 // two 32-column loads in flight per wait
                 constexpr int NB = BN / 32 < 2 ? 1 : 2;
 #pragma unroll
-                for (int c = 0; c < BN / 32; c += NB) {
+                for (int c = 0; c < (DUAL ? 0 : BN / 32); c += NB) {
                     uint32_t v[NB][32];
 #pragma unroll
                     for (int b = 0; b < NB; ++b) tmem_ld_32x32b_x32(taddr + (c + b) * 32, v[b]);
@@ -411,11 +450,11 @@ __global__ void __launch_bounds__(splitk_threads<PRO>(), 1)
             const size_t g = (size_t)(m0 + row) * N + xcol;
             uint4 rv = make_uint4(0u, 0u, 0u, 0u);
             if (res != nullptr) rv = *reinterpret_cast<const uint4*>(res + g);
-            float v[8];
+            float v[8], vu[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] = 0.f;
+            for (int e = 0; e < 8; ++e) v[e] = vu[e] = 0.f;
             float ss = 0.f;
-            const uint32_t a0 = ring + (uint32_t)(row * stride + xch * 8) * 4u;
+            const uint32_t a0 = ring + (uint32_t)(row * stride + xch * C::CHUNK_FLOATS) * 4u;
             const uint32_t s0 = ring + (uint32_t)(row * stride + stride - 4) * 4u;
 #pragma unroll
             for (int src = 0; src < 8; ++src) {
@@ -426,13 +465,26 @@ __global__ void __launch_bounds__(splitk_threads<PRO>(), 1)
                     v[2] += __uint_as_float(lo.z); v[3] += __uint_as_float(lo.w);
                     v[4] += __uint_as_float(hi.x); v[5] += __uint_as_float(hi.y);
                     v[6] += __uint_as_float(hi.z); v[7] += __uint_as_float(hi.w);
+                    if (DUAL) {
+                        const uint4 ulo = ld_shared_v4(a + 32), uhi = ld_shared_v4(a + 48);
+                        vu[0] += __uint_as_float(ulo.x); vu[1] += __uint_as_float(ulo.y);
+                        vu[2] += __uint_as_float(ulo.z); vu[3] += __uint_as_float(ulo.w);
+                        vu[4] += __uint_as_float(uhi.x); vu[5] += __uint_as_float(uhi.y);
+                        vu[6] += __uint_as_float(uhi.z); vu[7] += __uint_as_float(uhi.w);
+                    }
                     if (PRO == PRO_RMS) ss += ld_shared_f32(s0 + (uint32_t)src * slot_bytes);
                 }
             }
             const float rs = PRO == PRO_RMS ? rsqrtf(fmaf(ss, p.inv_k, p.eps)) : 1.f;
+            if (DUAL) {
+                // h = silu(gate) * up, both scaled by 1/rms
 #pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] = fmaf(v[e], rs, bb[e]);
-            if (act != ACT_NONE) {
+                for (int e = 0; e < 8; ++e) v[e] = act_apply(ACT_SILU, v[e] * rs) * (vu[e] * rs);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] = fmaf(v[e], rs, bb[e]);
+            }
+            if (!DUAL && act != ACT_NONE) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) v[e] = act_apply(act, v[e]);
             }
@@ -461,11 +513,12 @@ __global__ void __launch_bounds__(splitk_threads<PRO>(), 1)
     }
 }
 
-template <int DT, int BN, int PRO>
+template <int DT, int BN, int PRO, bool DUAL>
 cudaError_t splitk_configure() {
     static cudaError_t state = [] {
-        auto kern = fl_splitk_kernel<DT, BN, PRO>;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SplitCfg<BN>::SMEM_MAX);
+        auto kern = fl_splitk_kernel<DT, BN, PRO, DUAL>;
+        cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SplitCfg<BN, DUAL>::SMEM_MAX);
         if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
         return e;
     }();
@@ -474,10 +527,10 @@ cudaError_t splitk_configure() {
 
 // How many clusters of `splits` CTAs of this kernel, each with `smem_bytes`
 // of dynamic shared memory, can be resident at once.
-template <int DT, int BN, int PRO>
+template <int DT, int BN, int PRO, bool DUAL>
 int splitk_max_clusters(int splits, int smem_bytes) {
-    if (splitk_configure<DT, BN, PRO>() != cudaSuccess) return 0;
-    auto kern = fl_splitk_kernel<DT, BN, PRO>;
+    if (splitk_configure<DT, BN, PRO, DUAL>() != cudaSuccess) return 0;
+    auto kern = fl_splitk_kernel<DT, BN, PRO, DUAL>;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(splits, 1, 1);
     cfg.blockDim = dim3(splitk_threads<PRO>(), 1, 1);
@@ -497,11 +550,11 @@ int splitk_max_clusters(int splits, int smem_bytes) {
     return n;
 }
 
-template <int DT, int BN, int PRO>
+template <int DT, int BN, int PRO, bool DUAL>
 cudaError_t launch_splitk(const GemmParams& p, int grid, int splits, cudaStream_t stream) {
-    using C = SplitCfg<BN>;
-    auto kern = fl_splitk_kernel<DT, BN, PRO>;
-    cudaError_t e = splitk_configure<DT, BN, PRO>();
+    using C = SplitCfg<BN, DUAL>;
+    auto kern = fl_splitk_kernel<DT, BN, PRO, DUAL>;
+    cudaError_t e = splitk_configure<DT, BN, PRO, DUAL>();
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);

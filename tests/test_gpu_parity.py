@@ -427,6 +427,53 @@ def test_swiglu_ffn_small_all_elements(dt, with_bias, shape):
 
 
 @pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("shape", [(1, 512, 1376), (16, 1024, 2816), (77, 256, 3008), (128, 512, 1024),
+                                   (32, 4096, 11008)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_swiglu_ffn_decode_rows(dt, shape):
+    """Decode row counts: the gate/up GEMM runs as the split-K form with Wg and Wu
+    in every stage (two accumulators exchanged together)."""
+    M, D, F = shape
+    t = syn.swiglu_inputs(M, D, F, dt, with_bias=M == 77)
+    g = {k: dev(v) for k, v in t.items()}
+    ws = torch.empty(fl.swiglu_ffn_workspace_size(M, F, dt), dtype=torch.uint8, device="cuda")
+    got = fl.swiglu_ffn(g["x"], g["gamma"], g["Wg"], g["Wu"], g["Wd"], bias_down=g["bias_down"], eps=1e-6,
+                        workspace=ws)
+    torch.cuda.synchronize()
+    fl.device_status()
+    f = {k: f64(v) for k, v in t.items()}
+    ref = oracle.swiglu_ffn(f["x"], f["gamma"], f["Wg"], f["Wu"], f["Wd"], f["bias_down"], 1e-6, dt)
+    chain = parity.chain_swiglu_ffn(f["x"], f["gamma"], f["Wg"], f["Wu"], f["Wd"], f["bias_down"], 1e-6, dt)
+    assert_close(got, ref, dt, f"swiglu decode {dt} {shape}", chain=chain)
+    h = ws.view(torch.bfloat16 if dt == "bf16" else torch.float16).view(M, F)
+    href = oracle.swiglu_hidden(f["x"], f["gamma"], f["Wg"], f["Wu"], 1e-6)
+    assert_close(h, href, dt, f"swiglu decode hidden {dt} {shape}")
+
+
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("splits", [1, 2, 3, 5, 8])
+def test_swiglu_gate_up_split_k_forced(dt, tile_n, splits):
+    """The split-K gate/up form at forced weight-tile widths (128; 256 selects 64)
+    and cluster sizes, including uneven column slices."""
+    M, D, F = 40, 2048, 1032
+    t = syn.swiglu_inputs(M, D, F, dt)
+    g = {k: dev(v) for k, v in t.items()}
+    fl.set_option("tile_n", tile_n)
+    fl.set_option("split_k", splits)
+    try:
+        got = fl.swiglu_ffn(g["x"], g["gamma"], g["Wg"], g["Wu"], g["Wd"], eps=1e-6)
+        torch.cuda.synchronize()
+        fl.device_status()
+    finally:
+        fl.set_option("tile_n", 0)
+        fl.set_option("split_k", 0)
+    f = {k: f64(v) for k, v in t.items()}
+    ref = oracle.swiglu_ffn(f["x"], f["gamma"], f["Wg"], f["Wu"], f["Wd"], None, 1e-6, dt)
+    assert_close(got, ref, dt, f"swiglu split-K gate/up {dt} BN={tile_n} x{splits}")
+
+
+@pytest.mark.parametrize("dt", DTYPES)
 @pytest.mark.parametrize("D", [1024, 2048, 4096])
 @pytest.mark.parametrize("M", [1, 32, 128, 512, 1024])
 def test_decode_sweep_rmsnorm_all_elements(dt, D, M):
