@@ -251,6 +251,9 @@ cudaError_t dispatch_splitk(int dt, int bn, int pro, bool dual, const GemmParams
     return cudaErrorInvalidValue;
 }
 
+// Largest row count whose SwiGLU gate/up GEMM takes the split-K form.
+constexpr int kDualSplitRows = 64;
+
 // Split-K plan for shapes with too few output tiles to fill the GPU: 64-wide
 // weight tiles, and as many K splits (one cluster, at most 8) as keep every
 // SM streaming weights. Returns false when the tile kernel is the better fit.
@@ -312,8 +315,8 @@ int max_clusters(int dt, int bn, int pro, bool dual, int splits, int a_rows, int
 }
 
 // dual: the SwiGLU gate/up form (two weights, SwiGLU epilogue), taken for
-// decode row counts (one 128-row block), where the CTA-pair and tile kernels
-// would run mostly empty 256- or 128-row MMAs over the whole K range.
+// decode row counts, where the CTA-pair and tile kernels would run mostly
+// empty 256- or 128-row MMAs over the whole K range.
 bool plan_splitk(int dt, int pro, bool dual, int M, const Outs& outs, int K, int sms, SplitPlan* plan) {
     const int variant = g_opt_variant.load();
     if (variant == 1 || variant == 3) return false;
@@ -332,7 +335,9 @@ bool plan_splitk(int dt, int pro, bool dual, int M, const Outs& outs, int K, int
     const int forced_bn = g_opt_tile_n.load();
     const int bn = forced_bn == 128 ? 128 : forced_bn == 256 ? 64 : (ctas_for(128) * 4 >= ctas_for(64) * 3 ? 128 : 64);
     const long long tiles = mb * nblocks(outs, bn);
-    if (dual && (mb > 1 || pro != fl::PRO_RMS)) return false;
+    // gate/up: up to 64 rows (at 128 rows the CTA-pair kernel measured faster:
+    // 78 against 91 us for the 4096 x 11008 bf16 block)
+    if (dual && (M > kDualSplitRows || pro != fl::PRO_RMS)) return false;
     if (variant == 0 && !dual) {
         // the tile kernel fills at least half the SMs: it reuses each staged
         // tile across the whole K loop and needs no reduction
@@ -423,7 +428,7 @@ bool use_pair(int dt, int pro, int M, const Outs& outs, int K, PairPlan* plan, b
         // stacked); no K split, no 128-wide variant. Decode row counts (one
         // 128-row block) take the split-K form instead.
         if (pro != fl::PRO_RMS) return false;
-        if (variant != 3 && M <= fl::kBM) return false;
+        if (variant != 3 && M <= kDualSplitRows) return false;
         const long long tiles = (long long)((M + 255) / 256) * nblocks(outs, 128);
         const int maxp = pair_max(dt, 256, pro, 1);
         if (maxp <= 0) return false;
@@ -743,7 +748,7 @@ fl_status fl_norm_gemm_multi(const void* x, const void* gamma, const void* beta,
     if (!valid_dtype(dtype)) return fail(FL_ERR_INVALID_ARG, "bad dtype %d", (int)dtype);
     if (norm_kind != FL_NORM_RMS && norm_kind != FL_NORM_LAYER)
         return fail(FL_ERR_INVALID_ARG, "bad norm kind %d", (int)norm_kind);
-    if (n_out < 1 || n_out > FL_MAX_OUTPUTS)
+    if (n_out < 1 || n_out > FL_MAX_OUTPUTS || n_out > fl::kMaxOut)
         return fail(FL_ERR_INVALID_ARG, "n_out must be 1..%d, got %d", FL_MAX_OUTPUTS, n_out);
     if (W == nullptr || out == nullptr || N == nullptr)
         return fail(FL_ERR_INVALID_ARG, "W, out and N arrays must not be null");

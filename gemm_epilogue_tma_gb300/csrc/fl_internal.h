@@ -24,7 +24,10 @@ constexpr int kBK = 64;
 
 // Outputs one launch may write: several weights applied to the same
 // (normalised) activation, side by side along N (horizontal fusion).
-constexpr int kMaxOut = 4;
+#ifndef FL_MAX_OUT_PARAMS
+#define FL_MAX_OUT_PARAMS 4
+#endif
+constexpr int kMaxOut = FL_MAX_OUT_PARAMS;
 
 // Parameters of the tile kernel. Passed by value as a __grid_constant__ so the
 // tensor maps sit in parameter space, where TMA may read them.
