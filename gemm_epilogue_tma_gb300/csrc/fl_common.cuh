@@ -172,13 +172,37 @@ struct OutSel {
     int nb;  // column block within that output
 };
 
-__device__ __forceinline__ OutSel out_sel(const GemmParams& p, int nb) {
+__device__ __forceinline__ OutSel out_sel(const GemmParams&, int nb) { return OutSel{0, nb}; }
+
+__device__ __forceinline__ OutSel out_sel(const GemmParamsMulti& p, int nb) {
     int oi = 0;
 #pragma unroll
     for (int i = 1; i < kMaxOut; ++i)
         if (i < p.n_out && nb >= p.nb0[i]) oi = i;
     return OutSel{oi, nb - p.nb0[oi]};
 }
+
+// Fields of output oi: a single-output launch has only output 0.
+__device__ __forceinline__ const CUtensorMap* tm_b(const GemmParams& p, int) { return &p.tmB; }
+__device__ __forceinline__ const CUtensorMap* tm_out(const GemmParams& p, int) { return &p.tmOut; }
+__device__ __forceinline__ const void* out_bias(const GemmParams& p, int) { return p.bias; }
+__device__ __forceinline__ void* out_ptr(const GemmParams& p, int) { return p.out_ptr; }
+__device__ __forceinline__ int out_n(const GemmParams& p, int) { return p.N; }
+__device__ __forceinline__ int out_act(const GemmParams& p, int) { return p.act; }
+__device__ __forceinline__ const CUtensorMap* tm_b(const GemmParamsMulti& p, int oi) {
+    return oi == 0 ? &p.tmB : &p.tmBx[oi - 1];
+}
+__device__ __forceinline__ const CUtensorMap* tm_out(const GemmParamsMulti& p, int oi) {
+    return oi == 0 ? &p.tmOut : &p.tmOutx[oi - 1];
+}
+__device__ __forceinline__ const void* out_bias(const GemmParamsMulti& p, int oi) {
+    return oi == 0 ? p.bias : p.biasx[oi - 1];
+}
+__device__ __forceinline__ void* out_ptr(const GemmParamsMulti& p, int oi) {
+    return oi == 0 ? p.out_ptr : p.out_ptrx[oi - 1];
+}
+__device__ __forceinline__ int out_n(const GemmParamsMulti& p, int oi) { return oi == 0 ? p.N : p.Nx[oi - 1]; }
+__device__ __forceinline__ int out_act(const GemmParamsMulti& p, int oi) { return oi == 0 ? p.act : p.actx[oi - 1]; }
 
 // Hardware tanh (one special-function op; relative error about 2^-11).
 __device__ __forceinline__ float tanh_approx(float x) {

@@ -36,9 +36,9 @@ namespace fl {
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <int DT, int BN, int PRO, bool DUAL>
+template <int DT, int BN, int PRO, bool DUAL, bool MULTI>
 __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
-    fl_gemm_kernel(const __grid_constant__ GemmParams p) {
+    fl_gemm_kernel(const __grid_constant__ ParamsT<MULTI> p) {
     using C = TileCfg<BN, DUAL>;
     using Ops = DTypeOps<DT>;
     constexpr int S = C::STAGES;
@@ -99,8 +99,8 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&p.tmA);
         for (int i = 0; i < p.n_out; ++i) {
-            tma_prefetch_desc(&p.tmB[i]);
-            tma_prefetch_desc(&p.tmOut[i]);
+            tma_prefetch_desc(tm_b(p, i));
+            tma_prefetch_desc(tm_out(p, i));
         }
         if (DUAL) tma_prefetch_desc(&p.tmB2);
         if (PRO != PRO_NONE) tma_prefetch_desc(&p.tmGamma);
@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         const OutSel o = out_sel(p, blockIdx.x / p.num_m_blocks);
         const int n0 = o.nb * BN;
         for (int kb = 0; kb < S && kb < nk; ++kb) {
-            tma_prefetch_2d(&p.tmB[o.oi], kb * kBK, n0);
+            tma_prefetch_2d(tm_b(p, o.oi), kb * kBK, n0);
             if (DUAL) tma_prefetch_2d(&p.tmB2, kb * kBK, n0);
         }
     }
@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                 const int m0 = (tile % p.num_m_blocks) * kBM;
                 const OutSel o = out_sel(p, tile / p.num_m_blocks);
                 const int n0 = o.nb * BN;
-                const CUtensorMap* tb = &p.tmB[o.oi];
+                const CUtensorMap* tb = tm_b(p, o.oi);
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!wait_bar(empty_bar(s), ph ^ 1u, p.status, p.timeout_ns, 1)) {
                         ok = false;
@@ -362,9 +362,9 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
             const int m0 = (tile % p.num_m_blocks) * kBM;
             const OutSel o = out_sel(p, tile / p.num_m_blocks);
             const int n0 = o.nb * BN;
-            const int N = p.N[o.oi];
-            const int act = p.act[o.oi];
-            const T* bias = reinterpret_cast<const T*>(p.bias[o.oi]);
+            const int N = out_n(p, o.oi);
+            const int act = out_act(p, o.oi);
+            const T* bias = reinterpret_cast<const T*>(out_bias(p, o.oi));
             const int buf = NBUF == 2 ? (it & 1) : 0;
             const uint32_t tph = NBUF == 2 ? (uint32_t)((it >> 1) & 1) : (uint32_t)(it & 1);
             if (!wait_bar(tfull_bar(buf), tph, p.status, p.timeout_ns, 8)) break;
@@ -467,7 +467,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&p.tmOut[o.oi], ebuf, col0, m0 + q * 32);
+                        tma_store_2d(tm_out(p, o.oi), ebuf, col0, m0 + q * 32);
                         bulk_commit_group();
                     }
                 }
@@ -486,10 +486,10 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     }
 }
 
-template <int DT, int BN, int PRO, bool DUAL>
-cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream) {
+template <int DT, int BN, int PRO, bool DUAL, bool MULTI>
+cudaError_t launch_gemm(const ParamsT<MULTI>& p, int grid, cudaStream_t stream) {
     using C = TileCfg<BN, DUAL>;
-    auto kern = fl_gemm_kernel<DT, BN, PRO, DUAL>;
+    auto kern = fl_gemm_kernel<DT, BN, PRO, DUAL, MULTI>;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);

@@ -19,6 +19,7 @@
 #include "fl_internal.h"
 
 using fl::GemmParams;
+using fl::GemmParamsMulti;
 
 // Device status word: kernels record a bounded-wait expiry here.
 __device__ int g_fl_status;
@@ -182,19 +183,22 @@ long long nblocks(const Outs& outs, int b) {
 }
 
 // Per-output parameters of a launch whose tiles are `width` columns wide.
-// The weight maps have boxes of `b_rows` rows.
-fl_status fill_outputs(GemmParams& p, int dt, const Outs& outs, int M, int K, int width, int b_rows) {
+// The weight maps have boxes of `b_rows` rows. Output 0 goes to the base
+// block, the others to the multi-output extension.
+fl_status fill_outputs(GemmParamsMulti& p, int dt, const Outs& outs, int M, int K, int width, int b_rows) {
     fl_status st;
     p.n_out = outs.n;
     int nb = 0;
     for (int i = 0; i < outs.n; ++i) {
         const OutDesc& o = outs.o[i];
-        if ((st = encode_2d(&p.tmB[i], dt, o.W, K, o.N, fl::kBK, b_rows)) != FL_OK) return st;
-        if ((st = encode_2d(&p.tmOut[i], dt, o.out, o.N, M, 64, 32)) != FL_OK) return st;
-        p.bias[i] = o.bias;
-        p.out_ptr[i] = o.out;
-        p.N[i] = o.N;
-        p.act[i] = o.act;
+        CUtensorMap* tb = i == 0 ? &p.tmB : &p.tmBx[i - 1];
+        CUtensorMap* to = i == 0 ? &p.tmOut : &p.tmOutx[i - 1];
+        if ((st = encode_2d(tb, dt, o.W, K, o.N, fl::kBK, b_rows)) != FL_OK) return st;
+        if ((st = encode_2d(to, dt, o.out, o.N, M, 64, 32)) != FL_OK) return st;
+        (i == 0 ? p.bias : p.biasx[i - 1]) = o.bias;
+        (i == 0 ? p.out_ptr : p.out_ptrx[i - 1]) = o.out;
+        (i == 0 ? p.N : p.Nx[i - 1]) = o.N;
+        (i == 0 ? p.act : p.actx[i - 1]) = o.act;
         p.nb0[i] = nb;
         nb += (o.N + width - 1) / width;
     }
@@ -206,33 +210,36 @@ fl_status fill_outputs(GemmParams& p, int dt, const Outs& outs, int M, int K, in
 // ---------------------------------------------------------------------------
 // tile kernel dispatch
 // ---------------------------------------------------------------------------
-cudaError_t dispatch_tile(int dt, int bn, int pro, bool dual, const GemmParams& p, int grid, cudaStream_t s) {
+cudaError_t dispatch_tile(int dt, int bn, int pro, bool dual, const GemmParamsMulti& p, int grid, cudaStream_t s) {
+    const bool multi = p.n_out > 1;
 #define FL_CASE(DT, BN, PRO, DUAL) \
-    if (dt == DT && bn == BN && pro == PRO && dual == DUAL) return fl::launch_gemm<DT, BN, PRO, DUAL>(p, grid, s);
-    FL_CASE(0, 128, 0, false)
-    FL_CASE(0, 256, 0, false)
-    FL_CASE(0, 128, 1, false)
-    FL_CASE(0, 256, 1, false)
-    FL_CASE(0, 128, 2, false)
-    FL_CASE(0, 256, 2, false)
-    FL_CASE(0, 128, 3, false)
-    FL_CASE(0, 256, 3, false)
+    if (dt == DT && bn == BN && pro == PRO && dual == DUAL && !multi) return fl::launch_gemm<DT, BN, PRO, DUAL>(p, grid, s);
+    FL_CASE(0, 128, 0, false) FL_CASE(0, 256, 0, false) FL_CASE(0, 128, 1, false) FL_CASE(0, 256, 1, false)
+    FL_CASE(0, 128, 2, false) FL_CASE(0, 256, 2, false) FL_CASE(0, 128, 3, false) FL_CASE(0, 256, 3, false)
     FL_CASE(0, 128, 1, true)
-    FL_CASE(1, 128, 0, false)
-    FL_CASE(1, 256, 0, false)
-    FL_CASE(1, 128, 1, false)
-    FL_CASE(1, 256, 1, false)
-    FL_CASE(1, 128, 2, false)
-    FL_CASE(1, 256, 2, false)
-    FL_CASE(1, 128, 3, false)
-    FL_CASE(1, 256, 3, false)
+    FL_CASE(1, 128, 0, false) FL_CASE(1, 256, 0, false) FL_CASE(1, 128, 1, false) FL_CASE(1, 256, 1, false)
+    FL_CASE(1, 128, 2, false) FL_CASE(1, 256, 2, false) FL_CASE(1, 128, 3, false) FL_CASE(1, 256, 3, false)
     FL_CASE(1, 128, 1, true)
+#undef FL_CASE
+#define FL_CASE(DT, BN, PRO) \
+    if (dt == DT && bn == BN && pro == PRO && !dual && multi) return fl::launch_gemm<DT, BN, PRO, false, true>(p, grid, s);
+    FL_CASE(0, 128, 1) FL_CASE(0, 256, 1) FL_CASE(0, 128, 2) FL_CASE(0, 256, 2)
+    FL_CASE(1, 128, 1) FL_CASE(1, 256, 1) FL_CASE(1, 128, 2) FL_CASE(1, 256, 2)
 #undef FL_CASE
     return cudaErrorInvalidValue;
 }
 
-cudaError_t dispatch_splitk(int dt, int bn, int pro, bool dual, const GemmParams& p, int grid, int splits,
+cudaError_t dispatch_splitk(int dt, int bn, int pro, bool dual, const GemmParamsMulti& p, int grid, int splits,
                             cudaStream_t s) {
+    if (p.n_out > 1) {
+#define FL_CASE(DT, BN, PRO) \
+        if (dt == DT && bn == BN && pro == PRO && !dual)   \
+            return fl::launch_splitk<DT, BN, PRO, false, true>(p, grid, splits, s);
+        FL_CASE(0, 64, 1) FL_CASE(0, 64, 2) FL_CASE(0, 128, 1) FL_CASE(0, 128, 2)
+        FL_CASE(1, 64, 1) FL_CASE(1, 64, 2) FL_CASE(1, 128, 1) FL_CASE(1, 128, 2)
+#undef FL_CASE
+        return cudaErrorInvalidValue;
+    }
     if (dual) {
         if (pro != fl::PRO_RMS) return cudaErrorInvalidValue;
         if (bn == 64) return dt == 0 ? fl::launch_splitk<0, 64, fl::PRO_RMS, true>(p, grid, splits, s)
@@ -392,7 +399,17 @@ int pair_max(int dt, int bn, int pro, int ks) {
     return v;
 }
 
-cudaError_t dispatch_pair(int dt, int bn, int pro, int ks, bool dual, const GemmParams& p, int grid, cudaStream_t s) {
+cudaError_t dispatch_pair(int dt, int bn, int pro, int ks, bool dual, const GemmParamsMulti& p, int grid,
+                          cudaStream_t s) {
+    if (p.n_out > 1) {
+#define FL_CASE(DT, PRO, KS) \
+        if (dt == DT && bn == 256 && pro == PRO && ks == KS && !dual)   \
+            return fl::launch_pair<DT, 256, PRO, KS, false, true>(p, grid, s);
+        FL_CASE(0, 1, 1) FL_CASE(0, 2, 1) FL_CASE(0, 1, 2) FL_CASE(0, 2, 2)
+        FL_CASE(1, 1, 1) FL_CASE(1, 2, 1) FL_CASE(1, 1, 2) FL_CASE(1, 2, 2)
+#undef FL_CASE
+        return cudaErrorInvalidValue;
+    }
     if (dual) {
         if (bn != 256 || pro != fl::PRO_RMS || ks != 1) return cudaErrorInvalidValue;
         return dt == 0 ? fl::launch_pair<0, 256, fl::PRO_RMS, 1, true>(p, grid, s)
@@ -441,7 +458,7 @@ bool use_pair(int dt, int pro, int M, const Outs& outs, int K, PairPlan* plan, b
     const long long mp = (M + 255) / 256;
     const long long t256 = mp * nblocks(outs, 256), t128 = mp * nblocks(outs, 128);
     const int nk = (K + fl::kBK - 1) / fl::kBK;
-    if (variant == 3 && forced_bn == 128) {
+    if (variant == 3 && forced_bn == 128 && outs.n == 1) {
         const int maxp = pair_max(dt, 128, pro, 1);
         if (maxp <= 0) return false;
         *plan = PairPlan{128, 1, (int)(t128 < maxp ? t128 : maxp)};
@@ -464,7 +481,7 @@ bool use_pair(int dt, int pro, int M, const Outs& outs, int K, PairPlan* plan, b
 }
 
 // Fields every launch shares.
-void fill_common(GemmParams& p, const void* A, const void* residual, const void* gamma, const void* beta,
+void fill_common(GemmParamsMulti& p, const void* A, const void* residual, const void* gamma, const void* beta,
                  const void* ln_stats, int M, int K, float eps, DeviceInfo* di) {
     p.ln_stats = ln_stats;
     p.residual = residual;
@@ -480,7 +497,7 @@ void fill_common(GemmParams& p, const void* A, const void* residual, const void*
     p.pdl = g_opt_pdl.load();
 }
 
-fl_status encode_prologue(GemmParams& p, int dt, int pro, const void* gamma, const void* beta, int K) {
+fl_status encode_prologue(GemmParamsMulti& p, int dt, int pro, const void* gamma, const void* beta, int K) {
     fl_status st;
     if (pro != fl::PRO_NONE && (st = encode_2d(&p.tmGamma, dt, gamma, K, 1, fl::kBK, 1, false)) != FL_OK) return st;
     if (pro == fl::PRO_LN && beta != nullptr && (st = encode_2d(&p.tmBeta, dt, beta, K, 1, fl::kBK, 1, false)) != FL_OK)
@@ -492,7 +509,7 @@ fl_status run_pair(int dt, int pro, bool dual, const void* A, const Outs& outs, 
                    const void* gamma, const void* beta, const void* ln_stats, int M, int K, float eps,
                    const PairPlan& plan, DeviceInfo* di, cudaStream_t stream) {
     const int bn = plan.bn;
-    GemmParams p;
+    GemmParamsMulti p;
     memset(&p, 0, sizeof(p));
     fill_common(p, A, residual, gamma, beta, ln_stats, M, K, eps, di);
     fl_status st;
@@ -533,7 +550,7 @@ int choose_bn(int M, const Outs& outs, bool dual, int sms) {
 fl_status run_splitk(int dt, int pro, bool dual, const void* A, const Outs& outs, const void* W2,
                      const void* residual, const void* gamma, const void* beta, const void* ln_stats, int M, int K,
                      float eps, const SplitPlan& plan, DeviceInfo* di, cudaStream_t stream) {
-    GemmParams p;
+    GemmParamsMulti p;
     memset(&p, 0, sizeof(p));
     fill_common(p, A, residual, gamma, beta, ln_stats, M, K, eps, di);
     const int a_rows = plan.a_rows;
@@ -582,7 +599,7 @@ fl_status run_kernels(int dt, int pro, bool dual, const void* A, const Outs& out
     if (plan_splitk(dt, pro, dual, M, outs, K, di->sms, &plan))
         return run_splitk(dt, pro, dual, A, outs, W2, residual, gamma, beta, ln_stats, M, K, eps, plan, di, stream);
     const int bn = choose_bn(M, outs, dual, di->sms);
-    GemmParams p;
+    GemmParamsMulti p;
     memset(&p, 0, sizeof(p));
     fill_common(p, A, residual, gamma, beta, ln_stats, M, K, eps, di);
     if ((st = encode_2d(&p.tmA, dt, A, K, M, fl::kBK, fl::kBM)) != FL_OK) return st;

@@ -29,27 +29,30 @@ constexpr int kBK = 64;
 #endif
 constexpr int kMaxOut = FL_MAX_OUT_PARAMS;
 
-// Parameters of the tile kernel. Passed by value as a __grid_constant__ so the
-// tensor maps sit in parameter space, where TMA may read them.
+// Parameters of one launch. Passed by value as a __grid_constant__ so the
+// tensor maps sit in parameter space, where TMA may read them. The first
+// output's fields are here; a launch with several outputs passes
+// GemmParamsMulti, which appends the others (a single-output launch keeps the
+// smaller block: parameter bytes cost launch time on short kernels, 1.5 us on
+// the 512 x 1024 x 1024 GEMM).
 struct GemmParams {
-    CUtensorMap tmA;             // activation [M, K], box {64, 128}, 128B swizzle
-    CUtensorMap tmB[kMaxOut];    // weight of output i [N_i, K], box {64, BN}, 128B swizzle
-    CUtensorMap tmB2;            // second weight [N, K] of the gate/up kernel (else unused)
-    CUtensorMap tmOut[kMaxOut];  // output i [M, N_i], box {64, 32}, 128B swizzle
+    CUtensorMap tmA;      // activation [M, K], box {64, 128}, 128B swizzle
+    CUtensorMap tmB;      // weight of output 0 [N, K], box {64, BN}, 128B swizzle
+    CUtensorMap tmB2;     // second weight [N, K] of the gate/up kernel (else unused)
+    CUtensorMap tmOut;    // output 0 [M, N], box {64, 32}, 128B swizzle
     CUtensorMap tmGamma;  // gamma (RMS, LayerNorm) or the input bias, as a [1, K] matrix, box {64, 1}
     CUtensorMap tmBeta;   // beta as a [1, K] matrix, box {64, 1} (LayerNorm with beta)
-    const void* bias[kMaxOut];  // output bias [N_i] or null
+    const void* bias;      // output 0 bias [N] or null
     const void* residual;  // [M, N] or null (single-output launches only)
     const void* gamma;     // [K] (prologues)
     const void* beta;      // [K] or null (LayerNorm)
     const void* a_ptr;     // activation [M, K]
     const void* ln_stats;  // LayerNorm: float2 (mean, 1/sqrt(var + eps)) per activation row
-    void* out_ptr[kMaxOut];  // output i [M, N_i] (split-K kernel stores directly)
+    void* out_ptr;         // output 0 [M, N] (split-K kernel stores directly)
     int* status;           // device status word
     unsigned long long timeout_ns;
-    int M, K;
-    int N[kMaxOut];        // columns of output i
-    int act[kMaxOut];      // activation of output i
+    int M, N, K;           // N: columns of output 0
+    int act;               // activation of output 0
     int n_out;             // outputs of this launch (1 .. kMaxOut)
     // first column block (in tiles of this launch's width) of each output;
     // nb0[n_out] is the total, num_n_blocks
@@ -74,6 +77,27 @@ struct GemmParams {
     unsigned long long* trace;  // phase timestamps, builds with FL_TRACE only (else unused, null)
 };
 
+// Outputs 1 .. n_out - 1 of a multi-output launch.
+struct GemmParamsMulti : GemmParams {
+    CUtensorMap tmBx[kMaxOut - 1];
+    CUtensorMap tmOutx[kMaxOut - 1];
+    const void* biasx[kMaxOut - 1];
+    void* out_ptrx[kMaxOut - 1];
+    int Nx[kMaxOut - 1];
+    int actx[kMaxOut - 1];
+};
+
+template <bool MULTI>
+struct ParamsOf {
+    using type = GemmParams;
+};
+template <>
+struct ParamsOf<true> {
+    using type = GemmParamsMulti;
+};
+template <bool MULTI>
+using ParamsT = typename ParamsOf<MULTI>::type;
+
 // Records a status message for fl_last_error() on this thread; returns status.
 int set_last_error(int status, const char* message);
 
@@ -86,17 +110,17 @@ cudaError_t launch_rms_norm(int dt, const void* x, const void* gamma, void* y, i
                             int sms, cudaStream_t stream);
 
 // Kernel launchers, explicitly instantiated in the kernel translation units.
-template <int DT, int BN, int PRO, bool DUAL>
-cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream);
+template <int DT, int BN, int PRO, bool DUAL, bool MULTI = false>
+cudaError_t launch_gemm(const ParamsT<MULTI>& p, int grid, cudaStream_t stream);
 
-template <int DT, int BN, int PRO, bool DUAL = false>
-cudaError_t launch_splitk(const GemmParams& p, int grid, int splits, cudaStream_t stream);
+template <int DT, int BN, int PRO, bool DUAL = false, bool MULTI = false>
+cudaError_t launch_splitk(const ParamsT<MULTI>& p, int grid, int splits, cudaStream_t stream);
 
 template <int DT, int BN, int PRO, bool DUAL = false>
 int splitk_max_clusters(int splits, int smem_bytes);
 
-template <int DT, int BN, int PRO, int KS, bool DUAL>
-cudaError_t launch_pair(const GemmParams& p, int grid, cudaStream_t stream);
+template <int DT, int BN, int PRO, int KS, bool DUAL, bool MULTI = false>
+cudaError_t launch_pair(const ParamsT<MULTI>& p, int grid, cudaStream_t stream);
 
 template <int DT, int BN, int PRO, int KS>
 int pair_max_clusters();

@@ -80,9 +80,9 @@ struct PairCfg {
 // [n0, n0 + 128) of Wg (even CTA) stacked over the same rows of Wu (odd CTA),
 // so one 256 x 256 MMA yields gate | up for 128 output columns, and the
 // epilogue writes silu(gate) * up.
-template <int DT, int BN, int PRO, int KS, bool DUAL>
+template <int DT, int BN, int PRO, int KS, bool DUAL, bool MULTI>
 __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
-    fl_pair_kernel(const __grid_constant__ GemmParams p) {
+    fl_pair_kernel(const __grid_constant__ ParamsT<MULTI> p) {
     using C = PairCfg<BN, PRO, KS>;
     static_assert(!DUAL || (BN == 256 && KS == 1), "gate/up pairs use 256-wide tiles without a K split");
     constexpr int OUT_COLS = DUAL ? BN / 2 : BN;  // output columns of a tile
@@ -188,8 +188,8 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&p.tmA);
         for (int i = 0; i < p.n_out; ++i) {
-            tma_prefetch_desc(&p.tmB[i]);
-            tma_prefetch_desc(&p.tmOut[i]);
+            tma_prefetch_desc(tm_b(p, i));
+            tma_prefetch_desc(tm_out(p, i));
         }
         if (DUAL) tma_prefetch_desc(&p.tmB2);
         if (PRO != PRO_NONE) tma_prefetch_desc(&p.tmGamma);
@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     if (warp == 0 && lane == 0 && t_begin < t_end) {
         const OutSel o = out_sel(p, tile_nb(t_begin));
         const int nh = DUAL ? o.nb * OUT_COLS : o.nb * C::BN + (int)rank * C::HALF;
-        const CUtensorMap* tb = DUAL && rank ? &p.tmB2 : &p.tmB[o.oi];
+        const CUtensorMap* tb = DUAL && rank ? &p.tmB2 : tm_b(p, o.oi);
         for (int kb = kb_begin; kb < kb_begin + S && kb < kb_end; ++kb) tma_prefetch_2d(tb, kb * kBK, nh);
     }
     // LayerNorm: this grid directly follows the row-statistics kernel, which
@@ -232,10 +232,10 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     // broadcast shared loads instead of global loads on its critical path.
     auto stage_bias = [&](int n0, int q, int oi) -> uint32_t {
         const uint32_t buf = sbase + C::OFF_BIAS + (uint32_t)(q * C::BN * 2);
-        if (p.bias[oi] != nullptr) {
-            const uint16_t* b = reinterpret_cast<const uint16_t*>(p.bias[oi]);
+        if (out_bias(p, oi) != nullptr) {
+            const uint16_t* b = reinterpret_cast<const uint16_t*>(out_bias(p, oi));
             for (int c = (int)(threadIdx.x & 31) * 8; c < C::BN; c += 256) {
-                const uint4 v = n0 + c < p.N[oi] ? ldg_v4(b + n0 + c) : make_uint4(0u, 0u, 0u, 0u);
+                const uint4 v = n0 + c < out_n(p, oi) ? ldg_v4(b + n0 + c) : make_uint4(0u, 0u, 0u, 0u);
                 st_shared_v4(buf + (uint32_t)c * 2u, v.x, v.y, v.z, v.w);
             }
         }
@@ -373,7 +373,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                 // tile's rows of Wg / Wu
                 const OutSel o = out_sel(p, tile_nb(tile));
                 const int nh = DUAL ? o.nb * OUT_COLS : o.nb * C::BN + (int)rank * C::HALF;
-                const CUtensorMap* tb = DUAL && rank ? &p.tmB2 : &p.tmB[o.oi];
+                const CUtensorMap* tb = DUAL && rank ? &p.tmB2 : tm_b(p, o.oi);
                 for (int kb = kb_begin; kb < kb_end; ++kb) {
                     if (!wait_bar(empty_bar(s), ph ^ 1u, p.status, p.timeout_ns, 31)) {
                         ok = false;
@@ -549,14 +549,14 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         const int m0 = tile_mb(tile) * 2 * kBM + (int)rank * kBM;
         const OutSel osel = out_sel(p, tile_nb(tile));
         const int n0 = osel.nb * C::BN;
-        const int N = p.N[osel.oi];
-        const int act = p.act[osel.oi];
+        const int N = out_n(p, osel.oi);
+        const int act = out_act(p, osel.oi);
         const int own_c0 = khalf * HALF_N, oth_c0 = (1 - khalf) * HALF_N;
         const uint32_t bias_s = stage_bias(n0, q, osel.oi);
         const uint32_t tl = tmem_base + ((uint32_t)(q * 32) << 16);
         const uint32_t row_off = (uint32_t)(rl * C::XROW) * 4u;  // within a chunk
         using T = uint16_t;
-        const T* bias = reinterpret_cast<const T*>(p.bias[osel.oi]);
+        const T* bias = reinterpret_cast<const T*>(out_bias(p, osel.oi));
         const T* res = reinterpret_cast<const T*>(p.residual);
         bool ok = true;
         float ss_upper = 0.f;  // RMS, shared fold: the row's sum of squares over this warpgroup's share
@@ -693,7 +693,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&p.tmOut[osel.oi], sbuf, col0, m0 + q * 32);
+                        tma_store_2d(tm_out(p, osel.oi), sbuf, col0, m0 + q * 32);
                         bulk_commit_group();
                     }
                 }
@@ -721,9 +721,9 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
             const int m0 = tile_mb(tile) * 2 * kBM + (int)rank * kBM;
             const OutSel osel = out_sel(p, tile_nb(tile));
             const int n0 = osel.nb * OUT_COLS;
-            const int N = p.N[osel.oi];
-            const int act = p.act[osel.oi];
-            const T* bias = reinterpret_cast<const T*>(p.bias[osel.oi]);
+            const int N = out_n(p, osel.oi);
+            const int act = out_act(p, osel.oi);
+            const T* bias = reinterpret_cast<const T*>(out_bias(p, osel.oi));
             const int buf = C::NBUF == 2 ? (it & 1) : 0;
             const uint32_t tph = C::NBUF == 2 ? (uint32_t)((it >> 1) & 1) : (uint32_t)(it & 1);
             const uint32_t bias_s = stage_bias(n0, q, osel.oi);
@@ -839,7 +839,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&p.tmOut[osel.oi], ebuf, col0, m0 + q * 32);
+                        tma_store_2d(tm_out(p, osel.oi), ebuf, col0, m0 + q * 32);
                         bulk_commit_group();
                     }
                 }
@@ -865,7 +865,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
 template <int DT, int BN, int PRO, int KS>
 int pair_max_clusters() {
     using C = PairCfg<BN, PRO, KS>;
-    auto kern = fl_pair_kernel<DT, BN, PRO, KS, false>;
+    auto kern = fl_pair_kernel<DT, BN, PRO, KS, false, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg = {};
@@ -887,10 +887,10 @@ int pair_max_clusters() {
     return n;
 }
 
-template <int DT, int BN, int PRO, int KS, bool DUAL>
-cudaError_t launch_pair(const GemmParams& p, int grid, cudaStream_t stream) {
+template <int DT, int BN, int PRO, int KS, bool DUAL, bool MULTI>
+cudaError_t launch_pair(const ParamsT<MULTI>& p, int grid, cudaStream_t stream) {
     using C = PairCfg<BN, PRO, KS>;
-    auto kern = fl_pair_kernel<DT, BN, PRO, KS, DUAL>;
+    auto kern = fl_pair_kernel<DT, BN, PRO, KS, DUAL, MULTI>;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);

@@ -41,9 +41,9 @@ namespace fl {
 template <int PRO>
 constexpr int splitk_threads() { return PRO != PRO_NONE ? 320 : 256; }
 
-template <int DT, int BN, int PRO, bool DUAL>
+template <int DT, int BN, int PRO, bool DUAL, bool MULTI>
 __global__ void __launch_bounds__(splitk_threads<PRO>(), 1)
-    fl_splitk_kernel(const __grid_constant__ GemmParams p) {
+    fl_splitk_kernel(const __grid_constant__ ParamsT<MULTI> p) {
     if (threadIdx.x == 0) FL_MARK(p, 0);
     using C = SplitCfg<BN, DUAL>;
     static_assert(!DUAL || PRO == PRO_RMS, "the gate/up kernel has the RMS prologue");
@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(splitk_threads<PRO>(), 1)
     const int m0 = (tile % p.num_m_blocks) * kBM;
     const OutSel osel = out_sel(p, tile / p.num_m_blocks);
     const int n0 = osel.nb * BN;
-    const CUtensorMap* tmB = &p.tmB[osel.oi];
+    const CUtensorMap* tmB = tm_b(p, osel.oi);
     const int nk = p.num_k_blocks;
     const int kb0 = rank * p.kps;
     const int kb1 = min(nk, kb0 + p.kps);
@@ -295,10 +295,10 @@ __global__ void __launch_bounds__(splitk_threads<PRO>(), 1)
             // cache while the main loop runs (a miss there costs an L2
             // round trip on the critical path)
             uint32_t touch = (uint32_t)p.xc_stride ^ p.xc_owner[lane] ^ p.xc_pos[lane] ^ p.xc_c0[lane & 7] ^
-                             __float_as_uint(p.inv_k) ^ __float_as_uint(p.eps) ^ (uint32_t)p.act[osel.oi] ^
-                             (uint32_t)p.N[osel.oi] ^ (uint32_t)reinterpret_cast<uintptr_t>(p.residual) ^
-                             (uint32_t)reinterpret_cast<uintptr_t>(p.out_ptr[osel.oi]) ^
-                             (uint32_t)reinterpret_cast<uintptr_t>(p.bias[osel.oi]);
+                             __float_as_uint(p.inv_k) ^ __float_as_uint(p.eps) ^ (uint32_t)out_act(p, osel.oi) ^
+                             (uint32_t)out_n(p, osel.oi) ^ (uint32_t)reinterpret_cast<uintptr_t>(p.residual) ^
+                             (uint32_t)reinterpret_cast<uintptr_t>(out_ptr(p, osel.oi)) ^
+                             (uint32_t)reinterpret_cast<uintptr_t>(out_bias(p, osel.oi));
             asm volatile("" ::"r"(touch));
         }
 
@@ -418,9 +418,9 @@ __global__ void __launch_bounds__(splitk_threads<PRO>(), 1)
     const int xsh = xw > 8 ? 4 : 3;
     const int xch = threadIdx.x & ((1 << xsh) - 1);
     const int xcol = n0 + (xc0 + xch) * 8;
-    const int N = p.N[osel.oi];
-    const int act = p.act[osel.oi];
-    const void* obias = p.bias[osel.oi];
+    const int N = out_n(p, osel.oi);
+    const int act = out_act(p, osel.oi);
+    const void* obias = out_bias(p, osel.oi);
     const bool xmine = xch < xw && xcol < N;
     float bb[8];
 #pragma unroll
@@ -442,7 +442,7 @@ __global__ void __launch_bounds__(splitk_threads<PRO>(), 1)
     if (xchg_ok && xmine) {
         using T = uint16_t;
         const T* res = reinterpret_cast<const T*>(p.residual);
-        T* out = reinterpret_cast<T*>(p.out_ptr[osel.oi]);
+        T* out = reinterpret_cast<T*>(out_ptr(p, osel.oi));
         const int stride = p.xc_stride;
         const uint32_t slot_bytes = (uint32_t)(rows * stride) * 4u;
         const int nthreads = (int)blockDim.x;
@@ -513,10 +513,10 @@ __global__ void __launch_bounds__(splitk_threads<PRO>(), 1)
     }
 }
 
-template <int DT, int BN, int PRO, bool DUAL>
+template <int DT, int BN, int PRO, bool DUAL, bool MULTI>
 cudaError_t splitk_configure() {
     static cudaError_t state = [] {
-        auto kern = fl_splitk_kernel<DT, BN, PRO, DUAL>;
+        auto kern = fl_splitk_kernel<DT, BN, PRO, DUAL, MULTI>;
         cudaError_t e =
             cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SplitCfg<BN, DUAL>::SMEM_MAX);
         if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
@@ -529,8 +529,8 @@ cudaError_t splitk_configure() {
 // of dynamic shared memory, can be resident at once.
 template <int DT, int BN, int PRO, bool DUAL>
 int splitk_max_clusters(int splits, int smem_bytes) {
-    if (splitk_configure<DT, BN, PRO, DUAL>() != cudaSuccess) return 0;
-    auto kern = fl_splitk_kernel<DT, BN, PRO, DUAL>;
+    if (splitk_configure<DT, BN, PRO, DUAL, false>() != cudaSuccess) return 0;
+    auto kern = fl_splitk_kernel<DT, BN, PRO, DUAL, false>;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(splits, 1, 1);
     cfg.blockDim = dim3(splitk_threads<PRO>(), 1, 1);
@@ -550,11 +550,11 @@ int splitk_max_clusters(int splits, int smem_bytes) {
     return n;
 }
 
-template <int DT, int BN, int PRO, bool DUAL>
-cudaError_t launch_splitk(const GemmParams& p, int grid, int splits, cudaStream_t stream) {
+template <int DT, int BN, int PRO, bool DUAL, bool MULTI>
+cudaError_t launch_splitk(const ParamsT<MULTI>& p, int grid, int splits, cudaStream_t stream) {
     using C = SplitCfg<BN, DUAL>;
-    auto kern = fl_splitk_kernel<DT, BN, PRO, DUAL>;
-    cudaError_t e = splitk_configure<DT, BN, PRO, DUAL>();
+    auto kern = fl_splitk_kernel<DT, BN, PRO, DUAL, MULTI>;
+    cudaError_t e = splitk_configure<DT, BN, PRO, DUAL, MULTI>();
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
