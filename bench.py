@@ -478,6 +478,7 @@ def run_ours(args, w: dict, rank: int, world: int, local: int):
     # the benchmark's weights are never written: the small-M kernel may stage
     # them before its programmatic dependency on the previous step resolves
     fl.set_option("weight_preload", 0 if args.no_weight_preload else 1)
+    fl.set_option("launch_cache", 0 if args.no_launch_cache else 1)
     dev = torch.device("cuda", local)
     t = make_inputs(w)
     set_bytes = sum(v.numel() * v.element_size() for v in t.values() if v is not None)
@@ -674,6 +675,8 @@ def main(argv=None):
     ap.add_argument("--variant", type=int, default=0, help="force 1 = tile kernel, 2 = small-M split-K kernel")
     ap.add_argument("--split-k", type=int, default=0, help="force the K split of the small-M kernel")
     ap.add_argument("--no-graph", action="store_true", help="time plain stream calls instead of graph replays")
+    ap.add_argument("--no-launch-cache", action="store_true",
+                    help="prepare every call afresh (FL_OPT_LAUNCH_CACHE off): host cost without the cache")
     ap.add_argument("--separate", action="store_true",
                     help="multi workloads: one fl_norm_gemm call per weight instead of one fl_norm_gemm_multi call")
     ap.add_argument("--load-seconds", type=float, default=0.3,

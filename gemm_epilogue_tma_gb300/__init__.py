@@ -29,7 +29,8 @@ ACTS = {"none": 0, "gelu": 1, "silu": 2, "relu": 3}
 DTYPE_CODES = {"f16": 0, "bf16": 1}
 STATUS_NAMES = {0: "FL_OK", 1: "FL_ERR_INVALID_ARG", 2: "FL_ERR_UNSUPPORTED", 3: "FL_ERR_ALIGNMENT",
                 4: "FL_ERR_WORKSPACE", 5: "FL_ERR_CUDA", 6: "FL_ERR_TIMEOUT"}
-OPTIONS = {"tile_n": 0, "variant": 1, "timeout_ms": 2, "split_k": 3, "pdl": 4, "weight_preload": 5}
+OPTIONS = {"tile_n": 0, "variant": 1, "timeout_ms": 2, "split_k": 3, "pdl": 4, "weight_preload": 5,
+           "launch_cache": 6}
 
 class LayerDesc(ctypes.Structure):
     """fl_layer_desc: sizes, dtype, eps and the device pointers of one decoder layer's dense part."""
@@ -54,6 +55,8 @@ SIGNATURES = {
     "fl_layer_launch": (_i, [_vp, _i, _vp]),
     "fl_layer_issue": (_i, [_vp, _i, _vp]),
     "fl_layer_destroy": (None, [_vp]),
+    "fl_launch_cache_stats": (_i, [ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_longlong)]),
+    "fl_launch_cache_clear": (None, []),
     "fl_last_error": (ctypes.c_char_p, []),
     "fl_device_status": (_i, [_vp]),
     "fl_set_option": (_i, [_i, _i]),
@@ -305,6 +308,17 @@ def swiglu_ffn_noalloc(x, gamma, Wg, Wu, Wd, bias_down=None, out=None, eps=1e-6,
     _check(lib().fl_swiglu_ffn_noalloc(_ptr(x), _ptr(gamma), _ptr(Wg), _ptr(Wu), _ptr(Wd), _ptr(bias_down),
                                        _ptr(out), M, D, F, float(eps), _dtype_code(x), _stream(stream)))
     return out
+
+
+def launch_cache_stats():
+    """(hits, misses) of the host-side launch cache since the library was loaded."""
+    h, m = ctypes.c_longlong(), ctypes.c_longlong()
+    _check(lib().fl_launch_cache_stats(ctypes.byref(h), ctypes.byref(m)))
+    return h.value, m.value
+
+
+def launch_cache_clear() -> None:
+    lib().fl_launch_cache_clear()
 
 
 def device_status(stream=None) -> None:

@@ -47,6 +47,7 @@ std::atomic<int> g_opt_timeout_ms{2000};
 std::atomic<int> g_opt_split_k{0};
 std::atomic<int> g_opt_pdl{1};
 std::atomic<int> g_opt_preload{0};
+std::atomic<int> g_opt_cache{1};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -108,6 +109,12 @@ fl_status device_info(DeviceInfo** out) {
                     d.minor);
     *out = &d;
     return FL_OK;
+}
+
+int device_index() {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    return dev;
 }
 
 // ---------------------------------------------------------------------------
@@ -505,13 +512,22 @@ fl_status encode_prologue(GemmParamsMulti& p, int dt, int pro, const void* gamma
     return FL_OK;
 }
 
-fl_status run_pair(int dt, int pro, bool dual, const void* A, const Outs& outs, const void* W2, const void* residual,
-                   const void* gamma, const void* beta, const void* ln_stats, int M, int K, float eps,
-                   const PairPlan& plan, DeviceInfo* di, cudaStream_t stream) {
-    const int bn = plan.bn;
+// A launch whose parameters are built: the kernel family, its template
+// arguments, the grid and the parameter block (tensor maps encoded).
+enum LaunchPath : int { PATH_TILE = 0, PATH_SPLITK = 1, PATH_PAIR = 2 };
+struct Prepared {
+    int path, dt, pro, bn, ks, splits, grid;
+    bool dual;
     GemmParamsMulti p;
+};
+
+fl_status prepare_pair(int dt, int pro, bool dual, const void* A, const Outs& outs, const void* W2,
+                       const void* residual, const void* gamma, const void* beta, int M, int K, float eps,
+                       const PairPlan& plan, DeviceInfo* di, Prepared* out) {
+    const int bn = plan.bn;
+    GemmParamsMulti& p = out->p;
     memset(&p, 0, sizeof(p));
-    fill_common(p, A, residual, gamma, beta, ln_stats, M, K, eps, di);
+    fill_common(p, A, residual, gamma, beta, nullptr, M, K, eps, di);
     fl_status st;
     if ((st = encode_2d(&p.tmA, dt, A, K, M, fl::kBK, fl::kBM)) != FL_OK) return st;
     // output columns of a tile: the pair's 256-row weight tile holds bn
@@ -523,12 +539,11 @@ fl_status run_pair(int dt, int pro, bool dual, const void* A, const Outs& outs, 
     p.num_tiles = p.num_m_blocks * p.num_n_blocks;
     p.splits = plan.ks;
     p.kps = (p.num_k_blocks + plan.ks - 1) / plan.ks;
-#ifdef FL_TRACE
-    if (const char* tp = getenv("FL_TRACE_PTR")) p.trace = reinterpret_cast<unsigned long long*>(strtoull(tp, nullptr, 10));
-#endif
-    cudaError_t e = dispatch_pair(dt, bn, pro, plan.ks, dual, p, 2 * plan.ks * plan.clusters, stream);
-    if (e != cudaSuccess) return fail(FL_ERR_CUDA, "pair kernel launch failed: %s", cudaGetErrorString(e));
-    return ok();
+    out->path = PATH_PAIR;
+    out->bn = bn;
+    out->ks = plan.ks;
+    out->grid = 2 * plan.ks * plan.clusters;
+    return FL_OK;
 }
 
 // CTA tile width. A wider tile halves the activation re-reads and the shared
@@ -547,12 +562,12 @@ int choose_bn(int M, const Outs& outs, bool dual, int sms) {
     return c256 <= c128 ? 256 : 128;
 }
 
-fl_status run_splitk(int dt, int pro, bool dual, const void* A, const Outs& outs, const void* W2,
-                     const void* residual, const void* gamma, const void* beta, const void* ln_stats, int M, int K,
-                     float eps, const SplitPlan& plan, DeviceInfo* di, cudaStream_t stream) {
-    GemmParamsMulti p;
+fl_status prepare_splitk(int dt, int pro, bool dual, const void* A, const Outs& outs, const void* W2,
+                         const void* residual, const void* gamma, const void* beta, int M, int K, float eps,
+                         const SplitPlan& plan, DeviceInfo* di, Prepared* out) {
+    GemmParamsMulti& p = out->p;
     memset(&p, 0, sizeof(p));
-    fill_common(p, A, residual, gamma, beta, ln_stats, M, K, eps, di);
+    fill_common(p, A, residual, gamma, beta, nullptr, M, K, eps, di);
     const int a_rows = plan.a_rows;
     fl_status st;
     if ((st = encode_2d(&p.tmA, dt, A, K, M, fl::kBK, a_rows)) != FL_OK) return st;
@@ -579,39 +594,153 @@ fl_status run_splitk(int dt, int pro, bool dual, const void* A, const Outs& outs
         p.xc_stride = (nch + s - 1) / s * 8 * (dual ? 2 : 1) + 4;  // SplitCfg::xchg_stride
         p.inv_k = 1.0f / (float)K;
     }
-#ifdef FL_TRACE
-    if (const char* tp = getenv("FL_TRACE_PTR")) p.trace = reinterpret_cast<unsigned long long*>(strtoull(tp, nullptr, 10));
-#endif
-    const int grid = p.num_tiles * plan.splits;
-    cudaError_t e = dispatch_splitk(dt, plan.bn, pro, dual, p, grid, plan.splits, stream);
-    if (e != cudaSuccess) return fail(FL_ERR_CUDA, "split-K kernel launch failed: %s", cudaGetErrorString(e));
-    return ok();
+    out->path = PATH_SPLITK;
+    out->bn = plan.bn;
+    out->splits = plan.splits;
+    out->grid = p.num_tiles * plan.splits;
+    return FL_OK;
 }
 
-fl_status run_kernels(int dt, int pro, bool dual, const void* A, const Outs& outs, const void* W2,
-                      const void* residual, const void* gamma, const void* beta, const void* ln_stats, int M, int K,
-                      float eps, DeviceInfo* di, cudaStream_t stream) {
-    fl_status st;
+fl_status prepare_kernels(int dt, int pro, bool dual, const void* A, const Outs& outs, const void* W2,
+                          const void* residual, const void* gamma, const void* beta, int M, int K, float eps,
+                          DeviceInfo* di, Prepared* out) {
+    out->dt = dt;
+    out->pro = pro;
+    out->dual = dual;
+    out->ks = out->splits = 1;
     PairPlan pplan;
     if (use_pair(dt, pro, M, outs, K, &pplan, dual))
-        return run_pair(dt, pro, dual, A, outs, W2, residual, gamma, beta, ln_stats, M, K, eps, pplan, di, stream);
+        return prepare_pair(dt, pro, dual, A, outs, W2, residual, gamma, beta, M, K, eps, pplan, di, out);
     SplitPlan plan;
     if (plan_splitk(dt, pro, dual, M, outs, K, di->sms, &plan))
-        return run_splitk(dt, pro, dual, A, outs, W2, residual, gamma, beta, ln_stats, M, K, eps, plan, di, stream);
+        return prepare_splitk(dt, pro, dual, A, outs, W2, residual, gamma, beta, M, K, eps, plan, di, out);
     const int bn = choose_bn(M, outs, dual, di->sms);
-    GemmParamsMulti p;
+    GemmParamsMulti& p = out->p;
     memset(&p, 0, sizeof(p));
-    fill_common(p, A, residual, gamma, beta, ln_stats, M, K, eps, di);
+    fill_common(p, A, residual, gamma, beta, nullptr, M, K, eps, di);
+    fl_status st;
     if ((st = encode_2d(&p.tmA, dt, A, K, M, fl::kBK, fl::kBM)) != FL_OK) return st;
     if ((st = fill_outputs(p, dt, outs, M, K, bn, bn)) != FL_OK) return st;
     if (dual && (st = encode_2d(&p.tmB2, dt, W2, K, outs.o[0].N, fl::kBK, bn)) != FL_OK) return st;
     if ((st = encode_prologue(p, dt, pro, gamma, beta, K)) != FL_OK) return st;
     p.num_m_blocks = (M + fl::kBM - 1) / fl::kBM;
     p.num_tiles = p.num_m_blocks * p.num_n_blocks;
-    const int grid = p.num_tiles < di->sms ? p.num_tiles : di->sms;
-    cudaError_t e = dispatch_tile(dt, bn, pro, dual, p, grid, stream);
-    if (e != cudaSuccess) return fail(FL_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+    out->path = PATH_TILE;
+    out->bn = bn;
+    out->grid = p.num_tiles < di->sms ? p.num_tiles : di->sms;
+    return FL_OK;
+}
+
+fl_status launch_prepared(const Prepared& L, cudaStream_t stream) {
+    cudaError_t e;
+    const char* what;
+    if (L.path == PATH_PAIR) {
+        e = dispatch_pair(L.dt, L.bn, L.pro, L.ks, L.dual, L.p, L.grid, stream);
+        what = "pair kernel launch failed";
+    } else if (L.path == PATH_SPLITK) {
+        e = dispatch_splitk(L.dt, L.bn, L.pro, L.dual, L.p, L.grid, L.splits, stream);
+        what = "split-K kernel launch failed";
+    } else {
+        e = dispatch_tile(L.dt, L.bn, L.pro, L.dual, L.p, L.grid, stream);
+        what = "kernel launch failed";
+    }
+    if (e != cudaSuccess) return fail(FL_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
     return ok();
+}
+
+// ---------------------------------------------------------------------------
+// launch cache
+// ---------------------------------------------------------------------------
+// A call repeated with the same pointers, sizes and options (every step of a
+// decode loop, every layer of a model) gets the same kernel choice and the
+// same tensor maps: those are kept per argument set, so a repeated call only
+// validates, looks up and launches. Key: everything the preparation reads,
+// compared byte for byte (the key is zeroed before it is filled, so padding
+// compares equal).
+struct CallKey {
+    int device, dt, pro, dual, M, K, n;
+    uint32_t eps_bits;
+    const void *A, *W2, *residual, *gamma, *beta;
+    OutDesc o[fl::kMaxOut];
+    int opt_tile_n, opt_variant, opt_split_k, opt_pdl, opt_preload, opt_timeout_ms;
+};
+
+constexpr int kCacheSlots = 64;
+struct CacheSlot {
+    bool used = false;
+    CallKey key;
+    Prepared prep;
+};
+CacheSlot g_cache[kCacheSlots];
+std::mutex g_cache_mu;
+std::atomic<long long> g_cache_hits{0}, g_cache_misses{0};
+
+uint64_t hash_bytes(const void* data, size_t n) {
+    const unsigned char* b = static_cast<const unsigned char*>(data);
+    uint64_t h = 1469598103934665603ull;  // FNV-1a
+    for (size_t i = 0; i < n; ++i) {
+        h ^= b[i];
+        h *= 1099511628211ull;
+    }
+    return h;
+}
+
+fl_status run_kernels(int dt, int pro, bool dual, const void* A, const Outs& outs, const void* W2,
+                      const void* residual, const void* gamma, const void* beta, const void* ln_stats, int M, int K,
+                      float eps, DeviceInfo* di, int device, cudaStream_t stream) {
+    CallKey key;
+    memset(&key, 0, sizeof(key));
+    key.device = device;
+    key.dt = dt;
+    key.pro = pro;
+    key.dual = dual;
+    key.M = M;
+    key.K = K;
+    key.n = outs.n;
+    memcpy(&key.eps_bits, &eps, sizeof(float));
+    key.A = A;
+    key.W2 = W2;
+    key.residual = residual;
+    key.gamma = gamma;
+    key.beta = beta;
+    for (int i = 0; i < outs.n; ++i) key.o[i] = outs.o[i];
+    key.opt_tile_n = g_opt_tile_n.load();
+    key.opt_variant = g_opt_variant.load();
+    key.opt_split_k = g_opt_split_k.load();
+    key.opt_pdl = g_opt_pdl.load();
+    key.opt_preload = g_opt_preload.load();
+    key.opt_timeout_ms = g_opt_timeout_ms.load();
+    CacheSlot& slot = g_cache[hash_bytes(&key, sizeof(key)) % kCacheSlots];
+    // one prepared launch per call on the stack (about 2 KB)
+    Prepared prep;
+    bool hit = false;
+    const bool use_cache = g_opt_cache.load() != 0;
+    if (use_cache) {
+        std::lock_guard<std::mutex> lk(g_cache_mu);
+        if (slot.used && memcmp(&slot.key, &key, sizeof(key)) == 0) {
+            prep = slot.prep;
+            hit = true;
+        }
+    }
+    if (hit) {
+        g_cache_hits.fetch_add(1, std::memory_order_relaxed);
+    } else {
+        g_cache_misses.fetch_add(1, std::memory_order_relaxed);
+        fl_status st = prepare_kernels(dt, pro, dual, A, outs, W2, residual, gamma, beta, M, K, eps, di, &prep);
+        if (st != FL_OK) return st;
+        if (use_cache) {
+            std::lock_guard<std::mutex> lk(g_cache_mu);
+            slot.key = key;
+            slot.prep = prep;
+            slot.used = true;
+        }
+    }
+    prep.p.ln_stats = ln_stats;  // per-call scratch, not part of the key
+#ifdef FL_TRACE
+    if (const char* tp = getenv("FL_TRACE_PTR"))
+        prep.p.trace = reinterpret_cast<unsigned long long*>(strtoull(tp, nullptr, 10));
+#endif
+    return launch_prepared(prep, stream);
 }
 
 // One fused call. LayerNorm first computes the row statistics (8 bytes per
@@ -633,7 +762,7 @@ fl_status run_tile(int dt, int pro, bool dual, const void* A, const Outs& outs, 
             return fail(FL_ERR_CUDA, "LayerNorm statistics kernel launch failed: %s", cudaGetErrorString(e));
         }
     }
-    st = run_kernels(dt, pro, dual, A, outs, W2, residual, gamma, beta, stats, M, K, eps, di, stream);
+    st = run_kernels(dt, pro, dual, A, outs, W2, residual, gamma, beta, stats, M, K, eps, di, device_index(), stream);
     if (stats != nullptr) cudaFreeAsync(stats, stream);
     return st;
 }
@@ -697,6 +826,10 @@ fl_status fl_set_option(fl_option key, int value) {
         case FL_OPT_WEIGHT_PRELOAD:
             if (value < 0 || value > 1) return fail(FL_ERR_INVALID_ARG, "weight preload must be 0 or 1");
             g_opt_preload = value;
+            return ok();
+        case FL_OPT_LAUNCH_CACHE:
+            if (value < 0 || value > 1) return fail(FL_ERR_INVALID_ARG, "launch cache must be 0 or 1");
+            g_opt_cache = value;
             return ok();
         default:
             return fail(FL_ERR_INVALID_ARG, "unknown option %d", (int)key);
@@ -891,6 +1024,18 @@ fl_status fl_swiglu_ffn(const void* x, const void* gamma, const void* Wg, const 
     // down: out = h Wd^T (+ bias_down) + x
     return run_tile(dtype, fl::PRO_NONE, false, workspace, single_out(Wd, bias_down, out, D, fl::ACT_NONE), nullptr, x,
                     nullptr, nullptr, M, F, 0.f, s);
+}
+
+fl_status fl_launch_cache_stats(long long* hits, long long* misses) {
+    if (hits == nullptr || misses == nullptr) return fail(FL_ERR_INVALID_ARG, "null output pointer");
+    *hits = g_cache_hits.load();
+    *misses = g_cache_misses.load();
+    return ok();
+}
+
+void fl_launch_cache_clear(void) {
+    std::lock_guard<std::mutex> lk(g_cache_mu);
+    for (CacheSlot& c : g_cache) c.used = false;
 }
 
 fl_status fl_device_status(void* stream) {

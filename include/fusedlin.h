@@ -314,6 +314,11 @@ fl_status fl_device_status(void* stream);
  *                       dependency on the previous kernel of the stream, so its
  *                       set-up overlaps that kernel's tail (all of its memory
  *                       accesses still wait for it); 0 = plain stream order.
+ *   FL_OPT_LAUNCH_CACHE: 1 (default) = keep the prepared launch (kernel choice
+ *                       and encoded tensor maps) of each recent argument set,
+ *                       so a call repeated with the same pointers, sizes and
+ *                       options skips that host work (see fl_launch_cache_stats);
+ *                       0 = prepare every call afresh.
  *   FL_OPT_WEIGHT_PRELOAD: 0 (default) or 1. With 1 the caller promises that
  *                       no kernel on the stream writes the weight matrix W
  *                       between its last host-ordered write and this call (the
@@ -334,9 +339,26 @@ typedef enum {
     FL_OPT_TIMEOUT_MS = 2,
     FL_OPT_SPLIT_K = 3,
     FL_OPT_PDL = 4,
-    FL_OPT_WEIGHT_PRELOAD = 5
+    FL_OPT_WEIGHT_PRELOAD = 5,
+    FL_OPT_LAUNCH_CACHE = 6
 } fl_option;
 fl_status fl_set_option(fl_option key, int value);
+
+/*
+ * Host-side launch cache. Every fused call first validates its arguments,
+ * then needs a kernel choice and the TMA tensor maps of its operands (a
+ * driver call per map). Both depend only on the call's pointers, sizes, dtype
+ * and options, so the library keeps them for the last 64 argument sets (one
+ * slot per set, replaced on collision) and a repeated call only looks them up
+ * and launches; the mutable per-call state (the LayerNorm scratch) is set at
+ * launch. fl_launch_cache_stats returns the hits and misses since the library
+ * was loaded; fl_launch_cache_clear forgets every entry (e.g. after freeing
+ * buffers whose addresses may be reused with other contents: entries hold
+ * addresses and shapes only, never data, so a stale entry is still correct
+ * for the same address and shape).
+ */
+fl_status fl_launch_cache_stats(long long* hits, long long* misses);
+void fl_launch_cache_clear(void);
 
 /*
  * Test hook for the bounded-wait machinery: launches one CTA that waits on a
