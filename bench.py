@@ -71,8 +71,9 @@ def parse_workload(name: str) -> dict:
         _, dt, M, K = parts
         return dict(kind="rmsnorm", dtype=dt, M=int(M), K=int(K), eps=1e-6, name=name)
     if parts[0] == "layer":
-        _, dt, M, D, Dkv, F = parts
-        return dict(kind="layer", dtype=dt, M=int(M), D=int(D), Dkv=int(Dkv), F=int(F), eps=1e-6, name=name)
+        _, dt, M, D, Dkv, F = parts[:6]
+        L = int(parts[6]) if len(parts) > 6 else 4
+        return dict(kind="layer", dtype=dt, M=int(M), D=int(D), Dkv=int(Dkv), F=int(F), L=L, eps=1e-6, name=name)
     if parts[0] == "pattern":
         _, pat, dt, M, N, K = parts
         return dict(kind="pattern", pattern=pat, dtype=dt, M=int(M), N=int(N), K=int(K), name=name)
@@ -102,8 +103,9 @@ def describe(w: dict) -> str:
     if w["kind"] == "rmsnorm":
         return f"standalone rmsnorm {w['dtype']}: x[{w['M']},{w['K']}] gamma[{w['K']}] eps={w['eps']:g}"
     if w["kind"] == "layer":
-        return (f"decoder layer dense part {w['dtype']}: M={w['M']} D={w['D']} Dkv={w['Dkv']} F={w['F']} "
-                f"(RMSNorm+QKV, attention output projection + residual, RMSNorm+SwiGLU FFN + residual)")
+        return (f"{w['L']} chained decoder layers, dense part, {w['dtype']}: M={w['M']} D={w['D']} Dkv={w['Dkv']} "
+                f"F={w['F']} (RMSNorm+QKV, attention output projection + residual, RMSNorm+SwiGLU FFN + residual; "
+                f"the attention output is a fixed input)")
     return (f"swiglu_ffn {w['dtype']}: x[{w['M']},{w['D']}] RMSNorm, Wg/Wu[{w['F']},{w['D']}], "
             f"Wd[{w['D']},{w['F']}], + x")
 
@@ -134,7 +136,7 @@ def launches_of(w, separate=False) -> int:
     if w["kind"] == "swiglu":
         return 2
     if w["kind"] == "layer":
-        return 4  # QKV, output projection, gate/up, down
+        return 4 * w["L"]  # per layer: QKV, output projection, gate/up, down
     if w["kind"] == "multi":
         calls = len(w["Ns"]) if separate else 1
         return calls * (2 if w["norm"] == "layer" else 1)
@@ -156,9 +158,9 @@ def flops_per_step(w: dict) -> float:
         return 4.0 * w["M"] * w["K"]  # square-accumulate (2), scale by 1/rms and by gamma (2)
     if w["kind"] == "layer":
         M, D, Dkv, F = w["M"], w["D"], w["Dkv"], w["F"]
-        return (2.0 * M * D * (D + 2 * Dkv) + 3 * M * D + M * (D + 2 * Dkv)  # RMSNorm + QKV
-                + 2.0 * M * D * D + 2 * M * D                                 # output projection, bias, residual
-                + 6.0 * M * D * F + 3 * M * D + 2 * M * F + 4 * M * F + M * F + M * D)  # FFN
+        return w["L"] * (2.0 * M * D * (D + 2 * Dkv) + 3 * M * D + M * (D + 2 * Dkv)  # RMSNorm + QKV
+                         + 2.0 * M * D * D + 2 * M * D                                 # output projection, residual
+                         + 6.0 * M * D * F + 3 * M * D + 2 * M * F + 4 * M * F + M * F + M * D)  # FFN
     M, N, K = w["M"], w["N"], w["K"]
     f = 2.0 * M * N * K
     if w["kind"] == "biasin":
@@ -186,7 +188,7 @@ def bytes_per_step(w: dict) -> float:
         M, D, Dkv, F = w["M"], w["D"], w["Dkv"], w["F"]
         weights = D * (D + 2 * Dkv) + D * D + 3 * D * F + 2 * D
         acts = M * D + M * (D + 2 * Dkv) + M * D + M * D + 2 * M * F + M * D  # x, q/k/v, attn, h, h_ffn w+r, out
-        return e * (weights + acts)
+        return e * w["L"] * (weights + acts)  # the layers share one set of weights, read once per layer
     M, N, K = w["M"], w["N"], w["K"]
     b = e * (M * K + N * K + M * N)
     if w["kind"] == "biasin":
@@ -228,9 +230,9 @@ def out_shapes(w: dict):
         return [(w["M"], w["D"])]
     if w["kind"] == "rmsnorm":
         return [(w["M"], w["K"])]
-    if w["kind"] == "layer":  # out, then q, k, v, h
+    if w["kind"] == "layer":  # the last layer's out, then per layer q, k, v, h, out
         M, D, Dkv = w["M"], w["D"], w["Dkv"]
-        return [(M, D), (M, D), (M, Dkv), (M, Dkv), (M, D)]
+        return [(M, D)] + [(M, D), (M, Dkv), (M, Dkv), (M, D), (M, D)] * w["L"]
     return [(w["M"], w["N"])]
 
 
@@ -493,9 +495,17 @@ def run_ours(args, w: dict, rank: int, world: int, local: int):
         g["outs"] = [torch.empty(sh, dtype=t[next(iter(t))].dtype, device=dev) for sh in shapes]
         g["out"] = g["outs"][0]
         if w["kind"] == "layer":
+            # L layers chained through their outputs (layer l reads layer l-1's
+            # out as x), sharing the weights and the attention stand-in
             o = g["outs"]
-            g["layer"] = fl.DecoderLayer(eps=w["eps"], out=o[0], q=o[1], k=o[2], v=o[3], h=o[4], bias_o=None,
-                                         **{k: v for k, v in g.items() if k not in ("outs", "out")})
+            base = {k: v for k, v in g.items() if k not in ("outs", "out", "x")}
+            g["layers"], x = [], g["x"]
+            for l in range(w["L"]):
+                q, k_, v_, h, out_l = o[1 + 5 * l: 6 + 5 * l]
+                g["layers"].append(fl.DecoderLayer(eps=w["eps"], x=x, out=out_l, q=q, k=k_, v=v_, h=h, bias_o=None,
+                                                   **base))
+                x = out_l
+            g["out"] = g["outs"][0] = x
         if w["kind"] == "swiglu":
             g["ws"] = torch.empty(fl.swiglu_ffn_workspace_size(w["M"], w["F"], w["dtype"]), dtype=torch.uint8,
                                   device=dev)
@@ -505,11 +515,12 @@ def run_ours(args, w: dict, rank: int, world: int, local: int):
 
     def step(g, stream=None):
         if w["kind"] == "layer":
-            for half in (0, 1):
-                if args.separate:
-                    g["layer"].issue(half, stream=stream)
-                else:
-                    g["layer"].launch(half, stream=stream)
+            for layer in g["layers"]:
+                for half in (0, 1):
+                    if args.separate:  # the plan's own two graphs per layer
+                        layer.launch(half, stream=stream)
+                    else:
+                        layer.issue(half, stream=stream)
         elif w["kind"] == "multi" and args.separate:
             for i in range(n_out):
                 fl.norm_gemm(g["x"], g["gamma"], g[f"W{i}"], beta=g.get("beta"), out=g["outs"][i], eps=w["eps"],
@@ -598,7 +609,9 @@ def run_ours(args, w: dict, rank: int, world: int, local: int):
 
     # end to end through the same call: pinned host inputs in, result back to pinned host
     host = {k: t[k].pin_memory() for k in e2e_input_keys(w, t)}
-    houts = [torch.empty(sh, dtype=sets[0]["out"].dtype).pin_memory() for sh in shapes]
+    # the step's result read back: a layer stack's last output, else every output
+    d2h_shapes = shapes[:1] if w["kind"] == "layer" else shapes
+    houts = [torch.empty(sh, dtype=sets[0]["out"].dtype).pin_memory() for sh in d2h_shapes]
     g = sets[0]
     h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
     e2e_steps = max(3, min(args.steps, 200))
@@ -644,16 +657,16 @@ def run_ours(args, w: dict, rank: int, world: int, local: int):
                          + ("> 129 MB L2)" if nsets * (set_bytes + out_bytes) > L2_BYTES else
                             "< 129 MB L2: the operands are L2-resident)"),
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "launch": ("two fl_layer graph launches per step" if w["kind"] == "layer" and not args.separate
+                   "launch": ("two fl_layer graph launches per layer" if w["kind"] == "layer" and args.separate
                               else "stream calls" if args.no_graph
-                              else f"CUDA graphs of {nsets} library calls, replayed"),
+                              else f"CUDA graphs of {nsets} steps of library calls, replayed"),
                    "weights": "read-only; " + ("read after the previous step" if args.no_weight_preload else
                                                "first tiles staged before the programmatic dependency resolves"),
                    "vs_baseline_ref": "A30 fused RMSNorm->Linear 0.208 ms (LLMBoost page), other hardware",
                    "host_enqueue_us_per_step": enqueue_s * 1e6 / args.steps},
         "roofline": roofline,
         "e2e": {"value": flops * e2e_steps * world / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out_bytes},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": sum(a * b * 2 for a, b in d2h_shapes)},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
@@ -687,9 +700,8 @@ def main(argv=None):
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")
     w = parse_workload(args.workload)
-    if w["kind"] == "layer":
-        # the layer is its own pair of CUDA graphs (or, with --separate, the
-        # same library calls issued directly): timed as stream calls
+    if w["kind"] == "layer" and args.separate:
+        # the layer plans' own graphs, launched as stream calls
         args.no_graph = True
     rank, world, local = dist_setup()
     if world > 1:
