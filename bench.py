@@ -517,10 +517,7 @@ def run_ours(args, w: dict, rank: int, world: int, local: int):
         if w["kind"] == "layer":
             for layer in g["layers"]:
                 for half in (0, 1):
-                    if args.separate:  # the plan's own two graphs per layer
-                        layer.launch(half, stream=stream)
-                    else:
-                        layer.issue(half, stream=stream)
+                    layer.issue(half, stream=stream)
         elif w["kind"] == "multi" and args.separate:
             for i in range(n_out):
                 fl.norm_gemm(g["x"], g["gamma"], g[f"W{i}"], beta=g.get("beta"), out=g["outs"][i], eps=w["eps"],
@@ -555,6 +552,14 @@ def run_ours(args, w: dict, rank: int, world: int, local: int):
     def capture(n):
         if n == 0 or args.no_graph:
             return None
+        if args.library_capture:
+            side = torch.cuda.Stream(dev)
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                gr = fl.Graph.capture(lambda: [step(sets[j % nsets], stream=side) for j in range(n)], stream=side)
+            stream.wait_stream(side)
+            gr.replay = gr.launch
+            return gr
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             for j in range(n):
@@ -657,9 +662,10 @@ def run_ours(args, w: dict, rank: int, world: int, local: int):
                          + ("> 129 MB L2)" if nsets * (set_bytes + out_bytes) > L2_BYTES else
                             "< 129 MB L2: the operands are L2-resident)"),
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "launch": ("two fl_layer graph launches per layer" if w["kind"] == "layer" and args.separate
-                              else "stream calls" if args.no_graph
-                              else f"CUDA graphs of {nsets} steps of library calls, replayed"),
+                   "launch": ("stream calls" if args.no_graph
+                              else f"CUDA graphs of {nsets} steps of library calls, replayed"
+                              + (" (captured with fl_capture_begin / fl_capture_end)" if args.library_capture
+                                 else "")),
                    "weights": "read-only; " + ("read after the previous step" if args.no_weight_preload else
                                                "first tiles staged before the programmatic dependency resolves"),
                    "vs_baseline_ref": "A30 fused RMSNorm->Linear 0.208 ms (LLMBoost page), other hardware",
@@ -688,6 +694,8 @@ def main(argv=None):
     ap.add_argument("--variant", type=int, default=0, help="force 1 = tile kernel, 2 = small-M split-K kernel")
     ap.add_argument("--split-k", type=int, default=0, help="force the K split of the small-M kernel")
     ap.add_argument("--no-graph", action="store_true", help="time plain stream calls instead of graph replays")
+    ap.add_argument("--library-capture", action="store_true",
+                    help="capture the replayed graphs with the library's fl_capture_begin / fl_capture_end")
     ap.add_argument("--no-launch-cache", action="store_true",
                     help="prepare every call afresh (FL_OPT_LAUNCH_CACHE off): host cost without the cache")
     ap.add_argument("--separate", action="store_true",
@@ -700,9 +708,10 @@ def main(argv=None):
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")
     w = parse_workload(args.workload)
-    if w["kind"] == "layer" and args.separate:
-        # the layer plans' own graphs, launched as stream calls
-        args.no_graph = True
+    if w["kind"] == "layer":
+        # a decode step through a layer stack: captured with the library's own
+        # capture calls (fl_capture_begin / fl_capture_end)
+        args.library_capture = True
     rank, world, local = dist_setup()
     if world > 1:
         import torch.distributed as dist

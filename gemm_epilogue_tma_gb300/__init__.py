@@ -52,9 +52,12 @@ SIGNATURES = {
     "fl_input_bias_gemm": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
     "fl_rms_norm": (_i, [_vp, _vp, _vp, _i, _i, _f, _i, _vp]),
     "fl_layer_create": (_i, [ctypes.POINTER(LayerDesc), ctypes.POINTER(_vp)]),
-    "fl_layer_launch": (_i, [_vp, _i, _vp]),
     "fl_layer_issue": (_i, [_vp, _i, _vp]),
     "fl_layer_destroy": (None, [_vp]),
+    "fl_capture_begin": (_i, [_vp]),
+    "fl_capture_end": (_i, [_vp, ctypes.POINTER(_vp)]),
+    "fl_graph_launch": (_i, [_vp, _vp]),
+    "fl_graph_destroy": (None, [_vp]),
     "fl_launch_cache_stats": (_i, [ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_longlong)]),
     "fl_launch_cache_clear": (None, []),
     "fl_last_error": (ctypes.c_char_p, []),
@@ -227,12 +230,12 @@ def rms_norm(x, gamma, out=None, eps=1e-6, stream=None):
 
 
 class DecoderLayer:
-    """The dense part of a decoder layer captured into two CUDA graphs (fl_layer_*).
+    """The dense part of a decoder layer as a prepared call sequence (fl_layer_*).
 
     half 0: q, k, v = RMSNorm(x) [Wq; Wk; Wv]^T; the caller's attention then
     writes attn; half 1: h = attn Wo^T (+ bias_o) + x, out = SwiGLU_FFN(h) + h.
-    Every tensor is fixed for the life of the layer (the graphs hold their
-    addresses): write new inputs into x and attn in place.
+    Every tensor is fixed for the life of the layer: write new inputs into x
+    and attn in place. Capture whole steps with Graph.capture().
     """
 
     NAMES = ("x", "gamma_attn", "Wq", "Wk", "Wv", "q", "k", "v", "attn", "Wo", "bias_o", "h", "gamma_ffn", "Wg",
@@ -251,16 +254,47 @@ class DecoderLayer:
         _check(lib().fl_layer_create(ctypes.byref(desc), ctypes.byref(h)))
         self._h = h
 
-    def launch(self, half: int, stream=None) -> None:
-        _check(lib().fl_layer_launch(self._h, int(half), _stream(stream)))
-
     def issue(self, half: int, stream=None) -> None:
-        """The same half as ordinary library calls (no graph)."""
+        """Issue half 0 or 1 on the stream (capturable)."""
         _check(lib().fl_layer_issue(self._h, int(half), _stream(stream)))
 
     def close(self) -> None:
         if getattr(self, "_h", None):
             lib().fl_layer_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class Graph:
+    """A CUDA graph of library calls (fl_capture_begin / fl_capture_end / fl_graph_launch)."""
+
+    def __init__(self, handle):
+        self._h = handle
+
+    @classmethod
+    def capture(cls, fn, stream=None):
+        """Run fn() (which issues library calls on `stream`) under capture; returns the graph."""
+        s = _stream(stream)
+        _check(lib().fl_capture_begin(s))
+        try:
+            fn()
+        finally:
+            h = ctypes.c_void_p()
+            st = lib().fl_capture_end(s, ctypes.byref(h))
+        _check(st)
+        return cls(h)
+
+    def launch(self, stream=None) -> None:
+        _check(lib().fl_graph_launch(self._h, _stream(stream)))
+
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            lib().fl_graph_destroy(self._h)
             self._h = None
 
     def __del__(self):

@@ -228,22 +228,22 @@ fl_status fl_swiglu_ffn_noalloc(const void* x, const void* gamma, const void* Wg
                                 int F, float eps, fl_dtype dtype, void* stream);
 
 /*
- * The dense part of a Llama-style decoder layer, captured into CUDA graphs.
+ * The dense part of a Llama-style decoder layer as a prepared call sequence.
  * At decode sizes every kernel of a layer takes a few microseconds, so host
- * launch costs and the gaps between launches weigh as much as the kernels;
- * capturing the layer once and replaying it removes them (the "Fusion
- * Compiler" glossary pairs fusion with CUDA Graph capture as the coarse-grained
- * launch optimisation). The layer is split where the attention core sits,
- * which this library does not compute:
+ * launch costs weigh as much as the kernels; a decode step is meant to be
+ * captured once, every layer with the caller's attention in between, into
+ * one CUDA graph (fl_capture_begin .. fl_capture_end) and replayed with one
+ * launch (the "Fusion Compiler" glossary pairs fusion with CUDA Graph capture
+ * as the coarse-grained launch optimisation). The layer is split where the
+ * attention core sits, which this library does not compute:
  *   half 0:  q, k, v = RMSNorm(x; gamma_attn) [Wq; Wk; Wv]^T       (fl_norm_gemm_multi)
  *   ... the caller's attention reads q, k, v and writes attn ...
  *   half 1:  h   = attn Wo^T (+ bias_o) + x                        (fl_gemm_epilogue)
  *            out = silu(hn Wg^T) * (hn Wu^T) Wd^T + h, hn = RMSNorm(h; gamma_ffn)   (fl_swiglu_ffn)
  * Shapes: x, attn, h, out, q [M, D]; k, v [M, Dkv]; Wq, Wo [D, D];
  * Wk, Wv [Dkv, D]; Wg, Wu [F, D]; Wd [D, F]; gamma_* and bias_o [D]. All are
- * caller-owned device pointers, fixed for the life of the layer: the graphs
- * hold them. bias_o may be NULL (no bias). eps is the RMSNorm epsilon of both
- * norms.
+ * caller-owned device pointers, fixed for the life of the layer. bias_o may
+ * be NULL (no bias). eps is the RMSNorm epsilon of both norms.
  */
 typedef struct {
     fl_dtype dtype;
@@ -272,23 +272,36 @@ typedef struct fl_layer fl_layer;
 
 /*
  * Validates the description, allocates the layer's own device memory (the
- * FFN hidden activation, M * F * 2 bytes, and D zeros when bias_o is NULL),
- * runs both halves once uncaptured (the one-time kernel set-up; this writes
- * q, k, v, h and out from whatever x and attn hold), then captures each half
- * into a CUDA graph on an internal stream and instantiates it. Call it at
- * initialisation, not inside another stream capture. On failure *layer is
- * NULL and nothing is left allocated.
+ * FFN hidden activation, M * F * 2 bytes, and D zeros when bias_o is NULL)
+ * and runs both halves once on an internal stream (the one-time kernel
+ * set-up; this writes q, k, v, h and out from whatever x and attn hold), so
+ * that every later call of the layer hits the launch cache. Call it at
+ * initialisation, not inside a stream capture. On failure *layer is NULL and
+ * nothing is left allocated.
  */
 fl_status fl_layer_create(const fl_layer_desc* desc, fl_layer** layer);
 
-/* Launches half 0 or 1 as one graph launch on `stream`; allocates nothing. */
-fl_status fl_layer_launch(fl_layer* layer, int half, void* stream);
-
-/* Issues the same half as ordinary library calls on `stream` (no graph), for comparison. */
+/* Issues half 0 or 1 on `stream` (capturable); allocates nothing. */
 fl_status fl_layer_issue(const fl_layer* layer, int half, void* stream);
 
-/* Frees the graphs, the internal stream and the layer's device memory. NULL is a no-op. */
+/* Frees the layer's device memory and stream. NULL is a no-op. */
 void fl_layer_destroy(fl_layer* layer);
+
+/*
+ * Capture of library calls (and any other work the caller issues on the same
+ * stream from the same thread) into one CUDA graph: fl_capture_begin starts
+ * a thread-local capture of `stream`; fl_capture_end ends it, instantiates
+ * and uploads the graph and returns its handle (*graph_exec, a
+ * cudaGraphExec_t); fl_graph_launch replays it on a stream; fl_graph_destroy
+ * frees it (NULL is a no-op). Every call of this library except
+ * fl_layer_create and fl_device_status may be captured; the first call of a
+ * kernel configuration should come before the capture (its one-time set-up
+ * is not capturable), which fl_layer_create does for a layer.
+ */
+fl_status fl_capture_begin(void* stream);
+fl_status fl_capture_end(void* stream, void** graph_exec);
+fl_status fl_graph_launch(void* graph_exec, void* stream);
+void fl_graph_destroy(void* graph_exec);
 
 /* Message for the last non-OK status returned on this thread ("" if none). */
 const char* fl_last_error(void);

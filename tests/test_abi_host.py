@@ -241,5 +241,8 @@ def test_layer_create_validation(L):
     d.h = d.x
     assert L.fl_layer_create(ctypes.byref(d), ctypes.byref(h)) == INVALID
     assert not h.value
-    assert L.fl_layer_launch(None, 0, None) == INVALID
+    assert L.fl_layer_issue(None, 0, None) == INVALID
     L.fl_layer_destroy(None)  # no-op
+    assert L.fl_graph_launch(None, None) == INVALID
+    assert L.fl_capture_end(None, None) == INVALID
+    L.fl_graph_destroy(None)  # no-op

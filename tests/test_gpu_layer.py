@@ -1,12 +1,12 @@
-"""The graph-captured decoder layer (fl_layer_*) against the float64 oracle
-(needs an sm_103a GPU).
+"""The decoder layer's dense part (fl_layer_*) and graph capture of library
+calls (fl_capture_*), against the float64 oracle (needs an sm_103a GPU).
 
 Each stage is compared with the oracle on the tensors it reads: q, k, v with
 oracle.norm_gemm of x; h with attn Wo^T (+ bias) + x; out with
 oracle.swiglu_ffn of the layer's own h (h is stored in the dtype between the
-two halves, so it is the exact input of the FFN). Graph launches must equal
-the same calls issued without a graph, bit for bit, and a relaunch after x is
-rewritten in place must follow the new x.
+two halves, so it is the exact input of the FFN). A captured graph of two
+chained layers must equal the same calls issued directly, bit for bit, and a
+replay after x is rewritten in place must follow the new x.
 """
 import numpy as np
 import pytest
@@ -66,31 +66,49 @@ def check_layer(T, dt, rows, what):
 @pytest.mark.parametrize("dt", ["f16", "bf16"])
 @pytest.mark.parametrize("shape", [(1, 1024, 256, 2816), (32, 4096, 1024, 11008), (200, 512, 128, 1376)],
                          ids=lambda s: "x".join(map(str, s)))
-def test_layer_graph_matches_oracle_and_direct_calls(dt, shape):
+def test_layer_stack_graph_matches_oracle_and_direct_calls(dt, shape):
     M, D, Dkv, F = shape
     T = make_layer(M, D, Dkv, F, dt, with_bias=M == 200)
-    layer = fl.DecoderLayer(eps=1e-6, **T)
+    # a second layer reading the first one's output, with its own buffers
+    T2 = dict(T)
+    dtype = T["x"].dtype
+    T2["x"] = T["out"]
+    for name, shp in (("q", (M, D)), ("k", (M, Dkv)), ("v", (M, Dkv)), ("h", (M, D)), ("out", (M, D))):
+        T2[name] = torch.empty(shp, dtype=dtype, device="cuda")
+    layers = [fl.DecoderLayer(eps=1e-6, **T), fl.DecoderLayer(eps=1e-6, **T2)]
+    names = ("q", "k", "v", "h", "out")
+    graph = None
     try:
-        layer.launch(0)
-        layer.launch(1)
+        def step():
+            for layer in layers:
+                layer.issue(0)
+                layer.issue(1)
+
+        step()
         torch.cuda.synchronize()
         fl.device_status()
         rows = sample_rows(M, n=64)
-        check_layer(T, dt, rows, f"layer graph {dt} {shape}")
-        got = {n: T[n].clone() for n in ("q", "k", "v", "h", "out")}
-        # the same calls without the graph give the same bits
-        for n in got:
-            T[n].zero_()
-        layer.issue(0)
-        layer.issue(1)
+        check_layer(T, dt, rows, f"layer 1 {dt} {shape}")
+        check_layer(T2, dt, rows, f"layer 2 {dt} {shape}")
+        direct = [{n: t[n].clone() for n in names} for t in (T, T2)]
+        # one graph of both layers: the same bits
+        graph = fl.Graph.capture(step)
+        for t in (T, T2):
+            for n in names:
+                t[n].zero_()
+        graph.launch()
         torch.cuda.synchronize()
-        for n in got:
-            assert torch.equal(T[n], got[n]), n
+        for t, d in zip((T, T2), direct):
+            for n in names:
+                assert torch.equal(t[n], d[n]), n
         # new x written in place: the replay follows it
         T["x"].copy_(T["x"].flip(0) * 0.5)
-        layer.launch(0)
-        layer.launch(1)
+        graph.launch()
         torch.cuda.synchronize()
-        check_layer(T, dt, rows, f"layer relaunch {dt} {shape}")
+        check_layer(T, dt, rows, f"layer 1 replay {dt} {shape}")
+        check_layer(T2, dt, rows, f"layer 2 replay {dt} {shape}")
     finally:
-        layer.close()
+        if graph is not None:
+            graph.close()
+        for layer in layers:
+            layer.close()
