@@ -278,7 +278,8 @@ class Graph:
 
     @classmethod
     def capture(cls, fn, stream=None):
-        """Run fn() (which issues library calls on `stream`) under capture; returns the graph."""
+        """Run fn() (which issues library calls on `stream`) under capture; returns the graph.
+        The stream must not be the legacy default stream (CUDA cannot capture it)."""
         s = _stream(stream)
         _check(lib().fl_capture_begin(s))
         try:

@@ -91,8 +91,13 @@ def test_layer_stack_graph_matches_oracle_and_direct_calls(dt, shape):
         check_layer(T, dt, rows, f"layer 1 {dt} {shape}")
         check_layer(T2, dt, rows, f"layer 2 {dt} {shape}")
         direct = [{n: t[n].clone() for n in names} for t in (T, T2)]
-        # one graph of both layers: the same bits
-        graph = fl.Graph.capture(step)
+        # one graph of both layers (captured on a side stream: the legacy
+        # default stream cannot be captured): the same bits
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            graph = fl.Graph.capture(step)
+        torch.cuda.current_stream().wait_stream(side)
         for t in (T, T2):
             for n in names:
                 t[n].zero_()
