@@ -746,12 +746,51 @@ fl_status run_kernels(int dt, int pro, bool dual, const void* A, const Outs& out
 // One fused call. LayerNorm first computes the row statistics (8 bytes per
 // row of stream-ordered scratch from the library pool, freed on the stream
 // right after the GEMM kernel that reads them), once for all outputs.
+// Decode row counts go to the CUDA-core kernel (whole weight rows per warp, no
+// reduction across CTAs); FL_OPT_VARIANT = 4 forces it where it fits.
+bool use_gemv(int M, int K, bool dual) {
+    const int variant = g_opt_variant.load();
+    if (dual || (variant != 0 && variant != 4)) return false;
+    if (M > fl::kGemvMaxRows || (long long)M * K * 2 > fl::kGemvSmemMax) return false;
+    return true;
+}
+
+fl_status run_gemv(int dt, int pro, const void* A, const Outs& outs, const void* residual, const void* gamma,
+                   const void* beta, int M, int K, float eps, DeviceInfo* di, cudaStream_t stream) {
+    fl::GemvParams g;
+    memset(&g, 0, sizeof(g));
+    g.x = static_cast<const uint16_t*>(A);
+    g.gamma = static_cast<const uint16_t*>(gamma);
+    g.beta = static_cast<const uint16_t*>(beta);
+    g.n_out = outs.n;
+    int rows = 0;
+    for (int i = 0; i < outs.n; ++i) {
+        g.W[i] = static_cast<const uint16_t*>(outs.o[i].W);
+        g.bias[i] = static_cast<const uint16_t*>(outs.o[i].bias);
+        g.out[i] = static_cast<uint16_t*>(outs.o[i].out);
+        g.N[i] = outs.o[i].N;
+        g.act[i] = outs.o[i].act;
+        g.row0[i] = rows;
+        rows += outs.o[i].N;
+    }
+    for (int i = outs.n; i <= 4; ++i) g.row0[i] = rows;
+    g.residual = static_cast<const uint16_t*>(residual);
+    g.M = M;
+    g.K = K;
+    g.eps = eps;
+    const cudaError_t e = fl::launch_gemv(dt, pro, g, di->sms, g_opt_pdl.load(), stream);
+    if (e != cudaSuccess) return fail(FL_ERR_CUDA, "decode kernel launch failed: %s", cudaGetErrorString(e));
+    return ok();
+}
+
 fl_status run_tile(int dt, int pro, bool dual, const void* A, const Outs& outs, const void* W2,
                    const void* residual, const void* gamma, const void* beta, int M, int K, float eps,
                    cudaStream_t stream) {
     DeviceInfo* di = nullptr;
     fl_status st = device_info(&di);
     if (st != FL_OK) return st;
+    // (the decode kernel computes its few rows' LayerNorm statistics itself)
+    if (use_gemv(M, K, dual)) return run_gemv(dt, pro, A, outs, residual, gamma, beta, M, K, eps, di, stream);
     void* stats = nullptr;
     if (pro == fl::PRO_LN) {
         cudaError_t e = cudaMallocFromPoolAsync(&stats, (size_t)M * 8, di->pool, stream);
@@ -808,7 +847,7 @@ fl_status fl_set_option(fl_option key, int value) {
             g_opt_tile_n = value;
             return ok();
         case FL_OPT_VARIANT:
-            if (value < 0 || value > 3) return fail(FL_ERR_INVALID_ARG, "variant must be 0..3");
+            if (value < 0 || value > 4) return fail(FL_ERR_INVALID_ARG, "variant must be 0..4");
             g_opt_variant = value;
             return ok();
         case FL_OPT_TIMEOUT_MS:
@@ -982,9 +1021,14 @@ fl_status fl_rms_norm(const void* x, const void* gamma, void* out, int M, int K,
     return ok();
 }
 
+// Decode FFN in one launch: h, then (at a 256-byte boundary) the grid
+// barrier's counter.
+size_t ffn_counter_offset(int M, int F) { return ((size_t)M * (size_t)F * 2 + 255) / 256 * 256; }
+
 size_t fl_swiglu_ffn_workspace_size(int M, int F, fl_dtype dtype) {
     (void)dtype;
     if (M < 1 || F < 1) return 0;
+    if (M <= fl::kGemvMaxRows) return ffn_counter_offset(M, F) + 256;
     return (size_t)M * (size_t)F * 2;
 }
 
@@ -1017,6 +1061,36 @@ fl_status fl_swiglu_ffn(const void* x, const void* gamma, const void* Wg, const 
     }
     if (overlap(workspace, need, out, ob)) return fail(FL_ERR_INVALID_ARG, "workspace overlaps out");
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // decode rows: the whole block in one launch (gate/up, grid barrier, down)
+    const int variant = g_opt_variant.load();
+    if ((variant == 0 || variant == 4) && M <= fl::kGemvMaxRows) {
+        DeviceInfo* di = nullptr;
+        if ((st = device_info(&di)) != FL_OK) return st;
+        const int grid = fl::ffn_decode_grid(dtype, M, D, F, di->sms);
+        if (grid > 0) {
+            fl::FfnDecodeParams q;
+            memset(&q, 0, sizeof(q));
+            q.x = static_cast<const uint16_t*>(x);
+            q.gamma = static_cast<const uint16_t*>(gamma);
+            q.Wg = static_cast<const uint16_t*>(Wg);
+            q.Wu = static_cast<const uint16_t*>(Wu);
+            q.Wd = static_cast<const uint16_t*>(Wd);
+            q.bias_down = static_cast<const uint16_t*>(bias_down);
+            q.h = static_cast<uint16_t*>(workspace);
+            q.out = static_cast<uint16_t*>(out);
+            q.counter = reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) + ffn_counter_offset(M, F));
+            q.status = di->status;
+            q.timeout_ns = (unsigned long long)g_opt_timeout_ms.load() * 1000000ull;
+            q.M = M;
+            q.D = D;
+            q.F = F;
+            q.eps = eps;
+            cudaError_t e = cudaMemsetAsync(q.counter, 0, sizeof(unsigned int), s);
+            if (e == cudaSuccess) e = fl::launch_ffn_decode(dtype, q, grid, g_opt_pdl.load(), s);
+            if (e != cudaSuccess) return fail(FL_ERR_CUDA, "decode FFN launch failed: %s", cudaGetErrorString(e));
+            return ok();
+        }
+    }
     // gate/up: h = silu(RMSNorm(x) Wg^T) * (RMSNorm(x) Wu^T)
     st = run_tile(dtype, fl::PRO_RMS, true, x, single_out(Wg, nullptr, workspace, F, fl::ACT_NONE), Wu, nullptr, gamma,
                   nullptr, M, D, eps, s);

@@ -65,7 +65,7 @@ extern "C" fl_status fl_swiglu_ffn_noalloc(const void* x, const void* gamma, con
         return (fl_status)fl::set_last_error(FL_ERR_INVALID_ARG, "fl_swiglu_ffn_noalloc: sizes must be positive");
     if (x == nullptr || gamma == nullptr || Wg == nullptr || Wu == nullptr || Wd == nullptr || out == nullptr)
         return (fl_status)fl::set_last_error(FL_ERR_INVALID_ARG, "fl_swiglu_ffn_noalloc: a required pointer is null");
-    if ((size_t)M * (size_t)F * 2 > kScratchBytes) {
+    if (fl_swiglu_ffn_workspace_size(M, F, dtype) > kScratchBytes) {
         char msg[256];
         snprintf(msg, sizeof(msg),
                  "fl_swiglu_ffn_noalloc: h [%d, %d] needs %zu bytes, more than the library's fixed %zu-byte array; "
@@ -77,6 +77,6 @@ extern "C" fl_status fl_swiglu_ffn_noalloc(const void* x, const void* gamma, con
     fl_status st = scratch_address(&scratch);
     if (st != FL_OK) return st;
     // h needs no clearing: the gate/up kernel writes every element the down
-    // projection reads.
+    // projection reads (the one-launch decode form zeroes its barrier word).
     return fl_swiglu_ffn(x, gamma, Wg, Wu, Wd, bias_down, out, M, D, F, eps, scratch, kScratchBytes, dtype, stream);
 }

@@ -188,3 +188,72 @@ def test_rms_norm_in_place():
     assert y.data_ptr() == x.data_ptr()
     ref = oracle.rms_norm(f64(t["x"]), f64(t["gamma"]), 1e-6)
     assert_close(y, ref, "bf16", "rms_norm in place")
+
+
+# ---------------------------------------------------------------------------
+# the CUDA-core decode kernel (1 to 4 rows), forced and automatic
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("M", [1, 2, 3, 4])
+@pytest.mark.parametrize("NK", [(8, 8), (264, 136), (1032, 4096), (64, 11008)], ids=lambda s: "x".join(map(str, s)))
+def test_decode_kernel_all_patterns(dt, M, NK):
+    N, K = NK
+    t = syn.dense_layer_inputs(M, N, K, dt)
+    A, W = dev(t["A"]), dev(t["W"])
+    fl.set_option("variant", 4)
+    try:
+        for pattern in syn.PATTERNS:
+            eps = 1e-5 if pattern == "layernorm_gemm" else 1e-6
+            if pattern == "rmsnorm_gemm":
+                got = fl.norm_gemm(A, dev(t["gamma"]), W, eps=eps, norm="rms")
+            elif pattern == "layernorm_gemm":
+                got = fl.norm_gemm(A, dev(t["gamma"]), W, beta=dev(t["beta"]), eps=eps, norm="layer")
+            else:
+                got = fl.gemm_epilogue(A, W, bias=dev(t["bias"]), residual=dev(t["residual"]), pattern=pattern)
+            torch.cuda.synchronize()
+            args = (f64(t["A"]), f64(t["W"]), f64(t["bias"]), f64(t["residual"]), f64(t["gamma"]), f64(t["beta"]))
+            ref = oracle.fused_pattern(pattern, *args, eps=eps)
+            assert_close(got, ref, dt, f"decode kernel {pattern} {dt} M={M} {N}x{K}",
+                         chain=parity.chain_pattern(pattern, *args, eps, dt))
+        run_input_bias(M, N, K, dt, "silu", with_bias=True, with_res=True, opts={"variant": 4})
+        fl.device_status()
+    finally:
+        fl.set_option("variant", 0)
+
+
+@pytest.mark.parametrize("dt", DTYPES)
+@pytest.mark.parametrize("norm", ["rms", "layer"])
+def test_decode_kernel_multi_and_degenerate_rows(dt, norm):
+    # QKV at one and three rows, automatic choice
+    for M in (1, 3):
+        run_multi(M, (1024, 256, 256), 1024, norm, dt, acts=["none", "gelu", "none"])
+    # zero and constant rows through the in-kernel LayerNorm statistics
+    t = syn.norm_gemm_inputs(4, 136, 456, norm, dt, with_bias=True)
+    x = t["x"].clone()
+    x[0] = 0.0
+    x[1] = 40.0
+    x[2] = -0.75
+    got = fl.norm_gemm(dev(x), dev(t["gamma"]), dev(t["W"]), beta=dev(t["beta"]), bias=dev(t["bias"]), eps=1e-5,
+                       norm=norm)
+    torch.cuda.synchronize()
+    ref = oracle.norm_gemm(f64(x), f64(t["gamma"]), f64(t["beta"]), f64(t["W"]), f64(t["bias"]), 1e-5, norm)
+    assert_close(got, ref, dt, f"decode kernel degenerate rows {norm} {dt}")
+
+
+@pytest.mark.parametrize("dt", DTYPES)
+def test_decode_ffn_repeated_and_noalloc(dt):
+    """The one-launch decode FFN twice in a row on one workspace (its barrier
+    word is re-zeroed per call), and through the allocation-free entry point."""
+    M, D, F = 2, 1024, 2816
+    t = syn.swiglu_inputs(M, D, F, dt, with_bias=True)
+    g = {k: dev(v) for k, v in t.items()}
+    ws = torch.empty(fl.swiglu_ffn_workspace_size(M, F, dt), dtype=torch.uint8, device="cuda")
+    outs = [fl.swiglu_ffn(g["x"], g["gamma"], g["Wg"], g["Wu"], g["Wd"], bias_down=g["bias_down"], eps=1e-6,
+                          workspace=ws) for _ in range(2)]
+    na = fl.swiglu_ffn_noalloc(g["x"], g["gamma"], g["Wg"], g["Wu"], g["Wd"], bias_down=g["bias_down"], eps=1e-6)
+    torch.cuda.synchronize()
+    fl.device_status()
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], na)
+    f = {k: f64(v) for k, v in t.items()}
+    ref = oracle.swiglu_ffn(f["x"], f["gamma"], f["Wg"], f["Wu"], f["Wd"], f["bias_down"], 1e-6, dt)
+    assert_close(outs[0], ref, dt, f"decode ffn {dt}")
