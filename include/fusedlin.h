@@ -181,7 +181,9 @@ fl_status fl_input_bias_gemm(const void* A, const void* bias_in, const void* W, 
 fl_status fl_rms_norm(const void* x, const void* gamma, void* out, int M, int K, float eps,
                       fl_dtype dtype, void* stream);
 
-/* Bytes of workspace fl_swiglu_ffn needs: the hidden activation h [M,F] in the dtype. */
+/* Bytes of workspace fl_swiglu_ffn needs: the hidden activation h [M,F] in the
+ * dtype; for 1 to 4 rows (the one-launch decode form) h rounded up to 256
+ * bytes plus 256 bytes for that kernel's grid-barrier word. */
 size_t fl_swiglu_ffn_workspace_size(int M, int F, fl_dtype dtype);
 
 /*
@@ -317,10 +319,14 @@ fl_status fl_device_status(void* stream);
  * Tuning overrides, for benchmarks and tests (process-wide, not thread-safe):
  *   FL_OPT_TILE_N:      0 = automatic, else the CTA tile width (128 or 256).
  *   FL_OPT_VARIANT:     0 = automatic, 1 = tile kernel, 2 = small-M split-K kernel
- *                       (not used by the SwiGLU gate/up kernel, which then
- *                       takes the tile kernel), 3 = CTA-pair kernel (256 x 256
- *                       tiles on two SMs; for the gate/up kernel, Wg and Wu
- *                       rows stacked in one tile).
+ *                       (for the SwiGLU gate/up GEMM only up to 64 rows, else
+ *                       the tile kernel), 3 = CTA-pair kernel (256 x 256 tiles
+ *                       on two SMs; for the gate/up kernel, Wg and Wu rows
+ *                       stacked in one tile), 4 = the CUDA-core decode kernel
+ *                       (1 to 4 rows whose transformed activation fits in
+ *                       96 KB of shared memory; for fl_swiglu_ffn the whole
+ *                       block in one launch). Automatic choice takes the
+ *                       decode kernel for 1 to 4 rows where it fits.
  *   FL_OPT_TIMEOUT_MS:  limit of every device-side wait (default 2000).
  *   FL_OPT_SPLIT_K:     0 = automatic, else the K split of the small-M kernel (1..8).
  *   FL_OPT_PDL:         1 (default) = launch each kernel with a programmatic

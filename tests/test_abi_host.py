@@ -147,7 +147,7 @@ def test_swiglu_validation(L):
 def test_options(L):
     assert L.fl_set_option(0, 100) == INVALID
     assert L.fl_set_option(0, 256) == OK and L.fl_set_option(0, 0) == OK
-    assert L.fl_set_option(1, 4) == INVALID and L.fl_set_option(1, 3) == OK and L.fl_set_option(1, 0) == OK
+    assert L.fl_set_option(1, 5) == INVALID and L.fl_set_option(1, 4) == OK and L.fl_set_option(1, 0) == OK
     assert L.fl_set_option(2, 0) == INVALID and L.fl_set_option(2, 2000) == OK
     assert L.fl_set_option(3, 9) == INVALID and L.fl_set_option(3, 0) == OK
     assert L.fl_set_option(4, 2) == INVALID and L.fl_set_option(4, 0) == OK and L.fl_set_option(4, 1) == OK
