@@ -12,8 +12,9 @@
 // dot product per activation row, adds them across the warp with a fixed
 // butterfly and applies the epilogue (row scale, bias, activation, residual).
 // No reduction crosses a warp, so there is no cluster, no tensor memory and
-// no exchange. Weight rows are dealt to warps round-robin over the grid, so
-// every SM streams the same number of bytes to within one row.
+// no exchange. Weight rows are dealt to warps round-robin over the grid, CTA
+// by CTA, so every SM streams the same number of bytes to within one row, and
+// each warp keeps two rows' loads in flight.
 //
 // The FFN kernel runs the gate/up product (h = silu(g) * u, rounded once),
 // then a grid-wide barrier, then the down projection with the residual, in
@@ -32,119 +33,176 @@ namespace {
 constexpr int kGemvThreads = 256;
 constexpr int kGemvWarps = kGemvThreads / 32;
 constexpr int kVec = 8;                 // 16-bit elements per 16-byte vector
-constexpr int kChunk = 16;              // vectors per lane in flight (16 x 8 x 32 = 4096 elements per warp)
 
 // Rows of the prologue-transformed activation, in shared memory: xs[m][k],
 // M <= MAXM rows of K 16-bit values; rscale[m] = the RMS row scale (else 1).
+// Every thread loads its share of the raw rows at once (one memory round
+// trip), the row statistics are added in a fixed order (per-thread partials,
+// warp butterflies, then the warps in index order), and the fold rewrites the
+// rows in place in shared memory.
 template <int DT, int PRO, int MAXM>
 __device__ void build_rows(const GemvParams& p, uint16_t* xs, float* rscale) {
     using Ops = DTypeOps<DT>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int M = p.M, K = p.K;
+    const int M = p.M, K = p.K, kv = K / kVec, vecs = M * kv;
+    __shared__ float part[kGemvWarps][MAXM][2];
     __shared__ float st_mean[MAXM], st_rstd[MAXM];
-    // per-row statistics: one warp per row
-    if (warp < M) {
-        const uint16_t* xr = p.x + (size_t)warp * K;
-        float s1 = 0.f, s2 = 0.f, c = 0.f;
-        if (PRO == PRO_LN) {
-            // shift by the mean of the row's first eight values (no cancellation)
-            const uint4 h = ldg_v4(xr);
+    // LayerNorm shifts each row by the mean of its first eight values
+    float c[MAXM];
+#pragma unroll
+    for (int m = 0; m < MAXM; ++m) {
+        c[m] = 0.f;
+        if (PRO == PRO_LN && m < M) {
+            const uint4 h = ldg_v4(p.x + (size_t)m * K);
             const float2 a = Ops::unpack(h.x), b = Ops::unpack(h.y), d = Ops::unpack(h.z), e = Ops::unpack(h.w);
-            c = (((a.x + a.y) + (b.x + b.y)) + ((d.x + d.y) + (e.x + e.y))) * 0.125f;
-        }
-        for (int k = lane * kVec; k < K; k += 32 * kVec) {
-            const uint4 v = ldg_v4(xr + k);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 f = Ops::unpack(w[e]);
-                const float d0 = f.x - c, d1 = f.y - c;
-                s1 += d0 + d1;
-                s2 = fmaf(d0, d0, fmaf(d1, d1, s2));
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            s1 += __shfl_xor_sync(0xffffffffu, s1, o);
-            s2 += __shfl_xor_sync(0xffffffffu, s2, o);
-        }
-        if (lane == 0) {
-            const float inv_k = 1.0f / (float)K;
-            if (PRO == PRO_RMS) {
-                rscale[warp] = rsqrtf(s2 * inv_k + p.eps);
-            } else if (PRO == PRO_LN) {
-                const float d = s1 * inv_k;
-                st_mean[warp] = c + d;
-                st_rstd[warp] = rsqrtf(fmaxf(fmaf(-d, d, s2 * inv_k), 0.f) + p.eps);
-                rscale[warp] = 1.f;
-            } else {
-                rscale[warp] = 1.f;
-            }
+            c[m] = (((a.x + a.y) + (b.x + b.y)) + ((d.x + d.y) + (e.x + e.y))) * 0.125f;
         }
     }
-    __syncthreads();
-    // the fold, rounded once to the dtype
-    const int vecs = M * (K / kVec);
-    for (int i = threadIdx.x; i < vecs; i += blockDim.x) {
-        const int m = i / (K / kVec), k = (i % (K / kVec)) * kVec;
-        const uint4 v = ldg_v4(p.x + (size_t)m * K + k);
-        uint4 o = v;
-        if (PRO == PRO_RMS) {
-            const uint4 g = ldg_v4(p.gamma + k);
-            o = make_uint4(Ops::mul2(v.x, g.x), Ops::mul2(v.y, g.y), Ops::mul2(v.z, g.z), Ops::mul2(v.w, g.w));
-        } else if (PRO == PRO_ADD) {
-            const uint4 g = ldg_v4(p.gamma + k);
-            o = make_uint4(Ops::add2(v.x, g.x), Ops::add2(v.y, g.y), Ops::add2(v.z, g.z), Ops::add2(v.w, g.w));
-        } else if (PRO == PRO_LN) {
-            const uint4 g = ldg_v4(p.gamma + k);
-            const uint4 b = p.beta != nullptr ? ldg_v4(p.beta + k) : make_uint4(0u, 0u, 0u, 0u);
-            const float mean = st_mean[m], rstd = st_rstd[m];
-            const uint32_t xw[4] = {v.x, v.y, v.z, v.w}, gw[4] = {g.x, g.y, g.z, g.w}, bw[4] = {b.x, b.y, b.z, b.w};
-            uint32_t ow[4];
+    float s1[MAXM], s2[MAXM];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 f = Ops::unpack(xw[e]), gg = Ops::unpack(gw[e]), bb = Ops::unpack(bw[e]);
-                ow[e] = Ops::pack(fmaf((f.x - mean) * rstd, gg.x, bb.x), fmaf((f.y - mean) * rstd, gg.y, bb.y));
-            }
-            o = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+    for (int m = 0; m < MAXM; ++m) s1[m] = s2[m] = 0.f;
+    constexpr int U = 4;
+    for (int i0 = threadIdx.x; i0 < vecs; i0 += U * kGemvThreads) {
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = i0 + u * kGemvThreads;
+            if (i < vecs) v[u] = ldg_v4(p.x + (size_t)(i / kv) * K + (size_t)(i % kv) * kVec);
         }
-        *reinterpret_cast<uint4*>(xs + (size_t)m * K + k) = o;
-    }
-    __syncthreads();
-}
-
-// acc[m] += sum over this lane's part of the row of xs[m][k] * w[k]: one
-// weight row of K values, lanes taking 16-byte vectors at a 512-byte stride,
-// up to kChunk vectors in flight per lane.
-template <int DT, int MAXM>
-__device__ __forceinline__ void dot_row(const uint16_t* __restrict__ w, const uint16_t* xs, int M, int K, int lane,
-                                        float (&acc)[MAXM]) {
-    using Ops = DTypeOps<DT>;
-    for (int k0 = lane * kVec; k0 < K; k0 += 32 * kVec * kChunk) {
-        uint4 v[kChunk];
 #pragma unroll
-        for (int u = 0; u < kChunk; ++u)
-            if (k0 + u * 32 * kVec < K) v[u] = ldg_v4(w + k0 + u * 32 * kVec);
+        for (int u = 0; u < U; ++u) {
+            const int i = i0 + u * kGemvThreads;
+            if (i < vecs) {
+                const int m = i / kv;
+                *reinterpret_cast<uint4*>(xs + (size_t)m * K + (size_t)(i % kv) * kVec) = v[u];
+                if (PRO == PRO_RMS || PRO == PRO_LN) {
+                    const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
-        for (int u = 0; u < kChunk; ++u) {
-            const int k = k0 + u * 32 * kVec;
-            if (k < K) {
-                const uint32_t ww[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-                float2 wf[4];
+                    for (int mm = 0; mm < MAXM; ++mm) {
+                        if (mm == m) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) wf[e] = Ops::unpack(ww[e]);
-#pragma unroll
-                for (int m = 0; m < MAXM; ++m) {
-                    if (m < M) {
-                        const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)m * K + k);
-                        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 xf = Ops::unpack(xw[e]);
-                            acc[m] = fmaf(xf.x, wf[e].x, fmaf(xf.y, wf[e].y, acc[m]));
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 f = Ops::unpack(w[e]);
+                                const float d0 = f.x - c[mm], d1 = f.y - c[mm];
+                                s1[mm] += d0 + d1;
+                                s2[mm] = fmaf(d0, d0, fmaf(d1, d1, s2[mm]));
+                            }
                         }
                     }
                 }
+            }
+        }
+    }
+    if (PRO == PRO_RMS || PRO == PRO_LN) {
+#pragma unroll
+        for (int m = 0; m < MAXM; ++m) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                s1[m] += __shfl_xor_sync(0xffffffffu, s1[m], o);
+                s2[m] += __shfl_xor_sync(0xffffffffu, s2[m], o);
+            }
+            if (lane == 0) {
+                part[warp][m][0] = s1[m];
+                part[warp][m][1] = s2[m];
+            }
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x < MAXM) {
+        const int m = threadIdx.x;
+        float a1 = 0.f, a2 = 0.f;
+        if (PRO == PRO_RMS || PRO == PRO_LN)
+            for (int w = 0; w < kGemvWarps; ++w) {
+                a1 += part[w][m][0];
+                a2 += part[w][m][1];
+            }
+        const float inv_k = 1.0f / (float)K;
+        rscale[m] = PRO == PRO_RMS ? rsqrtf(a2 * inv_k + p.eps) : 1.f;
+        if (PRO == PRO_LN) {
+            const float d = a1 * inv_k;
+            st_mean[m] = c[m] + d;
+            st_rstd[m] = rsqrtf(fmaxf(fmaf(-d, d, a2 * inv_k), 0.f) + p.eps);
+        }
+    }
+    __syncthreads();
+    // the fold, in place, rounded once to the dtype
+    if (PRO != PRO_NONE) {
+        for (int i = threadIdx.x; i < vecs; i += kGemvThreads) {
+            const int m = i / kv, k = (i % kv) * kVec;
+            uint4* slot = reinterpret_cast<uint4*>(xs + (size_t)m * K + k);
+            const uint4 v = *slot;
+            const uint4 g = ldg_v4(p.gamma + k);
+            uint4 o;
+            if (PRO == PRO_RMS) {
+                o = make_uint4(Ops::mul2(v.x, g.x), Ops::mul2(v.y, g.y), Ops::mul2(v.z, g.z), Ops::mul2(v.w, g.w));
+            } else if (PRO == PRO_ADD) {
+                o = make_uint4(Ops::add2(v.x, g.x), Ops::add2(v.y, g.y), Ops::add2(v.z, g.z), Ops::add2(v.w, g.w));
+            } else {
+                const uint4 b = p.beta != nullptr ? ldg_v4(p.beta + k) : make_uint4(0u, 0u, 0u, 0u);
+                const float mean = st_mean[m], rstd = st_rstd[m];
+                const uint32_t xw[4] = {v.x, v.y, v.z, v.w}, gw[4] = {g.x, g.y, g.z, g.w},
+                               bw[4] = {b.x, b.y, b.z, b.w};
+                uint32_t ow[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = Ops::unpack(xw[e]), gg = Ops::unpack(gw[e]), bb = Ops::unpack(bw[e]);
+                    ow[e] = Ops::pack(fmaf((f.x - mean) * rstd, gg.x, bb.x), fmaf((f.y - mean) * rstd, gg.y, bb.y));
+                }
+                o = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+            }
+            *slot = o;
+        }
+        __syncthreads();
+    }
+}
+
+// Two weight rows at once (a and b; b may be null): acc_a[m] += xs[m] . a and
+// acc_b[m] += xs[m] . b over this lane's part of the K values, lanes taking
+// 16-byte vectors at a 512-byte stride, both rows' loads of a chunk issued
+// before any is used (2 x kChunk2 vectors in flight per lane).
+constexpr int kChunk2 = 8;
+
+template <int DT, int MAXM>
+__device__ __forceinline__ void fma_vec(const uint4& wv, const uint16_t* xs, int M, int K, int k, float (&acc)[MAXM]) {
+    using Ops = DTypeOps<DT>;
+    const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+    float2 wf[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) wf[e] = Ops::unpack(ww[e]);
+#pragma unroll
+    for (int m = 0; m < MAXM; ++m) {
+        if (m < M) {
+            const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)m * K + k);
+            const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 xf = Ops::unpack(xw[e]);
+                acc[m] = fmaf(xf.x, wf[e].x, fmaf(xf.y, wf[e].y, acc[m]));
+            }
+        }
+    }
+}
+
+template <int DT, int MAXM>
+__device__ __forceinline__ void dot_rows2(const uint16_t* __restrict__ a, const uint16_t* __restrict__ b,
+                                          const uint16_t* xs, int M, int K, int lane, float (&acc_a)[MAXM],
+                                          float (&acc_b)[MAXM]) {
+    for (int k0 = lane * kVec; k0 < K; k0 += 32 * kVec * kChunk2) {
+        uint4 va[kChunk2], vb[kChunk2];
+#pragma unroll
+        for (int u = 0; u < kChunk2; ++u) {
+            const int k = k0 + u * 32 * kVec;
+            if (k < K) {
+                va[u] = ldg_v4(a + k);
+                if (b != nullptr) vb[u] = ldg_v4(b + k);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kChunk2; ++u) {
+            const int k = k0 + u * 32 * kVec;
+            if (k < K) {
+                fma_vec<DT, MAXM>(va[u], xs, M, K, k, acc_a);
+                if (b != nullptr) fma_vec<DT, MAXM>(vb[u], xs, M, K, k, acc_b);
             }
         }
     }
@@ -174,7 +232,9 @@ __global__ void __launch_bounds__(kGemvThreads) fl_gemv_kernel(const __grid_cons
     uint16_t* xs = reinterpret_cast<uint16_t*>(smem);
     __shared__ float rscale[MAXM];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int gw = blockIdx.x * kGemvWarps + warp, nw = gridDim.x * kGemvWarps;
+    // warp-major numbering: consecutive rows go to different CTAs, so every SM
+    // gets the same number of rows to within one
+    const int gw = warp * gridDim.x + blockIdx.x, nw = gridDim.x * kGemvWarps;
     const int rows = p.row0[p.n_out];
     auto row_of = [&](int r, int& oi, int& n) {
         oi = 0;
@@ -191,15 +251,10 @@ __global__ void __launch_bounds__(kGemvThreads) fl_gemv_kernel(const __grid_cons
     griddep_wait();
     build_rows<DT, PRO, MAXM>(p, xs, rscale);
     griddep_launch_dependents();
-    for (int r = gw; r < rows; r += nw) {
+    // lane m finishes output row m of weight row r
+    auto finish = [&](int r, const float (&acc)[MAXM]) {
         int oi, n;
         row_of(r, oi, n);
-        float acc[MAXM];
-#pragma unroll
-        for (int m = 0; m < MAXM; ++m) acc[m] = 0.f;
-        dot_row<DT, MAXM>(p.W[oi] + (size_t)n * p.K, xs, p.M, p.K, lane, acc);
-        warp_allreduce<MAXM>(acc);
-        // lane m finishes output row m of column n
 #pragma unroll
         for (int m = 0; m < MAXM; ++m) {
             if (lane == m && m < p.M) {
@@ -210,6 +265,24 @@ __global__ void __launch_bounds__(kGemvThreads) fl_gemv_kernel(const __grid_cons
                 const uint32_t packed = Ops::pack(v, 0.f);
                 p.out[oi][(size_t)m * p.N[oi] + n] = (uint16_t)(packed & 0xffffu);
             }
+        }
+    };
+    // two of this warp's rows per pass (r and r + nw), loads of both in flight
+    for (int r = gw; r < rows; r += 2 * nw) {
+        const int r2 = r + nw;
+        int oi, n, oi2 = 0, n2 = 0;
+        row_of(r, oi, n);
+        if (r2 < rows) row_of(r2, oi2, n2);
+        float acc[MAXM], acc2[MAXM];
+#pragma unroll
+        for (int m = 0; m < MAXM; ++m) acc[m] = acc2[m] = 0.f;
+        dot_rows2<DT, MAXM>(p.W[oi] + (size_t)n * p.K, r2 < rows ? p.W[oi2] + (size_t)n2 * p.K : nullptr, xs, p.M,
+                            p.K, lane, acc, acc2);
+        warp_allreduce<MAXM>(acc);
+        finish(r, acc);
+        if (r2 < rows) {
+            warp_allreduce<MAXM>(acc2);
+            finish(r2, acc2);
         }
     }
 }
@@ -252,7 +325,9 @@ __global__ void __launch_bounds__(kGemvThreads) fl_ffn_decode_kernel(const __gri
     uint16_t* xs = reinterpret_cast<uint16_t*>(smem);
     __shared__ float rscale[MAXM];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int gw = blockIdx.x * kGemvWarps + warp, nw = gridDim.x * kGemvWarps;
+    // warp-major numbering: consecutive rows go to different CTAs, so every SM
+    // gets the same number of rows to within one
+    const int gw = warp * gridDim.x + blockIdx.x, nw = gridDim.x * kGemvWarps;
     const int M = q.M, D = q.D, F = q.F;
     if (gw < F) {
         prefetch_row(q.Wg + (size_t)gw * D, D, lane);
@@ -273,8 +348,7 @@ __global__ void __launch_bounds__(kGemvThreads) fl_ffn_decode_kernel(const __gri
         float g[MAXM], u[MAXM];
 #pragma unroll
         for (int m = 0; m < MAXM; ++m) g[m] = u[m] = 0.f;
-        dot_row<DT, MAXM>(q.Wg + (size_t)f * D, xs, M, D, lane, g);
-        dot_row<DT, MAXM>(q.Wu + (size_t)f * D, xs, M, D, lane, u);
+        dot_rows2<DT, MAXM>(q.Wg + (size_t)f * D, q.Wu + (size_t)f * D, xs, M, D, lane, g, u);
         warp_allreduce<MAXM>(g);
         warp_allreduce<MAXM>(u);
 #pragma unroll
@@ -291,18 +365,23 @@ __global__ void __launch_bounds__(kGemvThreads) fl_ffn_decode_kernel(const __gri
     if (!ok) return;
     // phase 2: out = h Wd^T (+ bias_down) + x, h staged from L2 (not L1: it was
     // written by other SMs during this launch)
-    for (int i = threadIdx.x; i < M * (F / kVec); i += blockDim.x) {
-        const int m = i / (F / kVec), k = (i % (F / kVec)) * kVec;
-        *reinterpret_cast<uint4*>(xs + (size_t)m * F + k) =
-            __ldcg(reinterpret_cast<const uint4*>(q.h + (size_t)m * F + k));
+    {
+        // h is M * F / 8 vectors: every thread's share issued at once
+        const int hv = M * (F / kVec);
+        constexpr int U = 8;
+        for (int i0 = threadIdx.x; i0 < hv; i0 += U * kGemvThreads) {
+            uint4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (i0 + u * kGemvThreads < hv)
+                    v[u] = __ldcg(reinterpret_cast<const uint4*>(q.h) + i0 + u * kGemvThreads);
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (i0 + u * kGemvThreads < hv) reinterpret_cast<uint4*>(xs)[i0 + u * kGemvThreads] = v[u];
+        }
     }
     __syncthreads();
-    for (int d = gw; d < D; d += nw) {
-        float acc[MAXM];
-#pragma unroll
-        for (int m = 0; m < MAXM; ++m) acc[m] = 0.f;
-        dot_row<DT, MAXM>(q.Wd + (size_t)d * F, xs, M, F, lane, acc);
-        warp_allreduce<MAXM>(acc);
+    auto finish = [&](int d, const float (&acc)[MAXM]) {
 #pragma unroll
         for (int m = 0; m < MAXM; ++m) {
             if (lane == m && m < M) {
@@ -311,6 +390,19 @@ __global__ void __launch_bounds__(kGemvThreads) fl_ffn_decode_kernel(const __gri
                 v += Ops::unpack(q.x[(size_t)m * D + d] | 0u).x;
                 q.out[(size_t)m * D + d] = (uint16_t)(Ops::pack(v, 0.f) & 0xffffu);
             }
+        }
+    };
+    for (int d = gw; d < D; d += 2 * nw) {
+        const int d2 = d + nw;
+        float acc[MAXM], acc2[MAXM];
+#pragma unroll
+        for (int m = 0; m < MAXM; ++m) acc[m] = acc2[m] = 0.f;
+        dot_rows2<DT, MAXM>(q.Wd + (size_t)d * F, d2 < D ? q.Wd + (size_t)d2 * F : nullptr, xs, M, F, lane, acc, acc2);
+        warp_allreduce<MAXM>(acc);
+        finish(d, acc);
+        if (d2 < D) {
+            warp_allreduce<MAXM>(acc2);
+            finish(d2, acc2);
         }
     }
 }
