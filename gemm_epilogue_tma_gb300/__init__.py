@@ -60,6 +60,7 @@ SIGNATURES = {
     "fl_graph_destroy": (None, [_vp]),
     "fl_launch_cache_stats": (_i, [ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_longlong)]),
     "fl_launch_cache_clear": (None, []),
+    "fl_kernel_launches": (_i, [ctypes.POINTER(ctypes.c_longlong)]),
     "fl_last_error": (ctypes.c_char_p, []),
     "fl_device_status": (_i, [_vp]),
     "fl_set_option": (_i, [_i, _i]),
@@ -354,6 +355,13 @@ def launch_cache_stats():
 
 def launch_cache_clear() -> None:
     lib().fl_launch_cache_clear()
+
+
+def kernel_launches() -> int:
+    """Kernels the library has launched (or recorded into a capture) since it was loaded."""
+    n = ctypes.c_longlong()
+    _check(lib().fl_kernel_launches(ctypes.byref(n)))
+    return n.value
 
 
 def device_status(stream=None) -> None:

@@ -1,28 +1,30 @@
-// Decode kernels for one to four activation rows: the dense layer as a
-// weight-streaming matrix-vector product on the CUDA cores, and the whole
-// SwiGLU FFN block in one launch.
+// Decode kernel for one to eight activation rows: the dense layer (and the
+// SwiGLU gate/up pair) as a weight-streaming matrix-vector product.
 //
-// With M <= 4 rows a 128-row tensor-core MMA is more than 97 % padding and the
+// With M <= 8 rows a 128-row tcgen05 MMA is more than 93 % padding and the
 // step is bound by reading the weights once from HBM; what decides its time
-// is how early the weight stream starts and how little fixed work surrounds
-// it. Here every CTA builds the prologue-transformed activation rows in
-// shared memory (RMSNorm / LayerNorm statistics of the few rows, then the
-// fold, rounded once to the dtype as in the tensor-core kernels), and every
-// warp streams whole weight rows with 16-byte loads, keeps one fp32 partial
-// dot product per activation row, adds them across the warp with a fixed
-// butterfly and applies the epilogue (row scale, bias, activation, residual).
-// No reduction crosses a warp, so there is no cluster, no tensor memory and
-// no exchange. Weight rows are dealt to warps round-robin over the grid, CTA
-// by CTA, so every SM streams the same number of bytes to within one row, and
-// each warp keeps two rows' loads in flight.
+// is how early the weight stream starts, how many bytes each SM keeps in
+// flight, and how little fixed work surrounds it. Here the weights are the
+// B operand of warp-level m16n8k16 tensor-core MMAs fed straight from
+// registers: each lane loads 16-byte weight vectors (8 consecutive k of one
+// row) with non-allocating global loads, in blocks of 8 per lane, double
+// buffered so the next block's loads are in flight while the current block's
+// MMAs run (the first block is issued before the activation rows arrive).
+// The activation rows (at most 8, the A operand's rows 0..7; rows 8..15 are
+// zero) come from shared memory. Inside each 32-wide k chunk the MMA's k
+// order is a fixed permutation of the physical one, applied identically to
+// both operands (lane quad t holds physical k = 8t .. 8t+7 as the MMA's
+// k = 2t, 2t+1, 2t+8, 2t+9 of two consecutive MMAs), so a dot product's terms
+// are the same; the fp32 accumulation order differs from the tcgen05 kernels'
+// but is fixed, so results are bit-reproducible.
 //
-// The FFN kernel runs the gate/up product (h = silu(g) * u, rounded once),
-// then a grid-wide barrier, then the down projection with the residual, in
-// one launch: h goes to the caller's workspace and is read back through L2,
-// never waiting on a second launch. Its grid is sized so every CTA is
-// resident, and it lets the next kernel on the stream in only after the
-// barrier, so a dependent grid cannot take the slots its CTAs need. Every
-// wait is bounded.
+// The unit of work is a block of 8 weight rows; a CTA's 8 warps split its K
+// range into 8 slices and add their partial sums through shared memory in
+// warp order. Every CTA builds the prologue-transformed activation rows in
+// shared memory (RMSNorm / LayerNorm statistics of the few rows, then the
+// fold, rounded once to the dtype as in the tcgen05 kernels). The epilogue
+// (RMS row scale, bias, activation, residual; or for the gate/up pair
+// h = silu(g) * u) is applied to the reduced sums.
 #include "fl_common.cuh"
 #include "fl_internal.h"
 
@@ -32,384 +34,442 @@ namespace {
 
 constexpr int kGemvThreads = 256;
 constexpr int kGemvWarps = kGemvThreads / 32;
-constexpr int kVec = 8;                 // 16-bit elements per 16-byte vector
+constexpr int kVec = 8;      // 16-bit elements per 16-byte vector
+constexpr int kChunk = 32;   // k values per MMA pair: 4 lanes x 8
+constexpr int kBlock = 8;    // 16-byte weight vectors per lane per register block
 
-// Rows of the prologue-transformed activation, in shared memory: xs[m][k],
-// M <= MAXM rows of K 16-bit values; rscale[m] = the RMS row scale (else 1).
-// Every thread loads its share of the raw rows at once (one memory round
-// trip), the row statistics are added in a fixed order (per-thread partials,
-// warp butterflies, then the warps in index order), and the fold rewrites the
-// rows in place in shared memory.
-template <int DT, int PRO, int MAXM>
-__device__ void build_rows(const GemvParams& p, uint16_t* xs, float* rscale) {
-    using Ops = DTypeOps<DT>;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int M = p.M, K = p.K, kv = K / kVec, vecs = M * kv;
-    __shared__ float part[kGemvWarps][MAXM][2];
-    __shared__ float st_mean[MAXM], st_rstd[MAXM];
-    // LayerNorm shifts each row by the mean of its first eight values
-    float c[MAXM];
+// Row stride of the activation rows in shared memory, in elements: a multiple
+// of 64 plus 32 (128 k-bytes + 64), so the 8 lanes of a quarter warp (two
+// rows, four 16-byte vectors each) hit 32 different banks.
+__host__ __device__ __forceinline__ int xs_stride(int K) { return (K + 63) / 64 * 64 + 32; }
+
+// Shared memory of one CTA: the activation rows, then for LayerNorm gamma
+// and beta.
+__host__ __device__ __forceinline__ int smem_bytes(int M, int K, int pro) {
+    return (M * xs_stride(K) + (pro == PRO_LN ? 2 * K : 0)) * 2;
+}
+
+__device__ __forceinline__ uint4 ld_stream(const uint16_t* p) {
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
+    return v;
+}
+
+// D[16x8] += A[16x16] B[16x8], fp32 accumulate; A rows 8..15 are zero.
+template <int DT>
+__device__ __forceinline__ void mma_rows8(float (&c)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+    if constexpr (DT == 0) {
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+            "{%0, %1, %2, %3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+    } else {
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+            "{%0, %1, %2, %3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+    }
+}
+
+// One 32-wide k chunk: lane (g, t) holds physical k = 8t .. 8t+7 of its
+// activation row (xv) and of its weight row (wv).
+template <int DT>
+__device__ __forceinline__ void mma_chunk(float (&c)[4], const uint4& xv, const uint4& wv) {
+    mma_rows8<DT>(c, xv.x, xv.y, wv.x, wv.y);
+    mma_rows8<DT>(c, xv.z, xv.w, wv.z, wv.w);
+}
+
+// This warp's slice of the K chunks: [c0, c1).
+struct Slice {
+    int c0, c1;
+};
+__device__ __forceinline__ Slice warp_slice(int K, int warp) {
+    const int chunks = (K + kChunk - 1) / kChunk, per = (chunks + kGemvWarps - 1) / kGemvWarps;
+    const int c0 = min(chunks, warp * per);
+    return {c0, min(chunks, c0 + per)};
+}
+
+// L2 prefetch of the lines this lane will read first from one weight row
+// (before the dependency wait: weights are not written by the previous
+// kernel, and L2 is the point of coherence, so a prefetch cannot bring in
+// stale data).
+__device__ __forceinline__ void prefetch_slice(const uint16_t* row, Slice s, int t) {
+    for (int c = s.c0 + 2 * t; c < s.c1 && c < s.c0 + 2 * kBlock; c += 8)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(row + (size_t)c * kChunk));
+}
+
+// One block of a warp's weight stream: kBlock / NW consecutive chunks of its
+// K slice, for NW weight matrices read with the same activation rows, in
+// registers (kBlock 16-byte vectors per lane).
+template <int NW>
+struct WBlock {
+    static constexpr int U = kBlock / NW;
+    uint4 w[NW][U];
+};
+
+// Issues the loads of block b (chunks s.c0 + b*U ..) of the unit whose
+// weight rows (this lane's row g, one per matrix) are rows[]; zeros past K.
+template <int NW>
+__device__ __forceinline__ void load_block(WBlock<NW>& B, const uint16_t* const (&rows)[NW], int b, Slice s, int K,
+                                           int t) {
+    constexpr int U = WBlock<NW>::U;
 #pragma unroll
-    for (int m = 0; m < MAXM; ++m) {
-        c[m] = 0.f;
-        if (PRO == PRO_LN && m < M) {
-            const uint4 h = ldg_v4(p.x + (size_t)m * K);
-            const float2 a = Ops::unpack(h.x), b = Ops::unpack(h.y), d = Ops::unpack(h.z), e = Ops::unpack(h.w);
-            c[m] = (((a.x + a.y) + (b.x + b.y)) + ((d.x + d.y) + (e.x + e.y))) * 0.125f;
+    for (int i = 0; i < U; ++i) {
+        const int c = s.c0 + b * U + i, k = c * kChunk + 8 * t;
+        const bool in = c < s.c1 && k < K;
+#pragma unroll
+        for (int j = 0; j < NW; ++j) B.w[j][i] = in ? ld_stream(rows[j] + k) : make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+// acc[j] += activation rows . block b of matrix j.
+template <int DT, int NW>
+__device__ __forceinline__ void mma_block(const WBlock<NW>& B, const uint16_t* xrow, int b, Slice s, int K, int t,
+                                          float (&acc)[NW][4]) {
+    constexpr int U = WBlock<NW>::U;
+#pragma unroll
+    for (int i = 0; i < U; ++i) {
+        const int c = s.c0 + b * U + i, k = c * kChunk + 8 * t;
+        if (c < s.c1) {  // warp-uniform
+            const uint4 xv = (xrow != nullptr && k < K) ? *reinterpret_cast<const uint4*>(xrow + k)
+                                                        : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int j = 0; j < NW; ++j) mma_chunk<DT>(acc[j], xv, B.w[j][i]);
         }
     }
-    float s1[MAXM], s2[MAXM];
-#pragma unroll
-    for (int m = 0; m < MAXM; ++m) s1[m] = s2[m] = 0.f;
-    constexpr int U = 4;
-    for (int i0 = threadIdx.x; i0 < vecs; i0 += U * kGemvThreads) {
-        uint4 v[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int i = i0 + u * kGemvThreads;
-            if (i < vecs) v[u] = ldg_v4(p.x + (size_t)(i / kv) * K + (size_t)(i % kv) * kVec);
+}
+
+// The units of this CTA (blockIdx.x, + gridDim.x, ..), each an 8-row weight
+// block over all of K: this warp streams its K slice of each unit in
+// register blocks, the loads of the next block (of this unit or the next)
+// issued before the MMAs of the current one, then every warp's partial sums
+// go through shared memory (fixed warp order) to finish(unit, lane sums).
+// A (block 0 of the first unit) must have been loaded by the caller.
+// rows_of(u, rows) gives this lane's weight row of each matrix in unit u.
+template <int DT, int NW, typename RowsOf, typename Finish>
+__device__ __forceinline__ void stream_units(WBlock<NW>& A, int units, int K, const uint16_t* xrow, Slice s,
+                                             RowsOf rows_of, float (*red)[kGemvWarps][32][2 * NW], Finish finish) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t = lane & 3;
+    const int nblk = (s.c1 - s.c0 + WBlock<NW>::U - 1) / WBlock<NW>::U;
+    WBlock<NW> B;
+    int q = 0, buf = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, buf ^= 1) {
+        float acc[NW][4] = {};
+        for (int b = 0; b < nblk; ++b, ++q) {
+            int nu = u, nb = b + 1;
+            if (nb == nblk) {
+                nu += gridDim.x;
+                nb = 0;
+            }
+            const uint16_t* rows[NW];
+            if (nu < units) rows_of(nu, rows);
+            if ((q & 1) == 0) {
+                if (nu < units) load_block<NW>(B, rows, nb, s, K, t);
+                mma_block<DT, NW>(A, xrow, b, s, K, t, acc);
+            } else {
+                if (nu < units) load_block<NW>(A, rows, nb, s, K, t);
+                mma_block<DT, NW>(B, xrow, b, s, K, t, acc);
+            }
         }
+        // lane (g, t): rows m = g, columns 2t, 2t+1 of each matrix
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int i = i0 + u * kGemvThreads;
-            if (i < vecs) {
-                const int m = i / kv;
-                *reinterpret_cast<uint4*>(xs + (size_t)m * K + (size_t)(i % kv) * kVec) = v[u];
-                if (PRO == PRO_RMS || PRO == PRO_LN) {
-                    const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        for (int j = 0; j < NW; ++j) {
+            red[buf][warp][lane][2 * j] = acc[j][0];
+            red[buf][warp][lane][2 * j + 1] = acc[j][1];
+        }
+        __syncthreads();
+        if (warp == 0) {
+            float v[2 * NW];
 #pragma unroll
-                    for (int mm = 0; mm < MAXM; ++mm) {
-                        if (mm == m) {
+            for (int e = 0; e < 2 * NW; ++e) v[e] = red[buf][0][lane][e];
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float2 f = Ops::unpack(w[e]);
-                                const float d0 = f.x - c[mm], d1 = f.y - c[mm];
-                                s1[mm] += d0 + d1;
-                                s2[mm] = fmaf(d0, d0, fmaf(d1, d1, s2[mm]));
+            for (int w = 1; w < kGemvWarps; ++w)
+#pragma unroll
+                for (int e = 0; e < 2 * NW; ++e) v[e] += red[buf][w][lane][e];
+            finish(u, v);
+        }
+        // (red is double-buffered: the next unit writes the other half, and
+        // the one after that only follows the next __syncthreads)
+    }
+}
+
+// Sum over the CTA of one value per activation row, in a fixed order
+// (per-thread partials, warp butterflies, the warps in index order); every
+// thread gets the sums in tot[]. Ends with __syncthreads.
+template <int R>
+__device__ __forceinline__ void row_sums(float (&v)[R], float (*part)[R], float* tot) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+    for (int m = 0; m < R; ++m) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v[m] += __shfl_xor_sync(0xffffffffu, v[m], o);
+        if (lane == 0) part[warp][m] = v[m];
+    }
+    __syncthreads();
+    if (threadIdx.x < R) {
+        float a = 0.f;
+        for (int w = 0; w < kGemvWarps; ++w) a += part[w][threadIdx.x];
+        tot[threadIdx.x] = a;
+    }
+    __syncthreads();
+}
+
+// 16-byte asynchronous copy global -> shared (allocating in L1: the CTAs on
+// one SM read the same rows), and the wait
+// for all of this thread's copies.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// Rows of the prologue-transformed activation, in shared memory: xs[m][k] at
+// row stride xs_stride(K), M <= kGemvMaxRows rows; rscale[m] = the RMS row
+// scale (else 1). Every thread owns the 16-byte columns c = tid, tid + 256,
+// .. of every row. RMSNorm, the input bias and the plain copy load two
+// columns of every row (and of gamma / the bias) into registers at a time,
+// all before using any, and store the folded values (x * gamma or x + bias,
+// rounded once; the RMS scale goes to the epilogue): one memory round trip
+// for K <= 4096. LayerNorm needs its rows three times, so it stages them
+// (and gamma, beta, into the side area after the rows) with asynchronous
+// copies, all in flight at once and holding no registers, takes the
+// corrected two-pass statistics over them (mean, then the sums of
+// d = x - mean and d^2: mean += sum(d) / K, var = sum(d^2) / K -
+// (sum(d) / K)^2) and folds in a third pass; a thread only touches its own
+// columns, so only the row sums need barriers. (Asynchronous or bulk-copy
+// staging of the RMSNorm rows measured about 1 us slower at K = 4096.)
+// R: a bound on M (2, 4 or 8), so the per-row loops unroll to no more rows
+// than there can be.
+template <int DT, int PRO, int R>
+__device__ void build_rows(const GemvParams& p, uint16_t* xs, float* rscale) {
+    using Ops = DTypeOps<DT>;
+    const int M = p.M, K = p.K, kv = K / kVec, ld = xs_stride(K);
+    __shared__ float part[kGemvWarps][R];
+    __shared__ float tot[R], tot2[R], mean_s[R], rstd_s[R];
+    if (PRO != PRO_LN) {
+        constexpr int G = 2;
+        float sq[R];
+#pragma unroll
+        for (int m = 0; m < R; ++m) sq[m] = 0.f;
+        for (int c0 = threadIdx.x; c0 < kv; c0 += G * kGemvThreads) {
+            uint4 v[G][R], gv[G];
+#pragma unroll
+            for (int j = 0; j < G; ++j) {
+                const int c = c0 + j * kGemvThreads;
+                if (c < kv) {
+                    if (PRO != PRO_NONE) gv[j] = ldg_v4(p.gamma + (size_t)c * kVec);
+#pragma unroll
+                    for (int m = 0; m < R; ++m)
+                        if (m < M) v[j][m] = ldg_v4(p.x + (size_t)m * K + (size_t)c * kVec);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < G; ++j) {
+                const int c = c0 + j * kGemvThreads;
+                if (c < kv) {
+#pragma unroll
+                    for (int m = 0; m < R; ++m) {
+                        if (m < M) {
+                            uint4 o = v[j][m];
+                            if (PRO == PRO_RMS) {
+                                const uint32_t w[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const float2 f = Ops::unpack(w[e]);
+                                    sq[m] = fmaf(f.x, f.x, fmaf(f.y, f.y, sq[m]));
+                                }
+                                o = make_uint4(Ops::mul2(o.x, gv[j].x), Ops::mul2(o.y, gv[j].y),
+                                               Ops::mul2(o.z, gv[j].z), Ops::mul2(o.w, gv[j].w));
+                            } else if (PRO == PRO_ADD) {
+                                o = make_uint4(Ops::add2(o.x, gv[j].x), Ops::add2(o.y, gv[j].y),
+                                               Ops::add2(o.z, gv[j].z), Ops::add2(o.w, gv[j].w));
                             }
+                            *reinterpret_cast<uint4*>(xs + (size_t)m * ld + (size_t)c * kVec) = o;
                         }
                     }
                 }
             }
         }
+        if (PRO == PRO_RMS) {
+            row_sums(sq, part, tot);
+            if (threadIdx.x < R) rscale[threadIdx.x] = rsqrtf(tot[threadIdx.x] / (float)K + p.eps);
+        } else if (threadIdx.x < R) {
+            rscale[threadIdx.x] = 1.f;
+        }
+        __syncthreads();
+        return;
     }
-    if (PRO == PRO_RMS || PRO == PRO_LN) {
+    // LayerNorm: stage, row sums, then the deviations from the first mean
+    uint16_t* gs = xs + (size_t)M * ld;  // gamma
+    uint16_t* bs = gs + K;               // beta
+    const bool has_beta = p.beta != nullptr;
+    for (int c = threadIdx.x; c < kv; c += kGemvThreads) {
+        for (int m = 0; m < M; ++m)
+            cp_async16(xs + (size_t)m * ld + (size_t)c * kVec, p.x + (size_t)m * K + (size_t)c * kVec);
+        cp_async16(gs + (size_t)c * kVec, p.gamma + (size_t)c * kVec);
+        if (has_beta) cp_async16(bs + (size_t)c * kVec, p.beta + (size_t)c * kVec);
+    }
+    cp_async_wait_all();
+    float sm[R];
 #pragma unroll
-        for (int m = 0; m < MAXM; ++m) {
+    for (int m = 0; m < R; ++m) sm[m] = 0.f;
+    for (int c = threadIdx.x; c < kv; c += kGemvThreads) {
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                s1[m] += __shfl_xor_sync(0xffffffffu, s1[m], o);
-                s2[m] += __shfl_xor_sync(0xffffffffu, s2[m], o);
-            }
-            if (lane == 0) {
-                part[warp][m][0] = s1[m];
-                part[warp][m][1] = s2[m];
+        for (int m = 0; m < R; ++m) {
+            if (m < M) {
+                const uint4 o = *reinterpret_cast<const uint4*>(xs + (size_t)m * ld + (size_t)c * kVec);
+                const uint32_t w[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = Ops::unpack(w[e]);
+                    sm[m] += f.x + f.y;
+                }
             }
         }
     }
-    __syncthreads();
-    if (threadIdx.x < MAXM) {
-        const int m = threadIdx.x;
-        float a1 = 0.f, a2 = 0.f;
-        if (PRO == PRO_RMS || PRO == PRO_LN)
-            for (int w = 0; w < kGemvWarps; ++w) {
-                a1 += part[w][m][0];
-                a2 += part[w][m][1];
+    row_sums(sm, part, tot);
+    float d1[R], d2[R], mu[R];
+#pragma unroll
+    for (int m = 0; m < R; ++m) {
+        d1[m] = d2[m] = 0.f;
+        mu[m] = tot[m] / (float)K;
+    }
+    for (int c = threadIdx.x; c < kv; c += kGemvThreads) {
+#pragma unroll
+        for (int m = 0; m < R; ++m) {
+            if (m < M) {
+                const float mean = mu[m];
+                const uint4 o = *reinterpret_cast<const uint4*>(xs + (size_t)m * ld + (size_t)c * kVec);
+                const uint32_t w[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = Ops::unpack(w[e]);
+                    const float a = f.x - mean, b = f.y - mean;
+                    d1[m] += a + b;
+                    d2[m] = fmaf(a, a, fmaf(b, b, d2[m]));
+                }
             }
-        const float inv_k = 1.0f / (float)K;
-        rscale[m] = PRO == PRO_RMS ? rsqrtf(a2 * inv_k + p.eps) : 1.f;
-        if (PRO == PRO_LN) {
-            const float d = a1 * inv_k;
-            st_mean[m] = c[m] + d;
-            st_rstd[m] = rsqrtf(fmaxf(fmaf(-d, d, a2 * inv_k), 0.f) + p.eps);
         }
     }
+    row_sums(d1, part, tot2);
+    if (threadIdx.x < R) mean_s[threadIdx.x] = tot[threadIdx.x] / (float)K + tot2[threadIdx.x] / (float)K;
+    row_sums(d2, part, tot);
+    if (threadIdx.x < R) {
+        const float e1 = tot2[threadIdx.x] / (float)K;
+        rstd_s[threadIdx.x] = rsqrtf(fmaxf(tot[threadIdx.x] / (float)K - e1 * e1, 0.f) + p.eps);
+        rscale[threadIdx.x] = 1.f;
+    }
     __syncthreads();
-    // the fold, in place, rounded once to the dtype
-    if (PRO != PRO_NONE) {
-        for (int i = threadIdx.x; i < vecs; i += kGemvThreads) {
-            const int m = i / kv, k = (i % kv) * kVec;
-            uint4* slot = reinterpret_cast<uint4*>(xs + (size_t)m * K + k);
-            const uint4 v = *slot;
-            const uint4 g = ldg_v4(p.gamma + k);
-            uint4 o;
-            if (PRO == PRO_RMS) {
-                o = make_uint4(Ops::mul2(v.x, g.x), Ops::mul2(v.y, g.y), Ops::mul2(v.z, g.z), Ops::mul2(v.w, g.w));
-            } else if (PRO == PRO_ADD) {
-                o = make_uint4(Ops::add2(v.x, g.x), Ops::add2(v.y, g.y), Ops::add2(v.z, g.z), Ops::add2(v.w, g.w));
-            } else {
-                const uint4 b = p.beta != nullptr ? ldg_v4(p.beta + k) : make_uint4(0u, 0u, 0u, 0u);
-                const float mean = st_mean[m], rstd = st_rstd[m];
-                const uint32_t xw[4] = {v.x, v.y, v.z, v.w}, gw[4] = {g.x, g.y, g.z, g.w},
-                               bw[4] = {b.x, b.y, b.z, b.w};
+    for (int c = threadIdx.x; c < kv; c += kGemvThreads) {
+        const uint4 gv = *reinterpret_cast<const uint4*>(gs + (size_t)c * kVec);
+        const uint4 bv =
+            has_beta ? *reinterpret_cast<const uint4*>(bs + (size_t)c * kVec) : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, bw[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+        for (int m = 0; m < R; ++m) {
+            if (m < M) {
+                uint4* slot = reinterpret_cast<uint4*>(xs + (size_t)m * ld + (size_t)c * kVec);
+                const uint4 o = *slot;
+                const uint32_t xw[4] = {o.x, o.y, o.z, o.w};
+                const float mean = mean_s[m], rstd = rstd_s[m];
                 uint32_t ow[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float2 f = Ops::unpack(xw[e]), gg = Ops::unpack(gw[e]), bb = Ops::unpack(bw[e]);
                     ow[e] = Ops::pack(fmaf((f.x - mean) * rstd, gg.x, bb.x), fmaf((f.y - mean) * rstd, gg.y, bb.y));
                 }
-                o = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                *slot = make_uint4(ow[0], ow[1], ow[2], ow[3]);
             }
-            *slot = o;
         }
-        __syncthreads();
     }
+    __syncthreads();
 }
 
-// Two weight rows at once (a and b; b may be null): acc_a[m] += xs[m] . a and
-// acc_b[m] += xs[m] . b over this lane's part of the K values, lanes taking
-// 16-byte vectors at a 512-byte stride, both rows' loads of a chunk issued
-// before any is used (2 x kChunk2 vectors in flight per lane).
-constexpr int kChunk2 = 8;
-
-template <int DT, int MAXM>
-__device__ __forceinline__ void fma_vec(const uint4& wv, const uint16_t* xs, int M, int K, int k, float (&acc)[MAXM]) {
+// DUAL: the SwiGLU gate/up pair, W[0] = Wg and W[1] = Wu, out[0] = h with
+// h = silu(g * rs) * (u * rs) (PRO_RMS only).
+template <int DT, int PRO, bool DUAL>
+__global__ void __launch_bounds__(kGemvThreads, 2) fl_gemv_kernel(const __grid_constant__ GemvParams p) {
     using Ops = DTypeOps<DT>;
-    const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
-    float2 wf[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) wf[e] = Ops::unpack(ww[e]);
-#pragma unroll
-    for (int m = 0; m < MAXM; ++m) {
-        if (m < M) {
-            const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)m * K + k);
-            const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 xf = Ops::unpack(xw[e]);
-                acc[m] = fmaf(xf.x, wf[e].x, fmaf(xf.y, wf[e].y, acc[m]));
-            }
-        }
-    }
-}
-
-template <int DT, int MAXM>
-__device__ __forceinline__ void dot_rows2(const uint16_t* __restrict__ a, const uint16_t* __restrict__ b,
-                                          const uint16_t* xs, int M, int K, int lane, float (&acc_a)[MAXM],
-                                          float (&acc_b)[MAXM]) {
-    for (int k0 = lane * kVec; k0 < K; k0 += 32 * kVec * kChunk2) {
-        uint4 va[kChunk2], vb[kChunk2];
-#pragma unroll
-        for (int u = 0; u < kChunk2; ++u) {
-            const int k = k0 + u * 32 * kVec;
-            if (k < K) {
-                va[u] = ldg_v4(a + k);
-                if (b != nullptr) vb[u] = ldg_v4(b + k);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kChunk2; ++u) {
-            const int k = k0 + u * 32 * kVec;
-            if (k < K) {
-                fma_vec<DT, MAXM>(va[u], xs, M, K, k, acc_a);
-                if (b != nullptr) fma_vec<DT, MAXM>(vb[u], xs, M, K, k, acc_b);
-            }
-        }
-    }
-}
-
-template <int MAXM>
-__device__ __forceinline__ void warp_allreduce(float (&acc)[MAXM]) {
-#pragma unroll
-    for (int m = 0; m < MAXM; ++m)
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], o);
-}
-
-// L2 prefetch of the start of a weight row (before the dependency wait:
-// weights are not written by the previous kernel, and L2 is the point of
-// coherence, so the prefetch cannot bring in stale data).
-__device__ __forceinline__ void prefetch_row(const uint16_t* w, int K, int lane) {
-    const int bytes = K * 2;
-    for (int off = lane * 128; off < bytes && off < 32 * 128 * 2; off += 32 * 128)
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(w) + off));
-}
-
-template <int DT, int PRO, int MAXM>
-__global__ void __launch_bounds__(kGemvThreads) fl_gemv_kernel(const __grid_constant__ GemvParams p) {
-    using Ops = DTypeOps<DT>;
+    constexpr int NW = DUAL ? 2 : 1;
     extern __shared__ __align__(16) uint8_t smem[];
     uint16_t* xs = reinterpret_cast<uint16_t*>(smem);
-    __shared__ float rscale[MAXM];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // warp-major numbering: consecutive rows go to different CTAs, so every SM
-    // gets the same number of rows to within one
-    const int gw = warp * gridDim.x + blockIdx.x, nw = gridDim.x * kGemvWarps;
-    const int rows = p.row0[p.n_out];
-    auto row_of = [&](int r, int& oi, int& n) {
+    __shared__ float rscale[kGemvMaxRows];
+    __shared__ float red[2][kGemvWarps][32][2 * NW];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int K = p.K, units = p.row0[p.n_out] / 8;
+    const Slice s = warp_slice(K, warp);
+    // output i, first row n of the 8-row unit u
+    auto unit_of = [&](int u, int& oi, int& n) {
+        const int r = u * 8;
         oi = 0;
 #pragma unroll
         for (int i = 1; i < 4; ++i)
             if (i < p.n_out && r >= p.row0[i]) oi = i;
         n = r - p.row0[oi];
     };
-    if (gw < rows) {
+    auto rows_of = [&](int u, const uint16_t* (&rows)[NW]) {
         int oi, n;
-        row_of(gw, oi, n);
-        prefetch_row(p.W[oi] + (size_t)n * p.K, p.K, lane);
+        unit_of(u, oi, n);
+        rows[0] = p.W[oi] + (size_t)(n + g) * K;
+        if constexpr (DUAL) rows[NW - 1] = p.W[1] + (size_t)(n + g) * K;
+    };
+    const bool first = (int)blockIdx.x < units;
+    const uint16_t* rows0[NW] = {};
+    if (first) {
+        rows_of(blockIdx.x, rows0);
+#pragma unroll
+        for (int j = 0; j < NW; ++j) prefetch_slice(rows0[j], s, t);
     }
     griddep_wait();
-    build_rows<DT, PRO, MAXM>(p, xs, rscale);
+    // the first weight block is in flight while the activation rows are staged
+    WBlock<NW> A;
+    if (first) load_block<NW>(A, rows0, 0, s, K, t);
+    if (p.M <= 2)
+        build_rows<DT, PRO, 2>(p, xs, rscale);
+    else if (p.M <= 4)
+        build_rows<DT, PRO, 4>(p, xs, rscale);
+    else
+        build_rows<DT, PRO, kGemvMaxRows>(p, xs, rscale);
     griddep_launch_dependents();
-    // lane m finishes output row m of weight row r
-    auto finish = [&](int r, const float (&acc)[MAXM]) {
-        int oi, n;
-        row_of(r, oi, n);
-#pragma unroll
-        for (int m = 0; m < MAXM; ++m) {
-            if (lane == m && m < p.M) {
-                float v = acc[m] * rscale[m];
-                if (p.bias[oi] != nullptr) v += Ops::unpack(p.bias[oi][n] | 0u).x;
-                v = act_apply(p.act[oi], v);
-                if (p.residual != nullptr) v += Ops::unpack(p.residual[(size_t)m * p.N[oi] + n] | 0u).x;
-                const uint32_t packed = Ops::pack(v, 0.f);
-                p.out[oi][(size_t)m * p.N[oi] + n] = (uint16_t)(packed & 0xffffu);
+    const uint16_t* xrow = g < p.M ? xs + (size_t)g * xs_stride(K) : nullptr;
+    // lane (g, t) finishes output row m = g, columns n0 + 2t, 2t+1
+    auto finish = [&](int u, const float (&v)[2 * NW]) {
+        if (g >= p.M) return;
+        int oi, n0;
+        unit_of(u, oi, n0);
+        const int m = g, n = n0 + 2 * t, N = p.N[oi];
+        const float rs = rscale[m];
+        float y0, y1;
+        if constexpr (DUAL) {
+            y0 = act_apply(ACT_SILU, v[0] * rs) * (v[2] * rs);
+            y1 = act_apply(ACT_SILU, v[1] * rs) * (v[3] * rs);
+        } else {
+            y0 = v[0] * rs;
+            y1 = v[1] * rs;
+            if (p.bias[oi] != nullptr) {
+                const float2 b = Ops::unpack(*reinterpret_cast<const uint32_t*>(p.bias[oi] + n));
+                y0 += b.x;
+                y1 += b.y;
+            }
+            y0 = act_apply(p.act[oi], y0);
+            y1 = act_apply(p.act[oi], y1);
+            if (p.residual != nullptr) {
+                const float2 r = Ops::unpack(*reinterpret_cast<const uint32_t*>(p.residual + (size_t)m * N + n));
+                y0 += r.x;
+                y1 += r.y;
             }
         }
+        *reinterpret_cast<uint32_t*>(p.out[oi] + (size_t)m * N + n) = Ops::pack(y0, y1);
     };
-    // two of this warp's rows per pass (r and r + nw), loads of both in flight
-    for (int r = gw; r < rows; r += 2 * nw) {
-        const int r2 = r + nw;
-        int oi, n, oi2 = 0, n2 = 0;
-        row_of(r, oi, n);
-        if (r2 < rows) row_of(r2, oi2, n2);
-        float acc[MAXM], acc2[MAXM];
-#pragma unroll
-        for (int m = 0; m < MAXM; ++m) acc[m] = acc2[m] = 0.f;
-        dot_rows2<DT, MAXM>(p.W[oi] + (size_t)n * p.K, r2 < rows ? p.W[oi2] + (size_t)n2 * p.K : nullptr, xs, p.M,
-                            p.K, lane, acc, acc2);
-        warp_allreduce<MAXM>(acc);
-        finish(r, acc);
-        if (r2 < rows) {
-            warp_allreduce<MAXM>(acc2);
-            finish(r2, acc2);
-        }
-    }
+    stream_units<DT, NW>(A, units, K, xrow, s, rows_of, red, finish);
 }
 
-// ---------------------------------------------------------------------------
-// the SwiGLU FFN block in one launch
-// ---------------------------------------------------------------------------
-// Bounded grid barrier on a counter the host zeroed before the launch.
-__device__ bool grid_barrier(unsigned int* counter, unsigned int expected, int* status,
-                             unsigned long long timeout_ns) {
-    __syncthreads();
-    bool ok = true;
-    __shared__ int bar_ok;
-    if (threadIdx.x == 0) {
-        __threadfence();  // this CTA's h is visible before it is counted
-        atomicAdd(counter, 1u);
-        const uint64_t t0 = globaltimer_ns();
-        for (uint32_t i = 1;; ++i) {
-            if (*reinterpret_cast<volatile unsigned int*>(counter) >= expected) break;
-            if ((i & 63) == 0) {
-                if (*reinterpret_cast<volatile int*>(status) != 0 || globaltimer_ns() - t0 > timeout_ns) {
-                    atomicCAS(status, 0, kStatusTimeout | (60 << 8));
-                    ok = false;
-                    break;
-                }
-                __nanosleep(64);
-            }
-        }
-        __threadfence();  // every CTA's h is visible to the reads below
-        bar_ok = ok ? 1 : 0;
-    }
-    __syncthreads();
-    return bar_ok != 0;
-}
-
-template <int DT, int MAXM>
-__global__ void __launch_bounds__(kGemvThreads) fl_ffn_decode_kernel(const __grid_constant__ FfnDecodeParams q) {
-    using Ops = DTypeOps<DT>;
-    extern __shared__ __align__(16) uint8_t smem[];
-    uint16_t* xs = reinterpret_cast<uint16_t*>(smem);
-    __shared__ float rscale[MAXM];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // warp-major numbering: consecutive rows go to different CTAs, so every SM
-    // gets the same number of rows to within one
-    const int gw = warp * gridDim.x + blockIdx.x, nw = gridDim.x * kGemvWarps;
-    const int M = q.M, D = q.D, F = q.F;
-    if (gw < F) {
-        prefetch_row(q.Wg + (size_t)gw * D, D, lane);
-        prefetch_row(q.Wu + (size_t)gw * D, D, lane);
-    }
-    griddep_wait();
-    // phase 1: h = silu(xs Wg^T * rs) * (xs Wu^T * rs), xs = x * gamma
-    {
-        GemvParams p = {};
-        p.x = q.x;
-        p.gamma = q.gamma;
-        p.M = M;
-        p.K = D;
-        p.eps = q.eps;
-        build_rows<DT, PRO_RMS, MAXM>(p, xs, rscale);
-    }
-    for (int f = gw; f < F; f += nw) {
-        float g[MAXM], u[MAXM];
-#pragma unroll
-        for (int m = 0; m < MAXM; ++m) g[m] = u[m] = 0.f;
-        dot_rows2<DT, MAXM>(q.Wg + (size_t)f * D, q.Wu + (size_t)f * D, xs, M, D, lane, g, u);
-        warp_allreduce<MAXM>(g);
-        warp_allreduce<MAXM>(u);
-#pragma unroll
-        for (int m = 0; m < MAXM; ++m) {
-            if (lane == m && m < M) {
-                const float v = act_apply(ACT_SILU, g[m] * rscale[m]) * (u[m] * rscale[m]);
-                q.h[(size_t)m * F + f] = (uint16_t)(Ops::pack(v, 0.f) & 0xffffu);
-            }
-        }
-    }
-    const bool ok = grid_barrier(q.counter, gridDim.x, q.status, q.timeout_ns);
-    // every CTA is resident and past phase 1: the next kernel may be scheduled
-    griddep_launch_dependents();
-    if (!ok) return;
-    // phase 2: out = h Wd^T (+ bias_down) + x, h staged from L2 (not L1: it was
-    // written by other SMs during this launch)
-    {
-        // h is M * F / 8 vectors: every thread's share issued at once
-        const int hv = M * (F / kVec);
-        constexpr int U = 8;
-        for (int i0 = threadIdx.x; i0 < hv; i0 += U * kGemvThreads) {
-            uint4 v[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (i0 + u * kGemvThreads < hv)
-                    v[u] = __ldcg(reinterpret_cast<const uint4*>(q.h) + i0 + u * kGemvThreads);
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (i0 + u * kGemvThreads < hv) reinterpret_cast<uint4*>(xs)[i0 + u * kGemvThreads] = v[u];
-        }
-    }
-    __syncthreads();
-    auto finish = [&](int d, const float (&acc)[MAXM]) {
-#pragma unroll
-        for (int m = 0; m < MAXM; ++m) {
-            if (lane == m && m < M) {
-                float v = acc[m];
-                if (q.bias_down != nullptr) v += Ops::unpack(q.bias_down[d] | 0u).x;
-                v += Ops::unpack(q.x[(size_t)m * D + d] | 0u).x;
-                q.out[(size_t)m * D + d] = (uint16_t)(Ops::pack(v, 0.f) & 0xffffu);
-            }
-        }
-    };
-    for (int d = gw; d < D; d += 2 * nw) {
-        const int d2 = d + nw;
-        float acc[MAXM], acc2[MAXM];
-#pragma unroll
-        for (int m = 0; m < MAXM; ++m) acc[m] = acc2[m] = 0.f;
-        dot_rows2<DT, MAXM>(q.Wd + (size_t)d * F, d2 < D ? q.Wd + (size_t)d2 * F : nullptr, xs, M, F, lane, acc, acc2);
-        warp_allreduce<MAXM>(acc);
-        finish(d, acc);
-        if (d2 < D) {
-            warp_allreduce<MAXM>(acc2);
-            finish(d2, acc2);
-        }
-    }
-}
-
-template <int DT, int PRO, int MAXM>
+template <int DT, int PRO, bool DUAL>
 cudaError_t gemv_launch(const GemvParams& p, int grid, int smem, int pdl, cudaStream_t stream) {
-    auto kern = fl_gemv_kernel<DT, PRO, MAXM>;
+    auto kern = fl_gemv_kernel<DT, PRO, DUAL>;
     static cudaError_t attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemvSmemMax);
     if (attr != cudaSuccess) return attr;
     cudaLaunchConfig_t cfg = {};
@@ -425,24 +485,6 @@ cudaError_t gemv_launch(const GemvParams& p, int grid, int smem, int pdl, cudaSt
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <int DT, int MAXM>
-cudaError_t ffn_launch(const FfnDecodeParams& q, int grid, int smem, int pdl, cudaStream_t stream) {
-    auto kern = fl_ffn_decode_kernel<DT, MAXM>;
-    static cudaError_t attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemvSmemMax);
-    if (attr != cudaSuccess) return attr;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid, 1, 1);
-    cfg.blockDim = dim3(kGemvThreads, 1, 1);
-    cfg.dynamicSmemBytes = (size_t)smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute a[1];
-    a[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    a[0].val.programmaticStreamSerializationAllowed = pdl;
-    cfg.attrs = a;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, q);
-}
-
 template <typename Kern>
 int resident_ctas(Kern kern, int smem) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemvSmemMax) != cudaSuccess) return 0;
@@ -456,47 +498,31 @@ int resident_ctas(Kern kern, int smem) {
 
 }  // namespace
 
-cudaError_t launch_gemv(int dt, int pro, const GemvParams& p, int sms, int pdl, cudaStream_t stream) {
-    const int smem = p.M * p.K * 2;
-    if (p.M < 1 || p.M > kGemvMaxRows || smem > kGemvSmemMax) return cudaErrorInvalidValue;
-    // enough warps to deal the weight rows out evenly, at most two waves' worth of CTAs per SM
-    const int rows = p.row0[p.n_out];
+int gemv_smem_bytes(int M, int K, int pro) { return smem_bytes(M, K, pro); }
+
+cudaError_t launch_gemv(int dt, int pro, bool dual, const GemvParams& p, int sms, int pdl, cudaStream_t stream) {
+    const int smem = smem_bytes(p.M, p.K, pro);
+    if (p.M < 1 || p.M > kGemvMaxRows || smem > kGemvSmemMax || p.K % 8 != 0) return cudaErrorInvalidValue;
+    if (dual && (pro != PRO_RMS || p.n_out != 1)) return cudaErrorInvalidValue;
+    for (int i = 0; i < p.n_out; ++i)
+        if (p.N[i] % 8 != 0) return cudaErrorInvalidValue;
+    // one CTA per 8-row unit, at most as many as are resident at once
+    const int units = p.row0[p.n_out] / 8;
     int per_sm = 0;
-#define FL_OCC(DT, PRO) \
-    if (dt == DT && pro == PRO) per_sm = resident_ctas(fl_gemv_kernel<DT, PRO, kGemvMaxRows>, smem);
-    FL_OCC(0, 0) FL_OCC(0, 1) FL_OCC(0, 2) FL_OCC(0, 3) FL_OCC(1, 0) FL_OCC(1, 1) FL_OCC(1, 2) FL_OCC(1, 3)
+#define FL_OCC(DT, PRO, DUAL) \
+    if (dt == DT && pro == PRO && dual == DUAL) per_sm = resident_ctas(fl_gemv_kernel<DT, PRO, DUAL>, smem);
+    FL_OCC(0, 0, false) FL_OCC(0, 1, false) FL_OCC(0, 2, false) FL_OCC(0, 3, false) FL_OCC(0, 1, true)
+    FL_OCC(1, 0, false) FL_OCC(1, 1, false) FL_OCC(1, 2, false) FL_OCC(1, 3, false) FL_OCC(1, 1, true)
 #undef FL_OCC
     if (per_sm < 1) return cudaErrorInvalidValue;
-    if (per_sm > 4) per_sm = 4;
     int grid = sms * per_sm;
-    const int need = (rows + kGemvWarps - 1) / kGemvWarps;
-    if (grid > need) grid = need;
-    const bool small = p.M <= 2;
-#define FL_CASE(DT, PRO)                                                                              \
-    if (dt == DT && pro == PRO)                                                                     \
-        return small ? gemv_launch<DT, PRO, 2>(p, grid, smem, pdl, stream)                           \
-                     : gemv_launch<DT, PRO, kGemvMaxRows>(p, grid, smem, pdl, stream);
-    FL_CASE(0, 0) FL_CASE(0, 1) FL_CASE(0, 2) FL_CASE(0, 3) FL_CASE(1, 0) FL_CASE(1, 1) FL_CASE(1, 2) FL_CASE(1, 3)
+    if (grid > units) grid = units;
+#define FL_CASE(DT, PRO, DUAL) \
+    if (dt == DT && pro == PRO && dual == DUAL) return gemv_launch<DT, PRO, DUAL>(p, grid, smem, pdl, stream);
+    FL_CASE(0, 0, false) FL_CASE(0, 1, false) FL_CASE(0, 2, false) FL_CASE(0, 3, false) FL_CASE(0, 1, true)
+    FL_CASE(1, 0, false) FL_CASE(1, 1, false) FL_CASE(1, 2, false) FL_CASE(1, 3, false) FL_CASE(1, 1, true)
 #undef FL_CASE
     return cudaErrorInvalidValue;
-}
-
-int ffn_decode_grid(int dt, int M, int D, int F, int sms) {
-    const int smem = M * (D > F ? D : F) * 2;
-    if (M < 1 || M > kGemvMaxRows || smem > kGemvSmemMax) return 0;
-    int per_sm = dt == 0 ? resident_ctas(fl_ffn_decode_kernel<0, kGemvMaxRows>, smem)
-                         : resident_ctas(fl_ffn_decode_kernel<1, kGemvMaxRows>, smem);
-    if (per_sm < 1) return 0;
-    if (per_sm > 4) per_sm = 4;
-    return sms * per_sm;  // every CTA resident at once: the grid barrier needs it
-}
-
-cudaError_t launch_ffn_decode(int dt, const FfnDecodeParams& q, int grid, int pdl, cudaStream_t stream) {
-    const int smem = q.M * (q.D > q.F ? q.D : q.F) * 2;
-    const bool small = q.M <= 2;
-    if (dt == 0)
-        return small ? ffn_launch<0, 2>(q, grid, smem, pdl, stream) : ffn_launch<0, kGemvMaxRows>(q, grid, smem, pdl, stream);
-    return small ? ffn_launch<1, 2>(q, grid, smem, pdl, stream) : ffn_launch<1, kGemvMaxRows>(q, grid, smem, pdl, stream);
 }
 
 }  // namespace fl

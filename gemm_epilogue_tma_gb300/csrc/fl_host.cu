@@ -631,6 +631,13 @@ fl_status prepare_kernels(int dt, int pro, bool dual, const void* A, const Outs&
     return FL_OK;
 }
 
+// Kernels launched (issued to a stream, or recorded into a captured graph)
+// since the library was loaded, counted on the host after each successful
+// launch call.
+std::atomic<long long> g_kernel_launches{0};
+
+void count_launch() { g_kernel_launches.fetch_add(1, std::memory_order_relaxed); }
+
 fl_status launch_prepared(const Prepared& L, cudaStream_t stream) {
     cudaError_t e;
     const char* what;
@@ -645,6 +652,7 @@ fl_status launch_prepared(const Prepared& L, cudaStream_t stream) {
         what = "kernel launch failed";
     }
     if (e != cudaSuccess) return fail(FL_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    count_launch();
     return ok();
 }
 
@@ -746,17 +754,24 @@ fl_status run_kernels(int dt, int pro, bool dual, const void* A, const Outs& out
 // One fused call. LayerNorm first computes the row statistics (8 bytes per
 // row of stream-ordered scratch from the library pool, freed on the stream
 // right after the GEMM kernel that reads them), once for all outputs.
-// Decode row counts go to the CUDA-core kernel (whole weight rows per warp, no
-// reduction across CTAs); FL_OPT_VARIANT = 4 forces it where it fits.
-bool use_gemv(int M, int K, bool dual) {
+// Decode row counts go to the weight-streaming decode kernel (8-row units per
+// CTA, warp-level MMAs, no reduction across CTAs); FL_OPT_VARIANT = 4 forces
+// it where it fits.
+// Automatic choice: up to 4 rows, and up to 8 rows while K <= 2048 (at 8 rows
+// and K = 4096 the split-K tensor-core kernel measured as fast: 10.1 against
+// 10.3 us for a 4096 x 4096 weight, 55 against 64 us for the 4096 / 11008
+// SwiGLU block).
+bool use_gemv(int M, int K, int pro) {
     const int variant = g_opt_variant.load();
-    if (dual || (variant != 0 && variant != 4)) return false;
-    if (M > fl::kGemvMaxRows || (long long)M * K * 2 > fl::kGemvSmemMax) return false;
-    return true;
+    if (variant != 0 && variant != 4) return false;
+    if (M > fl::kGemvMaxRows || fl::gemv_smem_bytes(M, K, pro) > fl::kGemvSmemMax) return false;
+    return variant == 4 || M <= 4 || K <= 2048;
 }
 
-fl_status run_gemv(int dt, int pro, const void* A, const Outs& outs, const void* residual, const void* gamma,
-                   const void* beta, int M, int K, float eps, DeviceInfo* di, cudaStream_t stream) {
+// dual: the SwiGLU gate/up pair (outs.o[0].W = Wg, W2 = Wu, out = h).
+fl_status run_gemv(int dt, int pro, bool dual, const void* A, const Outs& outs, const void* W2, const void* residual,
+                   const void* gamma, const void* beta, int M, int K, float eps, DeviceInfo* di,
+                   cudaStream_t stream) {
     fl::GemvParams g;
     memset(&g, 0, sizeof(g));
     g.x = static_cast<const uint16_t*>(A);
@@ -774,12 +789,14 @@ fl_status run_gemv(int dt, int pro, const void* A, const Outs& outs, const void*
         rows += outs.o[i].N;
     }
     for (int i = outs.n; i <= 4; ++i) g.row0[i] = rows;
+    if (dual) g.W[1] = static_cast<const uint16_t*>(W2);
     g.residual = static_cast<const uint16_t*>(residual);
     g.M = M;
     g.K = K;
     g.eps = eps;
-    const cudaError_t e = fl::launch_gemv(dt, pro, g, di->sms, g_opt_pdl.load(), stream);
+    const cudaError_t e = fl::launch_gemv(dt, pro, dual, g, di->sms, g_opt_pdl.load(), stream);
     if (e != cudaSuccess) return fail(FL_ERR_CUDA, "decode kernel launch failed: %s", cudaGetErrorString(e));
+    count_launch();
     return ok();
 }
 
@@ -790,7 +807,8 @@ fl_status run_tile(int dt, int pro, bool dual, const void* A, const Outs& outs, 
     fl_status st = device_info(&di);
     if (st != FL_OK) return st;
     // (the decode kernel computes its few rows' LayerNorm statistics itself)
-    if (use_gemv(M, K, dual)) return run_gemv(dt, pro, A, outs, residual, gamma, beta, M, K, eps, di, stream);
+    if (use_gemv(M, K, pro) && (!dual || pro == fl::PRO_RMS))
+        return run_gemv(dt, pro, dual, A, outs, W2, residual, gamma, beta, M, K, eps, di, stream);
     void* stats = nullptr;
     if (pro == fl::PRO_LN) {
         cudaError_t e = cudaMallocFromPoolAsync(&stats, (size_t)M * 8, di->pool, stream);
@@ -800,6 +818,7 @@ fl_status run_tile(int dt, int pro, bool dual, const void* A, const Outs& outs, 
             cudaFreeAsync(stats, stream);
             return fail(FL_ERR_CUDA, "LayerNorm statistics kernel launch failed: %s", cudaGetErrorString(e));
         }
+        count_launch();
     }
     st = run_kernels(dt, pro, dual, A, outs, W2, residual, gamma, beta, stats, M, K, eps, di, device_index(), stream);
     if (stats != nullptr) cudaFreeAsync(stats, stream);
@@ -1018,17 +1037,13 @@ fl_status fl_rms_norm(const void* x, const void* gamma, void* out, int M, int K,
     cudaError_t e = fl::launch_rms_norm(dtype, x, gamma, out, M, K, eps, g_opt_pdl.load(), di->sms,
                                           static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(FL_ERR_CUDA, "RMSNorm kernel launch failed: %s", cudaGetErrorString(e));
+    count_launch();
     return ok();
 }
-
-// Decode FFN in one launch: h, then (at a 256-byte boundary) the grid
-// barrier's counter.
-size_t ffn_counter_offset(int M, int F) { return ((size_t)M * (size_t)F * 2 + 255) / 256 * 256; }
 
 size_t fl_swiglu_ffn_workspace_size(int M, int F, fl_dtype dtype) {
     (void)dtype;
     if (M < 1 || F < 1) return 0;
-    if (M <= fl::kGemvMaxRows) return ffn_counter_offset(M, F) + 256;
     return (size_t)M * (size_t)F * 2;
 }
 
@@ -1061,36 +1076,6 @@ fl_status fl_swiglu_ffn(const void* x, const void* gamma, const void* Wg, const 
     }
     if (overlap(workspace, need, out, ob)) return fail(FL_ERR_INVALID_ARG, "workspace overlaps out");
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // decode rows: the whole block in one launch (gate/up, grid barrier, down)
-    const int variant = g_opt_variant.load();
-    if ((variant == 0 || variant == 4) && M <= fl::kGemvMaxRows) {
-        DeviceInfo* di = nullptr;
-        if ((st = device_info(&di)) != FL_OK) return st;
-        const int grid = fl::ffn_decode_grid(dtype, M, D, F, di->sms);
-        if (grid > 0) {
-            fl::FfnDecodeParams q;
-            memset(&q, 0, sizeof(q));
-            q.x = static_cast<const uint16_t*>(x);
-            q.gamma = static_cast<const uint16_t*>(gamma);
-            q.Wg = static_cast<const uint16_t*>(Wg);
-            q.Wu = static_cast<const uint16_t*>(Wu);
-            q.Wd = static_cast<const uint16_t*>(Wd);
-            q.bias_down = static_cast<const uint16_t*>(bias_down);
-            q.h = static_cast<uint16_t*>(workspace);
-            q.out = static_cast<uint16_t*>(out);
-            q.counter = reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) + ffn_counter_offset(M, F));
-            q.status = di->status;
-            q.timeout_ns = (unsigned long long)g_opt_timeout_ms.load() * 1000000ull;
-            q.M = M;
-            q.D = D;
-            q.F = F;
-            q.eps = eps;
-            cudaError_t e = cudaMemsetAsync(q.counter, 0, sizeof(unsigned int), s);
-            if (e == cudaSuccess) e = fl::launch_ffn_decode(dtype, q, grid, g_opt_pdl.load(), s);
-            if (e != cudaSuccess) return fail(FL_ERR_CUDA, "decode FFN launch failed: %s", cudaGetErrorString(e));
-            return ok();
-        }
-    }
     // gate/up: h = silu(RMSNorm(x) Wg^T) * (RMSNorm(x) Wu^T)
     st = run_tile(dtype, fl::PRO_RMS, true, x, single_out(Wg, nullptr, workspace, F, fl::ACT_NONE), Wu, nullptr, gamma,
                   nullptr, M, D, eps, s);
@@ -1098,6 +1083,12 @@ fl_status fl_swiglu_ffn(const void* x, const void* gamma, const void* Wg, const 
     // down: out = h Wd^T (+ bias_down) + x
     return run_tile(dtype, fl::PRO_NONE, false, workspace, single_out(Wd, bias_down, out, D, fl::ACT_NONE), nullptr, x,
                     nullptr, nullptr, M, F, 0.f, s);
+}
+
+fl_status fl_kernel_launches(long long* count) {
+    if (count == nullptr) return fail(FL_ERR_INVALID_ARG, "null output pointer");
+    *count = g_kernel_launches.load();
+    return ok();
 }
 
 fl_status fl_launch_cache_stats(long long* hits, long long* misses) {
@@ -1175,5 +1166,6 @@ extern "C" fl_status fl_debug_wait_timeout(int limit_us, void* stream) {
                                                                           (unsigned long long)limit_us * 1000ull);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(FL_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+    count_launch();
     return ok();
 }

@@ -105,16 +105,16 @@ int set_last_error(int status, const char* message);
 cudaError_t launch_ln_stats(int dt, const void* x, int M, int K, float eps, void* stats, int pdl,
                             cudaStream_t stream);
 
-// Decode kernels on the CUDA cores (M <= kGemvMaxRows activation rows; the
-// prologue-transformed rows must fit in kGemvSmemMax bytes of shared memory).
-constexpr int kGemvMaxRows = 4;
+// Decode kernel (M <= kGemvMaxRows activation rows; the transformed rows
+// must fit in kGemvSmemMax bytes of shared memory: gemv_smem_bytes).
+constexpr int kGemvMaxRows = 8;
 constexpr int kGemvSmemMax = 96 * 1024;
 
 struct GemvParams {
     const uint16_t* x;          // [M, K]
     const uint16_t* gamma;      // RMS / LayerNorm gamma, or the input bias (PRO_ADD)
     const uint16_t* beta;       // LayerNorm beta or null
-    const uint16_t* W[4];       // output i: weight [N_i, K]
+    const uint16_t* W[4];       // output i: weight [N_i, K] (gate/up pair: W[0] = Wg, W[1] = Wu)
     const uint16_t* bias[4];    // output i: bias [N_i] or null
     uint16_t* out[4];           // output i: [M, N_i]
     int N[4], act[4];
@@ -125,21 +125,9 @@ struct GemvParams {
     float eps;
 };
 
-struct FfnDecodeParams {
-    const uint16_t *x, *gamma, *Wg, *Wu, *Wd, *bias_down;
-    uint16_t* h;             // [M, F] hidden activation (workspace)
-    uint16_t* out;           // [M, D]
-    unsigned int* counter;   // grid-barrier counter, zeroed before the launch
-    int* status;
-    unsigned long long timeout_ns;
-    int M, D, F;
-    float eps;
-};
-
-cudaError_t launch_gemv(int dt, int pro, const GemvParams& p, int sms, int pdl, cudaStream_t stream);
-// Grid of the one-launch decode FFN (every CTA resident), 0 if it does not fit.
-int ffn_decode_grid(int dt, int M, int D, int F, int sms);
-cudaError_t launch_ffn_decode(int dt, const FfnDecodeParams& q, int grid, int pdl, cudaStream_t stream);
+int gemv_smem_bytes(int M, int K, int pro);
+// dual: the SwiGLU gate/up pair (pro = PRO_RMS, one output h = silu(g) * u).
+cudaError_t launch_gemv(int dt, int pro, bool dual, const GemvParams& p, int sms, int pdl, cudaStream_t stream);
 
 // Standalone RMSNorm y = x * gamma / sqrt(mean(x^2) + eps) of x [M, K].
 cudaError_t launch_rms_norm(int dt, const void* x, const void* gamma, void* y, int M, int K, float eps, int pdl,

@@ -182,8 +182,7 @@ fl_status fl_rms_norm(const void* x, const void* gamma, void* out, int M, int K,
                       fl_dtype dtype, void* stream);
 
 /* Bytes of workspace fl_swiglu_ffn needs: the hidden activation h [M,F] in the
- * dtype; for 1 to 4 rows (the one-launch decode form) h rounded up to 256
- * bytes plus 256 bytes for that kernel's grid-barrier word. */
+ * dtype, M * F * 2 (0 when M or F is below 1). */
 size_t fl_swiglu_ffn_workspace_size(int M, int F, fl_dtype dtype);
 
 /*
@@ -194,7 +193,8 @@ size_t fl_swiglu_ffn_workspace_size(int M, int F, fl_dtype dtype);
  *   out = h Wd^T (+ bias_down) + x               Wd [D,F], bias_down [D] or NULL
  * Two launches: a gate/up kernel that feeds one staged activation tile to both
  * weights and writes h, then a down-projection kernel with a residual
- * epilogue. workspace: device memory of at least
+ * epilogue (for 1 to 8 rows both on the decode kernel, where its activation
+ * rows fit in shared memory; see FL_OPT_VARIANT). workspace: device memory of at least
  * fl_swiglu_ffn_workspace_size(M, F, dtype) bytes, 16-byte aligned, owned by
  * the caller; its contents on return are h. out must not alias x.
  */
@@ -322,11 +322,12 @@ fl_status fl_device_status(void* stream);
  *                       (for the SwiGLU gate/up GEMM only up to 64 rows, else
  *                       the tile kernel), 3 = CTA-pair kernel (256 x 256 tiles
  *                       on two SMs; for the gate/up kernel, Wg and Wu rows
- *                       stacked in one tile), 4 = the CUDA-core decode kernel
- *                       (1 to 4 rows whose transformed activation fits in
- *                       96 KB of shared memory; for fl_swiglu_ffn the whole
- *                       block in one launch). Automatic choice takes the
- *                       decode kernel for 1 to 4 rows where it fits.
+ *                       stacked in one tile), 4 = the decode kernel (1 to 8
+ *                       rows; weight-streaming warp-level MMAs; the
+ *                       transformed activation rows must fit in 96 KB of
+ *                       shared memory). Automatic choice
+ *                       takes the decode kernel where it fits for 1 to 4
+ *                       rows, and for 5 to 8 rows when K <= 2048.
  *   FL_OPT_TIMEOUT_MS:  limit of every device-side wait (default 2000).
  *   FL_OPT_SPLIT_K:     0 = automatic, else the K split of the small-M kernel (1..8).
  *   FL_OPT_PDL:         1 (default) = launch each kernel with a programmatic
@@ -378,6 +379,15 @@ fl_status fl_set_option(fl_option key, int value);
  */
 fl_status fl_launch_cache_stats(long long* hits, long long* misses);
 void fl_launch_cache_clear(void);
+
+/*
+ * Kernels this library has launched since it was loaded (every thread and
+ * device together): incremented on the host after each successful kernel
+ * launch call, including launches recorded into a stream capture (a replayed
+ * graph adds nothing). *count = the total; FL_ERR_INVALID_ARG if count is
+ * NULL.
+ */
+fl_status fl_kernel_launches(long long* count);
 
 /*
  * Test hook for the bounded-wait machinery: launches one CTA that waits on a

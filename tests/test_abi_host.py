@@ -134,6 +134,7 @@ def ffn(L, x=addr(0), g=addr(1), Wg=addr(2), Wu=addr(3), Wd=addr(4), bd=None, ou
 
 def test_swiglu_validation(L):
     assert L.fl_swiglu_ffn_workspace_size(16, 128, 1) == 16 * 128 * 2
+    assert L.fl_swiglu_ffn_workspace_size(1, 136, 0) == 136 * 2
     assert L.fl_swiglu_ffn_workspace_size(0, 128, 1) == 0
     assert ffn(L, ws=None) == WORKSPACE
     assert ffn(L, wsb=16 * 128 * 2 - 1) == WORKSPACE
@@ -246,3 +247,14 @@ def test_layer_create_validation(L):
     assert L.fl_graph_launch(None, None) == INVALID
     assert L.fl_capture_end(None, None) == INVALID
     L.fl_graph_destroy(None)  # no-op
+
+
+def test_kernel_launch_counter_on_the_host(L):
+    # no GPU work was issued through this process's rejected calls: the
+    # counter only moves on successful launches
+    n = ctypes.c_longlong(-1)
+    assert L.fl_kernel_launches(ctypes.byref(n)) == OK and n.value >= 0
+    before = n.value
+    assert L.fl_gemm_epilogue(None, None, None, None, None, 0, 0, 0, 0, 0, None) != OK
+    assert L.fl_kernel_launches(ctypes.byref(n)) == OK and n.value == before
+    assert L.fl_kernel_launches(None) == INVALID

@@ -46,13 +46,6 @@ def test_roofline_bound_follows_arithmetic_intensity():
     assert abs(r["frac"] - r["tensor_frac"]) < 1e-12 and r["hbm_frac"] < r["tensor_frac"]
 
 
-def test_kernel_launches_per_step():
-    assert bench.launches_of(bench.parse_workload("rmsnorm_gemm_f16_512x4096x4096")) == 1
-    assert bench.launches_of(bench.parse_workload("norm:layer:f16:512:4096:4096")) == 2
-    assert bench.launches_of(bench.parse_workload("pattern:gemm_bias:bf16:8:16:32")) == 1
-    assert bench.launches_of(bench.parse_workload("swiglu_ffn_bf16_4096x4096x11008")) == 2
-
-
 def _free_port():
     s = socket.socket()
     s.bind(("127.0.0.1", 0))

@@ -191,11 +191,11 @@ def test_rms_norm_in_place():
 
 
 # ---------------------------------------------------------------------------
-# the CUDA-core decode kernel (1 to 4 rows), forced and automatic
+# the weight-streaming decode kernel (1 to 8 rows), forced and automatic
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("dt", DTYPES)
-@pytest.mark.parametrize("M", [1, 2, 3, 4])
-@pytest.mark.parametrize("NK", [(8, 8), (264, 136), (1032, 4096), (64, 11008)], ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("M", [1, 2, 3, 5, 8])
+@pytest.mark.parametrize("NK", [(8, 8), (264, 136), (1032, 4096), (64, 5560)], ids=lambda s: "x".join(map(str, s)))
 def test_decode_kernel_all_patterns(dt, M, NK):
     N, K = NK
     t = syn.dense_layer_inputs(M, N, K, dt)
@@ -224,15 +224,16 @@ def test_decode_kernel_all_patterns(dt, M, NK):
 @pytest.mark.parametrize("dt", DTYPES)
 @pytest.mark.parametrize("norm", ["rms", "layer"])
 def test_decode_kernel_multi_and_degenerate_rows(dt, norm):
-    # QKV at one and three rows, automatic choice
-    for M in (1, 3):
+    # QKV at one, three and eight rows, automatic choice
+    for M in (1, 3, 8):
         run_multi(M, (1024, 256, 256), 1024, norm, dt, acts=["none", "gelu", "none"])
     # zero and constant rows through the in-kernel LayerNorm statistics
-    t = syn.norm_gemm_inputs(4, 136, 456, norm, dt, with_bias=True)
+    t = syn.norm_gemm_inputs(7, 136, 456, norm, dt, with_bias=True)
     x = t["x"].clone()
     x[0] = 0.0
     x[1] = 40.0
     x[2] = -0.75
+    x[6] = 0.0
     got = fl.norm_gemm(dev(x), dev(t["gamma"]), dev(t["W"]), beta=dev(t["beta"]), bias=dev(t["bias"]), eps=1e-5,
                        norm=norm)
     torch.cuda.synchronize()
@@ -242,8 +243,9 @@ def test_decode_kernel_multi_and_degenerate_rows(dt, norm):
 
 @pytest.mark.parametrize("dt", DTYPES)
 def test_decode_ffn_repeated_and_noalloc(dt):
-    """The one-launch decode FFN twice in a row on one workspace (its barrier
-    word is re-zeroed per call), and through the allocation-free entry point."""
+    """The decode FFN (gate/up and down projections on the decode kernel) twice
+    in a row on one workspace, and through the allocation-free entry point:
+    the same bits each time."""
     M, D, F = 2, 1024, 2816
     t = syn.swiglu_inputs(M, D, F, dt, with_bias=True)
     g = {k: dev(v) for k, v in t.items()}
@@ -257,3 +259,25 @@ def test_decode_ffn_repeated_and_noalloc(dt):
     f = {k: f64(v) for k, v in t.items()}
     ref = oracle.swiglu_ffn(f["x"], f["gamma"], f["Wg"], f["Wu"], f["Wd"], f["bias_down"], 1e-6, dt)
     assert_close(outs[0], ref, dt, f"decode ffn {dt}")
+
+
+@pytest.mark.parametrize("dt", DTYPES)
+def test_kernel_launch_counts(dt):
+    """The library's own launch counter: one launch per fused call, plus the
+    LayerNorm statistics pass on the tensor-core path (not on the decode
+    kernel, which computes its rows' statistics itself); the SwiGLU block is
+    two launches on either path."""
+    def count(fn):
+        n0 = fl.kernel_launches()
+        fn()
+        torch.cuda.synchronize()
+        return fl.kernel_launches() - n0
+
+    for M, ln_launches in ((4, 1), (300, 2)):
+        t = syn.norm_gemm_inputs(M, 264, 512, "layer", dt, with_bias=True)
+        x, g, b, W = dev(t["x"]), dev(t["gamma"]), dev(t["beta"]), dev(t["W"])
+        assert count(lambda: fl.norm_gemm(x, g, W, beta=b, eps=1e-5, norm="layer")) == ln_launches
+        assert count(lambda: fl.norm_gemm(x, g, W, eps=1e-6, norm="rms")) == 1
+        s = syn.swiglu_inputs(M, 512, 1376, dt)
+        s = {k: dev(v) for k, v in s.items()}
+        assert count(lambda: fl.swiglu_ffn(s["x"], s["gamma"], s["Wg"], s["Wu"], s["Wd"], eps=1e-6)) == 2

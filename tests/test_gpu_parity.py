@@ -427,12 +427,12 @@ def test_swiglu_ffn_small_all_elements(dt, with_bias, shape):
 
 
 @pytest.mark.parametrize("dt", DTYPES)
-@pytest.mark.parametrize("shape", [(1, 512, 1376), (3, 1024, 2816), (4, 4096, 11008), (16, 1024, 2816),
+@pytest.mark.parametrize("shape", [(1, 512, 1376), (3, 1024, 2816), (4, 4096, 11008), (8, 1024, 2816), (16, 1024, 2816),
                                    (77, 256, 3008), (128, 512, 1024), (32, 4096, 11008), (2, 264, 136)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_swiglu_ffn_decode_rows(dt, shape):
-    """Decode row counts: up to 4 rows the whole block is one CUDA-core launch
-    (gate/up, grid barrier, down); up to 64 the gate/up GEMM is the split-K form
+    """Decode row counts: up to 8 rows the gate/up pair and the down projection
+    run on the decode kernel (where their rows fit in shared memory); up to 64 the gate/up GEMM is the split-K form
     with Wg and Wu in every stage (two accumulators exchanged together)."""
     M, D, F = shape
     t = syn.swiglu_inputs(M, D, F, dt, with_bias=M == 77)
