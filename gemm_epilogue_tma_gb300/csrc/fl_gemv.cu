@@ -51,7 +51,7 @@ __host__ __device__ __forceinline__ int smem_bytes(int M, int K, int pro) {
 
 __device__ __forceinline__ uint4 ld_stream(const uint16_t* p) {
     uint4 v;
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
         : "l"(p));
     return v;
@@ -92,9 +92,8 @@ __device__ __forceinline__ Slice warp_slice(int K, int warp) {
 }
 
 // L2 prefetch of the lines this lane will read first from one weight row
-// (before the dependency wait: weights are not written by the previous
-// kernel, and L2 is the point of coherence, so a prefetch cannot bring in
-// stale data).
+// (before the dependency wait: L2 is the point of coherence, so a prefetch
+// cannot bring in stale data even of a tensor the previous kernel writes).
 __device__ __forceinline__ void prefetch_slice(const uint16_t* row, Slice s, int t) {
     for (int c = s.c0 + 2 * t; c < s.c1 && c < s.c0 + 2 * kBlock; c += 8)
         asm volatile("prefetch.global.L2 [%0];" ::"l"(row + (size_t)c * kChunk));
@@ -146,11 +145,13 @@ __device__ __forceinline__ void mma_block(const WBlock<NW>& B, const uint16_t* x
 // register blocks, the loads of the next block (of this unit or the next)
 // issued before the MMAs of the current one, then every warp's partial sums
 // go through shared memory (fixed warp order) to finish(unit, lane sums).
-// A (block 0 of the first unit) must have been loaded by the caller.
+// A (block 0 of the first unit) must have been loaded by the caller; mark(s)
+// records trace slot s (timing builds only).
 // rows_of(u, rows) gives this lane's weight row of each matrix in unit u.
-template <int DT, int NW, typename RowsOf, typename Finish>
+template <int DT, int NW, typename RowsOf, typename Finish, typename Mark>
 __device__ __forceinline__ void stream_units(WBlock<NW>& A, int units, int K, const uint16_t* xrow, Slice s,
-                                             RowsOf rows_of, float (*red)[kGemvWarps][32][2 * NW], Finish finish) {
+                                             RowsOf rows_of, float (*red)[kGemvWarps][32][2 * NW], Finish finish,
+                                             Mark mark) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t = lane & 3;
     const int nblk = (s.c1 - s.c0 + WBlock<NW>::U - 1) / WBlock<NW>::U;
     WBlock<NW> B;
@@ -180,6 +181,7 @@ __device__ __forceinline__ void stream_units(WBlock<NW>& A, int units, int K, co
             red[buf][warp][lane][2 * j + 1] = acc[j][1];
         }
         __syncthreads();
+        if (threadIdx.x == 0) mark(u == (int)blockIdx.x ? 3 : 4);
         if (warp == 0) {
             float v[2 * NW];
 #pragma unroll
@@ -243,12 +245,13 @@ __device__ __forceinline__ void cp_async_wait_all() {
 // staging of the RMSNorm rows measured about 1 us slower at K = 4096.)
 // R: a bound on M (2, 4 or 8), so the per-row loops unroll to no more rows
 // than there can be.
-template <int DT, int PRO, int R>
-__device__ void build_rows(const GemvParams& p, uint16_t* xs, float* rscale) {
+template <int DT, int PRO, int R, typename Pre>
+__device__ void build_rows(const GemvParams& p, uint16_t* xs, float* rscale, Pre pre) {
     using Ops = DTypeOps<DT>;
     const int M = p.M, K = p.K, kv = K / kVec, ld = xs_stride(K);
     __shared__ float part[kGemvWarps][R];
     __shared__ float tot[R], tot2[R], mean_s[R], rstd_s[R];
+    bool pre_done = false;
     if (PRO != PRO_LN) {
         constexpr int G = 2;
         float sq[R];
@@ -265,6 +268,10 @@ __device__ void build_rows(const GemvParams& p, uint16_t* xs, float* rscale) {
                     for (int m = 0; m < R; ++m)
                         if (m < M) v[j][m] = ldg_v4(p.x + (size_t)m * K + (size_t)c * kVec);
                 }
+            }
+            if (!pre_done) {
+                pre();
+                pre_done = true;
             }
 #pragma unroll
             for (int j = 0; j < G; ++j) {
@@ -293,6 +300,7 @@ __device__ void build_rows(const GemvParams& p, uint16_t* xs, float* rscale) {
                 }
             }
         }
+        if (!pre_done) pre();
         if (PRO == PRO_RMS) {
             row_sums(sq, part, tot);
             if (threadIdx.x < R) rscale[threadIdx.x] = rsqrtf(tot[threadIdx.x] / (float)K + p.eps);
@@ -312,6 +320,7 @@ __device__ void build_rows(const GemvParams& p, uint16_t* xs, float* rscale) {
         cp_async16(gs + (size_t)c * kVec, p.gamma + (size_t)c * kVec);
         if (has_beta) cp_async16(bs + (size_t)c * kVec, p.beta + (size_t)c * kVec);
     }
+    pre();
     cp_async_wait_all();
     float sm[R];
 #pragma unroll
@@ -416,23 +425,45 @@ __global__ void __launch_bounds__(kGemvThreads, 2) fl_gemv_kernel(const __grid_c
         rows[0] = p.W[oi] + (size_t)(n + g) * K;
         if constexpr (DUAL) rows[NW - 1] = p.W[1] + (size_t)(n + g) * K;
     };
+    if (threadIdx.x == 0) FL_MARK(p, 0);
     const bool first = (int)blockIdx.x < units;
     const uint16_t* rows0[NW] = {};
+    // L2 prefetch of the activation rows and gamma / bias first, then of the
+    // first weight blocks, so the small reads the prologue waits for are not
+    // queued behind the weight stream (prefetches are safe before the
+    // dependency wait: L2 is the point of coherence)
+    {
+        // (each 128-byte line by one CTA of the grid: the others' loads then
+        // hit in L2 or on the request already in flight)
+        const int xl = (p.M * K * 2 + 127) / 128, gl = PRO != PRO_NONE ? (K * 2 + 127) / 128 : 0;
+        for (int i = (int)(threadIdx.x * gridDim.x + blockIdx.x); i < xl + gl; i += kGemvThreads * gridDim.x) {
+            const char* a = i < xl ? reinterpret_cast<const char*>(p.x) + (size_t)i * 128
+                                   : reinterpret_cast<const char*>(p.gamma) + (size_t)(i - xl) * 128;
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+        }
+    }
     if (first) {
         rows_of(blockIdx.x, rows0);
 #pragma unroll
         for (int j = 0; j < NW; ++j) prefetch_slice(rows0[j], s, t);
     }
     griddep_wait();
-    // the first weight block is in flight while the activation rows are staged
+    if (threadIdx.x == 0) FL_MARK(p, 1);
+    // the activation loads go out first (ahead of the weight stream in the
+    // memory queues), then the first weight block, in flight while the rows
+    // are built
     WBlock<NW> A;
-    if (first) load_block<NW>(A, rows0, 0, s, K, t);
+    auto pre = [&] {
+        asm volatile("" ::: "memory");
+        if (first) load_block<NW>(A, rows0, 0, s, K, t);
+    };
     if (p.M <= 2)
-        build_rows<DT, PRO, 2>(p, xs, rscale);
+        build_rows<DT, PRO, 2>(p, xs, rscale, pre);
     else if (p.M <= 4)
-        build_rows<DT, PRO, 4>(p, xs, rscale);
+        build_rows<DT, PRO, 4>(p, xs, rscale, pre);
     else
-        build_rows<DT, PRO, kGemvMaxRows>(p, xs, rscale);
+        build_rows<DT, PRO, kGemvMaxRows>(p, xs, rscale, pre);
+    if (threadIdx.x == 0) FL_MARK(p, 2);
     griddep_launch_dependents();
     const uint16_t* xrow = g < p.M ? xs + (size_t)g * xs_stride(K) : nullptr;
     // lane (g, t) finishes output row m = g, columns n0 + 2t, 2t+1
@@ -464,7 +495,8 @@ __global__ void __launch_bounds__(kGemvThreads, 2) fl_gemv_kernel(const __grid_c
         }
         *reinterpret_cast<uint32_t*>(p.out[oi] + (size_t)m * N + n) = Ops::pack(y0, y1);
     };
-    stream_units<DT, NW>(A, units, K, xrow, s, rows_of, red, finish);
+    stream_units<DT, NW>(A, units, K, xrow, s, rows_of, red, finish, [&](int slot) { FL_MARK(p, slot); });
+    if (threadIdx.x == 0) FL_MARK(p, 5);
 }
 
 template <int DT, int PRO, bool DUAL>

@@ -800,6 +800,10 @@ fl_status run_gemv(int dt, int pro, bool dual, const void* A, const Outs& outs, 
     g.M = M;
     g.K = K;
     g.eps = eps;
+#ifdef FL_TRACE
+    if (const char* tp = getenv("FL_TRACE_PTR"))
+        g.trace = reinterpret_cast<unsigned long long*>(strtoull(tp, nullptr, 10));
+#endif
     const cudaError_t e = fl::launch_gemv(dt, pro, dual, g, di->sms, g_opt_pdl.load(), stream);
     if (e != cudaSuccess) return fail(FL_ERR_CUDA, "decode kernel launch failed: %s", cudaGetErrorString(e));
     count_launch();

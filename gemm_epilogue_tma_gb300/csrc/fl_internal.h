@@ -123,6 +123,7 @@ struct GemvParams {
     const uint16_t* residual;   // [M, N_0] or null (single output)
     int M, K;
     float eps;
+    unsigned long long* trace;  // phase timestamps, builds with FL_TRACE only (else unused, null)
 };
 
 int gemv_smem_bytes(int M, int K, int pro);
