@@ -339,9 +339,10 @@ bool plan_splitk(int dt, int pro, bool dual, int M, const Outs& outs, int K, int
     // 128-wide weight tiles stage more bytes per pipeline slot (more bytes in
     // flight per SM); 64-wide ones give twice the CTAs. Prefer 128 unless it
     // leaves a quarter of the CTAs unused; past one 128-row block, where the
-    // step is no longer a pure weight stream, take 64 on a tie: the same CTAs
-    // with half the K split exchange half as much (512 x 1024 x 1024: 7.2
-    // against 8.3 us).
+    // step is no longer a pure weight stream, take 64 on a tie if it still
+    // splits K: the same CTAs with half the K split exchange half as much
+    // (512 x 1024 x 1024: 7.2 against 8.3 us), while no split at all leaves
+    // each CTA the whole K loop (512 x 2048 x 2048: 17.9 against 13.1 us).
     auto ctas_for = [&](int b) {
         const long long tl = mb * nblocks(outs, b);
         long long sp = sms / (tl > 0 ? tl : 1);
@@ -351,9 +352,10 @@ bool plan_splitk(int dt, int pro, bool dual, int M, const Outs& outs, int K, int
     };
     const int forced_bn = g_opt_tile_n.load();
     const long long c128 = ctas_for(128), c64 = ctas_for(64);
+    const bool split64 = c64 >= 2ll * mb * nblocks(outs, 64);
     const int bn = forced_bn == 128 ? 128
                    : forced_bn == 256 ? 64
-                   : (mb > 1 ? (c128 > c64 ? 128 : 64) : (c128 * 4 >= c64 * 3 ? 128 : 64));
+                   : (mb > 1 && split64 ? (c128 > c64 ? 128 : 64) : (c128 * 4 >= c64 * 3 ? 128 : 64));
     const long long tiles = mb * nblocks(outs, bn);
     // gate/up: up to 64 rows (at 128 rows the CTA-pair kernel measured faster:
     // 78 against 91 us for the 4096 x 11008 bf16 block)

@@ -145,27 +145,28 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     const int khalf = KS == 2 ? (int)(crank >> 1) : 0;
     const int kb_begin = KS == 2 ? khalf * p.kps : 0;
     const int kb_end = KS == 2 ? min(nk, kb_begin + p.kps) : nk;
-    // KS = 1: persistent pairs take the row-block-major tiles round-robin
-    // (pair q: q, q + npairs, ...), so the tiles in flight form a compact band
-    // of row blocks: the weight stays hot in L2 while the activation rows
-    // stream through once (contiguous ranges per pair spread the tiles in
-    // flight over the whole grid and re-read the weight from HBM: gemm_bias
-    // at 4096^3 2.4 % slower). The gate/up kernel keeps contiguous ranges, so
-    // consecutive tiles of a pair share their activation rows. KS = 2: one
-    // tile per cluster.
+    // KS = 1: persistent pairs take the tiles round-robin (pair q: q,
+    // q + npairs, ...), so the tiles in flight form a compact band and the
+    // operand they share is read from HBM once. Row-block-major for one
+    // weight (a band of row blocks over every column block: the weight stays
+    // hot in L2 while the activation rows stream through once; contiguous
+    // ranges per pair spread the tiles in flight over the whole grid and
+    // re-read the weight from HBM: gemm_bias at 4096^3 2.4 % slower).
+    // Column-block-major for the gate/up pair, whose Wg + Wu (180 MB at
+    // F = 11008) do not fit in L2 while the activation does: a band of column
+    // blocks over every row block, each weight tile read from HBM once
+    // (contiguous ranges had re-read it for every row block: 2.4 GB of DRAM
+    // reads per 4096-row launch against 0.2 GB of operands). KS = 2: one tile
+    // per cluster.
     const int npairs = KS == 2 ? p.num_tiles : (int)gridDim.x / 2;
     const int pair = KS == 2 ? (int)blockIdx.x / 4 : (int)blockIdx.x / 2;
     int t_begin = pair, t_end = pair + 1, t_step = 1;
-    if (KS == 1 && !DUAL) {
+    if (KS == 1) {
         t_end = p.num_tiles;
         t_step = npairs;
-    } else if (KS == 1) {
-        const int base = p.num_tiles / npairs, extra = p.num_tiles % npairs;
-        t_begin = pair * base + min(pair, extra);
-        t_end = t_begin + base + (pair < extra ? 1 : 0);
     }
-    auto tile_mb = [&](int t) { return t / p.num_n_blocks; };
-    auto tile_nb = [&](int t) { return t % p.num_n_blocks; };
+    auto tile_mb = [&](int t) { return DUAL ? t % p.num_m_blocks : t / p.num_n_blocks; };
+    auto tile_nb = [&](int t) { return DUAL ? t / p.num_m_blocks : t % p.num_n_blocks; };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
