@@ -446,13 +446,15 @@ struct PairPlan {
     int bn, ks, clusters;
 };
 
+int choose_bn(int M, const Outs& outs, bool dual, int sms);
+
 // The CTA-pair kernel, when its 256-wide tiles keep 80 % of the resident pairs
 // busy: directly, or with each tile's K range split over two pairs (a cluster
 // of four) when there are half as many tiles. A 128-wide pair tile moves as
 // many shared-memory bytes per MMA as the single-CTA 128 x 256 tile and
 // measures no faster, so it is used only when forced (FL_OPT_VARIANT = 3 with
 // FL_OPT_TILE_N = 128; FL_OPT_SPLIT_K = 2 forces the K split).
-bool use_pair(int dt, int pro, int M, const Outs& outs, int K, PairPlan* plan, bool dual) {
+bool use_pair(int dt, int pro, int M, const Outs& outs, int K, PairPlan* plan, bool dual, int sms) {
     const int variant = g_opt_variant.load();
     if (variant == 1 || variant == 2) return false;
     if (dual) {
@@ -490,7 +492,16 @@ bool use_pair(int dt, int pro, int M, const Outs& outs, int K, PairPlan* plan, b
         *plan = PairPlan{256, 2, (int)t256};
         return true;
     }
-    if (variant != 3 && !fills) return false;
+    // too few tiles to fill the pairs, but the pair tiles still cover as many
+    // SMs as the 1-CTA kernel's tiles would: the pair moves fewer shared-memory
+    // bytes per MMA (QKV 4096 + 1024 + 1024 at M = 512: 28.6 against 36.0 us)
+    long long tile_ctas = 0;
+    if (variant == 0 && !fills) {
+        const long long t1 = (long long)((M + fl::kBM - 1) / fl::kBM) * nblocks(outs, choose_bn(M, outs, false, sms));
+        tile_ctas = t1 < sms ? t1 : sms;
+    }
+    const bool covers = tile_ctas > 0 && t256 * 2 >= tile_ctas && t256 <= maxp;
+    if (variant != 3 && !fills && !covers) return false;
     *plan = PairPlan{256, 1, (int)(t256 < maxp ? t256 : maxp)};
     return true;
 }
@@ -617,7 +628,7 @@ fl_status prepare_kernels(int dt, int pro, bool dual, const void* A, const Outs&
     out->dual = dual;
     out->ks = out->splits = 1;
     PairPlan pplan;
-    if (use_pair(dt, pro, M, outs, K, &pplan, dual))
+    if (use_pair(dt, pro, M, outs, K, &pplan, dual, di->sms))
         return prepare_pair(dt, pro, dual, A, outs, W2, residual, gamma, beta, M, K, eps, pplan, di, out);
     SplitPlan plan;
     if (plan_splitk(dt, pro, dual, M, outs, K, di->sms, &plan))
