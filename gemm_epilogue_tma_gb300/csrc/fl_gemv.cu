@@ -235,14 +235,13 @@ __device__ __forceinline__ void cp_async_wait_all() {
 // columns of every row (and of gamma / the bias) into registers at a time,
 // all before using any, and store the folded values (x * gamma or x + bias,
 // rounded once; the RMS scale goes to the epilogue): one memory round trip
-// for K <= 4096. LayerNorm needs its rows three times, so it stages them
-// (and gamma, beta, into the side area after the rows) with asynchronous
-// copies, all in flight at once and holding no registers, takes the
-// corrected two-pass statistics over them (mean, then the sums of
-// d = x - mean and d^2: mean += sum(d) / K, var = sum(d^2) / K -
-// (sum(d) / K)^2) and folds in a third pass; a thread only touches its own
-// columns, so only the row sums need barriers. (Asynchronous or bulk-copy
-// staging of the RMSNorm rows measured about 1 us slower at K = 4096.)
+// for K <= 4096. LayerNorm needs its rows twice (shifted sums, then the
+// fold): up to two rows of K <= 4096 it holds them in registers too; beyond
+// that it stages them (and gamma, beta, into the side area after the rows)
+// with asynchronous copies, all in flight at once and holding no registers.
+// A thread only touches its own columns, so only the row sums need
+// barriers. (Asynchronous or bulk-copy staging of the RMSNorm rows measured
+// about 1 us slower at K = 4096.)
 // R: a bound on M (2, 4 or 8), so the per-row loops unroll to no more rows
 // than there can be.
 template <int DT, int PRO, int R, typename Pre>
@@ -250,7 +249,7 @@ __device__ void build_rows(const GemvParams& p, uint16_t* xs, float* rscale, Pre
     using Ops = DTypeOps<DT>;
     const int M = p.M, K = p.K, kv = K / kVec, ld = xs_stride(K);
     __shared__ float part[kGemvWarps][R];
-    __shared__ float tot[R], tot2[R], mean_s[R], rstd_s[R];
+    __shared__ float tot[R];
     bool pre_done = false;
     if (PRO != PRO_LN) {
         constexpr int G = 2;
@@ -310,10 +309,93 @@ __device__ void build_rows(const GemvParams& p, uint16_t* xs, float* rscale, Pre
         __syncthreads();
         return;
     }
-    // LayerNorm: stage, row sums, then the deviations from the first mean
-    uint16_t* gs = xs + (size_t)M * ld;  // gamma
-    uint16_t* bs = gs + K;               // beta
+    // LayerNorm: statistics in one pass of shifted sums, d = x - c with c the
+    // row's first element (exact for constant rows, no cancellation for rows
+    // with a large offset): mean = c + sum(d) / K, var = sum(d^2) / K -
+    // (sum(d) / K)^2; every thread derives the rows' mean and 1/sigma from
+    // the reduced sums, then folds its own columns.
     const bool has_beta = p.beta != nullptr;
+    __shared__ float part2[kGemvWarps][2 * R];
+    __shared__ float tot2r[2 * R];
+    float cm[R], sv[2 * R];
+#pragma unroll
+    for (int m = 0; m < R; ++m) {
+        cm[m] = m < M ? Ops::unpack((uint32_t)__ldg(reinterpret_cast<const unsigned short*>(p.x + (size_t)m * K))).x
+                      : 0.f;
+        sv[m] = sv[R + m] = 0.f;
+    }
+    auto stats_of = [&](const uint4& o, int m) {
+        const uint32_t w[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = Ops::unpack(w[e]);
+            const float a = f.x - cm[m], b = f.y - cm[m];
+            sv[m] += a + b;
+            sv[R + m] = fmaf(a, a, fmaf(b, b, sv[R + m]));
+        }
+    };
+    float mean[R], rstd[R];
+    auto finish_stats = [&] {
+        row_sums(sv, part2, tot2r);
+        const float inv_k = 1.0f / (float)K;
+#pragma unroll
+        for (int m = 0; m < R; ++m) {
+            const float e1 = tot2r[m] * inv_k;
+            mean[m] = cm[m] + e1;
+            rstd[m] = rsqrtf(fmaxf(tot2r[R + m] * inv_k - e1 * e1, 0.f) + p.eps);
+        }
+        if (threadIdx.x < R) rscale[threadIdx.x] = 1.f;
+    };
+    auto fold = [&](uint4 o, const uint4& gv, const uint4& bv, int m) {
+        const uint32_t xw[4] = {o.x, o.y, o.z, o.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w}, bw[4] = {bv.x, bv.y, bv.z, bv.w};
+        uint32_t ow[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = Ops::unpack(xw[e]), gg = Ops::unpack(gw[e]), bb = Ops::unpack(bw[e]);
+            ow[e] = Ops::pack(fmaf((f.x - mean[m]) * rstd[m], gg.x, bb.x), fmaf((f.y - mean[m]) * rstd[m], gg.y, bb.y));
+        }
+        return make_uint4(ow[0], ow[1], ow[2], ow[3]);
+    };
+    if (R <= 2 && kv <= 2 * kGemvThreads) {
+        // at most two columns per thread: rows, gamma and beta in registers,
+        // one memory round trip
+        uint4 v[2][R], gv[2], bv[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int c = threadIdx.x + j * kGemvThreads;
+            gv[j] = bv[j] = make_uint4(0u, 0u, 0u, 0u);
+            if (c < kv) {
+                gv[j] = ldg_v4(p.gamma + (size_t)c * kVec);
+                if (has_beta) bv[j] = ldg_v4(p.beta + (size_t)c * kVec);
+#pragma unroll
+                for (int m = 0; m < R; ++m)
+                    if (m < M) v[j][m] = ldg_v4(p.x + (size_t)m * K + (size_t)c * kVec);
+            }
+        }
+        pre();
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+            if (threadIdx.x + j * kGemvThreads < kv)
+#pragma unroll
+                for (int m = 0; m < R; ++m)
+                    if (m < M) stats_of(v[j][m], m);
+        finish_stats();
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int c = threadIdx.x + j * kGemvThreads;
+            if (c < kv)
+#pragma unroll
+                for (int m = 0; m < R; ++m)
+                    if (m < M)
+                        *reinterpret_cast<uint4*>(xs + (size_t)m * ld + (size_t)c * kVec) = fold(v[j][m], gv[j], bv[j], m);
+        }
+        __syncthreads();
+        return;
+    }
+    // more rows or columns: stage them (and gamma, beta into the side area
+    // after the rows) with asynchronous copies, all in flight at once
+    uint16_t* gs = xs + (size_t)M * ld;
+    uint16_t* bs = gs + K;
     for (int c = threadIdx.x; c < kv; c += kGemvThreads) {
         for (int m = 0; m < M; ++m)
             cp_async16(xs + (size_t)m * ld + (size_t)c * kVec, p.x + (size_t)m * K + (size_t)c * kVec);
@@ -322,75 +404,20 @@ __device__ void build_rows(const GemvParams& p, uint16_t* xs, float* rscale, Pre
     }
     pre();
     cp_async_wait_all();
-    float sm[R];
+    for (int c = threadIdx.x; c < kv; c += kGemvThreads)
 #pragma unroll
-    for (int m = 0; m < R; ++m) sm[m] = 0.f;
-    for (int c = threadIdx.x; c < kv; c += kGemvThreads) {
-#pragma unroll
-        for (int m = 0; m < R; ++m) {
-            if (m < M) {
-                const uint4 o = *reinterpret_cast<const uint4*>(xs + (size_t)m * ld + (size_t)c * kVec);
-                const uint32_t w[4] = {o.x, o.y, o.z, o.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 f = Ops::unpack(w[e]);
-                    sm[m] += f.x + f.y;
-                }
-            }
-        }
-    }
-    row_sums(sm, part, tot);
-    float d1[R], d2[R], mu[R];
-#pragma unroll
-    for (int m = 0; m < R; ++m) {
-        d1[m] = d2[m] = 0.f;
-        mu[m] = tot[m] / (float)K;
-    }
-    for (int c = threadIdx.x; c < kv; c += kGemvThreads) {
-#pragma unroll
-        for (int m = 0; m < R; ++m) {
-            if (m < M) {
-                const float mean = mu[m];
-                const uint4 o = *reinterpret_cast<const uint4*>(xs + (size_t)m * ld + (size_t)c * kVec);
-                const uint32_t w[4] = {o.x, o.y, o.z, o.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 f = Ops::unpack(w[e]);
-                    const float a = f.x - mean, b = f.y - mean;
-                    d1[m] += a + b;
-                    d2[m] = fmaf(a, a, fmaf(b, b, d2[m]));
-                }
-            }
-        }
-    }
-    row_sums(d1, part, tot2);
-    if (threadIdx.x < R) mean_s[threadIdx.x] = tot[threadIdx.x] / (float)K + tot2[threadIdx.x] / (float)K;
-    row_sums(d2, part, tot);
-    if (threadIdx.x < R) {
-        const float e1 = tot2[threadIdx.x] / (float)K;
-        rstd_s[threadIdx.x] = rsqrtf(fmaxf(tot[threadIdx.x] / (float)K - e1 * e1, 0.f) + p.eps);
-        rscale[threadIdx.x] = 1.f;
-    }
-    __syncthreads();
+        for (int m = 0; m < R; ++m)
+            if (m < M) stats_of(*reinterpret_cast<const uint4*>(xs + (size_t)m * ld + (size_t)c * kVec), m);
+    finish_stats();
     for (int c = threadIdx.x; c < kv; c += kGemvThreads) {
         const uint4 gv = *reinterpret_cast<const uint4*>(gs + (size_t)c * kVec);
         const uint4 bv =
             has_beta ? *reinterpret_cast<const uint4*>(bs + (size_t)c * kVec) : make_uint4(0u, 0u, 0u, 0u);
-        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, bw[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
         for (int m = 0; m < R; ++m) {
             if (m < M) {
                 uint4* slot = reinterpret_cast<uint4*>(xs + (size_t)m * ld + (size_t)c * kVec);
-                const uint4 o = *slot;
-                const uint32_t xw[4] = {o.x, o.y, o.z, o.w};
-                const float mean = mean_s[m], rstd = rstd_s[m];
-                uint32_t ow[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 f = Ops::unpack(xw[e]), gg = Ops::unpack(gw[e]), bb = Ops::unpack(bw[e]);
-                    ow[e] = Ops::pack(fmaf((f.x - mean) * rstd, gg.x, bb.x), fmaf((f.y - mean) * rstd, gg.y, bb.y));
-                }
-                *slot = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                *slot = fold(*slot, gv, bv, m);
             }
         }
     }

@@ -495,8 +495,11 @@ bool use_pair(int dt, int pro, int M, const Outs& outs, int K, PairPlan* plan, b
     // too few tiles to fill the pairs, but the pair tiles still cover as many
     // SMs as the 1-CTA kernel's tiles would: the pair moves fewer shared-memory
     // bytes per MMA (QKV 4096 + 1024 + 1024 at M = 512: 28.6 against 36.0 us)
+    // (Not where the split-K kernel takes the shape: few row blocks, where
+    // one K-split cluster per 128-row tile streams the weight once.)
     long long tile_ctas = 0;
-    if (variant == 0 && !fills) {
+    const long long mb128 = (M + fl::kBM - 1) / fl::kBM;
+    if (variant == 0 && !fills && (mb128 * nblocks(outs, 128) * 2 > sms || nk < 4)) {
         const long long t1 = (long long)((M + fl::kBM - 1) / fl::kBM) * nblocks(outs, choose_bn(M, outs, false, sms));
         tile_ctas = t1 < sms ? t1 : sms;
     }

@@ -239,6 +239,17 @@ def test_decode_kernel_multi_and_degenerate_rows(dt, norm):
     torch.cuda.synchronize()
     ref = oracle.norm_gemm(f64(x), f64(t["gamma"]), f64(t["beta"]), f64(t["W"]), f64(t["bias"]), 1e-5, norm)
     assert_close(got, ref, dt, f"decode kernel degenerate rows {norm} {dt}")
+    # two rows (the register-held prologue): a constant row and a row with a
+    # large offset (mean 200, unit spread: the shifted sums must not cancel)
+    t2 = syn.norm_gemm_inputs(2, 264, 4096, norm, dt, with_bias=True)
+    x2 = t2["x"].clone()
+    x2[0] = -3.5
+    x2[1] = x2[1] + 200.0
+    got = fl.norm_gemm(dev(x2), dev(t2["gamma"]), dev(t2["W"]), beta=dev(t2["beta"]), bias=dev(t2["bias"]), eps=1e-5,
+                       norm=norm)
+    torch.cuda.synchronize()
+    ref = oracle.norm_gemm(f64(x2), f64(t2["gamma"]), f64(t2["beta"]), f64(t2["W"]), f64(t2["bias"]), 1e-5, norm)
+    assert_close(got, ref, dt, f"decode kernel constant and offset rows {norm} {dt}")
 
 
 @pytest.mark.parametrize("dt", DTYPES)
