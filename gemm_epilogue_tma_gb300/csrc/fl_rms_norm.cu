@@ -9,7 +9,8 @@
 // lane moves 16-byte vectors at a 512-byte stride (coalesced across the
 // warp). Rows of up to 4096 elements stay in registers between the sum of
 // squares and the scaling (16 vectors per lane, all issued before the first
-// is used); longer rows are read a second time, from L2, for the scaling.
+// is used), and gamma is staged once per CTA in shared memory; longer rows
+// are read a second time, from L2, for the scaling.
 // The lanes' partial sums are added by a fixed butterfly, so the result does
 // not depend on timing. y may be x itself: every element is read before the
 // thread that reads it writes it, and the sum is complete before any write.
@@ -54,19 +55,44 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// One row per warp, rows taken grid-stride by a grid of at most two waves'
-// worth of CTAs.
+// One row longer than 4096 elements, by one warp.
 template <int DT>
 __device__ __forceinline__ void rms_norm_row(const uint16_t* x, const uint16_t* __restrict__ gamma, uint16_t* y,
                                              int row, int K, float eps, int lane);
 
 template <int DT>
-__global__ void __launch_bounds__(256) fl_rms_norm_kernel(const uint16_t* x, const uint16_t* __restrict__ gamma,
-                                                          uint16_t* y, int M, int K, float eps) {
+__global__ void __launch_bounds__(256, 2) fl_rms_norm_kernel(const uint16_t* x, const uint16_t* __restrict__ gamma,
+                                                             uint16_t* y, int M, int K, float eps) {
     griddep_wait();  // x may come from the previous kernel on the stream
     const int lane = threadIdx.x & 31;
-    for (int row = blockIdx.x * 8 + (threadIdx.x >> 5); row < M; row += gridDim.x * 8)
-        rms_norm_row<DT>(x, gamma, y, row, K, eps, lane);
+    const int row0 = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (K <= 256 * kVecPerLane) {
+        // gamma is the same for every row: staged once per CTA in shared
+        // memory (one memory round trip per row instead of two)
+        __shared__ uint4 gs[256 * kVecPerLane / 8];
+        for (int i = threadIdx.x; i < K / 8; i += blockDim.x) gs[i] = ldg_v4(gamma + i * 8);
+        __syncthreads();
+        for (int row = row0; row < M; row += gridDim.x * 8) {
+            const uint16_t* xr = x + (size_t)row * K;
+            uint16_t* yr = y + (size_t)row * K;
+            uint4 v[kVecPerLane];
+#pragma unroll
+            for (int u = 0; u < kVecPerLane; ++u)
+                if (lane * 8 + u * 256 < K) v[u] = ldg_v4(xr + lane * 8 + u * 256);
+            float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+            for (int u = 0; u < kVecPerLane; ++u)
+                if (lane * 8 + u * 256 < K) sq_acc_vec<DT>(v[u], s0, s1);
+            const float r = rsqrtf(warp_sum(s0 + s1) / (float)K + eps);
+#pragma unroll
+            for (int u = 0; u < kVecPerLane; ++u) {
+                const int k = lane * 8 + u * 256;
+                if (k < K) *reinterpret_cast<uint4*>(yr + k) = scale_vec<DT>(v[u], gs[k / 8], r);
+            }
+        }
+    } else {
+        for (int row = row0; row < M; row += gridDim.x * 8) rms_norm_row<DT>(x, gamma, y, row, K, eps, lane);
+    }
     // The next kernel is let in only once this CTA's rows are done: letting
     // it in earlier would park its CTAs on SM slots this grid still needs.
     griddep_launch_dependents();
@@ -78,24 +104,6 @@ __device__ __forceinline__ void rms_norm_row(const uint16_t* x, const uint16_t* 
     const uint16_t* xr = x + (size_t)row * K;
     uint16_t* yr = y + (size_t)row * K;
     float s0 = 0.f, s1 = 0.f;
-    if (K <= 256 * kVecPerLane) {
-        uint4 v[kVecPerLane];
-#pragma unroll
-        for (int u = 0; u < kVecPerLane; ++u)
-            if (lane * 8 + u * 256 < K) v[u] = ldg_v4(xr + lane * 8 + u * 256);
-#pragma unroll
-        for (int u = 0; u < kVecPerLane; ++u)
-            if (lane * 8 + u * 256 < K) sq_acc_vec<DT>(v[u], s0, s1);
-        const float r = rsqrtf(warp_sum(s0 + s1) / (float)K + eps);
-#pragma unroll
-        for (int u = 0; u < kVecPerLane; ++u) {
-            const int k = lane * 8 + u * 256;
-            if (k < K)
-                *reinterpret_cast<uint4*>(yr + k) =
-                    scale_vec<DT>(v[u], ldg_v4(gamma + k), r);
-        }
-        return;
-    }
     // long rows: sum of squares, then a second read for the scaling
     for (int k0 = lane * 8; k0 < K; k0 += 256 * 8) {
         uint4 v[8];
