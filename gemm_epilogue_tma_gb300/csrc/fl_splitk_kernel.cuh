@@ -42,7 +42,7 @@ template <int PRO>
 constexpr int splitk_threads() { return PRO != PRO_NONE ? 320 : 256; }
 
 template <int DT, int BN, int PRO, bool DUAL, bool MULTI>
-__global__ void __launch_bounds__(splitk_threads<PRO>(), 1)
+__global__ void __launch_bounds__(splitk_threads<PRO>(), 2)
     fl_splitk_kernel(const __grid_constant__ ParamsT<MULTI> p) {
     if (threadIdx.x == 0) FL_MARK(p, 0);
     using C = SplitCfg<BN, DUAL>;
