@@ -839,7 +839,7 @@ fl_status run_tile(int dt, int pro, bool dual, const void* A, const Outs& outs, 
     if (pro == fl::PRO_LN) {
         cudaError_t e = cudaMallocFromPoolAsync(&stats, (size_t)M * 8, di->pool, stream);
         if (e != cudaSuccess) return fail(FL_ERR_CUDA, "LayerNorm statistics scratch: %s", cudaGetErrorString(e));
-        e = fl::launch_ln_stats(dt, A, M, K, eps, stats, g_opt_pdl.load(), stream);
+        e = fl::launch_ln_stats(dt, A, M, K, eps, stats, g_opt_pdl.load(), di->sms, stream);
         if (e != cudaSuccess) {
             cudaFreeAsync(stats, stream);
             return fail(FL_ERR_CUDA, "LayerNorm statistics kernel launch failed: %s", cudaGetErrorString(e));

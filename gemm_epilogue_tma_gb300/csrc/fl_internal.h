@@ -102,7 +102,7 @@ using ParamsT = typename ParamsOf<MULTI>::type;
 int set_last_error(int status, const char* message);
 
 // LayerNorm row statistics of x [M, K] into stats (M float2: mean, rstd).
-cudaError_t launch_ln_stats(int dt, const void* x, int M, int K, float eps, void* stats, int pdl,
+cudaError_t launch_ln_stats(int dt, const void* x, int M, int K, float eps, void* stats, int pdl, int sms,
                             cudaStream_t stream);
 
 // Decode kernel (M <= kGemvMaxRows activation rows; the transformed rows
