@@ -91,11 +91,13 @@ __device__ __forceinline__ Slice warp_slice(int K, int warp) {
     return {c0, min(chunks, c0 + per)};
 }
 
-// L2 prefetch of the lines this lane will read first from one weight row
-// (before the dependency wait: L2 is the point of coherence, so a prefetch
-// cannot bring in stale data even of a tensor the previous kernel writes).
+// L2 prefetch of the first register block this lane will read from one
+// weight row (before the dependency wait: L2 is the point of coherence, so a
+// prefetch cannot bring in stale data even of a tensor the previous kernel
+// writes). One block measured best: none 8.98, two blocks 8.37, one 8.19 us
+// at M = 1, 4096 x 4096.
 __device__ __forceinline__ void prefetch_slice(const uint16_t* row, Slice s, int t) {
-    for (int c = s.c0 + 2 * t; c < s.c1 && c < s.c0 + 2 * kBlock; c += 8)
+    for (int c = s.c0 + 2 * t; c < s.c1 && c < s.c0 + kBlock; c += 8)
         asm volatile("prefetch.global.L2 [%0];" ::"l"(row + (size_t)c * kChunk));
 }
 
