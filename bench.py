@@ -245,19 +245,23 @@ def load_peaks():
 HOST_ONLY_SOURCES = ("fl_host.cu", "fl_noalloc.cu")
 
 
-def kernel_sources_hash() -> str:
-    """Hash of the device-code sources (every kernel, its headers and instantiations)."""
+def kernel_sources_hash(files=None) -> str:
+    """Hash of device-code sources: the named files of csrc/ (the kernel a
+    traffic record was taken on, its headers and its instantiation unit), or
+    every kernel source when none are named."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gemm_epilogue_tma_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")) and name not in HOST_ONLY_SOURCES:
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    names = sorted(files) if files else [n for n in sorted(os.listdir(csrc))
+                                         if n.endswith((".cu", ".cuh", ".h")) and n not in HOST_ONLY_SOURCES]
+    for name in names:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(workload: str):
-    """DRAM bytes per launch from a committed ncu capture, if the kernel sources are unchanged since."""
+    """DRAM bytes per launch from a committed ncu capture, if the sources of the
+    captured kernel are unchanged since."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -265,7 +269,7 @@ def recorded_traffic(workload: str):
     except (OSError, ValueError):
         return None
     rec = d.get(workload)
-    if not rec or rec.get("sources") != kernel_sources_hash():
+    if not rec or rec.get("sources") != kernel_sources_hash(rec.get("files")):
         return None
     return rec.get("dram_bytes_per_launch")
 
