@@ -238,7 +238,7 @@ __device__ __forceinline__ void cp_async_wait_all() {
 // all before using any, and store the folded values (x * gamma or x + bias,
 // rounded once; the RMS scale goes to the epilogue): one memory round trip
 // for K <= 4096. LayerNorm needs its rows twice (shifted sums, then the
-// fold): up to two rows of K <= 4096 it holds them in registers too; beyond
+// fold): up to four rows of K <= 4096 it holds them in registers too; beyond
 // that it stages them (and gamma, beta, into the side area after the rows)
 // with asynchronous copies, all in flight at once and holding no registers.
 // A thread only touches its own columns, so only the row sums need
@@ -358,8 +358,8 @@ __device__ void build_rows(const GemvParams& p, uint16_t* xs, float* rscale, Pre
         }
         return make_uint4(ow[0], ow[1], ow[2], ow[3]);
     };
-    if (R <= 2 && kv <= 2 * kGemvThreads) {
-        // at most two columns per thread: rows, gamma and beta in registers,
+    if (R <= 4 && kv <= 2 * kGemvThreads) {
+        // at most four rows and two columns per thread: rows, gamma and beta in registers,
         // one memory round trip
         uint4 v[2][R], gv[2], bv[2];
 #pragma unroll
