@@ -779,15 +779,17 @@ fl_status run_kernels(int dt, int pro, bool dual, const void* A, const Outs& out
 // Decode row counts go to the weight-streaming decode kernel (8-row units per
 // CTA, warp-level MMAs, no reduction across CTAs); FL_OPT_VARIANT = 4 forces
 // it where it fits.
-// Automatic choice: up to 4 rows, and up to 8 rows while K <= 2048 (at 8 rows
-// and K = 4096 the split-K tensor-core kernel measured as fast: 10.1 against
-// 10.3 us for a 4096 x 4096 weight, 55 against 64 us for the 4096 / 11008
-// SwiGLU block).
-bool use_gemv(int M, int K, int pro) {
+// Automatic choice: up to 4 rows; up to 8 rows while K <= 2048; and 5 to 8
+// rows at larger K for plain or RMSNorm / input-bias prologues with one or
+// several outputs (4096 x 4096 at M = 5 / 6 / 8: 9.6 / 9.8 / 10.2 against
+// 10.1 us on the split-K tcgen05 kernel; QKV at M = 8: 13.4 against 14.8),
+// but not for the SwiGLU gate/up pair (62 against 55 us at M = 6 and 8,
+// 4096 / 11008) nor LayerNorm (14.7 against 13.3 us at M = 8).
+bool use_gemv(int M, int K, int pro, bool dual) {
     const int variant = g_opt_variant.load();
     if (variant != 0 && variant != 4) return false;
     if (M > fl::kGemvMaxRows || fl::gemv_smem_bytes(M, K, pro) > fl::kGemvSmemMax) return false;
-    return variant == 4 || M <= 4 || K <= 2048;
+    return variant == 4 || M <= 4 || K <= 2048 || (!dual && pro != fl::PRO_LN);
 }
 
 // dual: the SwiGLU gate/up pair (outs.o[0].W = Wg, W2 = Wu, out = h).
@@ -833,7 +835,7 @@ fl_status run_tile(int dt, int pro, bool dual, const void* A, const Outs& outs, 
     fl_status st = device_info(&di);
     if (st != FL_OK) return st;
     // (the decode kernel computes its few rows' LayerNorm statistics itself)
-    if (use_gemv(M, K, pro) && (!dual || pro == fl::PRO_RMS))
+    if (use_gemv(M, K, pro, dual) && (!dual || pro == fl::PRO_RMS))
         return run_gemv(dt, pro, dual, A, outs, W2, residual, gamma, beta, M, K, eps, di, stream);
     void* stats = nullptr;
     if (pro == fl::PRO_LN) {

@@ -327,7 +327,9 @@ fl_status fl_device_status(void* stream);
  *                       transformed activation rows must fit in 96 KB of
  *                       shared memory). Automatic choice
  *                       takes the decode kernel where it fits for 1 to 4
- *                       rows, and for 5 to 8 rows when K <= 2048.
+ *                       rows, and for 5 to 8 rows when K <= 2048 or the
+ *                       call is neither LayerNorm nor the SwiGLU gate/up
+ *                       pair.
  *   FL_OPT_TIMEOUT_MS:  limit of every device-side wait (default 2000).
  *   FL_OPT_SPLIT_K:     0 = automatic, else the K split of the small-M kernel (1..8).
  *   FL_OPT_PDL:         1 (default) = launch each kernel with a programmatic
