@@ -21,8 +21,9 @@
 using fl::GemmParams;
 using fl::GemmParamsMulti;
 
-// Device status word: kernels record a bounded-wait expiry here.
-__device__ int g_fl_status;
+// Device status words: a kernel records a bounded-wait expiry in the word of
+// the stream it was launched (or captured) on.
+__device__ int g_fl_status[fl::kStatusSlots];
 
 namespace {
 
@@ -66,7 +67,12 @@ struct DeviceInfo {
     std::atomic<bool> ready{false};
     int sms = 0;
     int major = 0, minor = 0;
-    int* status = nullptr;  // device address of g_fl_status
+    int* status = nullptr;  // device address of g_fl_status[0]
+    // stream handle of each status word (word 0: the legacy default stream
+    // and overflow), filled in first-use order under slot_mu
+    std::mutex slot_mu;
+    cudaStream_t slot_stream[fl::kStatusSlots] = {};
+    int slots_used = 1;
     // stream-ordered pool for per-call scratch (LayerNorm row statistics);
     // the library's own, so the process's default pool keeps its settings
     cudaMemPool_t pool = nullptr;
@@ -116,6 +122,32 @@ int device_index() {
     cudaGetDevice(&dev);
     return dev;
 }
+
+// Index of the status word of `stream` (see DeviceInfo::slot_stream). A thread
+// keeps its last answer, so a loop on one stream takes the lock once.
+int status_slot(DeviceInfo* di, cudaStream_t stream) {
+    thread_local const DeviceInfo* last_di = nullptr;
+    thread_local cudaStream_t last_stream = nullptr;
+    thread_local int last_slot = 0;
+    if (stream == nullptr) return 0;
+    if (last_di == di && last_stream == stream) return last_slot;
+    int i = 1;
+    {
+        std::lock_guard<std::mutex> lk(di->slot_mu);
+        while (i < di->slots_used && di->slot_stream[i] != stream) ++i;
+        if (i == di->slots_used && i < fl::kStatusSlots) {
+            di->slot_stream[i] = stream;
+            di->slots_used = i + 1;
+        }
+    }
+    if (i >= fl::kStatusSlots) i = 0;
+    last_di = di;
+    last_stream = stream;
+    last_slot = i;
+    return i;
+}
+
+int* stream_status(DeviceInfo* di, cudaStream_t stream) { return di->status + status_slot(di, stream); }
 
 // ---------------------------------------------------------------------------
 // TMA tensor maps
@@ -766,6 +798,7 @@ fl_status run_kernels(int dt, int pro, bool dual, const void* A, const Outs& out
         }
     }
     prep.p.ln_stats = ln_stats;  // per-call scratch, not part of the key
+    prep.p.status = stream_status(di, stream);
 #ifdef FL_TRACE
     if (const char* tp = getenv("FL_TRACE_PTR"))
         prep.p.trace = reinterpret_cast<unsigned long long*>(strtoull(tp, nullptr, 10));
@@ -1137,12 +1170,13 @@ fl_status fl_device_status(void* stream) {
     if (st != FL_OK) return st;
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(FL_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
+    const size_t off = (size_t)status_slot(di, static_cast<cudaStream_t>(stream)) * sizeof(int);
     int v = 0;
-    e = cudaMemcpyFromSymbol(&v, g_fl_status, sizeof(int));
+    e = cudaMemcpyFromSymbol(&v, g_fl_status, sizeof(int), off);
     if (e != cudaSuccess) return fail(FL_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
     if (v == 0) return ok();
     const int zero = 0;
-    e = cudaMemcpyToSymbol(g_fl_status, &zero, sizeof(int));
+    e = cudaMemcpyToSymbol(g_fl_status, &zero, sizeof(int), off);
     if (e != cudaSuccess) return fail(FL_ERR_CUDA, "status clear: %s", cudaGetErrorString(e));
     return fail(FL_ERR_TIMEOUT, "a device-side wait ran past its limit (code %d, wait site %d)", v & 0xff, v >> 8);
 }
@@ -1190,7 +1224,8 @@ extern "C" fl_status fl_debug_wait_timeout(int limit_us, void* stream) {
     DeviceInfo* di = nullptr;
     fl_status st = device_info(&di);
     if (st != FL_OK) return st;
-    fl_wait_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(di->status,
+    fl_wait_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        stream_status(di, static_cast<cudaStream_t>(stream)),
                                                                           (unsigned long long)limit_us * 1000ull);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(FL_ERR_CUDA, "launch: %s", cudaGetErrorString(e));

@@ -16,6 +16,9 @@ enum DTypeTag : int { DT_F16 = 0, DT_BF16 = 1 };
 
 // Device status word values (low byte = code; the next byte says which wait gave up).
 constexpr int kStatusTimeout = 6;
+// Status words per device: one per stream handle in first-use order; word 0
+// also serves the legacy default stream and every stream past the table.
+constexpr int kStatusSlots = 64;
 
 // CTA tile: 128 rows of the activation; 64 fp16/bf16 along K per stage (one
 // 128-byte swizzle row).
@@ -49,7 +52,7 @@ struct GemmParams {
     const void* a_ptr;     // activation [M, K]
     const void* ln_stats;  // LayerNorm: float2 (mean, 1/sqrt(var + eps)) per activation row
     void* out_ptr;         // output 0 [M, N] (split-K kernel stores directly)
-    int* status;           // device status word
+    int* status;           // the launching stream's device status word
     unsigned long long timeout_ns;
     int M, N, K;           // N: columns of output 0
     int act;               // activation of output 0

@@ -411,11 +411,12 @@ __global__ void __launch_bounds__(splitk_threads<PRO>(), 2)
     }
     // ---------------------------------------------------------------- reduction + epilogue
     // Every thread of the CTA sums the `splits` partials of my slice (rows x
-    // w chunks of 8 columns; 8, or 16, threads per row, one chunk each),
+    // w chunks of 8 columns; w rounded up to a power of two threads per row,
+    // one chunk each),
     // scales, adds bias, activation and residual, and stores 16 bytes.
     const int xc0 = p.xc_c0[rank];
     const int xw = p.xc_c0[rank + 1] - xc0;
-    const int xsh = xw > 8 ? 4 : 3;
+    const int xsh = xw > 1 ? 32 - __clz(xw - 1) : 0;  // 2^xsh >= xw threads per row
     const int xch = threadIdx.x & ((1 << xsh) - 1);
     const int xcol = n0 + (xc0 + xch) * 8;
     const int N = out_n(p, osel.oi);

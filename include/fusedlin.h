@@ -41,14 +41,15 @@
  *     memory pool and frees it on the stream after the GEMM (see there).
  *     fl_swiglu_ffn keeps its hidden activation in a caller-provided
  *     workspace; fl_swiglu_ffn_noalloc keeps it in a fixed 8 MiB array of the
- *     library instead. The library's other device state is one status word.
+ *     library instead. The library's other device state is a small table
+ *     of status words (one per stream, see fl_device_status).
  *   - out may alias residual exactly (same pointer); no other aliasing of an
  *     output with an input is allowed.
  *   - Errors: a call that fails validation returns a non-zero fl_status
  *     before launching anything and writes nothing; fl_last_error() then
  *     returns a message (per thread). A device-side wait that exceeds its time
- *     limit makes the kernel stop early and record FL_ERR_TIMEOUT in a device
- *     status word, which fl_device_status() reads (see there).
+ *     limit makes the kernel stop early and record FL_ERR_TIMEOUT in the
+ *     status word of its stream, which fl_device_status() reads (see there).
  */
 #ifndef FUSEDLIN_H
 #define FUSEDLIN_H
@@ -309,9 +310,16 @@ void fl_graph_destroy(void* graph_exec);
 const char* fl_last_error(void);
 
 /*
- * Synchronises `stream`, then reads and clears the device status word that
- * kernels set when a bounded wait runs out. Returns FL_OK, FL_ERR_TIMEOUT, or
- * FL_ERR_CUDA if the synchronisation itself failed.
+ * Synchronises `stream`, then reads and clears the status word of `stream`,
+ * which this library's kernels launched on that stream set when a bounded
+ * wait runs out. Returns FL_OK, FL_ERR_TIMEOUT, or FL_ERR_CUDA if the
+ * synchronisation itself failed.
+ * Each device keeps 64 status words: word 0 for the legacy default stream
+ * (NULL), then one per stream handle in the order the library first sees
+ * them; the 64th distinct handle and later ones share word 0. A kernel
+ * captured into a graph keeps the word of the stream it was captured on,
+ * wherever the graph is replayed. The word is sticky: until it is read, a
+ * later kernel on the same stream whose wait is slow gives up at once.
  */
 fl_status fl_device_status(void* stream);
 
@@ -395,8 +403,8 @@ fl_status fl_kernel_launches(long long* count);
  * Test hook for the bounded-wait machinery: launches one CTA that waits on a
  * device barrier that nothing ever completes, with a limit of `limit_us`
  * microseconds (1..1000000). The kernel gives up, records FL_ERR_TIMEOUT in the
- * device status word and returns; the GPU context stays usable. Follow it with
- * fl_device_status() to read (and clear) the status.
+ * status word of `stream` and returns; the GPU context stays usable. Follow it
+ * with fl_device_status(stream) to read (and clear) the status.
  */
 fl_status fl_debug_wait_timeout(int limit_us, void* stream);
 

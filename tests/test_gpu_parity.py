@@ -632,3 +632,27 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     t = syn.gemm_inputs(64, 64, 64, "gemm_bias", "f16")
     got, ref, chain = run_pattern(t, "gemm_bias")
     assert_close(got, ref, "f16", "after timeout", chain=chain)
+
+
+def test_timeout_is_reported_on_its_own_stream_only():
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    for s in (None, s1, s2):
+        fl.device_status(s)  # clean slate
+    fl.debug_wait_timeout(2000, stream=s1)
+    torch.cuda.synchronize()
+    fl.device_status(s2)  # another stream's word stays clear
+    fl.device_status()  # and so does the default stream's
+    # a kernel on the other stream runs normally while s1's word is set
+    t = syn.gemm_inputs(300, 512, 1024, "gemm_bias", "f16")
+    A, W, b = dev(t["A"]), dev(t["W"]), dev(t["bias"])
+    out = torch.empty(300, 512, dtype=torch.float16, device="cuda")
+    s2.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s2):
+        fl.gemm_epilogue(A, W, bias=b, out=out, pattern="gemm_bias", stream=s2)
+    fl.device_status(s2)
+    ref = oracle.gemm_epilogue(f64(t["A"]), f64(t["W"]), f64(t["bias"]), None, "gemm_bias")
+    assert_close(out, ref, "f16", "other stream after a timeout")
+    with pytest.raises(fl.FusedLinError) as e:
+        fl.device_status(s1)
+    assert e.value.status == 6
+    fl.device_status(s1)  # read once, then clear
