@@ -118,7 +118,9 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto afull_bar = [&](int s) { return bar0 + 8u * (S + s); };
     auto empty_bar = [&](int s) { return bar0 + 8u * (2 * S + s); };
-    auto xform_bar = [&](int s) { return bar0 + 8u * (3 * S + s); };
+    // (norm prologues: the folds of both CTAs arrive on the leader's `full`
+    // barrier itself, so the MMA thread tests one barrier per K step)
+    auto xform_bar = [&](int s) { return bar0 + 8u * s; };
     auto tfull_bar = [&](int b) { return bar0 + 8u * (4 * S + b); };
     auto tempty_bar = [&](int b) { return bar0 + 8u * (4 * S + 2 + b); };
     auto sready_bar = [&](int b) { return bar0 + 8u * (4 * S + 4 + b); };
@@ -170,10 +172,9 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(full_bar(s), 1);
+            mbar_init(full_bar(s), PRO != PRO_NONE ? 1 + (SHARE == SHARE_SPLIT ? 16 : 8) : 1);
             mbar_init(afull_bar(s), 1);
             mbar_init(empty_bar(s), 1);
-            mbar_init(xform_bar(s), SHARE == SHARE_SPLIT ? 16 : 8);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar(b), 1);
@@ -433,10 +434,6 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                         break;
                     }
                     if (it == 0) FL_MARK_STEP(p, 48, kb - kb_begin);
-                    if (PRO != PRO_NONE && !wait_bar_cluster(xform_bar(s), ph, p.status, p.timeout_ns, 36)) {
-                        ok = false;
-                        break;
-                    }
                     if (it == 0) FL_MARK_STEP(p, 56, kb - kb_begin);
                     tc_fence_after();
                     if (kb == kb_begin && it == 0) FL_MARK(p, 3);
