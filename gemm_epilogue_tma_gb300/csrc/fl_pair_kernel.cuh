@@ -91,17 +91,21 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     using Ops = DTypeOps<DT>;
     constexpr int S = C::STAGES;
     constexpr int EPI_WARP0 = PRO != PRO_NONE ? 8 : 4;
-    // Prologues with a single accumulator buffer: the epilogue warps, idle
+    // LayerNorm with a single accumulator buffer: the epilogue warps, idle
     // while a tile's MMAs run, take a share of the fold. SHARE_ALT: the fold
     // warps fold whole rows of the even K blocks (by a running block index)
     // and the epilogue warps those of the odd ones, so each warpgroup has two
     // MMA steps for one fold; SHARE_SPLIT: the fold warps fold chunks 0-3 of
-    // every K block and the epilogue warps chunks 4-7.
+    // every K block and the epilogue warps chunks 4-7. The RMSNorm and
+    // input-bias folds keep pace with the MMAs on the fold warps alone and
+    // measured faster unshared (the bench default 17.6 against 18.0 us,
+    // rmsnorm_gemm 4096^3 102.1 against 103.7 us); LayerNorm fp16 at 4096^3
+    // took 134.5 us unshared against 127.3 alternating.
     constexpr int SHARE_NONE = 0, SHARE_SPLIT = 1, SHARE_ALT = 2;
 #ifndef FL_PAIR_SHARE
 #define FL_PAIR_SHARE 2
 #endif
-    constexpr int SHARE = (PRO != PRO_NONE && C::NBUF == 1) ? FL_PAIR_SHARE : SHARE_NONE;
+    constexpr int SHARE = (PRO == PRO_LN && C::NBUF == 1) ? FL_PAIR_SHARE : SHARE_NONE;
     constexpr bool FOLD2 = SHARE != SHARE_NONE;
     static_assert(SHARE != SHARE_ALT || S % 2 == 0, "alternating folds need an even ring: a warpgroup's "
                   "blocks k and k + S must share a stage's phase sequence");
