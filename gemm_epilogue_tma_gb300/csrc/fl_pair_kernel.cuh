@@ -584,26 +584,36 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
         // ship the outgoing half chunk by chunk: each warp stages its rows and
         // sends them with one bulk copy as soon as the partner's ring is free
         bool peer_ready = false;
+        // (two chunks' tensor-memory loads in flight per wait)
+        static_assert(C::NCHUNK % 2 == 0, "chunks are shipped in pairs");
 #pragma unroll 1
-        for (int c = 0; c < C::NCHUNK; ++c) {
-            const uint32_t blk = (uint32_t)(c * C::XCHUNK + q * C::XBLOCK);
+        for (int c2 = 0; c2 < C::NCHUNK; c2 += 2) {
+            uint32_t v[2][32];
             if (ok) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tl + (uint32_t)(oth_c0 + C::XCOLS * c), v);
+                tmem_ld_32x32b_x32(tl + (uint32_t)(oth_c0 + C::XCOLS * c2), v[0]);
+                tmem_ld_32x32b_x32(tl + (uint32_t)(oth_c0 + C::XCOLS * (c2 + 1)), v[1]);
                 tmem_ld_wait();
-                const uint32_t src_row = sbase + C::OFF_SEND + (uint32_t)(c * C::XCHUNK) + row_off;
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    st_shared_v4(src_row + (uint32_t)(4 * j) * 4u, v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-                if (PRO == PRO_RMS && c == 0) st_shared_f32(src_row + (uint32_t)C::XCOLS * 4u, ss_own);
             }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (ok && lane == 0) {
-                if (!peer_ready) peer_ready = wait_bar_cluster(ringfree_bar, 0, p.status, p.timeout_ns, 44);
-                if (peer_ready)
-                    bulk_copy_to_cluster(mapa_cluster(sbase + blk, partner), sbase + C::OFF_SEND + blk,
-                                         (uint32_t)C::XBLOCK, mapa_cluster(recvd_bar(q, c), partner));
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int c = c2 + e;
+                const uint32_t blk = (uint32_t)(c * C::XCHUNK + q * C::XBLOCK);
+                if (ok) {
+                    const uint32_t src_row = sbase + C::OFF_SEND + (uint32_t)(c * C::XCHUNK) + row_off;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        st_shared_v4(src_row + (uint32_t)(4 * j) * 4u, v[e][4 * j], v[e][4 * j + 1], v[e][4 * j + 2],
+                                     v[e][4 * j + 3]);
+                    if (PRO == PRO_RMS && c == 0) st_shared_f32(src_row + (uint32_t)C::XCOLS * 4u, ss_own);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (ok && lane == 0) {
+                    if (!peer_ready) peer_ready = wait_bar_cluster(ringfree_bar, 0, p.status, p.timeout_ns, 44);
+                    if (peer_ready)
+                        bulk_copy_to_cluster(mapa_cluster(sbase + blk, partner), sbase + C::OFF_SEND + blk,
+                                             (uint32_t)C::XBLOCK, mapa_cluster(recvd_bar(q, c), partner));
+                }
             }
         }
         if (threadIdx.x == 32 * EPI_WARP0) FL_MARK(p, 6);
@@ -618,11 +628,15 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                     // the two 64-column chunks use two staging buffers
                     const uint32_t sbuf = c == 0 ? ebuf : sbase + C::OFF_EPI2 + q * C::EPI_BUF_BYTES;
                     const uint32_t srow = sbuf + lane * 128;
+                    // both 32-column halves of this CTA's accumulator, one wait
+                    uint32_t accp[2][32];
+                    tmem_ld_32x32b_x32(tl + (uint32_t)(own_c0 + c * 64), accp[0]);
+                    tmem_ld_32x32b_x32(tl + (uint32_t)(own_c0 + c * 64 + 32), accp[1]);
+                    tmem_ld_wait();
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int cbase = col0 + h * 32;
                         const int xc = c * 2 + h;        // exchange chunk
-                        const int lc = xc * C::XCOLS;    // column within the own half
                         const uint32_t recv_row = sbase + (uint32_t)(xc * C::XCHUNK) + row_off;
                         // residual of these 32 columns, requested before the waits
                         // and TMEM loads below so its latency overlaps them
@@ -639,9 +653,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                             const float ss = ss_own + ld_shared_f32(recv_row + (uint32_t)C::XCOLS * 4u);
                             rs = rsqrtf(fmaf(ss, 1.0f / (float)p.K, p.eps));
                         }
-                        uint32_t acc[32];
-                        tmem_ld_32x32b_x32(tl + (uint32_t)(own_c0 + lc), acc);
-                        tmem_ld_wait();
+                        const uint32_t (&acc)[32] = accp[h];
                         float v[32];
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
