@@ -324,7 +324,11 @@ const char* fl_last_error(void);
 fl_status fl_device_status(void* stream);
 
 /*
- * Tuning overrides, for benchmarks and tests (process-wide, not thread-safe):
+ * Tuning overrides, for benchmarks and tests. They are process-wide: each value
+ * is stored and read atomically, and a change applies to the calls any thread
+ * prepares after it (a call repeated from the launch cache keeps the choice
+ * it was prepared with only while the options are unchanged: they are part
+ * of the cache key).
  *   FL_OPT_TILE_N:      0 = automatic, else the CTA tile width (128 or 256).
  *   FL_OPT_VARIANT:     0 = automatic, 1 = tile kernel, 2 = small-M split-K kernel
  *                       (for the SwiGLU gate/up GEMM only up to 64 rows, else
