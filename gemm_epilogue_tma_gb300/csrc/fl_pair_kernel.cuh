@@ -773,6 +773,14 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
             {
                 for (int c = 0; c < nchunks; ++c) {
                     const int col0 = n0 + c * 64;
+                    // (one wait for both halves' accumulator columns)
+                    uint32_t accp[DUAL ? 1 : 2][32];
+                    if (!DUAL) {
+                        tmem_ld_32x32b_x32(tbase + c * 64, accp[0]);
+                        tmem_ld_32x32b_x32(tbase + c * 64 + 32, accp[DUAL ? 0 : 1]);
+                        tmem_ld_wait();
+                        if (c == nchunks - 1) release_acc();
+                    }
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int cbase = col0 + h * 32;
@@ -786,10 +794,10 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                                 rres[j] = cbase + j * 8 < N ? *reinterpret_cast<const uint4*>(rrow + cbase + j * 8)
                                                             : make_uint4(0u, 0u, 0u, 0u);
                         }
-                        uint32_t acc[32];
-                        tmem_ld_32x32b_x32(tbase + c * 64 + h * 32, acc);
                         float v[32];
                         if (DUAL) {
+                            uint32_t acc[32];
+                            tmem_ld_32x32b_x32(tbase + c * 64 + h * 32, acc);
                             // gate in accumulator columns [0, 128), up in [128, 256)
                             uint32_t up[32];
                             tmem_ld_32x32b_x32(tbase + OUT_COLS + c * 64 + h * 32, up);
@@ -799,10 +807,8 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
                             for (int e = 0; e < 32; ++e)
                                 v[e] = act_apply(ACT_SILU, __uint_as_float(acc[e]) * rs) * (__uint_as_float(up[e]) * rs);
                         } else {
-                            tmem_ld_wait();
-                            if (h == 1 && c == nchunks - 1) release_acc();
 #pragma unroll
-                            for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(acc[e]) * rs;
+                            for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(accp[DUAL ? 0 : h][e]) * rs;
                         }
                         if (!DUAL && bias != nullptr) {
 #pragma unroll
