@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     using Ops = DTypeOps<DT>;
     constexpr int S = C::STAGES;
     constexpr int EPI_WARP0 = PRO != PRO_NONE ? 8 : 4;
-    // LayerNorm with a single accumulator buffer: the epilogue warps, idle
+    // fp16 LayerNorm with a single accumulator buffer: the epilogue warps, idle
     // while a tile's MMAs run, take a share of the fold. SHARE_ALT: the fold
     // warps fold whole rows of the even K blocks (by a running block index)
     // and the epilogue warps those of the odd ones, so each warpgroup has two
@@ -100,12 +100,14 @@ __global__ void __launch_bounds__(PRO != PRO_NONE ? 384 : 256, 1)
     // input-bias folds keep pace with the MMAs on the fold warps alone and
     // measured faster unshared (the bench default 17.6 against 18.0 us,
     // rmsnorm_gemm 4096^3 102.1 against 103.7 us); LayerNorm fp16 at 4096^3
-    // took 134.5 us unshared against 127.3 alternating.
+    // took 134.5 us unshared against 127.3 alternating, but LayerNorm bf16
+    // (whose fold widens with one mixed-precision FMA) 126.4 against 131.7,
+    // so only fp16 LayerNorm shares.
     constexpr int SHARE_NONE = 0, SHARE_SPLIT = 1, SHARE_ALT = 2;
 #ifndef FL_PAIR_SHARE
 #define FL_PAIR_SHARE 2
 #endif
-    constexpr int SHARE = (PRO == PRO_LN && C::NBUF == 1) ? FL_PAIR_SHARE : SHARE_NONE;
+    constexpr int SHARE = (PRO == PRO_LN && DT == DT_F16 && C::NBUF == 1) ? FL_PAIR_SHARE : SHARE_NONE;
     constexpr bool FOLD2 = SHARE != SHARE_NONE;
     static_assert(SHARE != SHARE_ALT || S % 2 == 0, "alternating folds need an even ring: a warpgroup's "
                   "blocks k and k + S must share a stage's phase sequence");
